@@ -1,0 +1,217 @@
+/*
+ * smcsd.h -- C ABI of libsmcsd.so: the per-step particle update of Sequential
+ * Monte Carlo speculative decoding (SMC-SD) and single-particle
+ * speculative-sampling verification, on one NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow these pages:
+ *   [SMC]  "Faster LLM Inference via Sequential Monte Carlo" (gist.science
+ *          explainer; zh section 2 "核心流程" / es section 2 "Metodología:
+ *          SMC-SD"): N particles, K drafted tokens each; Score & Bonus,
+ *          Reweight by the target/draft ratio, ESS, Resample below a
+ *          threshold; always K+1 tokens per particle per step.
+ *          Section 2 "系统优化设计" / "Ventajas Sistémicas": KV cache managed on
+ *          resampling by pointer exchange and reference counts, no KV copy,
+ *          shared prefixes.  Section 3 "通用性扩展": unnormalised targets such
+ *          as p^alpha (power sampling).
+ *   [SpS]  "Accelerating Large Language Model Decoding with Speculative
+ *          Sampling" (blog notes; sections 1 and 4.2 "Modified Rejection
+ *          Sampling"): accept drafted tokens with probability min(1, p/q),
+ *          resample from max(0, p - q) at the first rejection.
+ *
+ * Conventions for every entry point
+ *   - All array arguments are DEVICE pointers owned by the caller, row-major
+ *     and contiguous, unless stated otherwise.  Parameter structs are HOST
+ *     pointers, read during the call only.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call is asynchronous on that stream: it validates its
+ *     arguments on the host, launches kernels, and returns without syncing.
+ *   - The library allocates no memory.  Scratch space is the caller's
+ *     `workspace`, sized by smc_workspace_bytes(), 256-byte aligned, and
+ *     zero-filled once before first use (smc_workspace_init).  Each call
+ *     leaves the workspace's counters zero again, so it can be reused by the
+ *     next call on the same stream without clearing.  Two calls that run
+ *     concurrently must not share a workspace.
+ *   - Return value: SMC_OK or a negative SMC_ERR_* code for a host-side
+ *     failure (nothing was launched).  Conditions only the GPU can see (a bad
+ *     token id, a non-finite logit, an exhausted block pool ...) set bits of a
+ *     status word inside the workspace; read them with smc_device_status().
+ *     When a status bit is set the outputs of that call are unspecified.
+ *     No kernel traps or spins: a bad input never hangs or faults the GPU.
+ *   - Logits: `dtype` SMC_F32 (IEEE fp32) or SMC_BF16 (bfloat16 stored as
+ *     16-bit words).  Arithmetic is fp32 with fp32 accumulation, except the
+ *     sampling sums (bonus and residual tokens), which are carried in
+ *     float-float (about 48 significant bits) so that the drawn token agrees
+ *     with an exact-arithmetic sampler except on genuine near ties.
+ *   - Randomness: Philox4x32-10, key (seed mod 2^32, seed >> 32), counter
+ *     (step, stream, position, purpose); u = (word0 >> 8) * 2^-24.  Streams
+ *     and purposes are listed with each entry point.
+ */
+#ifndef SMCSD_H
+#define SMCSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SMCSD_ABI_VERSION 1
+
+/* ---- host-side return codes ------------------------------------------- */
+#define SMC_OK             0
+#define SMC_ERR_ARG       (-1)   /* NULL pointer, size out of range, bad shape */
+#define SMC_ERR_DTYPE     (-2)   /* dtype is neither SMC_F32 nor SMC_BF16      */
+#define SMC_ERR_WORKSPACE (-3)   /* workspace NULL, too small or misaligned    */
+#define SMC_ERR_LAUNCH    (-4)   /* a kernel launch was rejected by CUDA       */
+#define SMC_ERR_CUDA      (-5)   /* a CUDA runtime call failed                 */
+
+/* ---- device status bits (smc_device_status) ---------------------------- */
+#define SMC_DEV_BAD_TOKEN        0x01  /* drafted token id outside [0, V)          */
+#define SMC_DEV_NONFINITE        0x02  /* NaN/+inf logit, or NaN/+inf log-weight   */
+#define SMC_DEV_EMPTY_ROW        0x04  /* a logit row that is -inf everywhere      */
+#define SMC_DEV_ALL_ZERO_WEIGHT  0x08  /* every particle of a prompt has weight 0  */
+#define SMC_DEV_POOL_EXHAUSTED   0x10  /* free-block stack cannot cover an append  */
+#define SMC_DEV_TABLE_OVERFLOW   0x20  /* a particle would need more than T blocks */
+#define SMC_DEV_BAD_BLOCK        0x40  /* a block id outside its prompt's pool     */
+
+/* ---- limits ------------------------------------------------------------ */
+#define SMC_MAX_N  256        /* particles per prompt                           */
+#define SMC_MAX_K  64         /* drafted tokens per particle                    */
+#define SMC_MAX_V  (1 << 24)  /* vocabulary size                                */
+
+/* ---- Philox purposes (4th counter word) -------------------------------- */
+#define SMC_PURPOSE_BONUS     1  /* stream b*N+n, position K                     */
+#define SMC_PURPOSE_ACCEPT    2  /* stream b, position k (sps_verify)            */
+#define SMC_PURPOSE_RESIDUAL  3  /* stream b, position j (sps_verify)            */
+#define SMC_PURPOSE_RESAMPLE  4  /* stream b, position 0                         */
+
+typedef enum { SMC_F32 = 0, SMC_BF16 = 1 } smc_dtype;
+
+/* Shape and scalars of one step. */
+typedef struct {
+  int32_t B;          /* prompts (independent problems), >= 1                   */
+  int32_t N;          /* particles per prompt, 1..SMC_MAX_N                     */
+  int32_t K;          /* drafted tokens per particle, 1..SMC_MAX_K              */
+  int32_t V;          /* vocabulary size, 1..SMC_MAX_V                          */
+  int32_t dtype;      /* smc_dtype of both logit tensors                        */
+  float alpha;        /* target exponent: the target is p^alpha (1 = plain p),
+                         finite and > 0                                          */
+  float ess_frac;     /* resample iff ESS < ess_frac * N (strict)               */
+  uint64_t seed;      /* Philox key                                             */
+  uint32_t step;      /* Philox counter word 0; callers advance it per step     */
+} smc_params;
+
+/* Paged KV block tables of all prompts (see kv_blocktable_remap).  Every
+ * pointer is device memory, int32.  Block ids are global: prompt b owns ids
+ * b*P .. b*P+P-1. */
+typedef struct {
+  int32_t *tables;     /* [B, N, T] block id per table slot, -1 past the used  */
+  int32_t *seq_len;    /* [B, N]    tokens held by each particle               */
+  int32_t *refcount;   /* [B * P]   table references to each block             */
+  int32_t *free_list;  /* [B, P]    prompt b's LIFO stack of free ids          */
+  int32_t *free_top;   /* [B]       entries on prompt b's stack                */
+  int32_t *cow_pairs;  /* [B, N, 2] out: (src, dst) blocks to copy, in order   */
+  int32_t *n_cow;      /* [B]       out: pairs written for prompt b            */
+  int32_t T;           /* table slots per particle, >= 1                       */
+  int32_t block_size;  /* tokens per block, >= 1                               */
+  int32_t P;           /* pool blocks per prompt, >= 1                         */
+} smc_kv;
+
+/* Library ABI version (SMCSD_ABI_VERSION of the build). */
+int32_t smc_abi_version(void);
+
+/* Human-readable text of a return code or of a device status word. */
+const char *smc_strerror(int32_t code);
+
+/* Bytes of workspace that smc_step, sps_verify, smc_resample and
+ * kv_blocktable_remap need for shape `p` and, when `kv` is not NULL, for its
+ * T and P.  Returns 0 when the shape is invalid. */
+size_t smc_workspace_bytes(const smc_params *p, const smc_kv *kv);
+
+/* Zero-fill a workspace (cudaMemsetAsync on `stream`). */
+int32_t smc_workspace_init(void *workspace, size_t ws_bytes, void *stream);
+
+/* Reads the device status word of `workspace` into *out_bits (host memory):
+ * a bitwise OR of SMC_DEV_* over every call since it was last cleared.
+ * Synchronises `stream`.  When `clear` is non-zero the word is reset to 0. */
+int32_t smc_device_status(void *workspace, int32_t clear, int32_t *out_bits,
+                          void *stream);
+
+/* One SMC-SD step for B prompts x N particles ([SMC] section 2).
+ *
+ * target_logits [B, N, K+1, V]  row k < K scores drafted token k, row K is the
+ *                               bonus distribution.
+ * draft_logits  [B, N, K, V]    row k is the distribution token k was drawn from.
+ * draft_tokens  [B, N, K] int32 drafted tokens x_k.
+ * log_weights   [B, N] fp32, in/out: unnormalised log-weights.
+ * Outputs (device): tokens_out [B, N, K+1] int32, ancestors [B, N] int32,
+ *                   ess [B] fp32, resampled [B] int32 (0/1).
+ * kv (host struct of device pointers) may be NULL; when given, the step also
+ * runs kv_blocktable_remap's remap and appends K+1 tokens to every particle.
+ *
+ * Per particle (b, n):  lse_k = log sum_v exp(l_{k,v}) of each row;
+ *   delta = sum_{k<K} [alpha (lp_k[x_k] - lseP_k) - (lq_k[x_k] - lseQ_k)]
+ *         + (alpha != 1 ? lse(alpha lp_K) - alpha lseP_K : 0);
+ *   log_weights += delta;  bonus = inverse-CDF draw, in vocabulary order, from
+ *   softmax(alpha lp_K) with u(step, b*N+n, K, BONUS).
+ * Per prompt b:  w = softmax(log_weights), ESS = 1 / sum w^2;  if
+ *   ESS < ess_frac*N: systematic resampling with u0(step, b, 0, RESAMPLE),
+ *   ancestor a_i = min{j : sum_{t<=j} w_t > (u0+i)/N}, and log_weights := 0;
+ *   else a_i = i.  tokens_out[b,i] = (x[b,a_i,0..K-1], bonus[b,a_i]).
+ * ess[b] is the ESS before resampling. */
+int32_t smc_step(const smc_params *p, const void *target_logits,
+                 const void *draft_logits, const int32_t *draft_tokens,
+                 float *log_weights, int32_t *tokens_out, int32_t *ancestors,
+                 float *ess, int32_t *resampled, const smc_kv *kv,
+                 void *workspace, size_t ws_bytes, void *stream);
+
+/* Normalise, ESS and systematic resampling alone ([SMC] section 2, Resample),
+ * for callers that computed the weights themselves.  log_weights [B, N] fp32
+ * in/out (reset to 0 where resampled); ancestors [B, N] int32; ess [B] fp32;
+ * resampled [B] int32.  Same rule and uniforms as smc_step. */
+int32_t smc_resample(const smc_params *p, float *log_weights,
+                     int32_t *ancestors, float *ess, int32_t *resampled,
+                     void *workspace, size_t ws_bytes, void *stream);
+
+/* Block-table remap by ancestors, then append n_append tokens per particle
+ * ([SMC] section 2, KV Cache 优化: pointer exchange + reference counts).
+ *
+ * For each prompt b with resampled[b] != 0: particle i takes ancestor a_i's
+ * table and token count; each new table reference adds 1 to its block's
+ * count and each old one subtracts 1; blocks that reach 0 are pushed on
+ * prompt b's free stack in ascending id order.  Then, when n_append > 0,
+ * every particle grows by n_append tokens: a partially filled tail block held
+ * by several particles stays with the lowest index and every other holder
+ * pops a fresh block and records (src, dst) in cow_pairs (the caller copies
+ * that block's KV; no KV data is touched here); further blocks are popped in
+ * ascending particle order.  Popped blocks get count 1.  If the prompt's pops
+ * exceed its stack (SMC_DEV_POOL_EXHAUSTED) or a particle would need more
+ * than T blocks (SMC_DEV_TABLE_OVERFLOW), that prompt's append is skipped.
+ * ancestors [B, N] int32 and resampled [B] int32 are device arrays (as written
+ * by smc_resample).  p supplies B and N. */
+int32_t kv_blocktable_remap(const smc_params *p, const smc_kv *kv,
+                            const int32_t *ancestors, const int32_t *resampled,
+                            int32_t n_append, void *workspace, size_t ws_bytes,
+                            void *stream);
+
+/* Speculative-sampling verify of B prompts with one particle each ([SpS]
+ * section 4.2; p->N must be 1, p->alpha must be 1, p->B at most 65535).
+ *
+ * target_logits [B, K+1, V], draft_logits [B, K, V], draft_tokens [B, K].
+ * For k = 0..K-1: accept x_k iff u(step, b, k, ACCEPT) < p_k(x_k)/q_k(x_k).
+ * At the first rejection j: draw one token by inverse CDF from
+ * max(0, p_j - q_j) (or from p_j should that have no mass) with
+ * u(step, b, j, RESIDUAL); n_emitted = j+1.  If all are accepted: draw the
+ * bonus token from p_K with u(step, b, K, BONUS); n_emitted = K+1.
+ * Outputs: tokens_out [B, K+1] int32 (-1 past n_emitted), n_emitted [B]. */
+int32_t sps_verify(const smc_params *p, const void *target_logits,
+                   const void *draft_logits, const int32_t *draft_tokens,
+                   int32_t *tokens_out, int32_t *n_emitted, void *workspace,
+                   size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SMCSD_H */

@@ -193,11 +193,12 @@ def score_particle(target_rows, draft_rows, tokens, alpha):
 
 
 def smc_step(target, draft, draft_tokens, log_weights, *, alpha=1.0,
-             ess_frac=0.5, seed=0, step=0):
+             ess_frac=0.5, seed=0, step=0, dtype=None):
     """One SMC-SD step over B prompts x N particles (no KV state).
 
-    target: [B, N, K+1, V] fp64 (widened), draft: [B, N, K, V] fp64,
-    draft_tokens: [B, N, K] ints, log_weights: [B, N].
+    target: [B, N, K+1, V], draft: [B, N, K, V], either already fp64 or, when
+    ``dtype`` is given, stored logits that are widened one particle at a time
+    (see ``widen``); draft_tokens: [B, N, K] ints, log_weights: [B, N].
 
     Returns a dict with
       delta[B,N], log_weights_pre[B,N] (after reweighting), log_weights[B,N]
@@ -218,11 +219,13 @@ def smc_step(target, draft, draft_tokens, log_weights, *, alpha=1.0,
         bonus_margin=np.zeros((big_b, n_part)))
     for b in range(big_b):
         for n in range(n_part):
-            s = score_particle(target[b, n], draft[b, n], draft_tokens[b, n], alpha)
+            t_rows = widen(target[b, n], dtype) if dtype else target[b, n]
+            d_rows = widen(draft[b, n], dtype) if dtype else draft[b, n]
+            s = score_particle(t_rows, d_rows, draft_tokens[b, n], alpha)
             for key in ("lse_p", "g_p", "lse_q", "g_q", "lse_alpha", "delta"):
                 out[key][b, n] = s[key]
             u = philox.uniform(seed, step, b * n_part + n, k_drafts, philox.BONUS)
-            tok, margin = inverse_cdf(bonus_weights(target[b, n, k_drafts], alpha), u)
+            tok, margin = inverse_cdf(bonus_weights(t_rows[k_drafts], alpha), u)
             out["bonus"][b, n] = tok
             out["bonus_margin"][b, n] = margin
     lw_pre = np.asarray(log_weights, dtype=np.float64) + out["delta"]

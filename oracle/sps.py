@@ -21,7 +21,7 @@ The notes do not restate the rule; the plain form of it is taken:
 import numpy as np
 
 from . import philox
-from .smc import row_logsumexp, inverse_cdf, bonus_weights
+from .smc import row_logsumexp, inverse_cdf, bonus_weights, widen
 from .errors import OracleError, DEV_BAD_TOKEN
 
 
@@ -69,10 +69,11 @@ def verify_one(target_rows, draft_rows, tokens, u_accept, u_residual, u_bonus):
     return out, accept_margins, margin
 
 
-def sps_verify(target, draft, draft_tokens, *, seed=0, step=0):
+def sps_verify(target, draft, draft_tokens, *, seed=0, step=0, dtype=None):
     """Verify B independent prompts (N = 1 particle each).
 
-    target [B, K+1, V], draft [B, K, V] fp64, draft_tokens [B, K].
+    target [B, K+1, V], draft [B, K, V] fp64 (or stored logits widened per
+    prompt when ``dtype`` is given, see ``smc.widen``), draft_tokens [B, K].
     Uniforms: ACCEPT and RESIDUAL keyed by (step, b, k), BONUS by (step, b, K).
     Returns dict(tokens_out [B, K+1] padded with -1, n_emitted [B],
     accept_margin [B, K] (inf where not tested), final_margin [B]).
@@ -87,7 +88,9 @@ def sps_verify(target, draft, draft_tokens, *, seed=0, step=0):
         ua = [philox.uniform(seed, step, b, k, philox.ACCEPT) for k in range(k_drafts)]
         ur = [philox.uniform(seed, step, b, k, philox.RESIDUAL) for k in range(k_drafts)]
         ub = philox.uniform(seed, step, b, k_drafts, philox.BONUS)
-        toks, margins, fm = verify_one(target[b], draft[b], draft_tokens[b], ua, ur, ub)
+        t_rows = widen(target[b], dtype) if dtype else target[b]
+        d_rows = widen(draft[b], dtype) if dtype else draft[b]
+        toks, margins, fm = verify_one(t_rows, d_rows, draft_tokens[b], ua, ur, ub)
         tokens_out[b, :len(toks)] = toks
         n_emitted[b] = len(toks)
         accept_margin[b, :len(margins)] = margins

@@ -1,0 +1,245 @@
+// C ABI of libsmcsd.so (declared in include/smcsd.h): argument validation,
+// workspace layout and kernel launches.  No allocation, no synchronisation
+// except in smc_device_status.
+#include <cmath>
+#include <cstring>
+
+#include "kernels.h"
+#include "smcsd.h"
+
+namespace smcsd {
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws) {
+  const size_t rows = static_cast<size_t>(s.B) * s.N * (2 * s.K + 1);
+  const size_t nch = static_cast<size_t>(chunks_per_row(s.dtype, s.V));
+  const size_t words = P > 0 ? static_cast<size_t>(P + 31) / 32 : 0;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  // region that must start at zero (counters and the freed-block bitmap)
+  const size_t o_status = take(sizeof(unsigned));
+  const size_t o_pt = take(sizeof(unsigned) * s.B);
+  const size_t o_rt = take(sizeof(unsigned) * rows);
+  const size_t o_sa = take(sizeof(unsigned) * s.B);
+  const size_t o_sb = take(sizeof(unsigned) * s.B);
+  const size_t o_bm = take(sizeof(unsigned) * s.B * words);
+  const size_t zero_bytes = off;
+  // scratch that every call overwrites before reading
+  const size_t o_part = take(sizeof(RowPartial) * rows * nch);
+  const size_t o_res = take(sizeof(RowResult) * rows);
+  const size_t o_rej = take(sizeof(int32_t) * s.B);
+  const size_t o_sst = take(sizeof(float4) * s.B);
+  const size_t o_spq = take(sizeof(float4) * s.B * nch * 2);
+  const size_t o_spr = take(sizeof(float2) * s.B * nch);
+  const size_t o_kt = take(sizeof(int32_t) * static_cast<size_t>(s.B) * s.N * (T > 0 ? T : 0));
+  const size_t o_kl = take(sizeof(int32_t) * static_cast<size_t>(s.B) * s.N);
+  if (ws && base) {
+    char *p = static_cast<char *>(base);
+    ws->status = reinterpret_cast<unsigned *>(p + o_status);
+    ws->prompt_ticket = reinterpret_cast<unsigned *>(p + o_pt);
+    ws->row_ticket = reinterpret_cast<unsigned *>(p + o_rt);
+    ws->sps_ticket_a = reinterpret_cast<unsigned *>(p + o_sa);
+    ws->sps_ticket_b = reinterpret_cast<unsigned *>(p + o_sb);
+    ws->kv_bitmap = reinterpret_cast<unsigned *>(p + o_bm);
+    ws->partials = reinterpret_cast<RowPartial *>(p + o_part);
+    ws->results = reinterpret_cast<RowResult *>(p + o_res);
+    ws->sps_rej = reinterpret_cast<int32_t *>(p + o_rej);
+    ws->sps_stats = reinterpret_cast<float4 *>(p + o_sst);
+    ws->sps_part_pq = reinterpret_cast<float4 *>(p + o_spq);
+    ws->sps_part_r = reinterpret_cast<float2 *>(p + o_spr);
+    ws->kv_old_tables = reinterpret_cast<int32_t *>(p + o_kt);
+    ws->kv_old_len = reinterpret_cast<int32_t *>(p + o_kl);
+    ws->zero_bytes = zero_bytes;
+  }
+  return off;
+}
+
+static bool shape_ok(const smc_params *p) {
+  if (!p) return false;
+  if (p->B < 1 || p->N < 1 || p->N > SMC_MAX_N || p->K < 1 || p->K > SMC_MAX_K) return false;
+  if (p->V < 1 || p->V > SMC_MAX_V) return false;
+  if (!(std::isfinite(p->alpha) && p->alpha > 0.f)) return false;
+  if (!std::isfinite(p->ess_frac)) return false;
+  const double rows = static_cast<double>(p->B) * p->N * (2 * p->K + 1);
+  const double grid = rows * chunks_per_row(p->dtype == SMC_BF16 ? 1 : 0, p->V);
+  return grid < 2147483647.0;
+}
+
+static bool kv_ok(const smc_params *p, const smc_kv *kv) {
+  if (!kv) return true;
+  if (kv->T < 1 || kv->block_size < 1 || kv->P < 1) return false;
+  if (static_cast<double>(p->B) * kv->P >= 2147483647.0) return false;
+  if (static_cast<double>(p->N) * kv->T >= 2147483647.0) return false;
+  return kv->tables && kv->seq_len && kv->refcount && kv->free_list && kv->free_top &&
+         kv->cow_pairs && kv->n_cow;
+}
+
+static Shape to_shape(const smc_params *p) {
+  Shape s{};
+  s.B = p->B; s.N = p->N; s.K = p->K; s.V = p->V;
+  s.dtype = p->dtype;
+  s.alpha = p->alpha; s.ess_frac = p->ess_frac;
+  s.seed = p->seed; s.step = p->step;
+  return s;
+}
+
+static KvArgs to_kv(const smc_kv *kv) {
+  KvArgs k{};
+  k.tables = kv->tables; k.seq_len = kv->seq_len; k.refcount = kv->refcount;
+  k.free_list = kv->free_list; k.free_top = kv->free_top; k.cow_pairs = kv->cow_pairs;
+  k.n_cow = kv->n_cow; k.T = kv->T; k.block_size = kv->block_size; k.P = kv->P;
+  return k;
+}
+
+// Validates the workspace and carves it; returns SMC_OK or an error.
+static int32_t prepare_ws(const smc_params *p, const smc_kv *kv, void *workspace, size_t ws_bytes,
+                          Workspace *ws) {
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return SMC_ERR_WORKSPACE;
+  const Shape s = to_shape(p);
+  const size_t need = carve_workspace(s, kv ? kv->T : 0, kv ? kv->P : 0, nullptr, nullptr);
+  if (ws_bytes < need) return SMC_ERR_WORKSPACE;
+  carve_workspace(s, kv ? kv->T : 0, kv ? kv->P : 0, workspace, ws);
+  return SMC_OK;
+}
+
+}  // namespace smcsd
+
+using namespace smcsd;
+
+extern "C" {
+
+int32_t smc_abi_version(void) { return SMCSD_ABI_VERSION; }
+
+const char *smc_strerror(int32_t code) {
+  switch (code) {
+    case SMC_OK: return "ok";
+    case SMC_ERR_ARG: return "invalid argument (null pointer, size out of range or bad shape)";
+    case SMC_ERR_DTYPE: return "unsupported logit dtype";
+    case SMC_ERR_WORKSPACE: return "workspace null, misaligned or smaller than smc_workspace_bytes()";
+    case SMC_ERR_LAUNCH: return "kernel launch failed";
+    case SMC_ERR_CUDA: return "CUDA runtime call failed";
+    case SMC_DEV_BAD_TOKEN: return "device: drafted token outside [0, V)";
+    case SMC_DEV_NONFINITE: return "device: NaN/+inf logit or log-weight";
+    case SMC_DEV_EMPTY_ROW: return "device: logit row is -inf everywhere";
+    case SMC_DEV_ALL_ZERO_WEIGHT: return "device: every particle of a prompt has weight 0";
+    case SMC_DEV_POOL_EXHAUSTED: return "device: free block stack exhausted";
+    case SMC_DEV_TABLE_OVERFLOW: return "device: block table too short";
+    case SMC_DEV_BAD_BLOCK: return "device: block id outside its prompt's pool or bad KV state";
+    default: return code > 0 ? "device: several status bits set" : "unknown error";
+  }
+}
+
+size_t smc_workspace_bytes(const smc_params *p, const smc_kv *kv) {
+  if (!shape_ok(p) || (p->dtype != SMC_F32 && p->dtype != SMC_BF16)) return 0;
+  if (kv && (kv->T < 1 || kv->P < 1)) return 0;
+  return carve_workspace(to_shape(p), kv ? kv->T : 0, kv ? kv->P : 0, nullptr, nullptr);
+}
+
+int32_t smc_workspace_init(void *workspace, size_t ws_bytes, void *stream) {
+  if (!workspace) return SMC_ERR_WORKSPACE;
+  if (cudaMemsetAsync(workspace, 0, ws_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    return SMC_ERR_CUDA;
+  }
+  return SMC_OK;
+}
+
+int32_t smc_device_status(void *workspace, int32_t clear, int32_t *out_bits, void *stream) {
+  if (!workspace || !out_bits) return SMC_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned bits = 0;
+  if (cudaMemcpyAsync(&bits, workspace, sizeof(bits), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess) {
+    return SMC_ERR_CUDA;
+  }
+  *out_bits = static_cast<int32_t>(bits);
+  if (clear && cudaMemsetAsync(workspace, 0, sizeof(unsigned), st) != cudaSuccess) return SMC_ERR_CUDA;
+  return SMC_OK;
+}
+
+int32_t smc_step(const smc_params *p, const void *target_logits, const void *draft_logits,
+                 const int32_t *draft_tokens, float *log_weights, int32_t *tokens_out,
+                 int32_t *ancestors, float *ess, int32_t *resampled, const smc_kv *kv,
+                 void *workspace, size_t ws_bytes, void *stream) {
+  if (!p) return SMC_ERR_ARG;
+  if (p->dtype != SMC_F32 && p->dtype != SMC_BF16) return SMC_ERR_DTYPE;
+  if (!shape_ok(p) || !kv_ok(p, kv)) return SMC_ERR_ARG;
+  if (!target_logits || !draft_logits || !draft_tokens || !log_weights || !tokens_out ||
+      !ancestors || !ess || !resampled) {
+    return SMC_ERR_ARG;
+  }
+  Workspace ws{};
+  const int32_t rc = prepare_ws(p, kv, workspace, ws_bytes, &ws);
+  if (rc != SMC_OK) return rc;
+  StepOutputs out{};
+  out.log_weights = log_weights;
+  out.tokens_out = tokens_out;
+  out.ancestors = ancestors;
+  out.resampled = resampled;
+  out.ess = ess;
+  KvArgs k{};
+  if (kv) k = to_kv(kv);
+  const cudaError_t e = launch_step_rows(to_shape(p), 0, target_logits, draft_logits, draft_tokens,
+                                         out, kv ? &k : nullptr, ws,
+                                         static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SMC_OK : SMC_ERR_LAUNCH;
+}
+
+int32_t smc_resample(const smc_params *p, float *log_weights, int32_t *ancestors, float *ess,
+                     int32_t *resampled, void *workspace, size_t ws_bytes, void *stream) {
+  if (!p) return SMC_ERR_ARG;
+  if (p->dtype != SMC_F32 && p->dtype != SMC_BF16) return SMC_ERR_DTYPE;
+  if (!shape_ok(p) || !log_weights || !ancestors || !ess || !resampled) return SMC_ERR_ARG;
+  Workspace ws{};
+  const int32_t rc = prepare_ws(p, nullptr, workspace, ws_bytes, &ws);
+  if (rc != SMC_OK) return rc;
+  const cudaError_t e = launch_resample(to_shape(p), log_weights, ancestors, ess, resampled, ws,
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SMC_OK : SMC_ERR_LAUNCH;
+}
+
+int32_t kv_blocktable_remap(const smc_params *p, const smc_kv *kv, const int32_t *ancestors,
+                            const int32_t *resampled, int32_t n_append, void *workspace,
+                            size_t ws_bytes, void *stream) {
+  if (!p) return SMC_ERR_ARG;
+  if (p->dtype != SMC_F32 && p->dtype != SMC_BF16) return SMC_ERR_DTYPE;
+  if (!shape_ok(p) || !kv || !kv_ok(p, kv) || !ancestors || !resampled || n_append < 0) {
+    return SMC_ERR_ARG;
+  }
+  Workspace ws{};
+  const int32_t rc = prepare_ws(p, kv, workspace, ws_bytes, &ws);
+  if (rc != SMC_OK) return rc;
+  const cudaError_t e = launch_kv_remap(to_shape(p), to_kv(kv), ancestors, resampled, n_append, ws,
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SMC_OK : SMC_ERR_LAUNCH;
+}
+
+int32_t sps_verify(const smc_params *p, const void *target_logits, const void *draft_logits,
+                   const int32_t *draft_tokens, int32_t *tokens_out, int32_t *n_emitted,
+                   void *workspace, size_t ws_bytes, void *stream) {
+  if (!p) return SMC_ERR_ARG;
+  if (p->dtype != SMC_F32 && p->dtype != SMC_BF16) return SMC_ERR_DTYPE;
+  if (!shape_ok(p) || p->N != 1 || p->alpha != 1.f || p->B > 65535) return SMC_ERR_ARG;
+  if (!target_logits || !draft_logits || !draft_tokens || !tokens_out || !n_emitted) {
+    return SMC_ERR_ARG;
+  }
+  Workspace ws{};
+  const int32_t rc = prepare_ws(p, nullptr, workspace, ws_bytes, &ws);
+  if (rc != SMC_OK) return rc;
+  StepOutputs out{};
+  out.tokens_out = tokens_out;
+  out.n_emitted = n_emitted;
+  const Shape s = to_shape(p);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_step_rows(s, 1, target_logits, draft_logits, draft_tokens, out, nullptr,
+                                   ws, st);
+  if (e != cudaSuccess) return SMC_ERR_LAUNCH;
+  e = launch_sps_residual(s, target_logits, draft_logits, tokens_out, ws, st);
+  return e == cudaSuccess ? SMC_OK : SMC_ERR_LAUNCH;
+}
+
+}  // extern "C"

@@ -1,0 +1,328 @@
+// Device building blocks shared by the SMC-SD kernels: Philox4x32-10,
+// float-float arithmetic, the accurate exp2 used by sampling sums, vector
+// loads of logit chunks, and block-wide reductions and scans.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "exp2_table.cuh"
+
+namespace smcsd {
+
+constexpr int kThreads = 256;            // threads per CTA of every kernel here
+constexpr int kWarps = kThreads / 32;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): word 0 of one block.
+// Counter (step, stream, position, purpose), key (seed lo, seed hi).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t philox_word0(uint32_t c0, uint32_t c1, uint32_t c2,
+                                                 uint32_t c3, uint32_t k0, uint32_t k1) {
+  constexpr uint32_t kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;
+  constexpr uint32_t kW0 = 0x9E3779B9u, kW1 = 0xBB67AE85u;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) { k0 += kW0; k1 += kW1; }
+    const uint32_t hi0 = __umulhi(kM0, c0), lo0 = kM0 * c0;
+    const uint32_t hi1 = __umulhi(kM1, c2), lo1 = kM1 * c2;
+    const uint32_t n0 = hi1 ^ c1 ^ k0;
+    const uint32_t n2 = hi0 ^ c3 ^ k1;
+    c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+  }
+  return c0;
+}
+
+// u in [0, 1) on the 2^-24 lattice; exact in fp32 and fp64.
+__device__ __forceinline__ float philox_uniform(uint64_t seed, uint32_t step, uint32_t stream,
+                                                uint32_t position, uint32_t purpose) {
+  const uint32_t x = philox_word0(step, stream, position, purpose,
+                                  static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+  return static_cast<float>(x >> 8) * 0x1p-24f;
+}
+
+// ---------------------------------------------------------------------------
+// float-float arithmetic (Knuth two-sum, Dekker fast-two-sum, FMA two-product).
+// Relies on IEEE fp32 with no reassociation (the build does not use fast-math).
+// ---------------------------------------------------------------------------
+struct ff { float hi, lo; };
+
+__device__ __forceinline__ ff two_sum(float a, float b) {
+  const float s = a + b;
+  const float bb = s - a;
+  const float e = (a - (s - bb)) + (b - bb);
+  return {s, e};
+}
+__device__ __forceinline__ ff fast_two_sum(float a, float b) {  // needs |a| >= |b| or a == 0
+  const float s = a + b;
+  return {s, b - (s - a)};
+}
+__device__ __forceinline__ ff two_prod(float a, float b) {
+  const float p = a * b;
+  return {p, fmaf(a, b, -p)};
+}
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+  ff s = two_sum(a.hi, b.hi);
+  s.lo += a.lo + b.lo;
+  return fast_two_sum(s.hi, s.lo);
+}
+__device__ __forceinline__ ff ff_sub(ff a, ff b) { return ff_add(a, ff{-b.hi, -b.lo}); }
+__device__ __forceinline__ ff ff_mul(ff a, ff b) {
+  ff p = two_prod(a.hi, b.hi);
+  p.lo += a.hi * b.lo + a.lo * b.hi;
+  return fast_two_sum(p.hi, p.lo);
+}
+__device__ __forceinline__ ff ff_mul_f(ff a, float b) {
+  ff p = two_prod(a.hi, b);
+  p.lo = fmaf(a.lo, b, p.lo);
+  return fast_two_sum(p.hi, p.lo);
+}
+__device__ __forceinline__ ff ff_div(ff a, ff b) {
+  const float q1 = a.hi / b.hi;
+  const ff r = ff_sub(a, ff_mul_f(b, q1));
+  const float q2 = r.hi / b.hi;
+  return fast_two_sum(q1, q2);
+}
+// a > b, exact on the represented values (both normalised).
+__device__ __forceinline__ bool ff_gt(ff a, ff b) {
+  return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo);
+}
+__device__ __forceinline__ double ff_to_double(ff a) {
+  return static_cast<double>(a.hi) + static_cast<double>(a.lo);
+}
+__device__ __forceinline__ ff ff_from_double(double x) {
+  const float hi = static_cast<float>(x);
+  return {hi, static_cast<float>(x - static_cast<double>(hi))};
+}
+
+// ---------------------------------------------------------------------------
+// Accurate 2^y for y = yh + yl <= ~0, as an unnormalised float pair with
+// relative error about 3e-10: y = n + j/64 + r, |r| <= 1/128;
+// 2^(j/64) from a float-float table, 2^r - 1 from its Taylor polynomial.
+// `tab` points at the table staged in shared memory.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ ff accurate_exp2(float yh, float yl, const float2 *tab) {
+  if (!(yh > -120.f)) return {0.f, 0.f};           // below 2^-120 (or NaN -> 0; NaN
+                                                  // rows are reported by the fast path)
+  const float k = rintf(yh * 64.f);
+  const float rh = fmaf(k, -0.015625f, yh);        // exact: y_hi - k/64
+  const float r = rh + yl;
+  const int ki = static_cast<int>(k);
+  const int j = ki & 63;
+  const int n = ki >> 6;                           // floor division: ki = 64 n + j
+  float q = fmaf(r, kC4, kC3);
+  q = fmaf(r, q, kC2);
+  q = fmaf(r, q, kC1Lo);
+  const float p = fmaf(r, kC1Hi, r * q);           // 2^r - 1
+  const float2 t = tab[j];
+  const float lo = fmaf(t.x, p, fmaf(t.y, p, t.y));
+  const float sc = __int_as_float((n + 127) << 23); // 2^n, n >= -120 here
+  return {t.x * sc, lo * sc};
+}
+
+// 2^(log2(e) * d) for d given as a float pair (d, dl): exp(d + dl).
+__device__ __forceinline__ ff accurate_exp(float d, float dl, const float2 *tab) {
+  const float yh = d * kLog2eHi;
+  const float yl = fmaf(d, kLog2eHi, -yh) + fmaf(d, kLog2eLo, dl * kLog2eHi);
+  return accurate_exp2(yh, yl, tab);
+}
+
+// Accumulate an unnormalised pair into a running float-float sum.
+__device__ __forceinline__ void ff_accum(ff &acc, ff t) {
+  ff s = two_sum(acc.hi, t.hi);
+  acc.hi = s.hi;
+  acc.lo += s.lo + t.lo;
+}
+__device__ __forceinline__ ff ff_norm(ff a) { return fast_two_sum(a.hi, a.lo); }
+
+__device__ __forceinline__ void stage_exp2_table(float2 *s_tab) {
+  if (threadIdx.x < 64) s_tab[threadIdx.x] = kExp2Tab[threadIdx.x];
+}
+
+// ---------------------------------------------------------------------------
+// Fast-path exp2 (MUFU) and logit widening.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// 16-byte streaming load that bypasses L1 allocation.
+__device__ __forceinline__ uint4 ld_stream16(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+template <typename T> struct LogitTraits;
+template <> struct LogitTraits<float> {
+  static constexpr int kPerVec = 4;               // logits per 16-byte vector
+  __device__ __forceinline__ static float at(const uint4 &v, int e) {
+    const uint32_t w = e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+    return __uint_as_float(w);
+  }
+  __device__ __forceinline__ static float scalar(const void *row, int64_t i) {
+    return __ldg(static_cast<const float *>(row) + i);
+  }
+};
+struct bf16_tag {};
+template <> struct LogitTraits<bf16_tag> {
+  static constexpr int kPerVec = 8;
+  __device__ __forceinline__ static float at(const uint4 &v, int e) {
+    const uint32_t w = (e >> 1) == 0 ? v.x : (e >> 1) == 1 ? v.y : (e >> 1) == 2 ? v.z : v.w;
+    return (e & 1) ? bf16_hi(w) : bf16_lo(w);
+  }
+  __device__ __forceinline__ static float scalar(const void *row, int64_t i) {
+    const uint16_t b = __ldg(static_cast<const unsigned short *>(row) + i);
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Block-wide reductions and scans over kThreads threads.  `scratch` is shared
+// memory of at least 2*kWarps words.  All threads must call them.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float block_max(float v, float *scratch) {
+  v = warp_max(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  v = lane < kWarps ? scratch[lane] : kNegInf;
+  return warp_max(v);
+}
+
+__device__ __forceinline__ ff warp_ff_sum(ff v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ff w{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+    v = ff_add(v, w);
+  }
+  return v;
+}
+__device__ __forceinline__ ff block_ff_sum(ff v, float2 *scratch) {
+  v = warp_ff_sum(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) scratch[warp] = make_float2(v.hi, v.lo);
+  __syncthreads();
+  ff w = lane < kWarps ? ff{scratch[lane].x, scratch[lane].y} : ff{0.f, 0.f};
+  return warp_ff_sum(w);
+}
+
+// Inclusive float-float scan across the block in thread order.
+__device__ __forceinline__ ff block_ff_scan(ff v, float2 *scratch, ff *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    ff w{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+    if (lane >= o) v = ff_add(w, v);
+  }
+  __syncthreads();
+  if (lane == 31) scratch[warp] = make_float2(v.hi, v.lo);
+  __syncthreads();
+  ff base{0.f, 0.f};
+  ff all{0.f, 0.f};
+  for (int w = 0; w < kWarps; ++w) {
+    const ff s{scratch[w].x, scratch[w].y};
+    if (w < warp) base = ff_add(base, s);
+    all = ff_add(all, s);
+  }
+  *total = all;
+  return ff_add(base, v);
+}
+
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ double warp_max_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ double block_sum_d(double v, double *scratch) {
+  v = warp_sum_d(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  v = lane < kWarps ? scratch[lane] : 0.0;
+  return warp_sum_d(v);
+}
+__device__ __forceinline__ double block_max_d(double v, double *scratch) {
+  v = warp_max_d(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  v = lane < kWarps ? scratch[lane] : -__longlong_as_double(0x7ff0000000000000ll);
+  return warp_max_d(v);
+}
+// Inclusive scan of doubles in thread order.
+__device__ __forceinline__ double block_scan_d(double v, double *scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double w = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += w;
+  }
+  __syncthreads();
+  if (lane == 31) scratch[warp] = v;
+  __syncthreads();
+  double base = 0.0;
+  for (int w = 0; w < warp; ++w) base += scratch[w];
+  return base + v;
+}
+// Exclusive scan of ints in thread order; *total gets the sum.
+__device__ __forceinline__ int block_excl_scan_i(int v, int *scratch, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int w = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += w;
+  }
+  __syncthreads();
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  int base = 0, all = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < warp) base += scratch[w];
+    all += scratch[w];
+  }
+  *total = all;
+  return base + x - v;
+}
+__device__ __forceinline__ int block_min_i(int v, int *scratch) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  v = lane < kWarps ? scratch[lane] : 0x7fffffff;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Device status word: OR in error bits (never traps, never waits).
+__device__ __forceinline__ void raise_status(unsigned *status, unsigned bits) {
+  atomicOr(status, bits);
+}
+
+}  // namespace smcsd

@@ -1,0 +1,76 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernels.
+// Host-only declarations; no CUDA types beyond cudaStream_t.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace smcsd {
+
+// Per-(row, chunk) partial of a vocabulary reduction: chunk max m, fast fp32
+// sum s of exp(l - m), and the float-float sum (shi, slo) of the sampling
+// weights exp(alpha (l - m)) (bonus rows only).
+struct RowPartial { float m, s, shi, slo; };
+
+// Per-row result: log-sum-exp, gathered logit of the drafted token, the
+// log-sum-exp of alpha*l (bonus rows), and the bonus token (bonus rows).
+struct RowResult { float lse, g, lse_alpha; int32_t tok; };
+
+struct KvArgs {
+  int32_t *tables, *seq_len, *refcount, *free_list, *free_top, *cow_pairs, *n_cow;
+  int32_t T, block_size, P;
+};
+
+// Workspace carve-up shared by every entry point.
+struct Workspace {
+  unsigned *status;          // [1]  device status bits
+  unsigned *prompt_ticket;   // [B]
+  unsigned *row_ticket;      // [rows]
+  unsigned *sps_ticket_a;    // [B]
+  unsigned *sps_ticket_b;    // [B]
+  unsigned *kv_bitmap;       // [B * ceil(P/32)]
+  RowPartial *partials;      // [rows * nch]
+  RowResult *results;        // [rows]
+  int32_t *sps_rej;          // [B]  first rejected position, -1 if none
+  float4 *sps_stats;         // [B]  precise (lse_p hi, lo, lse_q hi, lo) of row j
+  float4 *sps_part_pq;       // [B * nch * 2]  per-chunk stats of rows p_j, q_j
+  float2 *sps_part_r;        // [B * nch]      per-chunk residual mass
+  int32_t *kv_old_tables;    // [B * N * T]
+  int32_t *kv_old_len;       // [B * N]
+  size_t zero_bytes;         // bytes from the start that must start at zero
+};
+
+struct Shape {
+  int B, N, K, V, dtype;     // dtype 0 = f32, 1 = bf16
+  float alpha, ess_frac;
+  uint64_t seed;
+  uint32_t step;
+};
+
+// Elements per chunk of the row reductions for a dtype.
+int chunk_elems(int dtype);
+int chunks_per_row(int dtype, int V);
+
+// Lays out `base` for the shape; returns the bytes needed (base may be null).
+size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws);
+
+struct StepOutputs {
+  float *log_weights;
+  int32_t *tokens_out, *ancestors, *resampled, *n_emitted;
+  float *ess;
+};
+
+// mode 0: SMC step; mode 1: SpS verify (first launch).
+cudaError_t launch_step_rows(const Shape &s, int mode, const void *target, const void *draft,
+                             const int32_t *tokens, const StepOutputs &out, const KvArgs *kv,
+                             const Workspace &ws, cudaStream_t stream);
+cudaError_t launch_resample(const Shape &s, float *log_weights, int32_t *ancestors, float *ess,
+                            int32_t *resampled, const Workspace &ws, cudaStream_t stream);
+cudaError_t launch_kv_remap(const Shape &s, const KvArgs &kv, const int32_t *ancestors,
+                            const int32_t *resampled, int n_append, const Workspace &ws,
+                            cudaStream_t stream);
+cudaError_t launch_sps_residual(const Shape &s, const void *target, const void *draft,
+                                int32_t *tokens_out, const Workspace &ws, cudaStream_t stream);
+
+}  // namespace smcsd

@@ -1,0 +1,192 @@
+// Row-level device helpers shared by the step kernel and the SpS residual
+// kernels: chunk streaming, sampling-weight terms, and the two stages of an
+// inverse-CDF draw in vocabulary order (which chunk, then which element).
+#pragma once
+
+#include "device_common.cuh"
+
+namespace smcsd {
+
+constexpr int kNV = 4;  // 16-byte vectors per thread per chunk
+
+template <typename T> struct ChunkGeom {
+  static constexpr int kEPV = LogitTraits<T>::kPerVec;
+  static constexpr int kEPT = kNV * kEPV;          // logits per thread
+  static constexpr int kCH = kThreads * kEPT;      // logits per chunk
+  static constexpr int kESZ = sizeof(T) == 4 ? 4 : 2;
+};
+
+// Stream `n_valid` logits of a chunk starting at `chunk_base` into x[]
+// (positions past n_valid read as -inf).  VEC: 16-byte streaming loads,
+// requires a 16-byte aligned base and n_valid a multiple of the vector width.
+// Element x[i*EPV + e] is logit (i*kThreads + tid)*EPV + e of the chunk (VEC)
+// or logit i*kThreads + tid (scalar path); order does not matter to callers.
+template <typename T, bool VEC>
+__device__ __forceinline__ void load_chunk(const char *chunk_base, int n_valid,
+                                           float (&x)[ChunkGeom<T>::kEPT]) {
+  using Tr = LogitTraits<T>;
+  constexpr int EPV = ChunkGeom<T>::kEPV;
+  const int tid = threadIdx.x;
+  if (VEC) {
+    const uint4 *base = reinterpret_cast<const uint4 *>(chunk_base);
+    uint4 v[kNV];
+#pragma unroll
+    for (int i = 0; i < kNV; ++i) {
+      const int vi = i * kThreads + tid;
+      v[i] = vi * EPV < n_valid ? ld_stream16(base + vi) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < kNV; ++i) {
+      const bool ok = (i * kThreads + tid) * EPV < n_valid;
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) x[i * EPV + e] = ok ? Tr::at(v[i], e) : kNegInf;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < ChunkGeom<T>::kEPT; ++i) {
+      const int idx = i * kThreads + tid;
+      x[i] = idx < n_valid ? Tr::scalar(chunk_base, idx) : kNegInf;
+    }
+  }
+}
+
+// exp(alpha (x - m)) as a float pair, accurate to ~3e-10 relative; -inf -> 0.
+// EXACT_DIFF: x - m is exact in fp32 (bf16 logits against a bf16 max, where
+// it matters); otherwise the rounding error of x - m is carried along.
+template <bool EXACT_DIFF>
+__device__ __forceinline__ ff weight_term(float x, float m, float alpha, const float2 *tab) {
+  if (!(x > kNegInf)) return {0.f, 0.f};
+  float d, dl;
+  if (EXACT_DIFF) {
+    d = x - m; dl = 0.f;
+  } else {
+    const ff s = two_sum(x, -m);
+    d = s.hi; dl = s.lo;
+  }
+  ff ad = two_prod(alpha, d);
+  ad.lo = fmaf(alpha, dl, ad.lo);
+  return accurate_exp(ad.hi, ad.lo, tab);
+}
+
+// exp(x - L) for a float-float L: exp((x - L.hi) - L.lo).
+__device__ __forceinline__ ff prob_term(float x, ff big_l, const float2 *tab) {
+  if (!(x > kNegInf)) return {0.f, 0.f};
+  const ff s = two_sum(x, -big_l.hi);
+  return accurate_exp(s.hi, s.lo - big_l.lo, tab);
+}
+
+__device__ __forceinline__ ff warp_ff_incl_scan(ff v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    ff w{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+    if (lane >= o) v = ff_add(w, v);
+  }
+  return v;
+}
+
+__device__ __forceinline__ float block_sum_f(float v, float *scratch) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  v = lane < kWarps ? scratch[lane] : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ ff shfl_ff(ff v, int src) {
+  return ff{__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
+}
+
+// Stage 1 of an inverse-CDF draw, run by one full warp.  chunk(c, &val, &f)
+// gives chunk c's mass `val` in absolute units and the factor `f` from the
+// chunk's own units to absolute ones.  Finds the first chunk with positive
+// mass whose inclusive prefix exceeds `target` and returns it with the
+// remaining target in that chunk's units; if rounding leaves none, returns
+// the last chunk with positive mass and its full mass (the draw then takes
+// its last element).  Returns -1 when no chunk has mass.
+template <typename ChunkFn>
+__device__ int warp_find_chunk(int nch, ff target, ChunkFn chunk, ff *rem_local) {
+  const int lane = threadIdx.x & 31;
+  ff carry{0.f, 0.f};
+  int sel = -1, last = -1;
+  ff sel_excl{0.f, 0.f}, sel_f{1.f, 0.f}, last_val{0.f, 0.f}, last_f{1.f, 0.f};
+  for (int c0w = 0; c0w < nch && sel < 0; c0w += 32) {
+    const int c = c0w + lane;
+    ff val{0.f, 0.f}, f{1.f, 0.f};
+    if (c < nch) chunk(c, &val, &f);
+    const ff incl = ff_add(carry, warp_ff_incl_scan(val));
+    const ff excl = ff_sub(incl, val);
+    const bool pos = c < nch && val.hi > 0.f;
+    const unsigned hit = __ballot_sync(0xffffffffu, pos && ff_gt(incl, target));
+    const unsigned any = __ballot_sync(0xffffffffu, pos);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      sel = c0w + src;
+      sel_excl = shfl_ff(excl, src);
+      sel_f = shfl_ff(f, src);
+    } else if (any) {
+      const int src = 31 - __clz(any);
+      last = c0w + src;
+      last_val = shfl_ff(val, src);
+      last_f = shfl_ff(f, src);
+    }
+    carry = shfl_ff(incl, 31);
+  }
+  if (sel >= 0) {
+    *rem_local = ff_div(ff_sub(target, sel_excl), sel_f);
+    return sel;
+  }
+  *rem_local = last >= 0 ? ff_div(last_val, last_f) : ff{0.f, 0.f};
+  return last;
+}
+
+// Stage 2, run by the whole CTA: inside chunk [c0, c0+len), the first element
+// with a positive weight whose running sum exceeds `target` (in the chunk's
+// units); if rounding leaves none, the last positive element.  Thread t scans
+// the contiguous segment [t*seg, (t+1)*seg).  term(i) is the weight of
+// vocabulary index i.  Returns the vocabulary index, or -1 with no mass.
+template <typename TermFn>
+__device__ int block_select_in_chunk(int64_t c0, int len, ff target, TermFn term,
+                                     float2 *s_ff, int *s_int) {
+  const int seg = (len + kThreads - 1) / kThreads;
+  const int beg = min(static_cast<int>(threadIdx.x) * seg, len);
+  const int end = min(beg + seg, len);
+  ff part{0.f, 0.f};
+  int last_pos = -1, first_pos = -1;
+  for (int e = beg; e < end; ++e) {
+    const ff t = term(c0 + e);
+    if (t.hi > 0.f) {
+      last_pos = e;
+      if (first_pos < 0) first_pos = e;
+    }
+    ff_accum(part, t);
+  }
+  part = ff_norm(part);
+  ff total;
+  const ff incl = block_ff_scan(part, s_ff, &total);
+  const ff excl = ff_sub(incl, part);
+  int cand = 0x7fffffff;
+  if (part.hi > 0.f) {
+    if (ff_gt(excl, target)) {
+      cand = first_pos;                 // target below this segment (rounding)
+    } else if (ff_gt(incl, target)) {
+      ff run = excl;
+      for (int e = beg; e < end; ++e) {
+        const ff t = term(c0 + e);
+        run = ff_add(run, ff_norm(t));
+        if (t.hi > 0.f && ff_gt(run, target)) { cand = e; break; }
+      }
+      if (cand == 0x7fffffff) cand = last_pos;
+    }
+  }
+  cand = block_min_i(cand, s_int);
+  if (cand == 0x7fffffff) cand = -block_min_i(-last_pos, s_int);  // max over threads
+  return cand < 0 ? -1 : static_cast<int>(c0 + cand);
+}
+
+}  // namespace smcsd

@@ -1,0 +1,262 @@
+// Speculative-sampling residual draw for sm_103a ("Accelerating Large
+// Language Model Decoding with Speculative Sampling", section 4.2 "Modified
+// Rejection Sampling"): at the first rejected position j, one token is drawn
+// from max(0, p_j - q_j) normalised, by inverse CDF in vocabulary order.
+//
+// Runs after the row kernel in SpS mode, which wrote the first rejected
+// position of every prompt (or -1).  Two launches over (chunk, prompt):
+//   sps_stats_kernel:    float-float log-sum-exp of rows p_j and q_j, so that
+//                        p_v and q_v are known to ~1e-10 relative;
+//   sps_residual_kernel: per-chunk residual mass; the last CTA of the prompt
+//                        picks the chunk and the element.
+// CTAs of prompts with no rejection exit at once.
+#include <cmath>
+
+#include "row_common.cuh"
+#include "kernels.h"
+#include "smcsd.h"
+
+namespace smcsd {
+
+struct SpsArgs {
+  const char *target, *draft;
+  int B, K, V, nch;
+  uint64_t seed;
+  uint32_t step;
+  int32_t *tokens_out;
+  Workspace ws;
+};
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kThreads) sps_stats_kernel(const SpsArgs a) {
+  using G = ChunkGeom<T>;
+  constexpr bool kExactDiff = sizeof(T) != 4;
+  __shared__ float s_red[2 * kWarps];
+  __shared__ float2 s_ff[kWarps];
+  __shared__ float2 s_tab[64];
+  __shared__ int s_last;
+  const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
+  const int jr = a.ws.sps_rej[b];
+  if (jr < 0) return;
+  stage_exp2_table(s_tab);
+  const int64_t c0 = static_cast<int64_t>(c) * G::kCH;
+  const int n_valid = static_cast<int>(min(static_cast<int64_t>(G::kCH), a.V - c0));
+  const char *rows[2] = {
+      a.target + (static_cast<size_t>(b) * (a.K + 1) + jr) * static_cast<size_t>(a.V) * G::kESZ,
+      a.draft + (static_cast<size_t>(b) * a.K + jr) * static_cast<size_t>(a.V) * G::kESZ};
+  for (int r = 0; r < 2; ++r) {
+    float x[G::kEPT];
+    load_chunk<T, VEC>(rows[r] + c0 * G::kESZ, n_valid, x);
+    float m = kNegInf;
+#pragma unroll
+    for (int e = 0; e < G::kEPT; ++e) m = fmaxf(m, x[e]);
+    const float mc = block_max(m, s_red);
+    ff S{0.f, 0.f};
+    if (mc > kNegInf && mc < -kNegInf) {
+#pragma unroll
+      for (int e = 0; e < G::kEPT; ++e) ff_accum(S, weight_term<kExactDiff>(x[e], mc, 1.f, s_tab));
+    }
+    S = block_ff_sum(ff_norm(S), s_ff);
+    if (tid == 0) a.ws.sps_part_pq[(static_cast<size_t>(b) * a.nch + c) * 2 + r] = make_float4(mc, S.hi, S.lo, 0.f);
+  }
+  if (tid == 0) {
+    __threadfence();
+    s_last = atomicAdd(&a.ws.sps_ticket_a[b], 1u) == static_cast<unsigned>(a.nch - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (tid < 32) {
+    const int lane = tid;
+    float lse[2][2];
+    for (int r = 0; r < 2; ++r) {
+      float M = kNegInf;
+      for (int cc = lane; cc < a.nch; cc += 32) {
+        M = fmaxf(M, __ldcg(&a.ws.sps_part_pq[(static_cast<size_t>(b) * a.nch + cc) * 2 + r].x));
+      }
+      M = warp_max(M);
+      ff tot{0.f, 0.f};
+      for (int c0w = 0; c0w < a.nch; c0w += 32) {
+        const int cc = c0w + lane;
+        ff val{0.f, 0.f};
+        if (cc < a.nch && M > kNegInf) {
+          const float4 q = __ldcg(&a.ws.sps_part_pq[(static_cast<size_t>(b) * a.nch + cc) * 2 + r]);
+          if (q.x > kNegInf) val = ff_mul(ff{q.y, q.z}, ff_norm(weight_term<false>(q.x, M, 1.f, s_tab)));
+        }
+        tot = ff_add(tot, warp_ff_sum(val));
+      }
+      const ff l = ff_from_double(static_cast<double>(M) + log(ff_to_double(tot)));
+      lse[r][0] = l.hi;
+      lse[r][1] = l.lo;
+    }
+    if (lane == 0) {
+      a.ws.sps_stats[b] = make_float4(lse[0][0], lse[0][1], lse[1][0], lse[1][1]);
+      a.ws.sps_ticket_a[b] = 0u;
+    }
+  }
+}
+
+// Residual weight max(0, p_v - q_v) of vocabulary index i.
+template <typename T>
+__device__ __forceinline__ ff residual_term(const char *prow, const char *qrow, int64_t i, ff lp,
+                                            ff lq, const float2 *tab) {
+  using Tr = LogitTraits<T>;
+  const ff p = ff_norm(prob_term(Tr::scalar(prow, i), lp, tab));
+  const ff q = ff_norm(prob_term(Tr::scalar(qrow, i), lq, tab));
+  const ff d = ff_sub(p, q);
+  return d.hi > 0.f ? d : ff{0.f, 0.f};
+}
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kThreads) sps_residual_kernel(const SpsArgs a) {
+  using G = ChunkGeom<T>;
+  using Tr = LogitTraits<T>;
+  constexpr bool kExactDiff = sizeof(T) != 4;
+  __shared__ float2 s_ff[kWarps];
+  __shared__ float2 s_tab[64];
+  __shared__ int s_int[2 * kWarps];
+  __shared__ int s_last;
+  __shared__ int s_sel;
+  __shared__ int s_mode;
+  __shared__ float s_sel_m;
+  __shared__ ff s_rem;
+  const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
+  const int jr = a.ws.sps_rej[b];
+  if (jr < 0) return;
+  stage_exp2_table(s_tab);
+  const float4 st = a.ws.sps_stats[b];
+  const ff lp{st.x, st.y}, lq{st.z, st.w};
+  const int64_t c0 = static_cast<int64_t>(c) * G::kCH;
+  const int n_valid = static_cast<int>(min(static_cast<int64_t>(G::kCH), a.V - c0));
+  const char *prow = a.target + (static_cast<size_t>(b) * (a.K + 1) + jr) * static_cast<size_t>(a.V) * G::kESZ;
+  const char *qrow = a.draft + (static_cast<size_t>(b) * a.K + jr) * static_cast<size_t>(a.V) * G::kESZ;
+  float xp[G::kEPT], xq[G::kEPT];
+  load_chunk<T, VEC>(prow + c0 * G::kESZ, n_valid, xp);
+  load_chunk<T, VEC>(qrow + c0 * G::kESZ, n_valid, xq);
+  __syncthreads();  // table staged
+  ff R{0.f, 0.f};
+#pragma unroll
+  for (int e = 0; e < G::kEPT; ++e) {
+    const ff p = ff_norm(prob_term(xp[e], lp, s_tab));
+    const ff q = ff_norm(prob_term(xq[e], lq, s_tab));
+    const ff d = ff_sub(p, q);
+    if (d.hi > 0.f) ff_accum(R, d);
+  }
+  R = block_ff_sum(ff_norm(R), s_ff);
+  if (tid == 0) {
+    a.ws.sps_part_r[static_cast<size_t>(b) * a.nch + c] = make_float2(R.hi, R.lo);
+    __threadfence();
+    s_last = atomicAdd(&a.ws.sps_ticket_b[b], 1u) == static_cast<unsigned>(a.nch - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (tid < 32) {
+    const int lane = tid;
+    const float2 *pr = a.ws.sps_part_r + static_cast<size_t>(b) * a.nch;
+    ff total{0.f, 0.f};
+    for (int c0w = 0; c0w < a.nch; c0w += 32) {
+      const int cc = c0w + lane;
+      ff val{0.f, 0.f};
+      if (cc < a.nch) val = ff{__ldcg(&pr[cc].x), __ldcg(&pr[cc].y)};
+      total = ff_add(total, warp_ff_sum(val));
+    }
+    const float u = philox_uniform(a.seed, a.step, b, jr, SMC_PURPOSE_RESIDUAL);
+    ff rem{0.f, 0.f};
+    int sel, mode;
+    float sel_m = 0.f;
+    if (total.hi > 0.f) {
+      mode = 0;  // residual mass, absolute units in every chunk
+      sel = warp_find_chunk(a.nch, ff_mul_f(total, u),
+                            [&](int cc, ff *val, ff *f) {
+                              *val = ff{__ldcg(&pr[cc].x), __ldcg(&pr[cc].y)};
+                            },
+                            &rem);
+    } else {
+      mode = 1;  // no residual mass (p_j == q_j up to rounding): draw from p_j
+      const float4 *pq = a.ws.sps_part_pq + static_cast<size_t>(b) * a.nch * 2;
+      float M = kNegInf;
+      for (int cc = lane; cc < a.nch; cc += 32) M = fmaxf(M, __ldcg(&pq[cc * 2].x));
+      M = warp_max(M);
+      auto chunk_mass = [&](int cc, ff *val, ff *f) {
+        const float4 q = __ldcg(&pq[cc * 2]);
+        if (q.x > kNegInf) {
+          *f = ff_norm(weight_term<false>(q.x, M, 1.f, s_tab));
+          *val = ff_mul(ff{q.y, q.z}, *f);
+        }
+      };
+      ff ptot{0.f, 0.f};
+      for (int c0w = 0; c0w < a.nch; c0w += 32) {
+        const int cc = c0w + lane;
+        ff val{0.f, 0.f}, f{1.f, 0.f};
+        if (cc < a.nch) chunk_mass(cc, &val, &f);
+        ptot = ff_add(ptot, warp_ff_sum(val));
+      }
+      sel = warp_find_chunk(a.nch, ff_mul_f(ptot, u), chunk_mass, &rem);
+      if (sel >= 0) sel_m = __ldcg(&pq[sel * 2].x);
+    }
+    if (lane == 0) {
+      s_sel = sel;
+      s_mode = mode;
+      s_sel_m = sel_m;
+      s_rem = rem;
+      a.ws.sps_ticket_b[b] = 0u;
+    }
+  }
+  __syncthreads();
+  const int sel = s_sel;
+  int tok = -1;
+  if (sel >= 0) {
+    const int64_t sc0 = static_cast<int64_t>(sel) * G::kCH;
+    const int len = static_cast<int>(min(static_cast<int64_t>(G::kCH), a.V - sc0));
+    if (s_mode == 0) {
+      tok = block_select_in_chunk(
+          sc0, len, s_rem,
+          [&](int64_t i) { return residual_term<T>(prow, qrow, i, lp, lq, s_tab); }, s_ff, s_int);
+    } else {
+      const float cm = s_sel_m;
+      tok = block_select_in_chunk(
+          sc0, len, s_rem,
+          [&](int64_t i) { return weight_term<kExactDiff>(Tr::scalar(prow, i), cm, 1.f, s_tab); },
+          s_ff, s_int);
+    }
+  }
+  if (tid == 0) a.tokens_out[static_cast<size_t>(b) * (a.K + 1) + jr] = tok;
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cudaError_t launch_sps_residual(const Shape &s, const void *target, const void *draft,
+                                int32_t *tokens_out, const Workspace &ws, cudaStream_t stream) {
+  SpsArgs a{};
+  a.target = static_cast<const char *>(target);
+  a.draft = static_cast<const char *>(draft);
+  a.B = s.B; a.K = s.K; a.V = s.V;
+  a.nch = chunks_per_row(s.dtype, s.V);
+  a.seed = s.seed; a.step = s.step;
+  a.tokens_out = tokens_out;
+  a.ws = ws;
+  const int esz = s.dtype == SMC_BF16 ? 2 : 4;
+  const bool vec = aligned16(target) && aligned16(draft) && (static_cast<long long>(s.V) * esz) % 16 == 0;
+  dim3 g(a.nch, s.B), blk(kThreads);
+  if (s.dtype == SMC_BF16) {
+    if (vec) {
+      sps_stats_kernel<bf16_tag, true><<<g, blk, 0, stream>>>(a);
+      sps_residual_kernel<bf16_tag, true><<<g, blk, 0, stream>>>(a);
+    } else {
+      sps_stats_kernel<bf16_tag, false><<<g, blk, 0, stream>>>(a);
+      sps_residual_kernel<bf16_tag, false><<<g, blk, 0, stream>>>(a);
+    }
+  } else {
+    if (vec) {
+      sps_stats_kernel<float, true><<<g, blk, 0, stream>>>(a);
+      sps_residual_kernel<float, true><<<g, blk, 0, stream>>>(a);
+    } else {
+      sps_stats_kernel<float, false><<<g, blk, 0, stream>>>(a);
+      sps_residual_kernel<float, false><<<g, blk, 0, stream>>>(a);
+    }
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace smcsd
