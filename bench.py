@@ -1,0 +1,458 @@
+"""Throughput of the SMC-SD per-step particle update on GB300.
+
+One step = one smc_step call over the batched-serving workload (16 prompts x
+16 particles, K = 4 drafted tokens, V = 128256, bf16 logits, KV block tables
+with a 2048-token shared prefix): every logit row's log-sum-exp and drafted
+token gather, the bonus-token draw, the importance-weight update, ESS,
+systematic resampling when ESS < N/2, token emission and the block-table
+remap.  The metric is particle-tokens per second (B*N*(K+1) tokens per step).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (torchrun, one rank per GPU): prompts are independent, so every rank
+runs its own 16 prompts (weak scaling, no collective on the data path); the
+timed region is bracketed by barriers and the slowest rank's time is used.
+
+Inputs are resident in HBM before timing; each step reads 591 MB of logits,
+more than the 129 MB L2, from a ring of two distinct step inputs, so no step
+finds its logits in L2.  The KV state and weights are reset every 128 steps
+(the workload's episode length), outside the timed region.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SMC step particle-tokens/s at V=128256 bf16; % of GB300 HBM roofline"
+WORKLOAD = "batched_serving_v128256"
+KERNEL = "step_rows_kernel"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "step_rows_kernel_batched_serving_v128256.md")
+KERNEL_SOURCES = ["smc_step.cu", "row_common.cuh", "device_common.cuh", "exp2_table.cuh"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4096)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--sigma-d", type=float, default=None, help="draft noise override")
+    ap.add_argument("--episode", type=int, default=128, help="steps between KV resets")
+    ap.add_argument("--e2e-steps", type=int, default=64)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU work budget of the oracle baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload(args):
+    from smc_speculative_decoding_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.sigma_d is not None:
+        w = w.with_(sigma_d=args.sigma_d)
+    return w
+
+
+def algorithmic_bytes(w, T, resampled_prompts):
+    """Bytes one step must move: every logit once, the particle state, and the
+    block tables of prompts that resampled (read + write)."""
+    logits = w.B * w.N * (2 * w.K + 1) * w.V * w.bytes_per_logit
+    particle = w.B * w.N * (4 * w.K        # drafted tokens read
+                            + 8             # log-weight read + write
+                            + 4 * (w.K + 1)  # emitted tokens
+                            + 4)            # ancestor
+    tables = resampled_prompts * w.N * (T * 4 * 2 + 8)
+    return logits + particle + tables
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "smc_speculative_decoding_gb300", "csrc")
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    text = open(PROFILE_SUMMARY).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s+kernel_source_hash:\s*([0-9a-f]+)", text)
+    if not m or m.group(2) != kernel_hash():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows]
+        load = [float(r[1]) for r in rows if float(r[3]) > 200.0] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": float(rows[0][2]),
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(load),
+                "power_w_max": max(float(r[3]) for r in rows)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, world, rank, local):
+    import smc_speculative_decoding_gb300 as smcsd
+    from smc_speculative_decoding_gb300 import build
+    from smc_speculative_decoding_gb300.workloads import make_step_inputs, make_kv_state
+
+    build.build()
+    dev = f"cuda:{local}"
+    w = workload(args)
+    T, P = w.kv_dims(args.episode)
+    ring = [make_step_inputs(w, 1000 + rank, device=dev, step=s) for s in range(2)]
+    kv0 = make_kv_state(w.B, w.N, w.prefix, w.block_size, T, P, device=dev)
+    kv = {k: v.clone() for k, v in kv0.items()}
+    p0 = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, 0)
+    kv_s = smcsd.make_kv(p0, kv, w.block_size)
+    ws = smcsd.alloc_workspace(p0, kv_s, device=dev)
+    lw = torch.zeros(w.B * w.N, device=dev)
+    tok = torch.empty(w.B * w.N * (w.K + 1), dtype=torch.int32, device=dev)
+    anc = torch.empty(w.B * w.N, dtype=torch.int32, device=dev)
+    ess = torch.empty(w.B, device=dev)
+    res = torch.empty(w.B, dtype=torch.int32, device=dev)
+    res_count = torch.zeros(w.B, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def reset():
+        for k in kv:
+            kv[k].copy_(kv0[k])
+        lw.zero_()
+
+    def step(s, count=False):
+        # s is the global step counter (the Philox counter of the step)
+        inp = ring[s % 2]
+        p = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, s)
+        smcsd.smc_step(p, inp["target"], inp["draft"], inp["draft_tokens"],
+                       lw, tok, anc, ess, res, kv=kv_s, workspace=ws, stream=stream)
+        if count:
+            res_count.add_(res)
+
+    # warm-up
+    reset()
+    for s in range(args.warmup):
+        step(s)
+        if (s + 1) % args.episode == 0:
+            reset()
+    torch.cuda.synchronize()
+    assert smcsd.smc_device_status(ws, clear=True) == 0
+
+    # timed region: episodes of `episode` steps, KV reset between them (untimed)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    total_ms = 0.0
+    launch_ms = []
+    done = 0
+    while done < args.steps:
+        reset()
+        n = min(args.episode, args.steps - done)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        ev[0].record(stream)
+        for s in range(n):
+            step(args.warmup + done + s, count=True)
+            ev[s + 1].record(stream)
+        torch.cuda.synchronize()
+        total_ms += ev[0].elapsed_time(ev[n])
+        launch_ms += [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+        done += n
+    barrier(world)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    bits = smcsd.smc_device_status(ws, clear=True)
+    if bits:
+        raise RuntimeError(f"device status during timing: {smcsd.status_names(bits)}")
+    total_ms = max_over_ranks(total_ms, world)
+    resampled_prompts = float(res_count.sum().item()) / args.steps
+
+    ptok = w.particle_tokens * args.steps * world
+    value = ptok / (total_ms / 1e3)
+    avg_launch_ms = float(np.mean(launch_ms))
+    bytes_step = algorithmic_bytes(w, T, resampled_prompts)
+    achieved = bytes_step / (avg_launch_ms / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "particle-tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "N": w.N, "K": w.K, "V": w.V,
+                   "logits": w.dtype, "sigma_t": w.sigma_t, "top_m": w.top_m,
+                   "sigma_d": w.sigma_d, "alpha": w.alpha, "ess_frac": w.ess_frac,
+                   "prefix": w.prefix, "block_size": w.block_size, "episode_steps": args.episode,
+                   "parallelism": f"prompt-sharded x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: 591 MB of logits per step from a ring of "
+                         "2 distinct steps (129 MB L2)"},
+        "steps_per_s": args.steps * world / (total_ms / 1e3),
+        "resampled_prompts_per_step": resampled_prompts,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic(),
+                     "algorithmic_bytes_per_launch": bytes_step,
+                     "avg_launch_ms": avg_launch_ms, "kernel": KERNEL,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if not args.no_e2e:
+        out["e2e"] = run_e2e(args, w, dev, smcsd, world)
+    return out
+
+
+def run_e2e(args, w, dev, smcsd, world):
+    """Same metric through the public API with host buffers: every step copies
+    its logits and drafted tokens from pinned host memory and reads the emitted
+    tokens and weights back, inside the timed region."""
+    from smc_speculative_decoding_gb300.workloads import make_step_inputs, make_kv_state
+    T, P = w.kv_dims(args.episode)
+    host = []
+    for s in range(2):
+        inp = make_step_inputs(w, 2000, device=dev, step=s)
+        host.append({k: v.cpu().pin_memory() for k, v in inp.items()})
+        del inp
+    d_in = {k: torch.empty_like(v, device=dev) for k, v in host[0].items()}
+    kv0 = make_kv_state(w.B, w.N, w.prefix, w.block_size, T, P, device=dev)
+    kv = {k: v.clone() for k, v in kv0.items()}
+    p0 = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, 0)
+    kv_s = smcsd.make_kv(p0, kv, w.block_size)
+    ws = smcsd.alloc_workspace(p0, kv_s, device=dev)
+    lw = torch.zeros(w.B * w.N, device=dev)
+    tok = torch.empty(w.B * w.N * (w.K + 1), dtype=torch.int32, device=dev)
+    anc = torch.empty(w.B * w.N, dtype=torch.int32, device=dev)
+    ess = torch.empty(w.B, device=dev)
+    res = torch.empty(w.B, dtype=torch.int32, device=dev)
+    h_tok = torch.empty(tok.shape, dtype=torch.int32).pin_memory()
+    h_lw = torch.empty(lw.shape, dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream()
+    n_steps = min(args.e2e_steps, args.steps)
+    h2d = sum(v.numel() * v.element_size() for v in host[0].values())
+    d2h = h_tok.numel() * 4 + h_lw.numel() * 4
+
+    def one(s):
+        for k in d_in:
+            d_in[k].copy_(host[s % 2][k], non_blocking=True)
+        p = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, s)
+        smcsd.smc_step(p, d_in["target"], d_in["draft"], d_in["draft_tokens"], lw, tok, anc, ess,
+                       res, kv=kv_s, workspace=ws, stream=stream)
+        h_tok.copy_(tok, non_blocking=True)
+        h_lw.copy_(lw, non_blocking=True)
+
+    for s in range(3):
+        one(s)
+    torch.cuda.synchronize()
+    for k in kv:
+        kv[k].copy_(kv0[k])
+    lw.zero_()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(n_steps):
+        one(s)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
+    return {"value": w.particle_tokens * n_steps * world / (ms / 1e3), "unit": "particle-tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_steps,
+            "ms_per_step": ms / n_steps}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline of our line)
+# ---------------------------------------------------------------------------
+def oracle_prompt_steps(w, budget_s, max_steps=None, seed=3000):
+    """Runs the fp64 oracle on one prompt at a time (N particles, full rows,
+    weights, resampling and KV remap) until `budget_s` seconds or
+    `max_steps` prompt-steps; returns (prompt_steps, seconds)."""
+    from smc_speculative_decoding_gb300.workloads import make_step_inputs, make_kv_state, \
+        to_numpy_logits
+    from oracle import smc as osmc, kv as okv
+    w1 = w.with_(B=1)
+    T, P = w1.kv_dims(128)
+    inputs = []
+    for s in range(2):
+        inp = make_step_inputs(w1, seed, device="cpu", step=s)
+        inputs.append((to_numpy_logits(inp["target"]), to_numpy_logits(inp["draft"]),
+                       inp["draft_tokens"].numpy().astype(np.int64)))
+    kv = {k: v.numpy().astype(np.int64) for k, v in
+          make_kv_state(1, w1.N, w1.prefix, w1.block_size, T, P).items()}
+    lw = np.zeros((1, w1.N))
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        tgt, dft, x = inputs[done % 2]
+        r = osmc.smc_step(tgt, dft, x, lw, alpha=w1.alpha, ess_frac=w1.ess_frac, seed=0,
+                          step=done, dtype=w1.dtype)
+        k2 = okv.remap_append(kv["tables"], kv["seq_len"], kv["refcount"], kv["free_list"],
+                              kv["free_top"], r["ancestors"], r["resampled"], w1.K + 1,
+                              w1.block_size, P)
+        kv = {k: k2[k] for k in ("tables", "seq_len", "refcount", "free_list", "free_top")}
+        lw = r["log_weights"]
+        done += 1
+        if done % 100 == 0:
+            kv = {k: v.numpy().astype(np.int64) for k, v in
+                  make_kv_state(1, w1.N, w1.prefix, w1.block_size, T, P).items()}
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_steps is not None and done >= max_steps):
+            return done, el
+
+
+def cpu_baseline(w, budget_s):
+    n, el = oracle_prompt_steps(w, budget_s)
+    return {"value": n * w.N * (w.K + 1) / el, "unit": "particle-tokens/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{n} prompt-steps of {w.name} (1 prompt x {w.N} particles x "
+                      f"{2 * w.K + 1} rows of V={w.V}, tail and KV remap) in {el:.1f} s, "
+                      f"numpy fp64, single thread"}
+
+
+def run_reference(args, world, rank):
+    """The oracle timed on host cores, as the reference arm: each step is a
+    bounded sample of the workload (one prompt of 16), the whole run kept to a
+    few minutes."""
+    w = workload(args)
+    budget = 150.0
+    # warm-up sample steps
+    oracle_prompt_steps(w, 5.0, max_steps=max(1, min(args.warmup, 3)))
+    n, el = oracle_prompt_steps(w, budget, max_steps=args.steps)
+    value = n * w.N * (w.K + 1) / el
+    sample = (f"{n} of {args.steps} steps timed (time budget {budget:.0f} s); each step one "
+              f"prompt of {w.B} ({w.N} particles x {2 * w.K + 1} rows of V={w.V}, weights, "
+              f"resampling, KV remap), numpy fp64, single thread")
+    return {"metric": METRIC, "value": value, "unit": "particle-tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / n * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "B": w.B, "N": w.N, "K": w.K, "V": w.V,
+                       "logits": w.dtype, "sigma_d": w.sigma_d, "prefix": w.prefix},
+            "cpu_baseline": {"value": value, "unit": "particle-tokens/s", "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "particle-tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, world, rank)), flush=True)
+        return 0
+    world, rank, local = dist_setup(args.gpus)
+    out = run_ours(args, world, rank, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(workload(args), args.cpu_seconds)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
