@@ -210,6 +210,34 @@ int32_t sps_verify(const smc_params *p, const void *target_logits,
                    int32_t *tokens_out, int32_t *n_emitted, void *workspace,
                    size_t ws_bytes, void *stream);
 
+
+/* ---- allocation-free variant of smc_step -------------------------------
+ * No counterpart in the pages: a deployment convenience.  For callers that
+ * cannot allocate device memory themselves (a plugin inside a serving
+ * runtime whose allocator owns the GPU's memory, or a loop where cudaMalloc,
+ * which may synchronise the device, is not allowed) and so have no
+ * workspace to pass.  Same operation, arguments and outputs as smc_step,
+ * without workspace arguments: the scratch is a fixed array of
+ * SMC_NOALLOC_WS_BYTES bytes in the library's own device memory, which every
+ * GPU that loads the library holds until the process exits.  Calls no
+ * allocating routine.
+ *   - Shapes whose smc_workspace_bytes(p, kv) exceeds SMC_NOALLOC_WS_BYTES
+ *     are rejected with SMC_ERR_WORKSPACE before anything is launched.
+ *   - status_bits: DEVICE pointer to one int32, written (asynchronously, on
+ *     `stream`) with this call's SMC_DEV_* bits.
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array; each call clears the
+ *     parts that must start at zero.  Calls whose GPU work overlaps (issued
+ *     on different streams without ordering) race on the array. */
+#define SMC_NOALLOC_WS_BYTES (8u << 20)
+int32_t smc_step_noalloc(const smc_params *p, const void *target_logits,
+                         const void *draft_logits, const int32_t *draft_tokens,
+                         float *log_weights, int32_t *tokens_out, int32_t *ancestors,
+                         float *ess, int32_t *resampled, const smc_kv *kv,
+                         int32_t *status_bits, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

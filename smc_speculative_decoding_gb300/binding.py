@@ -223,3 +223,30 @@ def sps_verify(params, target_logits, draft_logits, draft_tokens, tokens_out, n_
         _ptr(tokens_out, "tokens_out", torch.int32, B * (K + 1)),
         _ptr(n_emitted, "n_emitted", torch.int32, B),
         _ptr(workspace, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def smc_step_noalloc(params, target_logits, draft_logits, draft_tokens, log_weights, tokens_out,
+                     ancestors, ess, resampled, status_bits, kv=None, stream=None):
+    """smc_step without a caller workspace: the library's own fixed scratch
+    array is used (see smc_step_noalloc in smcsd.h).  status_bits is a CUDA
+    int32 tensor of one element that receives this call's device status."""
+    fn = lib().smc_step_noalloc
+    fn.restype = ctypes.c_int32
+    fn.argtypes = [ctypes.POINTER(smc_params)] + [ctypes.c_void_p] * 8 + \
+        [ctypes.POINTER(smc_kv), ctypes.c_void_p, ctypes.c_void_p]
+    B, N, K, V = params.B, params.N, params.K, params.V
+    ld = _logit_dtype(params)
+    args = [
+        _ptr(target_logits, "target_logits", ld, B * N * (K + 1) * V),
+        _ptr(draft_logits, "draft_logits", ld, B * N * K * V),
+        _ptr(draft_tokens, "draft_tokens", torch.int32, B * N * K),
+        _ptr(log_weights, "log_weights", torch.float32, B * N),
+        _ptr(tokens_out, "tokens_out", torch.int32, B * N * (K + 1)),
+        _ptr(ancestors, "ancestors", torch.int32, B * N),
+        _ptr(ess, "ess", torch.float32, B),
+        _ptr(resampled, "resampled", torch.int32, B),
+    ]
+    _check("smc_step_noalloc", fn(ctypes.byref(params), *args,
+                                  ctypes.byref(kv) if kv is not None else None,
+                                  _ptr(status_bits, "status_bits", torch.int32, 1),
+                                  _stream(stream)))
