@@ -37,8 +37,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "SMC step particle-tokens/s at V=128256 bf16; % of GB300 HBM roofline"
 WORKLOAD = "batched_serving_v128256"
-KERNEL = "step_rows_kernel"
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "step_rows_kernel_batched_serving_v128256.md")
+KERNEL = "row_stream_kernel"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "row_stream_kernel_batched_serving_v128256.md")
 KERNEL_SOURCES = ["smc_step.cu", "row_common.cuh", "device_common.cuh", "exp2_table.cuh"]
 
 

@@ -36,7 +36,8 @@
  *     token id, a non-finite logit, an exhausted block pool ...) set bits of a
  *     status word inside the workspace; read them with smc_device_status().
  *     When a status bit is set the outputs of that call are unspecified.
- *     No kernel traps or spins: a bad input never hangs or faults the GPU.
+ *     No kernel traps, and every wait inside a kernel is bounded: a bad input
+ *     never hangs or faults the GPU.
  *   - Logits: `dtype` SMC_F32 (IEEE fp32) or SMC_BF16 (bfloat16 stored as
  *     16-bit words).  Arithmetic is fp32 with fp32 accumulation, except the
  *     sampling sums (bonus and residual tokens), which are carried in
@@ -73,7 +74,10 @@ extern "C" {
 #define SMC_DEV_ALL_ZERO_WEIGHT  0x08  /* every particle of a prompt has weight 0  */
 #define SMC_DEV_POOL_EXHAUSTED   0x10  /* free-block stack cannot cover an append  */
 #define SMC_DEV_TABLE_OVERFLOW   0x20  /* a particle would need more than T blocks */
-#define SMC_DEV_BAD_BLOCK        0x40  /* a block id outside its prompt's pool     */
+#define SMC_DEV_BAD_BLOCK        0x40  /* a block id outside its prompt's pool, or a
+                                          negative or oversized token count      */
+#define SMC_DEV_TIMEOUT          0x80  /* a bounded wait for a bulk copy gave up;
+                                          re-initialise the workspace            */
 
 /* ---- limits ------------------------------------------------------------ */
 #define SMC_MAX_N  256        /* particles per prompt                           */

@@ -20,7 +20,7 @@ SMC_F32, SMC_BF16 = 0, 1
 # device status bits (smcsd.h)
 DEV_BITS = {
     0x01: "bad_token", 0x02: "nonfinite", 0x04: "empty_row", 0x08: "all_zero_weight",
-    0x10: "pool_exhausted", 0x20: "table_overflow", 0x40: "bad_block",
+    0x10: "pool_exhausted", 0x20: "table_overflow", 0x40: "bad_block", 0x80: "timeout",
 }
 
 

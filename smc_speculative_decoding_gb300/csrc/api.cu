@@ -28,9 +28,12 @@ size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws) 
   const size_t o_sa = take(sizeof(unsigned) * s.B);
   const size_t o_sb = take(sizeof(unsigned) * s.B);
   const size_t o_bm = take(sizeof(unsigned) * s.B * words);
+  const size_t o_wc = take(sizeof(unsigned) * 4);
   const size_t zero_bytes = off;
   // scratch that every call overwrites before reading
   const size_t o_part = take(sizeof(RowPartial) * rows * nch);
+  const size_t o_ip = take(sizeof(float2) * rows * nch * 8);
+  const size_t o_bp = take(sizeof(int4) * static_cast<size_t>(s.B) * s.N * nch * 8);
   const size_t o_res = take(sizeof(RowResult) * rows);
   const size_t o_rej = take(sizeof(int32_t) * s.B);
   const size_t o_sst = take(sizeof(float4) * s.B);
@@ -46,7 +49,11 @@ size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws) 
     ws->sps_ticket_a = reinterpret_cast<unsigned *>(p + o_sa);
     ws->sps_ticket_b = reinterpret_cast<unsigned *>(p + o_sb);
     ws->kv_bitmap = reinterpret_cast<unsigned *>(p + o_bm);
+    ws->work_counter = reinterpret_cast<unsigned *>(p + o_wc);
+    ws->exit_counter = ws->work_counter + 2;
     ws->partials = reinterpret_cast<RowPartial *>(p + o_part);
+    ws->item_part = reinterpret_cast<float2 *>(p + o_ip);
+    ws->bonus_part = reinterpret_cast<int4 *>(p + o_bp);
     ws->results = reinterpret_cast<RowResult *>(p + o_res);
     ws->sps_rej = reinterpret_cast<int32_t *>(p + o_rej);
     ws->sps_stats = reinterpret_cast<float4 *>(p + o_sst);
@@ -130,6 +137,7 @@ const char *smc_strerror(int32_t code) {
     case SMC_DEV_POOL_EXHAUSTED: return "device: free block stack exhausted";
     case SMC_DEV_TABLE_OVERFLOW: return "device: block table too short";
     case SMC_DEV_BAD_BLOCK: return "device: block id outside its prompt's pool or bad KV state";
+    case SMC_DEV_TIMEOUT: return "device: a bounded wait gave up; re-initialise the workspace";
     default: return code > 0 ? "device: several status bits set" : "unknown error";
   }
 }

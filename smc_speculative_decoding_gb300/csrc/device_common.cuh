@@ -104,22 +104,28 @@ __device__ __forceinline__ ff ff_from_double(double x) {
 // `tab` points at the table staged in shared memory.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ ff accurate_exp2(float yh, float yl, const float2 *tab) {
-  if (!(yh > -120.f)) return {0.f, 0.f};           // below 2^-120 (or NaN -> 0; NaN
-                                                  // rows are reported by the fast path)
-  const float k = rintf(yh * 64.f);
-  const float rh = fmaf(k, -0.015625f, yh);        // exact: y_hi - k/64
+  // below 2^-120 the weight is taken as 0 (and -inf or NaN inputs give 0;
+  // NaN rows are reported separately)
+  const bool live = yh > -120.f;
+  const float yc = fmaxf(yh, -120.f);
+  // round yc*64 to an integer ki with the 1.5*2^23 shift: the low mantissa
+  // bits of t then hold ki, a multiple-of-64 offset from the shift's pattern
+  constexpr float kShift = 12582912.f;               // 1.5 * 2^23
+  const float t = fmaf(yc, 64.f, kShift);
+  const float k = t - kShift;                        // ki as a float, exact
+  const int bits = __float_as_int(t) - 0x4B400000;   // ki
+  const float rh = fmaf(k, -0.015625f, yc);          // exact: y - ki/64
   const float r = rh + yl;
-  const int ki = static_cast<int>(k);
-  const int j = ki & 63;
-  const int n = ki >> 6;                           // floor division: ki = 64 n + j
+  const int j = bits & 63;
+  const int n = bits >> 6;                           // floor(ki / 64)
   float q = fmaf(r, kC4, kC3);
   q = fmaf(r, q, kC2);
   q = fmaf(r, q, kC1Lo);
-  const float p = fmaf(r, kC1Hi, r * q);           // 2^r - 1
-  const float2 t = tab[j];
-  const float lo = fmaf(t.x, p, fmaf(t.y, p, t.y));
-  const float sc = __int_as_float((n + 127) << 23); // 2^n, n >= -120 here
-  return {t.x * sc, lo * sc};
+  const float p = fmaf(r, kC1Hi, r * q);             // 2^r - 1
+  const float2 tv = tab[j];
+  const float lo = fmaf(tv.x, p, fmaf(tv.y, p, tv.y));
+  const float sc = __int_as_float((n + 127) << 23);  // 2^n, n >= -120
+  return live ? ff{tv.x * sc, lo * sc} : ff{0.f, 0.f};
 }
 
 // 2^(log2(e) * d) for d given as a float pair (d, dl): exp(d + dl).
@@ -148,6 +154,43 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+// Packed pairs of fp32 (one 64-bit register pair) for the sm_100+ f32x2 ops.
+__device__ __forceinline__ unsigned long long f2pack(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(unsigned long long r, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// Lane-wise max of two packed bfloat16 pairs that propagates NaN.
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+// Lane-wise max of two packed bfloat16 pairs (NaN yields the other operand).
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -318,6 +361,65 @@ __device__ __forceinline__ int block_min_i(int v, int *scratch) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
+}
+
+
+// ---------------------------------------------------------------------------
+// mbarrier and bulk-copy (TMA, non-tensor) primitives, sm_90+ PTX.
+// Every wait is bounded: it gives up after `limit` polls and returns false.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// try_wait suspends the thread until the phase completes or about
+// `suspend_ns` nanoseconds pass, so a waiting warp issues few instructions.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity,
+                                              uint32_t suspend_ns = 20000u) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(suspend_ns)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+  }
+  return false;
+}
+// Order this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// global to shared memory; completion is signalled on `bar` as tx bytes.
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes,
+                                              uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
 }
 
 // Device status word: OR in error bits (never traps, never waits).

@@ -25,12 +25,17 @@ struct KvArgs {
 // Workspace carve-up shared by every entry point.
 struct Workspace {
   unsigned *status;          // [1]  device status bits
-  unsigned *prompt_ticket;   // [B]
+  unsigned *prompt_ticket;   // [B]  (unused: the tail is its own kernel)
   unsigned *row_ticket;      // [rows]
   unsigned *sps_ticket_a;    // [B]
   unsigned *sps_ticket_b;    // [B]
   unsigned *kv_bitmap;       // [B * ceil(P/32)]
-  RowPartial *partials;      // [rows * nch]
+  unsigned *work_counter;    // [2]  next fast-row item, next bonus chunk (streaming kernel)
+  unsigned *exit_counter;    // [1]  CTAs of the streaming kernel that finished
+  RowPartial *partials;      // [rows * nch]  (per-chunk kernel)
+  float2 *item_part;         // [rows * nch * 8]  (m, s) per work item and warp (streaming kernel)
+  int4 *bonus_part;          // [B * N * nch * 8] (ref bits, fixed-point sum lo, hi, -)
+                             // per chunk and warp
   RowResult *results;        // [rows]
   int32_t *sps_rej;          // [B]  first rejected position, -1 if none
   float4 *sps_stats;         // [B]  precise (lse_p hi, lo, lse_q hi, lo) of row j

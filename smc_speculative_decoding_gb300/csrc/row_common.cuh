@@ -55,6 +55,9 @@ __device__ __forceinline__ void load_chunk(const char *chunk_base, int n_valid,
 // it matters); otherwise the rounding error of x - m is carried along.
 template <bool EXACT_DIFF>
 __device__ __forceinline__ ff weight_term(float x, float m, float alpha, const float2 *tab) {
+  if (EXACT_DIFF && alpha == 1.f) {  // bf16 logits, plain target: exp(x - m) directly
+    return accurate_exp(x - m, 0.f, tab);  // -inf gives yh = -inf -> 0
+  }
   if (!(x > kNegInf)) return {0.f, 0.f};
   float d, dl;
   if (EXACT_DIFF) {
@@ -73,6 +76,82 @@ __device__ __forceinline__ ff prob_term(float x, ff big_l, const float2 *tab) {
   if (!(x > kNegInf)) return {0.f, 0.f};
   const ff s = two_sum(x, -big_l.hi);
   return accurate_exp(s.hi, s.lo - big_l.lo, tab);
+}
+
+
+// ---------------------------------------------------------------------------
+// Sampling weights as exact fixed-point integers.
+//
+// weight_fixed returns exp(alpha (x - ref)) for x <= ref in units of 2^-52,
+// rounded to an integer: the exponential is evaluated in float-float (about
+// 3e-10 relative) and each of its two float parts is converted exactly, so a
+// sum of these integers is order-independent and exact, and a prefix sum can
+// be compared with a target without rounding.  Weights below 2^-60 are 0, so
+// -inf (and NaN) logits weigh 0.  A sum of 2^10 weights stays below 2^63.
+// ---------------------------------------------------------------------------
+constexpr int kFixBits = 52;
+
+template <bool EXACT_DIFF>
+__device__ __forceinline__ long long weight_fixed(float x, float ref, float alpha,
+                                                  const float2 *tab) {
+  float yh, yl;
+  if (EXACT_DIFF && alpha == 1.f) {           // bf16 logits, plain target: x - ref is exact
+    const float d = x - ref;
+    yh = d * kLog2eHi;
+    yl = fmaf(d, kLog2eLo, fmaf(d, kLog2eHi, -yh));
+  } else {
+    const ff s = two_sum(x, -ref);            // fp32 logits: keep the rounding of x - ref
+    ff ad = two_prod(alpha, s.hi);
+    ad.lo = fmaf(alpha, s.lo, ad.lo);
+    yh = ad.hi * kLog2eHi;
+    yl = fmaf(ad.hi, kLog2eHi, -yh) + fmaf(ad.hi, kLog2eLo, ad.lo * kLog2eHi);
+  }
+  const bool live = yh > -60.f;               // false for -inf and NaN
+  const float yc = fmaxf(yh, -60.f);
+  constexpr float kShift = 12582912.f;        // 1.5 * 2^23: rounds yc*64 into the low bits
+  const float t = fmaf(yc, 64.f, kShift);
+  const float k = t - kShift;
+  const int ki = __float_as_int(t) - 0x4B400000;
+  const float r = fmaf(k, -0.015625f, yc) + yl;  // y - ki/64, |r| <= 1/128 + tiny
+  float q = fmaf(r, kC4, kC3);
+  q = fmaf(r, q, kC2);
+  q = fmaf(r, q, kC1Lo);
+  const float p = fmaf(r, kC1Hi, r * q);      // 2^r - 1
+  const float2 tv = tab[ki & 63];             // 2^(j/64), float-float
+  const float lo = fmaf(tv.x, p, fmaf(tv.y, p, tv.y));
+  const float sc = __int_as_float(((ki >> 6) + kFixBits + 127) << 23);  // 2^(n + 52)
+  const long long v = __float2ll_rn(tv.x * sc) + __float2ll_rn(lo * sc);
+  return live ? v : 0ll;
+}
+
+__device__ __forceinline__ long long shfl_xor_ll(long long v, int o) {
+  return __shfl_xor_sync(0xffffffffu, v, o);
+}
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += shfl_xor_ll(v, o);
+  return v;
+}
+__device__ __forceinline__ long long warp_incl_scan_ll(long long v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long w = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += w;
+  }
+  return v;
+}
+// A non-negative float-float value times 2^52, rounded to an integer.
+__device__ __forceinline__ long long ff_to_fixed(ff a) {
+  const float sc = __int_as_float((kFixBits + 127) << 23);
+  return __float2ll_rn(a.hi * sc) + __float2ll_rn(a.lo * sc);
+}
+// A fixed-point integer (units of 2^-52) as a float-float value.
+__device__ __forceinline__ ff fixed_to_ff(long long v) {
+  const float hi = __ll2float_rn(v);
+  const long long rest = v - __float2ll_rn(hi);
+  const float sc = __int_as_float((127 - kFixBits) << 23);
+  return fast_two_sum(hi * sc, __ll2float_rn(rest) * sc);
 }
 
 __device__ __forceinline__ ff warp_ff_incl_scan(ff v) {

@@ -39,46 +39,63 @@ struct StepArgs {
 };
 
 // Blocks that hold `len` tokens (64-bit, so a corrupt length cannot overflow).
-__device__ __forceinline__ long long nblk(long long len, int bs) { return (len + bs - 1) / bs; }
-
 // ---------------------------------------------------------------------------
 // Normalise one prompt's log-weights, compute ESS and, below the threshold,
-// resample systematically.  Thread i < N holds lw_i.  On return s_anc[i]
-// holds the ancestor of particle i for every i < N.
+// resample systematically.  fp32 throughout (FP64 is a slow path on this
+// GPU, and the row statistics feeding the weights are fp32-accurate).  The
+// block version serves any N <= 256; thread i < N holds lw_i and, on return,
+// s_anc[i] holds the ancestor of particle i.
 // ---------------------------------------------------------------------------
-struct ResampleResult { bool resampled; double ess; };
+struct ResampleResult { bool resampled; float ess; };
 
-__device__ ResampleResult normalise_resample(int b, int N, double lw, bool valid, float ess_frac,
+// Smallest j in [0, n) with c[j] > pt, clamped to n-1.
+__device__ __forceinline__ int first_above(const float *c, int n, float pt) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (c[mid] > pt) hi = mid; else lo = mid + 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ float block_scan_f(float v, float *scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float w = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += w;
+  }
+  __syncthreads();
+  if (lane == 31) scratch[warp] = v;
+  __syncthreads();
+  float base = 0.f;
+  for (int w = 0; w < warp; ++w) base += scratch[w];
+  return base + v;
+}
+
+__device__ ResampleResult normalise_resample(int b, int N, float lw, bool valid, float ess_frac,
                                              uint64_t seed, uint32_t step, unsigned *status,
-                                             int *s_anc, double *s_c, double *s_dred) {
-  const double kInf = __longlong_as_double(0x7ff0000000000000ll);
+                                             int *s_anc, float *s_c, float *s_red) {
+  constexpr float kInf = -kNegInf;
   unsigned bits = 0;
   if (valid && (isnan(lw) || lw == kInf)) bits |= SMC_DEV_NONFINITE;
-  const double m = block_max_d(valid && !isnan(lw) ? lw : -kInf, s_dred);
-  const bool ok = m > -kInf && m < kInf;
-  if (threadIdx.x == 0 && m == -kInf) bits |= SMC_DEV_ALL_ZERO_WEIGHT;
+  const float m = block_max(valid && !isnan(lw) ? lw : kNegInf, s_red);
+  const bool ok = m > kNegInf && m < kInf;
+  if (threadIdx.x == 0 && m == kNegInf) bits |= SMC_DEV_ALL_ZERO_WEIGHT;
   if (bits) raise_status(status, bits);
-  const double e = (valid && ok) ? exp(lw - m) : 0.0;
-  const double se = block_sum_d(e, s_dred);
-  const double big_l = m + log(se);
-  const double w = (valid && ok) ? exp(lw - big_l) : 0.0;
-  const double w2 = block_sum_d(w * w, s_dred);
-  const double ess = 1.0 / w2;
-  const bool resample = ok && ess < static_cast<double>(ess_frac) * N;
+  const float e = (valid && ok) ? expf(lw - m) : 0.f;
+  const float big_l = m + logf(block_sum_f(e, s_red));
+  const float w = (valid && ok) ? expf(lw - big_l) : 0.f;
+  const float ess = 1.f / block_sum_f(w * w, s_red);
+  const bool resample = ok && ess < ess_frac * static_cast<float>(N);
   int anc = threadIdx.x;
   if (resample) {
-    const double c = block_scan_d(w, s_dred);
+    const float c = block_scan_f(w, s_red);
     if (valid) s_c[threadIdx.x] = c;
     __syncthreads();
     if (valid) {
-      const double u0 = philox_uniform(seed, step, b, 0, SMC_PURPOSE_RESAMPLE);
-      const double pt = (u0 + threadIdx.x) / N;
-      int lo = 0, hi = N - 1;            // smallest j with c_j > pt, clamped to N-1
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (s_c[mid] > pt) hi = mid; else lo = mid + 1;
-      }
-      anc = lo;
+      const float u0 = philox_uniform(seed, step, b, 0, SMC_PURPOSE_RESAMPLE);
+      anc = first_above(s_c, N, (u0 + static_cast<float>(threadIdx.x)) / static_cast<float>(N));
     }
   }
   if (valid) s_anc[threadIdx.x] = anc;
@@ -86,140 +103,200 @@ __device__ ResampleResult normalise_resample(int b, int N, double lw, bool valid
   return {resample, ess};
 }
 
+// The same for N <= 32, by warp 0 alone with shuffles (no CTA barrier).
+__device__ ResampleResult normalise_resample_warp(int b, int N, float lw, bool valid,
+                                                  float ess_frac, uint64_t seed, uint32_t step,
+                                                  unsigned *status, int *s_anc, float *s_c) {
+  constexpr float kInf = -kNegInf;
+  const int lane = threadIdx.x & 31;
+  unsigned bits = 0;
+  if (valid && (isnan(lw) || lw == kInf)) bits |= SMC_DEV_NONFINITE;
+  const float m = warp_max(valid && !isnan(lw) ? lw : kNegInf);
+  const bool ok = m > kNegInf && m < kInf;
+  if (lane == 0 && m == kNegInf) bits |= SMC_DEV_ALL_ZERO_WEIGHT;
+  if (bits) raise_status(status, bits);
+  float e = (valid && ok) ? expf(lw - m) : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
+  const float big_l = m + logf(e);
+  const float w = (valid && ok) ? expf(lw - big_l) : 0.f;
+  float w2 = w * w;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) w2 += __shfl_xor_sync(0xffffffffu, w2, o);
+  const float ess = 1.f / w2;
+  const bool resample = ok && ess < ess_frac * static_cast<float>(N);
+  int anc = lane;
+  if (resample) {
+    float c = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float v = __shfl_up_sync(0xffffffffu, c, o);
+      if (lane >= o) c += v;
+    }
+    if (valid) s_c[lane] = c;
+    __syncwarp();
+    if (valid) {
+      const float u0 = philox_uniform(seed, step, b, 0, SMC_PURPOSE_RESAMPLE);
+      anc = first_above(s_c, N, (u0 + static_cast<float>(lane)) / static_cast<float>(N));
+    }
+  }
+  if (valid) s_anc[lane] = anc;
+  __syncwarp();
+  return {resample, ess};
+}
+
 // ---------------------------------------------------------------------------
 // Block-table remap by ancestors and append of n_append tokens, one prompt,
 // one CTA.  Reference counts count table references; the free stack of prompt
 // b is free_list[b*P .. b*P + free_top[b]).  See smcsd.h (kv_blocktable_remap).
+//
+// old_t / old_l / bits hold a copy of the prompt's tables and token counts and
+// a cleared freed-block bitmap: in shared memory (staged) or in workspace
+// scratch.  s_nb holds each particle's used block count.  Loops run a warp
+// per particle and a lane per table slot, so no index needs a division.
 // ---------------------------------------------------------------------------
-__device__ void kv_remap_append_block(const KvArgs &kv, int b, int N, const int *s_anc,
-                                      bool resampled, int n_append, const Workspace &ws,
-                                      int *s_i, int *s_tail) {
+struct KvScratch {
+  int *old_t;      // [N*T]
+  int *old_l;      // [N]
+  unsigned *bits;  // [ceil(P/32)]
+};
+
+// Copy prompt b's tables and counts into the scratch and clear the bitmap,
+// using threads [t0, t0 + nt) of the CTA; no barrier inside.
+__device__ void kv_copy_in(const KvArgs &kv, int b, int N, const KvScratch &sc, int t0, int nt) {
+  const int T = kv.T;
+  const int words = (kv.P + 31) / 32;
+  const int32_t *tables = kv.tables + static_cast<size_t>(b) * N * T;
+  const int32_t *seq_len = kv.seq_len + static_cast<size_t>(b) * N;
+  const int t = static_cast<int>(threadIdx.x) - t0;
+  if (t < 0 || t >= nt) return;
+  const int NT = N * T;
+#pragma unroll 4
+  for (int idx = t; idx < NT; idx += nt) sc.old_t[idx] = tables[idx];
+  for (int i = t; i < N; i += nt) sc.old_l[i] = seq_len[i];
+  for (int w = t; w < words; w += nt) sc.bits[w] = 0u;
+}
+
+__device__ void kv_remap_append(const KvArgs &kv, int b, int N, const int *s_anc, bool resampled,
+                                int n_append, const Workspace &ws, int *s_i, int *s_tail,
+                                int *s_nb, const KvScratch &sc, bool copied) {
   __shared__ int s_flag;
   const int T = kv.T, bs = kv.block_size, P = kv.P;
   const int lo_id = b * P;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int words = (P + 31) / 32;
   int32_t *tables = kv.tables + static_cast<size_t>(b) * N * T;
   int32_t *seq_len = kv.seq_len + static_cast<size_t>(b) * N;
   int32_t *stack = kv.free_list + static_cast<size_t>(b) * P;
+  const long long cap = static_cast<long long>(T) * bs;  // tokens a full table holds
   if (tid == 0) {
     const int top0 = kv.free_top[b];
     s_flag = (top0 < 0 || top0 > P) ? 1 : 0;
     kv.n_cow[b] = 0;
   }
+  if (!copied) kv_copy_in(kv, b, N, sc, 0, kThreads);
   __syncthreads();
-  if (s_flag) {
-    if (tid == 0) raise_status(ws.status, SMC_DEV_BAD_BLOCK);
-    return;
-  }
   auto in_pool = [&](int blk) { return blk >= lo_id && blk < lo_id + P; };
+  auto fail = [&]() {
+    if (tid == 0) raise_status(ws.status, SMC_DEV_BAD_BLOCK);
+  };
+  if (s_flag) { fail(); return; }
+  // used blocks of every (pre-remap) particle; a bad count is an error
+  for (int i = tid; i < N; i += kThreads) {
+    const int len = sc.old_l[i];
+    if (len < 0 || len > cap) {
+      s_flag = 1;
+      s_nb[i] = 0;
+    } else {
+      s_nb[i] = static_cast<int>((static_cast<long long>(len) + bs - 1) / bs);
+    }
+  }
+  __syncthreads();
+  if (s_flag) { fail(); return; }
 
   if (resampled) {
-    int32_t *old_t = ws.kv_old_tables + static_cast<size_t>(b) * N * T;
-    int32_t *old_l = ws.kv_old_len + static_cast<size_t>(b) * N;
-    for (int idx = tid; idx < N * T; idx += kThreads) old_t[idx] = tables[idx];
-    for (int i = tid; i < N; i += kThreads) {
-      const int len = seq_len[i];
-      old_l[i] = len;
-      if (len < 0 || nblk(len, bs) > T) s_flag = 1;
-    }
-    __syncthreads();
-    for (int idx = tid; idx < N * T; idx += kThreads) {
-      const int i = idx / T, t = idx - (idx / T) * T;
-      const int len = old_l[i];
-      if (len >= 0 && t < nblk(len, bs) && !in_pool(old_t[idx])) s_flag = 1;
-    }
-    __syncthreads();
-    if (s_flag) {
-      if (tid == 0) raise_status(ws.status, SMC_DEV_BAD_BLOCK);
-      return;
-    }
-    // new references first, so no count touches 0 before every increment is in
-    for (int idx = tid; idx < N * T; idx += kThreads) {
-      const int i = idx / T, t = idx - (idx / T) * T;
-      const int a = s_anc[i];
-      const int nb_new = static_cast<int>(nblk(old_l[a], bs));
-      const int nb_old = static_cast<int>(nblk(old_l[i], bs));
-      if (t < nb_new) {
-        const int blk = old_t[a * T + t];
-        if (!(t < nb_old && old_t[idx] == blk)) atomicAdd(&kv.refcount[blk], 1);
+    for (int i = warp; i < N; i += kWarps) {
+      for (int t = lane; t < s_nb[i]; t += 32) {
+        if (!in_pool(sc.old_t[i * T + t])) s_flag = 1;
       }
     }
     __syncthreads();
-    unsigned *bitmap = ws.kv_bitmap + static_cast<size_t>(b) * ((P + 31) / 32);
-    for (int idx = tid; idx < N * T; idx += kThreads) {
-      const int i = idx / T, t = idx - (idx / T) * T;
+    if (s_flag) { fail(); return; }
+    // new references first, so no count touches 0 before every increment is in
+    for (int i = warp; i < N; i += kWarps) {
       const int a = s_anc[i];
-      const int nb_new = static_cast<int>(nblk(old_l[a], bs));
-      const int nb_old = static_cast<int>(nblk(old_l[i], bs));
-      if (t < nb_old) {
-        const int blk = old_t[idx];
-        if (!(t < nb_new && old_t[a * T + t] == blk)) {
-          if (atomicSub(&kv.refcount[blk], 1) == 1) {
-            const int rel = blk - lo_id;
-            atomicOr(&bitmap[rel >> 5], 1u << (rel & 31));
+      const int nb_new = s_nb[a], nb_old = s_nb[i];
+      for (int t = lane; t < nb_new; t += 32) {
+        const int blk = sc.old_t[a * T + t];
+        if (!(t < nb_old && sc.old_t[i * T + t] == blk)) atomicAdd(&kv.refcount[blk], 1);
+      }
+    }
+    __syncthreads();
+    for (int i = warp; i < N; i += kWarps) {
+      const int a = s_anc[i];
+      const int nb_new = s_nb[a], nb_old = s_nb[i];
+      for (int t = lane; t < T; t += 32) {
+        const int nv = sc.old_t[a * T + t];
+        if (t < nb_old) {
+          const int blk = sc.old_t[i * T + t];
+          if (!(t < nb_new && nv == blk)) {
+            if (atomicSub(&kv.refcount[blk], 1) == 1) {
+              const int rel = blk - lo_id;
+              atomicOr(&sc.bits[rel >> 5], 1u << (rel & 31));
+            }
           }
         }
+        tables[i * T + t] = nv;
       }
-      tables[idx] = old_t[a * T + t];
     }
-    for (int i = tid; i < N; i += kThreads) seq_len[i] = old_l[s_anc[i]];
+    for (int i = tid; i < N; i += kThreads) seq_len[i] = sc.old_l[s_anc[i]];
     __syncthreads();
     // push freed blocks in ascending id order
-    const int words = (P + 31) / 32;
     int top = kv.free_top[b];
     for (int w0 = 0; w0 < words; w0 += kThreads) {
       const int w = w0 + tid;
-      unsigned bits = w < words ? bitmap[w] : 0u;
+      unsigned fb = w < words ? sc.bits[w] : 0u;
       int total;
-      int pos = top + block_excl_scan_i(__popc(bits), s_i, &total);
-      if (bits) bitmap[w] = 0u;
-      while (bits) {
-        const int bit = __ffs(bits) - 1;
-        bits &= bits - 1;
+      int pos = top + block_excl_scan_i(__popc(fb), s_i, &total);
+      if (fb) sc.bits[w] = 0u;
+      while (fb) {
+        const int bit = __ffs(fb) - 1;
+        fb &= fb - 1;
         if (pos < P) stack[pos] = lo_id + w * 32 + bit;
         ++pos;
       }
       top += total;
     }
-    if (top > P) s_flag = 1;                 // counts did not match the tables
+    if (top > P) s_flag = 1;  // counts did not match the tables
     __syncthreads();
     if (tid == 0) kv.free_top[b] = min(top, P);
-    if (s_flag) {
-      if (tid == 0) raise_status(ws.status, SMC_DEV_BAD_BLOCK);
-      return;
-    }
+    if (s_flag) { fail(); return; }
     __syncthreads();
   }
   if (n_append <= 0) return;
 
-  // ---- append: fork shared partial tails, then grow ------------------------
+  // ---- append: particle i's table is now row src(i) of the copy -----------
   const bool valid = tid < N;
+  const int src = valid ? (resampled ? s_anc[tid] : tid) : 0;
   int len = 0, nb = 0, tail = -1;
   if (valid) {
-    len = seq_len[tid];
-    if (len < 0 || nblk(len, bs) > T) {
-      s_flag = 1;
-    } else {
-      nb = static_cast<int>(nblk(len, bs));
-      if (len % bs) {
-        tail = tables[tid * T + nb - 1];
-        if (!in_pool(tail)) s_flag = 1;
-      }
+    len = sc.old_l[src];
+    nb = s_nb[src];
+    if (len % bs) {
+      tail = sc.old_t[src * T + nb - 1];
+      if (!in_pool(tail)) s_flag = 1;
     }
     s_tail[tid] = tail;
   }
   __syncthreads();
-  if (s_flag) {
-    if (tid == 0) raise_status(ws.status, SMC_DEV_BAD_BLOCK);
-    return;
-  }
+  if (s_flag) { fail(); return; }
   int fork = 0;
   if (valid && tail >= 0) {
     for (int i2 = 0; i2 < tid; ++i2) {
       if (s_tail[i2] == tail) { fork = 1; break; }
     }
   }
-  const long long nb2 = valid ? nblk(static_cast<long long>(len) + n_append, bs) : 0;
+  const long long nb2 = valid ? (static_cast<long long>(len) + n_append + bs - 1) / bs : 0;
   if (valid && nb2 > T) s_flag = 2;
   const int grow = (valid && nb2 <= T) ? static_cast<int>(nb2) - nb : 0;
   int total_pops, n_forks;
@@ -269,56 +346,95 @@ __device__ void kv_remap_append_block(const KvArgs &kv, int b, int N, const int 
   }
 }
 
+// Shared-memory words a staged remap needs, and whether a shape fits.
+__host__ __device__ inline size_t kv_stage_words(int N, int T, int P) {
+  return static_cast<size_t>(N) * T + N + (P + 31) / 32;
+}
+constexpr size_t kKvStageMaxBytes = 96 * 1024;
+
+// Scratch of a remap: staged in `dyn` shared memory, or workspace scratch.
+__device__ inline KvScratch kv_scratch(const KvArgs &kv, int b, int N, const Workspace &ws,
+                                       int *dyn, bool staged) {
+  KvScratch sc;
+  if (staged) {
+    sc.old_t = dyn;
+    sc.old_l = dyn + static_cast<size_t>(N) * kv.T;
+    sc.bits = reinterpret_cast<unsigned *>(sc.old_l + N);
+  } else {
+    sc.old_t = ws.kv_old_tables + static_cast<size_t>(b) * N * kv.T;
+    sc.old_l = ws.kv_old_len + static_cast<size_t>(b) * N;
+    sc.bits = ws.kv_bitmap + static_cast<size_t>(b) * ((kv.P + 31) / 32);
+  }
+  return sc;
+}
+
 // ---------------------------------------------------------------------------
 // Prompt tails.
 // ---------------------------------------------------------------------------
 struct TailSmem {
-  double c[SMC_MAX_N];
-  double dred[kWarps];
+  float c[SMC_MAX_N];
+  float red[2 * kWarps];
   int anc[SMC_MAX_N];
   int bonus[SMC_MAX_N];
   int tail[SMC_MAX_N];
+  int nb[SMC_MAX_N];
   int ired[2 * kWarps];
 };
 
-__device__ void smc_tail(const StepArgs &a, int b, TailSmem &sm) {
+__device__ void smc_tail(const StepArgs &a, int b, TailSmem &sm, int *dyn, bool kv_staged) {
   const int N = a.N, K = a.K, rpp = 2 * K + 1;
   const int tid = threadIdx.x;
-  const bool valid = tid < N;
-  float lwf = 0.f;
-  if (valid) {
-    const int part = b * N + tid;
-    const RowResult *r = a.ws.results + static_cast<size_t>(part) * rpp;
-    double delta = 0.0;
-    for (int k = 0; k < K; ++k) {
-      const float4 rp = __ldcg(reinterpret_cast<const float4 *>(r + k));
-      const float4 rq = __ldcg(reinterpret_cast<const float4 *>(r + K + 1 + k));
-      delta += static_cast<double>(a.alpha) * (static_cast<double>(rp.y) - rp.x)
-             - (static_cast<double>(rq.y) - rq.x);
+  const bool small = N <= 32;
+  __shared__ int s_res;
+  const KvScratch sc = a.use_kv ? kv_scratch(a.kv, b, N, a.ws, dyn, kv_staged) : KvScratch{};
+  // with N <= 32, warp 0 does the weights while the other warps copy the KV tables
+  const bool weights_thread = small ? tid < 32 : true;
+  if (small && a.use_kv && tid >= 32) kv_copy_in(a.kv, b, N, sc, 32, kThreads - 32);
+  if (weights_thread) {
+    const bool valid = tid < N;
+    float lwf = 0.f;
+    if (valid) {
+      const int part = b * N + tid;
+      const RowResult *r = a.ws.results + static_cast<size_t>(part) * rpp;
+      const float4 rb = __ldcg(reinterpret_cast<const float4 *>(r + K));
+      const float lw0 = a.out.log_weights[part];
+      float delta = 0.f;
+#pragma unroll 4
+      for (int k = 0; k < K; ++k) {
+        const float4 rp = __ldcg(reinterpret_cast<const float4 *>(r + k));
+        const float4 rq = __ldcg(reinterpret_cast<const float4 *>(r + K + 1 + k));
+        delta += a.alpha * (rp.y - rp.x) - (rq.y - rq.x);
+      }
+      if (a.alpha != 1.f) delta += rb.z - a.alpha * rb.x;
+      sm.bonus[tid] = __float_as_int(rb.w);
+      lwf = lw0 + delta;
     }
-    const float4 rb = __ldcg(reinterpret_cast<const float4 *>(r + K));
-    if (a.alpha != 1.f) delta += static_cast<double>(rb.z) - static_cast<double>(a.alpha) * rb.x;
-    sm.bonus[tid] = __float_as_int(rb.w);
-    lwf = static_cast<float>(static_cast<double>(a.out.log_weights[part]) + delta);
+    const ResampleResult rr =
+        small ? normalise_resample_warp(b, N, lwf, valid, a.ess_frac, a.seed, a.step, a.ws.status,
+                                        sm.anc, sm.c)
+              : normalise_resample(b, N, lwf, valid, a.ess_frac, a.seed, a.step, a.ws.status,
+                                   sm.anc, sm.c, sm.red);
+    if (valid) {
+      const int part = b * N + tid;
+      const int anc = sm.anc[tid];
+      a.out.log_weights[part] = rr.resampled ? 0.f : lwf;
+      a.out.ancestors[part] = anc;
+      int32_t *dst = a.out.tokens_out + static_cast<size_t>(part) * (K + 1);
+      const int32_t *srcp = a.tokens + static_cast<size_t>(b * N + anc) * K;
+#pragma unroll 4
+      for (int k = 0; k < K; ++k) dst[k] = srcp[k];
+      dst[K] = sm.bonus[anc];
+    }
+    if (tid == 0) {
+      a.out.ess[b] = rr.ess;
+      a.out.resampled[b] = rr.resampled ? 1 : 0;
+      s_res = rr.resampled ? 1 : 0;
+    }
   }
-  const ResampleResult rr = normalise_resample(b, N, lwf, valid, a.ess_frac, a.seed, a.step,
-                                               a.ws.status, sm.anc, sm.c, sm.dred);
-  if (valid) {
-    const int part = b * N + tid;
-    const int anc = sm.anc[tid];
-    a.out.log_weights[part] = rr.resampled ? 0.f : lwf;
-    a.out.ancestors[part] = anc;
-    int32_t *dst = a.out.tokens_out + static_cast<size_t>(part) * (K + 1);
-    const int32_t *src = a.tokens + static_cast<size_t>(b * N + anc) * K;
-    for (int k = 0; k < K; ++k) dst[k] = src[k];
-    dst[K] = sm.bonus[anc];
-  }
-  if (tid == 0) {
-    a.out.ess[b] = static_cast<float>(rr.ess);
-    a.out.resampled[b] = rr.resampled ? 1 : 0;
-  }
+  __syncthreads();
   if (a.use_kv) {
-    kv_remap_append_block(a.kv, b, N, sm.anc, rr.resampled, K + 1, a.ws, sm.ired, sm.tail);
+    kv_remap_append(a.kv, b, N, sm.anc, s_res != 0, K + 1, a.ws, sm.ired, sm.tail, sm.nb, sc,
+                    small);
   }
 }
 
@@ -330,8 +446,8 @@ __device__ void sps_tail(const StepArgs &a, int b, TailSmem &sm) {
   if (tid < K) {
     const float4 rp = __ldcg(reinterpret_cast<const float4 *>(r + tid));
     const float4 rq = __ldcg(reinterpret_cast<const float4 *>(r + K + 1 + tid));
-    const double ratio = exp((static_cast<double>(rp.y) - rp.x) - (static_cast<double>(rq.y) - rq.x));
-    const double u = philox_uniform(a.seed, a.step, b, tid, SMC_PURPOSE_ACCEPT);
+    const float ratio = expf((rp.y - rp.x) - (rq.y - rq.x));
+    const float u = philox_uniform(a.seed, a.step, b, tid, SMC_PURPOSE_ACCEPT);
     if (!(u < ratio)) cand = tid;
   }
   int j = block_min_i(cand, sm.ired);
@@ -532,28 +648,529 @@ __global__ void __launch_bounds__(kThreads, 4) step_rows_kernel(const StepArgs a
     }
     if (tid == 0) a.ws.results[row].tok = tok;
   }
+}
 
-  // ---- last row of the prompt: the prompt's tail ---------------------------
-  __syncthreads();
-  const int b = part / a.N;
-  if (tid == 0) {
-    __threadfence();
-    const unsigned t = atomicAdd(&a.ws.prompt_ticket[b], 1u);
-    s_last = t == static_cast<unsigned>(a.N * rpp - 1);
+// ---------------------------------------------------------------------------
+// Streaming row kernel (shapes whose rows are 16-byte aligned).
+//
+// Each CTA has 8 consumer warps and 1 producer warp.  The producer claims
+// work items (G consecutive 16 KB chunks of one row) from an atomic counter,
+// in row order, and streams their chunks through a ring of kStages shared-
+// memory slots with bulk copies (cp.async.bulk; completion counted as tx
+// bytes on a per-slot mbarrier), as far ahead as the ring allows.  Consumer
+// warp w owns the contiguous eighth w of every chunk.  A lane folds its
+// logits into a running (max, sum of exp) pair over the item; at the item's
+// end the warp reduces it and writes one partial per (item, warp).  For the
+// bonus row each warp also writes, per chunk, the float-float sum of its
+// sampling weights relative to its own max there.  Every partial is
+// followed by an arrival on the row's ticket; the warp that arrives last
+// combines the row alone: log-sum-exp and gather, or for the bonus row the
+// inverse-CDF draw (which (chunk, warp) range, then which element, rescanned
+// by that warp).  There is no CTA-wide barrier after set-up.  The per-prompt
+// tail runs in tail_kernel, launched after this kernel.
+// ---------------------------------------------------------------------------
+constexpr int kStages = 4;
+constexpr int kChunkBytes = 16384;      // ChunkGeom<T>::kCH * kESZ for both dtypes
+constexpr int kConsumerWarps = 8;
+constexpr int kStreamThreads = (kConsumerWarps + 1) * 32;
+constexpr uint32_t kWaitLimit = 1u << 18;  // polls; each may suspend up to 20 us
+
+enum : int { kSlotFirst = 1, kSlotLast = 2, kSlotEnd = 4 };
+
+struct SlotMeta { int row, chunk, n, flags; };
+
+struct StreamArgs {
+  StepArgs a;
+  int G;              // chunks per work item of a non-bonus row
+  int ipr;            // work items per non-bonus row
+  int n_fast_items;   // non-bonus rows * ipr
+  int n_bonus_items;  // bonus rows * nch (one chunk per item)
+};
+
+constexpr size_t stream_dyn_smem() {
+  return static_cast<size_t>(kStages) * kChunkBytes + 2 * kStages * sizeof(uint64_t) +
+         kStages * sizeof(SlotMeta);
+}
+
+template <typename T>
+__device__ __forceinline__ const char *row_base(const StepArgs &a, int row) {
+  const int rpp = 2 * a.K + 1;
+  const int part = row / rpp, j = row - part * rpp;
+  constexpr int ESZ = ChunkGeom<T>::kESZ;
+  return j <= a.K
+      ? a.target + (static_cast<size_t>(part) * (a.K + 1) + j) * static_cast<size_t>(a.V) * ESZ
+      : a.draft + (static_cast<size_t>(part) * a.K + (j - a.K - 1)) * static_cast<size_t>(a.V) * ESZ;
+}
+
+// Warp-level inverse-CDF selection inside the range [r0, r0 + len) of a row
+// (r0 and len multiples of the 16-byte vector width, len <= 32 * SEG), in
+// exact fixed-point arithmetic: the first element with a positive weight
+// weight_fixed(l, ref) whose inclusive prefix exceeds `target`; if none does
+// (the target at or past the range's total), the last positive element; -1
+// with no mass.  Lane l holds the contiguous segment [l*SEG, (l+1)*SEG),
+// loaded with 16-byte loads (one round trip).
+template <typename T, int SEG>
+__device__ int warp_select_fixed(const char *rowp, int64_t r0, int len, long long target,
+                                 float ref, float alpha, const float2 *tab) {
+  using Tr = LogitTraits<T>;
+  constexpr int EPV = Tr::kPerVec;
+  constexpr int NV = SEG / EPV;
+  constexpr bool kExactDiff = sizeof(T) != 4;
+  const int lane = threadIdx.x & 31;
+  const int beg = lane * SEG;
+  const uint4 *src = reinterpret_cast<const uint4 *>(rowp + (r0 + beg) * ChunkGeom<T>::kESZ);
+  uint4 q[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    q[v] = beg + v * EPV < len ? src[v] : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u,
+                                                     0xff80ff80u);
   }
+  if (sizeof(T) == 4) {
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      if (!(beg + v * EPV < len)) q[v] = make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+    }
+  }
+  long long part = 0;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) part += weight_fixed<kExactDiff>(Tr::at(q[v], e), ref, alpha, tab);
+  }
+  const long long incl = warp_incl_scan_ll(part);
+  int cand = 0x7fffffff, last_pos = -1;
+  if (part > 0) {
+    // lanes holding mass walk their segment again, one vector at a time
+    // (reloaded from L2), recomputing the weights identically
+    long long run = incl - part;
+#pragma unroll 1
+    for (int v = 0; v < NV; ++v) {
+      if (!(beg + v * EPV < len)) break;
+      const uint4 qv = src[v];
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const long long wv = weight_fixed<kExactDiff>(Tr::at(qv, e), ref, alpha, tab);
+        run += wv;
+        if (wv > 0) {
+          last_pos = beg + v * EPV + e;
+          if (cand == 0x7fffffff && run > target) cand = beg + v * EPV + e;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
+  if (cand == 0x7fffffff) {
+    cand = last_pos;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cand = max(cand, __shfl_xor_sync(0xffffffffu, cand, o));
+  }
+  return cand < 0 ? -1 : static_cast<int>(r0 + cand);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kStreamThreads, 3) row_stream_kernel(const StreamArgs sa) {
+  using Tr = LogitTraits<T>;
+  using Gm = ChunkGeom<T>;
+  constexpr int EPV = Gm::kEPV;                       // logits per 16-byte vector
+  constexpr int CH = Gm::kCH;                         // logits per chunk
+  constexpr int ESZ = Gm::kESZ;
+  constexpr int WCH = CH / kConsumerWarps;            // logits per warp range
+  constexpr int VPL = WCH / EPV / 32;                 // vectors per lane per chunk
+  constexpr bool kExactDiff = sizeof(T) != 4;
+  constexpr float kInf = -kNegInf;
+  const StepArgs &a = sa.a;
+
+  extern __shared__ __align__(128) unsigned char dyn_smem[];
+  uint4 *bufs = reinterpret_cast<uint4 *>(dyn_smem);
+  uint64_t *full = reinterpret_cast<uint64_t *>(dyn_smem + kStages * kChunkBytes);
+  uint64_t *empty = full + kStages;
+  SlotMeta *meta = reinterpret_cast<SlotMeta *>(empty + kStages);
+  __shared__ float2 s_tab[64];
+  __shared__ int s_exited;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rpp = 2 * a.K + 1;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    mbar_init_fence();
+    s_exited = 0;
+  }
+  stage_exp2_table(s_tab);
+  __syncthreads();  // the only CTA-wide barrier
+
+  // ---- producer warp -----------------------------------------------------------
+  // Work comes from two queues: items of G chunks of the non-bonus rows, and
+  // single chunks of the bonus rows (whose weights cost far more to compute).
+  // The producer alternates between them so that every CTA, all through the
+  // kernel, mixes streaming-bound and arithmetic-bound chunks.
+  if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      const int rest = rpp - 1;  // non-bonus rows per particle
+      int row = 0, first = 0, chunk = 0, end = 0;
+      int n_fast = 0, n_bonus = 0;
+      bool have = false, fast_done = sa.n_fast_items == 0, bonus_done = sa.n_bonus_items == 0;
+      for (int i = 0;; ++i) {
+        const int slot = i % kStages;
+        if (i >= kStages &&
+            !mbar_wait(&empty[slot], static_cast<uint32_t>(i / kStages - 1) & 1u, kWaitLimit)) {
+          raise_status(a.ws.status, SMC_DEV_TIMEOUT);
+          meta[slot].flags = kSlotEnd;  // consumers time out on this slot too
+          break;
+        }
+        while (!have || chunk >= end) {
+          have = false;
+          if (fast_done && bonus_done) break;
+          const bool take_bonus = !bonus_done && (fast_done || n_bonus < n_fast);
+          if (take_bonus) {
+            const unsigned id = atomicAdd(&a.ws.work_counter[1], 1u);
+            if (id >= static_cast<unsigned>(sa.n_bonus_items)) { bonus_done = true; continue; }
+            ++n_bonus;
+            const int part = static_cast<int>(id) / a.nch;
+            row = part * rpp + a.K;
+            first = static_cast<int>(id) - part * a.nch;
+            end = first + 1;
+          } else {
+            const unsigned id = atomicAdd(&a.ws.work_counter[0], 1u);
+            if (id >= static_cast<unsigned>(sa.n_fast_items)) { fast_done = true; continue; }
+            ++n_fast;
+            const int rf = static_cast<int>(id) / sa.ipr;
+            const int g = static_cast<int>(id) - rf * sa.ipr;
+            const int part = rf / rest, jj = rf - (rf / rest) * rest;
+            row = part * rpp + (jj < a.K ? jj : jj + 1);
+            first = g * sa.G;
+            end = min(first + sa.G, a.nch);
+          }
+          chunk = first;
+          have = true;
+        }
+        if (!have) {
+          SlotMeta &mt = meta[slot];
+          mt.row = -1; mt.chunk = 0; mt.n = 0; mt.flags = kSlotEnd;
+          mbar_arrive(&full[slot]);
+          break;
+        }
+        const int64_t c0 = static_cast<int64_t>(chunk) * CH;
+        const int n = static_cast<int>(min(static_cast<int64_t>(CH), a.V - c0));
+        SlotMeta &mt = meta[slot];
+        mt.row = row;
+        mt.chunk = chunk;
+        mt.n = n;
+        mt.flags = (chunk == first ? kSlotFirst : 0) | (chunk + 1 == end ? kSlotLast : 0);
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(n * ESZ));
+        bulk_copy_g2s(bufs + static_cast<size_t>(slot) * (kChunkBytes / 16),
+                      row_base<T>(a, row) + c0 * ESZ, static_cast<uint32_t>(n * ESZ), &full[slot]);
+        ++chunk;
+      }
+    }
+    return;
+  }
+
+  // ---- consumer warps --------------------------------------------------------
+  float m_t = kNegInf, s_t = 0.f;  // this lane's running (max, sum exp) over the item
+  for (int i = 0;; ++i) {
+    const int slot = i % kStages;
+    const uint32_t par = static_cast<uint32_t>(i / kStages) & 1u;
+    if (!mbar_wait(&full[slot], par, kWaitLimit)) {
+      raise_status(a.ws.status, SMC_DEV_TIMEOUT);
+      break;
+    }
+    const SlotMeta mt = meta[slot];
+    if (mt.flags & kSlotEnd) break;
+    const int row = mt.row;
+    const int part = row / rpp;
+    const int j = row - part * rpp;
+    const bool is_bonus = j == a.K;
+    const bool fast = !is_bonus || a.alpha != 1.f;
+    if (mt.flags & kSlotFirst) { m_t = kNegInf; s_t = 0.f; }
+
+    // this warp's range of the chunk: logits [warp*WCH, (warp+1)*WCH).  A
+    // vector past the chunk's valid logits reads as -inf.
+    constexpr uint32_t kNegInfBits = sizeof(T) == 4 ? 0xff800000u : 0xff80ff80u;
+    uint4 q[VPL];
+    const uint4 *buf = bufs + static_cast<size_t>(slot) * (kChunkBytes / 16) + warp * (WCH / EPV);
+    const int wbase = warp * WCH;
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+      const bool ok = wbase + (v * 32 + lane) * EPV < mt.n;
+      q[v] = ok ? buf[v * 32 + lane] : make_uint4(kNegInfBits, kNegInfBits, kNegInfBits, kNegInfBits);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);  // this warp is done reading the slot
+
+    // the words of my vectors: 2 bf16 or 1 fp32 logit each
+    const uint32_t *wd = reinterpret_cast<const uint32_t *>(q);
+    constexpr int NW = VPL * 4;
+    float cm;
+    if (sizeof(T) == 4) {
+      cm = __uint_as_float(wd[0]);
+#pragma unroll
+      for (int k = 1; k < NW; ++k) cm = fmaxf(cm, __uint_as_float(wd[k]));
+    } else {
+      uint32_t mw = wd[0];
+#pragma unroll
+      for (int k = 1; k < NW; ++k) mw = bmax2(mw, wd[k]);
+      cm = fmaxf(bf16_lo(mw), bf16_hi(mw));
+    }
+    if (fast) {
+      if (cm > m_t) {
+        if (m_t > kNegInf) s_t *= fast_exp2((m_t - cm) * kLog2e);
+        m_t = cm;
+      }
+      if (m_t > kNegInf && m_t < kInf) {
+        const float mb = m_t * kLog2e;
+        const unsigned long long l2 = f2pack(kLog2e, kLog2e), nmb = f2pack(-mb, -mb);
+        unsigned long long acc = 0ull;
+        if (sizeof(T) == 4) {
+#pragma unroll
+          for (int k = 0; k < NW; k += 2) {
+            float y0, y1;
+            f2unpack(fma2(f2pack(__uint_as_float(wd[k]), __uint_as_float(wd[k + 1])), l2, nmb), y0, y1);
+            acc = add2(acc, f2pack(fast_exp2(y0), fast_exp2(y1)));
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < NW; ++k) {
+            float y0, y1;
+            f2unpack(fma2(f2pack(bf16_lo(wd[k]), bf16_hi(wd[k])), l2, nmb), y0, y1);
+            acc = add2(acc, f2pack(fast_exp2(y0), fast_exp2(y1)));
+          }
+        }
+        float a0, a1;
+        f2unpack(acc, a0, a1);
+        s_t += a0 + a1;  // NaN logits propagate and are reported at the row combine
+      } else if (m_t == kInf) {
+        s_t = __int_as_float(0x7fc00000);
+      }
+    }
+    if (is_bonus) {
+      // NaN or +inf anywhere in the row is an error: a NaN-propagating max
+      float cmn;
+      if (sizeof(T) == 4) {
+        cmn = __uint_as_float(wd[0]);
+#pragma unroll
+        for (int k = 1; k < NW; ++k) cmn = fmax_nan(cmn, __uint_as_float(wd[k]));
+      } else {
+        uint32_t mw = wd[0];
+#pragma unroll
+        for (int k = 1; k < NW; ++k) mw = bmax2_nan(mw, wd[k]);
+        cmn = fmax_nan(bf16_lo(mw), bf16_hi(mw));
+      }
+      if (!(cmn < kInf)) raise_status(a.ws.status, SMC_DEV_NONFINITE);
+      const float ref = warp_max(cm);  // this unit's reference: its max logit
+      long long acc = 0;
+      if (ref > kNegInf && ref < kInf) {
+#pragma unroll
+        for (int k = 0; k < NW; ++k) {
+          if (sizeof(T) == 4) {
+            acc += weight_fixed<kExactDiff>(__uint_as_float(wd[k]), ref, a.alpha, s_tab);
+          } else {
+            acc += weight_fixed<kExactDiff>(bf16_lo(wd[k]), ref, a.alpha, s_tab);
+            acc += weight_fixed<kExactDiff>(bf16_hi(wd[k]), ref, a.alpha, s_tab);
+          }
+        }
+      }
+      acc = warp_sum_ll(acc);
+      if (lane == 0) {
+        a.ws.bonus_part[(static_cast<size_t>(part) * a.nch + mt.chunk) * kConsumerWarps + warp] =
+            make_int4(__float_as_int(ref), static_cast<int>(acc & 0xffffffffll),
+                      static_cast<int>(acc >> 32), 0);
+      }
+    }
+
+    if (!(mt.flags & kSlotLast)) continue;
+
+    // ---- end of this warp's share of a work item: its partial -----------------
+    if (fast) {
+      const float M = warp_max(m_t);
+      float contrib = 0.f;
+      if (m_t > kNegInf && M < kInf) contrib = s_t * fast_exp2((m_t - M) * kLog2e);
+      else if (s_t != 0.f) contrib = s_t;  // NaN marker
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) contrib += __shfl_xor_sync(0xffffffffu, contrib, o);
+      if (lane == 0) {
+        const int g = is_bonus ? mt.chunk : mt.chunk / sa.G;
+        a.ws.item_part[(static_cast<size_t>(row) * a.nch + g) * kConsumerWarps + warp] =
+            make_float2(M, contrib);
+      }
+    }
+  }
+
+  // ---- consumer exit: let the finish kernel launch; reset the work counters ---
+  if (lane == 0) {
+    if (atomicAdd(&s_exited, 1) == kConsumerWarps - 1) {
+      asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+      __threadfence();
+      if (atomicAdd(a.ws.exit_counter, 1u) == gridDim.x - 1) {
+        a.ws.work_counter[0] = 0u;
+        a.ws.work_counter[1] = 0u;
+        *a.ws.exit_counter = 0u;
+      }
+    }
+  }
+}
+
+
+// ---------------------------------------------------------------------------
+// Row combine, one warp per row, after the streaming kernel: the row's
+// log-sum-exp from its (item, warp) partials and the drafted token's logit;
+// for the bonus row, the inverse-CDF draw in vocabulary order: which (chunk,
+// warp) unit, from the units' exact fixed-point sums, then which element,
+// rescanning that unit exactly.  Launched with programmatic dependent launch;
+// waits for the streaming kernel before reading its partials.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa) {
+  using Tr = LogitTraits<T>;
+  using Gm = ChunkGeom<T>;
+  constexpr int CH = Gm::kCH;
+  constexpr int WCH = CH / kConsumerWarps;
+  constexpr float kInf = -kNegInf;
+  const StepArgs &a = sa.a;
+  __shared__ float2 s_tab[64];
+  stage_exp2_table(s_tab);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (tid == 0) a.ws.prompt_ticket[b] = 0u;
-  __shared__ TailSmem tail_sm;
-  if (a.mode == 0) smc_tail(a, b, tail_sm);
-  else sps_tail(a, b, tail_sm);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int rpp = 2 * a.K + 1;
+  const long long rows = static_cast<long long>(a.B) * a.N * rpp;
+  const long long row_ll = static_cast<long long>(blockIdx.x) * kWarps + warp;
+  if (row_ll >= rows) return;
+  const int row = static_cast<int>(row_ll);
+  const int part = row / rpp, j = row - part * rpp;
+  const bool is_bonus = j == a.K;
+  const bool fast = !is_bonus || a.alpha != 1.f;
+  const char *rowp = row_base<T>(a, row);
+  const int gtok = is_bonus ? 0 : a.tokens[static_cast<size_t>(part) * a.K + (j < a.K ? j : j - a.K - 1)];
+  const float2 *ip = a.ws.item_part + static_cast<size_t>(row) * a.nch * kConsumerWarps;
+  const int n_ip = (is_bonus ? a.nch : sa.ipr) * kConsumerWarps;
+  float fM = kNegInf, fS = 0.f;  // fast log-sum-exp pieces of the row
+  if (fast) {
+    float lm = kNegInf, ls = 0.f;
+#pragma unroll 4
+    for (int c = lane; c < n_ip; c += 32) {
+      const float2 pv = ip[c];
+      if (pv.x > lm) {
+        if (lm > kNegInf && pv.x < kInf) ls *= expf(lm - pv.x);
+        else if (pv.x == kInf) ls = 0.f;
+        lm = pv.x;
+      }
+      if (pv.x > kNegInf && lm < kInf) ls += pv.y * expf(pv.x - lm);
+      else if (pv.y != 0.f) ls += pv.y;  // NaN marker
+    }
+    fM = warp_max(lm);
+    fS = (lm > kNegInf && fM < kInf) ? ls * expf(lm - fM) : ls;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) fS += __shfl_xor_sync(0xffffffffu, fS, o);
+  }
+  if (!is_bonus) {
+    if (lane == 0) {
+      unsigned bits = 0;
+      if (fM == kNegInf) bits |= SMC_DEV_EMPTY_ROW;
+      else if (!(fS < kInf) || fM == kInf) bits |= SMC_DEV_NONFINITE;
+      const float lse = fM + logf(fS);
+      if (gtok < 0 || gtok >= a.V) bits |= SMC_DEV_BAD_TOKEN;
+      const float gv =
+          (gtok < 0 || gtok >= a.V) ? __int_as_float(0x7fc00000) : Tr::scalar(rowp, gtok);
+      if (bits) raise_status(a.ws.status, bits);
+      a.ws.results[row] = RowResult{lse, gv, 0.f, -1};
+    }
+    return;
+  }
+  // bonus row: units are (chunk, warp) ranges of WCH logits in vocabulary
+  // order, each with its max as reference and an exact fixed-point sum
+  const float alpha = a.alpha;
+  const int4 *bp = a.ws.bonus_part + static_cast<size_t>(part) * a.nch * kConsumerWarps;
+  const int n_units = a.nch * kConsumerWarps;
+  // the first kPre units of each lane stay in registers; longer rows reload
+  constexpr int kPre = 4;
+  int4 pre[kPre];
+#pragma unroll
+  for (int r = 0; r < kPre; ++r) {
+    const int q = r * 32 + lane;
+    pre[r] = q < n_units ? bp[q] : make_int4(__float_as_int(kNegInf), 0, 0, 0);
+  }
+  float M = kNegInf;
+#pragma unroll
+  for (int r = 0; r < kPre; ++r) M = fmaxf(M, __int_as_float(pre[r].x));
+  for (int q = kPre * 32 + lane; q < n_units; q += 32) M = fmaxf(M, __int_as_float(bp[q].x));
+  M = warp_max(M);
+  const bool ok = M > kNegInf && M < kInf;
+  auto unit_of = [&](int q) -> int4 {
+    const int r = (q - lane) >> 5;
+    if (q < kPre * 32) {
+      int4 v = pre[0];
+#pragma unroll
+      for (int k = 1; k < kPre; ++k) v = r == k ? pre[k] : v;
+      return v;
+    }
+    return bp[q];
+  };
+  auto unit_mass = [&](int q, ff *val, ff *f) {
+    const int4 pv = unit_of(q);
+    const float ref = __int_as_float(pv.x);
+    if (ok && ref > kNegInf) {
+      const long long sq = (static_cast<long long>(pv.z) << 32) |
+                           static_cast<long long>(static_cast<unsigned>(pv.y));
+      *f = ff_norm(weight_term<false>(ref, M, alpha, s_tab));  // exp(alpha (ref - M))
+      *val = ff_mul(fixed_to_ff(sq), *f);
+    }
+  };
+  ff total{0.f, 0.f};
+  for (int q0 = 0; q0 < n_units; q0 += 32) {
+    ff val{0.f, 0.f}, f{1.f, 0.f};
+    if (q0 + lane < n_units) unit_mass(q0 + lane, &val, &f);
+    total = ff_add(total, warp_ff_sum(val));
+  }
+  const float u = philox_uniform(a.seed, a.step, part, a.K, SMC_PURPOSE_BONUS);
+  ff rem{0.f, 0.f};
+  const int sel = ok ? warp_find_chunk(n_units, ff_mul_f(total, u), unit_mass, &rem) : -1;
+  int tok = -1;
+  if (sel >= 0) {
+    const float ref = __int_as_float(bp[sel].x);
+    const int c = sel / kConsumerWarps, w = sel - c * kConsumerWarps;
+    const int64_t r0 = static_cast<int64_t>(c) * CH + static_cast<int64_t>(w) * WCH;
+    const int len = static_cast<int>(max(static_cast<int64_t>(0),
+                                         min(static_cast<int64_t>(WCH), a.V - r0)));
+    tok = warp_select_fixed<T, WCH / 32>(rowp, r0, len, ff_to_fixed(rem), ref, alpha, s_tab);
+  }
+  if (lane == 0) {
+    float lse, lse_alpha;
+    if (ok) {
+      lse_alpha = alpha * M + (logf(total.hi) + total.lo / total.hi);
+      lse = alpha != 1.f ? fM + logf(fS) : lse_alpha;
+    } else {
+      lse = lse_alpha = M == kNegInf ? kNegInf : __int_as_float(0x7fc00000);
+      raise_status(a.ws.status, M == kNegInf ? SMC_DEV_EMPTY_ROW : SMC_DEV_NONFINITE);
+    }
+    a.ws.results[row] = RowResult{lse, 0.f, lse_alpha, tok};
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Per-prompt tail, one CTA per prompt: weights, ESS, resampling, emission and
+// KV remap (SMC mode), or the acceptance scan (SpS mode).  Launched after a
+// row kernel; with programmatic dependent launch it may start early and
+// waits here until the row kernel has finished and its results are visible.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1) tail_kernel(const StepArgs a, int kv_staged) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ TailSmem sm;
+  extern __shared__ int dyn_i[];
+  if (a.mode == 0) smc_tail(a, blockIdx.x, sm, dyn_i, kv_staged != 0);
+  else sps_tail(a, blockIdx.x, sm);
 }
 
 // ---------------------------------------------------------------------------
 // Standalone resampling and remap kernels: one CTA per prompt.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)
 resample_kernel(int N, float ess_frac, uint64_t seed, uint32_t step, float *log_weights,
                 int32_t *ancestors, float *ess, int32_t *resampled, unsigned *status) {
   __shared__ TailSmem sm;
@@ -562,21 +1179,22 @@ resample_kernel(int N, float ess_frac, uint64_t seed, uint32_t step, float *log_
   const bool valid = tid < N;
   const float lwf = valid ? log_weights[static_cast<size_t>(b) * N + tid] : 0.f;
   const ResampleResult rr = normalise_resample(b, N, lwf, valid, ess_frac, seed, step, status,
-                                               sm.anc, sm.c, sm.dred);
+                                               sm.anc, sm.c, sm.red);
   if (valid) {
     log_weights[static_cast<size_t>(b) * N + tid] = rr.resampled ? 0.f : lwf;
     ancestors[static_cast<size_t>(b) * N + tid] = sm.anc[tid];
   }
   if (tid == 0) {
-    ess[b] = static_cast<float>(rr.ess);
+    ess[b] = rr.ess;
     resampled[b] = rr.resampled ? 1 : 0;
   }
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)
 kv_remap_kernel(int N, KvArgs kv, const int32_t *ancestors, const int32_t *resampled,
-                int n_append, Workspace ws) {
+                int n_append, Workspace ws, int kv_staged) {
   __shared__ TailSmem sm;
+  extern __shared__ int dyn_i[];
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const bool res = resampled[b] != 0;
@@ -589,13 +1207,109 @@ kv_remap_kernel(int N, KvArgs kv, const int32_t *ancestors, const int32_t *resam
     sm.anc[tid] = a;
   }
   __syncthreads();
-  kv_remap_append_block(kv, b, N, sm.anc, res, n_append, ws, sm.ired, sm.tail);
+  kv_remap_append(kv, b, N, sm.anc, res, n_append, ws, sm.ired, sm.tail, sm.nb,
+                  kv_scratch(kv, b, N, ws, dyn_i, kv_staged != 0), false);
 }
 
 // ---------------------------------------------------------------------------
 // Launchers.
 // ---------------------------------------------------------------------------
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Resident CTAs of the streaming kernel per SM and the SM count of the
+// current device (queried once per device).
+template <typename T>
+static cudaError_t stream_geometry(int *sms, int *per_sm) {
+  constexpr int kMaxDev = 64;
+  static int cache_sms[kMaxDev], cache_bps[kMaxDev];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int slot = dev < kMaxDev ? dev : kMaxDev - 1;
+  if (dev >= kMaxDev || cache_sms[slot] == 0) {
+    e = cudaFuncSetAttribute(row_stream_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(stream_dyn_smem()));
+    if (e != cudaSuccess) return e;
+    int n = 0, b = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, row_stream_kernel<T>, kStreamThreads,
+                                                      stream_dyn_smem());
+    if (e != cudaSuccess) return e;
+    cache_sms[slot] = n;
+    cache_bps[slot] = b > 0 ? b : 1;
+  }
+  *sms = cache_sms[slot];
+  *per_sm = cache_bps[slot];
+  return cudaSuccess;
+}
+
+template <typename T>
+static cudaError_t launch_stream(const StepArgs &a, long long rows, cudaStream_t stream) {
+  int sms = 0, per_sm = 0;
+  cudaError_t e = stream_geometry<T>(&sms, &per_sm);
+  if (e != cudaSuccess) return e;
+  const long long grid_max = static_cast<long long>(sms) * per_sm;
+  const long long total_chunks = rows * a.nch;
+  // about six work items per resident CTA, each 1..8 chunks
+  const long long g = total_chunks / (grid_max * 6);
+  StreamArgs sa{};
+  sa.a = a;
+  sa.G = static_cast<int>(g < 1 ? 1 : (g > 8 ? 8 : g));
+  sa.ipr = (a.nch + sa.G - 1) / sa.G;
+  const long long parts = rows / (2 * a.K + 1);
+  sa.n_fast_items = static_cast<int>(parts * 2 * a.K * sa.ipr);
+  sa.n_bonus_items = static_cast<int>(parts * a.nch);
+  const long long n_items = static_cast<long long>(sa.n_fast_items) + sa.n_bonus_items;
+  const long long grid = grid_max < n_items ? grid_max : n_items;
+  row_stream_kernel<T><<<static_cast<unsigned>(grid), kStreamThreads, stream_dyn_smem(), stream>>>(sa);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + kWarps - 1) / kWarps));
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, finish_kernel<T>, sa);
+}
+
+// The per-prompt tail, launched with programmatic dependent launch so that it
+// can be scheduled while the row kernel drains.
+// Dynamic shared memory for a staged KV remap, or 0 when it does not fit.
+static size_t kv_stage_bytes(int N, const KvArgs *kv) {
+  if (!kv) return 0;
+  const size_t bytes = kv_stage_words(N, kv->T, kv->P) * sizeof(int);
+  return bytes <= kKvStageMaxBytes ? bytes : 0;
+}
+
+template <typename K>
+static cudaError_t allow_dyn_smem(K kernel, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(bytes));
+}
+
+static cudaError_t launch_tail(const StepArgs &a, cudaStream_t stream) {
+  const size_t dyn = a.use_kv ? kv_stage_bytes(a.N, &a.kv) : 0;
+  cudaError_t e = allow_dyn_smem(tail_kernel, dyn);
+  if (e != cudaSuccess) return e;
+  const int staged = dyn > 0 ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = dyn;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tail_kernel, a, staged);
+}
 
 cudaError_t launch_step_rows(const Shape &s, int mode, const void *target, const void *draft,
                              const int32_t *tokens, const StepOutputs &out, const KvArgs *kv,
@@ -613,18 +1327,24 @@ cudaError_t launch_step_rows(const Shape &s, int mode, const void *target, const
   a.use_kv = kv != nullptr;
   if (kv) a.kv = *kv;
   const long long rows = static_cast<long long>(s.B) * s.N * (2 * s.K + 1);
-  const long long grid = rows * a.nch;
   const int esz = s.dtype == SMC_BF16 ? 2 : 4;
+  // bulk copies need 16-byte aligned rows and chunk sizes: aligned bases and V*esz % 16 == 0
   const bool vec = aligned16(target) && aligned16(draft) &&
                    (static_cast<long long>(s.V) * esz) % 16 == 0;
-  dim3 g(static_cast<unsigned>(grid)), blk(kThreads);
-  if (s.dtype == SMC_BF16) {
-    if (vec) step_rows_kernel<bf16_tag, true><<<g, blk, 0, stream>>>(a);
-    else step_rows_kernel<bf16_tag, false><<<g, blk, 0, stream>>>(a);
+  cudaError_t e;
+  if (vec) {
+    e = s.dtype == SMC_BF16 ? launch_stream<bf16_tag>(a, rows, stream)
+                            : launch_stream<float>(a, rows, stream);
   } else {
-    if (vec) step_rows_kernel<float, true><<<g, blk, 0, stream>>>(a);
+    const long long grid = rows * a.nch;
+    dim3 g(static_cast<unsigned>(grid)), blk(kThreads);
+    if (s.dtype == SMC_BF16) step_rows_kernel<bf16_tag, false><<<g, blk, 0, stream>>>(a);
     else step_rows_kernel<float, false><<<g, blk, 0, stream>>>(a);
+    e = cudaGetLastError();
   }
+  if (e != cudaSuccess) return e;
+  e = launch_tail(a, stream);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -638,7 +1358,11 @@ cudaError_t launch_resample(const Shape &s, float *log_weights, int32_t *ancesto
 cudaError_t launch_kv_remap(const Shape &s, const KvArgs &kv, const int32_t *ancestors,
                             const int32_t *resampled, int n_append, const Workspace &ws,
                             cudaStream_t stream) {
-  kv_remap_kernel<<<s.B, kThreads, 0, stream>>>(s.N, kv, ancestors, resampled, n_append, ws);
+  const size_t dyn = kv_stage_bytes(s.N, &kv);
+  cudaError_t e = allow_dyn_smem(kv_remap_kernel, dyn);
+  if (e != cudaSuccess) return e;
+  kv_remap_kernel<<<s.B, kThreads, dyn, stream>>>(s.N, kv, ancestors, resampled, n_append, ws,
+                                                   dyn > 0 ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -198,10 +198,11 @@ def test_smc_resample_bit_exact_on_identical_weights(N):
     g_lw = d_lw.cpu().numpy().reshape(B, N)
     for b in range(B):
         r = osmc.resample_prompt(lw[b].astype(np.float64), 0.7, 123, 9, b)
-        assert abs(ess[b].item() - r["ess"]) <= 1e-6 * r["ess"]
-        assert bool(res[b].item()) == r["resampled"] or r["ess_margin"] < 1e-9
+        # the GPU normalises in fp32: decisions agree except within fp32 rounding
+        assert abs(ess[b].item() - r["ess"]) <= 1e-5 * r["ess"]
+        assert bool(res[b].item()) == r["resampled"] or r["ess_margin"] < 1e-5
         if r["resampled"]:
-            ok = (g_anc[b] == r["ancestors"]) | (r["margins"] < 1e-12)
+            ok = (g_anc[b] == r["ancestors"]) | (r["margins"] < 1e-6)
             assert ok.all()
             assert (g_lw[b] == 0).all()
         else:
@@ -209,10 +210,13 @@ def test_smc_resample_bit_exact_on_identical_weights(N):
             assert np.array_equal(g_lw[b], lw[b])
 
 
-@pytest.mark.parametrize("prefix,bs", [(10, 4), (32, 16), (0, 8)])
-def test_kv_blocktable_remap_bit_exact(prefix, bs):
-    B, N, steps, n_app = 3, 12, 8, 5
-    T = (prefix + steps * n_app + bs - 1) // bs + 1
+@pytest.mark.parametrize("prefix,bs,N,T_min", [(10, 4, 12, 0), (32, 16, 12, 0), (0, 8, 12, 0),
+                                               (40, 4, 256, 120)])
+def test_kv_blocktable_remap_bit_exact(prefix, bs, N, T_min):
+    """Small tables take the shared-memory staged path; N*T = 30720 entries
+    (last case) exceeds the staging budget and takes the global-scratch path."""
+    B, steps, n_app = 3 if N < 100 else 2, 8, 5
+    T = max(T_min, (prefix + steps * n_app + bs - 1) // bs + 1)
     P = N * T
     params = smcsd.make_params(B, N, 4, 8, "f32")
     kv = make_kv_state(B, N, prefix, bs, T, P, device="cuda")
