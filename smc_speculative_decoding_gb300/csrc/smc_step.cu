@@ -677,7 +677,7 @@ constexpr uint32_t kWaitLimit = 1u << 18;  // polls; each may suspend up to 20 u
 
 enum : int { kSlotFirst = 1, kSlotLast = 2, kSlotEnd = 4 };
 
-struct SlotMeta { int row, chunk, n, flags; };
+struct SlotMeta { int row, part, j, chunk, n, flags, pad0, pad1; };
 
 struct StreamArgs {
   StepArgs a;
@@ -850,7 +850,7 @@ __global__ void __launch_bounds__(kStreamThreads, 3) row_stream_kernel(const Str
         }
         if (!have) {
           SlotMeta &mt = meta[slot];
-          mt.row = -1; mt.chunk = 0; mt.n = 0; mt.flags = kSlotEnd;
+          mt.row = -1; mt.part = 0; mt.j = 0; mt.chunk = 0; mt.n = 0; mt.flags = kSlotEnd;
           mbar_arrive(&full[slot]);
           break;
         }
@@ -858,6 +858,8 @@ __global__ void __launch_bounds__(kStreamThreads, 3) row_stream_kernel(const Str
         const int n = static_cast<int>(min(static_cast<int64_t>(CH), a.V - c0));
         SlotMeta &mt = meta[slot];
         mt.row = row;
+        mt.part = row / rpp;
+        mt.j = row - mt.part * rpp;
         mt.chunk = chunk;
         mt.n = n;
         mt.flags = (chunk == first ? kSlotFirst : 0) | (chunk + 1 == end ? kSlotLast : 0);
@@ -883,8 +885,8 @@ __global__ void __launch_bounds__(kStreamThreads, 3) row_stream_kernel(const Str
     const SlotMeta mt = meta[slot];
     if (mt.flags & kSlotEnd) break;
     const int row = mt.row;
-    const int part = row / rpp;
-    const int j = row - part * rpp;
+    const int part = mt.part;
+    const int j = mt.j;
     const bool is_bonus = j == a.K;
     const bool fast = !is_bonus || a.alpha != 1.f;
     if (mt.flags & kSlotFirst) { m_t = kNegInf; s_t = 0.f; }
@@ -894,11 +896,17 @@ __global__ void __launch_bounds__(kStreamThreads, 3) row_stream_kernel(const Str
     constexpr uint32_t kNegInfBits = sizeof(T) == 4 ? 0xff800000u : 0xff80ff80u;
     uint4 q[VPL];
     const uint4 *buf = bufs + static_cast<size_t>(slot) * (kChunkBytes / 16) + warp * (WCH / EPV);
-    const int wbase = warp * WCH;
+    if (mt.n == CH) {  // a full chunk: every vector is valid
 #pragma unroll
-    for (int v = 0; v < VPL; ++v) {
-      const bool ok = wbase + (v * 32 + lane) * EPV < mt.n;
-      q[v] = ok ? buf[v * 32 + lane] : make_uint4(kNegInfBits, kNegInfBits, kNegInfBits, kNegInfBits);
+      for (int v = 0; v < VPL; ++v) q[v] = buf[v * 32 + lane];
+    } else {
+      const int wbase = warp * WCH;
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) {
+        const bool ok = wbase + (v * 32 + lane) * EPV < mt.n;
+        q[v] = ok ? buf[v * 32 + lane]
+                  : make_uint4(kNegInfBits, kNegInfBits, kNegInfBits, kNegInfBits);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);  // this warp is done reading the slot
