@@ -293,7 +293,8 @@ def run_ours(args, world, rank, local):
                      "algorithmic_bytes_per_launch": bytes_step,
                      "avg_launch_ms": avg_launch_ms, "kernel": KERNEL,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
-        "gpu_launches": args.steps,
+        # each smc_step launches row_stream_kernel, finish_kernel and tail_kernel
+        "gpu_launches": 3 * args.steps,
         "clocks": clk,
     }
     if not args.no_e2e:

@@ -51,23 +51,13 @@ __device__ __forceinline__ void load_chunk(const char *chunk_base, int n_valid,
 }
 
 // exp(alpha (x - m)) as a float pair, accurate to ~3e-10 relative; -inf -> 0.
-// EXACT_DIFF: x - m is exact in fp32 (bf16 logits against a bf16 max, where
-// it matters); otherwise the rounding error of x - m is carried along.
-template <bool EXACT_DIFF>
+// x - m is taken exactly (two_sum): even for bf16 logits the difference is
+// not always a float (a logit 2^-16 times smaller than the max, say).
 __device__ __forceinline__ ff weight_term(float x, float m, float alpha, const float2 *tab) {
-  if (EXACT_DIFF && alpha == 1.f) {  // bf16 logits, plain target: exp(x - m) directly
-    return accurate_exp(x - m, 0.f, tab);  // -inf gives yh = -inf -> 0
-  }
   if (!(x > kNegInf)) return {0.f, 0.f};
-  float d, dl;
-  if (EXACT_DIFF) {
-    d = x - m; dl = 0.f;
-  } else {
-    const ff s = two_sum(x, -m);
-    d = s.hi; dl = s.lo;
-  }
-  ff ad = two_prod(alpha, d);
-  ad.lo = fmaf(alpha, dl, ad.lo);
+  const ff s = two_sum(x, -m);
+  ff ad = two_prod(alpha, s.hi);
+  ad.lo = fmaf(alpha, s.lo, ad.lo);
   return accurate_exp(ad.hi, ad.lo, tab);
 }
 
@@ -82,30 +72,22 @@ __device__ __forceinline__ ff prob_term(float x, ff big_l, const float2 *tab) {
 // ---------------------------------------------------------------------------
 // Sampling weights as exact fixed-point integers.
 //
-// weight_fixed returns exp(alpha (x - ref)) for x <= ref in units of 2^-52,
+// weight_fixed returns exp(alpha (x - ref)) for x <= ref in units of 2^-50,
 // rounded to an integer: the exponential is evaluated in float-float (about
 // 3e-10 relative) and each of its two float parts is converted exactly, so a
 // sum of these integers is order-independent and exact, and a prefix sum can
 // be compared with a target without rounding.  Weights below 2^-60 are 0, so
-// -inf (and NaN) logits weigh 0.  A sum of 2^10 weights stays below 2^63.
+// -inf (and NaN) logits weigh 0.  A sum of 2^12 weights stays below 2^63.
 // ---------------------------------------------------------------------------
-constexpr int kFixBits = 52;
+constexpr int kFixBits = 50;
 
-template <bool EXACT_DIFF>
 __device__ __forceinline__ long long weight_fixed(float x, float ref, float alpha,
                                                   const float2 *tab) {
-  float yh, yl;
-  if (EXACT_DIFF && alpha == 1.f) {           // bf16 logits, plain target: x - ref is exact
-    const float d = x - ref;
-    yh = d * kLog2eHi;
-    yl = fmaf(d, kLog2eLo, fmaf(d, kLog2eHi, -yh));
-  } else {
-    const ff s = two_sum(x, -ref);            // fp32 logits: keep the rounding of x - ref
-    ff ad = two_prod(alpha, s.hi);
-    ad.lo = fmaf(alpha, s.lo, ad.lo);
-    yh = ad.hi * kLog2eHi;
-    yl = fmaf(ad.hi, kLog2eHi, -yh) + fmaf(ad.hi, kLog2eLo, ad.lo * kLog2eHi);
-  }
+  const ff s = two_sum(x, -ref);              // x - ref exactly
+  ff ad = two_prod(alpha, s.hi);
+  ad.lo = fmaf(alpha, s.lo, ad.lo);
+  const float yh = ad.hi * kLog2eHi;
+  const float yl = fmaf(ad.hi, kLog2eHi, -yh) + fmaf(ad.hi, kLog2eLo, ad.lo * kLog2eHi);
   const bool live = yh > -60.f;               // false for -inf and NaN
   const float yc = fmaxf(yh, -60.f);
   constexpr float kShift = 12582912.f;        // 1.5 * 2^23: rounds yc*64 into the low bits
@@ -119,9 +101,97 @@ __device__ __forceinline__ long long weight_fixed(float x, float ref, float alph
   const float p = fmaf(r, kC1Hi, r * q);      // 2^r - 1
   const float2 tv = tab[ki & 63];             // 2^(j/64), float-float
   const float lo = fmaf(tv.x, p, fmaf(tv.y, p, tv.y));
-  const float sc = __int_as_float(((ki >> 6) + kFixBits + 127) << 23);  // 2^(n + 52)
+  const float sc = __int_as_float(((ki >> 6) + kFixBits + 127) << 23);  // 2^(n + kFixBits)
   const long long v = __float2ll_rn(tv.x * sc) + __float2ll_rn(lo * sc);
   return live ? v : 0ll;
+}
+
+// ---------------------------------------------------------------------------
+// Sampling-weight sums of a bonus row, two logits at a time on the packed
+// fp32x2 pipes (f32x2 add / sub / mul / fma).
+//
+// add() evaluates exp(alpha (x - ref)) for two logits x <= ref the way
+// weight_fixed does (x - ref exactly by two_sum; y = alpha (x - ref) log2(e)
+// as a float pair; 2^y = 2^n * 2^(j/64) * 2^r; 2^r - 1 by its Taylor
+// polynomial to r^3, whose remainder is below 4e-11 for |r| <= 1/128), about
+// 3e-10 relative, and adds them to a float-float running sum per half.
+// Logits below lb = ref - 40/alpha (also -inf and NaN) are raised to lb, so
+// they weigh e^-40 instead of less; init() reports whether lb is usable
+// (false when ref is so large that ref - 40/alpha rounds to ref).  The
+// running sums start at 2, above any single weight (<= 1), so fast_two_sum
+// is exact at every addition; total() removes the offset.
+// ---------------------------------------------------------------------------
+struct BonusPairSum {
+  unsigned long long acc, lo;        // packed running sums: head, tail
+  unsigned long long nref, al, nal;  // -ref, alpha, -alpha in both halves
+  float lb;
+
+  __device__ __forceinline__ bool init(float ref, float alpha, float span) {
+    acc = f2dup(2.f);
+    lo = 0ull;
+    nref = f2dup(-ref);
+    al = f2dup(alpha);
+    nal = f2dup(-alpha);
+    lb = ref - span;
+    return lb < ref && lb > kNegInf;
+  }
+
+  __device__ __forceinline__ void add(float x0, float x1, const float *th, const float *tl) {
+    constexpr float kShift = 12582912.f;  // 1.5 * 2^23: rounds 64 y into the low bits
+    const unsigned long long X = f2pack(fmaxf(x0, lb), fmaxf(x1, lb));
+    // d = x - ref as S + SE, exactly
+    const unsigned long long S = add2(X, nref);
+    const unsigned long long BB = sub2(S, X);
+    const unsigned long long SE = add2(sub2(X, sub2(S, BB)), sub2(nref, BB));
+    // a = alpha d as AH + AL
+    const unsigned long long AH = mul2(al, S);
+    const unsigned long long NAE = fma2(nal, S, AH);  // minus the rounding error of AH
+    const unsigned long long AL = sub2(mul2(al, SE), NAE);
+    // y = a log2(e) as YH - NYL
+    const unsigned long long YH = mul2(AH, f2dup(kLog2eHi));
+    const unsigned long long NYE = fma2(AH, f2dup(-kLog2eHi), YH);
+    const unsigned long long NYL =
+        fma2(AH, f2dup(-kLog2eLo), fma2(AL, f2dup(-kLog2eHi), NYE));
+    // y = ki/64 + r
+    const unsigned long long T = fma2(YH, f2dup(64.f), f2dup(kShift));
+    const unsigned long long K = sub2(T, f2dup(kShift));
+    const unsigned long long R = sub2(fma2(K, f2dup(-0.015625f), YH), NYL);
+    unsigned long long Q = fma2(R, f2dup(kC3), f2dup(kC2));
+    Q = fma2(R, Q, f2dup(kC1Lo));
+    const unsigned long long P = fma2(R, f2dup(kC1Hi), mul2(R, Q));  // 2^r - 1
+    float t0, t1;
+    f2unpack(T, t0, t1);
+    const int k0 = __float_as_int(t0) - 0x4B400000, k1 = __float_as_int(t1) - 0x4B400000;
+    const int j0 = k0 & 63, j1 = k1 & 63;
+    const unsigned long long TH = f2pack(th[j0], th[j1]), TL = f2pack(tl[j0], tl[j1]);
+    const unsigned long long LO = fma2(TH, P, fma2(TL, P, TL));  // 2^(j/64) 2^r - head
+    const unsigned long long SC = f2pack(__int_as_float(((k0 >> 6) + 127) << 23),
+                                         __int_as_float(((k1 >> 6) + 127) << 23));
+    const unsigned long long HT = mul2(TH, SC), LT = mul2(LO, SC);
+    const unsigned long long S2 = add2(acc, HT);
+    lo = add2(lo, add2(sub2(HT, sub2(S2, acc)), LT));
+    acc = S2;
+  }
+
+  // This lane's sum of the weights it added, as a float-float value.
+  __device__ __forceinline__ ff total() const {
+    float a0, a1, l0, l1;
+    f2unpack(acc, a0, a1);
+    f2unpack(lo, l0, l1);
+    ff e = two_sum(a0, -2.f), o = two_sum(a1, -2.f);
+    e.lo += l0;
+    o.lo += l1;
+    return ff_add(ff_norm(e), ff_norm(o));
+  }
+};
+
+// The 2^(j/64) table as separate head and tail arrays in shared memory.
+__device__ __forceinline__ void stage_exp2_split(float *th, float *tl) {
+  if (threadIdx.x < 64) {
+    const float2 v = kExp2Tab[threadIdx.x];
+    th[threadIdx.x] = v.x;
+    tl[threadIdx.x] = v.y;
+  }
 }
 
 __device__ __forceinline__ long long shfl_xor_ll(long long v, int o) {
@@ -141,12 +211,12 @@ __device__ __forceinline__ long long warp_incl_scan_ll(long long v) {
   }
   return v;
 }
-// A non-negative float-float value times 2^52, rounded to an integer.
+// A non-negative float-float value times 2^kFixBits, rounded to an integer.
 __device__ __forceinline__ long long ff_to_fixed(ff a) {
   const float sc = __int_as_float((kFixBits + 127) << 23);
   return __float2ll_rn(a.hi * sc) + __float2ll_rn(a.lo * sc);
 }
-// A fixed-point integer (units of 2^-52) as a float-float value.
+// A fixed-point integer (units of 2^-kFixBits) as a float-float value.
 __device__ __forceinline__ ff fixed_to_ff(long long v) {
   const float hi = __ll2float_rn(v);
   const long long rest = v - __float2ll_rn(hi);

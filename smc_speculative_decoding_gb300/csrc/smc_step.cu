@@ -1,17 +1,27 @@
 // SMC-SD step kernels for sm_103a.
 //
-// step_rows_kernel: one CTA per (row, chunk) of the logits.  It streams one
-// chunk of a target or draft row with 16-byte loads, reduces it to the chunk
-// max and sum of exp (fp32, MUFU ex2), and for the bonus row (target row K)
-// also to the float-float sum of the sampling weights exp(alpha (l - m)).
-// The last CTA to finish a row (atomic ticket, no waiting) combines the chunk
-// partials into the row's log-sum-exp, gathers the drafted token's logit, and
-// for the bonus row draws the bonus token by inverse CDF in vocabulary order.
-// The last row of a prompt then runs the prompt's tail in the same CTA:
-// importance-weight update, normalisation, ESS, systematic resampling, token
-// emission and the KV block-table remap ("Faster LLM Inference via Sequential
-// Monte Carlo", section 2 "核心流程" and "系统优化设计").  In SpS mode the tail
-// instead runs the acceptance scan of speculative sampling.
+// One step ("Faster LLM Inference via Sequential Monte Carlo", section 2
+// "核心流程": Score & Bonus, Reweight, Resample; "系统优化设计": KV pointer
+// exchange) runs as three kernels chained by programmatic dependent launch:
+//
+//   row_stream_kernel  every target and draft row once, through a shared-
+//                      memory ring filled by bulk copies: per (item, warp)
+//                      partial (max, sum of exp) of the log-sum-exp rows, and
+//                      per (chunk, warp) float-float sums of the bonus row's
+//                      sampling weights;
+//   finish_kernel      one warp per row: log-sum-exp and the drafted token's
+//                      logit, or for the bonus row the inverse-CDF draw (which
+//                      unit from the unit sums, then which element by an exact
+//                      fixed-point rescan of that unit);
+//   tail_kernel        one CTA per prompt: weight update, normalisation, ESS,
+//                      systematic resampling, token emission, KV remap; in SpS
+//                      mode the acceptance scan instead.
+//
+// Rows that are not 16-byte aligned (V * bytes per logit not a multiple of
+// 16, or a misaligned base pointer) take step_rows_kernel instead: one CTA per
+// (row, 16 KB chunk) with plain loads, and the last CTA of a row (atomic
+// ticket) combines it.  smc_resample and kv_blocktable_remap run the tail's
+// pieces alone (resample_kernel, kv_remap_kernel).
 #include <cmath>
 
 #include "row_common.cuh"
@@ -475,7 +485,6 @@ __global__ void __launch_bounds__(kThreads, 4) step_rows_kernel(const StepArgs a
   constexpr int EPT = G::kEPT;
   constexpr int CH = G::kCH;
   constexpr int ESZ = G::kESZ;
-  constexpr bool kExactDiff = sizeof(T) != 4;  // bf16 logits
 
   __shared__ float s_red[2 * kWarps];
   __shared__ float2 s_ff[kWarps];
@@ -536,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 4) step_rows_kernel(const StepArgs a
       const bool need_fast = a.alpha != 1.f;
 #pragma unroll
       for (int e = 0; e < EPT; ++e) {
-        ff_accum(S, weight_term<kExactDiff>(x[e], mc, a.alpha, s_tab));
+        ff_accum(S, weight_term(x[e], mc, a.alpha, s_tab));
         if (need_fast) s += fast_exp2(fmaf(x[e], kLog2e, -mb));
       }
     }
@@ -597,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 4) step_rows_kernel(const StepArgs a
       auto chunk_mass = [&](int c, ff *val, ff *f) {
         const float cm = __ldcg(&pp[c].m);
         if (ok && cm > kNegInf) {
-          *f = ff_norm(weight_term<false>(cm, M, alpha, s_tab));  // exp(alpha (m_c - M))
+          *f = ff_norm(weight_term(cm, M, alpha, s_tab));  // exp(alpha (m_c - M))
           *val = ff_mul(ff{__ldcg(&pp[c].shi), __ldcg(&pp[c].slo)}, *f);
         }
       };
@@ -643,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 4) step_rows_kernel(const StepArgs a
       const int len = static_cast<int>(min(static_cast<int64_t>(CH), a.V - sc0));
       tok = block_select_in_chunk(
           sc0, len, s_target,
-          [&](int64_t i) { return weight_term<kExactDiff>(Tr::scalar(rowp, i), cm, alpha, s_tab); },
+          [&](int64_t i) { return weight_term(Tr::scalar(rowp, i), cm, alpha, s_tab); },
           s_ff, s_int);
     }
     if (tid == 0) a.ws.results[row].tok = tok;
@@ -653,24 +662,24 @@ __global__ void __launch_bounds__(kThreads, 4) step_rows_kernel(const StepArgs a
 // ---------------------------------------------------------------------------
 // Streaming row kernel (shapes whose rows are 16-byte aligned).
 //
-// Each CTA has 8 consumer warps and 1 producer warp.  The producer claims
-// work items (G consecutive 16 KB chunks of one row) from an atomic counter,
-// in row order, and streams their chunks through a ring of kStages shared-
-// memory slots with bulk copies (cp.async.bulk; completion counted as tx
-// bytes on a per-slot mbarrier), as far ahead as the ring allows.  Consumer
-// warp w owns the contiguous eighth w of every chunk.  A lane folds its
-// logits into a running (max, sum of exp) pair over the item; at the item's
-// end the warp reduces it and writes one partial per (item, warp).  For the
-// bonus row each warp also writes, per chunk, the float-float sum of its
-// sampling weights relative to its own max there.  Every partial is
-// followed by an arrival on the row's ticket; the warp that arrives last
-// combines the row alone: log-sum-exp and gather, or for the bonus row the
-// inverse-CDF draw (which (chunk, warp) range, then which element, rescanned
-// by that warp).  There is no CTA-wide barrier after set-up.  The per-prompt
-// tail runs in tail_kernel, launched after this kernel.
+// Persistent CTAs, two per SM, each with 8 consumer warps and 1 producer
+// warp.  The producer claims work from two atomic queues, alternating: items
+// of G consecutive 32 KB chunks of one target or draft row (the log-sum-exp
+// rows), and single chunks of the bonus rows (target row K, whose sampling
+// weights cost far more arithmetic per logit).  It streams each chunk into a
+// ring of kStages shared-memory slots with one bulk copy (cp.async.bulk,
+// completion counted in bytes on the slot's mbarrier), as far ahead as the
+// ring allows.  Consumer warp w owns the contiguous eighth w of every chunk:
+// it copies its part to registers, releases the slot, and folds the logits
+// into a running (max, sum of exp) pair per lane (MUFU ex2, packed f32x2
+// arithmetic); at an item's end the warp writes one partial per (item,
+// warp).  For a bonus chunk the warp instead sums the sampling weights of
+// its range relative to the range's max in float-float (BonusPairSum) and
+// writes one unit partial.  No CTA-wide barrier after set-up; every wait is
+// bounded and reports SMC_DEV_TIMEOUT when it gives up.
 // ---------------------------------------------------------------------------
-constexpr int kStages = 4;
-constexpr int kChunkBytes = 16384;      // ChunkGeom<T>::kCH * kESZ for both dtypes
+constexpr int kStages = 3;
+constexpr int kChunkBytes = 32768;      // one ring slot: 16384 bf16 or 8192 fp32 logits
 constexpr int kConsumerWarps = 8;
 constexpr int kStreamThreads = (kConsumerWarps + 1) * 32;
 constexpr uint32_t kWaitLimit = 1u << 18;  // polls; each may suspend up to 20 us
@@ -679,12 +688,22 @@ enum : int { kSlotFirst = 1, kSlotLast = 2, kSlotEnd = 4 };
 
 struct SlotMeta { int row, part, j, chunk, n, flags, pad0, pad1; };
 
+// Logits per ring slot and per 16-byte vector of the streaming kernel.
+template <typename T> struct StreamGeom {
+  static constexpr int kESZ = sizeof(T) == 4 ? 4 : 2;
+  static constexpr int kEPV = 16 / kESZ;
+  static constexpr int kCH = kChunkBytes / kESZ;
+  static constexpr int kWCH = kCH / kConsumerWarps;  // logits of one consumer warp's range
+};
+
 struct StreamArgs {
   StepArgs a;
+  int snch;           // ring-slot chunks per row: ceil(V / StreamGeom<T>::kCH)
+  float wspan;        // 40 / alpha: logits further below a range's max weigh e^-40
   int G;              // chunks per work item of a non-bonus row
   int ipr;            // work items per non-bonus row
   int n_fast_items;   // non-bonus rows * ipr
-  int n_bonus_items;  // bonus rows * nch (one chunk per item)
+  int n_bonus_items;  // bonus rows * snch (one chunk per item)
 };
 
 constexpr size_t stream_dyn_smem() {
@@ -715,7 +734,6 @@ __device__ int warp_select_fixed(const char *rowp, int64_t r0, int len, long lon
   using Tr = LogitTraits<T>;
   constexpr int EPV = Tr::kPerVec;
   constexpr int NV = SEG / EPV;
-  constexpr bool kExactDiff = sizeof(T) != 4;
   const int lane = threadIdx.x & 31;
   const int beg = lane * SEG;
   const uint4 *src = reinterpret_cast<const uint4 *>(rowp + (r0 + beg) * ChunkGeom<T>::kESZ);
@@ -735,7 +753,7 @@ __device__ int warp_select_fixed(const char *rowp, int64_t r0, int len, long lon
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
 #pragma unroll
-    for (int e = 0; e < EPV; ++e) part += weight_fixed<kExactDiff>(Tr::at(q[v], e), ref, alpha, tab);
+    for (int e = 0; e < EPV; ++e) part += weight_fixed(Tr::at(q[v], e), ref, alpha, tab);
   }
   const long long incl = warp_incl_scan_ll(part);
   int cand = 0x7fffffff, last_pos = -1;
@@ -749,7 +767,7 @@ __device__ int warp_select_fixed(const char *rowp, int64_t r0, int len, long lon
       const uint4 qv = src[v];
 #pragma unroll
       for (int e = 0; e < EPV; ++e) {
-        const long long wv = weight_fixed<kExactDiff>(Tr::at(qv, e), ref, alpha, tab);
+        const long long wv = weight_fixed(Tr::at(qv, e), ref, alpha, tab);
         run += wv;
         if (wv > 0) {
           last_pos = beg + v * EPV + e;
@@ -769,15 +787,13 @@ __device__ int warp_select_fixed(const char *rowp, int64_t r0, int len, long lon
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kStreamThreads, 3) row_stream_kernel(const StreamArgs sa) {
-  using Tr = LogitTraits<T>;
-  using Gm = ChunkGeom<T>;
+__global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const StreamArgs sa) {
+  using Gm = StreamGeom<T>;
   constexpr int EPV = Gm::kEPV;                       // logits per 16-byte vector
   constexpr int CH = Gm::kCH;                         // logits per chunk
   constexpr int ESZ = Gm::kESZ;
-  constexpr int WCH = CH / kConsumerWarps;            // logits per warp range
+  constexpr int WCH = Gm::kWCH;                       // logits per warp range
   constexpr int VPL = WCH / EPV / 32;                 // vectors per lane per chunk
-  constexpr bool kExactDiff = sizeof(T) != 4;
   constexpr float kInf = -kNegInf;
   const StepArgs &a = sa.a;
 
@@ -786,7 +802,7 @@ __global__ void __launch_bounds__(kStreamThreads, 3) row_stream_kernel(const Str
   uint64_t *full = reinterpret_cast<uint64_t *>(dyn_smem + kStages * kChunkBytes);
   uint64_t *empty = full + kStages;
   SlotMeta *meta = reinterpret_cast<SlotMeta *>(empty + kStages);
-  __shared__ float2 s_tab[64];
+  __shared__ float s_th[64], s_tl[64];
   __shared__ int s_exited;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -800,7 +816,7 @@ __global__ void __launch_bounds__(kStreamThreads, 3) row_stream_kernel(const Str
     mbar_init_fence();
     s_exited = 0;
   }
-  stage_exp2_table(s_tab);
+  stage_exp2_split(s_th, s_tl);
   __syncthreads();  // the only CTA-wide barrier
 
   // ---- producer warp -----------------------------------------------------------
@@ -830,9 +846,9 @@ __global__ void __launch_bounds__(kStreamThreads, 3) row_stream_kernel(const Str
             const unsigned id = atomicAdd(&a.ws.work_counter[1], 1u);
             if (id >= static_cast<unsigned>(sa.n_bonus_items)) { bonus_done = true; continue; }
             ++n_bonus;
-            const int part = static_cast<int>(id) / a.nch;
+            const int part = static_cast<int>(id) / sa.snch;
             row = part * rpp + a.K;
-            first = static_cast<int>(id) - part * a.nch;
+            first = static_cast<int>(id) - part * sa.snch;
             end = first + 1;
           } else {
             const unsigned id = atomicAdd(&a.ws.work_counter[0], 1u);
@@ -843,7 +859,7 @@ __global__ void __launch_bounds__(kStreamThreads, 3) row_stream_kernel(const Str
             const int part = rf / rest, jj = rf - (rf / rest) * rest;
             row = part * rpp + (jj < a.K ? jj : jj + 1);
             first = g * sa.G;
-            end = min(first + sa.G, a.nch);
+            end = min(first + sa.G, sa.snch);
           }
           chunk = first;
           have = true;
@@ -914,16 +930,33 @@ __global__ void __launch_bounds__(kStreamThreads, 3) row_stream_kernel(const Str
     // the words of my vectors: 2 bf16 or 1 fp32 logit each
     const uint32_t *wd = reinterpret_cast<const uint32_t *>(q);
     constexpr int NW = VPL * 4;
+    // chunk max; for the bonus row NaN-propagating, since a NaN or +inf
+    // anywhere in it is an error
     float cm;
     if (sizeof(T) == 4) {
       cm = __uint_as_float(wd[0]);
+      if (is_bonus) {
 #pragma unroll
-      for (int k = 1; k < NW; ++k) cm = fmaxf(cm, __uint_as_float(wd[k]));
+        for (int k = 1; k < NW; ++k) cm = fmax_nan(cm, __uint_as_float(wd[k]));
+      } else {
+#pragma unroll
+        for (int k = 1; k < NW; ++k) cm = fmaxf(cm, __uint_as_float(wd[k]));
+      }
     } else {
       uint32_t mw = wd[0];
+      if (is_bonus) {
 #pragma unroll
-      for (int k = 1; k < NW; ++k) mw = bmax2(mw, wd[k]);
-      cm = fmaxf(bf16_lo(mw), bf16_hi(mw));
+        for (int k = 1; k < NW; ++k) mw = bmax2_nan(mw, wd[k]);
+        cm = fmax_nan(bf16_lo(mw), bf16_hi(mw));
+      } else {
+#pragma unroll
+        for (int k = 1; k < NW; ++k) mw = bmax2(mw, wd[k]);
+        cm = fmaxf(bf16_lo(mw), bf16_hi(mw));
+      }
+    }
+    if (is_bonus && !(cm < kInf)) {
+      raise_status(a.ws.status, SMC_DEV_NONFINITE);
+      cm = kNegInf;  // the outputs are unspecified now; keep the arithmetic finite
     }
     if (fast) {
       if (cm > m_t) {
@@ -957,37 +990,30 @@ __global__ void __launch_bounds__(kStreamThreads, 3) row_stream_kernel(const Str
       }
     }
     if (is_bonus) {
-      // NaN or +inf anywhere in the row is an error: a NaN-propagating max
-      float cmn;
-      if (sizeof(T) == 4) {
-        cmn = __uint_as_float(wd[0]);
-#pragma unroll
-        for (int k = 1; k < NW; ++k) cmn = fmax_nan(cmn, __uint_as_float(wd[k]));
-      } else {
-        uint32_t mw = wd[0];
-#pragma unroll
-        for (int k = 1; k < NW; ++k) mw = bmax2_nan(mw, wd[k]);
-        cmn = fmax_nan(bf16_lo(mw), bf16_hi(mw));
-      }
-      if (!(cmn < kInf)) raise_status(a.ws.status, SMC_DEV_NONFINITE);
-      const float ref = warp_max(cm);  // this unit's reference: its max logit
-      long long acc = 0;
-      if (ref > kNegInf && ref < kInf) {
-#pragma unroll
-        for (int k = 0; k < NW; ++k) {
+      // this unit's reference is its max logit; the weights relative to it
+      // are summed in float-float
+      const float ref = warp_max(cm);
+      ff usum{0.f, 0.f};
+      int flag = 0;
+      if (ref > kNegInf) {
+        BonusPairSum bs;
+        if (bs.init(ref, a.alpha, sa.wspan)) {
           if (sizeof(T) == 4) {
-            acc += weight_fixed<kExactDiff>(__uint_as_float(wd[k]), ref, a.alpha, s_tab);
+#pragma unroll
+            for (int k = 0; k < NW; k += 2)
+              bs.add(__uint_as_float(wd[k]), __uint_as_float(wd[k + 1]), s_th, s_tl);
           } else {
-            acc += weight_fixed<kExactDiff>(bf16_lo(wd[k]), ref, a.alpha, s_tab);
-            acc += weight_fixed<kExactDiff>(bf16_hi(wd[k]), ref, a.alpha, s_tab);
+#pragma unroll
+            for (int k = 0; k < NW; ++k) bs.add(bf16_lo(wd[k]), bf16_hi(wd[k]), s_th, s_tl);
           }
+          usum = warp_ff_sum(bs.total());
+        } else {
+          flag = 1;  // ref too large for the clamp: the finish kernel sums this unit
         }
       }
-      acc = warp_sum_ll(acc);
       if (lane == 0) {
-        a.ws.bonus_part[(static_cast<size_t>(part) * a.nch + mt.chunk) * kConsumerWarps + warp] =
-            make_int4(__float_as_int(ref), static_cast<int>(acc & 0xffffffffll),
-                      static_cast<int>(acc >> 32), 0);
+        a.ws.bonus_part[(static_cast<size_t>(part) * sa.snch + mt.chunk) * kConsumerWarps + warp] =
+            make_int4(__float_as_int(ref), __float_as_int(usum.hi), __float_as_int(usum.lo), flag);
       }
     }
 
@@ -1003,7 +1029,7 @@ __global__ void __launch_bounds__(kStreamThreads, 3) row_stream_kernel(const Str
       for (int o = 16; o > 0; o >>= 1) contrib += __shfl_xor_sync(0xffffffffu, contrib, o);
       if (lane == 0) {
         const int g = is_bonus ? mt.chunk : mt.chunk / sa.G;
-        a.ws.item_part[(static_cast<size_t>(row) * a.nch + g) * kConsumerWarps + warp] =
+        a.ws.item_part[(static_cast<size_t>(row) * sa.snch + g) * kConsumerWarps + warp] =
             make_float2(M, contrib);
       }
     }
@@ -1035,9 +1061,8 @@ __global__ void __launch_bounds__(kStreamThreads, 3) row_stream_kernel(const Str
 template <typename T>
 __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa) {
   using Tr = LogitTraits<T>;
-  using Gm = ChunkGeom<T>;
-  constexpr int CH = Gm::kCH;
-  constexpr int WCH = CH / kConsumerWarps;
+  constexpr int CH = StreamGeom<T>::kCH;
+  constexpr int WCH = StreamGeom<T>::kWCH;
   constexpr float kInf = -kNegInf;
   const StepArgs &a = sa.a;
   __shared__ float2 s_tab[64];
@@ -1056,8 +1081,8 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa) {
   const bool fast = !is_bonus || a.alpha != 1.f;
   const char *rowp = row_base<T>(a, row);
   const int gtok = is_bonus ? 0 : a.tokens[static_cast<size_t>(part) * a.K + (j < a.K ? j : j - a.K - 1)];
-  const float2 *ip = a.ws.item_part + static_cast<size_t>(row) * a.nch * kConsumerWarps;
-  const int n_ip = (is_bonus ? a.nch : sa.ipr) * kConsumerWarps;
+  const float2 *ip = a.ws.item_part + static_cast<size_t>(row) * sa.snch * kConsumerWarps;
+  const int n_ip = (is_bonus ? sa.snch : sa.ipr) * kConsumerWarps;
   float fM = kNegInf, fS = 0.f;  // fast log-sum-exp pieces of the row
   if (fast) {
     float lm = kNegInf, ls = 0.f;
@@ -1092,10 +1117,33 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa) {
     return;
   }
   // bonus row: units are (chunk, warp) ranges of WCH logits in vocabulary
-  // order, each with its max as reference and an exact fixed-point sum
+  // order, each with its max as reference and the float-float sum of its
+  // weights relative to it
   const float alpha = a.alpha;
-  const int4 *bp = a.ws.bonus_part + static_cast<size_t>(part) * a.nch * kConsumerWarps;
-  const int n_units = a.nch * kConsumerWarps;
+  int4 *bp = a.ws.bonus_part + static_cast<size_t>(part) * sa.snch * kConsumerWarps;
+  const int n_units = sa.snch * kConsumerWarps;
+  // a unit whose max was too large for the streaming kernel's clamp (flag
+  // set) is summed here instead, in exact fixed point
+  {
+    bool any = false;
+    for (int q = lane; q < n_units; q += 32) any |= bp[q].w != 0;
+    if (__any_sync(0xffffffffu, any)) {
+      for (int q = 0; q < n_units; ++q) {
+        const int4 pv = bp[q];
+        if (pv.w == 0) continue;
+        const float ref = __int_as_float(pv.x);
+        const int c = q / kConsumerWarps, w = q - c * kConsumerWarps;
+        const int64_t r0 = static_cast<int64_t>(c) * CH + static_cast<int64_t>(w) * WCH;
+        const int len = static_cast<int>(min(static_cast<int64_t>(WCH), a.V - r0));
+        long long sum = 0;
+        for (int i = lane; i < len; i += 32) sum += weight_fixed(Tr::scalar(rowp, r0 + i), ref, alpha, s_tab);
+        const ff v = fixed_to_ff(warp_sum_ll(sum));
+        __syncwarp();
+        if (lane == 0) bp[q] = make_int4(pv.x, __float_as_int(v.hi), __float_as_int(v.lo), 0);
+        __syncwarp();
+      }
+    }
+  }
   // the first kPre units of each lane stay in registers; longer rows reload
   constexpr int kPre = 4;
   int4 pre[kPre];
@@ -1124,10 +1172,8 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa) {
     const int4 pv = unit_of(q);
     const float ref = __int_as_float(pv.x);
     if (ok && ref > kNegInf) {
-      const long long sq = (static_cast<long long>(pv.z) << 32) |
-                           static_cast<long long>(static_cast<unsigned>(pv.y));
-      *f = ff_norm(weight_term<false>(ref, M, alpha, s_tab));  // exp(alpha (ref - M))
-      *val = ff_mul(fixed_to_ff(sq), *f);
+      *f = ff_norm(weight_term(ref, M, alpha, s_tab));  // exp(alpha (ref - M))
+      *val = ff_mul(ff{__int_as_float(pv.y), __int_as_float(pv.z)}, *f);
     }
   };
   ff total{0.f, 0.f};
@@ -1258,16 +1304,19 @@ static cudaError_t launch_stream(const StepArgs &a, long long rows, cudaStream_t
   cudaError_t e = stream_geometry<T>(&sms, &per_sm);
   if (e != cudaSuccess) return e;
   const long long grid_max = static_cast<long long>(sms) * per_sm;
-  const long long total_chunks = rows * a.nch;
-  // about six work items per resident CTA, each 1..8 chunks
-  const long long g = total_chunks / (grid_max * 6);
   StreamArgs sa{};
   sa.a = a;
+  sa.snch = static_cast<int>((static_cast<long long>(a.V) + StreamGeom<T>::kCH - 1) /
+                             StreamGeom<T>::kCH);
+  sa.wspan = 40.f / a.alpha;
+  const long long total_chunks = rows * sa.snch;
+  // about six work items per resident CTA, each 1..8 chunks
+  const long long g = total_chunks / (grid_max * 6);
   sa.G = static_cast<int>(g < 1 ? 1 : (g > 8 ? 8 : g));
-  sa.ipr = (a.nch + sa.G - 1) / sa.G;
+  sa.ipr = (sa.snch + sa.G - 1) / sa.G;
   const long long parts = rows / (2 * a.K + 1);
   sa.n_fast_items = static_cast<int>(parts * 2 * a.K * sa.ipr);
-  sa.n_bonus_items = static_cast<int>(parts * a.nch);
+  sa.n_bonus_items = static_cast<int>(parts * sa.snch);
   const long long n_items = static_cast<long long>(sa.n_fast_items) + sa.n_bonus_items;
   const long long grid = grid_max < n_items ? grid_max : n_items;
   row_stream_kernel<T><<<static_cast<unsigned>(grid), kStreamThreads, stream_dyn_smem(), stream>>>(sa);

@@ -30,7 +30,6 @@ struct SpsArgs {
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kThreads) sps_stats_kernel(const SpsArgs a) {
   using G = ChunkGeom<T>;
-  constexpr bool kExactDiff = sizeof(T) != 4;
   __shared__ float s_red[2 * kWarps];
   __shared__ float2 s_ff[kWarps];
   __shared__ float2 s_tab[64];
@@ -54,7 +53,7 @@ __global__ void __launch_bounds__(kThreads) sps_stats_kernel(const SpsArgs a) {
     ff S{0.f, 0.f};
     if (mc > kNegInf && mc < -kNegInf) {
 #pragma unroll
-      for (int e = 0; e < G::kEPT; ++e) ff_accum(S, weight_term<kExactDiff>(x[e], mc, 1.f, s_tab));
+      for (int e = 0; e < G::kEPT; ++e) ff_accum(S, weight_term(x[e], mc, 1.f, s_tab));
     }
     S = block_ff_sum(ff_norm(S), s_ff);
     if (tid == 0) a.ws.sps_part_pq[(static_cast<size_t>(b) * a.nch + c) * 2 + r] = make_float4(mc, S.hi, S.lo, 0.f);
@@ -81,7 +80,7 @@ __global__ void __launch_bounds__(kThreads) sps_stats_kernel(const SpsArgs a) {
         ff val{0.f, 0.f};
         if (cc < a.nch && M > kNegInf) {
           const float4 q = __ldcg(&a.ws.sps_part_pq[(static_cast<size_t>(b) * a.nch + cc) * 2 + r]);
-          if (q.x > kNegInf) val = ff_mul(ff{q.y, q.z}, ff_norm(weight_term<false>(q.x, M, 1.f, s_tab)));
+          if (q.x > kNegInf) val = ff_mul(ff{q.y, q.z}, ff_norm(weight_term(q.x, M, 1.f, s_tab)));
         }
         tot = ff_add(tot, warp_ff_sum(val));
       }
@@ -111,7 +110,6 @@ template <typename T, bool VEC>
 __global__ void __launch_bounds__(kThreads) sps_residual_kernel(const SpsArgs a) {
   using G = ChunkGeom<T>;
   using Tr = LogitTraits<T>;
-  constexpr bool kExactDiff = sizeof(T) != 4;
   __shared__ float2 s_ff[kWarps];
   __shared__ float2 s_tab[64];
   __shared__ int s_int[2 * kWarps];
@@ -181,7 +179,7 @@ __global__ void __launch_bounds__(kThreads) sps_residual_kernel(const SpsArgs a)
       auto chunk_mass = [&](int cc, ff *val, ff *f) {
         const float4 q = __ldcg(&pq[cc * 2]);
         if (q.x > kNegInf) {
-          *f = ff_norm(weight_term<false>(q.x, M, 1.f, s_tab));
+          *f = ff_norm(weight_term(q.x, M, 1.f, s_tab));
           *val = ff_mul(ff{q.y, q.z}, *f);
         }
       };
@@ -217,7 +215,7 @@ __global__ void __launch_bounds__(kThreads) sps_residual_kernel(const SpsArgs a)
       const float cm = s_sel_m;
       tok = block_select_in_chunk(
           sc0, len, s_rem,
-          [&](int64_t i) { return weight_term<kExactDiff>(Tr::scalar(prow, i), cm, 1.f, s_tab); },
+          [&](int64_t i) { return weight_term(Tr::scalar(prow, i), cm, 1.f, s_tab); },
           s_ff, s_int);
     }
   }
