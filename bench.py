@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--sigma-d", type=float, default=None, help="draft noise override")
     ap.add_argument("--episode", type=int, default=128, help="steps between KV resets")
     ap.add_argument("--e2e-steps", type=int, default=64)
+    ap.add_argument("--row-steps", type=int, default=256,
+                    help="steps of the separate row-pass timing run")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -84,9 +86,16 @@ def max_over_ranks(x, world):
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def input_seed(rank):
+    """Each rank draws its own prompts: the path shards by prompt, so the
+    ranks share nothing and the per-GPU work is fixed (weak scaling)."""
+    return 1000 + rank
 
 
 def workload(args):
@@ -201,7 +210,7 @@ def run_ours(args, world, rank, local):
     dev = f"cuda:{local}"
     w = workload(args)
     T, P = w.kv_dims(args.episode)
-    ring = [make_step_inputs(w, 1000 + rank, device=dev, step=s) for s in range(2)]
+    ring = [make_step_inputs(w, input_seed(rank), device=dev, step=s) for s in range(2)]
     kv0 = make_kv_state(w.B, w.N, w.prefix, w.block_size, T, P, device=dev)
     kv = {k: v.clone() for k, v in kv0.items()}
     p0 = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, 0)
@@ -267,11 +276,32 @@ def run_ours(args, world, rank, local):
     total_ms = max_over_ranks(total_ms, world)
     resampled_prompts = float(res_count.sum().item()) / args.steps
 
+    # the row pass alone: a second run of the same steps with the library's
+    # row-timing hook recording CUDA events around the streaming kernel
+    row_ms = []
+    done = 0
+    n_rows_steps = min(args.steps, args.row_steps)
+    while done < n_rows_steps:
+        reset()
+        n = min(args.episode, n_rows_steps - done)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for s in range(n):
+            smcsd.smc_set_row_timing_events(*evs[s])
+            step(args.warmup + done + s)
+        smcsd.smc_set_row_timing_events(None, None)
+        torch.cuda.synchronize()
+        row_ms += [b.elapsed_time(e) for b, e in evs]
+        done += n
+    row_launch_ms = max_over_ranks(float(np.mean(row_ms)), world)
+
     ptok = w.particle_tokens * args.steps * world
     value = ptok / (total_ms / 1e3)
     avg_launch_ms = float(np.mean(launch_ms))
     bytes_step = algorithmic_bytes(w, T, resampled_prompts)
-    achieved = bytes_step / (avg_launch_ms / 1e3) / 1e9
+    step_gbs = bytes_step / (avg_launch_ms / 1e3) / 1e9
+    row_bytes = w.B * w.N * (2 * w.K + 1) * w.V * w.bytes_per_logit
+    achieved = row_bytes / (row_launch_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak()
 
     out = {
@@ -290,9 +320,15 @@ def run_ours(args, world, rank, local):
         "resampled_prompts_per_step": resampled_prompts,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(),
-                     "algorithmic_bytes_per_launch": bytes_step,
-                     "avg_launch_ms": avg_launch_ms, "kernel": KERNEL,
+                     "kernel": KERNEL, "algorithmic_bytes_per_launch": row_bytes,
+                     "avg_launch_ms": row_launch_ms,
+                     "launch_timing": f"CUDA events around the row pass (library hook), "
+                                      f"{len(row_ms)} steps after the timed region",
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
+        "step_roofline": {"achieved": step_gbs, "frac": step_gbs / peak, "unit": "GB/s",
+                          "algorithmic_bytes_per_step": bytes_step,
+                          "avg_step_ms": avg_launch_ms,
+                          "kernels": ["row_stream_kernel", "finish_kernel", "tail_kernel"]},
         # each smc_step launches row_stream_kernel, finish_kernel and tail_kernel
         "gpu_launches": 3 * args.steps,
         "clocks": clk,

@@ -142,6 +142,20 @@ int32_t smc_workspace_init(void *workspace, size_t ws_bytes, void *stream);
 int32_t smc_device_status(void *workspace, int32_t clear, int32_t *out_bits,
                           void *stream);
 
+/* Measurement hook (no counterpart in the pages).  While set, every later
+ * smc_step, smc_step_noalloc and sps_verify records `rows_begin` on its
+ * stream just before the row pass (the kernel that streams the target and
+ * draft rows) and `rows_end` just after it, so a caller can time the
+ * vocabulary reduction alone with cudaEventElapsedTime.  Both are
+ * cudaEvent_t handles passed as void*, created and owned by the caller and
+ * created without cudaEventDisableTiming; NULL, NULL (the initial state)
+ * turns the hook off.  Recording `rows_end` separates the row pass from the
+ * kernels after it, which otherwise start while it drains, so a step timed
+ * with the hook on runs slightly longer.  One process-wide setting; set it
+ * from the thread that makes the calls.  Returns SMC_OK, or SMC_ERR_ARG when
+ * exactly one of the two is NULL. */
+int32_t smc_set_row_timing_events(void *rows_begin, void *rows_end);
+
 /* One SMC-SD step for B prompts x N particles ([SMC] section 2).
  *
  * target_logits [B, N, K+1, V]  row k < K scores drafted token k, row K is the

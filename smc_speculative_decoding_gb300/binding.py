@@ -64,6 +64,7 @@ _SIGS = {
                                              ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "sps_verify": (ctypes.c_int32, [ctypes.POINTER(smc_params)] + [ctypes.c_void_p] * 5 +
                    [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "smc_set_row_timing_events": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_void_p]),
 }
 
 
@@ -166,6 +167,24 @@ def smc_device_status(workspace, clear=False, stream=None):
     _check("smc_device_status", lib().smc_device_status(
         _ptr(workspace, "workspace"), int(bool(clear)), ctypes.byref(out), _stream(stream)))
     return out.value
+
+
+def smc_set_row_timing_events(rows_begin=None, rows_end=None):
+    """Record two torch.cuda.Event objects (created with enable_timing=True)
+    around the row pass of every later step; None, None turns it off.
+
+    The events are recorded once here, on the current stream, so that torch
+    creates them and treats them as recorded; the library records them
+    again, around the row pass, at every later step."""
+    def handle(ev):
+        if ev is None:
+            return None
+        if not isinstance(ev, torch.cuda.Event):
+            raise TypeError("expected a torch.cuda.Event")
+        ev.record()
+        return ctypes.c_void_p(ev.cuda_event)
+    _check("smc_set_row_timing_events",
+           lib().smc_set_row_timing_events(handle(rows_begin), handle(rows_end)))
 
 
 def status_names(bits):

@@ -169,6 +169,13 @@ int32_t smc_device_status(void *workspace, int32_t clear, int32_t *out_bits, voi
   return SMC_OK;
 }
 
+int32_t smc_set_row_timing_events(void *rows_begin, void *rows_end) {
+  if ((rows_begin == nullptr) != (rows_end == nullptr)) return SMC_ERR_ARG;
+  set_row_timing_events(static_cast<cudaEvent_t>(rows_begin),
+                        static_cast<cudaEvent_t>(rows_end));
+  return SMC_OK;
+}
+
 int32_t smc_step(const smc_params *p, const void *target_logits, const void *draft_logits,
                  const int32_t *draft_tokens, float *log_weights, int32_t *tokens_out,
                  int32_t *ancestors, float *ess, int32_t *resampled, const smc_kv *kv,

@@ -75,6 +75,9 @@ cudaError_t launch_resample(const Shape &s, float *log_weights, int32_t *ancesto
 cudaError_t launch_kv_remap(const Shape &s, const KvArgs &kv, const int32_t *ancestors,
                             const int32_t *resampled, int n_append, const Workspace &ws,
                             cudaStream_t stream);
+// Events recorded around the row pass of every later step (null: none).
+void set_row_timing_events(cudaEvent_t begin, cudaEvent_t end);
+
 cudaError_t launch_sps_residual(const Shape &s, const void *target, const void *draft,
                                 int32_t *tokens_out, const Workspace &ws, cudaStream_t stream);
 

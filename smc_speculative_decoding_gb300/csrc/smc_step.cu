@@ -160,51 +160,97 @@ __device__ ResampleResult normalise_resample_warp(int b, int N, float lw, bool v
 // one CTA.  Reference counts count table references; the free stack of prompt
 // b is free_list[b*P .. b*P + free_top[b]).  See smcsd.h (kv_blocktable_remap).
 //
-// old_t / old_l / bits hold a copy of the prompt's tables and token counts and
-// a cleared freed-block bitmap: in shared memory (staged) or in workspace
-// scratch.  s_nb holds each particle's used block count.  Loops run a warp
-// per particle and a lane per table slot, so no index needs a division.
+// The scratch holds a copy of the prompt's tables and token counts and a
+// cleared freed-block bitmap, in shared memory (staged) or in workspace
+// scratch.  Staged, it also holds copies of the prompt's reference counts,
+// of free_top and of the top kStackPre entries of the free stack, all read
+// while the weights are computed, so that the remap itself waits on no
+// global load; `delta` collects each block's net count change and then the
+// list of blocks freed by this remap.  s_nb holds each particle's used block
+// count.  Loops run a warp per particle and a lane per table slot, so no
+// index needs a division.
 // ---------------------------------------------------------------------------
+constexpr int kStackPre = 512;
+
 struct KvScratch {
   int *old_t;      // [N*T]
   int *old_l;      // [N]
   unsigned *bits;  // [ceil(P/32)]
+  int *rc;         // [P]  staged: reference counts of the prompt's pool (else null)
+  int *delta;      // [P]  staged: count changes, then the freed blocks (else null)
+  int *stk;        // [kStackPre] staged: stk[k] = free stack entry k below the top
+  int *top0;       // [1]  staged: free_top at copy-in
 };
 
-// Copy prompt b's tables and counts into the scratch and clear the bitmap,
-// using threads [t0, t0 + nt) of the CTA; no barrier inside.
+// dst[i] = src[i] for i in [0, n), by thread t of nt, with kB loads in
+// flight per thread before the first store.
+__device__ __forceinline__ void copy_batched(int *dst, const int32_t *src, int n, int t, int nt) {
+  constexpr int kB = 16;
+  for (int base = t; base < n; base += nt * kB) {
+    int v[kB];
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      const int i = base + u * nt;
+      v[u] = i < n ? __ldcg(src + i) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      const int i = base + u * nt;
+      if (i < n) dst[i] = v[u];
+    }
+  }
+}
+
+// Copy prompt b's state into the scratch and clear the bitmap, using threads
+// [t0, t0 + nt) of the CTA; no barrier inside.
 __device__ void kv_copy_in(const KvArgs &kv, int b, int N, const KvScratch &sc, int t0, int nt) {
-  const int T = kv.T;
-  const int words = (kv.P + 31) / 32;
-  const int32_t *tables = kv.tables + static_cast<size_t>(b) * N * T;
-  const int32_t *seq_len = kv.seq_len + static_cast<size_t>(b) * N;
+  const int T = kv.T, P = kv.P;
+  const int words = (P + 31) / 32;
   const int t = static_cast<int>(threadIdx.x) - t0;
   if (t < 0 || t >= nt) return;
-  const int NT = N * T;
-#pragma unroll 4
-  for (int idx = t; idx < NT; idx += nt) sc.old_t[idx] = tables[idx];
-  for (int i = t; i < N; i += nt) sc.old_l[i] = seq_len[i];
+  int top = 0;
+  if (sc.rc) top = __ldcg(kv.free_top + b);  // every thread; one transaction per warp
+  copy_batched(sc.old_t, kv.tables + static_cast<size_t>(b) * N * T, N * T, t, nt);
+  copy_batched(sc.old_l, kv.seq_len + static_cast<size_t>(b) * N, N, t, nt);
   for (int w = t; w < words; w += nt) sc.bits[w] = 0u;
+  if (sc.rc) {
+    const int32_t *stack = kv.free_list + static_cast<size_t>(b) * P;
+    copy_batched(sc.rc, kv.refcount + static_cast<size_t>(b) * P, P, t, nt);
+    for (int k = t; k < P; k += nt) sc.delta[k] = 0;
+    if (t == 0) *sc.top0 = top;
+    const int n_pre = (top >= 0 && top <= P) ? min(top, kStackPre) : 0;
+    for (int k = t; k < n_pre; k += nt) sc.stk[k] = __ldcg(stack + top - 1 - k);
+  }
 }
 
 __device__ void kv_remap_append(const KvArgs &kv, int b, int N, const int *s_anc, bool resampled,
                                 int n_append, const Workspace &ws, int *s_i, int *s_tail,
                                 int *s_nb, const KvScratch &sc, bool copied) {
-  __shared__ int s_flag;
+  __shared__ int s_flag, s_top_old, s_n_freed;
   const int T = kv.T, bs = kv.block_size, P = kv.P;
   const int lo_id = b * P;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int words = (P + 31) / 32;
+  const bool staged = sc.rc != nullptr;
   int32_t *tables = kv.tables + static_cast<size_t>(b) * N * T;
   int32_t *seq_len = kv.seq_len + static_cast<size_t>(b) * N;
   int32_t *stack = kv.free_list + static_cast<size_t>(b) * P;
   const long long cap = static_cast<long long>(T) * bs;  // tokens a full table holds
-  if (tid == 0) {
+  if (!copied) kv_copy_in(kv, b, N, sc, 0, kThreads);
+  if (!staged && tid == 0) {
     const int top0 = kv.free_top[b];
+    s_top_old = top0;
     s_flag = (top0 < 0 || top0 > P) ? 1 : 0;
     kv.n_cow[b] = 0;
   }
-  if (!copied) kv_copy_in(kv, b, N, sc, 0, kThreads);
+  __syncthreads();
+  if (staged && tid == 0) {
+    const int top0 = *sc.top0;
+    s_top_old = top0;
+    s_flag = (top0 < 0 || top0 > P) ? 1 : 0;
+    kv.n_cow[b] = 0;
+  }
+  if (tid == 0) s_n_freed = 0;
   __syncthreads();
   auto in_pool = [&](int blk) { return blk >= lo_id && blk < lo_id + P; };
   auto fail = [&]() {
@@ -232,37 +278,65 @@ __device__ void kv_remap_append(const KvArgs &kv, int b, int N, const int *s_anc
     }
     __syncthreads();
     if (s_flag) { fail(); return; }
-    // new references first, so no count touches 0 before every increment is in
-    for (int i = warp; i < N; i += kWarps) {
-      const int a = s_anc[i];
-      const int nb_new = s_nb[a], nb_old = s_nb[i];
-      for (int t = lane; t < nb_new; t += 32) {
-        const int blk = sc.old_t[a * T + t];
-        if (!(t < nb_old && sc.old_t[i * T + t] == blk)) atomicAdd(&kv.refcount[blk], 1);
+    if (staged) {
+      // net reference-count change per block in shared memory, then one pass
+      // over the pool applies it; a count reaching 0 frees the block
+      for (int i = warp; i < N; i += kWarps) {
+        const int a = s_anc[i];
+        const int nb_new = s_nb[a], nb_old = s_nb[i];
+        for (int t = lane; t < T; t += 32) {
+          const int nv = sc.old_t[a * T + t];
+          const int ov = t < nb_old ? sc.old_t[i * T + t] : -1;
+          if (t < nb_new && !(t < nb_old && ov == nv)) atomicAdd(&sc.delta[nv - lo_id], 1);
+          if (t < nb_old && !(t < nb_new && nv == ov)) atomicSub(&sc.delta[ov - lo_id], 1);
+          tables[i * T + t] = nv;
+        }
       }
-    }
-    __syncthreads();
-    for (int i = warp; i < N; i += kWarps) {
-      const int a = s_anc[i];
-      const int nb_new = s_nb[a], nb_old = s_nb[i];
-      for (int t = lane; t < T; t += 32) {
-        const int nv = sc.old_t[a * T + t];
-        if (t < nb_old) {
-          const int blk = sc.old_t[i * T + t];
-          if (!(t < nb_new && nv == blk)) {
-            if (atomicSub(&kv.refcount[blk], 1) == 1) {
-              const int rel = blk - lo_id;
-              atomicOr(&sc.bits[rel >> 5], 1u << (rel & 31));
+      for (int i = tid; i < N; i += kThreads) seq_len[i] = sc.old_l[s_anc[i]];
+      __syncthreads();
+      for (int k = tid; k < P; k += kThreads) {
+        const int d = sc.delta[k];
+        if (d != 0) {
+          const int nr = sc.rc[k] + d;
+          kv.refcount[lo_id + k] = nr;
+          if (nr == 0) atomicOr(&sc.bits[k >> 5], 1u << (k & 31));
+        }
+      }
+      __syncthreads();
+    } else {
+      // new references first, so no count touches 0 before every increment is in
+      for (int i = warp; i < N; i += kWarps) {
+        const int a = s_anc[i];
+        const int nb_new = s_nb[a], nb_old = s_nb[i];
+        for (int t = lane; t < nb_new; t += 32) {
+          const int blk = sc.old_t[a * T + t];
+          if (!(t < nb_old && sc.old_t[i * T + t] == blk)) atomicAdd(&kv.refcount[blk], 1);
+        }
+      }
+      __syncthreads();
+      for (int i = warp; i < N; i += kWarps) {
+        const int a = s_anc[i];
+        const int nb_new = s_nb[a], nb_old = s_nb[i];
+        for (int t = lane; t < T; t += 32) {
+          const int nv = sc.old_t[a * T + t];
+          if (t < nb_old) {
+            const int blk = sc.old_t[i * T + t];
+            if (!(t < nb_new && nv == blk)) {
+              if (atomicSub(&kv.refcount[blk], 1) == 1) {
+                const int rel = blk - lo_id;
+                atomicOr(&sc.bits[rel >> 5], 1u << (rel & 31));
+              }
             }
           }
+          tables[i * T + t] = nv;
         }
-        tables[i * T + t] = nv;
       }
+      for (int i = tid; i < N; i += kThreads) seq_len[i] = sc.old_l[s_anc[i]];
+      __syncthreads();
     }
-    for (int i = tid; i < N; i += kThreads) seq_len[i] = sc.old_l[s_anc[i]];
-    __syncthreads();
-    // push freed blocks in ascending id order
-    int top = kv.free_top[b];
+    // push freed blocks in ascending id order (staged: also list them in
+    // `delta`, whose counts are spent)
+    int top = s_top_old;
     for (int w0 = 0; w0 < words; w0 += kThreads) {
       const int w = w0 + tid;
       unsigned fb = w < words ? sc.bits[w] : 0u;
@@ -272,14 +346,20 @@ __device__ void kv_remap_append(const KvArgs &kv, int b, int N, const int *s_anc
       while (fb) {
         const int bit = __ffs(fb) - 1;
         fb &= fb - 1;
-        if (pos < P) stack[pos] = lo_id + w * 32 + bit;
+        if (pos < P) {
+          stack[pos] = lo_id + w * 32 + bit;
+          if (staged) sc.delta[pos - s_top_old] = lo_id + w * 32 + bit;
+        }
         ++pos;
       }
       top += total;
     }
     if (top > P) s_flag = 1;  // counts did not match the tables
     __syncthreads();
-    if (tid == 0) kv.free_top[b] = min(top, P);
+    if (tid == 0) {
+      kv.free_top[b] = min(top, P);
+      s_n_freed = min(top, P) - s_top_old;
+    }
     if (s_flag) { fail(); return; }
     __syncthreads();
   }
@@ -312,7 +392,8 @@ __device__ void kv_remap_append(const KvArgs &kv, int b, int N, const int *s_anc
   int total_pops, n_forks;
   const int off = block_excl_scan_i(fork + grow, s_i, &total_pops);
   const int cidx = block_excl_scan_i(fork, s_i, &n_forks);
-  const int top = kv.free_top[b];
+  const int n_freed = s_n_freed, top_old = s_top_old;
+  const int top = top_old + n_freed;
   __syncthreads();
   if (s_flag == 2) {
     if (tid == 0) raise_status(ws.status, SMC_DEV_TABLE_OVERFLOW);
@@ -322,10 +403,18 @@ __device__ void kv_remap_append(const KvArgs &kv, int b, int N, const int *s_anc
     if (tid == 0) raise_status(ws.status, SMC_DEV_POOL_EXHAUSTED);
     return;
   }
+  // the k-th pop from the top: this remap's freed blocks first (the last
+  // pushed on top), then the stack as it was
+  auto pop = [&](int k) -> int {
+    if (!staged) return stack[top - 1 - k];
+    if (k < n_freed) return sc.delta[n_freed - 1 - k];
+    const int j = k - n_freed;
+    return j < kStackPre ? sc.stk[j] : stack[top_old - 1 - j];
+  };
   if (valid) {
     int k = off;
     if (fork) {
-      const int d = stack[top - 1 - k];
+      const int d = pop(k);
       ++k;
       if (in_pool(d)) {
         int32_t *pair = kv.cow_pairs + (static_cast<size_t>(b) * N + cidx) * 2;
@@ -339,7 +428,7 @@ __device__ void kv_remap_append(const KvArgs &kv, int b, int N, const int *s_anc
       }
     }
     for (int g = 0; g < grow; ++g) {
-      const int d = stack[top - 1 - k];
+      const int d = pop(k);
       ++k;
       if (in_pool(d)) {
         tables[tid * T + nb + g] = d;
@@ -358,18 +447,24 @@ __device__ void kv_remap_append(const KvArgs &kv, int b, int N, const int *s_anc
 
 // Shared-memory words a staged remap needs, and whether a shape fits.
 __host__ __device__ inline size_t kv_stage_words(int N, int T, int P) {
-  return static_cast<size_t>(N) * T + N + (P + 31) / 32;
+  return static_cast<size_t>(N) * T + N + (P + 31) / 32 + 2 * static_cast<size_t>(P) +
+         kStackPre + 1;
 }
 constexpr size_t kKvStageMaxBytes = 96 * 1024;
 
 // Scratch of a remap: staged in `dyn` shared memory, or workspace scratch.
 __device__ inline KvScratch kv_scratch(const KvArgs &kv, int b, int N, const Workspace &ws,
                                        int *dyn, bool staged) {
-  KvScratch sc;
+  KvScratch sc{};
   if (staged) {
+    const int P = kv.P;
     sc.old_t = dyn;
     sc.old_l = dyn + static_cast<size_t>(N) * kv.T;
     sc.bits = reinterpret_cast<unsigned *>(sc.old_l + N);
+    sc.rc = reinterpret_cast<int *>(sc.bits + (P + 31) / 32);
+    sc.delta = sc.rc + P;
+    sc.stk = sc.delta + P;
+    sc.top0 = sc.stk + kStackPre;
   } else {
     sc.old_t = ws.kv_old_tables + static_cast<size_t>(b) * N * kv.T;
     sc.old_l = ws.kv_old_len + static_cast<size_t>(b) * N;
@@ -381,7 +476,10 @@ __device__ inline KvScratch kv_scratch(const KvArgs &kv, int b, int N, const Wor
 // ---------------------------------------------------------------------------
 // Prompt tails.
 // ---------------------------------------------------------------------------
+constexpr int kTailTokens = 2048;  // drafted tokens of a prompt staged in shared memory
+
 struct TailSmem {
+  int tok[kTailTokens];
   float c[SMC_MAX_N];
   float red[2 * kWarps];
   int anc[SMC_MAX_N];
@@ -391,23 +489,34 @@ struct TailSmem {
   int ired[2 * kWarps];
 };
 
+// Runs in tail_kernel, launched with programmatic dependent launch while the
+// finish kernel still runs.  The KV state, the incoming log-weights and the
+// drafted tokens were all written before this step's first kernel, so they
+// are read before waiting for the finish kernel; only the row results are
+// read after.
 __device__ void smc_tail(const StepArgs &a, int b, TailSmem &sm, int *dyn, bool kv_staged) {
   const int N = a.N, K = a.K, rpp = 2 * K + 1;
   const int tid = threadIdx.x;
   const bool small = N <= 32;
   __shared__ int s_res;
   const KvScratch sc = a.use_kv ? kv_scratch(a.kv, b, N, a.ws, dyn, kv_staged) : KvScratch{};
-  // with N <= 32, warp 0 does the weights while the other warps copy the KV tables
+  if (a.use_kv) kv_copy_in(a.kv, b, N, sc, 0, kThreads);
+  const bool tok_staged = N * K <= kTailTokens;
+  if (tok_staged) {
+    copy_batched(sm.tok, a.tokens + static_cast<size_t>(b) * N * K, N * K, tid, kThreads);
+  }
+  const bool valid = tid < N;
+  const int part = b * N + tid;
+  const float lw0 = valid ? __ldcg(a.out.log_weights + part) : 0.f;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (tok_staged) __syncthreads();  // sm.tok complete
+  // with N <= 32, warp 0 alone does the weights (shuffles, no CTA barrier)
   const bool weights_thread = small ? tid < 32 : true;
-  if (small && a.use_kv && tid >= 32) kv_copy_in(a.kv, b, N, sc, 32, kThreads - 32);
   if (weights_thread) {
-    const bool valid = tid < N;
     float lwf = 0.f;
     if (valid) {
-      const int part = b * N + tid;
       const RowResult *r = a.ws.results + static_cast<size_t>(part) * rpp;
       const float4 rb = __ldcg(reinterpret_cast<const float4 *>(r + K));
-      const float lw0 = a.out.log_weights[part];
       float delta = 0.f;
 #pragma unroll 4
       for (int k = 0; k < K; ++k) {
@@ -425,14 +534,19 @@ __device__ void smc_tail(const StepArgs &a, int b, TailSmem &sm, int *dyn, bool 
               : normalise_resample(b, N, lwf, valid, a.ess_frac, a.seed, a.step, a.ws.status,
                                    sm.anc, sm.c, sm.red);
     if (valid) {
-      const int part = b * N + tid;
       const int anc = sm.anc[tid];
       a.out.log_weights[part] = rr.resampled ? 0.f : lwf;
       a.out.ancestors[part] = anc;
       int32_t *dst = a.out.tokens_out + static_cast<size_t>(part) * (K + 1);
-      const int32_t *srcp = a.tokens + static_cast<size_t>(b * N + anc) * K;
+      if (tok_staged) {
+        const int *srcp = sm.tok + anc * K;
 #pragma unroll 4
-      for (int k = 0; k < K; ++k) dst[k] = srcp[k];
+        for (int k = 0; k < K; ++k) dst[k] = srcp[k];
+      } else {
+        const int32_t *srcp = a.tokens + static_cast<size_t>(b * N + anc) * K;
+#pragma unroll 4
+        for (int k = 0; k < K; ++k) dst[k] = srcp[k];
+      }
       dst[K] = sm.bonus[anc];
     }
     if (tid == 0) {
@@ -444,7 +558,7 @@ __device__ void smc_tail(const StepArgs &a, int b, TailSmem &sm, int *dyn, bool 
   __syncthreads();
   if (a.use_kv) {
     kv_remap_append(a.kv, b, N, sm.anc, s_res != 0, K + 1, a.ws, sm.ired, sm.tail, sm.nb, sc,
-                    small);
+                    true);
   }
 }
 
@@ -721,71 +835,6 @@ __device__ __forceinline__ const char *row_base(const StepArgs &a, int row) {
       : a.draft + (static_cast<size_t>(part) * a.K + (j - a.K - 1)) * static_cast<size_t>(a.V) * ESZ;
 }
 
-// Warp-level inverse-CDF selection inside the range [r0, r0 + len) of a row
-// (r0 and len multiples of the 16-byte vector width, len <= 32 * SEG), in
-// exact fixed-point arithmetic: the first element with a positive weight
-// weight_fixed(l, ref) whose inclusive prefix exceeds `target`; if none does
-// (the target at or past the range's total), the last positive element; -1
-// with no mass.  Lane l holds the contiguous segment [l*SEG, (l+1)*SEG),
-// loaded with 16-byte loads (one round trip).
-template <typename T, int SEG>
-__device__ int warp_select_fixed(const char *rowp, int64_t r0, int len, long long target,
-                                 float ref, float alpha, const float2 *tab) {
-  using Tr = LogitTraits<T>;
-  constexpr int EPV = Tr::kPerVec;
-  constexpr int NV = SEG / EPV;
-  const int lane = threadIdx.x & 31;
-  const int beg = lane * SEG;
-  const uint4 *src = reinterpret_cast<const uint4 *>(rowp + (r0 + beg) * ChunkGeom<T>::kESZ);
-  uint4 q[NV];
-#pragma unroll
-  for (int v = 0; v < NV; ++v) {
-    q[v] = beg + v * EPV < len ? src[v] : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u,
-                                                     0xff80ff80u);
-  }
-  if (sizeof(T) == 4) {
-#pragma unroll
-    for (int v = 0; v < NV; ++v) {
-      if (!(beg + v * EPV < len)) q[v] = make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
-    }
-  }
-  long long part = 0;
-#pragma unroll
-  for (int v = 0; v < NV; ++v) {
-#pragma unroll
-    for (int e = 0; e < EPV; ++e) part += weight_fixed(Tr::at(q[v], e), ref, alpha, tab);
-  }
-  const long long incl = warp_incl_scan_ll(part);
-  int cand = 0x7fffffff, last_pos = -1;
-  if (part > 0) {
-    // lanes holding mass walk their segment again, one vector at a time
-    // (reloaded from L2), recomputing the weights identically
-    long long run = incl - part;
-#pragma unroll 1
-    for (int v = 0; v < NV; ++v) {
-      if (!(beg + v * EPV < len)) break;
-      const uint4 qv = src[v];
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) {
-        const long long wv = weight_fixed(Tr::at(qv, e), ref, alpha, tab);
-        run += wv;
-        if (wv > 0) {
-          last_pos = beg + v * EPV + e;
-          if (cand == 0x7fffffff && run > target) cand = beg + v * EPV + e;
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
-  if (cand == 0x7fffffff) {
-    cand = last_pos;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) cand = max(cand, __shfl_xor_sync(0xffffffffu, cand, o));
-  }
-  return cand < 0 ? -1 : static_cast<int>(r0 + cand);
-}
-
 template <typename T>
 __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const StreamArgs sa) {
   using Gm = StreamGeom<T>;
@@ -830,6 +879,10 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
       int row = 0, first = 0, chunk = 0, end = 0;
       int n_fast = 0, n_bonus = 0;
       bool have = false, fast_done = sa.n_fast_items == 0, bonus_done = sa.n_bonus_items == 0;
+      // each queue's next claim is issued one item ahead, so that the
+      // atomic's round trip overlaps the copies of the current item
+      unsigned next_fast = fast_done ? 0u : atomicAdd(&a.ws.work_counter[0], 1u);
+      unsigned next_bonus = bonus_done ? 0u : atomicAdd(&a.ws.work_counter[1], 1u);
       for (int i = 0;; ++i) {
         const int slot = i % kStages;
         if (i >= kStages &&
@@ -843,16 +896,18 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
           if (fast_done && bonus_done) break;
           const bool take_bonus = !bonus_done && (fast_done || n_bonus < n_fast);
           if (take_bonus) {
-            const unsigned id = atomicAdd(&a.ws.work_counter[1], 1u);
+            const unsigned id = next_bonus;
             if (id >= static_cast<unsigned>(sa.n_bonus_items)) { bonus_done = true; continue; }
+            next_bonus = atomicAdd(&a.ws.work_counter[1], 1u);
             ++n_bonus;
             const int part = static_cast<int>(id) / sa.snch;
             row = part * rpp + a.K;
             first = static_cast<int>(id) - part * sa.snch;
             end = first + 1;
           } else {
-            const unsigned id = atomicAdd(&a.ws.work_counter[0], 1u);
+            const unsigned id = next_fast;
             if (id >= static_cast<unsigned>(sa.n_fast_items)) { fast_done = true; continue; }
+            next_fast = atomicAdd(&a.ws.work_counter[0], 1u);
             ++n_fast;
             const int rf = static_cast<int>(id) / sa.ipr;
             const int g = static_cast<int>(id) - rf * sa.ipr;
@@ -1051,40 +1106,135 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
 
 
 // ---------------------------------------------------------------------------
-// Row combine, one warp per row, after the streaming kernel: the row's
-// log-sum-exp from its (item, warp) partials and the drafted token's logit;
-// for the bonus row, the inverse-CDF draw in vocabulary order: which (chunk,
-// warp) unit, from the units' exact fixed-point sums, then which element,
-// rescanning that unit exactly.  Launched with programmatic dependent launch;
-// waits for the streaming kernel before reading its partials.
+// CTA-wide inverse-CDF selection inside the range [r0, r0 + len) of a row, in
+// exact fixed-point arithmetic: the first element with a positive weight
+// weight_fixed(l, ref) whose inclusive prefix exceeds `target`; if none does
+// (the target at or past the range's total), the last positive element; -1
+// with no mass.  Thread t holds the one 16-byte vector [t*EPT, (t+1)*EPT)
+// (EPT logits); r0 and len are multiples of EPT, len <= kThreads * EPT, and
+// the row is 16-byte aligned.  All threads must call it; all get the result.
+// ---------------------------------------------------------------------------
+template <typename T, int EPT>
+__device__ int block_select_fixed(const char *rowp, int64_t r0, int len, long long target,
+                                  float ref, float alpha, const float2 *tab,
+                                  long long *s_ll, int *s_i) {
+  using Tr = LogitTraits<T>;
+  static_assert(EPT == Tr::kPerVec, "one 16-byte vector per thread");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int beg = tid * EPT;
+  long long w[EPT];
+  long long part = 0;
+  const bool have = beg < len;
+  const uint4 v = have ? *reinterpret_cast<const uint4 *>(rowp + (r0 + beg) * StreamGeom<T>::kESZ)
+                       : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    w[e] = have ? weight_fixed(Tr::at(v, e), ref, alpha, tab) : 0ll;
+    part += w[e];
+  }
+  // block inclusive scan of the per-thread sums
+  const long long incl_w = warp_incl_scan_ll(part);
+  if (lane == 31) s_ll[warp] = incl_w;
+  __syncthreads();
+  long long base = 0;
+  for (int k = 0; k < warp; ++k) base += s_ll[k];
+  const long long incl = base + incl_w;
+  int cand = 0x7fffffff, last = -1;
+  long long run = incl - part;
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    run += w[e];
+    if (w[e] > 0) {
+      last = beg + e;
+      if (cand == 0x7fffffff && run > target) cand = beg + e;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
+    last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+  }
+  if (lane == 0) {
+    s_i[warp] = cand;
+    s_i[kWarps + warp] = last;
+  }
+  __syncthreads();
+  int c = 0x7fffffff, l = -1;
+#pragma unroll
+  for (int k = 0; k < kWarps; ++k) {
+    c = min(c, s_i[k]);
+    l = max(l, s_i[kWarps + k]);
+  }
+  __syncthreads();  // s_ll and s_i may be reused by the caller
+  if (c == 0x7fffffff) c = l;
+  return c < 0 ? -1 : static_cast<int>(r0 + c);
+}
+
+// ---------------------------------------------------------------------------
+// Row combine after the streaming kernel, launched with programmatic
+// dependent launch (it waits for the streaming kernel before reading its
+// partials).  The first n_fast_ctas CTAs take the log-sum-exp rows, one warp
+// per row: the row's log-sum-exp from its (item, warp) partials and the
+// drafted token's logit.  Each further CTA takes one bonus row: warp 0 finds
+// which (chunk, warp) unit holds u times the total from the units'
+// float-float sums, then the whole CTA rescans that unit in exact fixed
+// point to find the element (inverse CDF in vocabulary order).
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa) {
+__global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa, int n_fast_ctas) {
   using Tr = LogitTraits<T>;
   constexpr int CH = StreamGeom<T>::kCH;
   constexpr int WCH = StreamGeom<T>::kWCH;
   constexpr float kInf = -kNegInf;
   const StepArgs &a = sa.a;
   __shared__ float2 s_tab[64];
+  __shared__ long long s_ll[kWarps];
+  __shared__ int s_i[2 * kWarps];
+  __shared__ long long s_target;
+  __shared__ int s_sel;
+  __shared__ float s_ref;
+  __shared__ float s_red[2 * kWarps];
+  __shared__ float2 s_f2[kWarps];
   stage_exp2_table(s_tab);
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int rpp = 2 * a.K + 1;
-  const long long rows = static_cast<long long>(a.B) * a.N * rpp;
-  const long long row_ll = static_cast<long long>(blockIdx.x) * kWarps + warp;
-  if (row_ll >= rows) return;
-  const int row = static_cast<int>(row_ll);
-  const int part = row / rpp, j = row - part * rpp;
+  const bool bonus_cta = static_cast<int>(blockIdx.x) >= n_fast_ctas;
+  int row, part, j;
+  bool live = true;
+  if (!bonus_cta) {
+    const long long n_fast_rows = static_cast<long long>(a.B) * a.N * 2 * a.K;
+    const long long rf = static_cast<long long>(blockIdx.x) * kWarps + warp;
+    live = rf < n_fast_rows;
+    part = live ? static_cast<int>(rf / (2 * a.K)) : 0;
+    const int jj = live ? static_cast<int>(rf - static_cast<long long>(part) * 2 * a.K) : 0;
+    j = jj < a.K ? jj : jj + 1;
+  } else {
+    part = static_cast<int>(blockIdx.x) - n_fast_ctas;
+    j = a.K;
+  }
+  row = part * rpp + j;
   const bool is_bonus = j == a.K;
   const bool fast = !is_bonus || a.alpha != 1.f;
   const char *rowp = row_base<T>(a, row);
-  const int gtok = is_bonus ? 0 : a.tokens[static_cast<size_t>(part) * a.K + (j < a.K ? j : j - a.K - 1)];
-  const float2 *ip = a.ws.item_part + static_cast<size_t>(row) * sa.snch * kConsumerWarps;
-  const int n_ip = (is_bonus ? sa.snch : sa.ipr) * kConsumerWarps;
-  float fM = kNegInf, fS = 0.f;  // fast log-sum-exp pieces of the row
+  // the drafted token and its logit are inputs of the step: gathered while
+  // the streaming kernel still runs
+  int gtok = 0;
+  float gv = 0.f;
+  if (!is_bonus && live && lane == 0) {
+    gtok = a.tokens[static_cast<size_t>(part) * a.K + (j < a.K ? j : j - a.K - 1)];
+    gv = (gtok < 0 || gtok >= a.V) ? __int_as_float(0x7fc00000) : Tr::scalar(rowp, gtok);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __syncthreads();
+  if (!live) return;
+
+  // fast log-sum-exp pieces of the row (every warp of a bonus CTA computes
+  // them; only warp 0's are used)
+  float fM = kNegInf, fS = 0.f;
   if (fast) {
+    const float2 *ip = a.ws.item_part + static_cast<size_t>(row) * sa.snch * kConsumerWarps;
+    const int n_ip = (is_bonus ? sa.snch : sa.ipr) * kConsumerWarps;
     float lm = kNegInf, ls = 0.f;
 #pragma unroll 4
     for (int c = lane; c < n_ip; c += 32) {
@@ -1109,22 +1259,21 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa) {
       else if (!(fS < kInf) || fM == kInf) bits |= SMC_DEV_NONFINITE;
       const float lse = fM + logf(fS);
       if (gtok < 0 || gtok >= a.V) bits |= SMC_DEV_BAD_TOKEN;
-      const float gv =
-          (gtok < 0 || gtok >= a.V) ? __int_as_float(0x7fc00000) : Tr::scalar(rowp, gtok);
       if (bits) raise_status(a.ws.status, bits);
       a.ws.results[row] = RowResult{lse, gv, 0.f, -1};
     }
     return;
   }
-  // bonus row: units are (chunk, warp) ranges of WCH logits in vocabulary
+
+  // ---- bonus row: units are (chunk, warp) ranges of WCH logits in vocabulary
   // order, each with its max as reference and the float-float sum of its
   // weights relative to it
   const float alpha = a.alpha;
   int4 *bp = a.ws.bonus_part + static_cast<size_t>(part) * sa.snch * kConsumerWarps;
   const int n_units = sa.snch * kConsumerWarps;
-  // a unit whose max was too large for the streaming kernel's clamp (flag
-  // set) is summed here instead, in exact fixed point
-  {
+  if (warp == 0) {
+    // a unit whose max was too large for the streaming kernel's clamp (flag
+    // set) is summed here instead, in exact fixed point
     bool any = false;
     for (int q = lane; q < n_units; q += 32) any |= bp[q].w != 0;
     if (__any_sync(0xffffffffu, any)) {
@@ -1144,67 +1293,97 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa) {
       }
     }
   }
-  // the first kPre units of each lane stay in registers; longer rows reload
-  constexpr int kPre = 4;
-  int4 pre[kPre];
-#pragma unroll
-  for (int r = 0; r < kPre; ++r) {
-    const int q = r * 32 + lane;
-    pre[r] = q < n_units ? bp[q] : make_int4(__float_as_int(kNegInf), 0, 0, 0);
-  }
-  float M = kNegInf;
-#pragma unroll
-  for (int r = 0; r < kPre; ++r) M = fmaxf(M, __int_as_float(pre[r].x));
-  for (int q = kPre * 32 + lane; q < n_units; q += 32) M = fmaxf(M, __int_as_float(bp[q].x));
-  M = warp_max(M);
-  const bool ok = M > kNegInf && M < kInf;
-  auto unit_of = [&](int q) -> int4 {
-    const int r = (q - lane) >> 5;
-    if (q < kPre * 32) {
-      int4 v = pre[0];
-#pragma unroll
-      for (int k = 1; k < kPre; ++k) v = r == k ? pre[k] : v;
-      return v;
-    }
-    return bp[q];
-  };
-  auto unit_mass = [&](int q, ff *val, ff *f) {
-    const int4 pv = unit_of(q);
-    const float ref = __int_as_float(pv.x);
-    if (ok && ref > kNegInf) {
-      *f = ff_norm(weight_term(ref, M, alpha, s_tab));  // exp(alpha (ref - M))
-      *val = ff_mul(ff{__int_as_float(pv.y), __int_as_float(pv.z)}, *f);
-    }
-  };
-  ff total{0.f, 0.f};
-  for (int q0 = 0; q0 < n_units; q0 += 32) {
-    ff val{0.f, 0.f}, f{1.f, 0.f};
-    if (q0 + lane < n_units) unit_mass(q0 + lane, &val, &f);
-    total = ff_add(total, warp_ff_sum(val));
-  }
+  __syncthreads();
   const float u = philox_uniform(a.seed, a.step, part, a.K, SMC_PURPOSE_BONUS);
-  ff rem{0.f, 0.f};
-  const int sel = ok ? warp_find_chunk(n_units, ff_mul_f(total, u), unit_mass, &rem) : -1;
-  int tok = -1;
-  if (sel >= 0) {
-    const float ref = __int_as_float(bp[sel].x);
-    const int c = sel / kConsumerWarps, w = sel - c * kConsumerWarps;
-    const int64_t r0 = static_cast<int64_t>(c) * CH + static_cast<int64_t>(w) * WCH;
-    const int len = static_cast<int>(max(static_cast<int64_t>(0),
-                                         min(static_cast<int64_t>(WCH), a.V - r0)));
-    tok = warp_select_fixed<T, WCH / 32>(rowp, r0, len, ff_to_fixed(rem), ref, alpha, s_tab);
-  }
-  if (lane == 0) {
-    float lse, lse_alpha;
-    if (ok) {
-      lse_alpha = alpha * M + (logf(total.hi) + total.lo / total.hi);
-      lse = alpha != 1.f ? fM + logf(fS) : lse_alpha;
-    } else {
-      lse = lse_alpha = M == kNegInf ? kNegInf : __int_as_float(0x7fc00000);
-      raise_status(a.ws.status, M == kNegInf ? SMC_DEV_EMPTY_ROW : SMC_DEV_NONFINITE);
+  if (n_units <= kThreads) {
+    // one unit per thread: its mass relative to the row's largest reference
+    // M, a CTA-wide inclusive prefix, and the first unit whose prefix exceeds
+    // u times the total
+    const int q = threadIdx.x;
+    const int4 pv = q < n_units ? bp[q] : make_int4(__float_as_int(kNegInf), 0, 0, 0);
+    const float ref = __int_as_float(pv.x);
+    const float M = block_max(ref, s_red);
+    const bool ok = M > kNegInf && M < kInf;
+    ff val{0.f, 0.f}, f{1.f, 0.f};
+    if (ok && ref > kNegInf) {
+      f = ff_norm(weight_term(ref, M, alpha, s_tab));  // exp(alpha (ref - M))
+      val = ff_mul(ff{__int_as_float(pv.y), __int_as_float(pv.z)}, f);
     }
-    a.ws.results[row] = RowResult{lse, 0.f, lse_alpha, tok};
+    ff total;
+    const ff incl = block_ff_scan(val, s_f2, &total);
+    const ff target = ff_mul_f(total, u);
+    const bool pos = val.hi > 0.f;
+    const bool hit = pos && ff_gt(incl, target);
+    const int first = block_min_i(hit ? q : 0x7fffffff, s_i);
+    const int last = -block_min_i(pos ? -q : 1, s_i);  // largest positive unit, or -1
+    const int sel = !ok ? -1 : (first != 0x7fffffff ? first : last);
+    if (q == sel) {
+      // the remaining target in the unit's own units; past the total
+      // (rounding), the unit's whole mass
+      const ff rem = first != 0x7fffffff ? ff_div(ff_sub(target, ff_sub(incl, val)), f)
+                                         : ff_div(val, f);
+      s_target = ff_to_fixed(rem);
+      s_ref = ref;
+    }
+    if (q == 0) {
+      s_sel = sel;
+      float lse, lse_alpha;
+      if (ok) {
+        lse_alpha = alpha * M + (logf(total.hi) + total.lo / total.hi);
+        lse = alpha != 1.f ? fM + logf(fS) : lse_alpha;
+      } else {
+        lse = lse_alpha = M == kNegInf ? kNegInf : __int_as_float(0x7fc00000);
+        raise_status(a.ws.status, M == kNegInf ? SMC_DEV_EMPTY_ROW : SMC_DEV_NONFINITE);
+      }
+      a.ws.results[row] = RowResult{lse, 0.f, lse_alpha, -1};
+    }
+  } else if (warp == 0) {
+    // longer rows: warp 0 computes unit masses on demand
+    float M = kNegInf;
+    for (int q = lane; q < n_units; q += 32) M = fmaxf(M, __int_as_float(bp[q].x));
+    M = warp_max(M);
+    const bool ok = M > kNegInf && M < kInf;
+    auto unit_mass = [&](int q, ff *val, ff *f) {
+      const int4 pv = bp[q];
+      const float ref = __int_as_float(pv.x);
+      if (ok && ref > kNegInf) {
+        *f = ff_norm(weight_term(ref, M, alpha, s_tab));  // exp(alpha (ref - M))
+        *val = ff_mul(ff{__int_as_float(pv.y), __int_as_float(pv.z)}, *f);
+      }
+    };
+    ff total{0.f, 0.f};
+    for (int q0 = 0; q0 < n_units; q0 += 32) {
+      ff val{0.f, 0.f}, f{1.f, 0.f};
+      if (q0 + lane < n_units) unit_mass(q0 + lane, &val, &f);
+      total = ff_add(total, warp_ff_sum(val));
+    }
+    ff rem{0.f, 0.f};
+    const int sel = ok ? warp_find_chunk(n_units, ff_mul_f(total, u), unit_mass, &rem) : -1;
+    if (lane == 0) {
+      s_sel = sel;
+      s_target = ff_to_fixed(rem);
+      s_ref = sel >= 0 ? __int_as_float(bp[sel].x) : 0.f;
+      float lse, lse_alpha;
+      if (ok) {
+        lse_alpha = alpha * M + (logf(total.hi) + total.lo / total.hi);
+        lse = alpha != 1.f ? fM + logf(fS) : lse_alpha;
+      } else {
+        lse = lse_alpha = M == kNegInf ? kNegInf : __int_as_float(0x7fc00000);
+        raise_status(a.ws.status, M == kNegInf ? SMC_DEV_EMPTY_ROW : SMC_DEV_NONFINITE);
+      }
+      a.ws.results[row] = RowResult{lse, 0.f, lse_alpha, -1};
+    }
   }
+  __syncthreads();
+  const int sel = s_sel;
+  if (sel < 0) return;  // uniform across the CTA
+  const int c = sel / kConsumerWarps, w = sel - c * kConsumerWarps;
+  const int64_t r0 = static_cast<int64_t>(c) * CH + static_cast<int64_t>(w) * WCH;
+  const int len = static_cast<int>(max(static_cast<int64_t>(0),
+                                       min(static_cast<int64_t>(WCH), a.V - r0)));
+  const int tok = block_select_fixed<T, WCH / kThreads>(rowp, r0, len, s_target, s_ref, alpha,
+                                                         s_tab, s_ll, s_i);
+  if (threadIdx.x == 0) a.ws.results[row].tok = tok;
 }
 
 // ---------------------------------------------------------------------------
@@ -1214,11 +1393,14 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa) {
 // waits here until the row kernel has finished and its results are visible.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1) tail_kernel(const StepArgs a, int kv_staged) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ TailSmem sm;
   extern __shared__ int dyn_i[];
-  if (a.mode == 0) smc_tail(a, blockIdx.x, sm, dyn_i, kv_staged != 0);
-  else sps_tail(a, blockIdx.x, sm);
+  if (a.mode == 0) {
+    smc_tail(a, blockIdx.x, sm, dyn_i, kv_staged != 0);  // waits inside
+  } else {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    sps_tail(a, blockIdx.x, sm);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1298,6 +1480,13 @@ static cudaError_t stream_geometry(int *sms, int *per_sm) {
   return cudaSuccess;
 }
 
+static cudaEvent_t g_rows_begin = nullptr, g_rows_end = nullptr;
+
+void set_row_timing_events(cudaEvent_t begin, cudaEvent_t end) {
+  g_rows_begin = begin;
+  g_rows_end = end;
+}
+
 template <typename T>
 static cudaError_t launch_stream(const StepArgs &a, long long rows, cudaStream_t stream) {
   int sms = 0, per_sm = 0;
@@ -1310,20 +1499,27 @@ static cudaError_t launch_stream(const StepArgs &a, long long rows, cudaStream_t
                              StreamGeom<T>::kCH);
   sa.wspan = 40.f / a.alpha;
   const long long total_chunks = rows * sa.snch;
-  // about six work items per resident CTA, each 1..8 chunks
-  const long long g = total_chunks / (grid_max * 6);
-  sa.G = static_cast<int>(g < 1 ? 1 : (g > 8 ? 8 : g));
-  sa.ipr = (sa.snch + sa.G - 1) / sa.G;
+  // about twelve work items per resident CTA, each 1..8 chunks, split evenly
+  // over a row (short items keep the CTAs' finishing times close together)
+  const long long g = total_chunks / (grid_max * 12);
+  const int g0 = static_cast<int>(g < 1 ? 1 : (g > 8 ? 8 : g));
+  sa.ipr = (sa.snch + g0 - 1) / g0;
+  sa.G = (sa.snch + sa.ipr - 1) / sa.ipr;
   const long long parts = rows / (2 * a.K + 1);
   sa.n_fast_items = static_cast<int>(parts * 2 * a.K * sa.ipr);
   sa.n_bonus_items = static_cast<int>(parts * sa.snch);
   const long long n_items = static_cast<long long>(sa.n_fast_items) + sa.n_bonus_items;
   const long long grid = grid_max < n_items ? grid_max : n_items;
+  if (g_rows_begin && (e = cudaEventRecord(g_rows_begin, stream)) != cudaSuccess) return e;
   row_stream_kernel<T><<<static_cast<unsigned>(grid), kStreamThreads, stream_dyn_smem(), stream>>>(sa);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (g_rows_end && (e = cudaEventRecord(g_rows_end, stream)) != cudaSuccess) return e;
+  // log-sum-exp rows: one warp each; bonus rows: one CTA each
+  const long long fast_rows = parts * 2 * a.K;
+  const int n_fast_ctas = static_cast<int>((fast_rows + kWarps - 1) / kWarps);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((rows + kWarps - 1) / kWarps));
+  cfg.gridDim = dim3(static_cast<unsigned>(n_fast_ctas + parts));
   cfg.blockDim = dim3(kThreads);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -1331,7 +1527,7 @@ static cudaError_t launch_stream(const StepArgs &a, long long rows, cudaStream_t
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, finish_kernel<T>, sa);
+  return cudaLaunchKernelEx(&cfg, finish_kernel<T>, sa, n_fast_ctas);
 }
 
 // The per-prompt tail, launched with programmatic dependent launch so that it
@@ -1395,9 +1591,11 @@ cudaError_t launch_step_rows(const Shape &s, int mode, const void *target, const
   } else {
     const long long grid = rows * a.nch;
     dim3 g(static_cast<unsigned>(grid)), blk(kThreads);
+    if (g_rows_begin && (e = cudaEventRecord(g_rows_begin, stream)) != cudaSuccess) return e;
     if (s.dtype == SMC_BF16) step_rows_kernel<bf16_tag, false><<<g, blk, 0, stream>>>(a);
     else step_rows_kernel<float, false><<<g, blk, 0, stream>>>(a);
     e = cudaGetLastError();
+    if (e == cudaSuccess && g_rows_end) e = cudaEventRecord(g_rows_end, stream);
   }
   if (e != cudaSuccess) return e;
   e = launch_tail(a, stream);

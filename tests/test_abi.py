@@ -114,6 +114,10 @@ def test_host_validation_without_gpu(lib):
     assert lib.kv_blocktable_remap(ctypes.byref(good), ctypes.byref(kv), fake, fake, -1, ws,
                                    1 << 30, None) == -1
     assert lib.smc_device_status(None, 0, None, None) == -1
+    # the row-timing hook takes both events or neither
+    assert lib.smc_set_row_timing_events(fake, None) == -1
+    assert lib.smc_set_row_timing_events(None, fake) == -1
+    assert lib.smc_set_row_timing_events(None, None) == 0
 
 
 def test_oracle_and_cuda_path_share_no_code():

@@ -248,6 +248,80 @@ def test_kv_blocktable_remap_bit_exact(prefix, bs, N, T_min):
 
 
 # ---------------------------------------------------------------------------
+# bonus rows with extreme value ranges
+# ---------------------------------------------------------------------------
+def _bonus_check(w, inp, seed=5):
+    """One step (no resampling) and the bonus tokens against the oracle."""
+    r = StepRunner(w, seed=seed, with_kv=False, ess_frac=0.0)
+    r.run(inp, 0)
+    torch.cuda.synchronize()
+    assert r.status() == 0
+    x = inp["draft_tokens"].cpu().numpy().astype(np.int64)
+    ref = osmc.smc_step(to_numpy_logits(inp["target"]), to_numpy_logits(inp["draft"]), x,
+                        np.zeros((w.B, w.N)), alpha=w.alpha, ess_frac=0.0, seed=seed, step=0,
+                        dtype=w.dtype)
+    g = r.tokens_out.cpu().numpy().reshape(w.B, w.N, w.K + 1)[:, :, w.K]
+    flagged = ref["bonus_margin"] < 1e-5
+    bad = (g != ref["bonus"]) & ~flagged
+    assert not bad.any(), (np.argwhere(bad)[:4], g[bad][:4], ref["bonus"][bad][:4])
+    lw = r.log_weights.cpu().numpy().reshape(w.B, w.N)
+    assert np.abs(lw - ref["log_weights_pre"]).max() <= (2e-3 if w.dtype == "bf16" else 1e-4)
+    return g, ref
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("log2_big", [30, 32])
+def test_bonus_row_with_huge_max(dtype, log2_big):
+    """Bonus rows with two equal maxima of 2^30 or 2^32 in different units,
+    everything else O(1): the token is the first maximum iff u < 1/2.  At
+    2^32, max - 40 rounds to max, so the streaming kernel flags those units
+    and the combine sums them exactly instead."""
+    w = WORKLOADS["single_prompt_v32000"].with_(B=2, N=4, K=2, V=40000, dtype=dtype)
+    inp = make_step_inputs(w, 21, device="cuda")
+    big = 2.0 ** log2_big
+    below = 2.0 ** (log2_big - (8 if dtype == "bf16" else 24))  # one step below big
+    t = inp["target"]
+    t[:, :, w.K, 3000] = big
+    t[:, :, w.K, 35000] = big
+    t[0, 1, w.K, 17] = big - below
+    g, ref = _bonus_check(w, inp)
+    assert set(np.unique(g)) <= {3000, 35000}
+
+
+def test_bonus_row_of_tiny_logits_under_a_large_max():
+    """bf16 logits 2^-20 in size against a max of 12: x - max is not a float
+    there, and the weights must still sum to the oracle's within tolerance."""
+    w = WORKLOADS["single_prompt_v32000"].with_(B=2, N=8, K=2, V=32000)
+    inp = make_step_inputs(w, 22, device="cuda")
+    t = inp["target"]
+    tiny = (torch.randn(t[:, :, w.K].shape, device="cuda") * 2.0 ** -20).to(t.dtype)
+    t[:, :, w.K] = tiny
+    t[:, :, w.K, 777] = 2.5
+    _bonus_check(w, inp)
+
+
+def test_row_timing_hook_records_the_row_pass_and_changes_nothing():
+    w = WORKLOADS["single_prompt_v32000"].with_(B=2)
+    inp = make_step_inputs(w, 3, device="cuda")
+    plain = StepRunner(w, seed=3, with_kv=True, steps=2)
+    plain.run(inp, 0)
+    hooked = StepRunner(w, seed=3, with_kv=True, steps=2)
+    b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    smcsd.smc_set_row_timing_events(b, e)
+    try:
+        hooked.run(inp, 0)
+    finally:
+        smcsd.smc_set_row_timing_events(None, None)
+    torch.cuda.synchronize()
+    assert b.elapsed_time(e) > 0.0
+    assert plain.status() == 0 and hooked.status() == 0
+    for name in ("log_weights", "tokens_out", "ancestors", "ess", "resampled"):
+        assert torch.equal(getattr(plain, name), getattr(hooked, name)), name
+    for key in plain.kv:
+        assert torch.equal(plain.kv[key], hooked.kv[key]), key
+
+
+# ---------------------------------------------------------------------------
 # errors: reported through the status word, never a trap
 # ---------------------------------------------------------------------------
 def _tiny_run(mutate, with_kv=False, kv_mut=None):
