@@ -138,3 +138,26 @@ def live_references(tables, seq_len, block_size):
                 blk = int(tables[b][i][t])
                 counts[blk] = counts.get(blk, 0) + 1
     return counts
+
+
+def usage(tables, seq_len, block_size):
+    """Blocks held with sharing against blocks N unshared copies would hold.
+
+    Per prompt b: used[b] = number of distinct blocks its particles' tables
+    reference; unshared[b] = sum over particles of the blocks each particle's
+    tokens fill on their own.  The SMC page (section 2, "系统优化设计") credits
+    prefix sharing and pointer exchange with a smaller KV cache; 1 -
+    used/unshared is that saving for one state.
+    """
+    big_b, n_part, _ = np.shape(tables)
+    used = np.zeros(big_b, dtype=np.int64)
+    unshared = np.zeros(big_b, dtype=np.int64)
+    for b in range(big_b):
+        seen = set()
+        for i in range(n_part):
+            nb = n_blocks(seq_len[b][i], block_size)
+            unshared[b] += nb
+            for t in range(nb):
+                seen.add(int(tables[b][i][t]))
+        used[b] = len(seen)
+    return used, unshared

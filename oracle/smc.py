@@ -192,13 +192,42 @@ def score_particle(target_rows, draft_rows, tokens, alpha):
                 lse_alpha=lse_alpha, delta=delta)
 
 
+def temperature_scale(temperature):
+    """The multiplier 1/T that a temperature T applies to every logit.
+
+    The pages fix no precision for it; it is taken as the fp32 rounding of
+    1/T computed from the fp32 value of T, the value a caller passing T as a
+    float arrives at, and is then applied exactly (in fp64) to the logits.
+    """
+    t32 = np.float32(temperature)
+    if not (np.isfinite(t32) and t32 > 0):
+        raise ValueError("temperature must be positive and finite")
+    return float(np.float32(np.float32(1.0) / t32))
+
+
+def effective_alpha(alpha, temperature=1.0):
+    """The exponent of the bonus distribution softmax(alpha * l / T), taken
+    as the fp32 product of alpha and the temperature's multiplier."""
+    return float(np.float32(np.float32(alpha) * np.float32(temperature_scale(temperature))))
+
+
 def smc_step(target, draft, draft_tokens, log_weights, *, alpha=1.0,
-             ess_frac=0.5, seed=0, step=0, dtype=None):
+             ess_frac=0.5, seed=0, step=0, dtype=None, temperature=1.0,
+             log_potential=None):
     """One SMC-SD step over B prompts x N particles (no KV state).
 
     target: [B, N, K+1, V], draft: [B, N, K, V], either already fp64 or, when
     ``dtype`` is given, stored logits that are widened one particle at a time
     (see ``widen``); draft_tokens: [B, N, K] ints, log_weights: [B, N].
+
+    temperature T: p and q are softmax(l / T) before they are scored or
+    sampled; the drafted tokens are taken to come from the tempered draft.
+    log_potential: optional [B, N] per-particle log-potential increment of
+    this step (for example a log reward ratio, or -inf for a particle that
+    breaks a constraint), added to the weight increment.  Both settings are
+    extensions the pages name without fixing (the SMC page's section 3 on
+    unnormalised targets such as rewards and constraints; the SpS notes'
+    evaluation at nucleus and temperature settings).
 
     Returns a dict with
       delta[B,N], log_weights_pre[B,N] (after reweighting), log_weights[B,N]
@@ -208,6 +237,8 @@ def smc_step(target, draft, draft_tokens, log_weights, *, alpha=1.0,
       statistics lse_p, g_p, lse_q, g_q, lse_alpha.
     """
     alpha = float(np.float32(alpha))
+    scale = temperature_scale(temperature)
+    bonus_alpha = effective_alpha(alpha, temperature)
     big_b, n_part, k1, v_size = target.shape
     k_drafts = k1 - 1
     draft_tokens = np.asarray(draft_tokens, dtype=np.int64)
@@ -221,13 +252,19 @@ def smc_step(target, draft, draft_tokens, log_weights, *, alpha=1.0,
         for n in range(n_part):
             t_rows = widen(target[b, n], dtype) if dtype else target[b, n]
             d_rows = widen(draft[b, n], dtype) if dtype else draft[b, n]
+            if scale != 1.0:
+                t_rows = np.asarray(t_rows, dtype=np.float64) * scale
+                d_rows = np.asarray(d_rows, dtype=np.float64) * scale
             s = score_particle(t_rows, d_rows, draft_tokens[b, n], alpha)
             for key in ("lse_p", "g_p", "lse_q", "g_q", "lse_alpha", "delta"):
                 out[key][b, n] = s[key]
             u = philox.uniform(seed, step, b * n_part + n, k_drafts, philox.BONUS)
-            tok, margin = inverse_cdf(bonus_weights(t_rows[k_drafts], alpha), u)
+            raw = widen(target[b, n, k_drafts], dtype) if dtype else target[b, n, k_drafts]
+            tok, margin = inverse_cdf(bonus_weights(raw, bonus_alpha), u)
             out["bonus"][b, n] = tok
             out["bonus_margin"][b, n] = margin
+    if log_potential is not None:
+        out["delta"] = out["delta"] + np.asarray(log_potential, dtype=np.float64)
     lw_pre = np.asarray(log_weights, dtype=np.float64) + out["delta"]
     out["log_weights_pre"] = lw_pre
     out["log_weights"] = np.zeros((big_b, n_part))
@@ -249,3 +286,28 @@ def smc_step(target, draft, draft_tokens, log_weights, *, alpha=1.0,
         out["tokens_out"][b, :, :k_drafts] = draft_tokens[b, a]
         out["tokens_out"][b, :, k_drafts] = out["bonus"][b, a]
     return out
+
+
+# --------------------------------------------------------------------------
+# the extend-side draft sampler
+# --------------------------------------------------------------------------
+def draft_sample(draft, position, *, alpha=1.0, seed=0, step=0, dtype=None):
+    """One drafted token per particle: x ~ softmax(alpha * l) of draft row
+    [B, N, V], by inverse CDF in vocabulary order with the uniform of
+    (seed, step, particle b*N+n, position, DRAFT).
+
+    The SMC page's Extend stage has the draft model extend every particle by
+    K tokens; this is the sampling half of one of those K positions.  alpha
+    is the inverse temperature of the draft (1: sample q itself).
+    Returns (tokens[B, N], margins[B, N]).
+    """
+    alpha = float(np.float32(alpha))
+    big_b, n_part, v_size = draft.shape
+    toks = np.zeros((big_b, n_part), dtype=np.int64)
+    margins = np.zeros((big_b, n_part))
+    for b in range(big_b):
+        for n in range(n_part):
+            row = widen(draft[b, n], dtype) if dtype else np.asarray(draft[b, n], np.float64)
+            u = philox.uniform(seed, step, b * n_part + n, position, philox.DRAFT)
+            toks[b, n], margins[b, n] = inverse_cdf(bonus_weights(row, alpha), u)
+    return toks, margins

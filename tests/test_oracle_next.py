@@ -1,0 +1,193 @@
+"""Pins of the oracle's extensions beyond the basic step (CPU): temperature,
+per-particle log-potentials, the draft-side sampler and KV-usage accounting."""
+import numpy as np
+import pytest
+from scipy.special import logsumexp, softmax
+from scipy.stats import chisquare
+
+from oracle import smc, kv
+from oracle.errors import OracleError, DEV_ALL_ZERO_WEIGHT
+
+
+def _inputs(rng, big_b=2, n=8, k=3, v=32, sigma=2.0, noise=1.0):
+    target = rng.normal(0, sigma, (big_b, n, k + 1, v))
+    draft = target[:, :, :k] + rng.normal(0, noise, (big_b, n, k, v))
+    toks = rng.integers(0, v, (big_b, n, k))
+    return target, draft, toks
+
+
+# ---------------------------------------------------------------------------
+# temperature
+# ---------------------------------------------------------------------------
+def test_temperature_divides_the_logits():
+    """Logits scaled by 4 at temperature 4 are the logits themselves at
+    temperature 1 (1/4 is exact in fp32): every output is identical.  Catches
+    a temperature that multiplies instead of dividing."""
+    rng = np.random.default_rng(3)
+    target, draft, toks = _inputs(rng)
+    lw = rng.normal(0, 1, (2, 8))
+    plain = smc.smc_step(target, draft, toks, lw, ess_frac=0.9, seed=5, step=2)
+    hot = smc.smc_step(4.0 * target, 4.0 * draft, toks, lw, ess_frac=0.9, seed=5, step=2,
+                       temperature=4.0)
+    for key in ("delta", "ess", "ancestors", "bonus", "tokens_out", "log_weights"):
+        assert np.array_equal(plain[key], hot[key]), key
+
+
+@pytest.mark.parametrize("temperature", [0.5, 2.0])
+def test_tempered_weight_increment_closed_form(temperature):
+    """delta = sum_k log p_T(x_k) - log q_T(x_k) with p_T = softmax(l / T),
+    from scipy's log-softmax of the scaled rows."""
+    rng = np.random.default_rng(11)
+    target, draft, toks = _inputs(rng, big_b=1, n=4)
+    out = smc.smc_step(target, draft, toks, np.zeros((1, 4)), temperature=temperature)
+    s = smc.temperature_scale(temperature)
+    for n in range(4):
+        lp = target[0, n, :3] * s - logsumexp(target[0, n, :3] * s, axis=1, keepdims=True)
+        lq = draft[0, n] * s - logsumexp(draft[0, n] * s, axis=1, keepdims=True)
+        expect = sum(lp[k, toks[0, n, k]] - lq[k, toks[0, n, k]] for k in range(3))
+        assert abs(out["delta"][0, n] - expect) < 1e-12
+
+
+def test_draft_equal_target_stays_unweighted_at_any_temperature():
+    rng = np.random.default_rng(2)
+    target, _, toks = _inputs(rng)
+    out = smc.smc_step(target, target[:, :, :3].copy(), toks, np.zeros((2, 8)), temperature=0.3)
+    assert np.array_equal(out["delta"], np.zeros((2, 8)))
+    assert not out["resampled"].any()
+
+
+def test_temperature_must_be_positive():
+    rng = np.random.default_rng(2)
+    target, draft, toks = _inputs(rng)
+    for bad in (0.0, -1.0, float("inf"), float("nan")):
+        with pytest.raises(ValueError):
+            smc.smc_step(target, draft, toks, np.zeros((2, 8)), temperature=bad)
+
+
+# ---------------------------------------------------------------------------
+# log-potentials
+# ---------------------------------------------------------------------------
+def test_constant_potential_changes_no_normalised_quantity():
+    rng = np.random.default_rng(4)
+    target, draft, toks = _inputs(rng)
+    lw = rng.normal(0, 1, (2, 8))
+    a = smc.smc_step(target, draft, toks, lw, ess_frac=0.9, seed=1, step=3)
+    b = smc.smc_step(target, draft, toks, lw, ess_frac=0.9, seed=1, step=3,
+                     log_potential=np.full((2, 8), -7.5))
+    assert np.allclose(a["ess"], b["ess"], rtol=1e-12, atol=0)
+    assert np.array_equal(a["ancestors"], b["ancestors"])
+    assert np.allclose(b["log_weights_pre"] - a["log_weights_pre"], -7.5, atol=1e-12)
+
+
+def test_potential_alone_sets_the_weights_closed_form():
+    """With draft == target the increment is the potential alone, so
+    ESS = (sum e^phi)^2 / sum e^(2 phi)."""
+    rng = np.random.default_rng(5)
+    target, _, toks = _inputs(rng)
+    phi = rng.normal(0, 1.5, (2, 8))
+    out = smc.smc_step(target, target[:, :, :3].copy(), toks, np.zeros((2, 8)),
+                       log_potential=phi, ess_frac=0.0)
+    w = np.exp(phi)
+    assert np.allclose(out["ess"], w.sum(1) ** 2 / (w ** 2).sum(1), rtol=1e-12, atol=0)
+
+
+def test_minus_infinity_potential_removes_a_particle():
+    """A particle with potential -inf (a violated constraint) weighs 0: it is
+    never an ancestor when the prompt resamples."""
+    rng = np.random.default_rng(6)
+    target, draft, toks = _inputs(rng)
+    phi = np.zeros((2, 8))
+    phi[:, 0] = -np.inf
+    phi[1, 5] = -np.inf
+    for step in range(20):
+        out = smc.smc_step(target, draft, toks, np.zeros((2, 8)), log_potential=phi,
+                           ess_frac=1.01, seed=9, step=step)
+        assert out["resampled"].all()
+        assert not (out["ancestors"][0] == 0).any()
+        assert not np.isin(out["ancestors"][1], [0, 5]).any()
+
+
+def test_all_minus_infinity_potentials_are_an_error():
+    rng = np.random.default_rng(7)
+    target, draft, toks = _inputs(rng)
+    with pytest.raises(OracleError) as e:
+        smc.smc_step(target, draft, toks, np.zeros((2, 8)), log_potential=np.full((2, 8), -np.inf))
+    assert e.value.kind == DEV_ALL_ZERO_WEIGHT
+
+
+# ---------------------------------------------------------------------------
+# draft-side sampler
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("alpha", [1.0, 0.5])
+def test_draft_sample_follows_the_tempered_softmax(alpha):
+    """Over 40000 (seed, step) draws, token counts of one row match
+    softmax(alpha * l) by a chi-square test."""
+    rng = np.random.default_rng(8)
+    v = 12
+    row = rng.normal(0, 1.5, v)
+    logits = np.broadcast_to(row, (1, 1, v))
+    counts = np.zeros(v)
+    for seed in range(200):
+        for step in range(200):
+            t, _ = smc.draft_sample(logits, position=2, alpha=alpha, seed=seed, step=step)
+            counts[t[0, 0]] += 1
+    p = softmax(alpha * row)
+    assert chisquare(counts, p * counts.sum()).pvalue > 1e-4
+
+
+def test_draft_sample_positions_draw_independently_and_masks_hold():
+    """-inf logits are never drawn; different positions use different
+    uniforms (so whole-row samples differ across positions)."""
+    rng = np.random.default_rng(9)
+    draft = rng.normal(0, 1.0, (3, 5, 40))
+    draft[:, :, ::3] = -np.inf
+    toks = np.stack([smc.draft_sample(draft, position=k, seed=4, step=1)[0] for k in range(4)])
+    assert (toks % 3 != 0).all()
+    assert not all(np.array_equal(toks[0], toks[k]) for k in range(1, 4))
+
+
+# ---------------------------------------------------------------------------
+# KV usage
+# ---------------------------------------------------------------------------
+def _state(big_b, n, prefix, bs, t_len, pool):
+    tables = np.full((big_b, n, t_len), -1, dtype=np.int64)
+    refcount = np.zeros(big_b * pool, dtype=np.int64)
+    free_list = np.zeros((big_b, pool), dtype=np.int64)
+    free_top = np.zeros(big_b, dtype=np.int64)
+    nb = -(-prefix // bs)
+    for b in range(big_b):
+        tables[b, :, :nb] = np.arange(b * pool, b * pool + nb)
+        refcount[b * pool: b * pool + nb] = n
+        free = np.arange(b * pool + pool - 1, b * pool + nb - 1, -1)
+        free_list[b, :len(free)] = free
+        free_top[b] = len(free)
+    seq_len = np.full((big_b, n), prefix, dtype=np.int64)
+    return tables, seq_len, refcount, free_list, free_top
+
+
+def test_usage_of_a_shared_prefix():
+    tables, seq_len, *_ = _state(2, 8, 40, 16, 10, 81)
+    used, unshared = kv.usage(tables, seq_len, 16)
+    assert list(used) == [3, 3] and list(unshared) == [24, 24]
+
+
+def test_usage_counts_the_blocks_with_live_references():
+    """After remaps with resampling and appends, used blocks are exactly the
+    pool blocks whose reference count is positive."""
+    rng = np.random.default_rng(10)
+    big_b, n, bs, t_len = 2, 6, 4, 12
+    pool = n * t_len + 1
+    tables, seq_len, refcount, free_list, free_top = _state(big_b, n, 6, bs, t_len, pool)
+    for step in range(5):
+        anc = rng.integers(0, n, (big_b, n))
+        res = rng.random(big_b) < 0.7
+        out = kv.remap_append(tables, seq_len, refcount, free_list, free_top, anc, res, 3, bs,
+                              pool)
+        assert all(not e for e in out["errors"])
+        tables, seq_len, refcount = out["tables"], out["seq_len"], out["refcount"]
+        free_list, free_top = out["free_list"], out["free_top"]
+        used, unshared = kv.usage(tables, seq_len, bs)
+        for b in range(big_b):
+            assert used[b] == int((np.asarray(refcount[b * pool:(b + 1) * pool]) > 0).sum())
+            assert unshared[b] == sum(-(-int(seq_len[b][i]) // bs) for i in range(n))
+            assert used[b] <= unshared[b]
