@@ -58,6 +58,8 @@ def parse_args():
                     help="CPU work budget of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the secondary measurements of the step's extensions")
     return ap.parse_args()
 
 
@@ -335,7 +337,72 @@ def run_ours(args, world, rank, local):
     }
     if not args.no_e2e:
         out["e2e"] = run_e2e(args, w, dev, smcsd, world)
+    if not args.no_extras:
+        out["extensions"] = run_extensions(w, dev, smcsd, ring)
     return out
+
+
+def run_extensions(w, dev, smcsd, ring, reps=50):
+    """Secondary measurements, not part of the step's line: the draft-side
+    sampler on one position of every particle (B*N rows of V), and smc_step_ex
+    at temperature 0.8 with log-potentials (the same step as the headline,
+    with the extensions on)."""
+    import torch
+    res = {}
+    params = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, 1.0, w.ess_frac, 0, 0)
+    ws = smcsd.alloc_workspace(params)
+    rows = ring[0]["draft"][:, :, 0].contiguous()
+    tok = torch.empty(w.B * w.N, dtype=torch.int32, device=dev)
+    for _ in range(5):
+        smcsd.smc_draft_sample(params, rows, 0, tok, ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 256 MB > L2
+    ms = []
+    for r in range(reps):
+        flush.zero_()
+        e0.record()
+        smcsd.smc_draft_sample(params, rows, r % w.K, tok, ws)
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    bytes_call = w.B * w.N * w.V * w.bytes_per_logit
+    med = float(np.median(ms))
+    res["draft_sample"] = {"rows": w.B * w.N, "V": w.V, "ms_per_call": med,
+                           "tokens_per_s": w.B * w.N / (med / 1e3),
+                           "achieved_gbs": bytes_call / (med / 1e3) / 1e9,
+                           "frac_of_hbm_peak": bytes_call / (med / 1e3) / 1e9 / measured_peak()[0],
+                           "l2": "256 MB buffer written between calls"}
+    T, P = w.kv_dims(64)
+    from smc_speculative_decoding_gb300.workloads import make_kv_state
+    kv = make_kv_state(w.B, w.N, w.prefix, w.block_size, T, P, device=dev)
+    kv_s = smcsd.make_kv(params, kv, w.block_size)
+    ws2 = smcsd.alloc_workspace(params, kv_s)
+    lw = torch.zeros(w.B * w.N, device=dev)
+    outs = dict(tok=torch.empty(w.B * w.N * (w.K + 1), dtype=torch.int32, device=dev),
+                anc=torch.empty(w.B * w.N, dtype=torch.int32, device=dev),
+                ess=torch.empty(w.B, device=dev), res=torch.empty(w.B, dtype=torch.int32, device=dev))
+    phi = torch.zeros(w.B * w.N, device=dev)
+    n = 48
+    for s in range(3):
+        p = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, s)
+        smcsd.smc_step_ex(p, ring[s % 2]["target"], ring[s % 2]["draft"], ring[s % 2]["draft_tokens"],
+                          lw, outs["tok"], outs["anc"], outs["ess"], outs["res"], kv=kv_s,
+                          workspace=ws2, temperature=0.8, log_potential=phi)
+    torch.cuda.synchronize()
+    e0.record()
+    for s in range(n):
+        p = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, 3 + s)
+        smcsd.smc_step_ex(p, ring[s % 2]["target"], ring[s % 2]["draft"], ring[s % 2]["draft_tokens"],
+                          lw, outs["tok"], outs["anc"], outs["ess"], outs["res"], kv=kv_s,
+                          workspace=ws2, temperature=0.8, log_potential=phi)
+    e1.record()
+    torch.cuda.synchronize()
+    assert smcsd.smc_device_status(ws2, clear=True) == 0
+    ms_step = e0.elapsed_time(e1) / n
+    res["step_ex_temperature_potential"] = {"ms_per_step": ms_step,
+                                            "particle_tokens_per_s": w.particle_tokens / (ms_step / 1e3),
+                                            "temperature": 0.8, "steps": n}
+    return res
 
 
 def run_e2e(args, w, dev, smcsd, world):

@@ -85,6 +85,7 @@ extern "C" {
 #define SMC_MAX_V  (1 << 24)  /* vocabulary size                                */
 
 /* ---- Philox purposes (4th counter word) -------------------------------- */
+#define SMC_PURPOSE_DRAFT     0  /* stream b*N+n, position k (smc_draft_sample)  */
 #define SMC_PURPOSE_BONUS     1  /* stream b*N+n, position K                     */
 #define SMC_PURPOSE_ACCEPT    2  /* stream b, position k (sps_verify)            */
 #define SMC_PURPOSE_RESIDUAL  3  /* stream b, position j (sps_verify)            */
@@ -183,6 +184,57 @@ int32_t smc_step(const smc_params *p, const void *target_logits,
                  float *log_weights, int32_t *tokens_out, int32_t *ancestors,
                  float *ess, int32_t *resampled, const smc_kv *kv,
                  void *workspace, size_t ws_bytes, void *stream);
+
+/* Per-call settings of smc_step_ex. */
+typedef struct {
+  const float *log_potential;  /* DEVICE [B, N] fp32, or NULL: a per-particle
+                                  log-potential increment added to delta (a log
+                                  reward ratio, or -inf for a particle that
+                                  breaks a constraint); NaN or +inf sets
+                                  SMC_DEV_NONFINITE                             */
+  float temperature;           /* T > 0, finite (1 = none): p and q are
+                                  softmax(l / T) wherever they are scored or
+                                  sampled; every logit is multiplied by the
+                                  fp32 value of 1/T                             */
+  int32_t reserved;            /* must be 0                                     */
+} smc_step_opts;
+
+/* smc_step with per-call settings ([SMC] section 3, "通用性扩展": the target
+ * may be reweighted by rewards or constraints; [SpS] section 6: decoding at
+ * temperature and nucleus settings).  opts may be NULL (= smc_step).  With
+ * temperature T and multiplier s = fl32(1/T): every lse and gathered logit
+ * is taken of s*l, the bonus is drawn from softmax(fl32(alpha*s) * l_K), and
+ * the drafted tokens are taken to come from the tempered draft.  With a
+ * log-potential phi: delta += phi[b, n] before normalisation.  Everything
+ * else, and every argument, is as for smc_step. */
+int32_t smc_step_ex(const smc_params *p, const smc_step_opts *opts,
+                    const void *target_logits, const void *draft_logits,
+                    const int32_t *draft_tokens, float *log_weights, int32_t *tokens_out,
+                    int32_t *ancestors, float *ess, int32_t *resampled, const smc_kv *kv,
+                    void *workspace, size_t ws_bytes, void *stream);
+
+/* The sampling half of one drafted position of the Extend stage ([SMC]
+ * section 2: the draft model extends every particle by K tokens, one
+ * position at a time).  draft_logits [B, N, V] (the draft's next-token
+ * logits of every particle); tokens_out [B, N] int32: x ~ softmax(alpha * l)
+ * by inverse CDF in vocabulary order with u(step, b*N+n, position, DRAFT).
+ * p->alpha is the draft's inverse temperature (1 = sample q itself); p->K and
+ * p->ess_frac are not used; `position` is the drafted position 0..K-1.  The
+ * workspace is one sized by smc_workspace_bytes(p, NULL) for the same B, N,
+ * V and dtype.  A row that is -inf everywhere gives token -1 and
+ * SMC_DEV_EMPTY_ROW; NaN or +inf gives SMC_DEV_NONFINITE. */
+int32_t smc_draft_sample(const smc_params *p, const void *draft_logits, int32_t position,
+                         int32_t *tokens_out, void *workspace, size_t ws_bytes,
+                         void *stream);
+
+/* KV-cache accounting ([SMC] section 2, "系统优化设计": prefix sharing and
+ * pointer exchange shrink the KV cache).  For each prompt b: used_blocks[b] =
+ * blocks of its pool with a positive reference count; unshared_blocks[b] =
+ * sum over its particles of ceil(seq_len / block_size), the blocks N
+ * unshared copies would hold.  1 - used/unshared is the saving.  Both outputs
+ * are device int32 [B]; p supplies B and N.  Reads the state only. */
+int32_t smc_kv_usage(const smc_params *p, const smc_kv *kv, int32_t *used_blocks,
+                     int32_t *unshared_blocks, void *stream);
 
 /* Normalise, ESS and systematic resampling alone ([SMC] section 2, Resample),
  * for callers that computed the weights themselves.  log_weights [B, N] fp32

@@ -46,6 +46,11 @@ class smc_kv(ctypes.Structure):
                 ("block_size", ctypes.c_int32), ("P", ctypes.c_int32)]
 
 
+class smc_step_opts(ctypes.Structure):
+    _fields_ = [("log_potential", ctypes.c_void_p), ("temperature", ctypes.c_float),
+                ("reserved", ctypes.c_int32)]
+
+
 _lib = None
 
 _SIGS = {
@@ -65,6 +70,14 @@ _SIGS = {
     "sps_verify": (ctypes.c_int32, [ctypes.POINTER(smc_params)] + [ctypes.c_void_p] * 5 +
                    [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "smc_set_row_timing_events": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_void_p]),
+    "smc_step_ex": (ctypes.c_int32, [ctypes.POINTER(smc_params), ctypes.POINTER(smc_step_opts)] +
+                    [ctypes.c_void_p] * 8 +
+                    [ctypes.POINTER(smc_kv), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "smc_draft_sample": (ctypes.c_int32, [ctypes.POINTER(smc_params), ctypes.c_void_p,
+                                          ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_size_t, ctypes.c_void_p]),
+    "smc_kv_usage": (ctypes.c_int32, [ctypes.POINTER(smc_params), ctypes.POINTER(smc_kv),
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
 }
 
 
@@ -212,6 +225,49 @@ def smc_step(params, target_logits, draft_logits, draft_tokens, log_weights, tok
     _check("smc_step", lib().smc_step(
         ctypes.byref(params), *args, ctypes.byref(kv) if kv is not None else None,
         _ptr(workspace, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def smc_step_ex(params, target_logits, draft_logits, draft_tokens, log_weights, tokens_out,
+                ancestors, ess, resampled, kv=None, workspace=None, stream=None,
+                temperature=1.0, log_potential=None):
+    """smc_step with a temperature and an optional [B, N] fp32 CUDA tensor of
+    per-particle log-potential increments (smc_step_ex in smcsd.h)."""
+    B, N, K, V = params.B, params.N, params.K, params.V
+    ld = _logit_dtype(params)
+    opts = smc_step_opts(
+        _ptr(log_potential, "log_potential", torch.float32, B * N) if log_potential is not None
+        else None, float(temperature), 0)
+    args = [
+        _ptr(target_logits, "target_logits", ld, B * N * (K + 1) * V),
+        _ptr(draft_logits, "draft_logits", ld, B * N * K * V),
+        _ptr(draft_tokens, "draft_tokens", torch.int32, B * N * K),
+        _ptr(log_weights, "log_weights", torch.float32, B * N),
+        _ptr(tokens_out, "tokens_out", torch.int32, B * N * (K + 1)),
+        _ptr(ancestors, "ancestors", torch.int32, B * N),
+        _ptr(ess, "ess", torch.float32, B),
+        _ptr(resampled, "resampled", torch.int32, B),
+    ]
+    _check("smc_step_ex", lib().smc_step_ex(
+        ctypes.byref(params), ctypes.byref(opts), *args,
+        ctypes.byref(kv) if kv is not None else None,
+        _ptr(workspace, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def smc_draft_sample(params, draft_logits, position, tokens_out, workspace, stream=None):
+    """One token per particle from softmax(alpha * l) of draft_logits [B, N, V]."""
+    B, N, V = params.B, params.N, params.V
+    _check("smc_draft_sample", lib().smc_draft_sample(
+        ctypes.byref(params), _ptr(draft_logits, "draft_logits", _logit_dtype(params), B * N * V),
+        int(position), _ptr(tokens_out, "tokens_out", torch.int32, B * N),
+        _ptr(workspace, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def smc_kv_usage(params, kv, used_blocks, unshared_blocks, stream=None):
+    """Per prompt: blocks in use with sharing, and blocks unshared copies would hold."""
+    B = params.B
+    _check("smc_kv_usage", lib().smc_kv_usage(
+        ctypes.byref(params), ctypes.byref(kv), _ptr(used_blocks, "used_blocks", torch.int32, B),
+        _ptr(unshared_blocks, "unshared_blocks", torch.int32, B), _stream(stream)))
 
 
 def smc_resample(params, log_weights, ancestors, ess, resampled, workspace, stream=None):

@@ -92,6 +92,8 @@ static Shape to_shape(const smc_params *p) {
   s.dtype = p->dtype;
   s.alpha = p->alpha; s.ess_frac = p->ess_frac;
   s.seed = p->seed; s.step = p->step;
+  s.tscale = 1.f;
+  s.potential = nullptr;
   return s;
 }
 
@@ -176,16 +178,33 @@ int32_t smc_set_row_timing_events(void *rows_begin, void *rows_end) {
   return SMC_OK;
 }
 
-int32_t smc_step(const smc_params *p, const void *target_logits, const void *draft_logits,
-                 const int32_t *draft_tokens, float *log_weights, int32_t *tokens_out,
-                 int32_t *ancestors, float *ess, int32_t *resampled, const smc_kv *kv,
-                 void *workspace, size_t ws_bytes, void *stream) {
+}  // extern "C"
+
+namespace smcsd {
+
+static int32_t step_impl(const smc_params *p, const smc_step_opts *opts,
+                         const void *target_logits, const void *draft_logits,
+                         const int32_t *draft_tokens, float *log_weights, int32_t *tokens_out,
+                         int32_t *ancestors, float *ess, int32_t *resampled, const smc_kv *kv,
+                         void *workspace, size_t ws_bytes, void *stream) {
   if (!p) return SMC_ERR_ARG;
   if (p->dtype != SMC_F32 && p->dtype != SMC_BF16) return SMC_ERR_DTYPE;
   if (!shape_ok(p) || !kv_ok(p, kv)) return SMC_ERR_ARG;
   if (!target_logits || !draft_logits || !draft_tokens || !log_weights || !tokens_out ||
       !ancestors || !ess || !resampled) {
     return SMC_ERR_ARG;
+  }
+  Shape s = to_shape(p);
+  if (opts) {
+    if (opts->reserved != 0) return SMC_ERR_ARG;
+    const float t = opts->temperature;
+    if (!(std::isfinite(t) && t > 0.f)) return SMC_ERR_ARG;
+    s.tscale = 1.f / t;
+    const float balpha = s.alpha * s.tscale;
+    if (!(std::isfinite(s.tscale) && s.tscale > 0.f && std::isfinite(balpha) && balpha > 0.f)) {
+      return SMC_ERR_ARG;
+    }
+    s.potential = opts->log_potential;
   }
   Workspace ws{};
   const int32_t rc = prepare_ws(p, kv, workspace, ws_bytes, &ws);
@@ -198,9 +217,57 @@ int32_t smc_step(const smc_params *p, const void *target_logits, const void *dra
   out.ess = ess;
   KvArgs k{};
   if (kv) k = to_kv(kv);
-  const cudaError_t e = launch_step_rows(to_shape(p), 0, target_logits, draft_logits, draft_tokens,
+  const cudaError_t e = launch_step_rows(s, 0, target_logits, draft_logits, draft_tokens,
                                          out, kv ? &k : nullptr, ws,
                                          static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SMC_OK : SMC_ERR_LAUNCH;
+}
+
+}  // namespace smcsd
+
+extern "C" {
+
+int32_t smc_step(const smc_params *p, const void *target_logits, const void *draft_logits,
+                 const int32_t *draft_tokens, float *log_weights, int32_t *tokens_out,
+                 int32_t *ancestors, float *ess, int32_t *resampled, const smc_kv *kv,
+                 void *workspace, size_t ws_bytes, void *stream) {
+  return step_impl(p, nullptr, target_logits, draft_logits, draft_tokens, log_weights,
+                   tokens_out, ancestors, ess, resampled, kv, workspace, ws_bytes, stream);
+}
+
+int32_t smc_step_ex(const smc_params *p, const smc_step_opts *opts,
+                    const void *target_logits, const void *draft_logits,
+                    const int32_t *draft_tokens, float *log_weights, int32_t *tokens_out,
+                    int32_t *ancestors, float *ess, int32_t *resampled, const smc_kv *kv,
+                    void *workspace, size_t ws_bytes, void *stream) {
+  return step_impl(p, opts, target_logits, draft_logits, draft_tokens, log_weights,
+                   tokens_out, ancestors, ess, resampled, kv, workspace, ws_bytes, stream);
+}
+
+int32_t smc_draft_sample(const smc_params *p, const void *draft_logits, int32_t position,
+                         int32_t *tokens_out, void *workspace, size_t ws_bytes,
+                         void *stream) {
+  if (!p) return SMC_ERR_ARG;
+  if (p->dtype != SMC_F32 && p->dtype != SMC_BF16) return SMC_ERR_DTYPE;
+  smc_params q = *p;
+  q.K = 1;  // not used; the workspace needs only what K = 1 needs
+  if (!shape_ok(&q) || position < 0 || !draft_logits || !tokens_out) return SMC_ERR_ARG;
+  Workspace ws{};
+  const int32_t rc = prepare_ws(&q, nullptr, workspace, ws_bytes, &ws);
+  if (rc != SMC_OK) return rc;
+  const cudaError_t e = launch_draft_sample(to_shape(&q), draft_logits, position, tokens_out, ws,
+                                            static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SMC_OK : SMC_ERR_LAUNCH;
+}
+
+int32_t smc_kv_usage(const smc_params *p, const smc_kv *kv, int32_t *used_blocks,
+                     int32_t *unshared_blocks, void *stream) {
+  if (!p || !kv || p->B < 1 || p->N < 1 || p->N > SMC_MAX_N || !kv_ok(p, kv) ||
+      !used_blocks || !unshared_blocks) {
+    return SMC_ERR_ARG;
+  }
+  const cudaError_t e = launch_kv_usage(to_shape(p), to_kv(kv), used_blocks, unshared_blocks,
+                                        static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SMC_OK : SMC_ERR_LAUNCH;
 }
 

@@ -51,6 +51,8 @@ struct Shape {
   float alpha, ess_frac;
   uint64_t seed;
   uint32_t step;
+  float tscale;              // 1/T of a temperature T (1: none)
+  const float *potential;    // [B*N] log-potential increments, or null
 };
 
 // Elements per chunk of the row reductions for a dtype.
@@ -66,10 +68,19 @@ struct StepOutputs {
   float *ess;
 };
 
-// mode 0: SMC step; mode 1: SpS verify (first launch).
+// mode 0: SMC step; mode 1: SpS verify (first launch); mode 2: draft
+// sampler (K = 0: every row is a bonus row, drawn into out.tokens_out).
 cudaError_t launch_step_rows(const Shape &s, int mode, const void *target, const void *draft,
                              const int32_t *tokens, const StepOutputs &out, const KvArgs *kv,
                              const Workspace &ws, cudaStream_t stream);
+// One token per row of `logits` [rows, V] from softmax(alpha l), by inverse
+// CDF with the DRAFT uniform of (seed, step, row, position).
+cudaError_t launch_draft_sample(const Shape &s, const void *logits, int position,
+                                int32_t *tokens_out, const Workspace &ws, cudaStream_t stream);
+// Per prompt: blocks with a positive reference count, and the blocks the
+// particles' token counts fill without sharing.
+cudaError_t launch_kv_usage(const Shape &s, const KvArgs &kv, int32_t *used, int32_t *unshared,
+                            cudaStream_t stream);
 cudaError_t launch_resample(const Shape &s, float *log_weights, int32_t *ancestors, float *ess,
                             int32_t *resampled, const Workspace &ws, cudaStream_t stream);
 cudaError_t launch_kv_remap(const Shape &s, const KvArgs &kv, const int32_t *ancestors,

@@ -136,6 +136,8 @@ struct BonusPairSum {
     return lb < ref && lb > kNegInf;
   }
 
+  // ALPHA1: the caller guarantees alpha == 1, so a = d needs no product.
+  template <bool ALPHA1>
   __device__ __forceinline__ void add(float x0, float x1, const float *th, const float *tl) {
     constexpr float kShift = 12582912.f;  // 1.5 * 2^23: rounds 64 y into the low bits
     const unsigned long long X = f2pack(fmaxf(x0, lb), fmaxf(x1, lb));
@@ -144,9 +146,12 @@ struct BonusPairSum {
     const unsigned long long BB = sub2(S, X);
     const unsigned long long SE = add2(sub2(X, sub2(S, BB)), sub2(nref, BB));
     // a = alpha d as AH + AL
-    const unsigned long long AH = mul2(al, S);
-    const unsigned long long NAE = fma2(nal, S, AH);  // minus the rounding error of AH
-    const unsigned long long AL = sub2(mul2(al, SE), NAE);
+    unsigned long long AH = S, AL = SE;
+    if (!ALPHA1) {
+      AH = mul2(al, S);
+      const unsigned long long NAE = fma2(nal, S, AH);  // minus the rounding error of AH
+      AL = sub2(mul2(al, SE), NAE);
+    }
     // y = a log2(e) as YH - NYL
     const unsigned long long YH = mul2(AH, f2dup(kLog2eHi));
     const unsigned long long NYE = fma2(AH, f2dup(-kLog2eHi), YH);

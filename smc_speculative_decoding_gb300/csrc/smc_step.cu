@@ -41,6 +41,11 @@ struct StepArgs {
   const int32_t *tokens;
   int B, N, K, V, nch, mode, use_kv;
   float alpha, ess_frac;
+  float tscale;               // 1/T: every logit is scaled by it
+  float balpha;               // exponent of the bonus distribution: alpha * tscale
+  bool bonus_lse;             // the bonus row's own log-sum-exp is needed (alpha != 1)
+  int bonus_purpose, bonus_position;  // Philox purpose and position of the bonus draw
+  const float *potential;     // [B*N] log-potential increments, or null
   uint64_t seed;
   uint32_t step;
   Workspace ws;
@@ -525,6 +530,7 @@ __device__ void smc_tail(const StepArgs &a, int b, TailSmem &sm, int *dyn, bool 
         delta += a.alpha * (rp.y - rp.x) - (rq.y - rq.x);
       }
       if (a.alpha != 1.f) delta += rb.z - a.alpha * rb.x;
+      if (a.potential) delta += __ldcg(a.potential + part);
       sm.bonus[tid] = __float_as_int(rb.w);
       lwf = lw0 + delta;
     }
@@ -636,14 +642,15 @@ __global__ void __launch_bounds__(kThreads, 4) step_rows_kernel(const StepArgs a
 
   float s = 0.f;
   ff S{0.f, 0.f};
+  const float l2s = a.tscale * kLog2e;  // log2(e) of the scaled logits
   if (!is_bonus) {
     if (finite_ref) {
-      const float mb = mc * kLog2e;
+      const float mb = mc * l2s;
       float s0 = 0.f, s1 = 0.f;
 #pragma unroll
       for (int e = 0; e < EPT; e += 2) {
-        s0 += fast_exp2(fmaf(x[e], kLog2e, -mb));
-        s1 += fast_exp2(fmaf(x[e + 1], kLog2e, -mb));
+        s0 += fast_exp2(fmaf(x[e], l2s, -mb));
+        s1 += fast_exp2(fmaf(x[e + 1], l2s, -mb));
       }
       s = s0 + s1;            // NaN logits propagate here and are reported at combine
     } else if (mc == -kNegInf) {
@@ -655,12 +662,12 @@ __global__ void __launch_bounds__(kThreads, 4) step_rows_kernel(const StepArgs a
     for (int e = 0; e < EPT; ++e) bad |= !(x[e] < -kNegInf);  // NaN or +inf
     if (bad) raise_status(a.ws.status, SMC_DEV_NONFINITE);
     if (finite_ref) {
-      const float mb = mc * kLog2e;
-      const bool need_fast = a.alpha != 1.f;
+      const float mb = mc * l2s;
+      const bool need_fast = a.bonus_lse;
 #pragma unroll
       for (int e = 0; e < EPT; ++e) {
-        ff_accum(S, weight_term(x[e], mc, a.alpha, s_tab));
-        if (need_fast) s += fast_exp2(fmaf(x[e], kLog2e, -mb));
+        ff_accum(S, weight_term(x[e], mc, a.balpha, s_tab));
+        if (need_fast) s += fast_exp2(fmaf(x[e], l2s, -mb));
       }
     }
     S = ff_norm(S);
@@ -689,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 4) step_rows_kernel(const StepArgs a
       float sum = 0.f;
       for (int c = lane; c < a.nch; c += 32) {
         const float cm = __ldcg(&pp[c].m), cs = __ldcg(&pp[c].s);
-        if (cm > kNegInf) sum += cs * expf(cm - M);
+        if (cm > kNegInf) sum += cs * expf(a.tscale * (cm - M));
         else if (cs != 0.f) sum += cs;  // NaN marker of a chunk holding +inf
       }
 #pragma unroll
@@ -699,11 +706,11 @@ __global__ void __launch_bounds__(kThreads, 4) step_rows_kernel(const StepArgs a
         float g = __int_as_float(0x7fc00000);
         if (M == kNegInf) bits |= SMC_DEV_EMPTY_ROW;
         else if (!(sum < -kNegInf) || M == -kNegInf) bits |= SMC_DEV_NONFINITE;
-        const float lse = M + logf(sum);
+        const float lse = a.tscale * M + logf(sum);
         const int k = j < a.K ? j : j - a.K - 1;
         const int tok = a.tokens[static_cast<size_t>(part) * a.K + k];
         if (tok < 0 || tok >= a.V) bits |= SMC_DEV_BAD_TOKEN;
-        else g = Tr::scalar(rowp, tok);
+        else g = a.tscale * Tr::scalar(rowp, tok);
         if (bits) raise_status(a.ws.status, bits);
         a.ws.results[row] = RowResult{lse, g, 0.f, -1};
       }
@@ -711,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 4) step_rows_kernel(const StepArgs a
   } else {
     // bonus row: float-float mass per chunk in absolute units (reference M),
     // then the inverse-CDF draw: which chunk, then which element.
-    const float alpha = a.alpha;
+    const float alpha = a.balpha;
     if (warp == 0) {
       float M = kNegInf;
       for (int c = lane; c < a.nch; c += 32) M = fmaxf(M, __ldcg(&pp[c].m));
@@ -732,13 +739,13 @@ __global__ void __launch_bounds__(kThreads, 4) step_rows_kernel(const StepArgs a
         if (c < a.nch) {
           chunk_mass(c, &val, &f);
           const float cm = __ldcg(&pp[c].m);
-          if (ok && cm > kNegInf) fast += __ldcg(&pp[c].s) * expf(cm - M);
+          if (ok && cm > kNegInf) fast += __ldcg(&pp[c].s) * expf(a.tscale * (cm - M));
         }
         total = ff_add(total, warp_ff_sum(val));
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) fast += __shfl_xor_sync(0xffffffffu, fast, o);
-      const float u = philox_uniform(a.seed, a.step, part, a.K, SMC_PURPOSE_BONUS);
+      const float u = philox_uniform(a.seed, a.step, part, a.bonus_position, a.bonus_purpose);
       ff rem{0.f, 0.f};
       const int sel = ok ? warp_find_chunk(a.nch, ff_mul_f(total, u), chunk_mass, &rem) : -1;
       if (lane == 0) {
@@ -749,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, 4) step_rows_kernel(const StepArgs a
         if (ok) {
           const double lt = log(ff_to_double(total));
           lse_alpha = static_cast<float>(static_cast<double>(alpha) * M + lt);
-          lse = alpha != 1.f ? M + logf(fast) : lse_alpha;
+          lse = a.bonus_lse ? a.tscale * M + logf(fast) : lse_alpha;
         } else {
           lse = lse_alpha = M == kNegInf ? kNegInf : __int_as_float(0x7fc00000);
           raise_status(a.ws.status, M == kNegInf ? SMC_DEV_EMPTY_ROW : SMC_DEV_NONFINITE);
@@ -769,7 +776,10 @@ __global__ void __launch_bounds__(kThreads, 4) step_rows_kernel(const StepArgs a
           [&](int64_t i) { return weight_term(Tr::scalar(rowp, i), cm, alpha, s_tab); },
           s_ff, s_int);
     }
-    if (tid == 0) a.ws.results[row].tok = tok;
+    if (tid == 0) {
+      a.ws.results[row].tok = tok;
+      if (a.mode == 2) a.out.tokens_out[part] = tok;
+    }
   }
 }
 
@@ -813,7 +823,7 @@ template <typename T> struct StreamGeom {
 struct StreamArgs {
   StepArgs a;
   int snch;           // ring-slot chunks per row: ceil(V / StreamGeom<T>::kCH)
-  float wspan;        // 40 / alpha: logits further below a range's max weigh e^-40
+  float wspan;        // 40 / balpha: logits further below a range's max weigh e^-40
   int G;              // chunks per work item of a non-bonus row
   int ipr;            // work items per non-bonus row
   int n_fast_items;   // non-bonus rows * ipr
@@ -871,8 +881,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
   // ---- producer warp -----------------------------------------------------------
   // Work comes from two queues: items of G chunks of the non-bonus rows, and
   // single chunks of the bonus rows (whose weights cost far more to compute).
-  // The producer alternates between them so that every CTA, all through the
-  // kernel, mixes streaming-bound and arithmetic-bound chunks.
+  // The producer interleaves them in the proportion of the whole step (2K
+  // non-bonus chunks per bonus chunk), so that every CTA, all through the
+  // kernel, mixes streaming-bound and arithmetic-bound chunks evenly.
   if (warp == kConsumerWarps) {
     if (lane == 0) {
       const int rest = rpp - 1;  // non-bonus rows per particle
@@ -894,7 +905,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
         while (!have || chunk >= end) {
           have = false;
           if (fast_done && bonus_done) break;
-          const bool take_bonus = !bonus_done && (fast_done || n_bonus < n_fast);
+          const bool take_bonus =
+              !bonus_done && (fast_done || n_bonus * 2 * a.K < n_fast * sa.G);
           if (take_bonus) {
             const unsigned id = next_bonus;
             if (id >= static_cast<unsigned>(sa.n_bonus_items)) { bonus_done = true; continue; }
@@ -945,6 +957,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
   }
 
   // ---- consumer warps --------------------------------------------------------
+  const float l2s = a.tscale * kLog2e;  // log2(e) of the scaled logits
   float m_t = kNegInf, s_t = 0.f;  // this lane's running (max, sum exp) over the item
   for (int i = 0;; ++i) {
     const int slot = i % kStages;
@@ -959,7 +972,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
     const int part = mt.part;
     const int j = mt.j;
     const bool is_bonus = j == a.K;
-    const bool fast = !is_bonus || a.alpha != 1.f;
+    const bool fast = !is_bonus || a.bonus_lse;
     if (mt.flags & kSlotFirst) { m_t = kNegInf; s_t = 0.f; }
 
     // this warp's range of the chunk: logits [warp*WCH, (warp+1)*WCH).  A
@@ -1015,12 +1028,12 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
     }
     if (fast) {
       if (cm > m_t) {
-        if (m_t > kNegInf) s_t *= fast_exp2((m_t - cm) * kLog2e);
+        if (m_t > kNegInf) s_t *= fast_exp2((m_t - cm) * l2s);
         m_t = cm;
       }
       if (m_t > kNegInf && m_t < kInf) {
-        const float mb = m_t * kLog2e;
-        const unsigned long long l2 = f2pack(kLog2e, kLog2e), nmb = f2pack(-mb, -mb);
+        const float mb = m_t * l2s;
+        const unsigned long long l2 = f2pack(l2s, l2s), nmb = f2pack(-mb, -mb);
         unsigned long long acc = 0ull;
         if (sizeof(T) == 4) {
 #pragma unroll
@@ -1052,14 +1065,18 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
       int flag = 0;
       if (ref > kNegInf) {
         BonusPairSum bs;
-        if (bs.init(ref, a.alpha, sa.wspan)) {
+        if (bs.init(ref, a.balpha, sa.wspan)) {
           if (sizeof(T) == 4) {
+            // fp32 logits: the general exponent only (the power-sampling case)
 #pragma unroll
             for (int k = 0; k < NW; k += 2)
-              bs.add(__uint_as_float(wd[k]), __uint_as_float(wd[k + 1]), s_th, s_tl);
+              bs.add<false>(__uint_as_float(wd[k]), __uint_as_float(wd[k + 1]), s_th, s_tl);
+          } else if (a.balpha == 1.f) {
+#pragma unroll
+            for (int k = 0; k < NW; ++k) bs.add<true>(bf16_lo(wd[k]), bf16_hi(wd[k]), s_th, s_tl);
           } else {
 #pragma unroll
-            for (int k = 0; k < NW; ++k) bs.add(bf16_lo(wd[k]), bf16_hi(wd[k]), s_th, s_tl);
+            for (int k = 0; k < NW; ++k) bs.add<false>(bf16_lo(wd[k]), bf16_hi(wd[k]), s_th, s_tl);
           }
           usum = warp_ff_sum(bs.total());
         } else {
@@ -1078,7 +1095,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
     if (fast) {
       const float M = warp_max(m_t);
       float contrib = 0.f;
-      if (m_t > kNegInf && M < kInf) contrib = s_t * fast_exp2((m_t - M) * kLog2e);
+      if (m_t > kNegInf && M < kInf) contrib = s_t * fast_exp2((m_t - M) * l2s);
       else if (s_t != 0.f) contrib = s_t;  // NaN marker
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) contrib += __shfl_xor_sync(0xffffffffu, contrib, o);
@@ -1214,7 +1231,7 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa, i
   }
   row = part * rpp + j;
   const bool is_bonus = j == a.K;
-  const bool fast = !is_bonus || a.alpha != 1.f;
+  const bool fast = !is_bonus || a.bonus_lse;
   const char *rowp = row_base<T>(a, row);
   // the drafted token and its logit are inputs of the step: gathered while
   // the streaming kernel still runs
@@ -1222,7 +1239,7 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa, i
   float gv = 0.f;
   if (!is_bonus && live && lane == 0) {
     gtok = a.tokens[static_cast<size_t>(part) * a.K + (j < a.K ? j : j - a.K - 1)];
-    gv = (gtok < 0 || gtok >= a.V) ? __int_as_float(0x7fc00000) : Tr::scalar(rowp, gtok);
+    gv = (gtok < 0 || gtok >= a.V) ? __int_as_float(0x7fc00000) : a.tscale * Tr::scalar(rowp, gtok);
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1240,15 +1257,15 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa, i
     for (int c = lane; c < n_ip; c += 32) {
       const float2 pv = ip[c];
       if (pv.x > lm) {
-        if (lm > kNegInf && pv.x < kInf) ls *= expf(lm - pv.x);
+        if (lm > kNegInf && pv.x < kInf) ls *= expf(a.tscale * (lm - pv.x));
         else if (pv.x == kInf) ls = 0.f;
         lm = pv.x;
       }
-      if (pv.x > kNegInf && lm < kInf) ls += pv.y * expf(pv.x - lm);
+      if (pv.x > kNegInf && lm < kInf) ls += pv.y * expf(a.tscale * (pv.x - lm));
       else if (pv.y != 0.f) ls += pv.y;  // NaN marker
     }
     fM = warp_max(lm);
-    fS = (lm > kNegInf && fM < kInf) ? ls * expf(lm - fM) : ls;
+    fS = (lm > kNegInf && fM < kInf) ? ls * expf(a.tscale * (lm - fM)) : ls;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) fS += __shfl_xor_sync(0xffffffffu, fS, o);
   }
@@ -1257,7 +1274,7 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa, i
       unsigned bits = 0;
       if (fM == kNegInf) bits |= SMC_DEV_EMPTY_ROW;
       else if (!(fS < kInf) || fM == kInf) bits |= SMC_DEV_NONFINITE;
-      const float lse = fM + logf(fS);
+      const float lse = a.tscale * fM + logf(fS);
       if (gtok < 0 || gtok >= a.V) bits |= SMC_DEV_BAD_TOKEN;
       if (bits) raise_status(a.ws.status, bits);
       a.ws.results[row] = RowResult{lse, gv, 0.f, -1};
@@ -1268,7 +1285,7 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa, i
   // ---- bonus row: units are (chunk, warp) ranges of WCH logits in vocabulary
   // order, each with its max as reference and the float-float sum of its
   // weights relative to it
-  const float alpha = a.alpha;
+  const float alpha = a.balpha;
   int4 *bp = a.ws.bonus_part + static_cast<size_t>(part) * sa.snch * kConsumerWarps;
   const int n_units = sa.snch * kConsumerWarps;
   if (warp == 0) {
@@ -1294,7 +1311,7 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa, i
     }
   }
   __syncthreads();
-  const float u = philox_uniform(a.seed, a.step, part, a.K, SMC_PURPOSE_BONUS);
+  const float u = philox_uniform(a.seed, a.step, part, a.bonus_position, a.bonus_purpose);
   if (n_units <= kThreads) {
     // one unit per thread: its mass relative to the row's largest reference
     // M, a CTA-wide inclusive prefix, and the first unit whose prefix exceeds
@@ -1330,7 +1347,7 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa, i
       float lse, lse_alpha;
       if (ok) {
         lse_alpha = alpha * M + (logf(total.hi) + total.lo / total.hi);
-        lse = alpha != 1.f ? fM + logf(fS) : lse_alpha;
+        lse = a.bonus_lse ? a.tscale * fM + logf(fS) : lse_alpha;
       } else {
         lse = lse_alpha = M == kNegInf ? kNegInf : __int_as_float(0x7fc00000);
         raise_status(a.ws.status, M == kNegInf ? SMC_DEV_EMPTY_ROW : SMC_DEV_NONFINITE);
@@ -1366,7 +1383,7 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa, i
       float lse, lse_alpha;
       if (ok) {
         lse_alpha = alpha * M + (logf(total.hi) + total.lo / total.hi);
-        lse = alpha != 1.f ? fM + logf(fS) : lse_alpha;
+        lse = a.bonus_lse ? a.tscale * fM + logf(fS) : lse_alpha;
       } else {
         lse = lse_alpha = M == kNegInf ? kNegInf : __int_as_float(0x7fc00000);
         raise_status(a.ws.status, M == kNegInf ? SMC_DEV_EMPTY_ROW : SMC_DEV_NONFINITE);
@@ -1376,14 +1393,20 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa, i
   }
   __syncthreads();
   const int sel = s_sel;
-  if (sel < 0) return;  // uniform across the CTA
+  if (sel < 0) {  // uniform across the CTA
+    if (a.mode == 2 && threadIdx.x == 0) a.out.tokens_out[part] = -1;
+    return;
+  }
   const int c = sel / kConsumerWarps, w = sel - c * kConsumerWarps;
   const int64_t r0 = static_cast<int64_t>(c) * CH + static_cast<int64_t>(w) * WCH;
   const int len = static_cast<int>(max(static_cast<int64_t>(0),
                                        min(static_cast<int64_t>(WCH), a.V - r0)));
   const int tok = block_select_fixed<T, WCH / kThreads>(rowp, r0, len, s_target, s_ref, alpha,
                                                          s_tab, s_ll, s_i);
-  if (threadIdx.x == 0) a.ws.results[row].tok = tok;
+  if (threadIdx.x == 0) {
+    a.ws.results[row].tok = tok;
+    if (a.mode == 2) a.out.tokens_out[part] = tok;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1497,7 +1520,7 @@ static cudaError_t launch_stream(const StepArgs &a, long long rows, cudaStream_t
   sa.a = a;
   sa.snch = static_cast<int>((static_cast<long long>(a.V) + StreamGeom<T>::kCH - 1) /
                              StreamGeom<T>::kCH);
-  sa.wspan = 40.f / a.alpha;
+  sa.wspan = 40.f / a.balpha;
   const long long total_chunks = rows * sa.snch;
   // about twelve work items per resident CTA, each 1..8 chunks, split evenly
   // over a row (short items keep the CTAs' finishing times close together)
@@ -1564,42 +1587,101 @@ static cudaError_t launch_tail(const StepArgs &a, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, tail_kernel, a, staged);
 }
 
-cudaError_t launch_step_rows(const Shape &s, int mode, const void *target, const void *draft,
-                             const int32_t *tokens, const StepOutputs &out, const KvArgs *kv,
-                             const Workspace &ws, cudaStream_t stream) {
-  StepArgs a{};
-  a.target = static_cast<const char *>(target);
-  a.draft = static_cast<const char *>(draft);
-  a.tokens = tokens;
-  a.B = s.B; a.N = s.N; a.K = s.K; a.V = s.V;
-  a.nch = chunks_per_row(s.dtype, s.V);
-  a.mode = mode;
-  a.alpha = s.alpha; a.ess_frac = s.ess_frac; a.seed = s.seed; a.step = s.step;
-  a.ws = ws;
-  a.out = out;
-  a.use_kv = kv != nullptr;
-  if (kv) a.kv = *kv;
-  const long long rows = static_cast<long long>(s.B) * s.N * (2 * s.K + 1);
-  const int esz = s.dtype == SMC_BF16 ? 2 : 4;
+// The row pass (streaming or per-chunk kernel, then the row combine).
+static cudaError_t launch_rows(const StepArgs &a, int dtype, long long rows, cudaStream_t stream) {
+  const int esz = dtype == SMC_BF16 ? 2 : 4;
   // bulk copies need 16-byte aligned rows and chunk sizes: aligned bases and V*esz % 16 == 0
-  const bool vec = aligned16(target) && aligned16(draft) &&
-                   (static_cast<long long>(s.V) * esz) % 16 == 0;
+  const bool vec = aligned16(a.target) && aligned16(a.draft) &&
+                   (static_cast<long long>(a.V) * esz) % 16 == 0;
   cudaError_t e;
   if (vec) {
-    e = s.dtype == SMC_BF16 ? launch_stream<bf16_tag>(a, rows, stream)
-                            : launch_stream<float>(a, rows, stream);
+    e = dtype == SMC_BF16 ? launch_stream<bf16_tag>(a, rows, stream)
+                          : launch_stream<float>(a, rows, stream);
   } else {
     const long long grid = rows * a.nch;
     dim3 g(static_cast<unsigned>(grid)), blk(kThreads);
     if (g_rows_begin && (e = cudaEventRecord(g_rows_begin, stream)) != cudaSuccess) return e;
-    if (s.dtype == SMC_BF16) step_rows_kernel<bf16_tag, false><<<g, blk, 0, stream>>>(a);
+    if (dtype == SMC_BF16) step_rows_kernel<bf16_tag, false><<<g, blk, 0, stream>>>(a);
     else step_rows_kernel<float, false><<<g, blk, 0, stream>>>(a);
     e = cudaGetLastError();
     if (e == cudaSuccess && g_rows_end) e = cudaEventRecord(g_rows_end, stream);
   }
+  return e;
+}
+
+static StepArgs step_args(const Shape &s, int mode, const Workspace &ws) {
+  StepArgs a{};
+  a.B = s.B; a.N = s.N; a.K = s.K; a.V = s.V;
+  a.nch = chunks_per_row(s.dtype, s.V);
+  a.mode = mode;
+  a.alpha = s.alpha; a.ess_frac = s.ess_frac; a.seed = s.seed; a.step = s.step;
+  a.tscale = s.tscale;
+  a.balpha = s.alpha * s.tscale;  // fp32 product, as the oracle takes it
+  a.bonus_lse = mode != 2 && s.alpha != 1.f;
+  a.bonus_purpose = SMC_PURPOSE_BONUS;
+  a.bonus_position = s.K;
+  a.potential = s.potential;
+  a.ws = ws;
+  return a;
+}
+
+cudaError_t launch_step_rows(const Shape &s, int mode, const void *target, const void *draft,
+                             const int32_t *tokens, const StepOutputs &out, const KvArgs *kv,
+                             const Workspace &ws, cudaStream_t stream) {
+  StepArgs a = step_args(s, mode, ws);
+  a.target = static_cast<const char *>(target);
+  a.draft = static_cast<const char *>(draft);
+  a.tokens = tokens;
+  a.out = out;
+  a.use_kv = kv != nullptr;
+  if (kv) a.kv = *kv;
+  const long long rows = static_cast<long long>(s.B) * s.N * (2 * s.K + 1);
+  cudaError_t e = launch_rows(a, s.dtype, rows, stream);
   if (e != cudaSuccess) return e;
   e = launch_tail(a, stream);
   if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_draft_sample(const Shape &s, const void *logits, int position,
+                                int32_t *tokens_out, const Workspace &ws, cudaStream_t stream) {
+  Shape s0 = s;
+  s0.K = 0;  // one row per particle, and it is the sampled ("bonus") row
+  StepArgs a = step_args(s0, 2, ws);
+  a.target = static_cast<const char *>(logits);
+  a.draft = static_cast<const char *>(logits);
+  a.bonus_purpose = SMC_PURPOSE_DRAFT;
+  a.bonus_position = position;
+  a.out.tokens_out = tokens_out;
+  return launch_rows(a, s.dtype, static_cast<long long>(s.B) * s.N, stream);
+}
+
+// Per prompt b (one CTA): blocks of its pool with a positive reference count,
+// and the blocks its particles' token counts fill without sharing.
+__global__ void __launch_bounds__(kThreads) kv_usage_kernel(int N, KvArgs kv, int32_t *used,
+                                                            int32_t *unshared) {
+  __shared__ int s_red[2 * kWarps];
+  const int b = blockIdx.x;
+  int u = 0, w = 0;
+  for (int k = threadIdx.x; k < kv.P; k += kThreads) {
+    u += __ldcg(kv.refcount + static_cast<size_t>(b) * kv.P + k) > 0;
+  }
+  for (int i = threadIdx.x; i < N; i += kThreads) {
+    const long long len = __ldcg(kv.seq_len + static_cast<size_t>(b) * N + i);
+    w += len > 0 ? static_cast<int>((len + kv.block_size - 1) / kv.block_size) : 0;
+  }
+  int tu, tw;
+  block_excl_scan_i(u, s_red, &tu);
+  block_excl_scan_i(w, s_red, &tw);
+  if (threadIdx.x == 0) {
+    used[b] = tu;
+    unshared[b] = tw;
+  }
+}
+
+cudaError_t launch_kv_usage(const Shape &s, const KvArgs &kv, int32_t *used, int32_t *unshared,
+                            cudaStream_t stream) {
+  kv_usage_kernel<<<s.B, kThreads, 0, stream>>>(s.N, kv, used, unshared);
   return cudaGetLastError();
 }
 

@@ -44,9 +44,11 @@ def kv_to_numpy(kv):
 class StepRunner:
     """Owns the device state of one workload run through smc_step."""
 
-    def __init__(self, w, seed=0, device="cuda", with_kv=True, steps=None, ess_frac=None):
+    def __init__(self, w, seed=0, device="cuda", with_kv=True, steps=None, ess_frac=None,
+                 temperature=None):
         self.w = w
         self.seed = seed
+        self.temperature = temperature  # None: plain smc_step; else smc_step_ex
         self.device = device
         self.ess_frac = w.ess_frac if ess_frac is None else ess_frac
         B, N, K = w.B, w.N, w.K
@@ -70,20 +72,30 @@ class StepRunner:
         return smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, self.ess_frac,
                                  self.seed, step)
 
-    def run(self, inputs, step):
-        smcsd.smc_step(self.params(step), inputs["target"], inputs["draft"],
-                       inputs["draft_tokens"], self.log_weights, self.tokens_out,
-                       self.ancestors, self.ess, self.resampled, kv=self.kv_struct,
-                       workspace=self.workspace)
+    def run(self, inputs, step, log_potential=None):
+        if self.temperature is None and log_potential is None:
+            smcsd.smc_step(self.params(step), inputs["target"], inputs["draft"],
+                           inputs["draft_tokens"], self.log_weights, self.tokens_out,
+                           self.ancestors, self.ess, self.resampled, kv=self.kv_struct,
+                           workspace=self.workspace)
+        else:
+            smcsd.smc_step_ex(self.params(step), inputs["target"], inputs["draft"],
+                              inputs["draft_tokens"], self.log_weights, self.tokens_out,
+                              self.ancestors, self.ess, self.resampled, kv=self.kv_struct,
+                              workspace=self.workspace,
+                              temperature=1.0 if self.temperature is None else self.temperature,
+                              log_potential=log_potential)
 
     def status(self):
         return smcsd.smc_device_status(self.workspace, clear=True)
 
 
 def lockstep(w, steps, seed=0, with_kv=True, ess_frac=None, tie=1e-5, resample_tie=1e-4,
-             lw_init=None):
-    """Run `steps` steps on GPU and oracle; return the Tally."""
-    runner = StepRunner(w, seed=seed, with_kv=with_kv, steps=steps, ess_frac=ess_frac)
+             lw_init=None, temperature=None, potential_fn=None):
+    """Run `steps` steps on GPU and oracle; return the Tally.  temperature and
+    potential_fn(step) -> [B, N] fp32 CUDA tensor (or None) select smc_step_ex."""
+    runner = StepRunner(w, seed=seed, with_kv=with_kv, steps=steps, ess_frac=ess_frac,
+                        temperature=temperature)
     if lw_init is not None:
         runner.log_weights.copy_(torch.as_tensor(lw_init, dtype=torch.float32).reshape(-1))
     B, N, K = w.B, w.N, w.K
@@ -92,7 +104,8 @@ def lockstep(w, steps, seed=0, with_kv=True, ess_frac=None, tie=1e-5, resample_t
         inp = make_step_inputs(w, seed, device="cuda", step=step)
         lw_in = runner.log_weights.cpu().numpy().reshape(B, N).astype(np.float64)
         kv_in = kv_to_numpy(runner.kv) if with_kv else None
-        runner.run(inp, step)
+        phi = potential_fn(step) if potential_fn is not None else None
+        runner.run(inp, step, log_potential=phi)
         torch.cuda.synchronize()
         bits = runner.status()
         assert bits == 0, f"device status {smcsd.status_names(bits)}"
@@ -105,7 +118,10 @@ def lockstep(w, steps, seed=0, with_kv=True, ess_frac=None, tie=1e-5, resample_t
         x = inp["draft_tokens"].cpu().numpy().astype(np.int64)
         ref = osmc.smc_step(to_numpy_logits(inp["target"]), to_numpy_logits(inp["draft"]), x,
                             lw_in, alpha=w.alpha, ess_frac=runner.ess_frac, seed=seed,
-                            step=step, dtype=w.dtype)
+                            step=step, dtype=w.dtype,
+                            temperature=1.0 if temperature is None else temperature,
+                            log_potential=None if phi is None else
+                            phi.cpu().numpy().reshape(B, N).astype(np.float64))
         check_step(w, ref, x, g_lw, g_tok, g_anc, g_ess, g_res, tally, tie, resample_tie)
         if with_kv:
             check_kv(w, runner, kv_in, g_anc, g_res)
@@ -128,8 +144,11 @@ def check_step(w, ref, x, g_lw, g_tok, g_anc, g_ess, g_res, tally, tie, resample
             assert np.array_equal(g_lw[b], np.zeros(N))
         else:
             assert np.array_equal(g_anc[b], np.arange(N))
-            err = np.abs(g_lw[b] - ref["log_weights_pre"][b])
-            assert err.max() <= tol, f"log-weights off by {err.max()} (tol {tol})"
+            r = ref["log_weights_pre"][b]
+            dead = np.isneginf(r)  # weight 0: a -inf increment (potential or masked token)
+            assert np.array_equal(np.isneginf(g_lw[b]), dead), "-inf log-weights differ"
+            err = np.abs(g_lw[b][~dead] - r[~dead])
+            assert err.size == 0 or err.max() <= tol, f"log-weights off by {err.max()} (tol {tol})"
         # tokens: drafted tokens of the GPU's ancestor, bonus of that ancestor
         a = g_anc[b]
         assert np.array_equal(g_tok[b, :, :K], x[b, a]), "drafted tokens not gathered by ancestor"

@@ -49,27 +49,30 @@ def test_struct_layout_matches_c_compiler(tmp_path):
     gcc = shutil.which("gcc")
     if gcc is None:
         pytest.skip("gcc not available")
-    from smc_speculative_decoding_gb300.binding import smc_params, smc_kv
+    from smc_speculative_decoding_gb300.binding import smc_params, smc_kv, smc_step_opts
     src = tmp_path / "layout.c"
     fields_p = [f[0] for f in smc_params._fields_]
     fields_k = [f[0] for f in smc_kv._fields_]
+    fields_o = [f[0] for f in smc_step_opts._fields_]
     body = ['#include <stdio.h>', '#include <stddef.h>', '#include "smcsd.h"', 'int main(void){',
-            'printf("%zu %zu\\n", sizeof(smc_params), sizeof(smc_kv));']
+            'printf("%zu %zu %zu\\n", sizeof(smc_params), sizeof(smc_kv), sizeof(smc_step_opts));']
     body += [f'printf("p {f} %zu\\n", offsetof(smc_params, {f}));' for f in fields_p]
     body += [f'printf("k {f} %zu\\n", offsetof(smc_kv, {f}));' for f in fields_k]
+    body += [f'printf("o {f} %zu\\n", offsetof(smc_step_opts, {f}));' for f in fields_o]
     body += ['return 0;}']
     src.write_text("\n".join(body))
     exe = tmp_path / "layout"
     subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", f"-I{ROOT}/include", str(src), "-o",
                     str(exe)], check=True, capture_output=True)
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
-    sp, sk = map(int, out[0].split())
+    sp, sk, so = map(int, out[0].split())
     assert sp == ctypes.sizeof(smc_params) and sk == ctypes.sizeof(smc_kv)
+    assert so == ctypes.sizeof(smc_step_opts)
     for line in out[1:]:
         if not line:
             continue
         kind, name, off = line.split()
-        cls = smc_params if kind == "p" else smc_kv
+        cls = {"p": smc_params, "k": smc_kv, "o": smc_step_opts}[kind]
         assert getattr(cls, name).offset == int(off), name
 
 
@@ -114,6 +117,17 @@ def test_host_validation_without_gpu(lib):
     assert lib.kv_blocktable_remap(ctypes.byref(good), ctypes.byref(kv), fake, fake, -1, ws,
                                    1 << 30, None) == -1
     assert lib.smc_device_status(None, 0, None, None) == -1
+    # smc_step_ex: temperature must be positive and finite, reserved zero
+    for t, r in ((0.0, 0), (-1.0, 0), (float("inf"), 0), (float("nan"), 0), (1e-45, 0), (1.0, 3)):
+        opts = bd.smc_step_opts(None, t, r)
+        assert lib.smc_step_ex(ctypes.byref(good), ctypes.byref(opts), *[fake] * 8, None, ws,
+                               need, None) == -1
+    # smc_draft_sample: a position below 0 or a missing output
+    assert lib.smc_draft_sample(ctypes.byref(good), fake, -1, fake, ws, need, None) == -1
+    assert lib.smc_draft_sample(ctypes.byref(good), fake, 0, None, ws, need, None) == -1
+    # smc_kv_usage needs the KV struct and both outputs
+    assert lib.smc_kv_usage(ctypes.byref(good), None, fake, fake, None) == -1
+    assert lib.smc_kv_usage(ctypes.byref(good), ctypes.byref(kv), None, fake, None) == -1
     # the row-timing hook takes both events or neither
     assert lib.smc_set_row_timing_events(fake, None) == -1
     assert lib.smc_set_row_timing_events(None, fake) == -1

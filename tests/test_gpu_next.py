@@ -1,0 +1,129 @@
+"""GPU parity of the step's extensions against the CPU oracle: smc_step_ex
+(temperature, per-particle log-potentials), smc_draft_sample (the draft-side
+sampler) and smc_kv_usage (KV-cache accounting).  Same bar as the basic
+step: integer outputs exact except draws the oracle flags as near ties,
+log-weights within 1e-4 (fp32 logits) or 2e-3 (bf16 logits)."""
+import numpy as np
+import pytest
+import torch
+
+import smc_speculative_decoding_gb300 as smcsd
+from smc_speculative_decoding_gb300.workloads import WORKLOADS, make_step_inputs, to_numpy_logits
+from oracle import smc as osmc, kv as okv
+
+from gpu_harness import lockstep, StepRunner, kv_to_numpy
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from smc_speculative_decoding_gb300 import build
+    build.build()
+
+
+def _potentials(w, seed):
+    """A step's log-potentials: N(0, 0.7^2), and -inf on one particle of each
+    prompt on odd steps (a violated constraint)."""
+    def fn(step):
+        g = torch.Generator(device="cuda")
+        g.manual_seed(seed * 7919 + step)
+        phi = torch.randn(w.B, w.N, generator=g, device="cuda") * 0.7
+        if step % 2:
+            phi[:, (step // 2) % w.N] = float("-inf")
+        return phi.reshape(-1).contiguous()
+    return fn
+
+
+@pytest.mark.parametrize("name,B,temperature", [("tiny_v64", 2, 0.7),
+                                                ("single_prompt_v32000", 2, 1.6),
+                                                ("power_sampling_v151936", 1, 0.8)])
+def test_step_ex_matches_oracle(name, B, temperature):
+    w = WORKLOADS[name].with_(B=B)
+    steps = 6 if w.V > 1000 else 10
+    t = lockstep(w, steps, seed=17, with_kv=True, temperature=temperature,
+                 potential_fn=_potentials(w, 17))
+    print(f"{name} T={temperature}: draws={t.draws} flagged={t.flagged} mismatched={t.mismatched}")
+
+
+def test_step_ex_serving_size_one_step():
+    w = WORKLOADS["batched_serving_v128256"].with_(B=4)
+    t = lockstep(w, 2, seed=5, with_kv=True, temperature=1.3, potential_fn=_potentials(w, 5))
+    print(f"serving T=1.3: draws={t.draws} flagged={t.flagged} mismatched={t.mismatched}")
+
+
+def test_step_ex_unaligned_vocab_takes_the_per_chunk_path():
+    w = WORKLOADS["single_prompt_v32000"].with_(V=1001, B=3)
+    lockstep(w, 4, seed=8, with_kv=False, temperature=0.6, potential_fn=_potentials(w, 8))
+
+
+def test_step_ex_defaults_equal_smc_step():
+    w = WORKLOADS["single_prompt_v32000"].with_(B=2)
+    inp = make_step_inputs(w, 4, device="cuda")
+    a = StepRunner(w, seed=4, with_kv=True, steps=2)
+    b = StepRunner(w, seed=4, with_kv=True, steps=2, temperature=1.0)
+    a.run(inp, 0)
+    b.run(inp, 0)
+    torch.cuda.synchronize()
+    for name in ("log_weights", "tokens_out", "ancestors", "ess", "resampled"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+    for key in a.kv:
+        assert torch.equal(a.kv[key], b.kv[key]), key
+
+
+@pytest.mark.parametrize("V,dtype,alpha", [(128256, "bf16", 1.0), (128256, "bf16", 0.5),
+                                           (151936, "f32", 1.0), (1001, "bf16", 1.0),
+                                           (64, "f32", 2.0)])
+def test_draft_sample_matches_oracle(V, dtype, alpha):
+    w = WORKLOADS["sweep_v128256"].with_(B=8, N=8, K=2, V=V, dtype=dtype)
+    draft = make_step_inputs(w, 31, device="cuda")["draft"][:, :, 0].contiguous()
+    params = smcsd.make_params(w.B, w.N, w.K, V, dtype, alpha, 0.5, 31, 3)
+    ws = smcsd.alloc_workspace(params)
+    out = torch.empty(w.B * w.N, dtype=torch.int32, device="cuda")
+    draws = mism = flagged = 0
+    for position in range(3):
+        smcsd.smc_draft_sample(params, draft, position, out, ws)
+        torch.cuda.synchronize()
+        assert smcsd.smc_device_status(ws, clear=True) == 0
+        ref, margin = osmc.draft_sample(to_numpy_logits(draft), position, alpha=alpha, seed=31,
+                                        step=3, dtype=dtype)
+        g = out.cpu().numpy().reshape(w.B, w.N)
+        bad = (g != ref) & (margin >= 1e-5)
+        assert not bad.any(), (np.argwhere(bad)[:4], g[bad][:4], ref[bad][:4])
+        draws += g.size
+        flagged += int((margin < 1e-5).sum())
+        mism += int((g != ref).sum())
+    print(f"draft sample V={V} {dtype} alpha={alpha}: draws={draws} flagged={flagged} "
+          f"mismatched={mism}")
+
+
+def test_draft_sample_empty_row_reports_and_returns_minus_one():
+    w = WORKLOADS["tiny_v64"].with_(B=1, N=4)
+    draft = make_step_inputs(w, 2, device="cuda")["draft"][:, :, 0].contiguous()
+    draft[0, 2, :] = float("-inf")
+    params = smcsd.make_params(1, 4, 3, 64, "f32", 1.0, 0.5, 2, 0)
+    ws = smcsd.alloc_workspace(params)
+    out = torch.zeros(4, dtype=torch.int32, device="cuda")
+    smcsd.smc_draft_sample(params, draft, 0, out, ws)
+    torch.cuda.synchronize()
+    assert "empty_row" in smcsd.status_names(smcsd.smc_device_status(ws, clear=True))
+    assert out[2].item() == -1
+
+
+def test_kv_usage_matches_oracle():
+    w = WORKLOADS["single_prompt_v32000"].with_(B=3, N=8)
+    r = StepRunner(w, seed=12, with_kv=True, steps=6)
+    params = r.params(0)
+    used = torch.empty(w.B, dtype=torch.int32, device="cuda")
+    unshared = torch.empty(w.B, dtype=torch.int32, device="cuda")
+    for step in range(6):
+        r.run(make_step_inputs(w, 12, device="cuda", step=step), step)
+        smcsd.smc_kv_usage(params, r.kv_struct, used, unshared)
+        torch.cuda.synchronize()
+        assert r.status() == 0
+        st = kv_to_numpy(r.kv)
+        ref_used, ref_unshared = okv.usage(st["tables"], st["seq_len"], w.block_size)
+        assert np.array_equal(used.cpu().numpy(), ref_used)
+        assert np.array_equal(unshared.cpu().numpy(), ref_unshared)
