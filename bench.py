@@ -408,7 +408,10 @@ def run_extensions(w, dev, smcsd, ring, reps=50):
 def run_e2e(args, w, dev, smcsd, world):
     """Same metric through the public API with host buffers: every step copies
     its logits and drafted tokens from pinned host memory and reads the emitted
-    tokens and weights back, inside the timed region."""
+    tokens and weights back, inside the timed region.  The copy of step s+1's
+    inputs runs on a second stream into the other half of a double buffer while
+    step s computes, as a serving loop whose inputs arrive from the host would
+    overlap them."""
     from smc_speculative_decoding_gb300.workloads import make_step_inputs, make_kv_state
     T, P = w.kv_dims(args.episode)
     host = []
@@ -416,7 +419,7 @@ def run_e2e(args, w, dev, smcsd, world):
         inp = make_step_inputs(w, 2000, device=dev, step=s)
         host.append({k: v.cpu().pin_memory() for k, v in inp.items()})
         del inp
-    d_in = {k: torch.empty_like(v, device=dev) for k, v in host[0].items()}
+    d_in = [{k: torch.empty_like(v, device=dev) for k, v in host[0].items()} for _ in range(2)]
     kv0 = make_kv_state(w.B, w.N, w.prefix, w.block_size, T, P, device=dev)
     kv = {k: v.clone() for k, v in kv0.items()}
     p0 = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, 0)
@@ -430,21 +433,39 @@ def run_e2e(args, w, dev, smcsd, world):
     h_tok = torch.empty(tok.shape, dtype=torch.int32).pin_memory()
     h_lw = torch.empty(lw.shape, dtype=torch.float32).pin_memory()
     stream = torch.cuda.current_stream()
+    copy_stream = torch.cuda.Stream()
     n_steps = min(args.e2e_steps, args.steps)
     h2d = sum(v.numel() * v.element_size() for v in host[0].values())
     d2h = h_tok.numel() * 4 + h_lw.numel() * 4
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    consumed = [torch.cuda.Event(), torch.cuda.Event()]
 
-    def one(s):
-        for k in d_in:
-            d_in[k].copy_(host[s % 2][k], non_blocking=True)
-        p = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, s)
-        smcsd.smc_step(p, d_in["target"], d_in["draft"], d_in["draft_tokens"], lw, tok, anc, ess,
-                       res, kv=kv_s, workspace=ws, stream=stream)
-        h_tok.copy_(tok, non_blocking=True)
-        h_lw.copy_(lw, non_blocking=True)
+    def upload(s):
+        # step s's inputs into buffer s % 2, once the step that used it last is done
+        b = s % 2
+        copy_stream.wait_event(consumed[b])
+        with torch.cuda.stream(copy_stream):
+            for k in d_in[b]:
+                d_in[b][k].copy_(host[s % 2][k], non_blocking=True)
+        copied[b].record(copy_stream)
 
-    for s in range(3):
-        one(s)
+    def run(s0, n):
+        for b in range(2):
+            consumed[b].record(stream)
+        upload(s0)
+        for s in range(s0, s0 + n):
+            if s + 1 < s0 + n:
+                upload(s + 1)
+            b = s % 2
+            stream.wait_event(copied[b])
+            p = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, s)
+            smcsd.smc_step(p, d_in[b]["target"], d_in[b]["draft"], d_in[b]["draft_tokens"], lw,
+                           tok, anc, ess, res, kv=kv_s, workspace=ws, stream=stream)
+            consumed[b].record(stream)
+            h_tok.copy_(tok, non_blocking=True)
+            h_lw.copy_(lw, non_blocking=True)
+
+    run(0, 3)
     torch.cuda.synchronize()
     for k in kv:
         kv[k].copy_(kv0[k])
@@ -453,14 +474,15 @@ def run_e2e(args, w, dev, smcsd, world):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for s in range(n_steps):
-        one(s)
+    run(0, n_steps)
     e1.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1), world)
     return {"value": w.particle_tokens * n_steps * world / (ms / 1e3), "unit": "particle-tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_steps,
-            "ms_per_step": ms / n_steps}
+            "ms_per_step": ms / n_steps,
+            "overlap": "step s+1's H2D copy on a second stream during step s (double buffer)",
+            "h2d_gbs": h2d * n_steps / (ms / 1e3) / 1e9}
 
 
 # ---------------------------------------------------------------------------

@@ -361,6 +361,30 @@ __device__ __forceinline__ int block_excl_scan_i(int v, int *scratch, int *total
   *total = all;
   return base + x - v;
 }
+// Exclusive CTA-wide prefix sum of a 64-bit value; *total gets the sum.
+// scratch: kWarps words of shared memory.  All threads must call it.
+__device__ __forceinline__ long long block_excl_scan_ll(long long v, long long *scratch,
+                                                        long long *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  long long base = 0, all = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    const long long s = scratch[w];
+    if (w < warp) base += s;
+    all += s;
+  }
+  *total = all;
+  return base + x - v;
+}
+
 __device__ __forceinline__ int block_min_i(int v, int *scratch) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -126,6 +126,15 @@ struct BonusPairSum {
   unsigned long long nref, al, nal;  // -ref, alpha, -alpha in both halves
   float lb;
 
+  // For bf16 logits x and their bf16 maximum ref, with every x at or above
+  // ref - span: x - ref fails to be a float only when x and ref differ in
+  // magnitude by 2^15 or more.  When |ref| >= span * 2^-13 that can only be a
+  // tiny x, so -ref is the larger operand and the fast two-sum is exact.
+  // (Logits raised to lb contribute about e^-40 and need no exact difference.)
+  __device__ __forceinline__ static bool fast_diff_ok(float ref, float span) {
+    return fabsf(ref) >= span * 0x1p-13f;
+  }
+
   __device__ __forceinline__ bool init(float ref, float alpha, float span) {
     acc = f2dup(2.f);
     lo = 0ull;
@@ -137,14 +146,21 @@ struct BonusPairSum {
   }
 
   // ALPHA1: the caller guarantees alpha == 1, so a = d needs no product.
-  template <bool ALPHA1>
+  // FAST_DIFF: the caller guarantees fast_diff_ok(): x - ref then needs only
+  // the three-operation exact difference (fast two-sum with -ref leading).
+  template <bool ALPHA1, bool FAST_DIFF>
   __device__ __forceinline__ void add(float x0, float x1, const float *th, const float *tl) {
     constexpr float kShift = 12582912.f;  // 1.5 * 2^23: rounds 64 y into the low bits
     const unsigned long long X = f2pack(fmaxf(x0, lb), fmaxf(x1, lb));
     // d = x - ref as S + SE, exactly
     const unsigned long long S = add2(X, nref);
-    const unsigned long long BB = sub2(S, X);
-    const unsigned long long SE = add2(sub2(X, sub2(S, BB)), sub2(nref, BB));
+    unsigned long long SE;
+    if (FAST_DIFF) {
+      SE = sub2(X, sub2(S, nref));
+    } else {
+      const unsigned long long BB = sub2(S, X);
+      SE = add2(sub2(X, sub2(S, BB)), sub2(nref, BB));
+    }
     // a = alpha d as AH + AL
     unsigned long long AH = S, AL = SE;
     if (!ALPHA1) {

@@ -232,6 +232,7 @@ __device__ void kv_remap_append(const KvArgs &kv, int b, int N, const int *s_anc
                                 int n_append, const Workspace &ws, int *s_i, int *s_tail,
                                 int *s_nb, const KvScratch &sc, bool copied) {
   __shared__ int s_flag, s_top_old, s_n_freed;
+  __shared__ long long s_ll[kWarps];
   const int T = kv.T, bs = kv.block_size, P = kv.P;
   const int lo_id = b * P;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -276,29 +277,31 @@ __device__ void kv_remap_append(const KvArgs &kv, int b, int N, const int *s_anc
   if (s_flag) { fail(); return; }
 
   if (resampled) {
-    for (int i = warp; i < N; i += kWarps) {
-      for (int t = lane; t < s_nb[i]; t += 32) {
-        if (!in_pool(sc.old_t[i * T + t])) s_flag = 1;
-      }
-    }
-    __syncthreads();
-    if (s_flag) { fail(); return; }
     if (staged) {
       // net reference-count change per block in shared memory, then one pass
-      // over the pool applies it; a count reaching 0 frees the block
+      // over the pool applies it; a count reaching 0 frees the block.  Every
+      // used slot of every old table is seen here (as ov of its particle),
+      // so the pool check of the ids happens in the same pass; a slot whose
+      // value does not change is not rewritten.
       for (int i = warp; i < N; i += kWarps) {
         const int a = s_anc[i];
         const int nb_new = s_nb[a], nb_old = s_nb[i];
         for (int t = lane; t < T; t += 32) {
           const int nv = sc.old_t[a * T + t];
-          const int ov = t < nb_old ? sc.old_t[i * T + t] : -1;
-          if (t < nb_new && !(t < nb_old && ov == nv)) atomicAdd(&sc.delta[nv - lo_id], 1);
-          if (t < nb_old && !(t < nb_new && nv == ov)) atomicSub(&sc.delta[ov - lo_id], 1);
-          tables[i * T + t] = nv;
+          const int ov = sc.old_t[i * T + t];
+          const bool has_new = t < nb_new, has_old = t < nb_old;
+          if ((has_new && !in_pool(nv)) || (has_old && !in_pool(ov))) {
+            s_flag = 1;
+            continue;
+          }
+          if (has_new && !(has_old && ov == nv)) atomicAdd(&sc.delta[nv - lo_id], 1);
+          if (has_old && !(has_new && nv == ov)) atomicSub(&sc.delta[ov - lo_id], 1);
+          if (nv != ov) tables[i * T + t] = nv;
         }
       }
       for (int i = tid; i < N; i += kThreads) seq_len[i] = sc.old_l[s_anc[i]];
       __syncthreads();
+      if (s_flag) { fail(); return; }
       for (int k = tid; k < P; k += kThreads) {
         const int d = sc.delta[k];
         if (d != 0) {
@@ -309,6 +312,13 @@ __device__ void kv_remap_append(const KvArgs &kv, int b, int N, const int *s_anc
       }
       __syncthreads();
     } else {
+      for (int i = warp; i < N; i += kWarps) {
+        for (int t = lane; t < s_nb[i]; t += 32) {
+          if (!in_pool(sc.old_t[i * T + t])) s_flag = 1;
+        }
+      }
+      __syncthreads();
+      if (s_flag) { fail(); return; }
       // new references first, so no count touches 0 before every increment is in
       for (int i = warp; i < N; i += kWarps) {
         const int a = s_anc[i];
@@ -394,9 +404,14 @@ __device__ void kv_remap_append(const KvArgs &kv, int b, int N, const int *s_anc
   const long long nb2 = valid ? (static_cast<long long>(len) + n_append + bs - 1) / bs : 0;
   if (valid && nb2 > T) s_flag = 2;
   const int grow = (valid && nb2 <= T) ? static_cast<int>(nb2) - nb : 0;
-  int total_pops, n_forks;
-  const int off = block_excl_scan_i(fork + grow, s_i, &total_pops);
-  const int cidx = block_excl_scan_i(fork, s_i, &n_forks);
+  // one scan of (forks, pops) packed in 64 bits: forks high, pops low
+  long long both_total;
+  const long long both = block_excl_scan_ll((static_cast<long long>(fork) << 32) | (fork + grow),
+                                            s_ll, &both_total);
+  const int off = static_cast<int>(both & 0xffffffffll);
+  const int cidx = static_cast<int>(both >> 32);
+  const int total_pops = static_cast<int>(both_total & 0xffffffffll);
+  const int n_forks = static_cast<int>(both_total >> 32);
   const int n_freed = s_n_freed, top_old = s_top_old;
   const int top = top_old + n_freed;
   __syncthreads();
@@ -1067,16 +1082,18 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
         BonusPairSum bs;
         if (bs.init(ref, a.balpha, sa.wspan)) {
           if (sizeof(T) == 4) {
-            // fp32 logits: the general exponent only (the power-sampling case)
+            // fp32 logits: the general path only (the power-sampling case)
 #pragma unroll
             for (int k = 0; k < NW; k += 2)
-              bs.add<false>(__uint_as_float(wd[k]), __uint_as_float(wd[k + 1]), s_th, s_tl);
-          } else if (a.balpha == 1.f) {
+              bs.add<false, false>(__uint_as_float(wd[k]), __uint_as_float(wd[k + 1]), s_th, s_tl);
+          } else if (a.balpha == 1.f && BonusPairSum::fast_diff_ok(ref, sa.wspan)) {
 #pragma unroll
-            for (int k = 0; k < NW; ++k) bs.add<true>(bf16_lo(wd[k]), bf16_hi(wd[k]), s_th, s_tl);
+            for (int k = 0; k < NW; ++k)
+              bs.add<true, true>(bf16_lo(wd[k]), bf16_hi(wd[k]), s_th, s_tl);
           } else {
 #pragma unroll
-            for (int k = 0; k < NW; ++k) bs.add<false>(bf16_lo(wd[k]), bf16_hi(wd[k]), s_th, s_tl);
+            for (int k = 0; k < NW; ++k)
+              bs.add<false, false>(bf16_lo(wd[k]), bf16_hi(wd[k]), s_th, s_tl);
           }
           usum = warp_ff_sum(bs.total());
         } else {
@@ -1288,12 +1305,15 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa, i
   const float alpha = a.balpha;
   int4 *bp = a.ws.bonus_part + static_cast<size_t>(part) * sa.snch * kConsumerWarps;
   const int n_units = sa.snch * kConsumerWarps;
-  if (warp == 0) {
+  // rows of up to kThreads units: thread q holds unit q from here on
+  int4 pv_own = threadIdx.x < n_units ? bp[threadIdx.x]
+                                      : make_int4(__float_as_int(kNegInf), 0, 0, 0);
+  bool flagged = pv_own.w != 0;
+  for (int q = kThreads + threadIdx.x; q < n_units; q += kThreads) flagged |= bp[q].w != 0;
+  if (__syncthreads_or(flagged)) {
     // a unit whose max was too large for the streaming kernel's clamp (flag
-    // set) is summed here instead, in exact fixed point
-    bool any = false;
-    for (int q = lane; q < n_units; q += 32) any |= bp[q].w != 0;
-    if (__any_sync(0xffffffffu, any)) {
+    // set) is summed here instead, in exact fixed point (rare)
+    if (warp == 0) {
       for (int q = 0; q < n_units; ++q) {
         const int4 pv = bp[q];
         if (pv.w == 0) continue;
@@ -1309,15 +1329,16 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa, i
         __syncwarp();
       }
     }
+    __syncthreads();
+    if (threadIdx.x < n_units) pv_own = bp[threadIdx.x];
   }
-  __syncthreads();
   const float u = philox_uniform(a.seed, a.step, part, a.bonus_position, a.bonus_purpose);
   if (n_units <= kThreads) {
     // one unit per thread: its mass relative to the row's largest reference
     // M, a CTA-wide inclusive prefix, and the first unit whose prefix exceeds
     // u times the total
     const int q = threadIdx.x;
-    const int4 pv = q < n_units ? bp[q] : make_int4(__float_as_int(kNegInf), 0, 0, 0);
+    const int4 pv = pv_own;
     const float ref = __int_as_float(pv.x);
     const float M = block_max(ref, s_red);
     const bool ok = M > kNegInf && M < kInf;
