@@ -192,6 +192,72 @@ def score_particle(target_rows, draft_rows, tokens, alpha):
                 lse_alpha=lse_alpha, delta=delta)
 
 
+def nucleus(row, top_p, scale=1.0):
+    """The top-p (nucleus) set of one row of logits.
+
+    With pi = softmax(scale * row), token v is kept iff the probability mass
+    of the tokens strictly more likely than v is below top_p; tokens of equal
+    logit are kept or dropped together (so the set does not depend on an
+    order among ties).  Returns (kept mask, log of the kept mass, margin): the
+    margin is the distance of top_p from the nearest value that mass-above
+    takes, so a draw is flagged as a near tie when it is small.
+    """
+    row = np.asarray(row, dtype=np.float64)
+    z = scale * row
+    finite = np.isfinite(z)
+    m = np.max(z[finite])
+    pi = np.where(finite, np.exp(z - m), 0.0)
+    pi = pi / np.sum(pi)
+    vals = np.unique(row[finite])[::-1]            # distinct logits, descending
+    mass = np.array([pi[row == v].sum() for v in vals])
+    above = np.concatenate([[0.0], np.cumsum(mass)[:-1]])   # mass strictly above each value
+    keep_vals = above < top_p
+    thresh = vals[keep_vals][-1]
+    kept = finite & (row >= thresh)
+    margin = float(np.min(np.abs(np.concatenate([above, [np.sum(mass)]]) - top_p)))
+    return kept, float(np.log(np.sum(pi[kept]))), margin
+
+
+def score_particle_topp(target_rows, draft_rows, tokens, top_p):
+    """score_particle (alpha = 1) with p and q restricted to their nuclei.
+
+    Rows are the already scaled (tempered) logits.  lse_p / lse_q become the
+    log-normalisers of the renormalised nuclei (lse + log kept mass), g_p is
+    -inf for a token outside the target's nucleus, and a token outside the
+    draft's nucleus raises (bad token).  Also returns the bonus row's kept
+    mask and the smallest nucleus margin over the particle's rows.
+    """
+    k_drafts = draft_rows.shape[0]
+    v_size = target_rows.shape[1]
+    tokens = np.asarray(tokens, dtype=np.int64)
+    if (tokens < 0).any() or (tokens >= v_size).any():
+        raise OracleError(DEV_BAD_TOKEN, "drafted token outside [0, V)")
+    lse_p = np.zeros(k_drafts + 1)
+    lse_q = np.zeros(k_drafts)
+    g_p = np.zeros(k_drafts)
+    g_q = np.zeros(k_drafts)
+    margin = np.inf
+    bonus_kept = None
+    for k in range(k_drafts + 1):
+        kept, log_z, mg = nucleus(target_rows[k], top_p)
+        margin = min(margin, mg)
+        lse_p[k] = row_logsumexp(target_rows[k]) + log_z
+        if k == k_drafts:
+            bonus_kept = kept
+        else:
+            g_p[k] = target_rows[k, tokens[k]] if kept[tokens[k]] else -np.inf
+    for k in range(k_drafts):
+        kept, log_z, mg = nucleus(draft_rows[k], top_p)
+        margin = min(margin, mg)
+        if not kept[tokens[k]]:
+            raise OracleError(DEV_BAD_TOKEN, "drafted token outside the draft's nucleus")
+        lse_q[k] = row_logsumexp(draft_rows[k]) + log_z
+        g_q[k] = draft_rows[k, tokens[k]]
+    delta = np.sum((g_p - lse_p[:k_drafts]) - (g_q - lse_q))
+    return dict(lse_p=lse_p, g_p=g_p, lse_q=lse_q, g_q=g_q, lse_alpha=lse_p[k_drafts],
+                delta=delta, bonus_kept=bonus_kept, margin=margin)
+
+
 def temperature_scale(temperature):
     """The multiplier 1/T that a temperature T applies to every logit.
 
@@ -213,7 +279,7 @@ def effective_alpha(alpha, temperature=1.0):
 
 def smc_step(target, draft, draft_tokens, log_weights, *, alpha=1.0,
              ess_frac=0.5, seed=0, step=0, dtype=None, temperature=1.0,
-             log_potential=None):
+             log_potential=None, top_p=1.0):
     """One SMC-SD step over B prompts x N particles (no KV state).
 
     target: [B, N, K+1, V], draft: [B, N, K, V], either already fp64 or, when
@@ -228,6 +294,13 @@ def smc_step(target, draft, draft_tokens, log_weights, *, alpha=1.0,
     extensions the pages name without fixing (the SMC page's section 3 on
     unnormalised targets such as rewards and constraints; the SpS notes'
     evaluation at nucleus and temperature settings).
+    top_p < 1 (alpha must be 1): p and q are each restricted to their nucleus
+    (see ``nucleus``) and renormalised, after the temperature; the bonus is
+    drawn from the target's nucleus.  A drafted token outside the draft's
+    nucleus could not have been drawn and is an error (bad token); one
+    outside the target's nucleus gives the particle weight 0.  The returned
+    dict then also holds topp_margin[B, N]: the smallest nucleus margin of the
+    particle's rows.
 
     Returns a dict with
       delta[B,N], log_weights_pre[B,N] (after reweighting), log_weights[B,N]
@@ -239,6 +312,12 @@ def smc_step(target, draft, draft_tokens, log_weights, *, alpha=1.0,
     alpha = float(np.float32(alpha))
     scale = temperature_scale(temperature)
     bonus_alpha = effective_alpha(alpha, temperature)
+    top_p = float(np.float32(top_p))
+    if not 0.0 < top_p <= 1.0:
+        raise ValueError("top_p must be in (0, 1]")
+    use_topp = top_p < 1.0
+    if use_topp and alpha != 1.0:
+        raise ValueError("top_p < 1 needs alpha == 1")
     big_b, n_part, k1, v_size = target.shape
     k_drafts = k1 - 1
     draft_tokens = np.asarray(draft_tokens, dtype=np.int64)
@@ -247,7 +326,7 @@ def smc_step(target, draft, draft_tokens, log_weights, *, alpha=1.0,
         lse_q=np.zeros((big_b, n_part, k_drafts)), g_q=np.zeros((big_b, n_part, k_drafts)),
         lse_alpha=np.zeros((big_b, n_part)), delta=np.zeros((big_b, n_part)),
         bonus=np.zeros((big_b, n_part), dtype=np.int64),
-        bonus_margin=np.zeros((big_b, n_part)))
+        bonus_margin=np.zeros((big_b, n_part)), topp_margin=np.full((big_b, n_part), np.inf))
     for b in range(big_b):
         for n in range(n_part):
             t_rows = widen(target[b, n], dtype) if dtype else target[b, n]
@@ -255,12 +334,18 @@ def smc_step(target, draft, draft_tokens, log_weights, *, alpha=1.0,
             if scale != 1.0:
                 t_rows = np.asarray(t_rows, dtype=np.float64) * scale
                 d_rows = np.asarray(d_rows, dtype=np.float64) * scale
-            s = score_particle(t_rows, d_rows, draft_tokens[b, n], alpha)
-            for key in ("lse_p", "g_p", "lse_q", "g_q", "lse_alpha", "delta"):
-                out[key][b, n] = s[key]
             u = philox.uniform(seed, step, b * n_part + n, k_drafts, philox.BONUS)
             raw = widen(target[b, n, k_drafts], dtype) if dtype else target[b, n, k_drafts]
-            tok, margin = inverse_cdf(bonus_weights(raw, bonus_alpha), u)
+            if use_topp:
+                s = score_particle_topp(t_rows, d_rows, draft_tokens[b, n], top_p)
+                out["topp_margin"][b, n] = s["margin"]
+                w = np.where(s["bonus_kept"], bonus_weights(raw, bonus_alpha), 0.0)
+            else:
+                s = score_particle(t_rows, d_rows, draft_tokens[b, n], alpha)
+                w = bonus_weights(raw, bonus_alpha)
+            for key in ("lse_p", "g_p", "lse_q", "g_q", "lse_alpha", "delta"):
+                out[key][b, n] = s[key]
+            tok, margin = inverse_cdf(w, u)
             out["bonus"][b, n] = tok
             out["bonus_margin"][b, n] = margin
     if log_potential is not None:

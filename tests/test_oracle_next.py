@@ -1,5 +1,6 @@
 """Pins of the oracle's extensions beyond the basic step (CPU): temperature,
-per-particle log-potentials, the draft-side sampler and KV-usage accounting."""
+per-particle log-potentials, top-p nuclei, the draft-side sampler and KV-usage
+accounting."""
 import numpy as np
 import pytest
 from scipy.special import logsumexp, softmax
@@ -191,3 +192,85 @@ def test_usage_counts_the_blocks_with_live_references():
             assert used[b] == int((np.asarray(refcount[b * pool:(b + 1) * pool]) > 0).sum())
             assert unshared[b] == sum(-(-int(seq_len[b][i]) // bs) for i in range(n))
             assert used[b] <= unshared[b]
+
+
+# ---------------------------------------------------------------------------
+# top-p (nucleus)
+# ---------------------------------------------------------------------------
+def _nucleus_by_sorting(row, top_p):
+    """Independent restatement: sort tokens by probability, walk down in
+    groups of equal logit, keep a group while the mass before it is below
+    top_p."""
+    pi = softmax(row)
+    order = np.argsort(-row, kind="stable")
+    kept = np.zeros(len(row), dtype=bool)
+    before = 0.0
+    i = 0
+    while i < len(order):
+        j = i
+        while j < len(order) and row[order[j]] == row[order[i]]:
+            j += 1
+        if before >= top_p:
+            break
+        kept[order[i:j]] = True
+        before += pi[order[i:j]].sum()
+        i = j
+    return kept
+
+
+@pytest.mark.parametrize("top_p", [0.3, 0.8, 0.95])
+def test_nucleus_matches_sorting(top_p):
+    rng = np.random.default_rng(int(top_p * 100))
+    for _ in range(40):
+        row = np.round(rng.normal(0, 2, 50) * 4) / 4  # coarse values: many ties
+        kept, log_z, _ = smc.nucleus(row, top_p)
+        assert np.array_equal(kept, _nucleus_by_sorting(row, top_p))
+        assert abs(log_z - np.log(softmax(row)[kept].sum())) < 1e-12
+
+
+def test_tiny_top_p_keeps_only_the_most_likely_tokens():
+    row = np.array([0.5, 2.0, -1.0, 2.0, 1.9])
+    kept, log_z, _ = smc.nucleus(row, 1e-6)
+    assert list(np.flatnonzero(kept)) == [1, 3]
+    assert abs(log_z - np.log(2 * softmax(row)[1])) < 1e-12
+
+
+def test_top_p_weight_expectation_closed_form():
+    """E_{x ~ q_top}[exp(delta)] = prod_k p_top,k(S_q,k): with both sides
+    truncated to nuclei, the weights average to the target nucleus mass that
+    the draft's nucleus covers.  Enumerates V^K."""
+    import itertools
+    rng = np.random.default_rng(12)
+    k, v, top_p = 2, 6, 0.8
+    target = rng.normal(0, 1.5, (k + 1, v))
+    draft = rng.normal(0, 1.5, (k, v))
+    total = 0.0
+    q_sets = [smc.nucleus(draft[i], top_p)[0] for i in range(k)]
+    for x in itertools.product(range(v), repeat=k):
+        if not all(q_sets[i][x[i]] for i in range(k)):
+            continue
+        s = smc.score_particle_topp(target, draft, np.array(x), top_p)
+        logq = sum(draft[i, x[i]] - s["lse_q"][i] for i in range(k))
+        total += np.exp(logq + s["delta"])
+    expect = 1.0
+    for i in range(k):
+        kept_p, log_zp, _ = smc.nucleus(target[i], top_p)
+        pt = np.where(kept_p, softmax(target[i]), 0.0) / np.exp(log_zp)
+        expect *= pt[q_sets[i]].sum()
+    assert abs(total - expect) < 1e-12
+
+
+def test_top_p_step_bonus_stays_in_the_nucleus_and_bad_drafts_raise():
+    rng = np.random.default_rng(13)
+    target, draft, _ = _inputs(rng, big_b=1, n=6, k=2, v=40)
+    toks = np.zeros((1, 6, 2), dtype=np.int64)
+    for n in range(6):
+        for i in range(2):
+            toks[0, n, i] = int(np.argmax(draft[0, n, i]))  # always in q's nucleus
+    out = smc.smc_step(target, draft, toks, np.zeros((1, 6)), top_p=0.7, seed=3, step=1)
+    for n in range(6):
+        kept, _, _ = smc.nucleus(target[0, n, 2], 0.7)
+        assert kept[out["bonus"][0, n]]
+    toks[0, 0, 1] = int(np.argmin(draft[0, 0, 1]))
+    with pytest.raises(OracleError):
+        smc.smc_step(target, draft, toks, np.zeros((1, 6)), top_p=0.7)
