@@ -402,6 +402,32 @@ def run_extensions(w, dev, smcsd, ring, reps=50):
     res["step_ex_temperature_potential"] = {"ms_per_step": ms_step,
                                             "particle_tokens_per_s": w.particle_tokens / (ms_step / 1e3),
                                             "temperature": 0.8, "steps": n}
+    # top-p 0.9: drafted tokens are each draft row's argmax, always inside its nucleus
+    ring_tp = [dict(r, draft_tokens=r["draft"].float().argmax(-1).to(torch.int32).contiguous())
+               for r in ring]
+    for k in kv:
+        kv[k].copy_(make_kv_state(w.B, w.N, w.prefix, w.block_size, T, P, device=dev)[k])
+    lw.zero_()
+
+    def tp_step(s):
+        p = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, s)
+        smcsd.smc_step_ex(p, ring_tp[s % 2]["target"], ring_tp[s % 2]["draft"],
+                          ring_tp[s % 2]["draft_tokens"], lw, outs["tok"], outs["anc"], outs["ess"],
+                          outs["res"], kv=kv_s, workspace=ws2, top_p=0.9)
+    for s in range(3):
+        tp_step(s)
+    torch.cuda.synchronize()
+    n_tp = 16
+    e0.record()
+    for s in range(n_tp):
+        tp_step(3 + s)
+    e1.record()
+    torch.cuda.synchronize()
+    assert smcsd.smc_device_status(ws2, clear=True) == 0
+    ms_tp = e0.elapsed_time(e1) / n_tp
+    res["step_ex_top_p"] = {"ms_per_step": ms_tp, "top_p": 0.9, "steps": n_tp,
+                            "particle_tokens_per_s": w.particle_tokens / (ms_tp / 1e3),
+                            "note": "the nucleus reads every row twice more (radix select)"}
     return res
 
 

@@ -196,7 +196,9 @@ typedef struct {
                                   softmax(l / T) wherever they are scored or
                                   sampled; every logit is multiplied by the
                                   fp32 value of 1/T                             */
-  int32_t reserved;            /* must be 0                                     */
+  float top_p;                 /* nucleus mass in (0, 1] (1 = none); below 1
+                                  needs p->alpha == 1                           */
+  int32_t reserved[2];         /* must be 0                                     */
 } smc_step_opts;
 
 /* smc_step with per-call settings ([SMC] section 3, "通用性扩展": the target
@@ -204,9 +206,15 @@ typedef struct {
  * temperature and nucleus settings).  opts may be NULL (= smc_step).  With
  * temperature T and multiplier s = fl32(1/T): every lse and gathered logit
  * is taken of s*l, the bonus is drawn from softmax(fl32(alpha*s) * l_K), and
- * the drafted tokens are taken to come from the tempered draft.  With a
- * log-potential phi: delta += phi[b, n] before normalisation.  Everything
- * else, and every argument, is as for smc_step. */
+ * the drafted tokens are taken to come from the tempered draft.  With top_p
+ * < 1: each row's distribution pi = softmax(s*l) is restricted to its
+ * nucleus (token v kept iff the mass of tokens with a larger logit is below
+ * top_p; equal logits go together) and renormalised; a drafted token outside
+ * the target's nucleus gives its particle weight 0, one outside the draft's
+ * nucleus sets SMC_DEV_BAD_TOKEN; the bonus is drawn from the target's
+ * nucleus.  Each row is then read twice more (four times for fp32 logits).
+ * With a log-potential phi: delta += phi[b, n] before normalisation.
+ * Everything else, and every argument, is as for smc_step. */
 int32_t smc_step_ex(const smc_params *p, const smc_step_opts *opts,
                     const void *target_logits, const void *draft_logits,
                     const int32_t *draft_tokens, float *log_weights, int32_t *tokens_out,

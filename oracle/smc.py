@@ -208,8 +208,9 @@ def nucleus(row, top_p, scale=1.0):
     m = np.max(z[finite])
     pi = np.where(finite, np.exp(z - m), 0.0)
     pi = pi / np.sum(pi)
-    vals = np.unique(row[finite])[::-1]            # distinct logits, descending
-    mass = np.array([pi[row == v].sum() for v in vals])
+    vals, inv = np.unique(row[finite], return_inverse=True)   # distinct logits, ascending
+    mass = np.bincount(inv, weights=pi[finite], minlength=len(vals))
+    vals, mass = vals[::-1], mass[::-1]                          # descending
     above = np.concatenate([[0.0], np.cumsum(mass)[:-1]])   # mass strictly above each value
     keep_vals = above < top_p
     thresh = vals[keep_vals][-1]

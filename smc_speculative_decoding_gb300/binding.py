@@ -48,7 +48,7 @@ class smc_kv(ctypes.Structure):
 
 class smc_step_opts(ctypes.Structure):
     _fields_ = [("log_potential", ctypes.c_void_p), ("temperature", ctypes.c_float),
-                ("reserved", ctypes.c_int32)]
+                ("top_p", ctypes.c_float), ("reserved", ctypes.c_int32 * 2)]
 
 
 _lib = None
@@ -229,14 +229,15 @@ def smc_step(params, target_logits, draft_logits, draft_tokens, log_weights, tok
 
 def smc_step_ex(params, target_logits, draft_logits, draft_tokens, log_weights, tokens_out,
                 ancestors, ess, resampled, kv=None, workspace=None, stream=None,
-                temperature=1.0, log_potential=None):
-    """smc_step with a temperature and an optional [B, N] fp32 CUDA tensor of
-    per-particle log-potential increments (smc_step_ex in smcsd.h)."""
+                temperature=1.0, log_potential=None, top_p=1.0):
+    """smc_step with a temperature, a top-p nucleus and an optional [B, N]
+    fp32 CUDA tensor of per-particle log-potential increments (smc_step_ex in
+    smcsd.h)."""
     B, N, K, V = params.B, params.N, params.K, params.V
     ld = _logit_dtype(params)
     opts = smc_step_opts(
         _ptr(log_potential, "log_potential", torch.float32, B * N) if log_potential is not None
-        else None, float(temperature), 0)
+        else None, float(temperature), float(top_p))
     args = [
         _ptr(target_logits, "target_logits", ld, B * N * (K + 1) * V),
         _ptr(draft_logits, "draft_logits", ld, B * N * K * V),

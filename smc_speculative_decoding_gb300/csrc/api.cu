@@ -94,6 +94,7 @@ static Shape to_shape(const smc_params *p) {
   s.seed = p->seed; s.step = p->step;
   s.tscale = 1.f;
   s.potential = nullptr;
+  s.top_p = 1.f;
   return s;
 }
 
@@ -196,7 +197,10 @@ static int32_t step_impl(const smc_params *p, const smc_step_opts *opts,
   }
   Shape s = to_shape(p);
   if (opts) {
-    if (opts->reserved != 0) return SMC_ERR_ARG;
+    if (opts->reserved[0] != 0 || opts->reserved[1] != 0) return SMC_ERR_ARG;
+    if (!(opts->top_p > 0.f && opts->top_p <= 1.f)) return SMC_ERR_ARG;
+    if (opts->top_p < 1.f && p->alpha != 1.f) return SMC_ERR_ARG;
+    s.top_p = opts->top_p;
     const float t = opts->temperature;
     if (!(std::isfinite(t) && t > 0.f)) return SMC_ERR_ARG;
     s.tscale = 1.f / t;

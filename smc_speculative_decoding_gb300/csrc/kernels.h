@@ -53,6 +53,7 @@ struct Shape {
   uint32_t step;
   float tscale;              // 1/T of a temperature T (1: none)
   const float *potential;    // [B*N] log-potential increments, or null
+  float top_p;               // nucleus mass (1: none)
 };
 
 // Elements per chunk of the row reductions for a dtype.

@@ -1608,6 +1608,154 @@ static cudaError_t launch_tail(const StepArgs &a, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, tail_kernel, a, staged);
 }
 
+// ---------------------------------------------------------------------------
+// Top-p (nucleus) restriction of every row, after the row combine: one CTA
+// per row.  With pi = softmax(s l), a token is kept iff the mass of tokens
+// strictly more likely than it is below top_p (tokens of equal logit go
+// together), so the kept set is {l >= l*} for a threshold logit l*.  l* is
+// found by a radix select over order-preserving keys of the logits, 8 bits
+// per pass (2 passes for bf16, 4 for fp32): each pass builds a 256-bin
+// histogram of count and fixed-point mass (units of 2^-40, summed exactly)
+// of the keys under the prefix chosen so far, and keeps the lowest
+// non-empty bin whose mass above stays below top_p times the row's total.
+// Then log(kept / total) is added to the row's log-sum-exp; a drafted token
+// outside the target's nucleus gets logit -inf (weight 0), one outside the
+// draft's nucleus is reported (SMC_DEV_BAD_TOKEN: it could not have been
+// drawn); the bonus row's token is redrawn by inverse CDF over the kept
+// tokens in exact fixed point (units of 2^-38 of the row's largest weight).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) topp_kernel(const StepArgs a, float top_p) {
+  using Tr = LogitTraits<T>;
+  constexpr int kPasses = sizeof(T) == 4 ? 4 : 2;
+  constexpr int kShift = 12;  // bonus weights in units of 2^-(kFixBits - kShift)
+  __shared__ unsigned long long s_mass[256];
+  __shared__ unsigned s_cnt[256];
+  __shared__ float2 s_tab[64];
+  __shared__ long long s_ll[kWarps];
+  __shared__ int s_i[2 * kWarps];
+  __shared__ float s_red[2 * kWarps];
+  __shared__ unsigned long long s_above;
+  __shared__ uint32_t s_prefix;
+  const int tid = threadIdx.x;
+  const int row = blockIdx.x;
+  const int rpp = 2 * a.K + 1;
+  const int part = row / rpp, j = row - part * rpp;
+  const char *rowp = row_base<T>(a, row);
+  const float lse = a.ws.results[row].lse;
+  const float l2s = a.tscale * kLog2e, l2lse = lse * kLog2e;
+  stage_exp2_table(s_tab);
+
+  unsigned long long total = 0;
+  uint32_t prefix = 0;
+  unsigned long long above = 0;  // mass of the keys above the current prefix range
+  for (int pass = 0; pass < kPasses; ++pass) {
+    const int shift = 32 - 8 * (pass + 1);
+    s_mass[tid] = 0ull;
+    s_cnt[tid] = 0u;
+    __syncthreads();
+    for (int64_t i = tid; i < a.V; i += kThreads) {
+      const float x = Tr::scalar(rowp, i);
+      const uint32_t key = order_key(x);
+      if (pass > 0 && (key >> (shift + 8)) != prefix) continue;
+      const float pm = fast_exp2(fmaf(x, l2s, -l2lse));  // pi, about 1e-7 relative
+      const unsigned long long fx =
+          x > kNegInf ? static_cast<unsigned long long>(pm * 0x1p40f) : 0ull;
+      atomicAdd(&s_mass[(key >> shift) & 255u], fx);
+      atomicAdd(&s_cnt[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    // bins in descending key order: mass strictly above bin b's range
+    const int b = 255 - tid;  // thread tid looks at bin 255 - tid (descending)
+    long long tot_ll;
+    const long long excl = block_excl_scan_ll(static_cast<long long>(s_mass[b]), s_ll, &tot_ll);
+    if (pass == 0) total = static_cast<unsigned long long>(tot_ll);
+    const unsigned long long limit =
+        static_cast<unsigned long long>(static_cast<double>(top_p) * static_cast<double>(total));
+    const unsigned long long a_b = above + static_cast<unsigned long long>(excl);
+    const bool cand = s_cnt[b] > 0u && a_b < limit;
+    // the lowest candidate bin = the largest tid among candidates
+    const int best = -block_min_i(cand ? -tid : 1, s_i);
+    if (tid == best) {
+      s_prefix = (prefix << 8) | static_cast<uint32_t>(b);
+      s_above = a_b;
+    }
+    __syncthreads();
+    if (best < 0) break;  // no candidate: an empty or non-finite row (reported elsewhere)
+    prefix = s_prefix;
+    above = s_above;
+    if (pass == kPasses - 1) {
+      // kept mass: everything above the last bin, plus the bin itself
+      if (tid == best) s_above = a_b + s_mass[b];
+      __syncthreads();
+      above = s_above;
+    }
+    __syncthreads();
+  }
+  const int kbits = 8 * kPasses;
+  auto kept = [&](float x) { return (order_key(x) >> (32 - kbits)) >= prefix; };
+  const float log_z = (total > 0 && above > 0)
+      ? static_cast<float>(log(static_cast<double>(above) / static_cast<double>(total)))
+      : 0.f;
+  if (j != a.K) {
+    if (tid == 0) {
+      RowResult r = a.ws.results[row];
+      const int tok = a.tokens[static_cast<size_t>(part) * a.K + (j < a.K ? j : j - a.K - 1)];
+      if (tok >= 0 && tok < a.V && !kept(Tr::scalar(rowp, tok))) {
+        if (j < a.K) r.g = kNegInf;                      // outside the target's nucleus
+        else raise_status(a.ws.status, SMC_DEV_BAD_TOKEN);  // could not have been drafted
+      }
+      r.lse += log_z;
+      a.ws.results[row] = r;
+    }
+    return;
+  }
+  // ---- bonus row: inverse CDF over the kept tokens, exact fixed point ------
+  float mx = kNegInf;
+  for (int64_t i = tid; i < a.V; i += kThreads) mx = fmaxf(mx, Tr::scalar(rowp, i));
+  const float M = block_max(mx, s_red);
+  const int seg = static_cast<int>((a.V + kThreads - 1) / kThreads);
+  const int64_t beg = static_cast<int64_t>(tid) * seg;
+  const int64_t end = min(static_cast<int64_t>(a.V), beg + seg);
+  long long part_sum = 0;
+  if (M > kNegInf && M < -kNegInf) {
+    for (int64_t i = beg; i < end; ++i) {
+      const float x = Tr::scalar(rowp, i);
+      if (kept(x)) part_sum += weight_fixed(x, M, a.balpha, s_tab) >> kShift;
+    }
+  }
+  long long total_w;
+  const long long excl_w = block_excl_scan_ll(part_sum, s_ll, &total_w);
+  const float u = philox_uniform(a.seed, a.step, part, a.K, SMC_PURPOSE_BONUS);
+  const unsigned long long u24 = static_cast<unsigned long long>(u * 16777216.f);
+  // floor(total * u), exactly: u = u24 / 2^24
+  const long long target = static_cast<long long>(
+      __umul64hi(static_cast<unsigned long long>(total_w), u24 << 40));
+  int cand = 0x7fffffff;
+  if (total_w > 0 && part_sum > 0 && excl_w <= target && excl_w + part_sum > target) {
+    long long run = excl_w;
+    for (int64_t i = beg; i < end; ++i) {
+      const float x = Tr::scalar(rowp, i);
+      if (!kept(x)) continue;
+      run += weight_fixed(x, M, a.balpha, s_tab) >> kShift;
+      if (run > target) { cand = static_cast<int>(i); break; }
+    }
+  }
+  const int tok = block_min_i(cand, s_i);
+  if (tid == 0) {
+    RowResult r = a.ws.results[row];
+    r.lse += log_z;
+    r.lse_alpha += log_z;
+    r.tok = tok == 0x7fffffff ? -1 : tok;
+    a.ws.results[row] = r;
+  }
+}
+
 // The row pass (streaming or per-chunk kernel, then the row combine).
 static cudaError_t launch_rows(const StepArgs &a, int dtype, long long rows, cudaStream_t stream) {
   const int esz = dtype == SMC_BF16 ? 2 : 4;
@@ -1659,6 +1807,12 @@ cudaError_t launch_step_rows(const Shape &s, int mode, const void *target, const
   const long long rows = static_cast<long long>(s.B) * s.N * (2 * s.K + 1);
   cudaError_t e = launch_rows(a, s.dtype, rows, stream);
   if (e != cudaSuccess) return e;
+  if (s.top_p < 1.f) {
+    if (s.dtype == SMC_BF16) topp_kernel<bf16_tag><<<static_cast<unsigned>(rows), kThreads, 0, stream>>>(a, s.top_p);
+    else topp_kernel<float><<<static_cast<unsigned>(rows), kThreads, 0, stream>>>(a, s.top_p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   e = launch_tail(a, stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

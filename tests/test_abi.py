@@ -118,10 +118,17 @@ def test_host_validation_without_gpu(lib):
                                    1 << 30, None) == -1
     assert lib.smc_device_status(None, 0, None, None) == -1
     # smc_step_ex: temperature must be positive and finite, reserved zero
-    for t, r in ((0.0, 0), (-1.0, 0), (float("inf"), 0), (float("nan"), 0), (1e-45, 0), (1.0, 3)):
-        opts = bd.smc_step_opts(None, t, r)
+    for t, tp, r in ((0.0, 1.0, 0), (-1.0, 1.0, 0), (float("inf"), 1.0, 0),
+                     (float("nan"), 1.0, 0), (1e-45, 1.0, 0), (1.0, 1.0, 3), (1.0, 0.0, 0),
+                     (1.0, 1.5, 0), (1.0, float("nan"), 0)):
+        opts = bd.smc_step_opts(None, t, tp, (ctypes.c_int32 * 2)(r, 0))
         assert lib.smc_step_ex(ctypes.byref(good), ctypes.byref(opts), *[fake] * 8, None, ws,
                                need, None) == -1
+    # top_p < 1 needs alpha == 1
+    power = P(2, 4, 3, 64, 0, 4.0, 0.5, 0, 0)
+    opts = bd.smc_step_opts(None, 1.0, 0.9, (ctypes.c_int32 * 2)(0, 0))
+    assert lib.smc_step_ex(ctypes.byref(power), ctypes.byref(opts), *[fake] * 8, None, ws,
+                           need, None) == -1
     # smc_draft_sample: a position below 0 or a missing output
     assert lib.smc_draft_sample(ctypes.byref(good), fake, -1, fake, ws, need, None) == -1
     assert lib.smc_draft_sample(ctypes.byref(good), fake, 0, None, ws, need, None) == -1

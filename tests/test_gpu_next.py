@@ -1,6 +1,6 @@
 """GPU parity of the step's extensions against the CPU oracle: smc_step_ex
-(temperature, per-particle log-potentials), smc_draft_sample (the draft-side
-sampler) and smc_kv_usage (KV-cache accounting).  Same bar as the basic
+(temperature, per-particle log-potentials, top-p nuclei), smc_draft_sample
+(the draft-side sampler) and smc_kv_usage (KV-cache accounting).  Same bar as the basic
 step: integer outputs exact except draws the oracle flags as near ties,
 log-weights within 1e-4 (fp32 logits) or 2e-3 (bf16 logits)."""
 import numpy as np
@@ -9,6 +9,7 @@ import torch
 
 import smc_speculative_decoding_gb300 as smcsd
 from smc_speculative_decoding_gb300.workloads import WORKLOADS, make_step_inputs, to_numpy_logits
+from smc_speculative_decoding_gb300.workloads import torch_dtype
 from oracle import smc as osmc, kv as okv
 
 from gpu_harness import lockstep, StepRunner, kv_to_numpy
@@ -127,3 +128,56 @@ def test_kv_usage_matches_oracle():
         ref_used, ref_unshared = okv.usage(st["tables"], st["seq_len"], w.block_size)
         assert np.array_equal(used.cpu().numpy(), ref_used)
         assert np.array_equal(unshared.cpu().numpy(), ref_unshared)
+
+
+def _nucleus_tokens(w, top_p, temperature, seed):
+    """Replaces each step's drafted tokens by tokens drawn from the draft
+    row's renormalised nucleus (computed by the oracle, on the CPU): inputs
+    that a top-p draft could have produced."""
+    rng = np.random.default_rng(seed)
+    s = osmc.temperature_scale(temperature)
+
+    def fn(inp, step):
+        d = to_numpy_logits(inp["draft"])
+        toks = np.zeros((w.B, w.N, w.K), dtype=np.int32)
+        for b in range(w.B):
+            for n in range(w.N):
+                rows = osmc.widen(d[b, n], w.dtype) * s
+                for k in range(w.K):
+                    kept, _, _ = osmc.nucleus(rows[k], top_p)
+                    pk = np.where(kept, np.exp(rows[k] - rows[k][kept].max()), 0.0)
+                    toks[b, n, k] = rng.choice(len(pk), p=pk / pk.sum())
+        inp["draft_tokens"].copy_(torch.from_numpy(toks).to(inp["draft_tokens"].device))
+    return fn
+
+
+@pytest.mark.parametrize("name,B,top_p,temperature", [("tiny_v64", 2, 0.8, 1.0),
+                                                      ("single_prompt_v32000", 2, 0.9, 1.0),
+                                                      ("single_prompt_v32000", 2, 0.5, 0.7)])
+def test_step_ex_top_p_matches_oracle(name, B, top_p, temperature):
+    w = WORKLOADS[name].with_(B=B)
+    steps = 4 if w.V > 1000 else 10
+    t = lockstep(w, steps, seed=23, with_kv=True, temperature=temperature, top_p=top_p,
+                 tokens_fn=_nucleus_tokens(w, top_p, temperature, 23))
+    print(f"{name} top_p={top_p} T={temperature}: draws={t.draws} flagged={t.flagged} "
+          f"mismatched={t.mismatched}")
+
+
+def test_step_ex_top_p_serving_size_and_unaligned():
+    w = WORKLOADS["batched_serving_v128256"].with_(B=2, N=8)
+    lockstep(w, 2, seed=29, with_kv=True, top_p=0.95,
+             tokens_fn=_nucleus_tokens(w, 0.95, 1.0, 29))
+    w = WORKLOADS["single_prompt_v32000"].with_(V=1001, B=2)
+    lockstep(w, 3, seed=30, with_kv=False, top_p=0.6, tokens_fn=_nucleus_tokens(w, 0.6, 1.0, 30))
+
+
+def test_step_ex_top_p_draft_outside_nucleus_is_reported():
+    w = WORKLOADS["tiny_v64"].with_(B=1)
+    inp = make_step_inputs(w, 3, device="cuda")
+    d = to_numpy_logits(inp["draft"])[0, 0, 0].astype(np.float64)
+    kept, _, _ = osmc.nucleus(d, 0.3)
+    inp["draft_tokens"][0, 0, 0] = int(np.flatnonzero(~kept)[0])
+    r = StepRunner(w, seed=3, with_kv=False, temperature=1.0)
+    r.run(inp, 0, top_p=0.3)
+    torch.cuda.synchronize()
+    assert "bad_token" in smcsd.status_names(r.status())
