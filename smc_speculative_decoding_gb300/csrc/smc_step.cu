@@ -1609,100 +1609,212 @@ static cudaError_t launch_tail(const StepArgs &a, cudaStream_t stream) {
 }
 
 // ---------------------------------------------------------------------------
-// Top-p (nucleus) restriction of every row, after the row combine: one CTA
-// per row.  With pi = softmax(s l), a token is kept iff the mass of tokens
-// strictly more likely than it is below top_p (tokens of equal logit go
-// together), so the kept set is {l >= l*} for a threshold logit l*.  l* is
-// found by a radix select over order-preserving keys of the logits, 8 bits
-// per pass (2 passes for bf16, 4 for fp32): each pass builds a 256-bin
-// histogram of count and fixed-point mass (units of 2^-40, summed exactly)
-// of the keys under the prefix chosen so far, and keeps the lowest
+// Top-p (nucleus) restriction of every row, after the row combine: one CTA of
+// kToppThreads threads per row, two CTAs per SM (so that the rows being
+// re-read stay in L2).  With pi = softmax(s l), a token is kept iff the mass
+// of the tokens strictly more likely than it is below top_p (tokens of equal
+// logit go together), so the kept set is {l >= l*} for a threshold logit l*.
+//
+// l* is found by a radix select over order-preserving 32-bit keys of the
+// logits: a first digit of 12 bits (4096 bins: sign, exponent and three
+// mantissa bits, so that no bin holds more than a few per cent of a row of
+// Gaussian-like logits), then 4 bits for bf16 (whose keys have 16 significant
+// bits) or 10 + 10 for fp32.  Each pass builds a histogram of the mass of the
+// keys under the prefix chosen so far, in fixed point: every finite logit
+// adds floor(pi 2^40) + 1 (the +1 marks the bin non-empty), as a 32-bit
+// shared atomic on the low word whose carry-out goes to the high word, so
+// the sums are exact and order-independent.  The pass keeps the lowest
 // non-empty bin whose mass above stays below top_p times the row's total.
+// The first pass streams the row from HBM; the later ones read it again
+// (from L2) and touch only the logits under the prefix.
+//
 // Then log(kept / total) is added to the row's log-sum-exp; a drafted token
 // outside the target's nucleus gets logit -inf (weight 0), one outside the
 // draft's nucleus is reported (SMC_DEV_BAD_TOKEN: it could not have been
-// drawn); the bonus row's token is redrawn by inverse CDF over the kept
-// tokens in exact fixed point (units of 2^-38 of the row's largest weight).
+// drawn).  The bonus row's token is redrawn by inverse CDF over the kept
+// tokens in exact fixed point (units of 2^-38 of the row's largest weight):
+// the row is cut into up to kToppEntries runs of 32G consecutive 16-byte
+// groups; one coalesced pass sums the kept weights of each run, a scan over
+// the runs finds the one the draw lands in, and a block-wide scan over that
+// run's logits finds the token.
 // ---------------------------------------------------------------------------
+constexpr int kToppThreads = 512;
+constexpr int kToppWarps = kToppThreads / 32;
+constexpr int kToppBins = 4096;     // bins of the first radix digit (12 bits)
+constexpr int kToppEntries = 4096;  // runs of a bonus row summed in the first pass
+constexpr int kToppUnroll = 4;      // 16-byte groups in flight per thread
+
 __device__ __forceinline__ uint32_t order_key(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kThreads) topp_kernel(const StepArgs a, float top_p) {
+// Digits of the radix select for the logit type T.
+template <typename T> struct ToppDigits {
+  static constexpr int kPasses = sizeof(T) == 4 ? 3 : 2;
+  static constexpr int kKeyBits = sizeof(T) == 4 ? 32 : 16;  // significant key bits
+  __device__ __forceinline__ static int width(int pass) {
+    return pass == 0 ? 12 : (sizeof(T) == 4 ? 10 : 4);
+  }
+  static constexpr uint32_t kNegInfWord = sizeof(T) == 4 ? 0xff800000u : 0xff80ff80u;
+};
+
+// Group g of a row: logits [g E, g E + E) as one 16-byte word (E = 8 bf16 or
+// 4 fp32); logits at or past V read as -inf.  VEC: rows are 16-byte aligned
+// and V is a multiple of E, so the group is one vector load.
+template <typename T, bool VEC>
+__device__ __forceinline__ uint4 topp_group(const char *rowp, int64_t g, int64_t V) {
+  if (VEC) return ld_stream16(rowp + g * 16);
+  uint32_t w[4];
+  if (sizeof(T) == 4) {
+    const float *r = reinterpret_cast<const float *>(rowp);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int64_t i = g * 4 + e;
+      w[e] = i < V ? __float_as_uint(__ldg(r + i)) : 0xff800000u;
+    }
+  } else {
+    const unsigned short *r = reinterpret_cast<const unsigned short *>(rowp);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int64_t i = g * 8 + 2 * e;
+      const uint32_t lo = i < V ? __ldg(r + i) : 0xff80u;
+      const uint32_t hi = i + 1 < V ? __ldg(r + i + 1) : 0xff80u;
+      w[e] = lo | (hi << 16);
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kToppThreads, 2) topp_kernel(const StepArgs a, float top_p) {
   using Tr = LogitTraits<T>;
-  constexpr int kPasses = sizeof(T) == 4 ? 4 : 2;
+  using Dg = ToppDigits<T>;
+  constexpr int E = Tr::kPerVec;
   constexpr int kShift = 12;  // bonus weights in units of 2^-(kFixBits - kShift)
-  __shared__ unsigned long long s_mass[256];
-  __shared__ unsigned s_cnt[256];
+  // the histogram (low words, then high words); a bonus row's run sums later
+  __shared__ __align__(16) unsigned long long s_buf[kToppBins];
   __shared__ float2 s_tab[64];
-  __shared__ long long s_ll[kWarps];
-  __shared__ int s_i[2 * kWarps];
-  __shared__ float s_red[2 * kWarps];
-  __shared__ unsigned long long s_above;
+  __shared__ unsigned long long s_u64[kToppWarps];
+  __shared__ int s_i[kToppWarps];
+  __shared__ float s_f[kToppWarps];
+  __shared__ unsigned long long s_above, s_kept, s_base;
   __shared__ uint32_t s_prefix;
-  const int tid = threadIdx.x;
+  __shared__ int s_sel;
+  __shared__ long long s_tok;
+  uint32_t *const s_lo = reinterpret_cast<uint32_t *>(s_buf);
+  uint32_t *const s_hi = s_lo + kToppBins;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int row = blockIdx.x;
   const int rpp = 2 * a.K + 1;
   const int part = row / rpp, j = row - part * rpp;
+  const bool bonus = j == a.K;
   const char *rowp = row_base<T>(a, row);
+  const int64_t V = a.V;
+  const int64_t ng = (V + E - 1) / E;
   const float lse = a.ws.results[row].lse;
   const float l2s = a.tscale * kLog2e, l2lse = lse * kLog2e;
-  stage_exp2_table(s_tab);
+  const uint4 pad = make_uint4(Dg::kNegInfWord, Dg::kNegInfWord, Dg::kNegInfWord, Dg::kNegInfWord);
+  if (bonus) stage_exp2_table(s_tab);
 
-  unsigned long long total = 0;
+  // adds floor(pi 2^40) + 1 for the finite logit x to bin b
+  auto add_mass = [&](uint32_t b, float x) {
+    const float pm = fminf(fast_exp2(fmaf(x, l2s, -l2lse)), 2.f);  // pi, about 1e-7 relative
+    const unsigned long long fx = __float2ull_rz(pm * 0x1p40f) + 1ull;
+    const uint32_t lo = static_cast<uint32_t>(fx);
+    const uint32_t old = atomicAdd(&s_lo[b], lo);
+    const uint32_t hi = static_cast<uint32_t>(fx >> 32) + (old + lo < lo ? 1u : 0u);
+    if (hi) atomicAdd(&s_hi[b], hi);
+  };
+
+  float mx = kNegInf;
   uint32_t prefix = 0;
-  unsigned long long above = 0;  // mass of the keys above the current prefix range
-  for (int pass = 0; pass < kPasses; ++pass) {
-    const int shift = 32 - 8 * (pass + 1);
-    s_mass[tid] = 0ull;
-    s_cnt[tid] = 0u;
+  int consumed = 0;           // key bits fixed so far
+  unsigned long long total = 0, above = 0;
+  bool ok = true;
+#pragma unroll 1
+  for (int pass = 0; pass < Dg::kPasses; ++pass) {
+    const int width = Dg::width(pass);
+    const int nb = 1 << width;
+    const int shift = 32 - consumed - width;
+    for (int b = tid; b < nb; b += kToppThreads) s_lo[b] = s_hi[b] = 0u;
     __syncthreads();
-    for (int64_t i = tid; i < a.V; i += kThreads) {
-      const float x = Tr::scalar(rowp, i);
-      const uint32_t key = order_key(x);
-      if (pass > 0 && (key >> (shift + 8)) != prefix) continue;
-      const float pm = fast_exp2(fmaf(x, l2s, -l2lse));  // pi, about 1e-7 relative
-      const unsigned long long fx =
-          x > kNegInf ? static_cast<unsigned long long>(pm * 0x1p40f) : 0ull;
-      atomicAdd(&s_mass[(key >> shift) & 255u], fx);
-      atomicAdd(&s_cnt[(key >> shift) & 255u], 1u);
+    for (int64_t g0 = tid; g0 < ng; g0 += static_cast<int64_t>(kToppThreads) * kToppUnroll) {
+      uint4 v[kToppUnroll];
+#pragma unroll
+      for (int u = 0; u < kToppUnroll; ++u) {
+        const int64_t g = g0 + static_cast<int64_t>(u) * kToppThreads;
+        v[u] = g < ng ? topp_group<T, VEC>(rowp, g, V) : pad;
+      }
+#pragma unroll
+      for (int u = 0; u < kToppUnroll; ++u) {
+        if (pass == 0) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const float x = Tr::at(v[u], e);
+            mx = fmaxf(mx, x);
+            if (x > kNegInf && x < -kNegInf) add_mass(order_key(x) >> shift, x);
+          }
+        } else {
+          // only the logits under the prefix: usually none of a group's
+          uint32_t m = 0;
+#pragma unroll
+          for (int e = 0; e < E; ++e)
+            if ((order_key(Tr::at(v[u], e)) >> (shift + width)) == prefix) m |= 1u << e;
+          while (m) {
+            const int e = __ffs(m) - 1;
+            m &= m - 1;
+            const float x = Tr::at(v[u], e);
+            if (x > kNegInf && x < -kNegInf)
+              add_mass((order_key(x) >> shift) & static_cast<uint32_t>(nb - 1), x);
+          }
+        }
+      }
     }
     __syncthreads();
-    // bins in descending key order: mass strictly above bin b's range
-    const int b = 255 - tid;  // thread tid looks at bin 255 - tid (descending)
-    long long tot_ll;
-    const long long excl = block_excl_scan_ll(static_cast<long long>(s_mass[b]), s_ll, &tot_ll);
-    if (pass == 0) total = static_cast<unsigned long long>(tot_ll);
+    // bins in descending key order: thread tid takes positions
+    // [tid c, tid c + c), position d being bin nb - 1 - d
+    const int c = (nb + kToppThreads - 1) / kToppThreads;
+    unsigned long long sum = 0;
+    for (int i = 0; i < c; ++i) {
+      const int d = tid * c + i;
+      if (d < nb) sum += (static_cast<unsigned long long>(s_hi[nb - 1 - d]) << 32) | s_lo[nb - 1 - d];
+    }
+    unsigned long long tot;
+    const unsigned long long excl = block_excl_scan_u64<kToppThreads>(sum, s_u64, &tot);
+    if (pass == 0) total = tot;
     const unsigned long long limit =
         static_cast<unsigned long long>(static_cast<double>(top_p) * static_cast<double>(total));
-    const unsigned long long a_b = above + static_cast<unsigned long long>(excl);
-    const bool cand = s_cnt[b] > 0u && a_b < limit;
-    // the lowest candidate bin = the largest tid among candidates
-    const int best = -block_min_i(cand ? -tid : 1, s_i);
-    if (tid == best) {
-      s_prefix = (prefix << 8) | static_cast<uint32_t>(b);
-      s_above = a_b;
+    // the lowest candidate: a non-empty bin whose mass above is below limit
+    int best = -1;
+    unsigned long long best_a = 0, best_v = 0, run = above + excl;
+    for (int i = 0; i < c; ++i) {
+      const int d = tid * c + i;
+      if (d >= nb) break;
+      const unsigned long long m =
+          (static_cast<unsigned long long>(s_hi[nb - 1 - d]) << 32) | s_lo[nb - 1 - d];
+      if (m > 0 && run < limit) { best = d; best_a = run; best_v = m; }
+      run += m;
+    }
+    const int bd = block_max_int<kToppThreads>(best, s_i);
+    if (bd >= 0 && best == bd) {
+      s_prefix = (prefix << width) | static_cast<uint32_t>(nb - 1 - bd);
+      s_above = best_a;
+      s_kept = best_a + best_v;
     }
     __syncthreads();
-    if (best < 0) break;  // no candidate: an empty or non-finite row (reported elsewhere)
+    if (bd < 0) { ok = false; break; }  // an empty or non-finite row (reported elsewhere)
     prefix = s_prefix;
     above = s_above;
-    if (pass == kPasses - 1) {
-      // kept mass: everything above the last bin, plus the bin itself
-      if (tid == best) s_above = a_b + s_mass[b];
-      __syncthreads();
-      above = s_above;
-    }
-    __syncthreads();
+    consumed += width;
   }
-  const int kbits = 8 * kPasses;
-  auto kept = [&](float x) { return (order_key(x) >> (32 - kbits)) >= prefix; };
-  const float log_z = (total > 0 && above > 0)
-      ? static_cast<float>(log(static_cast<double>(above) / static_cast<double>(total)))
+  // kept: logits at or above the threshold key (nothing when the select failed)
+  const unsigned long long kept_mass = ok ? s_kept : 0ull;
+  auto kept = [&](float x) { return ok && (order_key(x) >> (32 - Dg::kKeyBits)) >= prefix; };
+  const float log_z = (total > 0 && kept_mass > 0)
+      ? static_cast<float>(log(static_cast<double>(kept_mass) / static_cast<double>(total)))
       : 0.f;
-  if (j != a.K) {
+  if (!bonus) {
     if (tid == 0) {
       RowResult r = a.ws.results[row];
       const int tok = a.tokens[static_cast<size_t>(part) * a.K + (j < a.K ? j : j - a.K - 1)];
@@ -1715,43 +1827,102 @@ __global__ void __launch_bounds__(kThreads) topp_kernel(const StepArgs a, float 
     }
     return;
   }
+
   // ---- bonus row: inverse CDF over the kept tokens, exact fixed point ------
-  float mx = kNegInf;
-  for (int64_t i = tid; i < a.V; i += kThreads) mx = fmaxf(mx, Tr::scalar(rowp, i));
-  const float M = block_max(mx, s_red);
-  const int seg = static_cast<int>((a.V + kThreads - 1) / kThreads);
-  const int64_t beg = static_cast<int64_t>(tid) * seg;
-  const int64_t end = min(static_cast<int64_t>(a.V), beg + seg);
-  long long part_sum = 0;
-  if (M > kNegInf && M < -kNegInf) {
-    for (int64_t i = beg; i < end; ++i) {
-      const float x = Tr::scalar(rowp, i);
-      if (kept(x)) part_sum += weight_fixed(x, M, a.balpha, s_tab) >> kShift;
+  const float M = block_max_nt<kToppThreads>(mx, s_f);
+  const bool live = ok && M > kNegInf && M < -kNegInf;
+  auto weight = [&](float x) -> unsigned long long {
+    return static_cast<unsigned long long>(weight_fixed(x, M, a.balpha, s_tab) >> kShift);
+  };
+  // runs of gpe = 32 G consecutive groups, at most kToppEntries of them; the
+  // 32 groups one warp reads at a time always lie in one run
+  const int64_t G = (ng + 32ll * kToppEntries - 1) / (32ll * kToppEntries);
+  const int64_t gpe = 32 * G;
+  const int ne = static_cast<int>((ng + gpe - 1) / gpe);
+  unsigned long long *const s_run = s_buf;
+  for (int e = tid; e < ne; e += kToppThreads) s_run[e] = 0ull;
+  if (tid == 0) { s_sel = -1; s_tok = -1; }
+  __syncthreads();
+  if (live) {
+    // a warp-uniform trip count: the warp sums below take every lane
+    for (int64_t w0 = tid - lane; w0 < ng; w0 += static_cast<int64_t>(kToppThreads) * kToppUnroll) {
+      const int64_t g0 = w0 + lane;
+      uint4 v[kToppUnroll];
+#pragma unroll
+      for (int u = 0; u < kToppUnroll; ++u) {
+        const int64_t g = g0 + static_cast<int64_t>(u) * kToppThreads;
+        v[u] = g < ng ? topp_group<T, VEC>(rowp, g, V) : pad;
+      }
+#pragma unroll
+      for (int u = 0; u < kToppUnroll; ++u) {
+        const int64_t g = g0 + static_cast<int64_t>(u) * kToppThreads;
+        uint32_t m = 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+          if (kept(Tr::at(v[u], e))) m |= 1u << e;
+        unsigned long long acc = 0;
+        while (m) {
+          const int e = __ffs(m) - 1;
+          m &= m - 1;
+          acc += weight(Tr::at(v[u], e));
+        }
+        acc = warp_sum_u64(acc);
+        // g - lane is the warp's first group, a multiple of 32
+        if (lane == 0 && g - lane < ng && acc) atomicAdd(&s_run[(g - lane) / gpe], acc);
+      }
     }
   }
-  long long total_w;
-  const long long excl_w = block_excl_scan_ll(part_sum, s_ll, &total_w);
+  __syncthreads();
+  // the run the draw lands in
+  const int c = (ne + kToppThreads - 1) / kToppThreads;
+  unsigned long long sum = 0;
+  for (int i = 0; i < c; ++i) {
+    const int d = tid * c + i;
+    if (d < ne) sum += s_run[d];
+  }
+  unsigned long long total_w;
+  const unsigned long long excl_w = block_excl_scan_u64<kToppThreads>(sum, s_u64, &total_w);
   const float u = philox_uniform(a.seed, a.step, part, a.K, SMC_PURPOSE_BONUS);
   const unsigned long long u24 = static_cast<unsigned long long>(u * 16777216.f);
   // floor(total * u), exactly: u = u24 / 2^24
-  const long long target = static_cast<long long>(
-      __umul64hi(static_cast<unsigned long long>(total_w), u24 << 40));
-  int cand = 0x7fffffff;
-  if (total_w > 0 && part_sum > 0 && excl_w <= target && excl_w + part_sum > target) {
-    long long run = excl_w;
-    for (int64_t i = beg; i < end; ++i) {
-      const float x = Tr::scalar(rowp, i);
-      if (!kept(x)) continue;
-      run += weight_fixed(x, M, a.balpha, s_tab) >> kShift;
-      if (run > target) { cand = static_cast<int>(i); break; }
+  const unsigned long long target = __umul64hi(total_w, u24 << 40);
+  if (total_w > 0) {
+    unsigned long long run = excl_w;
+    for (int i = 0; i < c; ++i) {
+      const int d = tid * c + i;
+      if (d >= ne) break;
+      const unsigned long long w = s_run[d];
+      if (w > 0 && run <= target && target < run + w) { s_sel = d; s_base = run; }
+      run += w;
     }
   }
-  const int tok = block_min_i(cand, s_i);
+  __syncthreads();
+  const int sel = s_sel;
+  if (sel >= 0) {
+    // the token within the run, by a block-wide scan in index order
+    unsigned long long rem = target - s_base;
+    const int64_t i0 = static_cast<int64_t>(sel) * gpe * E;
+    const int64_t i1 = min(V, i0 + gpe * E);
+    for (int64_t base = i0; base < i1; base += kToppThreads) {
+      const int64_t i = base + tid;
+      unsigned long long w = 0;
+      if (i < i1) {
+        const float x = Tr::scalar(rowp, i);
+        if (kept(x)) w = weight(x);
+      }
+      unsigned long long tot;
+      const unsigned long long ex = block_excl_scan_u64<kToppThreads>(w, s_u64, &tot);
+      if (w > 0 && ex <= rem && rem < ex + w) s_tok = i;
+      if (rem < tot) break;  // the same for every thread
+      rem -= tot;
+    }
+  }
+  __syncthreads();
   if (tid == 0) {
     RowResult r = a.ws.results[row];
     r.lse += log_z;
     r.lse_alpha += log_z;
-    r.tok = tok == 0x7fffffff ? -1 : tok;
+    r.tok = static_cast<int>(s_tok);
     a.ws.results[row] = r;
   }
 }
@@ -1808,8 +1979,17 @@ cudaError_t launch_step_rows(const Shape &s, int mode, const void *target, const
   cudaError_t e = launch_rows(a, s.dtype, rows, stream);
   if (e != cudaSuccess) return e;
   if (s.top_p < 1.f) {
-    if (s.dtype == SMC_BF16) topp_kernel<bf16_tag><<<static_cast<unsigned>(rows), kThreads, 0, stream>>>(a, s.top_p);
-    else topp_kernel<float><<<static_cast<unsigned>(rows), kThreads, 0, stream>>>(a, s.top_p);
+    const int esz = s.dtype == SMC_BF16 ? 2 : 4;
+    const bool vec = aligned16(a.target) && aligned16(a.draft) &&
+                     (static_cast<long long>(a.V) * esz) % 16 == 0;
+    const dim3 g(static_cast<unsigned>(rows)), blk(kToppThreads);
+    if (s.dtype == SMC_BF16) {
+      if (vec) topp_kernel<bf16_tag, true><<<g, blk, 0, stream>>>(a, s.top_p);
+      else topp_kernel<bf16_tag, false><<<g, blk, 0, stream>>>(a, s.top_p);
+    } else {
+      if (vec) topp_kernel<float, true><<<g, blk, 0, stream>>>(a, s.top_p);
+      else topp_kernel<float, false><<<g, blk, 0, stream>>>(a, s.top_p);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

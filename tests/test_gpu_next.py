@@ -171,6 +171,30 @@ def test_step_ex_top_p_serving_size_and_unaligned():
     lockstep(w, 3, seed=30, with_kv=False, top_p=0.6, tokens_fn=_nucleus_tokens(w, 0.6, 1.0, 30))
 
 
+@pytest.mark.parametrize("dtype,V", [("f32", 600_001), ("bf16", 1_100_000)])
+def test_step_ex_top_p_long_rows(dtype, V):
+    """Rows long enough that a bonus row's runs span several warp reads, and
+    fp32 keys that take all three radix digits."""
+    w = WORKLOADS["single_prompt_v32000"].with_(B=1, N=2, K=2, V=V, dtype=dtype)
+    t = lockstep(w, 1, seed=41, with_kv=False, top_p=0.85,
+                 tokens_fn=_nucleus_tokens(w, 0.85, 1.0, 41))
+    print(f"{dtype} V={V}: draws={t.draws} flagged={t.flagged} mismatched={t.mismatched}")
+
+
+def test_step_ex_top_p_tied_logits():
+    """Logits rounded to multiples of 1/4, so that the nucleus boundary cuts
+    through large groups of equal logits (kept or dropped together)."""
+    w = WORKLOADS["single_prompt_v32000"].with_(B=2)
+    nucleus_fn = _nucleus_tokens(w, 0.7, 1.0, 43)
+
+    def fn(inp, step):
+        for key in ("target", "draft"):
+            inp[key].copy_((inp[key].float() * 4).round() / 4)
+        nucleus_fn(inp, step)
+    t = lockstep(w, 3, seed=43, with_kv=True, top_p=0.7, tokens_fn=fn)
+    print(f"tied: draws={t.draws} flagged={t.flagged} mismatched={t.mismatched}")
+
+
 def test_step_ex_top_p_draft_outside_nucleus_is_reported():
     w = WORKLOADS["tiny_v64"].with_(B=1)
     inp = make_step_inputs(w, 3, device="cuda")
