@@ -143,6 +143,25 @@ __device__ __forceinline__ void ff_accum(ff &acc, ff t) {
 }
 __device__ __forceinline__ ff ff_norm(ff a) { return fast_two_sum(a.hi, a.lo); }
 
+// round(f) to the nearest integer, ties away from zero, for |f| < 2^62
+// (larger magnitudes, infinities and NaN are not handled), decoded from the
+// float's sign, exponent and significand on the integer pipes: this GPU runs
+// 64-bit float-to-integer conversions on its narrow fp64 pipe.
+__device__ __forceinline__ long long float_to_ll_rn(float f) {
+  const uint32_t b = __float_as_uint(f);
+  const int e = min(static_cast<int>((b >> 23) & 0xffu) - 150, 38);  // |f| = m 2^e
+  const uint32_t m = (b & 0x7fffffu) | 0x800000u;
+  unsigned long long mag;
+  if (e >= 0) {
+    mag = static_cast<unsigned long long>(m) << e;
+  } else {
+    const int s = -e;  // the last kept bit is bit s of m; add half of it
+    mag = s > 24 ? 0ull : static_cast<unsigned long long>((m + (1u << (s - 1))) >> s);
+  }
+  const long long v = static_cast<long long>(mag);
+  return (b >> 31) ? -v : v;
+}
+
 __device__ __forceinline__ void stage_exp2_table(float2 *s_tab) {
   if (threadIdx.x < 64) s_tab[threadIdx.x] = kExp2Tab[threadIdx.x];
 }
@@ -440,6 +459,32 @@ __device__ __forceinline__ int block_max_int(int v, int *scratch) {
   if (lane == 0) scratch[warp] = v;
   __syncthreads();
   v = lane < NT / 32 ? scratch[lane] : -0x7fffffff - 1;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+template <int NT>
+__device__ __forceinline__ uint32_t block_min_u32(uint32_t v, int *scratch) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) scratch[warp] = static_cast<int>(v);
+  __syncthreads();
+  v = lane < NT / 32 ? static_cast<uint32_t>(scratch[lane]) : 0xffffffffu;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+template <int NT>
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, int *scratch) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) scratch[warp] = static_cast<int>(v);
+  __syncthreads();
+  v = lane < NT / 32 ? static_cast<uint32_t>(scratch[lane]) : 0u;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;

@@ -102,7 +102,7 @@ __device__ __forceinline__ long long weight_fixed(float x, float ref, float alph
   const float2 tv = tab[ki & 63];             // 2^(j/64), float-float
   const float lo = fmaf(tv.x, p, fmaf(tv.y, p, tv.y));
   const float sc = __int_as_float(((ki >> 6) + kFixBits + 127) << 23);  // 2^(n + kFixBits)
-  const long long v = __float2ll_rn(tv.x * sc) + __float2ll_rn(lo * sc);
+  const long long v = float_to_ll_rn(tv.x * sc) + float_to_ll_rn(lo * sc);
   return live ? v : 0ll;
 }
 
@@ -235,7 +235,7 @@ __device__ __forceinline__ long long warp_incl_scan_ll(long long v) {
 // A non-negative float-float value times 2^kFixBits, rounded to an integer.
 __device__ __forceinline__ long long ff_to_fixed(ff a) {
   const float sc = __int_as_float((kFixBits + 127) << 23);
-  return __float2ll_rn(a.hi * sc) + __float2ll_rn(a.lo * sc);
+  return float_to_ll_rn(a.hi * sc) + float_to_ll_rn(a.lo * sc);
 }
 // A fixed-point integer (units of 2^-kFixBits) as a float-float value.
 __device__ __forceinline__ ff fixed_to_ff(long long v) {

@@ -1610,46 +1610,86 @@ static cudaError_t launch_tail(const StepArgs &a, cudaStream_t stream) {
 
 // ---------------------------------------------------------------------------
 // Top-p (nucleus) restriction of every row, after the row combine: one CTA of
-// kToppThreads threads per row, two CTAs per SM (so that the rows being
-// re-read stay in L2).  With pi = softmax(s l), a token is kept iff the mass
-// of the tokens strictly more likely than it is below top_p (tokens of equal
-// logit go together), so the kept set is {l >= l*} for a threshold logit l*.
+// kToppThreads threads per row, two CTAs per SM (so that the rows being read
+// a second time are still in L2).  With pi = softmax(s l), a token is kept
+// iff the mass of the tokens strictly more likely than it is below top_p
+// (tokens of equal logit go together), so the kept set is {l >= l*} for a
+// threshold logit l*, found as an order-preserving 32-bit key v* of l*.
 //
-// l* is found by a radix select over order-preserving 32-bit keys of the
-// logits: a first digit of 12 bits (4096 bins: sign, exponent and three
-// mantissa bits, so that no bin holds more than a few per cent of a row of
-// Gaussian-like logits), then 4 bits for bf16 (whose keys have 16 significant
-// bits) or 10 + 10 for fp32.  Each pass builds a histogram of the mass of the
-// keys under the prefix chosen so far, in fixed point: every finite logit
-// adds floor(pi 2^40) + 1 (the +1 marks the bin non-empty), as a 32-bit
-// shared atomic on the low word whose carry-out goes to the high word, so
-// the sums are exact and order-independent.  The pass keeps the lowest
-// non-empty bin whose mass above stays below top_p times the row's total.
-// The first pass streams the row from HBM; the later ones read it again
-// (from L2) and touch only the logits under the prefix.
+// Main path (mass bins).  The first pass streams the row from HBM and puts
+// every logit into one of kToppMassBins bins by rn(-8 log2 pi): bins of 1/8
+// of a binary order of pi, in decreasing order of the logit (the last bin
+// also takes everything below 2^-48).  Within its bin, a logit's mass is
+// quantised relative to the bin's top, q = rn(pi 2^(b/8) 2^qb) with pi
+// 2^(b/8) in [2^-1/16, 2^1/16] (a relative error below 2^-(qb+1) / 0.95),
+// and added as a 32-bit shared atomic to a (bin, lane) cell: each lane owns
+// a column of cells, so a warp's adds never share a bank, and qb is chosen
+// so that no cell can overflow.  A bin's mass is then (sum q) 2^(26 - b/8)
+// in units of 2^-(26 + qb), exact integers throughout, so every sum is
+// order-independent.  A scan over the bins finds the threshold bin b*: the
+// lowest non-empty bin whose mass above stays below top_p times the total.
+// The second pass (from L2) copies the keys and q of b*'s logits into
+// shared memory, and a radix select over those keys, 8 bits at a time from
+// their highest differing bit, finds v* inside b*.  A threshold bin with
+// more than kToppListCap logits, or rows long enough that qb would fall
+// below 18, take the exact path instead.
 //
-// Then log(kept / total) is added to the row's log-sum-exp; a drafted token
-// outside the target's nucleus gets logit -inf (weight 0), one outside the
-// draft's nucleus is reported (SMC_DEV_BAD_TOKEN: it could not have been
-// drawn).  The bonus row's token is redrawn by inverse CDF over the kept
-// tokens in exact fixed point (units of 2^-38 of the row's largest weight):
-// the row is cut into up to kToppEntries runs of 32G consecutive 16-byte
-// groups; one coalesced pass sums the kept weights of each run, a scan over
-// the runs finds the one the draw lands in, and a block-wide scan over that
-// run's logits finds the token.
+// Exact path (radix select over the whole row).  Radix digits of 12 bits
+// then 4 (bf16) or 10 + 10 (fp32) over the keys; each pass histograms the
+// fixed-point mass round(pi 2^40) (lowest bit set, so a bin holding a finite
+// logit reads non-empty) of the logits under the prefix chosen so far, as a
+// 32-bit shared atomic on a low word whose carry goes to a high word.
+//
+// Either way log(kept / total) is added to the row's log-sum-exp; a drafted
+// token outside the target's nucleus gets logit -inf (weight 0), one outside
+// the draft's nucleus is reported (SMC_DEV_BAD_TOKEN: it could not have
+// been drawn).  The bonus row's token is redrawn by inverse CDF over the
+// kept tokens in exact integer weights (the quantised masses, or
+// exp(s (l - max)) in units of 2^-38 on the exact path): the row is cut
+// into up to kToppEntries runs of 32G consecutive 16-byte groups; one
+// coalesced pass sums the kept weights of each run, a scan over the runs
+// finds the one the draw lands in, and a block-wide scan over that run's
+// logits finds the token.
 // ---------------------------------------------------------------------------
 constexpr int kToppThreads = 512;
 constexpr int kToppWarps = kToppThreads / 32;
-constexpr int kToppBins = 4096;     // bins of the first radix digit (12 bits)
-constexpr int kToppEntries = 4096;  // runs of a bonus row summed in the first pass
-constexpr int kToppUnroll = 4;      // 16-byte groups in flight per thread
+constexpr int kToppUnroll = 4;       // 16-byte groups in flight per thread
+constexpr int kToppMassBins = 384;   // mass bins: pi from 1 down to 2^-48
+constexpr int kToppListCap = 2048;   // logits of the threshold bin held in shared memory
+constexpr int kToppBins = 4096;      // exact path: bins of the first radix digit (12 bits)
+constexpr int kToppEntries = 4096;   // runs of a bonus row summed in the first pass
+
+// 2^(26 - j/8) rounded to an integer, j = 0..7: the fractional part of a
+// mass bin's scale.
+__device__ const unsigned kToppFrac[8] = {67108864u, 61539100u, 56431603u, 51748008u,
+                                          47453133u, 43514715u, 39903169u, 36591368u};
+
+struct ToppScalars {
+  unsigned long long above, kept, base, bin_above, in_above, in_kept;
+  long long tok;
+  uint32_t prefix;
+  int sel, n;
+};
+struct ToppShared {
+  uint32_t cell[kToppMassBins * 32];  // mass cells; then the list, or the exact path's buffers
+  float2 tab[64];
+  uint32_t hq[256], hc[256];
+  unsigned long long u64s[kToppWarps];
+  int ints[kToppWarps];
+  float fl[kToppWarps];
+  unsigned frac[8];
+  ToppScalars s;
+};
+static_assert(sizeof(uint32_t) * kToppMassBins * 32 >= sizeof(unsigned long long) * kToppBins,
+              "the exact path's histogram and runs fit in the cells");
+static_assert(kToppMassBins * 32 >= 2 * kToppListCap, "the list fits in the cells");
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Digits of the radix select for the logit type T.
+// Digits of the exact path's radix select for the logit type T.
 template <typename T> struct ToppDigits {
   static constexpr int kPasses = sizeof(T) == 4 ? 3 : 2;
   static constexpr int kKeyBits = sizeof(T) == 4 ? 32 : 16;  // significant key bits
@@ -1686,41 +1726,314 @@ __device__ __forceinline__ uint4 topp_group(const char *rowp, int64_t g, int64_t
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Calls f(x) for every logit of the row, kToppUnroll groups in flight per
+// thread; thread t takes the groups g = t mod kToppThreads.
+template <typename T, bool VEC, typename F>
+__device__ __forceinline__ void topp_for_each(const char *rowp, int64_t V, F f) {
+  using Tr = LogitTraits<T>;
+  constexpr int E = Tr::kPerVec;
+  const int64_t ng = (V + E - 1) / E;
+  const uint4 pad = make_uint4(ToppDigits<T>::kNegInfWord, ToppDigits<T>::kNegInfWord,
+                               ToppDigits<T>::kNegInfWord, ToppDigits<T>::kNegInfWord);
+  for (int64_t g0 = threadIdx.x; g0 < ng; g0 += static_cast<int64_t>(kToppThreads) * kToppUnroll) {
+    uint4 v[kToppUnroll];
+#pragma unroll
+    for (int u = 0; u < kToppUnroll; ++u) {
+      const int64_t g = g0 + static_cast<int64_t>(u) * kToppThreads;
+      v[u] = g < ng ? topp_group<T, VEC>(rowp, g, V) : pad;
+    }
+#pragma unroll
+    for (int u = 0; u < kToppUnroll; ++u) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) f(Tr::at(v[u], e));
+    }
+  }
+}
+
+// The bonus row's draw: the first kept token whose inclusive prefix of
+// weight(x) (exact integers) exceeds floor(u total); -1 with no weight.
+template <typename T, bool VEC, typename KeptF, typename WeightF>
+__device__ long long topp_bonus_draw(const StepArgs &a, int part, const char *rowp, KeptF kept,
+                                     WeightF weight, ToppShared &sh) {
+  using Tr = LogitTraits<T>;
+  constexpr int E = Tr::kPerVec;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t V = a.V;
+  const int64_t ng = (V + E - 1) / E;
+  const uint4 pad = make_uint4(ToppDigits<T>::kNegInfWord, ToppDigits<T>::kNegInfWord,
+                               ToppDigits<T>::kNegInfWord, ToppDigits<T>::kNegInfWord);
+  // runs of gpe = 32 G consecutive groups, at most kToppEntries of them; the
+  // 32 groups one warp reads at a time always lie in one run
+  const int64_t G = (ng + 32ll * kToppEntries - 1) / (32ll * kToppEntries);
+  const int64_t gpe = 32 * G;
+  const int ne = static_cast<int>((ng + gpe - 1) / gpe);
+  unsigned long long *const s_run = reinterpret_cast<unsigned long long *>(sh.cell);
+  __syncthreads();  // the cells' previous contents are no longer read
+  for (int e = tid; e < ne; e += kToppThreads) s_run[e] = 0ull;
+  if (tid == 0) { sh.s.sel = -1; sh.s.tok = -1; }
+  __syncthreads();
+  // a warp-uniform trip count: the warp sums below take every lane
+  for (int64_t w0 = tid - lane; w0 < ng; w0 += static_cast<int64_t>(kToppThreads) * kToppUnroll) {
+    const int64_t g0 = w0 + lane;
+    uint4 v[kToppUnroll];
+#pragma unroll
+    for (int u = 0; u < kToppUnroll; ++u) {
+      const int64_t g = g0 + static_cast<int64_t>(u) * kToppThreads;
+      v[u] = g < ng ? topp_group<T, VEC>(rowp, g, V) : pad;
+    }
+#pragma unroll
+    for (int u = 0; u < kToppUnroll; ++u) {
+      const int64_t g = g0 + static_cast<int64_t>(u) * kToppThreads;
+      uint32_t m = 0;
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        if (kept(Tr::at(v[u], e))) m |= 1u << e;
+      unsigned long long acc = 0;
+      while (m) {
+        const int e = __ffs(m) - 1;
+        m &= m - 1;
+        acc += weight(Tr::at(v[u], e));
+      }
+      acc = warp_sum_u64(acc);
+      // g - lane is the warp's first group, a multiple of 32
+      if (lane == 0 && g - lane < ng && acc) atomicAdd(&s_run[(g - lane) / gpe], acc);
+    }
+  }
+  __syncthreads();
+  // the run the draw lands in
+  const int c = (ne + kToppThreads - 1) / kToppThreads;
+  unsigned long long sum = 0;
+  for (int i = 0; i < c; ++i) {
+    const int d = tid * c + i;
+    if (d < ne) sum += s_run[d];
+  }
+  unsigned long long total_w;
+  const unsigned long long excl_w = block_excl_scan_u64<kToppThreads>(sum, sh.u64s, &total_w);
+  const float u = philox_uniform(a.seed, a.step, part, a.K, SMC_PURPOSE_BONUS);
+  const unsigned long long u24 = static_cast<unsigned long long>(u * 16777216.f);
+  // floor(total * u), exactly: u = u24 / 2^24
+  const unsigned long long target = __umul64hi(total_w, u24 << 40);
+  if (total_w > 0) {
+    unsigned long long run = excl_w;
+    for (int i = 0; i < c; ++i) {
+      const int d = tid * c + i;
+      if (d >= ne) break;
+      const unsigned long long w = s_run[d];
+      if (w > 0 && run <= target && target < run + w) { sh.s.sel = d; sh.s.base = run; }
+      run += w;
+    }
+  }
+  __syncthreads();
+  const int sel = sh.s.sel;
+  if (sel >= 0) {
+    // the token within the run, by a block-wide scan in index order
+    unsigned long long rem = target - sh.s.base;
+    const int64_t i0 = static_cast<int64_t>(sel) * gpe * E;
+    const int64_t i1 = min(V, i0 + gpe * E);
+    for (int64_t base = i0; base < i1; base += kToppThreads) {
+      const int64_t i = base + tid;
+      unsigned long long w = 0;
+      if (i < i1) {
+        const float x = Tr::scalar(rowp, i);
+        if (kept(x)) w = weight(x);
+      }
+      unsigned long long tot;
+      const unsigned long long ex = block_excl_scan_u64<kToppThreads>(w, sh.u64s, &tot);
+      if (w > 0 && ex <= rem && rem < ex + w) sh.s.tok = i;
+      if (rem < tot) break;  // the same for every thread
+      rem -= tot;
+    }
+  }
+  __syncthreads();
+  return sh.s.tok;
+}
+
+// Writes a row's nucleus result: the log kept mass on its log-sum-exp(s), and
+// for a drafted position the check of its token.
+template <typename T, typename KeptF>
+__device__ __forceinline__ void topp_finish_fast(const StepArgs &a, int row, int part, int j,
+                                                 const char *rowp, float log_z, KeptF kept) {
+  using Tr = LogitTraits<T>;
+  RowResult r = a.ws.results[row];
+  const int tok = a.tokens[static_cast<size_t>(part) * a.K + (j < a.K ? j : j - a.K - 1)];
+  if (tok >= 0 && tok < a.V && !kept(Tr::scalar(rowp, tok))) {
+    if (j < a.K) r.g = kNegInf;                         // outside the target's nucleus
+    else raise_status(a.ws.status, SMC_DEV_BAD_TOKEN);  // could not have been drafted
+  }
+  r.lse += log_z;
+  a.ws.results[row] = r;
+}
+
+// Main path; returns false (and writes nothing) when the row needs the exact
+// path.  The return value is the same in every thread.
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(kToppThreads, 2) topp_kernel(const StepArgs a, float top_p) {
+__device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb, ToppShared &sh) {
+  constexpr int NT = kToppThreads;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int row = blockIdx.x;
+  const int rpp = 2 * a.K + 1;
+  const int part = row / rpp, j = row - part * rpp;
+  const char *rowp = row_base<T>(a, row);
+  const float lse = a.ws.results[row].lse;
+  const float l2s = a.tscale * kLog2e, l2lse = lse * kLog2e;
+  const float qsc = __int_as_float((qb + 127) << 23);  // 2^qb
+  uint32_t *const cell = sh.cell;
+  for (int i = tid; i < kToppMassBins * 32; i += NT) cell[i] = 0u;
+  if (tid < 8) sh.frac[tid] = kToppFrac[tid];
+  if (tid == 0) sh.s.n = 0;
+  __syncthreads();
+  // the mass bin of x (and log2 pi, and the rounding register for it)
+  auto mass_bin = [&](float x, float &y, float &t) -> uint32_t {
+    y = __fmaf_rn(x, l2s, -l2lse);               // log2 pi
+    t = __fmaf_rn(y, -8.f, 12582912.f);          // 1.5 2^23 + rn(-8 log2 pi)
+    return min(static_cast<uint32_t>(__float_as_int(t) - 0x4B400000), kToppMassBins - 1u);
+  };
+  // pi relative to the top of its bin, rn(pi 2^(b/8) 2^qb)
+  auto quantise = [&](float y, float t) -> uint32_t {
+    const float k = fminf(t - 12582912.f, kToppMassBins - 1.f);   // the bin, as a float
+    const float r = fminf(fast_exp2(__fmaf_rn(k, 0.125f, y)), 2.f);
+    return static_cast<uint32_t>(__float_as_int(__fmaf_rn(r, qsc, 8388608.f)) - 0x4B000000);
+  };
+
+  // ---- pass 1 (HBM): the (bin, lane) cells ----------------------------------
+  topp_for_each<T, VEC>(rowp, a.V, [&](float x) {
+    float y, t;
+    const uint32_t b = mass_bin(x, y, t);
+    atomicAdd(&cell[b * 32 + lane], quantise(y, t));
+  });
+  __syncthreads();
+  // bin masses in units of 2^-(26 + qb), in decreasing order of the logit
+  unsigned long long Q = 0, m = 0;
+  if (tid < kToppMassBins) {
+#pragma unroll 8
+    for (int l = 0; l < 32; ++l) Q += cell[tid * 32 + ((l + lane) & 31)];
+    m = (Q * sh.frac[tid & 7]) >> (tid >> 3);
+  }
+  unsigned long long total;
+  const unsigned long long above = block_excl_scan_u64<NT>(m, sh.u64s, &total);
+  const unsigned long long limit = __umul64hi(total, p64);  // floor(top_p total)
+  const bool cand = tid < kToppMassBins && Q > 0 && above < limit;
+  const int bstar = block_max_int<NT>(cand ? tid : -1, sh.ints);
+  if (bstar < 0) return false;  // an empty or non-finite row: the exact path reports it
+  if (tid == bstar) sh.s.bin_above = above;
+  __syncthreads();  // every cell has been read: they hold the list from here on
+
+  // ---- pass 2 (L2): the threshold bin's keys and quantised masses -----------
+  uint32_t *const lkey = cell;
+  uint32_t *const lq = cell + kToppListCap;
+  topp_for_each<T, VEC>(rowp, a.V, [&](float x) {
+    float y, t;
+    if (mass_bin(x, y, t) == static_cast<uint32_t>(bstar)) {
+      const int idx = atomicAdd(&sh.s.n, 1);
+      if (idx < kToppListCap) {
+        lkey[idx] = order_key(x);
+        lq[idx] = quantise(y, t);
+      }
+    }
+  });
+  __syncthreads();
+  const int n = sh.s.n;
+  if (n > kToppListCap || n == 0) return false;  // the exact path
+  const unsigned long long bin_above = sh.s.bin_above;
+  const unsigned fr = sh.frac[bstar & 7];
+  const int bsh = bstar >> 3;
+  auto to_mass = [&](unsigned long long s) { return (s * fr) >> bsh; };
+
+  // ---- radix select inside the threshold bin ---------------------------------
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+  unsigned long long qsum = 0;
+  for (int i = tid; i < n; i += NT) {
+    kmin = min(kmin, lkey[i]);
+    kmax = max(kmax, lkey[i]);
+    qsum += lq[i];
+  }
+  kmin = block_min_u32<NT>(kmin, sh.ints);
+  kmax = block_max_u32<NT>(kmax, sh.ints);
+  unsigned long long qtot;
+  block_excl_scan_u64<NT>(qsum, sh.u64s, &qtot);
+  const int hb = kmin == kmax ? -1 : 31 - __clz(kmin ^ kmax);  // highest differing bit
+  uint32_t prefix = hb == 31 ? 0u : (kmin >> (hb + 1));
+  unsigned long long in_above = 0, in_kept = qtot;
+  for (int top = hb; top >= 0; top -= 8) {
+    const int w = min(8, top + 1), sh_lo = top + 1 - w;
+    const int nb = 1 << w;
+    if (tid < 256) { sh.hq[tid] = 0u; sh.hc[tid] = 0u; }
+    __syncthreads();
+    for (int i = tid; i < n; i += NT) {
+      const uint32_t key = lkey[i];
+      if (top == 31 || (key >> (top + 1)) == prefix) {
+        const uint32_t d = (key >> sh_lo) & static_cast<uint32_t>(nb - 1);
+        atomicAdd(&sh.hq[d], lq[i]);
+        atomicAdd(&sh.hc[d], 1u);
+      }
+    }
+    __syncthreads();
+    const int dd = nb - 1 - tid;  // thread tid takes digit nb - 1 - tid (descending)
+    const unsigned long long hv = tid < nb ? sh.hq[dd] : 0ull;
+    unsigned long long tot_unused;
+    const unsigned long long ex = block_excl_scan_u64<NT>(hv, sh.u64s, &tot_unused);
+    const bool c = tid < nb && sh.hc[dd] > 0u && bin_above + to_mass(in_above + ex) < limit;
+    const int best = block_max_int<NT>(c ? tid : -1, sh.ints);
+    if (best < 0) return false;  // not reached: the bin's largest key is always a candidate
+    if (tid == best) {
+      sh.s.prefix = (prefix << w) | static_cast<uint32_t>(dd);
+      sh.s.in_above = in_above + ex;
+      sh.s.in_kept = in_above + ex + hv;
+    }
+    __syncthreads();
+    prefix = sh.s.prefix;
+    in_above = sh.s.in_above;
+    in_kept = sh.s.in_kept;
+  }
+  const uint32_t vstar = prefix;
+  const unsigned long long kept_mass = bin_above + to_mass(in_kept);
+  auto kept = [&](float x) { return order_key(x) >= vstar; };
+  const float log_z = (total > 0 && kept_mass > 0)
+      ? static_cast<float>(log(static_cast<double>(kept_mass) / static_cast<double>(total)))
+      : 0.f;
+  if (j != a.K) {
+    if (tid == 0) topp_finish_fast<T>(a, row, part, j, rowp, log_z, kept);
+    return true;
+  }
+  // the bonus row: the same quantised masses as integer weights
+  auto weight = [&](float x) -> unsigned long long {
+    float y, t;
+    const uint32_t b = mass_bin(x, y, t);
+    return (static_cast<unsigned long long>(quantise(y, t)) * sh.frac[b & 7]) >> (b >> 3);
+  };
+  const long long tok = topp_bonus_draw<T, VEC>(a, part, rowp, kept, weight, sh);
+  if (tid == 0) {
+    RowResult r = a.ws.results[row];
+    r.lse += log_z;
+    r.lse_alpha += log_z;
+    r.tok = static_cast<int>(tok);
+    a.ws.results[row] = r;
+  }
+  return true;
+}
+
+// Exact path: a radix select over the whole row's keys.
+template <typename T, bool VEC>
+__device__ void topp_exact(const StepArgs &a, float top_p, ToppShared &sh) {
   using Tr = LogitTraits<T>;
   using Dg = ToppDigits<T>;
-  constexpr int E = Tr::kPerVec;
   constexpr int kShift = 12;  // bonus weights in units of 2^-(kFixBits - kShift)
-  // the histogram (low words, then high words); a bonus row's run sums later
-  __shared__ __align__(16) unsigned long long s_buf[kToppBins];
-  __shared__ float2 s_tab[64];
-  __shared__ unsigned long long s_u64[kToppWarps];
-  __shared__ int s_i[kToppWarps];
-  __shared__ float s_f[kToppWarps];
-  __shared__ unsigned long long s_above, s_kept, s_base;
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_sel;
-  __shared__ long long s_tok;
-  uint32_t *const s_lo = reinterpret_cast<uint32_t *>(s_buf);
+  uint32_t *const s_lo = sh.cell;
   uint32_t *const s_hi = s_lo + kToppBins;
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x;
   const int row = blockIdx.x;
   const int rpp = 2 * a.K + 1;
   const int part = row / rpp, j = row - part * rpp;
   const bool bonus = j == a.K;
   const char *rowp = row_base<T>(a, row);
-  const int64_t V = a.V;
-  const int64_t ng = (V + E - 1) / E;
   const float lse = a.ws.results[row].lse;
   const float l2s = a.tscale * kLog2e, l2lse = lse * kLog2e;
-  const uint4 pad = make_uint4(Dg::kNegInfWord, Dg::kNegInfWord, Dg::kNegInfWord, Dg::kNegInfWord);
-  if (bonus) stage_exp2_table(s_tab);
+  if (bonus) stage_exp2_table(sh.tab);
 
-  // adds floor(pi 2^40) + 1 for the finite logit x to bin b
+  // adds round(pi 2^40), lowest bit set, for the finite logit x to bin b
   auto add_mass = [&](uint32_t b, float x) {
     const float pm = fminf(fast_exp2(fmaf(x, l2s, -l2lse)), 2.f);  // pi, about 1e-7 relative
-    const unsigned long long fx = __float2ull_rz(pm * 0x1p40f) + 1ull;
+    const unsigned long long fx = static_cast<unsigned long long>(float_to_ll_rn(pm * 0x1p40f)) | 1ull;
     const uint32_t lo = static_cast<uint32_t>(fx);
     const uint32_t old = atomicAdd(&s_lo[b], lo);
     const uint32_t hi = static_cast<uint32_t>(fx >> 32) + (old + lo < lo ? 1u : 0u);
@@ -1729,7 +2042,7 @@ __global__ void __launch_bounds__(kToppThreads, 2) topp_kernel(const StepArgs a,
 
   float mx = kNegInf;
   uint32_t prefix = 0;
-  int consumed = 0;           // key bits fixed so far
+  int consumed = 0;  // key bits fixed so far
   unsigned long long total = 0, above = 0;
   bool ok = true;
 #pragma unroll 1
@@ -1739,37 +2052,17 @@ __global__ void __launch_bounds__(kToppThreads, 2) topp_kernel(const StepArgs a,
     const int shift = 32 - consumed - width;
     for (int b = tid; b < nb; b += kToppThreads) s_lo[b] = s_hi[b] = 0u;
     __syncthreads();
-    for (int64_t g0 = tid; g0 < ng; g0 += static_cast<int64_t>(kToppThreads) * kToppUnroll) {
-      uint4 v[kToppUnroll];
-#pragma unroll
-      for (int u = 0; u < kToppUnroll; ++u) {
-        const int64_t g = g0 + static_cast<int64_t>(u) * kToppThreads;
-        v[u] = g < ng ? topp_group<T, VEC>(rowp, g, V) : pad;
-      }
-#pragma unroll
-      for (int u = 0; u < kToppUnroll; ++u) {
-        if (pass == 0) {
-#pragma unroll
-          for (int e = 0; e < E; ++e) {
-            const float x = Tr::at(v[u], e);
-            mx = fmaxf(mx, x);
-            if (x > kNegInf && x < -kNegInf) add_mass(order_key(x) >> shift, x);
-          }
-        } else {
-          // only the logits under the prefix: usually none of a group's
-          uint32_t m = 0;
-#pragma unroll
-          for (int e = 0; e < E; ++e)
-            if ((order_key(Tr::at(v[u], e)) >> (shift + width)) == prefix) m |= 1u << e;
-          while (m) {
-            const int e = __ffs(m) - 1;
-            m &= m - 1;
-            const float x = Tr::at(v[u], e);
-            if (x > kNegInf && x < -kNegInf)
-              add_mass((order_key(x) >> shift) & static_cast<uint32_t>(nb - 1), x);
-          }
-        }
-      }
+    if (pass == 0) {
+      topp_for_each<T, VEC>(rowp, a.V, [&](float x) {
+        mx = fmaxf(mx, x);
+        if (x > kNegInf && x < -kNegInf) add_mass(order_key(x) >> shift, x);
+      });
+    } else {
+      topp_for_each<T, VEC>(rowp, a.V, [&](float x) {
+        const uint32_t key = order_key(x);
+        if ((key >> (shift + width)) == prefix && x > kNegInf && x < -kNegInf)
+          add_mass((key >> shift) & static_cast<uint32_t>(nb - 1), x);
+      });
     }
     __syncthreads();
     // bins in descending key order: thread tid takes positions
@@ -1781,7 +2074,7 @@ __global__ void __launch_bounds__(kToppThreads, 2) topp_kernel(const StepArgs a,
       if (d < nb) sum += (static_cast<unsigned long long>(s_hi[nb - 1 - d]) << 32) | s_lo[nb - 1 - d];
     }
     unsigned long long tot;
-    const unsigned long long excl = block_excl_scan_u64<kToppThreads>(sum, s_u64, &tot);
+    const unsigned long long excl = block_excl_scan_u64<kToppThreads>(sum, sh.u64s, &tot);
     if (pass == 0) total = tot;
     const unsigned long long limit =
         static_cast<unsigned long long>(static_cast<double>(top_p) * static_cast<double>(total));
@@ -1796,135 +2089,92 @@ __global__ void __launch_bounds__(kToppThreads, 2) topp_kernel(const StepArgs a,
       if (m > 0 && run < limit) { best = d; best_a = run; best_v = m; }
       run += m;
     }
-    const int bd = block_max_int<kToppThreads>(best, s_i);
+    const int bd = block_max_int<kToppThreads>(best, sh.ints);
     if (bd >= 0 && best == bd) {
-      s_prefix = (prefix << width) | static_cast<uint32_t>(nb - 1 - bd);
-      s_above = best_a;
-      s_kept = best_a + best_v;
+      sh.s.prefix = (prefix << width) | static_cast<uint32_t>(nb - 1 - bd);
+      sh.s.above = best_a;
+      sh.s.kept = best_a + best_v;
     }
     __syncthreads();
     if (bd < 0) { ok = false; break; }  // an empty or non-finite row (reported elsewhere)
-    prefix = s_prefix;
-    above = s_above;
+    prefix = sh.s.prefix;
+    above = sh.s.above;
     consumed += width;
   }
   // kept: logits at or above the threshold key (nothing when the select failed)
-  const unsigned long long kept_mass = ok ? s_kept : 0ull;
+  const unsigned long long kept_mass = ok ? sh.s.kept : 0ull;
   auto kept = [&](float x) { return ok && (order_key(x) >> (32 - Dg::kKeyBits)) >= prefix; };
   const float log_z = (total > 0 && kept_mass > 0)
       ? static_cast<float>(log(static_cast<double>(kept_mass) / static_cast<double>(total)))
       : 0.f;
   if (!bonus) {
-    if (tid == 0) {
-      RowResult r = a.ws.results[row];
-      const int tok = a.tokens[static_cast<size_t>(part) * a.K + (j < a.K ? j : j - a.K - 1)];
-      if (tok >= 0 && tok < a.V && !kept(Tr::scalar(rowp, tok))) {
-        if (j < a.K) r.g = kNegInf;                      // outside the target's nucleus
-        else raise_status(a.ws.status, SMC_DEV_BAD_TOKEN);  // could not have been drafted
-      }
-      r.lse += log_z;
-      a.ws.results[row] = r;
-    }
+    if (tid == 0) topp_finish_fast<T>(a, row, part, j, rowp, log_z, kept);
     return;
   }
-
-  // ---- bonus row: inverse CDF over the kept tokens, exact fixed point ------
-  const float M = block_max_nt<kToppThreads>(mx, s_f);
+  // ---- bonus row: weights exp(s (x - M)) in exact fixed point ---------------
+  const float M = block_max_nt<kToppThreads>(mx, sh.fl);
   const bool live = ok && M > kNegInf && M < -kNegInf;
+  auto kept_live = [&](float x) { return live && kept(x); };
   auto weight = [&](float x) -> unsigned long long {
-    return static_cast<unsigned long long>(weight_fixed(x, M, a.balpha, s_tab) >> kShift);
+    return static_cast<unsigned long long>(weight_fixed(x, M, a.balpha, sh.tab) >> kShift);
   };
-  // runs of gpe = 32 G consecutive groups, at most kToppEntries of them; the
-  // 32 groups one warp reads at a time always lie in one run
-  const int64_t G = (ng + 32ll * kToppEntries - 1) / (32ll * kToppEntries);
-  const int64_t gpe = 32 * G;
-  const int ne = static_cast<int>((ng + gpe - 1) / gpe);
-  unsigned long long *const s_run = s_buf;
-  for (int e = tid; e < ne; e += kToppThreads) s_run[e] = 0ull;
-  if (tid == 0) { s_sel = -1; s_tok = -1; }
-  __syncthreads();
-  if (live) {
-    // a warp-uniform trip count: the warp sums below take every lane
-    for (int64_t w0 = tid - lane; w0 < ng; w0 += static_cast<int64_t>(kToppThreads) * kToppUnroll) {
-      const int64_t g0 = w0 + lane;
-      uint4 v[kToppUnroll];
-#pragma unroll
-      for (int u = 0; u < kToppUnroll; ++u) {
-        const int64_t g = g0 + static_cast<int64_t>(u) * kToppThreads;
-        v[u] = g < ng ? topp_group<T, VEC>(rowp, g, V) : pad;
-      }
-#pragma unroll
-      for (int u = 0; u < kToppUnroll; ++u) {
-        const int64_t g = g0 + static_cast<int64_t>(u) * kToppThreads;
-        uint32_t m = 0;
-#pragma unroll
-        for (int e = 0; e < E; ++e)
-          if (kept(Tr::at(v[u], e))) m |= 1u << e;
-        unsigned long long acc = 0;
-        while (m) {
-          const int e = __ffs(m) - 1;
-          m &= m - 1;
-          acc += weight(Tr::at(v[u], e));
-        }
-        acc = warp_sum_u64(acc);
-        // g - lane is the warp's first group, a multiple of 32
-        if (lane == 0 && g - lane < ng && acc) atomicAdd(&s_run[(g - lane) / gpe], acc);
-      }
-    }
-  }
-  __syncthreads();
-  // the run the draw lands in
-  const int c = (ne + kToppThreads - 1) / kToppThreads;
-  unsigned long long sum = 0;
-  for (int i = 0; i < c; ++i) {
-    const int d = tid * c + i;
-    if (d < ne) sum += s_run[d];
-  }
-  unsigned long long total_w;
-  const unsigned long long excl_w = block_excl_scan_u64<kToppThreads>(sum, s_u64, &total_w);
-  const float u = philox_uniform(a.seed, a.step, part, a.K, SMC_PURPOSE_BONUS);
-  const unsigned long long u24 = static_cast<unsigned long long>(u * 16777216.f);
-  // floor(total * u), exactly: u = u24 / 2^24
-  const unsigned long long target = __umul64hi(total_w, u24 << 40);
-  if (total_w > 0) {
-    unsigned long long run = excl_w;
-    for (int i = 0; i < c; ++i) {
-      const int d = tid * c + i;
-      if (d >= ne) break;
-      const unsigned long long w = s_run[d];
-      if (w > 0 && run <= target && target < run + w) { s_sel = d; s_base = run; }
-      run += w;
-    }
-  }
-  __syncthreads();
-  const int sel = s_sel;
-  if (sel >= 0) {
-    // the token within the run, by a block-wide scan in index order
-    unsigned long long rem = target - s_base;
-    const int64_t i0 = static_cast<int64_t>(sel) * gpe * E;
-    const int64_t i1 = min(V, i0 + gpe * E);
-    for (int64_t base = i0; base < i1; base += kToppThreads) {
-      const int64_t i = base + tid;
-      unsigned long long w = 0;
-      if (i < i1) {
-        const float x = Tr::scalar(rowp, i);
-        if (kept(x)) w = weight(x);
-      }
-      unsigned long long tot;
-      const unsigned long long ex = block_excl_scan_u64<kToppThreads>(w, s_u64, &tot);
-      if (w > 0 && ex <= rem && rem < ex + w) s_tok = i;
-      if (rem < tot) break;  // the same for every thread
-      rem -= tot;
-    }
-  }
-  __syncthreads();
+  const long long tok = topp_bonus_draw<T, VEC>(a, part, rowp, kept_live, weight, sh);
   if (tid == 0) {
     RowResult r = a.ws.results[row];
     r.lse += log_z;
     r.lse_alpha += log_z;
-    r.tok = static_cast<int>(s_tok);
+    r.tok = static_cast<int>(tok);
     a.ws.results[row] = r;
   }
+}
+
+// qb > 0: the mass-bin path with quantisation bits qb, falling back to the
+// exact path row by row; qb == 0: the exact path for every row.  p64 =
+// top_p 2^64.
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kToppThreads, 2)
+topp_kernel(const StepArgs a, float top_p, unsigned long long p64, int qb) {
+  extern __shared__ __align__(16) unsigned char topp_smem[];
+  ToppShared &sh = *reinterpret_cast<ToppShared *>(topp_smem);
+  if (qb > 0) {
+    if (topp_mass_bins<T, VEC>(a, p64, qb, sh)) return;
+    __syncthreads();
+  }
+  topp_exact<T, VEC>(a, top_p, sh);
+}
+
+// The nucleus kernel.  Its quantisation bits qb keep every (bin, lane) cell
+// of the mass-bin path below 2^32: a cell takes at most 16 threads' logits,
+// each q at most 2^qb 2^(1/16); below 18 bits the exact path takes every row.
+template <typename T, bool VEC>
+static cudaError_t launch_topp_t(const StepArgs &a, float top_p, long long rows,
+                                 cudaStream_t stream) {
+  constexpr int E = LogitTraits<T>::kPerVec;
+  const long long ng = (static_cast<long long>(a.V) + E - 1) / E;
+  const long long n_cell = (kToppThreads / 32) * ((ng + kToppThreads - 1) / kToppThreads) * E;
+  int lg = 0;
+  while ((1ll << lg) < n_cell) ++lg;
+  int qb = 31 - lg < 20 ? 31 - lg : 20;
+  if (qb < 18) qb = 0;
+  const unsigned long long p64 =
+      static_cast<unsigned long long>(std::ldexp(static_cast<double>(top_p), 64));
+  const size_t smem = sizeof(ToppShared);
+  cudaError_t e = allow_dyn_smem(topp_kernel<T, VEC>, smem);
+  if (e != cudaSuccess) return e;
+  topp_kernel<T, VEC><<<static_cast<unsigned>(rows), kToppThreads, smem, stream>>>(a, top_p, p64, qb);
+  return cudaGetLastError();
+}
+
+static cudaError_t launch_topp(const StepArgs &a, int dtype, float top_p, long long rows,
+                               cudaStream_t stream) {
+  const int esz = dtype == SMC_BF16 ? 2 : 4;
+  const bool vec = aligned16(a.target) && aligned16(a.draft) &&
+                   (static_cast<long long>(a.V) * esz) % 16 == 0;
+  if (dtype == SMC_BF16)
+    return vec ? launch_topp_t<bf16_tag, true>(a, top_p, rows, stream)
+               : launch_topp_t<bf16_tag, false>(a, top_p, rows, stream);
+  return vec ? launch_topp_t<float, true>(a, top_p, rows, stream)
+             : launch_topp_t<float, false>(a, top_p, rows, stream);
 }
 
 // The row pass (streaming or per-chunk kernel, then the row combine).
@@ -1979,17 +2229,8 @@ cudaError_t launch_step_rows(const Shape &s, int mode, const void *target, const
   cudaError_t e = launch_rows(a, s.dtype, rows, stream);
   if (e != cudaSuccess) return e;
   if (s.top_p < 1.f) {
-    const int esz = s.dtype == SMC_BF16 ? 2 : 4;
-    const bool vec = aligned16(a.target) && aligned16(a.draft) &&
-                     (static_cast<long long>(a.V) * esz) % 16 == 0;
-    const dim3 g(static_cast<unsigned>(rows)), blk(kToppThreads);
-    if (s.dtype == SMC_BF16) {
-      if (vec) topp_kernel<bf16_tag, true><<<g, blk, 0, stream>>>(a, s.top_p);
-      else topp_kernel<bf16_tag, false><<<g, blk, 0, stream>>>(a, s.top_p);
-    } else {
-      if (vec) topp_kernel<float, true><<<g, blk, 0, stream>>>(a, s.top_p);
-      else topp_kernel<float, false><<<g, blk, 0, stream>>>(a, s.top_p);
-    }
+    e = launch_topp(a, s.dtype, s.top_p, rows, stream);
+    if (e != cudaSuccess) return e;
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -195,6 +195,22 @@ def test_step_ex_top_p_tied_logits():
     print(f"tied: draws={t.draws} flagged={t.flagged} mismatched={t.mismatched}")
 
 
+@pytest.mark.parametrize("top_p", [0.5, 0.9])
+def test_step_ex_top_p_threshold_in_a_huge_tie_group(top_p):
+    """Two-valued logits (0 and 3): the threshold value is shared by thousands
+    of tokens, more than the threshold bin's shared-memory list holds, so the
+    rows take the exact radix select over the whole row."""
+    w = WORKLOADS["single_prompt_v32000"].with_(B=1, N=4)
+    nucleus_fn = _nucleus_tokens(w, top_p, 1.0, 47)
+
+    def fn(inp, step):
+        for key in ("target", "draft"):
+            inp[key].copy_(torch.where(inp[key].float() > 3.0, 3.0, 0.0))
+        nucleus_fn(inp, step)
+    t = lockstep(w, 2, seed=47, with_kv=False, top_p=top_p, tokens_fn=fn)
+    print(f"two-valued top_p={top_p}: draws={t.draws} flagged={t.flagged} mismatched={t.mismatched}")
+
+
 def test_step_ex_top_p_draft_outside_nucleus_is_reported():
     w = WORKLOADS["tiny_v64"].with_(B=1)
     inp = make_step_inputs(w, 3, device="cuda")
