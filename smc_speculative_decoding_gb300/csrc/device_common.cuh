@@ -477,16 +477,16 @@ __device__ __forceinline__ uint32_t block_min_u32(uint32_t v, int *scratch) {
   return v;
 }
 template <int NT>
-__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, int *scratch) {
+__device__ __forceinline__ uint32_t block_or_u32(uint32_t v, int *scratch) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __syncthreads();
   if (lane == 0) scratch[warp] = static_cast<int>(v);
   __syncthreads();
   v = lane < NT / 32 ? static_cast<uint32_t>(scratch[lane]) : 0u;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
 template <int NT>

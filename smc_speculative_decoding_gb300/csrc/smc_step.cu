@@ -1669,6 +1669,8 @@ struct ToppScalars {
   long long tok;
   uint32_t prefix;
   int sel, n;
+  float xlo, xhi;
+  bool last_bin;
 };
 struct ToppShared {
   uint32_t cell[kToppMassBins * 32];  // mass cells; then the list, or the exact path's buffers
@@ -1684,8 +1686,10 @@ static_assert(sizeof(uint32_t) * kToppMassBins * 32 >= sizeof(unsigned long long
               "the exact path's histogram and runs fit in the cells");
 static_assert(kToppMassBins * 32 >= 2 * kToppListCap, "the list fits in the cells");
 
+// An order-preserving 32-bit key of a logit; -0 and +0 (equal logits) share
+// the key of +0.
 __device__ __forceinline__ uint32_t order_key(float f) {
-  const uint32_t u = __float_as_uint(f);
+  const uint32_t u = __float_as_uint(f + 0.f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
@@ -1744,8 +1748,33 @@ __device__ __forceinline__ void topp_for_each(const char *rowp, int64_t V, F f) 
     }
 #pragma unroll
     for (int u = 0; u < kToppUnroll; ++u) {
+      if (g0 + static_cast<int64_t>(u) * kToppThreads >= ng) break;
 #pragma unroll
       for (int e = 0; e < E; ++e) f(Tr::at(v[u], e));
+    }
+  }
+}
+
+// The same, two consecutive logits at a time: f(x0, x1).
+template <typename T, bool VEC, typename F>
+__device__ __forceinline__ void topp_for_each_pair(const char *rowp, int64_t V, F f) {
+  using Tr = LogitTraits<T>;
+  constexpr int E = Tr::kPerVec;
+  const int64_t ng = (V + E - 1) / E;
+  const uint4 pad = make_uint4(ToppDigits<T>::kNegInfWord, ToppDigits<T>::kNegInfWord,
+                               ToppDigits<T>::kNegInfWord, ToppDigits<T>::kNegInfWord);
+  for (int64_t g0 = threadIdx.x; g0 < ng; g0 += static_cast<int64_t>(kToppThreads) * kToppUnroll) {
+    uint4 v[kToppUnroll];
+#pragma unroll
+    for (int u = 0; u < kToppUnroll; ++u) {
+      const int64_t g = g0 + static_cast<int64_t>(u) * kToppThreads;
+      v[u] = g < ng ? topp_group<T, VEC>(rowp, g, V) : pad;
+    }
+#pragma unroll
+    for (int u = 0; u < kToppUnroll; ++u) {
+      if (g0 + static_cast<int64_t>(u) * kToppThreads >= ng) break;
+#pragma unroll
+      for (int e = 0; e < E; e += 2) f(Tr::at(v[u], e), Tr::at(v[u], e + 1));
     }
   }
 }
@@ -1848,6 +1877,18 @@ __device__ long long topp_bonus_draw(const StepArgs &a, int part, const char *ro
   return sh.s.tok;
 }
 
+// log(kept / total) for 64-bit fixed-point masses, in float (each part
+// converted through its two 32-bit halves; about 2e-7 absolute); 0 without
+// mass.  One thread calls it.
+__device__ __forceinline__ float topp_log_ratio(unsigned long long kept, unsigned long long total) {
+  if (kept == 0 || total == 0) return 0.f;
+  auto to_f = [](unsigned long long v) {
+    return fmaf(__uint2float_rn(static_cast<uint32_t>(v >> 32)), 4294967296.f,
+                __uint2float_rn(static_cast<uint32_t>(v)));
+  };
+  return logf(to_f(kept) / to_f(total));
+}
+
 // Writes a row's nucleus result: the log kept mass on its log-sum-exp(s), and
 // for a drafted position the check of its token.
 template <typename T, typename KeptF>
@@ -1882,25 +1923,50 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
   if (tid < 8) sh.frac[tid] = kToppFrac[tid];
   if (tid == 0) sh.s.n = 0;
   __syncthreads();
-  // the mass bin of x (and log2 pi, and the rounding register for it)
+  // The mass bin of x: with y = max(log2 pi, -47.875) (-inf and NaN logits
+  // give -47.875: a mass of 2^-47.875, negligible), t = 1.5 2^23 + rn(-8 y)
+  // holds the bin in its low bits.  y <= 0 up to the rounding of the row's
+  // log-sum-exp; the unsigned clamp only guards rows whose log-sum-exp is
+  // not finite (reported elsewhere).
+  constexpr float kMagicB = 12582912.f;   // 1.5 2^23
+  constexpr float kMagicQ = 8388608.f;    // 2^23
+  constexpr float kFloorY = -47.875f;     // -(kToppMassBins - 1) / 8
   auto mass_bin = [&](float x, float &y, float &t) -> uint32_t {
-    y = __fmaf_rn(x, l2s, -l2lse);               // log2 pi
-    t = __fmaf_rn(y, -8.f, 12582912.f);          // 1.5 2^23 + rn(-8 log2 pi)
+    y = fmaxf(__fmaf_rn(x, l2s, -l2lse), kFloorY);
+    t = __fmaf_rn(y, -8.f, kMagicB);
     return min(static_cast<uint32_t>(__float_as_int(t) - 0x4B400000), kToppMassBins - 1u);
   };
-  // pi relative to the top of its bin, rn(pi 2^(b/8) 2^qb)
+  // pi relative to the top of its bin, rn(pi 2^(b/8) 2^qb), from y and t
   auto quantise = [&](float y, float t) -> uint32_t {
-    const float k = fminf(t - 12582912.f, kToppMassBins - 1.f);   // the bin, as a float
-    const float r = fminf(fast_exp2(__fmaf_rn(k, 0.125f, y)), 2.f);
-    return static_cast<uint32_t>(__float_as_int(__fmaf_rn(r, qsc, 8388608.f)) - 0x4B000000);
+    const float r = fast_exp2(__fmaf_rn(t - kMagicB, 0.125f, y));  // in [2^-1/16, 2^1/16]
+    return static_cast<uint32_t>(__float_as_int(__fmaf_rn(r, qsc, kMagicQ)) - 0x4B000000);
   };
 
   // ---- pass 1 (HBM): the (bin, lane) cells ----------------------------------
-  topp_for_each<T, VEC>(rowp, a.V, [&](float x) {
-    float y, t;
-    const uint32_t b = mass_bin(x, y, t);
-    atomicAdd(&cell[b * 32 + lane], quantise(y, t));
-  });
+  // the same arithmetic as mass_bin and quantise, two logits at a time on the
+  // packed fp32x2 pipes
+  {
+    const unsigned long long L2S = f2dup(l2s), NL2LSE = f2dup(-l2lse), M8 = f2dup(-8.f),
+                             MB = f2dup(kMagicB), EIGHTH = f2dup(0.125f), QSC = f2dup(qsc),
+                             MQ = f2dup(kMagicQ);
+    uint32_t *const lane_cell = cell + lane;
+    topp_for_each_pair<T, VEC>(rowp, a.V, [&](float x0, float x1) {
+      float y0, y1;
+      f2unpack(fma2(f2pack(x0, x1), L2S, NL2LSE), y0, y1);
+      const unsigned long long Y = f2pack(fmaxf(y0, kFloorY), fmaxf(y1, kFloorY));
+      const unsigned long long Tt = fma2(Y, M8, MB);
+      float t0, t1;
+      f2unpack(Tt, t0, t1);
+      const uint32_t b0 = min(static_cast<uint32_t>(__float_as_int(t0) - 0x4B400000), kToppMassBins - 1u);
+      const uint32_t b1 = min(static_cast<uint32_t>(__float_as_int(t1) - 0x4B400000), kToppMassBins - 1u);
+      float e0, e1;
+      f2unpack(fma2(sub2(Tt, MB), EIGHTH, Y), e0, e1);
+      float q0, q1;
+      f2unpack(fma2(f2pack(fast_exp2(e0), fast_exp2(e1)), QSC, MQ), q0, q1);
+      atomicAdd(lane_cell + b0 * 32, static_cast<uint32_t>(__float_as_int(q0) - 0x4B000000));
+      atomicAdd(lane_cell + b1 * 32, static_cast<uint32_t>(__float_as_int(q1) - 0x4B000000));
+    });
+  }
   __syncthreads();
   // bin masses in units of 2^-(26 + qb), in decreasing order of the logit
   unsigned long long Q = 0, m = 0;
@@ -1916,14 +1982,31 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
   const int bstar = block_max_int<NT>(cand ? tid : -1, sh.ints);
   if (bstar < 0) return false;  // an empty or non-finite row: the exact path reports it
   if (tid == bstar) sh.s.bin_above = above;
+  if (tid == 0) {
+    // A superset of bin b*'s logits as an interval [x_lo, x_hi]: its members
+    // have -8 y within 1/2 of b*, y = log2 pi rounded once (an error below
+    // 2^-18 for |y| < 64), so x l2s - l2lse lies within 1/16 + 2^-10 of
+    // -b*/8; widened by 1e-5 relative for the rounding of the bounds.  The list below still
+    // checks every logit's bin.
+    const float bf = static_cast<float>(bstar);
+    const float xl = (l2lse - fmaf(bf, 0.125f, 0.0625f + 0x1p-10f)) / l2s;
+    const float xh = (l2lse - fmaf(bf, 0.125f, -0.0625f - 0x1p-10f)) / l2s;
+    const float slack = 1e-6f * fabsf(l2lse) / l2s;  // the rounding of l2lse - c
+    sh.s.xlo = xl - 1e-5f * (fabsf(xl) + 1.f) - slack;
+    sh.s.xhi = xh + 1e-5f * (fabsf(xh) + 1.f) + slack;
+    // the last bin also holds everything below it, -inf and NaN included
+    sh.s.last_bin = bstar == kToppMassBins - 1;
+  }
   __syncthreads();  // every cell has been read: they hold the list from here on
 
   // ---- pass 2 (L2): the threshold bin's keys and quantised masses -----------
   uint32_t *const lkey = cell;
   uint32_t *const lq = cell + kToppListCap;
+  const float xlo = sh.s.xlo, xhi = sh.s.xhi;
+  const bool last_bin = sh.s.last_bin;
   topp_for_each<T, VEC>(rowp, a.V, [&](float x) {
     float y, t;
-    if (mass_bin(x, y, t) == static_cast<uint32_t>(bstar)) {
+    if (((x >= xlo && x <= xhi) || last_bin) && mass_bin(x, y, t) == static_cast<uint32_t>(bstar)) {
       const int idx = atomicAdd(&sh.s.n, 1);
       if (idx < kToppListCap) {
         lkey[idx] = order_key(x);
@@ -1940,22 +2023,25 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
   auto to_mass = [&](unsigned long long s) { return (s * fr) >> bsh; };
 
   // ---- radix select inside the threshold bin ---------------------------------
-  uint32_t kmin = 0xffffffffu, kmax = 0u;
+  // the bits in which the list's keys differ: [lb, hb]
+  uint32_t kmin = 0xffffffffu;
   unsigned long long qsum = 0;
   for (int i = tid; i < n; i += NT) {
     kmin = min(kmin, lkey[i]);
-    kmax = max(kmax, lkey[i]);
     qsum += lq[i];
   }
   kmin = block_min_u32<NT>(kmin, sh.ints);
-  kmax = block_max_u32<NT>(kmax, sh.ints);
+  uint32_t diff = 0u;
+  for (int i = tid; i < n; i += NT) diff |= lkey[i] ^ kmin;
+  diff = block_or_u32<NT>(diff, sh.ints);
   unsigned long long qtot;
   block_excl_scan_u64<NT>(qsum, sh.u64s, &qtot);
-  const int hb = kmin == kmax ? -1 : 31 - __clz(kmin ^ kmax);  // highest differing bit
+  const int hb = diff == 0u ? -1 : 31 - __clz(diff);
+  const int lb = diff == 0u ? 0 : __ffs(diff) - 1;
   uint32_t prefix = hb == 31 ? 0u : (kmin >> (hb + 1));
   unsigned long long in_above = 0, in_kept = qtot;
-  for (int top = hb; top >= 0; top -= 8) {
-    const int w = min(8, top + 1), sh_lo = top + 1 - w;
+  for (int top = hb; top >= lb; top -= 8) {
+    const int w = min(8, top + 1 - lb), sh_lo = top + 1 - w;
     const int nb = 1 << w;
     if (tid < 256) { sh.hq[tid] = 0u; sh.hc[tid] = 0u; }
     __syncthreads();
@@ -1985,14 +2071,12 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
     in_above = sh.s.in_above;
     in_kept = sh.s.in_kept;
   }
-  const uint32_t vstar = prefix;
+  // the bits below lb are the same in every key of the list
+  const uint32_t vstar = hb < 0 ? kmin : (prefix << lb) | (kmin & ((1u << lb) - 1u));
   const unsigned long long kept_mass = bin_above + to_mass(in_kept);
   auto kept = [&](float x) { return order_key(x) >= vstar; };
-  const float log_z = (total > 0 && kept_mass > 0)
-      ? static_cast<float>(log(static_cast<double>(kept_mass) / static_cast<double>(total)))
-      : 0.f;
   if (j != a.K) {
-    if (tid == 0) topp_finish_fast<T>(a, row, part, j, rowp, log_z, kept);
+    if (tid == 0) topp_finish_fast<T>(a, row, part, j, rowp, topp_log_ratio(kept_mass, total), kept);
     return true;
   }
   // the bonus row: the same quantised masses as integer weights
@@ -2003,6 +2087,7 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
   };
   const long long tok = topp_bonus_draw<T, VEC>(a, part, rowp, kept, weight, sh);
   if (tid == 0) {
+    const float log_z = topp_log_ratio(kept_mass, total);
     RowResult r = a.ws.results[row];
     r.lse += log_z;
     r.lse_alpha += log_z;
@@ -2014,7 +2099,7 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
 
 // Exact path: a radix select over the whole row's keys.
 template <typename T, bool VEC>
-__device__ void topp_exact(const StepArgs &a, float top_p, ToppShared &sh) {
+__device__ void topp_exact(const StepArgs &a, unsigned long long p64, ToppShared &sh) {
   using Tr = LogitTraits<T>;
   using Dg = ToppDigits<T>;
   constexpr int kShift = 12;  // bonus weights in units of 2^-(kFixBits - kShift)
@@ -2076,8 +2161,7 @@ __device__ void topp_exact(const StepArgs &a, float top_p, ToppShared &sh) {
     unsigned long long tot;
     const unsigned long long excl = block_excl_scan_u64<kToppThreads>(sum, sh.u64s, &tot);
     if (pass == 0) total = tot;
-    const unsigned long long limit =
-        static_cast<unsigned long long>(static_cast<double>(top_p) * static_cast<double>(total));
+    const unsigned long long limit = __umul64hi(total, p64);  // floor(top_p total)
     // the lowest candidate: a non-empty bin whose mass above is below limit
     int best = -1;
     unsigned long long best_a = 0, best_v = 0, run = above + excl;
@@ -2104,11 +2188,8 @@ __device__ void topp_exact(const StepArgs &a, float top_p, ToppShared &sh) {
   // kept: logits at or above the threshold key (nothing when the select failed)
   const unsigned long long kept_mass = ok ? sh.s.kept : 0ull;
   auto kept = [&](float x) { return ok && (order_key(x) >> (32 - Dg::kKeyBits)) >= prefix; };
-  const float log_z = (total > 0 && kept_mass > 0)
-      ? static_cast<float>(log(static_cast<double>(kept_mass) / static_cast<double>(total)))
-      : 0.f;
   if (!bonus) {
-    if (tid == 0) topp_finish_fast<T>(a, row, part, j, rowp, log_z, kept);
+    if (tid == 0) topp_finish_fast<T>(a, row, part, j, rowp, topp_log_ratio(kept_mass, total), kept);
     return;
   }
   // ---- bonus row: weights exp(s (x - M)) in exact fixed point ---------------
@@ -2120,6 +2201,7 @@ __device__ void topp_exact(const StepArgs &a, float top_p, ToppShared &sh) {
   };
   const long long tok = topp_bonus_draw<T, VEC>(a, part, rowp, kept_live, weight, sh);
   if (tid == 0) {
+    const float log_z = topp_log_ratio(kept_mass, total);
     RowResult r = a.ws.results[row];
     r.lse += log_z;
     r.lse_alpha += log_z;
@@ -2133,14 +2215,14 @@ __device__ void topp_exact(const StepArgs &a, float top_p, ToppShared &sh) {
 // top_p 2^64.
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kToppThreads, 2)
-topp_kernel(const StepArgs a, float top_p, unsigned long long p64, int qb) {
+topp_kernel(const StepArgs a, unsigned long long p64, int qb) {
   extern __shared__ __align__(16) unsigned char topp_smem[];
   ToppShared &sh = *reinterpret_cast<ToppShared *>(topp_smem);
   if (qb > 0) {
     if (topp_mass_bins<T, VEC>(a, p64, qb, sh)) return;
     __syncthreads();
   }
-  topp_exact<T, VEC>(a, top_p, sh);
+  topp_exact<T, VEC>(a, p64, sh);
 }
 
 // The nucleus kernel.  Its quantisation bits qb keep every (bin, lane) cell
@@ -2161,7 +2243,7 @@ static cudaError_t launch_topp_t(const StepArgs &a, float top_p, long long rows,
   const size_t smem = sizeof(ToppShared);
   cudaError_t e = allow_dyn_smem(topp_kernel<T, VEC>, smem);
   if (e != cudaSuccess) return e;
-  topp_kernel<T, VEC><<<static_cast<unsigned>(rows), kToppThreads, smem, stream>>>(a, top_p, p64, qb);
+  topp_kernel<T, VEC><<<static_cast<unsigned>(rows), kToppThreads, smem, stream>>>(a, p64, qb);
   return cudaGetLastError();
 }
 
