@@ -1692,6 +1692,10 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   const uint32_t u = __float_as_uint(f + 0.f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+// The logit whose key is k (the inverse of order_key, +0 for the key of 0).
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
+}
 
 // Digits of the exact path's radix select for the logit type T.
 template <typename T> struct ToppDigits {
@@ -1755,6 +1759,26 @@ __device__ __forceinline__ void topp_for_each(const char *rowp, int64_t V, F f) 
   }
 }
 
+// Calls f(v) for every group of the row (as one 16-byte word).
+template <typename T, bool VEC, typename F>
+__device__ __forceinline__ void topp_for_each_group(const char *rowp, int64_t V, F f) {
+  constexpr int E = LogitTraits<T>::kPerVec;
+  const int64_t ng = (V + E - 1) / E;
+  for (int64_t g0 = threadIdx.x; g0 < ng; g0 += static_cast<int64_t>(kToppThreads) * kToppUnroll) {
+    uint4 v[kToppUnroll];
+#pragma unroll
+    for (int u = 0; u < kToppUnroll; ++u) {
+      const int64_t g = g0 + static_cast<int64_t>(u) * kToppThreads;
+      if (g < ng) v[u] = topp_group<T, VEC>(rowp, g, V);
+    }
+#pragma unroll
+    for (int u = 0; u < kToppUnroll; ++u) {
+      if (g0 + static_cast<int64_t>(u) * kToppThreads >= ng) break;
+      f(v[u]);
+    }
+  }
+}
+
 // The same, two consecutive logits at a time: f(x0, x1).
 template <typename T, bool VEC, typename F>
 __device__ __forceinline__ void topp_for_each_pair(const char *rowp, int64_t V, F f) {
@@ -1779,54 +1803,70 @@ __device__ __forceinline__ void topp_for_each_pair(const char *rowp, int64_t V, 
   }
 }
 
-// The bonus row's draw: the first kept token whose inclusive prefix of
-// weight(x) (exact integers) exceeds floor(u total); -1 with no weight.
-template <typename T, bool VEC, typename KeptF, typename WeightF>
-__device__ long long topp_bonus_draw(const StepArgs &a, int part, const char *rowp, KeptF kept,
-                                     WeightF weight, ToppShared &sh) {
+// The largest logit of a group (NaN ignored; -inf for an all-NaN group).
+template <typename T>
+__device__ __forceinline__ float group_max(const uint4 &v) {
+  if (sizeof(T) == 4)
+    return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                 fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+  const uint32_t m = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
+  return fmaxf(bf16_lo(m), bf16_hi(m));
+}
+
+// The bonus row's draw over the kept logits {x >= thr} (none unless live):
+// the first whose inclusive prefix of weight(x) (exact integers) exceeds
+// floor(u total); -1 with no weight.  The row is cut into runs of 128 G
+// consecutive groups (at most kToppEntries runs); each warp sums whole runs,
+// reading kToppUnroll * 32 consecutive groups at a time, and skips any group
+// whose largest logit is below thr.
+template <typename T, bool VEC, typename WeightF>
+__device__ long long topp_bonus_draw(const StepArgs &a, int part, const char *rowp, bool live,
+                                     float thr, WeightF weight, ToppShared &sh) {
   using Tr = LogitTraits<T>;
   constexpr int E = Tr::kPerVec;
-  const int tid = threadIdx.x, lane = tid & 31;
+  constexpr int kRun = 32 * kToppUnroll;  // groups per warp read, and per run when G = 1
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t V = a.V;
   const int64_t ng = (V + E - 1) / E;
-  const uint4 pad = make_uint4(ToppDigits<T>::kNegInfWord, ToppDigits<T>::kNegInfWord,
-                               ToppDigits<T>::kNegInfWord, ToppDigits<T>::kNegInfWord);
-  // runs of gpe = 32 G consecutive groups, at most kToppEntries of them; the
-  // 32 groups one warp reads at a time always lie in one run
-  const int64_t G = (ng + 32ll * kToppEntries - 1) / (32ll * kToppEntries);
-  const int64_t gpe = 32 * G;
-  const int ne = static_cast<int>((ng + gpe - 1) / gpe);
+  const int64_t G = (ng + static_cast<int64_t>(kRun) * kToppEntries - 1) /
+                    (static_cast<int64_t>(kRun) * kToppEntries);
+  const int64_t gpr = kRun * G;  // groups per run
+  const int ne = static_cast<int>((ng + gpr - 1) / gpr);
+  const int rpw = (ne + kToppWarps - 1) / kToppWarps;  // runs per warp
   unsigned long long *const s_run = reinterpret_cast<unsigned long long *>(sh.cell);
   __syncthreads();  // the cells' previous contents are no longer read
-  for (int e = tid; e < ne; e += kToppThreads) s_run[e] = 0ull;
   if (tid == 0) { sh.s.sel = -1; sh.s.tok = -1; }
-  __syncthreads();
-  // a warp-uniform trip count: the warp sums below take every lane
-  for (int64_t w0 = tid - lane; w0 < ng; w0 += static_cast<int64_t>(kToppThreads) * kToppUnroll) {
-    const int64_t g0 = w0 + lane;
-    uint4 v[kToppUnroll];
+  // warp w sums runs [w rpw, (w + 1) rpw); its trip counts are warp-uniform
+  for (int r = warp * rpw; r < min(ne, (warp + 1) * rpw); ++r) {
+    unsigned long long acc = 0;
+    if (live) {
+      const int64_t r1 = min(ng, (r + 1) * gpr);
+      for (int64_t g0 = r * gpr + lane; g0 < r1; g0 += kRun) {
+        uint4 v[kToppUnroll];
 #pragma unroll
-    for (int u = 0; u < kToppUnroll; ++u) {
-      const int64_t g = g0 + static_cast<int64_t>(u) * kToppThreads;
-      v[u] = g < ng ? topp_group<T, VEC>(rowp, g, V) : pad;
-    }
+        for (int u = 0; u < kToppUnroll; ++u) {
+          const int64_t g = g0 + 32 * u;
+          v[u] = g < r1 ? topp_group<T, VEC>(rowp, g, V)
+                        : make_uint4(ToppDigits<T>::kNegInfWord, ToppDigits<T>::kNegInfWord,
+                                     ToppDigits<T>::kNegInfWord, ToppDigits<T>::kNegInfWord);
+        }
 #pragma unroll
-    for (int u = 0; u < kToppUnroll; ++u) {
-      const int64_t g = g0 + static_cast<int64_t>(u) * kToppThreads;
-      uint32_t m = 0;
+        for (int u = 0; u < kToppUnroll; ++u) {
+          if (!(group_max<T>(v[u]) >= thr)) continue;
+          uint32_t m = 0;
 #pragma unroll
-      for (int e = 0; e < E; ++e)
-        if (kept(Tr::at(v[u], e))) m |= 1u << e;
-      unsigned long long acc = 0;
-      while (m) {
-        const int e = __ffs(m) - 1;
-        m &= m - 1;
-        acc += weight(Tr::at(v[u], e));
+          for (int e = 0; e < E; ++e)
+            if (Tr::at(v[u], e) >= thr) m |= 1u << e;
+          while (m) {
+            const int e = __ffs(m) - 1;
+            m &= m - 1;
+            acc += weight(Tr::at(v[u], e));
+          }
+        }
       }
-      acc = warp_sum_u64(acc);
-      // g - lane is the warp's first group, a multiple of 32
-      if (lane == 0 && g - lane < ng && acc) atomicAdd(&s_run[(g - lane) / gpe], acc);
     }
+    acc = warp_sum_u64(acc);
+    if (lane == 0) s_run[r] = acc;
   }
   __syncthreads();
   // the run the draw lands in
@@ -1857,14 +1897,14 @@ __device__ long long topp_bonus_draw(const StepArgs &a, int part, const char *ro
   if (sel >= 0) {
     // the token within the run, by a block-wide scan in index order
     unsigned long long rem = target - sh.s.base;
-    const int64_t i0 = static_cast<int64_t>(sel) * gpe * E;
-    const int64_t i1 = min(V, i0 + gpe * E);
+    const int64_t i0 = static_cast<int64_t>(sel) * gpr * E;
+    const int64_t i1 = min(V, i0 + gpr * E);
     for (int64_t base = i0; base < i1; base += kToppThreads) {
       const int64_t i = base + tid;
       unsigned long long w = 0;
       if (i < i1) {
         const float x = Tr::scalar(rowp, i);
-        if (kept(x)) w = weight(x);
+        if (x >= thr) w = weight(x);
       }
       unsigned long long tot;
       const unsigned long long ex = block_excl_scan_u64<kToppThreads>(w, sh.u64s, &tot);
@@ -1923,18 +1963,17 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
   if (tid < 8) sh.frac[tid] = kToppFrac[tid];
   if (tid == 0) sh.s.n = 0;
   __syncthreads();
-  // The mass bin of x: with y = max(log2 pi, -47.875) (-inf and NaN logits
-  // give -47.875: a mass of 2^-47.875, negligible), t = 1.5 2^23 + rn(-8 y)
-  // holds the bin in its low bits.  y <= 0 up to the rounding of the row's
-  // log-sum-exp; the unsigned clamp only guards rows whose log-sum-exp is
-  // not finite (reported elsewhere).
+  // The mass bin of x: with y = log2 pi clamped to [-47.875, 0] (-inf and
+  // NaN logits give -47.875: a mass of 2^-47.875, negligible; y exceeds 0
+  // only by the rounding of the row's log-sum-exp), t = 1.5 2^23 + rn(-8 y)
+  // holds the bin, 0..383, in its low bits.
   constexpr float kMagicB = 12582912.f;   // 1.5 2^23
   constexpr float kMagicQ = 8388608.f;    // 2^23
   constexpr float kFloorY = -47.875f;     // -(kToppMassBins - 1) / 8
   auto mass_bin = [&](float x, float &y, float &t) -> uint32_t {
-    y = fmaxf(__fmaf_rn(x, l2s, -l2lse), kFloorY);
+    y = fminf(fmaxf(__fmaf_rn(x, l2s, -l2lse), kFloorY), 0.f);
     t = __fmaf_rn(y, -8.f, kMagicB);
-    return min(static_cast<uint32_t>(__float_as_int(t) - 0x4B400000), kToppMassBins - 1u);
+    return static_cast<uint32_t>(__float_as_int(t) - 0x4B400000);
   };
   // pi relative to the top of its bin, rn(pi 2^(b/8) 2^qb), from y and t
   auto quantise = [&](float y, float t) -> uint32_t {
@@ -1949,22 +1988,22 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
     const unsigned long long L2S = f2dup(l2s), NL2LSE = f2dup(-l2lse), M8 = f2dup(-8.f),
                              MB = f2dup(kMagicB), EIGHTH = f2dup(0.125f), QSC = f2dup(qsc),
                              MQ = f2dup(kMagicQ);
-    uint32_t *const lane_cell = cell + lane;
+    // cell index of bin b for this lane, b 32 + lane, from t's bits directly
+    // (modulo 2^32: the bias cancels)
+    const uint32_t lane_bias = static_cast<uint32_t>(lane) - (0x4B400000u << 5);
     topp_for_each_pair<T, VEC>(rowp, a.V, [&](float x0, float x1) {
       float y0, y1;
       f2unpack(fma2(f2pack(x0, x1), L2S, NL2LSE), y0, y1);
-      const unsigned long long Y = f2pack(fmaxf(y0, kFloorY), fmaxf(y1, kFloorY));
+      const unsigned long long Y = f2pack(fminf(fmaxf(y0, kFloorY), 0.f), fminf(fmaxf(y1, kFloorY), 0.f));
       const unsigned long long Tt = fma2(Y, M8, MB);
       float t0, t1;
       f2unpack(Tt, t0, t1);
-      const uint32_t b0 = min(static_cast<uint32_t>(__float_as_int(t0) - 0x4B400000), kToppMassBins - 1u);
-      const uint32_t b1 = min(static_cast<uint32_t>(__float_as_int(t1) - 0x4B400000), kToppMassBins - 1u);
       float e0, e1;
       f2unpack(fma2(sub2(Tt, MB), EIGHTH, Y), e0, e1);
       float q0, q1;
       f2unpack(fma2(f2pack(fast_exp2(e0), fast_exp2(e1)), QSC, MQ), q0, q1);
-      atomicAdd(lane_cell + b0 * 32, static_cast<uint32_t>(__float_as_int(q0) - 0x4B000000));
-      atomicAdd(lane_cell + b1 * 32, static_cast<uint32_t>(__float_as_int(q1) - 0x4B000000));
+      atomicAdd(&cell[(__float_as_uint(t0) << 5) + lane_bias], __float_as_uint(q0) - 0x4B000000u);
+      atomicAdd(&cell[(__float_as_uint(t1) << 5) + lane_bias], __float_as_uint(q1) - 0x4B000000u);
     });
   }
   __syncthreads();
@@ -2004,13 +2043,19 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
   uint32_t *const lq = cell + kToppListCap;
   const float xlo = sh.s.xlo, xhi = sh.s.xhi;
   const bool last_bin = sh.s.last_bin;
-  topp_for_each<T, VEC>(rowp, a.V, [&](float x) {
-    float y, t;
-    if (((x >= xlo && x <= xhi) || last_bin) && mass_bin(x, y, t) == static_cast<uint32_t>(bstar)) {
-      const int idx = atomicAdd(&sh.s.n, 1);
-      if (idx < kToppListCap) {
-        lkey[idx] = order_key(x);
-        lq[idx] = quantise(y, t);
+  topp_for_each_group<T, VEC>(rowp, a.V, [&](const uint4 &v) {
+    // most groups hold no logit as large as x_lo
+    if (!last_bin && !(group_max<T>(v) >= xlo)) return;
+#pragma unroll
+    for (int e = 0; e < LogitTraits<T>::kPerVec; ++e) {
+      const float x = LogitTraits<T>::at(v, e);
+      float y, t;
+      if ((last_bin || (x >= xlo && x <= xhi)) && mass_bin(x, y, t) == static_cast<uint32_t>(bstar)) {
+        const int idx = atomicAdd(&sh.s.n, 1);
+        if (idx < kToppListCap) {
+          lkey[idx] = order_key(x);
+          lq[idx] = quantise(y, t);
+        }
       }
     }
   });
@@ -2074,7 +2119,9 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
   // the bits below lb are the same in every key of the list
   const uint32_t vstar = hb < 0 ? kmin : (prefix << lb) | (kmin & ((1u << lb) - 1u));
   const unsigned long long kept_mass = bin_above + to_mass(in_kept);
-  auto kept = [&](float x) { return order_key(x) >= vstar; };
+  // keys order logits as floats do, with -0 = +0; NaN is never kept
+  const float thr = key_value(vstar);
+  auto kept = [&](float x) { return x >= thr; };
   if (j != a.K) {
     if (tid == 0) topp_finish_fast<T>(a, row, part, j, rowp, topp_log_ratio(kept_mass, total), kept);
     return true;
@@ -2085,7 +2132,7 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
     const uint32_t b = mass_bin(x, y, t);
     return (static_cast<unsigned long long>(quantise(y, t)) * sh.frac[b & 7]) >> (b >> 3);
   };
-  const long long tok = topp_bonus_draw<T, VEC>(a, part, rowp, kept, weight, sh);
+  const long long tok = topp_bonus_draw<T, VEC>(a, part, rowp, true, thr, weight, sh);
   if (tid == 0) {
     const float log_z = topp_log_ratio(kept_mass, total);
     RowResult r = a.ws.results[row];
@@ -2187,7 +2234,9 @@ __device__ void topp_exact(const StepArgs &a, unsigned long long p64, ToppShared
   }
   // kept: logits at or above the threshold key (nothing when the select failed)
   const unsigned long long kept_mass = ok ? sh.s.kept : 0ull;
-  auto kept = [&](float x) { return ok && (order_key(x) >> (32 - Dg::kKeyBits)) >= prefix; };
+  // the threshold logit: the key prefix, padded with zero bits
+  const float thr = key_value(prefix << (32 - Dg::kKeyBits));
+  auto kept = [&](float x) { return ok && x >= thr; };
   if (!bonus) {
     if (tid == 0) topp_finish_fast<T>(a, row, part, j, rowp, topp_log_ratio(kept_mass, total), kept);
     return;
@@ -2195,11 +2244,10 @@ __device__ void topp_exact(const StepArgs &a, unsigned long long p64, ToppShared
   // ---- bonus row: weights exp(s (x - M)) in exact fixed point ---------------
   const float M = block_max_nt<kToppThreads>(mx, sh.fl);
   const bool live = ok && M > kNegInf && M < -kNegInf;
-  auto kept_live = [&](float x) { return live && kept(x); };
   auto weight = [&](float x) -> unsigned long long {
     return static_cast<unsigned long long>(weight_fixed(x, M, a.balpha, sh.tab) >> kShift);
   };
-  const long long tok = topp_bonus_draw<T, VEC>(a, part, rowp, kept_live, weight, sh);
+  const long long tok = topp_bonus_draw<T, VEC>(a, part, rowp, live, thr, weight, sh);
   if (tid == 0) {
     const float log_z = topp_log_ratio(kept_mass, total);
     RowResult r = a.ws.results[row];
