@@ -1644,12 +1644,12 @@ static cudaError_t launch_tail(const StepArgs &a, cudaStream_t stream) {
 // token outside the target's nucleus gets logit -inf (weight 0), one outside
 // the draft's nucleus is reported (SMC_DEV_BAD_TOKEN: it could not have
 // been drawn).  The bonus row's token is redrawn by inverse CDF over the
-// kept tokens in exact integer weights (the quantised masses, or
-// exp(s (l - max)) in units of 2^-38 on the exact path): the row is cut
-// into up to kToppEntries runs of 32G consecutive 16-byte groups; one
-// coalesced pass sums the kept weights of each run, a scan over the runs
-// finds the one the draw lands in, and a block-wide scan over that run's
-// logits finds the token.
+// kept tokens in exact integer weights, exp(s (l - ref)) in units of 2^-38
+// (about 3e-10 relative; ref = lse / s on the main path, the row's max on
+// the exact path): the row is cut into up to kToppEntries runs of 128 G
+// consecutive 16-byte groups, each warp sums the kept weights of whole
+// runs, a scan over the runs finds the one the draw lands in, and a
+// block-wide scan over that run's logits finds the token.
 // ---------------------------------------------------------------------------
 constexpr int kToppThreads = 512;
 constexpr int kToppWarps = kToppThreads / 32;
@@ -1878,7 +1878,7 @@ __device__ long long topp_bonus_draw(const StepArgs &a, int part, const char *ro
   }
   unsigned long long total_w;
   const unsigned long long excl_w = block_excl_scan_u64<kToppThreads>(sum, sh.u64s, &total_w);
-  const float u = philox_uniform(a.seed, a.step, part, a.K, SMC_PURPOSE_BONUS);
+  const float u = philox_uniform(a.seed, a.step, part, a.bonus_position, a.bonus_purpose);
   const unsigned long long u24 = static_cast<unsigned long long>(u * 16777216.f);
   // floor(total * u), exactly: u = u24 / 2^24
   const unsigned long long target = __umul64hi(total_w, u24 << 40);
@@ -2126,11 +2126,14 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
     if (tid == 0) topp_finish_fast<T>(a, row, part, j, rowp, topp_log_ratio(kept_mass, total), kept);
     return true;
   }
-  // the bonus row: the same quantised masses as integer weights
+  // the bonus row: exact weights exp(s x - lse) = exp(s (x - lse / s)), as on
+  // the exact path (units of 2^-38; their sum is about 2^38), so that a draw
+  // can differ from exact arithmetic only within about 1e-9 of a boundary
+  stage_exp2_table(sh.tab);
+  __syncthreads();
+  const float ref = lse / a.tscale;
   auto weight = [&](float x) -> unsigned long long {
-    float y, t;
-    const uint32_t b = mass_bin(x, y, t);
-    return (static_cast<unsigned long long>(quantise(y, t)) * sh.frac[b & 7]) >> (b >> 3);
+    return static_cast<unsigned long long>(weight_fixed(x, ref, a.balpha, sh.tab) >> 12);
   };
   const long long tok = topp_bonus_draw<T, VEC>(a, part, rowp, true, thr, weight, sh);
   if (tid == 0) {

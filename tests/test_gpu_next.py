@@ -100,6 +100,41 @@ def test_draft_sample_matches_oracle(V, dtype, alpha):
           f"mismatched={mism}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_draft_sample_masked_vocab(dtype):
+    """Half of every row masked to -inf (a constrained vocabulary): draws land
+    in the unmasked half and match the oracle."""
+    w = WORKLOADS["single_prompt_v32000"].with_(B=2, N=8, dtype=dtype)
+    draft = make_step_inputs(w, 37, device="cuda")["draft"][:, :, 0].contiguous()
+    draft[..., ::2] = float("-inf")
+    params = smcsd.make_params(w.B, w.N, w.K, w.V, dtype, 1.0, 0.5, 37, 5)
+    ws = smcsd.alloc_workspace(params)
+    out = torch.empty(w.B * w.N, dtype=torch.int32, device="cuda")
+    smcsd.smc_draft_sample(params, draft, 1, out, ws)
+    torch.cuda.synchronize()
+    assert smcsd.smc_device_status(ws, clear=True) == 0
+    g = out.cpu().numpy().reshape(w.B, w.N)
+    assert (g % 2 == 1).all()
+    ref, margin = osmc.draft_sample(to_numpy_logits(draft), 1, alpha=1.0, seed=37, step=5,
+                                    dtype=dtype)
+    assert not ((g != ref) & (margin >= 1e-5)).any()
+
+
+def test_draft_sample_nonfinite_row_is_reported():
+    w = WORKLOADS["tiny_v64"].with_(B=1, N=4)
+    draft = make_step_inputs(w, 2, device="cuda")["draft"][:, :, 0].contiguous()
+    draft[0, 1, 7] = float("nan")
+    params = smcsd.make_params(1, 4, 3, 64, "f32", 1.0, 0.5, 2, 0)
+    ws = smcsd.alloc_workspace(params)
+    out = torch.zeros(4, dtype=torch.int32, device="cuda")
+    smcsd.smc_draft_sample(params, draft, 0, out, ws)
+    torch.cuda.synchronize()
+    # a status bit leaves that call's outputs unspecified; the call still
+    # writes a token or -1 for every particle
+    assert "nonfinite" in smcsd.status_names(smcsd.smc_device_status(ws, clear=True))
+    assert all(-1 <= t < 64 for t in out.tolist())
+
+
 def test_draft_sample_empty_row_reports_and_returns_minus_one():
     w = WORKLOADS["tiny_v64"].with_(B=1, N=4)
     draft = make_step_inputs(w, 2, device="cuda")["draft"][:, :, 0].contiguous()
