@@ -39,7 +39,8 @@ METRIC = "SMC step particle-tokens/s at V=128256 bf16; % of GB300 HBM roofline"
 WORKLOAD = "batched_serving_v128256"
 KERNEL = "row_stream_kernel"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "row_stream_kernel_batched_serving_v128256.md")
-KERNEL_SOURCES = ["smc_step.cu", "row_common.cuh", "device_common.cuh", "exp2_table.cuh"]
+KERNEL_SOURCES = ["smc_step.cu", "step_args.cuh", "row_common.cuh", "device_common.cuh",
+                  "exp2_table.cuh"]
 
 
 def parse_args():
