@@ -418,88 +418,6 @@ __device__ __forceinline__ int block_min_i(int v, int *scratch) {
 }
 
 
-// Variants for a CTA of NT threads (NT a multiple of 32, at most 1024);
-// scratch holds NT / 32 words.  All threads must call them.
-__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-// Exclusive prefix sum in thread order; *total gets the sum.
-template <int NT>
-__device__ __forceinline__ unsigned long long block_excl_scan_u64(unsigned long long v,
-                                                                  unsigned long long *scratch,
-                                                                  unsigned long long *total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  unsigned long long x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  __syncthreads();
-  if (lane == 31) scratch[warp] = x;
-  __syncthreads();
-  unsigned long long base = 0, all = 0;
-#pragma unroll
-  for (int w = 0; w < NT / 32; ++w) {
-    const unsigned long long s = scratch[w];
-    if (w < warp) base += s;
-    all += s;
-  }
-  *total = all;
-  return base + x - v;
-}
-template <int NT>
-__device__ __forceinline__ int block_max_int(int v, int *scratch) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __syncthreads();
-  if (lane == 0) scratch[warp] = v;
-  __syncthreads();
-  v = lane < NT / 32 ? scratch[lane] : -0x7fffffff - 1;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-template <int NT>
-__device__ __forceinline__ uint32_t block_min_u32(uint32_t v, int *scratch) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __syncthreads();
-  if (lane == 0) scratch[warp] = static_cast<int>(v);
-  __syncthreads();
-  v = lane < NT / 32 ? static_cast<uint32_t>(scratch[lane]) : 0xffffffffu;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-template <int NT>
-__device__ __forceinline__ uint32_t block_or_u32(uint32_t v, int *scratch) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __syncthreads();
-  if (lane == 0) scratch[warp] = static_cast<int>(v);
-  __syncthreads();
-  v = lane < NT / 32 ? static_cast<uint32_t>(scratch[lane]) : 0u;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-template <int NT>
-__device__ __forceinline__ float block_max_nt(float v, float *scratch) {
-  v = warp_max(v);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __syncthreads();
-  if (lane == 0) scratch[warp] = v;
-  __syncthreads();
-  v = lane < NT / 32 ? scratch[lane] : kNegInf;
-  return warp_max(v);
-}
-
 // ---------------------------------------------------------------------------
 // mbarrier and bulk-copy (TMA, non-tensor) primitives, sm_90+ PTX.
 // Every wait is bounded: it gives up after `limit` polls and returns false.

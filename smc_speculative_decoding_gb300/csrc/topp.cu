@@ -9,6 +9,96 @@
 
 namespace smcsd {
 
+// Variants for a CTA of NT threads (NT a multiple of 32, at most 1024);
+// scratch holds NT / 32 words.  All threads must call them.
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+// Exclusive prefix sum in thread order; *total gets the sum.  scratch holds
+// NT / 32 + 1 words: warp 0 scans the warp totals in place.
+template <int NT>
+__device__ __forceinline__ unsigned long long block_excl_scan_u64(unsigned long long v,
+                                                                  unsigned long long *scratch,
+                                                                  unsigned long long *total) {
+  constexpr int W = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned long long t = lane < W ? scratch[lane] : 0ull;
+    unsigned long long c = t;
+#pragma unroll
+    for (int o = 1; o < W; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, c, o);
+      if (lane >= o) c += y;
+    }
+    if (lane < W) scratch[lane] = c - t;
+    if (lane == W - 1) scratch[W] = c;
+  }
+  __syncthreads();
+  *total = scratch[W];
+  return scratch[warp] + x - v;
+}
+template <int NT>
+__device__ __forceinline__ int block_max_int(int v, int *scratch) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  v = lane < NT / 32 ? scratch[lane] : -0x7fffffff - 1;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+template <int NT>
+__device__ __forceinline__ uint32_t block_min_u32(uint32_t v, int *scratch) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) scratch[warp] = static_cast<int>(v);
+  __syncthreads();
+  v = lane < NT / 32 ? static_cast<uint32_t>(scratch[lane]) : 0xffffffffu;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+template <int NT>
+__device__ __forceinline__ uint32_t block_or_u32(uint32_t v, int *scratch) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) scratch[warp] = static_cast<int>(v);
+  __syncthreads();
+  v = lane < NT / 32 ? static_cast<uint32_t>(scratch[lane]) : 0u;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+template <int NT>
+__device__ __forceinline__ float block_max_nt(float v, float *scratch) {
+  v = warp_max(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  v = lane < NT / 32 ? scratch[lane] : kNegInf;
+  return warp_max(v);
+}
+
+
 // ---------------------------------------------------------------------------
 // Top-p (nucleus) restriction of every row, after the row combine: one CTA of
 // kToppThreads threads per row, two CTAs per SM (so that the rows being read
@@ -77,7 +167,7 @@ struct ToppShared {
   uint32_t cell[kToppMassBins * 32];  // mass cells; then the list, or the exact path's buffers
   float2 tab[64];
   uint32_t hq[256], hc[256];
-  unsigned long long u64s[kToppWarps];
+  unsigned long long u64s[kToppWarps + 1];
   int ints[kToppWarps];
   float fl[kToppWarps];
   unsigned frac[8];
@@ -110,23 +200,24 @@ template <typename T> struct ToppDigits {
 
 // Group g of a row: logits [g E, g E + E) as one 16-byte word (E = 8 bf16 or
 // 4 fp32); logits at or past V read as -inf.  VEC: rows are 16-byte aligned
-// and V is a multiple of E, so the group is one vector load.
+// and V is a multiple of E, so the group is one vector load.  Group and logit
+// indices fit in 32 bits (V <= 2^24).
 template <typename T, bool VEC>
-__device__ __forceinline__ uint4 topp_group(const char *rowp, int64_t g, int64_t V) {
-  if (VEC) return ld_stream16(rowp + g * 16);
+__device__ __forceinline__ uint4 topp_group(const char *rowp, int g, int V) {
+  if (VEC) return ld_stream16(rowp + static_cast<size_t>(g) * 16);
   uint32_t w[4];
   if (sizeof(T) == 4) {
     const float *r = reinterpret_cast<const float *>(rowp);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int64_t i = g * 4 + e;
+      const int i = g * 4 + e;
       w[e] = i < V ? __float_as_uint(__ldg(r + i)) : 0xff800000u;
     }
   } else {
     const unsigned short *r = reinterpret_cast<const unsigned short *>(rowp);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int64_t i = g * 8 + 2 * e;
+      const int i = g * 8 + 2 * e;
       const uint32_t lo = i < V ? __ldg(r + i) : 0xff80u;
       const uint32_t hi = i + 1 < V ? __ldg(r + i + 1) : 0xff80u;
       w[e] = lo | (hi << 16);
@@ -135,73 +226,45 @@ __device__ __forceinline__ uint4 topp_group(const char *rowp, int64_t g, int64_t
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Calls f(x) for every logit of the row, kToppUnroll groups in flight per
-// thread; thread t takes the groups g = t mod kToppThreads.
+// Calls f(v) for every group of the row (as one 16-byte word), kToppUnroll
+// groups in flight per thread; thread t takes the groups g = t mod
+// kToppThreads.
 template <typename T, bool VEC, typename F>
-__device__ __forceinline__ void topp_for_each(const char *rowp, int64_t V, F f) {
-  using Tr = LogitTraits<T>;
-  constexpr int E = Tr::kPerVec;
-  const int64_t ng = (V + E - 1) / E;
-  const uint4 pad = make_uint4(ToppDigits<T>::kNegInfWord, ToppDigits<T>::kNegInfWord,
-                               ToppDigits<T>::kNegInfWord, ToppDigits<T>::kNegInfWord);
-  for (int64_t g0 = threadIdx.x; g0 < ng; g0 += static_cast<int64_t>(kToppThreads) * kToppUnroll) {
-    uint4 v[kToppUnroll];
-#pragma unroll
-    for (int u = 0; u < kToppUnroll; ++u) {
-      const int64_t g = g0 + static_cast<int64_t>(u) * kToppThreads;
-      v[u] = g < ng ? topp_group<T, VEC>(rowp, g, V) : pad;
-    }
-#pragma unroll
-    for (int u = 0; u < kToppUnroll; ++u) {
-      if (g0 + static_cast<int64_t>(u) * kToppThreads >= ng) break;
-#pragma unroll
-      for (int e = 0; e < E; ++e) f(Tr::at(v[u], e));
-    }
-  }
-}
-
-// Calls f(v) for every group of the row (as one 16-byte word).
-template <typename T, bool VEC, typename F>
-__device__ __forceinline__ void topp_for_each_group(const char *rowp, int64_t V, F f) {
+__device__ __forceinline__ void topp_for_each_group(const char *rowp, int V, F f) {
   constexpr int E = LogitTraits<T>::kPerVec;
-  const int64_t ng = (V + E - 1) / E;
-  for (int64_t g0 = threadIdx.x; g0 < ng; g0 += static_cast<int64_t>(kToppThreads) * kToppUnroll) {
+  const int ng = (V + E - 1) / E;
+  for (int g0 = threadIdx.x; g0 < ng; g0 += kToppThreads * kToppUnroll) {
     uint4 v[kToppUnroll];
 #pragma unroll
     for (int u = 0; u < kToppUnroll; ++u) {
-      const int64_t g = g0 + static_cast<int64_t>(u) * kToppThreads;
+      const int g = g0 + u * kToppThreads;
       if (g < ng) v[u] = topp_group<T, VEC>(rowp, g, V);
     }
 #pragma unroll
     for (int u = 0; u < kToppUnroll; ++u) {
-      if (g0 + static_cast<int64_t>(u) * kToppThreads >= ng) break;
+      if (g0 + u * kToppThreads >= ng) break;
       f(v[u]);
     }
   }
 }
 
+// Calls f(x) for every logit of the row.
+template <typename T, bool VEC, typename F>
+__device__ __forceinline__ void topp_for_each(const char *rowp, int V, F f) {
+  topp_for_each_group<T, VEC>(rowp, V, [&](const uint4 &v) {
+#pragma unroll
+    for (int e = 0; e < LogitTraits<T>::kPerVec; ++e) f(LogitTraits<T>::at(v, e));
+  });
+}
+
 // The same, two consecutive logits at a time: f(x0, x1).
 template <typename T, bool VEC, typename F>
-__device__ __forceinline__ void topp_for_each_pair(const char *rowp, int64_t V, F f) {
-  using Tr = LogitTraits<T>;
-  constexpr int E = Tr::kPerVec;
-  const int64_t ng = (V + E - 1) / E;
-  const uint4 pad = make_uint4(ToppDigits<T>::kNegInfWord, ToppDigits<T>::kNegInfWord,
-                               ToppDigits<T>::kNegInfWord, ToppDigits<T>::kNegInfWord);
-  for (int64_t g0 = threadIdx.x; g0 < ng; g0 += static_cast<int64_t>(kToppThreads) * kToppUnroll) {
-    uint4 v[kToppUnroll];
+__device__ __forceinline__ void topp_for_each_pair(const char *rowp, int V, F f) {
+  topp_for_each_group<T, VEC>(rowp, V, [&](const uint4 &v) {
 #pragma unroll
-    for (int u = 0; u < kToppUnroll; ++u) {
-      const int64_t g = g0 + static_cast<int64_t>(u) * kToppThreads;
-      v[u] = g < ng ? topp_group<T, VEC>(rowp, g, V) : pad;
-    }
-#pragma unroll
-    for (int u = 0; u < kToppUnroll; ++u) {
-      if (g0 + static_cast<int64_t>(u) * kToppThreads >= ng) break;
-#pragma unroll
-      for (int e = 0; e < E; e += 2) f(Tr::at(v[u], e), Tr::at(v[u], e + 1));
-    }
-  }
+    for (int e = 0; e < LogitTraits<T>::kPerVec; e += 2)
+      f(LogitTraits<T>::at(v, e), LogitTraits<T>::at(v, e + 1));
+  });
 }
 
 // The largest logit of a group (NaN ignored; -inf for an all-NaN group).
@@ -227,12 +290,11 @@ __device__ long long topp_bonus_draw(const StepArgs &a, int part, const char *ro
   constexpr int E = Tr::kPerVec;
   constexpr int kRun = 32 * kToppUnroll;  // groups per warp read, and per run when G = 1
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t V = a.V;
-  const int64_t ng = (V + E - 1) / E;
-  const int64_t G = (ng + static_cast<int64_t>(kRun) * kToppEntries - 1) /
-                    (static_cast<int64_t>(kRun) * kToppEntries);
-  const int64_t gpr = kRun * G;  // groups per run
-  const int ne = static_cast<int>((ng + gpr - 1) / gpr);
+  const int V = a.V;
+  const int ng = (V + E - 1) / E;
+  const int G = (ng + kRun * kToppEntries - 1) / (kRun * kToppEntries);
+  const int gpr = kRun * G;  // groups per run
+  const int ne = (ng + gpr - 1) / gpr;
   const int rpw = (ne + kToppWarps - 1) / kToppWarps;  // runs per warp
   unsigned long long *const s_run = reinterpret_cast<unsigned long long *>(sh.cell);
   __syncthreads();  // the cells' previous contents are no longer read
@@ -241,12 +303,12 @@ __device__ long long topp_bonus_draw(const StepArgs &a, int part, const char *ro
   for (int r = warp * rpw; r < min(ne, (warp + 1) * rpw); ++r) {
     unsigned long long acc = 0;
     if (live) {
-      const int64_t r1 = min(ng, (r + 1) * gpr);
-      for (int64_t g0 = r * gpr + lane; g0 < r1; g0 += kRun) {
+      const int r1 = min(ng, (r + 1) * gpr);
+      for (int g0 = r * gpr + lane; g0 < r1; g0 += kRun) {
         uint4 v[kToppUnroll];
 #pragma unroll
         for (int u = 0; u < kToppUnroll; ++u) {
-          const int64_t g = g0 + 32 * u;
+          const int g = g0 + 32 * u;
           v[u] = g < r1 ? topp_group<T, VEC>(rowp, g, V)
                         : make_uint4(ToppDigits<T>::kNegInfWord, ToppDigits<T>::kNegInfWord,
                                      ToppDigits<T>::kNegInfWord, ToppDigits<T>::kNegInfWord);
@@ -298,10 +360,10 @@ __device__ long long topp_bonus_draw(const StepArgs &a, int part, const char *ro
   if (sel >= 0) {
     // the token within the run, by a block-wide scan in index order
     unsigned long long rem = target - sh.s.base;
-    const int64_t i0 = static_cast<int64_t>(sel) * gpr * E;
-    const int64_t i1 = min(V, i0 + gpr * E);
-    for (int64_t base = i0; base < i1; base += kToppThreads) {
-      const int64_t i = base + tid;
+    const int i0 = sel * gpr * E;
+    const int i1 = min(V, i0 + gpr * E);
+    for (int base = i0; base < i1; base += kToppThreads) {
+      const int i = base + tid;
       unsigned long long w = 0;
       if (i < i1) {
         const float x = Tr::scalar(rowp, i);
