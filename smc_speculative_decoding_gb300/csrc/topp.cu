@@ -2,6 +2,8 @@
 // smc_step_ex runs after the row combine when top_p < 1.
 #include <cmath>
 
+#include <cuda_bf16.h>
+
 #include "row_common.cuh"
 #include "kernels.h"
 #include "smcsd.h"
@@ -161,12 +163,14 @@ struct ToppScalars {
   uint32_t prefix;
   int sel, n;
   float xlo, xhi;
+  uint32_t lo2, hi2;
+  int klo, nk;  // direct mode: the 16-bit keys klo .. klo + nk - 1 of bf16 bin b*
   bool last_bin;
 };
 struct ToppShared {
   uint32_t cell[kToppMassBins * 32];  // mass cells; then the list, or the exact path's buffers
   float2 tab[64];
-  uint32_t hq[256], hc[256];
+  uint32_t hq[256], hc[256], hh[256];
   unsigned long long u64s[kToppWarps + 1];
   int ints[kToppWarps];
   float fl[kToppWarps];
@@ -275,6 +279,33 @@ __device__ __forceinline__ float group_max(const uint4 &v) {
                  fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
   const uint32_t m = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
   return fmaxf(bf16_lo(m), bf16_hi(m));
+}
+
+// Whether any logit of a group lies in [lo, hi].  For bf16 groups lo2 and
+// hi2 are the bounds as packed bf16 pairs (rounded outwards) and the test
+// takes four packed compares; NaN is in no interval.
+template <typename T>
+__device__ __forceinline__ bool group_hits(const uint4 &v, float lo, float hi, uint32_t lo2,
+                                           uint32_t hi2) {
+  if (sizeof(T) == 4) {
+    bool any = false;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x = LogitTraits<T>::at(v, e);
+      any |= x >= lo && x <= hi;
+    }
+    return any;
+  }
+  uint32_t m = 0;
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t ge, le;
+    asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(ge) : "r"(w[k]), "r"(lo2));
+    asm("set.le.u32.bf16x2 %0, %1, %2;" : "=r"(le) : "r"(w[k]), "r"(hi2));
+    m |= ge & le;
+  }
+  return m != 0u;
 }
 
 // The bonus row's draw over the kept logits {x >= thr} (none unless live):
@@ -392,6 +423,18 @@ __device__ __forceinline__ float topp_log_ratio(unsigned long long kept, unsigne
   return logf(to_f(kept) / to_f(total));
 }
 
+// The row of this CTA: the bonus rows (one per particle, the costliest) take
+// the first CTAs, so that their extra work is not left for the last wave;
+// the other 2K rows of each particle follow in order.
+__device__ __forceinline__ int topp_row(const StepArgs &a) {
+  const int rpp = 2 * a.K + 1;
+  const int parts = a.B * a.N;
+  const int b = blockIdx.x;
+  if (b < parts) return b * rpp + a.K;
+  const int f = b - parts, part = f / (2 * a.K), jj = f - part * (2 * a.K);
+  return part * rpp + (jj < a.K ? jj : jj + 1);
+}
+
 // Writes a row's nucleus result: the log kept mass on its log-sum-exp(s), and
 // for a drafted position the check of its token.
 template <typename T, typename KeptF>
@@ -414,7 +457,7 @@ template <typename T, bool VEC>
 __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb, ToppShared &sh) {
   constexpr int NT = kToppThreads;
   const int tid = threadIdx.x, lane = tid & 31;
-  const int row = blockIdx.x;
+  const int row = topp_row(a);
   const int rpp = 2 * a.K + 1;
   const int part = row / rpp, j = row - part * rpp;
   const char *rowp = row_base<T>(a, row);
@@ -496,91 +539,137 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
     const float slack = 1e-6f * fabsf(l2lse) / l2s;  // the rounding of l2lse - c
     sh.s.xlo = xl - 1e-5f * (fabsf(xl) + 1.f) - slack;
     sh.s.xhi = xh + 1e-5f * (fabsf(xh) + 1.f) + slack;
+    // the same bounds as bf16, rounded outwards, in both halves of a word
+    const uint32_t lb = __bfloat16_as_ushort(__float2bfloat16_rd(sh.s.xlo));
+    const uint32_t hb = __bfloat16_as_ushort(__float2bfloat16_ru(sh.s.xhi));
+    sh.s.lo2 = lb | (lb << 16);
+    sh.s.hi2 = hb | (hb << 16);
+    // bf16: a per-key histogram when b*'s interval spans at most 256 keys
+    const int klo = static_cast<int>(order_key(__uint_as_float(lb << 16)) >> 16);
+    const int khi = static_cast<int>(order_key(__uint_as_float(hb << 16)) >> 16);
+    sh.s.klo = klo;
+    sh.s.nk = sizeof(T) != 4 && bstar != kToppMassBins - 1 && khi - klo < 256 ? khi - klo + 1 : 0;
     // the last bin also holds everything below it, -inf and NaN included
     sh.s.last_bin = bstar == kToppMassBins - 1;
   }
+  if (tid < 256) { sh.hq[tid] = 0u; sh.hc[tid] = 0u; sh.hh[tid] = 0u; }
   __syncthreads();  // every cell has been read: they hold the list from here on
 
   // ---- pass 2 (L2): the threshold bin's keys and quantised masses -----------
   uint32_t *const lkey = cell;
   uint32_t *const lq = cell + kToppListCap;
   const float xlo = sh.s.xlo, xhi = sh.s.xhi;
+  const uint32_t lo2 = sh.s.lo2, hi2 = sh.s.hi2;
   const bool last_bin = sh.s.last_bin;
+  const int klo = sh.s.klo, nk = sh.s.nk;
   topp_for_each_group<T, VEC>(rowp, a.V, [&](const uint4 &v) {
-    // most groups hold no logit as large as x_lo
-    if (!last_bin && !(group_max<T>(v) >= xlo)) return;
+    // almost no group holds a logit of the interval
+    if (!last_bin && !group_hits<T>(v, xlo, xhi, lo2, hi2)) return;
 #pragma unroll
     for (int e = 0; e < LogitTraits<T>::kPerVec; ++e) {
       const float x = LogitTraits<T>::at(v, e);
       float y, t;
       if ((last_bin || (x >= xlo && x <= xhi)) && mass_bin(x, y, t) == static_cast<uint32_t>(bstar)) {
-        const int idx = atomicAdd(&sh.s.n, 1);
-        if (idx < kToppListCap) {
-          lkey[idx] = order_key(x);
-          lq[idx] = quantise(y, t);
+        const uint32_t q = quantise(y, t);
+        if (nk > 0) {
+          // x lies in [xlo, xhi], so its key lies in [klo, klo + nk)
+          const int d = static_cast<int>(order_key(x) >> 16) - klo;
+          const uint32_t old = atomicAdd(&sh.hq[d], q);
+          if (old + q < q) atomicAdd(&sh.hh[d], 1u);  // the carry out of the low word
+          atomicAdd(&sh.hc[d], 1u);
+        } else {
+          const int idx = atomicAdd(&sh.s.n, 1);
+          if (idx < kToppListCap) {
+            lkey[idx] = order_key(x);
+            lq[idx] = q;
+          }
         }
       }
     }
   });
   __syncthreads();
-  const int n = sh.s.n;
-  if (n > kToppListCap || n == 0) return false;  // the exact path
   const unsigned long long bin_above = sh.s.bin_above;
   const unsigned fr = sh.frac[bstar & 7];
   const int bsh = bstar >> 3;
   auto to_mass = [&](unsigned long long s) { return (s * fr) >> bsh; };
-
-  // ---- radix select inside the threshold bin ---------------------------------
-  // the bits in which the list's keys differ: [lb, hb]
-  uint32_t kmin = 0xffffffffu;
-  unsigned long long qsum = 0;
-  for (int i = tid; i < n; i += NT) {
-    kmin = min(kmin, lkey[i]);
-    qsum += lq[i];
-  }
-  kmin = block_min_u32<NT>(kmin, sh.ints);
-  uint32_t diff = 0u;
-  for (int i = tid; i < n; i += NT) diff |= lkey[i] ^ kmin;
-  diff = block_or_u32<NT>(diff, sh.ints);
-  unsigned long long qtot;
-  block_excl_scan_u64<NT>(qsum, sh.u64s, &qtot);
-  const int hb = diff == 0u ? -1 : 31 - __clz(diff);
-  const int lb = diff == 0u ? 0 : __ffs(diff) - 1;
-  uint32_t prefix = hb == 31 ? 0u : (kmin >> (hb + 1));
-  unsigned long long in_above = 0, in_kept = qtot;
-  for (int top = hb; top >= lb; top -= 8) {
-    const int w = min(8, top + 1 - lb), sh_lo = top + 1 - w;
-    const int nb = 1 << w;
-    if (tid < 256) { sh.hq[tid] = 0u; sh.hc[tid] = 0u; }
-    __syncthreads();
-    for (int i = tid; i < n; i += NT) {
-      const uint32_t key = lkey[i];
-      if (top == 31 || (key >> (top + 1)) == prefix) {
-        const uint32_t d = (key >> sh_lo) & static_cast<uint32_t>(nb - 1);
-        atomicAdd(&sh.hq[d], lq[i]);
-        atomicAdd(&sh.hc[d], 1u);
-      }
-    }
-    __syncthreads();
-    const int dd = nb - 1 - tid;  // thread tid takes digit nb - 1 - tid (descending)
-    const unsigned long long hv = tid < nb ? sh.hq[dd] : 0ull;
+  uint32_t vstar;
+  unsigned long long in_kept;
+  if (nk > 0) {
+    // ---- the threshold key from the per-key histogram, keys descending ------
+    const int d = nk - 1 - tid;  // thread tid takes key klo + nk - 1 - tid
+    const unsigned long long hv =
+        tid < nk ? (static_cast<unsigned long long>(sh.hh[d]) << 32) | sh.hq[d] : 0ull;
     unsigned long long tot_unused;
     const unsigned long long ex = block_excl_scan_u64<NT>(hv, sh.u64s, &tot_unused);
-    const bool c = tid < nb && sh.hc[dd] > 0u && bin_above + to_mass(in_above + ex) < limit;
+    const bool c = tid < nk && sh.hc[d] > 0u && bin_above + to_mass(ex) < limit;
     const int best = block_max_int<NT>(c ? tid : -1, sh.ints);
-    if (best < 0) return false;  // not reached: the bin's largest key is always a candidate
+    if (best < 0) return false;  // an empty threshold bin (not reached)
     if (tid == best) {
-      sh.s.prefix = (prefix << w) | static_cast<uint32_t>(dd);
-      sh.s.in_above = in_above + ex;
-      sh.s.in_kept = in_above + ex + hv;
+      const uint32_t k16 = static_cast<uint32_t>(klo + d);
+      // the 32-bit key of that bf16 logit: low half 0 (positive) or 1s (negative)
+      sh.s.prefix = (k16 << 16) | ((k16 & 0x8000u) ? 0u : 0xffffu);
+      sh.s.in_kept = ex + hv;
     }
     __syncthreads();
-    prefix = sh.s.prefix;
-    in_above = sh.s.in_above;
+    vstar = sh.s.prefix;
     in_kept = sh.s.in_kept;
+  } else {
+    const int n = sh.s.n;
+    if (n > kToppListCap || n == 0) return false;  // the exact path
+
+    // ---- otherwise a radix select over the list of the bin's logits -------------
+    // the bits in which the list's keys differ: [lb, hb]
+    uint32_t kmin = 0xffffffffu;
+    unsigned long long qsum = 0;
+    for (int i = tid; i < n; i += NT) {
+      kmin = min(kmin, lkey[i]);
+      qsum += lq[i];
+    }
+    kmin = block_min_u32<NT>(kmin, sh.ints);
+    uint32_t diff = 0u;
+    for (int i = tid; i < n; i += NT) diff |= lkey[i] ^ kmin;
+    diff = block_or_u32<NT>(diff, sh.ints);
+    unsigned long long qtot;
+    block_excl_scan_u64<NT>(qsum, sh.u64s, &qtot);
+    const int hb = diff == 0u ? -1 : 31 - __clz(diff);
+    const int lb = diff == 0u ? 0 : __ffs(diff) - 1;
+    uint32_t prefix = hb == 31 ? 0u : (kmin >> (hb + 1));
+    unsigned long long in_above = 0;
+    in_kept = qtot;
+    for (int top = hb; top >= lb; top -= 8) {
+      const int w = min(8, top + 1 - lb), sh_lo = top + 1 - w;
+      const int nb = 1 << w;
+      if (tid < 256) { sh.hq[tid] = 0u; sh.hc[tid] = 0u; }
+      __syncthreads();
+      for (int i = tid; i < n; i += NT) {
+        const uint32_t key = lkey[i];
+        if (top == 31 || (key >> (top + 1)) == prefix) {
+          const uint32_t d = (key >> sh_lo) & static_cast<uint32_t>(nb - 1);
+          atomicAdd(&sh.hq[d], lq[i]);
+          atomicAdd(&sh.hc[d], 1u);
+        }
+      }
+      __syncthreads();
+      const int dd = nb - 1 - tid;  // thread tid takes digit nb - 1 - tid (descending)
+      const unsigned long long hv = tid < nb ? sh.hq[dd] : 0ull;
+      unsigned long long tot_unused;
+      const unsigned long long ex = block_excl_scan_u64<NT>(hv, sh.u64s, &tot_unused);
+      const bool c = tid < nb && sh.hc[dd] > 0u && bin_above + to_mass(in_above + ex) < limit;
+      const int best = block_max_int<NT>(c ? tid : -1, sh.ints);
+      if (best < 0) return false;  // not reached: the bin's largest key is always a candidate
+      if (tid == best) {
+        sh.s.prefix = (prefix << w) | static_cast<uint32_t>(dd);
+        sh.s.in_above = in_above + ex;
+        sh.s.in_kept = in_above + ex + hv;
+      }
+      __syncthreads();
+      prefix = sh.s.prefix;
+      in_above = sh.s.in_above;
+      in_kept = sh.s.in_kept;
+    }
+    // the bits below lb are the same in every key of the list
+    vstar = hb < 0 ? kmin : (prefix << lb) | (kmin & ((1u << lb) - 1u));
   }
-  // the bits below lb are the same in every key of the list
-  const uint32_t vstar = hb < 0 ? kmin : (prefix << lb) | (kmin & ((1u << lb) - 1u));
   const unsigned long long kept_mass = bin_above + to_mass(in_kept);
   // keys order logits as floats do, with -0 = +0; NaN is never kept
   const float thr = key_value(vstar);
@@ -619,7 +708,7 @@ __device__ void topp_exact(const StepArgs &a, unsigned long long p64, ToppShared
   uint32_t *const s_lo = sh.cell;
   uint32_t *const s_hi = s_lo + kToppBins;
   const int tid = threadIdx.x;
-  const int row = blockIdx.x;
+  const int row = topp_row(a);
   const int rpp = 2 * a.K + 1;
   const int part = row / rpp, j = row - part * rpp;
   const bool bonus = j == a.K;
