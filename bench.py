@@ -552,13 +552,37 @@ def oracle_prompt_steps(w, budget_s, max_steps=None, seed=3000):
             return done, el
 
 
+def _oracle_worker(args):
+    """One process of the all-cores oracle timing: its own prompt stream."""
+    w, budget_s, seed = args
+    return oracle_prompt_steps(w, budget_s, seed=seed)
+
+
+def oracle_all_cores(w, budget_s):
+    """The same oracle on every host core at once, one independent prompt
+    stream per process (prompts share nothing); a spawned pool, since this
+    process already holds a CUDA context."""
+    import multiprocessing as mp
+    cores = os.cpu_count() or 1
+    try:
+        with mp.get_context("spawn").Pool(cores) as pool:
+            res = pool.map(_oracle_worker, [(w, budget_s, 3000 + i) for i in range(cores)])
+    except Exception as e:  # no pool on this host: report why
+        return {"value": None, "cores": cores, "error": str(e)[:200]}
+    n = sum(r[0] for r in res)
+    el = max(r[1] for r in res)
+    return {"value": n * w.N * (w.K + 1) / el, "unit": "particle-tokens/s", "cores": cores,
+            "sample": f"{n} prompt-steps over {cores} processes in {el:.1f} s"}
+
+
 def cpu_baseline(w, budget_s):
     n, el = oracle_prompt_steps(w, budget_s)
     return {"value": n * w.N * (w.K + 1) / el, "unit": "particle-tokens/s", "cores": 1,
             "kind": "oracle",
             "sample": f"{n} prompt-steps of {w.name} (1 prompt x {w.N} particles x "
                       f"{2 * w.K + 1} rows of V={w.V}, tail and KV remap) in {el:.1f} s, "
-                      f"numpy fp64, single thread"}
+                      f"numpy fp64, single thread",
+            "all_cores": oracle_all_cores(w, budget_s)}
 
 
 def run_reference(args, world, rank):
