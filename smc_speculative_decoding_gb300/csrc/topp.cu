@@ -463,7 +463,9 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
   const char *rowp = row_base<T>(a, row);
   const float lse = a.ws.results[row].lse;
   const float l2s = a.tscale * kLog2e, l2lse = lse * kLog2e;
-  const float qsc = __int_as_float((qb + 127) << 23);  // 2^qb
+  // 2^(qb - 149), a subnormal: r times it is a subnormal whose bits are
+  // rn(r 2^qb) (r 2^qb < 2^23), since fp32 arithmetic here keeps subnormals
+  const float qsc = __int_as_float(1 << qb);
   uint32_t *const cell = sh.cell;
   for (int i = tid; i < kToppMassBins * 32; i += NT) cell[i] = 0u;
   if (tid < 8) sh.frac[tid] = kToppFrac[tid];
@@ -474,7 +476,6 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
   // only by the rounding of the row's log-sum-exp), t = 1.5 2^23 + rn(-8 y)
   // holds the bin, 0..383, in its low bits.
   constexpr float kMagicB = 12582912.f;   // 1.5 2^23
-  constexpr float kMagicQ = 8388608.f;    // 2^23
   constexpr float kFloorY = -47.875f;     // -(kToppMassBins - 1) / 8
   auto mass_bin = [&](float x, float &y, float &t) -> uint32_t {
     y = fminf(fmaxf(__fmaf_rn(x, l2s, -l2lse), kFloorY), 0.f);
@@ -484,7 +485,7 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
   // pi relative to the top of its bin, rn(pi 2^(b/8) 2^qb), from y and t
   auto quantise = [&](float y, float t) -> uint32_t {
     const float r = fast_exp2(__fmaf_rn(t - kMagicB, 0.125f, y));  // in [2^-1/16, 2^1/16]
-    return static_cast<uint32_t>(__float_as_int(__fmaf_rn(r, qsc, kMagicQ)) - 0x4B000000);
+    return __float_as_uint(__fmul_rn(r, qsc));
   };
 
   // ---- pass 1 (HBM): the (bin, lane) cells ----------------------------------
@@ -492,8 +493,7 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
   // packed fp32x2 pipes
   {
     const unsigned long long L2S = f2dup(l2s), NL2LSE = f2dup(-l2lse), M8 = f2dup(-8.f),
-                             MB = f2dup(kMagicB), EIGHTH = f2dup(0.125f), QSC = f2dup(qsc),
-                             MQ = f2dup(kMagicQ);
+                             MB = f2dup(kMagicB), EIGHTH = f2dup(0.125f), QSC = f2dup(qsc);
     // cell index of bin b for this lane, b 32 + lane, from t's bits directly
     // (modulo 2^32: the bias cancels)
     const uint32_t lane_bias = static_cast<uint32_t>(lane) - (0x4B400000u << 5);
@@ -507,9 +507,9 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
       float e0, e1;
       f2unpack(fma2(sub2(Tt, MB), EIGHTH, Y), e0, e1);
       float q0, q1;
-      f2unpack(fma2(f2pack(fast_exp2(e0), fast_exp2(e1)), QSC, MQ), q0, q1);
-      atomicAdd(&cell[(__float_as_uint(t0) << 5) + lane_bias], __float_as_uint(q0) - 0x4B000000u);
-      atomicAdd(&cell[(__float_as_uint(t1) << 5) + lane_bias], __float_as_uint(q1) - 0x4B000000u);
+      f2unpack(mul2(f2pack(fast_exp2(e0), fast_exp2(e1)), QSC), q0, q1);
+      atomicAdd(&cell[(__float_as_uint(t0) << 5) + lane_bias], __float_as_uint(q0));
+      atomicAdd(&cell[(__float_as_uint(t1) << 5) + lane_bias], __float_as_uint(q1));
     });
   }
   __syncthreads();
