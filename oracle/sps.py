@@ -17,11 +17,20 @@ The notes do not restate the rule; the plain form of it is taken:
     step ends with K+1 tokens;
   * should the residual have no positive mass (only through rounding when
     p_j == q_j), the token is drawn from p_j instead.
+
+With a temperature T and a top-p threshold (the settings under which the
+notes evaluate the method, section 6), p and q are first replaced by
+softmax(l / T) restricted to their top-p nuclei and renormalised (the same
+reading as the SMC step's, ``smc.nucleus``); the rule above then runs on
+those distributions unchanged, so Theorem 1 holds for the tempered nucleus
+of the target.  A drafted token outside the draft's nucleus could not have
+been drawn and is reported.
 """
 import numpy as np
 
 from . import philox
-from .smc import row_logsumexp, inverse_cdf, bonus_weights, widen
+from .smc import (row_logsumexp, inverse_cdf, bonus_weights, widen, nucleus,
+                  temperature_scale)
 from .errors import OracleError, DEV_BAD_TOKEN
 
 
@@ -69,31 +78,97 @@ def verify_one(target_rows, draft_rows, tokens, u_accept, u_residual, u_bonus):
     return out, accept_margins, margin
 
 
-def sps_verify(target, draft, draft_tokens, *, seed=0, step=0, dtype=None):
+def tempered_logprobs(rows, scale, top_p):
+    """log of softmax(scale * row) restricted to the row's top-p nucleus and
+    renormalised, -inf outside it, for each row of ``rows`` [R, V] (fp64; the
+    product with an fp32 scale is exact).  Returns (log-probs [R, V], the
+    smallest nucleus margin over the rows; inf without a nucleus)."""
+    z = scale * np.asarray(rows, dtype=np.float64)
+    out = np.empty_like(z)
+    margin = np.inf
+    for r in range(z.shape[0]):
+        lse = row_logsumexp(z[r])
+        if top_p < 1.0:
+            kept, log_z, mg = nucleus(z[r], top_p)
+            margin = min(margin, mg)
+            out[r] = np.where(kept, z[r] - lse - log_z, -np.inf)
+        else:
+            out[r] = z[r] - lse
+    return out, margin
+
+
+def verify_one_logprobs(logp, logq, tokens, u_accept, u_residual, u_bonus):
+    """verify_one on given log-probability rows: logp [K+1, V] and logq [K, V]
+    (-inf outside a nucleus).  A drafted token with q = 0 could not have been
+    drawn from q and is reported.  Same results as verify_one."""
+    k_drafts, v_size = logq.shape
+    out = []
+    accept_margins = []
+    for k in range(k_drafts):
+        x = int(tokens[k])
+        if not 0 <= x < v_size:
+            raise OracleError(DEV_BAD_TOKEN, "drafted token outside [0, V)")
+        if logq[k, x] == -np.inf:
+            raise OracleError(DEV_BAD_TOKEN, "drafted token outside the draft's nucleus")
+        r = np.exp(logp[k, x] - logq[k, x])
+        accept_margins.append(abs(u_accept[k] - r))
+        if u_accept[k] < r:
+            out.append(x)
+            continue
+        p = np.exp(logp[k])
+        w = np.maximum(p - np.exp(logq[k]), 0.0)
+        if not np.sum(w) > 0:
+            w = p
+        y, margin = inverse_cdf(w, u_residual[k])
+        out.append(int(y))
+        return out, accept_margins, margin
+    last = logp[k_drafts]
+    y, margin = inverse_cdf(np.exp(last - np.max(last)), u_bonus)
+    out.append(int(y))
+    return out, accept_margins, margin
+
+
+def sps_verify(target, draft, draft_tokens, *, seed=0, step=0, dtype=None, temperature=1.0,
+               top_p=1.0):
     """Verify B independent prompts (N = 1 particle each).
 
     target [B, K+1, V], draft [B, K, V] fp64 (or stored logits widened per
     prompt when ``dtype`` is given, see ``smc.widen``), draft_tokens [B, K].
     Uniforms: ACCEPT and RESIDUAL keyed by (step, b, k), BONUS by (step, b, K).
+    With temperature != 1 or top_p < 1, p and q are the tempered nuclei
+    (``tempered_logprobs``).
     Returns dict(tokens_out [B, K+1] padded with -1, n_emitted [B],
-    accept_margin [B, K] (inf where not tested), final_margin [B]).
+    accept_margin [B, K] (inf where not tested), final_margin [B], and with
+    top_p < 1 topp_margin [B], each prompt's smallest nucleus margin).
     """
+    plain = temperature == 1.0 and top_p == 1.0
+    scale = temperature_scale(temperature)
     big_b, k1, _ = target.shape
     k_drafts = k1 - 1
     tokens_out = np.full((big_b, k1), -1, dtype=np.int64)
     n_emitted = np.zeros(big_b, dtype=np.int64)
     accept_margin = np.full((big_b, k_drafts), np.inf)
     final_margin = np.zeros(big_b)
+    topp_margin = np.full(big_b, np.inf)
     for b in range(big_b):
         ua = [philox.uniform(seed, step, b, k, philox.ACCEPT) for k in range(k_drafts)]
         ur = [philox.uniform(seed, step, b, k, philox.RESIDUAL) for k in range(k_drafts)]
         ub = philox.uniform(seed, step, b, k_drafts, philox.BONUS)
         t_rows = widen(target[b], dtype) if dtype else target[b]
         d_rows = widen(draft[b], dtype) if dtype else draft[b]
-        toks, margins, fm = verify_one(t_rows, d_rows, draft_tokens[b], ua, ur, ub)
+        if plain:
+            toks, margins, fm = verify_one(t_rows, d_rows, draft_tokens[b], ua, ur, ub)
+        else:
+            logp, mp = tempered_logprobs(t_rows, scale, top_p)
+            logq, mq = tempered_logprobs(d_rows, scale, top_p)
+            topp_margin[b] = min(mp, mq)
+            toks, margins, fm = verify_one_logprobs(logp, logq, draft_tokens[b], ua, ur, ub)
         tokens_out[b, :len(toks)] = toks
         n_emitted[b] = len(toks)
         accept_margin[b, :len(margins)] = margins
         final_margin[b] = fm
-    return dict(tokens_out=tokens_out, n_emitted=n_emitted,
-                accept_margin=accept_margin, final_margin=final_margin)
+    res = dict(tokens_out=tokens_out, n_emitted=n_emitted,
+               accept_margin=accept_margin, final_margin=final_margin)
+    if top_p < 1.0:
+        res["topp_margin"] = topp_margin
+    return res

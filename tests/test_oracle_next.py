@@ -274,3 +274,98 @@ def test_top_p_step_bonus_stays_in_the_nucleus_and_bad_drafts_raise():
     toks[0, 0, 1] = int(np.argmin(draft[0, 0, 1]))
     with pytest.raises(OracleError):
         smc.smc_step(target, draft, toks, np.zeros((1, 6)), top_p=0.7)
+
+
+# ---------------------------------------------------------------------------
+# speculative-sampling verify under temperature and top-p
+# ---------------------------------------------------------------------------
+from oracle import sps  # noqa: E402
+from oracle.errors import DEV_BAD_TOKEN  # noqa: E402
+
+SPS_GRID = (np.arange(2 ** 16) + 0.5) / 2 ** 16   # midpoints of a fine u lattice
+
+
+def _tempered_nucleus(row, temperature, top_p):
+    """softmax(row / T) restricted to its nucleus (found by sorting) and
+    renormalised: an independent restatement."""
+    z = row * float(np.float32(1.0) / np.float32(temperature))
+    kept = _nucleus_by_sorting(z, top_p)
+    p = np.where(kept, softmax(z), 0.0)
+    return p / p.sum()
+
+
+@pytest.mark.parametrize("temperature,top_p", [(0.7, 0.8), (1.5, 0.6), (1.0, 0.95)])
+def test_sps_tempered_nucleus_theorem1(temperature, top_p):
+    """Every emitted token follows the tempered nucleus of the target.  For
+    one position, verify_one_logprobs is run with every drafted token x of
+    the draft's nucleus and with uniforms on a lattice: the acceptance rate
+    of x and the law of the residual draw give the law of the emitted token,
+    sum_x q_top(x) [acc(x) 1{v = x} + (1 - acc(x)) res(v)], which must be
+    p_top (Theorem 1 applied to the restricted distributions).  Catches a
+    ratio or residual taken on the unrestricted p or q, or a nucleus that is
+    not renormalised."""
+    rng = np.random.default_rng(int(temperature * 10 + top_p * 100))
+    V = 8
+    grid = (np.arange(4096) + 0.5) / 4096
+    target = np.round(rng.normal(0, 1.5, (2, V)) * 8) / 8
+    draft = np.round((target[:1] + rng.normal(0, 1.0, (1, V))) * 8) / 8
+    scale = smc.temperature_scale(temperature)
+    logp, _ = sps.tempered_logprobs(target, scale, top_p)
+    logq, _ = sps.tempered_logprobs(draft, scale, top_p)
+    p = _tempered_nucleus(target[0], temperature, top_p)
+    q = _tempered_nucleus(draft[0], temperature, top_p)
+    assert np.allclose(np.exp(logp[0]), p, atol=1e-12)
+    assert np.allclose(np.exp(logq[0]), q, atol=1e-12)
+
+    def run(x, u, u2):
+        return sps.verify_one_logprobs(logp, logq, [x], [u], [u2], 0.5)[0]
+    law = np.zeros(V)
+    res = None
+    for x in np.flatnonzero(q > 0):
+        acc = np.mean([len(run(x, u, 0.5)) == 2 for u in grid])
+        if acc < 1 and res is None:
+            u_rej = 1 - 2 ** -24                       # rejects whenever p/q < 1
+            res = np.bincount([run(x, u_rej, u2)[0] for u2 in grid], minlength=V) / len(grid)
+        law[x] += q[x] * acc
+        if acc < 1:
+            law += q[x] * (1 - acc) * res
+    assert np.abs(law - p).max() < 3 * V / len(grid), (law, p)
+
+
+def test_sps_temperature_divides_the_logits():
+    """Rows scaled by 4 at temperature 4 give exactly the outputs of the
+    plain verify on the rows themselves (1/4 is exact in fp32)."""
+    rng = np.random.default_rng(11)
+    B, K, V = 40, 3, 16
+    target = rng.normal(0, 2, (B, K + 1, V))
+    draft = target[:, :K] + rng.normal(0, 1, (B, K, V))
+    toks = rng.integers(0, V, (B, K))
+    plain = sps.sps_verify(target, draft, toks, seed=3, step=4)
+    hot = sps.sps_verify(4.0 * target, 4.0 * draft, toks, seed=3, step=4, temperature=4.0)
+    assert (plain["n_emitted"] < K + 1).any()
+    assert np.array_equal(plain["tokens_out"], hot["tokens_out"])
+    assert np.array_equal(plain["n_emitted"], hot["n_emitted"])
+
+
+def test_sps_top_p_bonus_inside_nucleus_and_bad_draft_raises():
+    rng = np.random.default_rng(5)
+    B, K, V = 60, 2, 32
+    target = rng.normal(0, 2, (B, K + 1, V))
+    draft = target[:, :K] + rng.normal(0, 0.3, (B, K, V))
+    scale = smc.temperature_scale(1.0)
+    # drafted tokens: each draft row's argmax, always inside its nucleus
+    toks = draft.argmax(-1)
+    out = sps.sps_verify(target, draft, toks, seed=1, step=0, top_p=0.5)
+    assert (out["n_emitted"] < K + 1).any() and (out["n_emitted"] == K + 1).any()
+    for b in range(B):
+        n = out["n_emitted"][b]
+        last = out["tokens_out"][b, n - 1]
+        # a bonus draw, or a residual draw (zero outside the target's nucleus)
+        assert _nucleus_by_sorting(target[b, n - 1] * scale, 0.5)[last]
+    bad = toks.copy()
+    b0 = 0
+    kept_q = _nucleus_by_sorting(draft[b0, 0], 0.5)
+    bad[b0, 0] = int(np.flatnonzero(~kept_q)[0])
+    with pytest.raises(OracleError) as e:
+        sps.sps_verify(target[:1], draft[:1], bad[:1], seed=1, step=0, top_p=0.5)
+    assert e.value.kind == DEV_BAD_TOKEN
