@@ -288,6 +288,22 @@ int32_t sps_verify(const smc_params *p, const void *target_logits,
                    int32_t *tokens_out, int32_t *n_emitted, void *workspace,
                    size_t ws_bytes, void *stream);
 
+/* sps_verify under a temperature and a top-p nucleus ([SpS] section 6
+ * evaluates the method at several temperatures and with nucleus sampling).
+ * opts may be NULL (sps_verify itself); otherwise opts->log_potential must be
+ * NULL (SMC_ERR_ARG: one particle has no weight to tilt), and temperature and
+ * top_p are as for smc_step_ex: p and q become softmax(l / T) restricted to
+ * their top-p nuclei and renormalised, and the acceptance rule, the residual
+ * max(0, p_j - q_j) and the bonus draw run on those.  A drafted token outside
+ * the draft's nucleus sets SMC_DEV_BAD_TOKEN; one outside the target's
+ * nucleus is always rejected.  Arguments, outputs and errors otherwise as
+ * sps_verify. */
+int32_t sps_verify_ex(const smc_params *p, const void *target_logits,
+                      const void *draft_logits, const int32_t *draft_tokens,
+                      int32_t *tokens_out, int32_t *n_emitted,
+                      const smc_step_opts *opts, void *workspace, size_t ws_bytes,
+                      void *stream);
+
 
 /* ---- allocation-free variant of smc_step -------------------------------
  * No counterpart in the pages: a deployment convenience.  For callers that

@@ -69,6 +69,9 @@ _SIGS = {
                                              ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "sps_verify": (ctypes.c_int32, [ctypes.POINTER(smc_params)] + [ctypes.c_void_p] * 5 +
                    [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "sps_verify_ex": (ctypes.c_int32, [ctypes.POINTER(smc_params)] + [ctypes.c_void_p] * 5 +
+                      [ctypes.POINTER(smc_step_opts), ctypes.c_void_p, ctypes.c_size_t,
+                       ctypes.c_void_p]),
     "smc_set_row_timing_events": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_void_p]),
     "smc_step_ex": (ctypes.c_int32, [ctypes.POINTER(smc_params), ctypes.POINTER(smc_step_opts)] +
                     [ctypes.c_void_p] * 8 +
@@ -298,6 +301,22 @@ def sps_verify(params, target_logits, draft_logits, draft_tokens, tokens_out, n_
         _ptr(draft_tokens, "draft_tokens", torch.int32, B * K),
         _ptr(tokens_out, "tokens_out", torch.int32, B * (K + 1)),
         _ptr(n_emitted, "n_emitted", torch.int32, B),
+        _ptr(workspace, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def sps_verify_ex(params, target_logits, draft_logits, draft_tokens, tokens_out, n_emitted,
+                  workspace, stream=None, temperature=1.0, top_p=1.0):
+    """sps_verify under a temperature and a top-p nucleus (sps_verify_ex in
+    smcsd.h)."""
+    B, K, V = params.B, params.K, params.V
+    ld = _logit_dtype(params)
+    opts = smc_step_opts(None, float(temperature), float(top_p))
+    _check("sps_verify_ex", lib().sps_verify_ex(
+        ctypes.byref(params), _ptr(target_logits, "target_logits", ld, B * (K + 1) * V),
+        _ptr(draft_logits, "draft_logits", ld, B * K * V),
+        _ptr(draft_tokens, "draft_tokens", torch.int32, B * K),
+        _ptr(tokens_out, "tokens_out", torch.int32, B * (K + 1)),
+        _ptr(n_emitted, "n_emitted", torch.int32, B), ctypes.byref(opts),
         _ptr(workspace, "workspace"), workspace.numel(), _stream(stream)))
 
 

@@ -307,11 +307,30 @@ int32_t kv_blocktable_remap(const smc_params *p, const smc_kv *kv, const int32_t
 int32_t sps_verify(const smc_params *p, const void *target_logits, const void *draft_logits,
                    const int32_t *draft_tokens, int32_t *tokens_out, int32_t *n_emitted,
                    void *workspace, size_t ws_bytes, void *stream) {
+  return sps_verify_ex(p, target_logits, draft_logits, draft_tokens, tokens_out, n_emitted,
+                       nullptr, workspace, ws_bytes, stream);
+}
+
+int32_t sps_verify_ex(const smc_params *p, const void *target_logits, const void *draft_logits,
+                      const int32_t *draft_tokens, int32_t *tokens_out, int32_t *n_emitted,
+                      const smc_step_opts *opts, void *workspace, size_t ws_bytes,
+                      void *stream) {
   if (!p) return SMC_ERR_ARG;
   if (p->dtype != SMC_F32 && p->dtype != SMC_BF16) return SMC_ERR_DTYPE;
   if (!shape_ok(p) || p->N != 1 || p->alpha != 1.f || p->B > 65535) return SMC_ERR_ARG;
   if (!target_logits || !draft_logits || !draft_tokens || !tokens_out || !n_emitted) {
     return SMC_ERR_ARG;
+  }
+  Shape s = to_shape(p);
+  if (opts) {
+    if (opts->reserved[0] != 0 || opts->reserved[1] != 0) return SMC_ERR_ARG;
+    if (opts->log_potential) return SMC_ERR_ARG;  // one particle: no weights to tilt
+    if (!(opts->top_p > 0.f && opts->top_p <= 1.f)) return SMC_ERR_ARG;
+    s.top_p = opts->top_p;
+    const float t = opts->temperature;
+    if (!(std::isfinite(t) && t > 0.f)) return SMC_ERR_ARG;
+    s.tscale = 1.f / t;
+    if (!(std::isfinite(s.tscale) && s.tscale > 0.f)) return SMC_ERR_ARG;
   }
   Workspace ws{};
   const int32_t rc = prepare_ws(p, nullptr, workspace, ws_bytes, &ws);
@@ -319,7 +338,6 @@ int32_t sps_verify(const smc_params *p, const void *target_logits, const void *d
   StepOutputs out{};
   out.tokens_out = tokens_out;
   out.n_emitted = n_emitted;
-  const Shape s = to_shape(p);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_step_rows(s, 1, target_logits, draft_logits, draft_tokens, out, nullptr,
                                    ws, st);

@@ -10,6 +10,10 @@
 //   sps_residual_kernel: per-chunk residual mass; the last CTA of the prompt
 //                        picks the chunk and the element.
 // CTAs of prompts with no rejection exit at once.
+//
+// Under a temperature T the rows are s l with s = fl32(1/T); under top-p each
+// of p_j and q_j is restricted to its nucleus {l >= thr} (the thresholds the
+// nucleus kernel left in the rows' results) and renormalised.
 #include <cmath>
 
 #include "row_common.cuh"
@@ -21,11 +25,31 @@ namespace smcsd {
 struct SpsArgs {
   const char *target, *draft;
   int B, K, V, nch;
+  float tscale;  // s = 1/T
+  int topp;      // nonzero: thresholds in ws.results[row].tok
   uint64_t seed;
   uint32_t step;
   int32_t *tokens_out;
   Workspace ws;
 };
+
+// The nucleus thresholds of rows p_j and q_j of prompt b (-inf: every logit).
+__device__ __forceinline__ void sps_thresholds(const SpsArgs &a, int b, int jr, float *thr_p,
+                                               float *thr_q) {
+  const float kAll = kNegInf;
+  if (!a.topp) { *thr_p = *thr_q = kAll; return; }
+  const size_t base = static_cast<size_t>(b) * (2 * a.K + 1);
+  *thr_p = __int_as_float(__ldcg(&a.ws.results[base + jr].tok));
+  *thr_q = __int_as_float(__ldcg(&a.ws.results[base + a.K + 1 + jr].tok));
+}
+
+// exp(s x - L) for a float-float L, with s x taken exactly (two_prod).
+__device__ __forceinline__ ff prob_term_s(float x, float s, ff big_l, const float2 *tab) {
+  if (!(x > kNegInf)) return {0.f, 0.f};
+  const ff sx = two_prod(s, x);
+  const ff d = two_sum(sx.hi, -big_l.hi);
+  return accurate_exp(d.hi, d.lo + (sx.lo - big_l.lo), tab);
+}
 
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kThreads) sps_stats_kernel(const SpsArgs a) {
@@ -43,6 +67,8 @@ __global__ void __launch_bounds__(kThreads) sps_stats_kernel(const SpsArgs a) {
   const char *rows[2] = {
       a.target + (static_cast<size_t>(b) * (a.K + 1) + jr) * static_cast<size_t>(a.V) * G::kESZ,
       a.draft + (static_cast<size_t>(b) * a.K + jr) * static_cast<size_t>(a.V) * G::kESZ};
+  float thr[2];
+  sps_thresholds(a, b, jr, &thr[0], &thr[1]);
   for (int r = 0; r < 2; ++r) {
     float x[G::kEPT];
     load_chunk<T, VEC>(rows[r] + c0 * G::kESZ, n_valid, x);
@@ -53,7 +79,8 @@ __global__ void __launch_bounds__(kThreads) sps_stats_kernel(const SpsArgs a) {
     ff S{0.f, 0.f};
     if (mc > kNegInf && mc < -kNegInf) {
 #pragma unroll
-      for (int e = 0; e < G::kEPT; ++e) ff_accum(S, weight_term(x[e], mc, 1.f, s_tab));
+      for (int e = 0; e < G::kEPT; ++e)
+        if (x[e] >= thr[r]) ff_accum(S, weight_term(x[e], mc, a.tscale, s_tab));
     }
     S = block_ff_sum(ff_norm(S), s_ff);
     if (tid == 0) a.ws.sps_part_pq[(static_cast<size_t>(b) * a.nch + c) * 2 + r] = make_float4(mc, S.hi, S.lo, 0.f);
@@ -80,11 +107,13 @@ __global__ void __launch_bounds__(kThreads) sps_stats_kernel(const SpsArgs a) {
         ff val{0.f, 0.f};
         if (cc < a.nch && M > kNegInf) {
           const float4 q = __ldcg(&a.ws.sps_part_pq[(static_cast<size_t>(b) * a.nch + cc) * 2 + r]);
-          if (q.x > kNegInf) val = ff_mul(ff{q.y, q.z}, ff_norm(weight_term(q.x, M, 1.f, s_tab)));
+          if (q.x > kNegInf) val = ff_mul(ff{q.y, q.z}, ff_norm(weight_term(q.x, M, a.tscale, s_tab)));
         }
         tot = ff_add(tot, warp_ff_sum(val));
       }
-      const ff l = ff_from_double(static_cast<double>(M) + log(ff_to_double(tot)));
+      // log of the (kept) mass of exp(s l): s M + log(total), s M exact in double
+      const ff l = ff_from_double(static_cast<double>(a.tscale) * static_cast<double>(M) +
+                                  log(ff_to_double(tot)));
       lse[r][0] = l.hi;
       lse[r][1] = l.lo;
     }
@@ -95,13 +124,12 @@ __global__ void __launch_bounds__(kThreads) sps_stats_kernel(const SpsArgs a) {
   }
 }
 
-// Residual weight max(0, p_v - q_v) of vocabulary index i.
-template <typename T>
-__device__ __forceinline__ ff residual_term(const char *prow, const char *qrow, int64_t i, ff lp,
-                                            ff lq, const float2 *tab) {
-  using Tr = LogitTraits<T>;
-  const ff p = ff_norm(prob_term(Tr::scalar(prow, i), lp, tab));
-  const ff q = ff_norm(prob_term(Tr::scalar(qrow, i), lq, tab));
+// max(0, p_v - q_v) for logits xp, xq, each probability zero outside its
+// nucleus.
+__device__ __forceinline__ ff residual_of(float xp, float xq, float s, ff lp, ff lq, float thr_p,
+                                          float thr_q, const float2 *tab) {
+  const ff p = xp >= thr_p ? ff_norm(prob_term_s(xp, s, lp, tab)) : ff{0.f, 0.f};
+  const ff q = xq >= thr_q ? ff_norm(prob_term_s(xq, s, lq, tab)) : ff{0.f, 0.f};
   const ff d = ff_sub(p, q);
   return d.hi > 0.f ? d : ff{0.f, 0.f};
 }
@@ -124,6 +152,8 @@ __global__ void __launch_bounds__(kThreads) sps_residual_kernel(const SpsArgs a)
   stage_exp2_table(s_tab);
   const float4 st = a.ws.sps_stats[b];
   const ff lp{st.x, st.y}, lq{st.z, st.w};
+  float thr_p, thr_q;
+  sps_thresholds(a, b, jr, &thr_p, &thr_q);
   const int64_t c0 = static_cast<int64_t>(c) * G::kCH;
   const int n_valid = static_cast<int>(min(static_cast<int64_t>(G::kCH), a.V - c0));
   const char *prow = a.target + (static_cast<size_t>(b) * (a.K + 1) + jr) * static_cast<size_t>(a.V) * G::kESZ;
@@ -135,9 +165,7 @@ __global__ void __launch_bounds__(kThreads) sps_residual_kernel(const SpsArgs a)
   ff R{0.f, 0.f};
 #pragma unroll
   for (int e = 0; e < G::kEPT; ++e) {
-    const ff p = ff_norm(prob_term(xp[e], lp, s_tab));
-    const ff q = ff_norm(prob_term(xq[e], lq, s_tab));
-    const ff d = ff_sub(p, q);
+    const ff d = residual_of(xp[e], xq[e], a.tscale, lp, lq, thr_p, thr_q, s_tab);
     if (d.hi > 0.f) ff_accum(R, d);
   }
   R = block_ff_sum(ff_norm(R), s_ff);
@@ -179,7 +207,7 @@ __global__ void __launch_bounds__(kThreads) sps_residual_kernel(const SpsArgs a)
       auto chunk_mass = [&](int cc, ff *val, ff *f) {
         const float4 q = __ldcg(&pq[cc * 2]);
         if (q.x > kNegInf) {
-          *f = ff_norm(weight_term(q.x, M, 1.f, s_tab));
+          *f = ff_norm(weight_term(q.x, M, a.tscale, s_tab));
           *val = ff_mul(ff{q.y, q.z}, *f);
         }
       };
@@ -210,12 +238,19 @@ __global__ void __launch_bounds__(kThreads) sps_residual_kernel(const SpsArgs a)
     if (s_mode == 0) {
       tok = block_select_in_chunk(
           sc0, len, s_rem,
-          [&](int64_t i) { return residual_term<T>(prow, qrow, i, lp, lq, s_tab); }, s_ff, s_int);
+          [&](int64_t i) {
+            return residual_of(Tr::scalar(prow, i), Tr::scalar(qrow, i), a.tscale, lp, lq, thr_p,
+                               thr_q, s_tab);
+          },
+          s_ff, s_int);
     } else {
       const float cm = s_sel_m;
       tok = block_select_in_chunk(
           sc0, len, s_rem,
-          [&](int64_t i) { return weight_term(Tr::scalar(prow, i), cm, 1.f, s_tab); },
+          [&](int64_t i) {
+            const float x = Tr::scalar(prow, i);
+            return x >= thr_p ? weight_term(x, cm, a.tscale, s_tab) : ff{0.f, 0.f};
+          },
           s_ff, s_int);
     }
   }
@@ -231,6 +266,8 @@ cudaError_t launch_sps_residual(const Shape &s, const void *target, const void *
   a.draft = static_cast<const char *>(draft);
   a.B = s.B; a.K = s.K; a.V = s.V;
   a.nch = chunks_per_row(s.dtype, s.V);
+  a.tscale = s.tscale;
+  a.topp = s.top_p < 1.f;
   a.seed = s.seed; a.step = s.step;
   a.tokens_out = tokens_out;
   a.ws = ws;

@@ -435,13 +435,17 @@ __device__ __forceinline__ int topp_row(const StepArgs &a) {
   return part * rpp + (jj < a.K ? jj : jj + 1);
 }
 
-// Writes a row's nucleus result: the log kept mass on its log-sum-exp(s), and
-// for a drafted position the check of its token.
+// Writes a row's nucleus result: the log kept mass on its log-sum-exp(s), for
+// a drafted position the check of its token, and the threshold logit thr
+// (kept: l >= thr) in the row's otherwise unused token slot, where the
+// speculative-sampling residual reads it.
 template <typename T, typename KeptF>
 __device__ __forceinline__ void topp_finish_fast(const StepArgs &a, int row, int part, int j,
-                                                 const char *rowp, float log_z, KeptF kept) {
+                                                 const char *rowp, float log_z, KeptF kept,
+                                                 float thr) {
   using Tr = LogitTraits<T>;
   RowResult r = a.ws.results[row];
+  r.tok = __float_as_int(thr);
   const int tok = a.tokens[static_cast<size_t>(part) * a.K + (j < a.K ? j : j - a.K - 1)];
   if (tok >= 0 && tok < a.V && !kept(Tr::scalar(rowp, tok))) {
     if (j < a.K) r.g = kNegInf;                         // outside the target's nucleus
@@ -675,7 +679,7 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
   const float thr = key_value(vstar);
   auto kept = [&](float x) { return x >= thr; };
   if (j != a.K) {
-    if (tid == 0) topp_finish_fast<T>(a, row, part, j, rowp, topp_log_ratio(kept_mass, total), kept);
+    if (tid == 0) topp_finish_fast<T>(a, row, part, j, rowp, topp_log_ratio(kept_mass, total), kept, thr);
     return true;
   }
   // the bonus row: exact weights exp(s x - lse) = exp(s (x - lse / s)), as on
@@ -793,7 +797,9 @@ __device__ void topp_exact(const StepArgs &a, unsigned long long p64, ToppShared
   const float thr = key_value(prefix << (32 - Dg::kKeyBits));
   auto kept = [&](float x) { return ok && x >= thr; };
   if (!bonus) {
-    if (tid == 0) topp_finish_fast<T>(a, row, part, j, rowp, topp_log_ratio(kept_mass, total), kept);
+    if (tid == 0)
+      topp_finish_fast<T>(a, row, part, j, rowp, topp_log_ratio(kept_mass, total), kept,
+                          ok ? thr : -kNegInf);
     return;
   }
   // ---- bonus row: weights exp(s (x - M)) in exact fixed point ---------------

@@ -184,17 +184,25 @@ def check_kv(w, runner, kv_in, g_anc, g_res):
             assert np.array_equal(got["cow_pairs"][b, :len(pairs)], np.array(pairs)), "cow pairs differ"
 
 
-def sps_lockstep(w, seed=0, step=0, tie=1e-5):
-    """One sps_verify call (N = 1) against the oracle; returns the Tally."""
+def sps_lockstep(w, seed=0, step=0, tie=1e-5, temperature=1.0, top_p=1.0, tokens_fn=None):
+    """One sps_verify call (N = 1) against the oracle; returns the Tally.
+    temperature != 1 or top_p < 1 goes through sps_verify_ex; tokens_fn(inp,
+    step) may replace the drafted tokens first."""
     assert w.N == 1
     B, K = w.B, w.K
     inp = make_step_inputs(w, seed, device="cuda", step=step)
+    if tokens_fn is not None:
+        tokens_fn(inp, step)
     params = smcsd.make_params(B, 1, K, w.V, w.dtype, 1.0, 0.5, seed, step)
     ws = smcsd.alloc_workspace(params)
     tokens_out = torch.empty(B * (K + 1), dtype=torch.int32, device="cuda")
     n_emitted = torch.empty(B, dtype=torch.int32, device="cuda")
-    smcsd.sps_verify(params, inp["target"], inp["draft"], inp["draft_tokens"], tokens_out,
-                     n_emitted, ws)
+    if temperature == 1.0 and top_p == 1.0:
+        smcsd.sps_verify(params, inp["target"], inp["draft"], inp["draft_tokens"], tokens_out,
+                         n_emitted, ws)
+    else:
+        smcsd.sps_verify_ex(params, inp["target"], inp["draft"], inp["draft_tokens"], tokens_out,
+                            n_emitted, ws, temperature=temperature, top_p=top_p)
     torch.cuda.synchronize()
     bits = smcsd.smc_device_status(ws, clear=True)
     assert bits == 0, smcsd.status_names(bits)
@@ -203,13 +211,20 @@ def sps_lockstep(w, seed=0, step=0, tie=1e-5):
     x = inp["draft_tokens"].cpu().numpy().reshape(B, K).astype(np.int64)
     ref = osps.sps_verify(to_numpy_logits(inp["target"]).reshape(B, K + 1, w.V),
                           to_numpy_logits(inp["draft"]).reshape(B, K, w.V), x,
-                          seed=seed, step=step, dtype=w.dtype)
+                          seed=seed, step=step, dtype=w.dtype, temperature=temperature,
+                          top_p=top_p)
+    # a nucleus boundary within 1e-5 of top_p flags the whole prompt
+    tp = ref["topp_margin"] < 1e-5 if "topp_margin" in ref else np.zeros(B, dtype=bool)
     tally = Tally()
     for b in range(B):
         n_ref = ref["n_emitted"][b]
-        acc_flag = (ref["accept_margin"][b] < tie).any()
+        acc_flag = (ref["accept_margin"][b] < tie).any() or tp[b]
         if g_n[b] != n_ref:
             tally.add(1, [acc_flag], [True], f"accepted count of prompt {b}")
+            continue
+        if tp[b]:
+            tally.add(1, [True], [not np.array_equal(g_tok[b], ref["tokens_out"][b])],
+                      f"prompt {b} (nucleus near tie)")
             continue
         assert np.array_equal(g_tok[b, :n_ref - 1], ref["tokens_out"][b, :n_ref - 1])
         assert (g_tok[b, n_ref:] == -1).all()

@@ -129,6 +129,19 @@ def test_host_validation_without_gpu(lib):
     opts = bd.smc_step_opts(None, 1.0, 0.9, (ctypes.c_int32 * 2)(0, 0))
     assert lib.smc_step_ex(ctypes.byref(power), ctypes.byref(opts), *[fake] * 8, None, ws,
                            need, None) == -1
+    # sps_verify_ex: no log-potential (one particle), the same temperature and
+    # top_p rules
+    sps_p = P(2, 1, 3, 64, 0, 1.0, 0.5, 0, 0)
+    sps_need = lib.smc_workspace_bytes(ctypes.byref(sps_p), None)
+    opts = bd.smc_step_opts(fake, 1.0, 1.0, (ctypes.c_int32 * 2)(0, 0))
+    assert lib.sps_verify_ex(ctypes.byref(sps_p), *[fake] * 5, ctypes.byref(opts), ws, sps_need,
+                             None) == -1
+    for t, tp, r in ((0.0, 1.0, 0), (float("inf"), 1.0, 0), (1.0, 0.0, 0), (1.0, 1.5, 0),
+                     (1.0, 1.0, 1)):
+        opts = bd.smc_step_opts(None, t, tp, (ctypes.c_int32 * 2)(r, 0))
+        assert lib.sps_verify_ex(ctypes.byref(sps_p), *[fake] * 5, ctypes.byref(opts), ws,
+                                 sps_need, None) == -1
+    assert lib.sps_verify_ex(ctypes.byref(good), *[fake] * 5, None, ws, need, None) == -1
     # smc_draft_sample: a position below 0 or a missing output
     assert lib.smc_draft_sample(ctypes.byref(good), fake, -1, fake, ws, need, None) == -1
     assert lib.smc_draft_sample(ctypes.byref(good), fake, 0, None, ws, need, None) == -1

@@ -8,11 +8,12 @@ import pytest
 import torch
 
 import smc_speculative_decoding_gb300 as smcsd
-from smc_speculative_decoding_gb300.workloads import WORKLOADS, make_step_inputs, to_numpy_logits
+from smc_speculative_decoding_gb300.workloads import (WORKLOADS, Workload, make_step_inputs,
+                                                      to_numpy_logits)
 from smc_speculative_decoding_gb300.workloads import torch_dtype
 from oracle import smc as osmc, kv as okv
 
-from gpu_harness import lockstep, StepRunner, kv_to_numpy
+from gpu_harness import lockstep, sps_lockstep, StepRunner, kv_to_numpy
 
 pytestmark = pytest.mark.gpu
 
@@ -256,3 +257,58 @@ def test_step_ex_top_p_draft_outside_nucleus_is_reported():
     r.run(inp, 0, top_p=0.3)
     torch.cuda.synchronize()
     assert "bad_token" in smcsd.status_names(r.status())
+
+
+# ---------------------------------------------------------------------------
+# sps_verify under temperature and top-p
+# ---------------------------------------------------------------------------
+def _sps_nucleus_tokens(w, top_p, temperature, seed):
+    """Drafted tokens drawn from each draft row's tempered nucleus (oracle,
+    CPU): inputs that a top-p draft could have produced."""
+    rng = np.random.default_rng(seed)
+    s = osmc.temperature_scale(temperature)
+
+    def fn(inp, step):
+        d = to_numpy_logits(inp["draft"])
+        toks = np.zeros((w.B, 1, w.K), dtype=np.int32)
+        for b in range(w.B):
+            rows = osmc.widen(d[b, 0], w.dtype) * s
+            for k in range(w.K):
+                kept, _, _ = osmc.nucleus(rows[k], top_p)
+                pk = np.where(kept, np.exp(rows[k] - rows[k][kept].max()), 0.0)
+                toks[b, 0, k] = rng.choice(len(pk), p=pk / pk.sum())
+        inp["draft_tokens"].copy_(torch.from_numpy(toks).to(inp["draft_tokens"].device))
+    return fn
+
+
+@pytest.mark.parametrize("V,dtype,B,K,temperature,top_p", [
+    (64, "f32", 128, 3, 0.6, 1.0), (32000, "bf16", 32, 4, 1.3, 1.0),
+    (64, "f32", 128, 3, 1.0, 0.8), (32000, "bf16", 32, 4, 0.8, 0.9),
+    (1001, "bf16", 48, 2, 0.7, 0.95)])
+def test_sps_verify_ex_matches_oracle(V, dtype, B, K, temperature, top_p):
+    w = Workload("sps_ex", B=B, N=1, K=K, V=V, dtype=dtype, sigma_t=3.0 if V > 64 else 2.0,
+                 top_m=50 if V > 64 else 0, sigma_d=1.0, steps=1)
+    fn = _sps_nucleus_tokens(w, top_p, temperature, 17) if top_p < 1.0 else None
+    t, ref, g_n = sps_lockstep(w, seed=6, step=2, temperature=temperature, top_p=top_p,
+                               tokens_fn=fn)
+    print(f"sps_ex V={V} T={temperature} top_p={top_p}: draws={t.draws} flagged={t.flagged} "
+          f"mismatched={t.mismatched}")
+    assert (ref["n_emitted"] < K + 1).any(), "no rejection exercised"
+    assert t.mismatched <= max(1, t.draws // 1000)
+
+
+def test_sps_verify_ex_draft_outside_nucleus_is_reported():
+    w = Workload("sps_bad", B=4, N=1, K=2, V=64, dtype="f32", sigma_t=2.0, top_m=0,
+                 sigma_d=1.0, steps=1)
+    inp = make_step_inputs(w, 8, device="cuda")
+    d = to_numpy_logits(inp["draft"])[0, 0, 0].astype(np.float64)
+    kept, _, _ = osmc.nucleus(d, 0.3)
+    inp["draft_tokens"][0, 0, 0] = int(np.flatnonzero(~kept)[0])
+    params = smcsd.make_params(4, 1, 2, 64, "f32", 1.0, 0.5, 8, 0)
+    ws = smcsd.alloc_workspace(params)
+    tok = torch.empty(4 * 3, dtype=torch.int32, device="cuda")
+    n = torch.empty(4, dtype=torch.int32, device="cuda")
+    smcsd.sps_verify_ex(params, inp["target"], inp["draft"], inp["draft_tokens"], tok, n, ws,
+                        top_p=0.3)
+    torch.cuda.synchronize()
+    assert "bad_token" in smcsd.status_names(smcsd.smc_device_status(ws, clear=True))
