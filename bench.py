@@ -429,6 +429,40 @@ def run_extensions(w, dev, smcsd, ring, reps=50):
     res["step_ex_top_p"] = {"ms_per_step": ms_tp, "top_p": 0.9, "steps": n_tp,
                             "particle_tokens_per_s": w.particle_tokens / (ms_tp / 1e3),
                             "note": "the nucleus reads every row twice more (radix select)"}
+    # speculative-sampling verify on the same rows, one particle per prompt
+    # (B*N prompts), plain and under temperature 0.8 with top-p 0.9
+    nb = w.B * w.N
+    ps = smcsd.make_params(nb, 1, w.K, w.V, w.dtype, 1.0, 0.5, 0, 0)
+    ws3 = smcsd.alloc_workspace(ps)
+    s_tok = torch.empty(nb * (w.K + 1), dtype=torch.int32, device=dev)
+    s_n = torch.empty(nb, dtype=torch.int32, device=dev)
+    views = [(r["target"].view(nb, w.K + 1, w.V), r["draft"].view(nb, w.K, w.V), r["draft_tokens"].view(nb, w.K))
+             for r in ring_tp]
+
+    def sps_time(**kw):
+        fn = smcsd.sps_verify_ex if kw else smcsd.sps_verify
+        for s in range(3):
+            fn(ps, *views[s % 2], s_tok, s_n, ws3, **kw)
+        torch.cuda.synchronize()
+        n_sps, emitted = 16, 0
+        e0.record()
+        for s in range(n_sps):
+            fn(ps, *views[s % 2], s_tok, s_n, ws3, **kw)
+        e1.record()
+        torch.cuda.synchronize()
+        assert smcsd.smc_device_status(ws3, clear=True) == 0
+        emitted = int(s_n.sum().item())
+        return e0.elapsed_time(e1) / n_sps, emitted
+    ms_s, em = sps_time()
+    bytes_call = nb * (2 * w.K + 1) * w.V * w.bytes_per_logit
+    res["sps_verify"] = {"prompts": nb, "ms_per_call": ms_s,
+                         "tokens_per_s_last_call": em / (ms_s / 1e3),
+                         "achieved_gbs": bytes_call / (ms_s / 1e3) / 1e9,
+                         "frac_of_hbm_peak": bytes_call / (ms_s / 1e3) / 1e9 / measured_peak()[0],
+                         "bytes": "every row once; a rejection reads two rows again"}
+    ms_s2, em2 = sps_time(temperature=0.8, top_p=0.9)
+    res["sps_verify_ex_top_p"] = {"prompts": nb, "ms_per_call": ms_s2, "temperature": 0.8,
+                                  "top_p": 0.9, "tokens_per_s_last_call": em2 / (ms_s2 / 1e3)}
     return res
 
 
