@@ -247,6 +247,17 @@ def test_step_ex_top_p_threshold_in_a_huge_tie_group(top_p):
     print(f"two-valued top_p={top_p}: draws={t.draws} flagged={t.flagged} mismatched={t.mismatched}")
 
 
+@pytest.mark.parametrize("V,dtype", [(1, "f32"), (2, "bf16"), (37, "f32"), (9, "bf16")])
+def test_step_ex_top_p_tiny_and_ragged_vocab(V, dtype):
+    """Rows of a handful of logits, none a whole 16-byte group: the scalar
+    loads, padding and one-group rows of the nucleus kernel."""
+    w = Workload(f"topp_{V}", B=2, N=4, K=2, V=V, dtype=dtype, sigma_t=2.0, top_m=min(2, V),
+                 sigma_d=1.0, steps=3, prefix=5, block_size=4)
+    t = lockstep(w, 3, seed=53, with_kv=True, top_p=0.7,
+                 tokens_fn=_nucleus_tokens(w, 0.7, 1.0, 53))
+    print(f"top-p V={V} {dtype}: draws={t.draws} flagged={t.flagged} mismatched={t.mismatched}")
+
+
 def test_step_ex_top_p_draft_outside_nucleus_is_reported():
     w = WORKLOADS["tiny_v64"].with_(B=1)
     inp = make_step_inputs(w, 3, device="cuda")
