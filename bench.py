@@ -428,7 +428,7 @@ def run_extensions(w, dev, smcsd, ring, reps=50):
     ms_tp = e0.elapsed_time(e1) / n_tp
     res["step_ex_top_p"] = {"ms_per_step": ms_tp, "top_p": 0.9, "steps": n_tp,
                             "particle_tokens_per_s": w.particle_tokens / (ms_tp / 1e3),
-                            "note": "the nucleus reads every row twice more (radix select)"}
+                            "note": "the nucleus kernel reads every row once more from HBM and again from L2 (mass bins, then the threshold bin)"}
     # speculative-sampling verify on the same rows, one particle per prompt
     # (B*N prompts), plain and under temperature 0.8 with top-p 0.9
     nb = w.B * w.N
