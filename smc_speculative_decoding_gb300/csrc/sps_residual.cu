@@ -76,13 +76,18 @@ __global__ void __launch_bounds__(kThreads) sps_stats_kernel(const SpsArgs a) {
 #pragma unroll
     for (int e = 0; e < G::kEPT; ++e) m = fmaxf(m, x[e]);
     const float mc = block_max(m, s_red);
-    ff S{0.f, 0.f};
+    // two running sums, so that consecutive additions do not wait on each other
+    ff S0{0.f, 0.f}, S1{0.f, 0.f};
     if (mc > kNegInf && mc < -kNegInf) {
 #pragma unroll
-      for (int e = 0; e < G::kEPT; ++e)
-        if (x[e] >= thr[r]) ff_accum(S, weight_term(x[e], mc, a.tscale, s_tab));
+      for (int e = 0; e < G::kEPT; ++e) {
+        if (x[e] >= thr[r]) {
+          if (e & 1) ff_accum(S1, weight_term(x[e], mc, a.tscale, s_tab));
+          else ff_accum(S0, weight_term(x[e], mc, a.tscale, s_tab));
+        }
+      }
     }
-    S = block_ff_sum(ff_norm(S), s_ff);
+    const ff S = block_ff_sum(ff_add(ff_norm(S0), ff_norm(S1)), s_ff);
     if (tid == 0) a.ws.sps_part_pq[(static_cast<size_t>(b) * a.nch + c) * 2 + r] = make_float4(mc, S.hi, S.lo, 0.f);
   }
   if (tid == 0) {
@@ -162,13 +167,16 @@ __global__ void __launch_bounds__(kThreads) sps_residual_kernel(const SpsArgs a)
   load_chunk<T, VEC>(prow + c0 * G::kESZ, n_valid, xp);
   load_chunk<T, VEC>(qrow + c0 * G::kESZ, n_valid, xq);
   __syncthreads();  // table staged
-  ff R{0.f, 0.f};
+  ff R0{0.f, 0.f}, R1{0.f, 0.f};
 #pragma unroll
   for (int e = 0; e < G::kEPT; ++e) {
     const ff d = residual_of(xp[e], xq[e], a.tscale, lp, lq, thr_p, thr_q, s_tab);
-    if (d.hi > 0.f) ff_accum(R, d);
+    if (d.hi > 0.f) {
+      if (e & 1) ff_accum(R1, d);
+      else ff_accum(R0, d);
+    }
   }
-  R = block_ff_sum(ff_norm(R), s_ff);
+  const ff R = block_ff_sum(ff_add(ff_norm(R0), ff_norm(R1)), s_ff);
   if (tid == 0) {
     a.ws.sps_part_r[static_cast<size_t>(b) * a.nch + c] = make_float2(R.hi, R.lo);
     __threadfence();
