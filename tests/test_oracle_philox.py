@@ -40,7 +40,7 @@ def test_vectorised_matches_scalar():
         assert tuple(int(v[i]) for v in vec) == ref
 
 
-_ATEN_DRIVER = r"""
+_ATEN_HARNESS = r"""
 #include <ATen/core/PhiloxRNGEngine.h>
 #include <cstdio>
 int main() {
@@ -65,7 +65,7 @@ def test_matches_independent_library_implementation(tmp_path):
     if gxx is None or not os.path.exists(os.path.join(inc, "ATen/core/PhiloxRNGEngine.h")):
         pytest.skip("g++ or the PyTorch Philox header is not available")
     src = tmp_path / "aten_philox.cpp"
-    src.write_text(_ATEN_DRIVER)
+    src.write_text(_ATEN_HARNESS)
     exe = tmp_path / "aten_philox"
     subprocess.run([gxx, "-std=c++17", "-O1", f"-I{inc}", str(src), "-o", str(exe)],
                    check=True, capture_output=True)
