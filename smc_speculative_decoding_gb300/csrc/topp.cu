@@ -271,6 +271,13 @@ __device__ __forceinline__ void topp_for_each_pair(const char *rowp, int V, F f)
   });
 }
 
+// Lane-wise min of two packed bfloat16 pairs (NaN yields the other operand).
+__device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // The largest logit of a group (NaN ignored; -inf for an all-NaN group).
 template <typename T>
 __device__ __forceinline__ float group_max(const uint4 &v) {
@@ -475,14 +482,25 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
   if (tid < 8) sh.frac[tid] = kToppFrac[tid];
   if (tid == 0) sh.s.n = 0;
   __syncthreads();
-  // The mass bin of x: with y = log2 pi clamped to [-47.875, 0] (-inf and
-  // NaN logits give -47.875: a mass of 2^-47.875, negligible; y exceeds 0
-  // only by the rounding of the row's log-sum-exp), t = 1.5 2^23 + rn(-8 y)
-  // holds the bin, 0..383, in its low bits.
+  // Logits are first clamped to [x_lo, x_hi]: x_lo puts log2 pi at -47.5 or
+  // above (-inf, NaN and the far tail then weigh about 2^-47.5, negligible),
+  // x_hi at 1/32 or below.  Every finite logit lies below x_hi, since it is
+  // at most lse / s.  For bf16 rows both bounds are bf16 values (x_lo rounded
+  // up, x_hi down), so the clamp is exact on the packed pairs.  Then
+  // y = log2 pi lies in [-47.5, 1/32], and t = 1.5 2^23 + rn(-8 y) holds the
+  // bin, 0..380, in its low bits.  That needs |log2 lse| below 4096, where
+  // the rounding of the bounds moves y by at most 5e-4, and finite bounds;
+  // other rows (logits in the thousands, or a log-sum-exp that is not finite,
+  // which the row pass reports) take the exact path.
+  float x_lo = (l2lse - 47.5f) / l2s, x_hi = (l2lse + 0.03125f) / l2s;
+  if (sizeof(T) != 4) {
+    x_lo = __bfloat162float(__float2bfloat16_ru(x_lo));
+    x_hi = __bfloat162float(__float2bfloat16_rd(x_hi));
+  }
+  if (!(fabsf(l2lse) < 4096.f && fabsf(x_lo) < 3e38f && fabsf(x_hi) < 3e38f)) return false;
   constexpr float kMagicB = 12582912.f;   // 1.5 2^23
-  constexpr float kFloorY = -47.875f;     // -(kToppMassBins - 1) / 8
   auto mass_bin = [&](float x, float &y, float &t) -> uint32_t {
-    y = fminf(fmaxf(__fmaf_rn(x, l2s, -l2lse), kFloorY), 0.f);
+    y = __fmaf_rn(fminf(fmaxf(x, x_lo), x_hi), l2s, -l2lse);
     t = __fmaf_rn(y, -8.f, kMagicB);
     return static_cast<uint32_t>(__float_as_int(t) - 0x4B400000);
   };
@@ -494,17 +512,15 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
 
   // ---- pass 1 (HBM): the (bin, lane) cells ----------------------------------
   // the same arithmetic as mass_bin and quantise, two logits at a time on the
-  // packed fp32x2 pipes
+  // packed fp32x2 pipes (bf16 pairs clamped with packed bf16 min / max)
   {
     const unsigned long long L2S = f2dup(l2s), NL2LSE = f2dup(-l2lse), M8 = f2dup(-8.f),
                              MB = f2dup(kMagicB), EIGHTH = f2dup(0.125f), QSC = f2dup(qsc);
     // cell index of bin b for this lane, b 32 + lane, from t's bits directly
     // (modulo 2^32: the bias cancels)
     const uint32_t lane_bias = static_cast<uint32_t>(lane) - (0x4B400000u << 5);
-    topp_for_each_pair<T, VEC>(rowp, a.V, [&](float x0, float x1) {
-      float y0, y1;
-      f2unpack(fma2(f2pack(x0, x1), L2S, NL2LSE), y0, y1);
-      const unsigned long long Y = f2pack(fminf(fmaxf(y0, kFloorY), 0.f), fminf(fmaxf(y1, kFloorY), 0.f));
+    auto add_pair = [&](float x0, float x1) {
+      const unsigned long long Y = fma2(f2pack(x0, x1), L2S, NL2LSE);
       const unsigned long long Tt = fma2(Y, M8, MB);
       float t0, t1;
       f2unpack(Tt, t0, t1);
@@ -514,7 +530,23 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
       f2unpack(mul2(f2pack(fast_exp2(e0), fast_exp2(e1)), QSC), q0, q1);
       atomicAdd(&cell[(__float_as_uint(t0) << 5) + lane_bias], __float_as_uint(q0));
       atomicAdd(&cell[(__float_as_uint(t1) << 5) + lane_bias], __float_as_uint(q1));
-    });
+    };
+    if (sizeof(T) == 4) {
+      topp_for_each_pair<T, VEC>(rowp, a.V, [&](float x0, float x1) {
+        add_pair(fminf(fmaxf(x0, x_lo), x_hi), fminf(fmaxf(x1, x_lo), x_hi));
+      });
+    } else {
+      const uint32_t lo16 = __float_as_uint(x_lo) >> 16, hi16 = __float_as_uint(x_hi) >> 16;
+      const uint32_t LO2 = lo16 | (lo16 << 16), HI2 = hi16 | (hi16 << 16);
+      topp_for_each_group<T, VEC>(rowp, a.V, [&](const uint4 &v) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t c = bmin2(bmax2(w[k], LO2), HI2);  // NaN takes the bound
+          add_pair(bf16_lo(c), bf16_hi(c));
+        }
+      });
+    }
   }
   __syncthreads();
   // bin masses in units of 2^-(26 + qb), in decreasing order of the logit
