@@ -1,0 +1,66 @@
+"""GPU parity over the workload grids that the other parity tests sample only
+in part:
+
+- the batched-serving workload (B16 N16 K4 V128256 bf16, prefix 2048) at
+  every draft-noise level of its sweep, 0.25, 1 and 2;
+- the V = 128256 sweep over every (N, K) of N in {1..64} and K in {2, 4, 8},
+  with two prompts per case so the oracle stays fast;
+- speculative sampling (N = 1) on the sweep's rows at its full 32 prompts;
+- the power-sampling workload (alpha = 4, B8 N32 K8 V151936 fp32) at full size.
+
+The bar is the one of every parity test: integer outputs identical to the
+oracle except on draws the oracle flags as near ties (the harness fails on any
+other mismatch), log-weights within 2e-3 for bf16 logits and 1e-4 for fp32.
+"""
+import pytest
+import torch
+
+from smc_speculative_decoding_gb300.workloads import (WORKLOADS, SERVING_SIGMAS, SWEEP_N,
+                                                      SWEEP_K)
+
+from gpu_harness import lockstep, sps_lockstep
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from smc_speculative_decoding_gb300 import build
+    build.build()
+
+
+def _report(t, name):
+    print(f"{name}: draws={t.draws} flagged={t.flagged} mismatched={t.mismatched}")
+
+
+@pytest.mark.parametrize("sigma_d", SERVING_SIGMAS)
+def test_serving_at_each_draft_noise(sigma_d):
+    w = WORKLOADS["batched_serving_v128256"].with_(sigma_d=sigma_d)
+    t = lockstep(w, steps=2, seed=5)
+    _report(t, f"serving sigma_d={sigma_d}")
+    assert t.mismatched <= max(1, t.draws // 1000)
+
+
+@pytest.mark.parametrize("K", SWEEP_K)
+@pytest.mark.parametrize("N", SWEEP_N)
+def test_sweep_grid(N, K):
+    w = WORKLOADS["sweep_v128256"].with_(B=2, N=N, K=K)
+    t = lockstep(w, steps=2, seed=7)
+    assert t.mismatched <= max(1, t.draws // 1000)
+
+
+@pytest.mark.parametrize("K", SWEEP_K)
+def test_sweep_sps_verify_at_n1(K):
+    w = WORKLOADS["sweep_v128256"].with_(N=1, K=K)
+    t, ref, g_n = sps_lockstep(w, seed=7, step=3)
+    _report(t, f"sweep sps K={K}")
+    assert (ref["n_emitted"] < K + 1).any(), "no rejection exercised"
+    assert t.mismatched <= max(1, t.draws // 1000)
+
+
+def test_power_sampling_full_size_one_step():
+    t = lockstep(WORKLOADS["power_sampling_v151936"], steps=1, seed=9)
+    _report(t, "power sampling, full size")
+    assert t.mismatched <= max(1, t.draws // 1000)
