@@ -175,6 +175,43 @@ def test_sps_verify_draft_equals_target_accepts_all():
     assert (g_n == 5).all()
 
 
+def _swapped_pair_drafts(shift):
+    """tokens_fn for sps_lockstep: each draft row becomes its target row with
+    two logits swapped, a (target probability nearest 3e-5) and b (the
+    smallest logit), and every other logit moved by `shift`; every drafted
+    token is b, so position 0 rejects almost surely.  The residual then lies
+    on a and on the shifted bulk, where p/q is the same for every element and
+    within about 1e-4 of 1: the sign of p - q is a close call for every
+    element of the bulk, and the residual must still come out exact."""
+    def fn(inp, step):
+        K = inp["draft"].shape[2]
+        tg = inp["target"][:, 0, :K].float()
+        logp = torch.log_softmax(tg.double(), dim=-1)
+        a = (logp - np.log(3e-5)).abs().argmin(dim=-1, keepdim=True)
+        b = tg.argmin(dim=-1, keepdim=True)
+        d = tg + shift
+        d.scatter_(-1, a, tg.gather(-1, b))
+        d.scatter_(-1, b, tg.gather(-1, a))
+        inp["draft"][:, 0].copy_(d.to(inp["draft"].dtype))
+        inp["draft_tokens"][:, 0].copy_(b.squeeze(-1).to(torch.int32))
+    return fn
+
+
+@pytest.mark.parametrize("dtype,shift", [("bf16", 0.0), ("f32", -1.0), ("f32", 1.0)])
+def test_sps_verify_residual_with_a_bulk_of_close_calls(dtype, shift):
+    """shift 0: p = q exactly on the bulk (bf16 rows copied), so the sign of
+    p - q there is a tie that rounding decides; the bulk's residual is zero
+    and the draw must land on a.  shift -1 / +1 (fp32): p/q on the bulk is
+    1 + 5e-5 or 1 - 2e-5, so the bulk carries about 60 % of the residual mass,
+    or none of it."""
+    w = Workload("sps_close", B=32, N=1, K=2, V=128256, dtype=dtype, sigma_t=3.0, top_m=50,
+                 sigma_d=1.0, steps=1)
+    t, ref, g_n = sps_lockstep(w, seed=6, step=2, tokens_fn=_swapped_pair_drafts(shift))
+    _report(t, f"sps close calls {dtype} shift={shift}")
+    assert (ref["n_emitted"] == 1).mean() > 0.9, "position 0 should reject"
+    assert t.mismatched <= max(1, t.draws // 1000)
+
+
 # ---------------------------------------------------------------------------
 # standalone smc_resample and kv_blocktable_remap
 # ---------------------------------------------------------------------------
