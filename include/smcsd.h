@@ -144,7 +144,8 @@ int32_t smc_device_status(void *workspace, int32_t clear, int32_t *out_bits,
                           void *stream);
 
 /* Measurement hook (no counterpart in the pages).  While set, every later
- * smc_step, smc_step_noalloc and sps_verify records `rows_begin` on its
+ * smc_step, smc_step_ex, smc_step_noalloc, sps_verify, sps_verify_ex and
+ * smc_draft_sample records `rows_begin` on its
  * stream just before the row pass (the kernel that streams the target and
  * draft rows) and `rows_end` just after it, so a caller can time the
  * vocabulary reduction alone with cudaEventElapsedTime.  Both are
