@@ -280,7 +280,7 @@ def effective_alpha(alpha, temperature=1.0):
 
 def smc_step(target, draft, draft_tokens, log_weights, *, alpha=1.0,
              ess_frac=0.5, seed=0, step=0, dtype=None, temperature=1.0,
-             log_potential=None, top_p=1.0):
+             log_potential=None, top_p=1.0, prompt_offset=0):
     """One SMC-SD step over B prompts x N particles (no KV state).
 
     target: [B, N, K+1, V], draft: [B, N, K, V], either already fp64 or, when
@@ -302,6 +302,11 @@ def smc_step(target, draft, draft_tokens, log_weights, *, alpha=1.0,
     outside the target's nucleus gives the particle weight 0.  The returned
     dict then also holds topp_margin[B, N]: the smallest nucleus margin of the
     particle's rows.
+
+    prompt_offset: the batch is prompts prompt_offset .. prompt_offset+B-1
+    of a larger one; only the random streams depend on it (prompt b draws
+    with the stream numbers of prompt prompt_offset + b), so a batch can be
+    checked in slices.
 
     Returns a dict with
       delta[B,N], log_weights_pre[B,N] (after reweighting), log_weights[B,N]
@@ -335,7 +340,8 @@ def smc_step(target, draft, draft_tokens, log_weights, *, alpha=1.0,
             if scale != 1.0:
                 t_rows = np.asarray(t_rows, dtype=np.float64) * scale
                 d_rows = np.asarray(d_rows, dtype=np.float64) * scale
-            u = philox.uniform(seed, step, b * n_part + n, k_drafts, philox.BONUS)
+            u = philox.uniform(seed, step, (prompt_offset + b) * n_part + n, k_drafts,
+                               philox.BONUS)
             raw = widen(target[b, n, k_drafts], dtype) if dtype else target[b, n, k_drafts]
             if use_topp:
                 s = score_particle_topp(t_rows, d_rows, draft_tokens[b, n], top_p)
@@ -361,7 +367,7 @@ def smc_step(target, draft, draft_tokens, log_weights, *, alpha=1.0,
     out["ess_margin"] = np.zeros(big_b)
     out["tokens_out"] = np.zeros((big_b, n_part, k1), dtype=np.int64)
     for b in range(big_b):
-        r = resample_prompt(lw_pre[b], ess_frac, seed, step, b)
+        r = resample_prompt(lw_pre[b], ess_frac, seed, step, prompt_offset + b)
         out["log_weights"][b] = r["log_weights_out"]
         out["ess"][b] = r["ess"]
         out["resampled"][b] = r["resampled"]
@@ -377,7 +383,7 @@ def smc_step(target, draft, draft_tokens, log_weights, *, alpha=1.0,
 # --------------------------------------------------------------------------
 # the extend-side draft sampler
 # --------------------------------------------------------------------------
-def draft_sample(draft, position, *, alpha=1.0, seed=0, step=0, dtype=None):
+def draft_sample(draft, position, *, alpha=1.0, seed=0, step=0, dtype=None, prompt_offset=0):
     """One drafted token per particle: x ~ softmax(alpha * l) of draft row
     [B, N, V], by inverse CDF in vocabulary order with the uniform of
     (seed, step, particle b*N+n, position, DRAFT).
@@ -385,6 +391,7 @@ def draft_sample(draft, position, *, alpha=1.0, seed=0, step=0, dtype=None):
     The SMC page's Extend stage has the draft model extend every particle by
     K tokens; this is the sampling half of one of those K positions.  alpha
     is the inverse temperature of the draft (1: sample q itself).
+    prompt_offset shifts the stream numbers as in ``smc_step``.
     Returns (tokens[B, N], margins[B, N]).
     """
     alpha = float(np.float32(alpha))
@@ -394,6 +401,7 @@ def draft_sample(draft, position, *, alpha=1.0, seed=0, step=0, dtype=None):
     for b in range(big_b):
         for n in range(n_part):
             row = widen(draft[b, n], dtype) if dtype else np.asarray(draft[b, n], np.float64)
-            u = philox.uniform(seed, step, b * n_part + n, position, philox.DRAFT)
+            u = philox.uniform(seed, step, (prompt_offset + b) * n_part + n, position,
+                               philox.DRAFT)
             toks[b, n], margins[b, n] = inverse_cdf(bonus_weights(row, alpha), u)
     return toks, margins

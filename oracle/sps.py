@@ -129,14 +129,16 @@ def verify_one_logprobs(logp, logq, tokens, u_accept, u_residual, u_bonus):
 
 
 def sps_verify(target, draft, draft_tokens, *, seed=0, step=0, dtype=None, temperature=1.0,
-               top_p=1.0):
+               top_p=1.0, prompt_offset=0):
     """Verify B independent prompts (N = 1 particle each).
 
     target [B, K+1, V], draft [B, K, V] fp64 (or stored logits widened per
     prompt when ``dtype`` is given, see ``smc.widen``), draft_tokens [B, K].
     Uniforms: ACCEPT and RESIDUAL keyed by (step, b, k), BONUS by (step, b, K).
     With temperature != 1 or top_p < 1, p and q are the tempered nuclei
-    (``tempered_logprobs``).
+    (``tempered_logprobs``).  prompt_offset: the batch is prompts
+    prompt_offset .. prompt_offset+B-1 of a larger one (the uniforms use those
+    prompt numbers).
     Returns dict(tokens_out [B, K+1] padded with -1, n_emitted [B],
     accept_margin [B, K] (inf where not tested), final_margin [B], and with
     top_p < 1 topp_margin [B], each prompt's smallest nucleus margin).
@@ -151,9 +153,10 @@ def sps_verify(target, draft, draft_tokens, *, seed=0, step=0, dtype=None, tempe
     final_margin = np.zeros(big_b)
     topp_margin = np.full(big_b, np.inf)
     for b in range(big_b):
-        ua = [philox.uniform(seed, step, b, k, philox.ACCEPT) for k in range(k_drafts)]
-        ur = [philox.uniform(seed, step, b, k, philox.RESIDUAL) for k in range(k_drafts)]
-        ub = philox.uniform(seed, step, b, k_drafts, philox.BONUS)
+        pb = prompt_offset + b
+        ua = [philox.uniform(seed, step, pb, k, philox.ACCEPT) for k in range(k_drafts)]
+        ur = [philox.uniform(seed, step, pb, k, philox.RESIDUAL) for k in range(k_drafts)]
+        ub = philox.uniform(seed, step, pb, k_drafts, philox.BONUS)
         t_rows = widen(target[b], dtype) if dtype else target[b]
         d_rows = widen(draft[b], dtype) if dtype else draft[b]
         if plain:

@@ -137,3 +137,35 @@ def test_step_emits_k_plus_one_tokens_of_the_ancestor():
             assert list(out["tokens_out"][b, i]) == list(toks[b, a]) + [out["bonus"][b, a]]
     assert np.array_equal(out["log_weights"], np.zeros((big_b, n)))
     assert np.allclose(out["log_weights_pre"], lw + out["delta"])
+
+
+def test_prompt_offset_slices_equal_the_whole_batch():
+    """The oracle on a batch equals the oracle on its prompt slices with
+    prompt_offset set, for the step, the verify and the draft sampler: only
+    the random streams depend on a prompt's number, and the offset keeps them."""
+    from smc_speculative_decoding_gb300.workloads import Workload, make_step_inputs, \
+        to_numpy_logits
+    from oracle import sps as osps
+    w = Workload("slices", B=5, N=3, K=2, V=40, dtype="f32", sigma_t=2.0, top_m=3,
+                 sigma_d=1.5)
+    inp = make_step_inputs(w, 9)
+    t, d = to_numpy_logits(inp["target"]), to_numpy_logits(inp["draft"])
+    x = inp["draft_tokens"].numpy().astype(np.int64)
+    lw = np.random.default_rng(2).normal(0, 1, (w.B, w.N))
+    whole = smc.smc_step(t, d, x, lw, ess_frac=0.9, seed=4, step=3)
+    for b0, b1 in ((0, 2), (2, 3), (3, 5)):
+        part = smc.smc_step(t[b0:b1], d[b0:b1], x[b0:b1], lw[b0:b1], ess_frac=0.9, seed=4,
+                            step=3, prompt_offset=b0)
+        for key in ("bonus", "ancestors", "tokens_out", "ess", "resampled"):
+            assert np.array_equal(part[key], whole[key][b0:b1]), key
+    assert whole["resampled"].any() and not whole["resampled"].all()
+    one = t[:, 0]  # [B, K+1, V] as one-particle prompts
+    sw = osps.sps_verify(one, d[:, 0], x[:, 0], seed=4, step=3)
+    sp = osps.sps_verify(one[1:4], d[1:4, 0], x[1:4, 0], seed=4, step=3, prompt_offset=1)
+    assert np.array_equal(sp["tokens_out"], sw["tokens_out"][1:4])
+    dw, _ = smc.draft_sample(d[:, :, 0], 1, seed=4, step=3)
+    dp, _ = smc.draft_sample(d[2:, :, 0], 1, seed=4, step=3, prompt_offset=2)
+    assert np.array_equal(dp, dw[2:])
+    # a wrong offset changes the draws
+    moved = smc.smc_step(t[2:5], d[2:5], x[2:5], lw[2:5], ess_frac=0.9, seed=4, step=3)
+    assert not np.array_equal(moved["bonus"], whole["bonus"][2:5])
