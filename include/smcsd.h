@@ -322,7 +322,14 @@ int32_t sps_verify_ex(const smc_params *p, const void *target_logits,
  *     `stream`) with this call's SMC_DEV_* bits.
  *   - The first call on a device, with that device current, looks up the
  *     array's device address (cudaGetSymbolAddress); make that first call
- *     before any stream capture.
+ *     before any stream capture.  If the library's device code is not yet
+ *     loaded on that device (lazy module loading), the lookup loads it, which
+ *     reserves the array: make the first call before a host allocator
+ *     reserves the device's free memory, or use eager module loading.
+ *   - The address is kept for the life of the process: a device reset
+ *     (cudaDeviceReset) is not supported.
+ *   - Every argument check of smc_step runs before anything is queued; when
+ *     a non-zero code is returned, *status_bits is left unwritten.
  *   - Every call on a device shares the one array; each call clears the
  *     parts that must start at zero.  Calls whose GPU work overlaps (issued
  *     on different streams without ordering) race on the array. */

@@ -183,11 +183,11 @@ int32_t smc_set_row_timing_events(void *rows_begin, void *rows_end) {
 
 namespace smcsd {
 
-static int32_t step_impl(const smc_params *p, const smc_step_opts *opts,
-                         const void *target_logits, const void *draft_logits,
-                         const int32_t *draft_tokens, float *log_weights, int32_t *tokens_out,
-                         int32_t *ancestors, float *ess, int32_t *resampled, const smc_kv *kv,
-                         void *workspace, size_t ws_bytes, void *stream) {
+int32_t check_step_args(const smc_params *p, const void *target_logits,
+                        const void *draft_logits, const int32_t *draft_tokens,
+                        const float *log_weights, const int32_t *tokens_out,
+                        const int32_t *ancestors, const float *ess, const int32_t *resampled,
+                        const smc_kv *kv) {
   if (!p) return SMC_ERR_ARG;
   if (p->dtype != SMC_F32 && p->dtype != SMC_BF16) return SMC_ERR_DTYPE;
   if (!shape_ok(p) || !kv_ok(p, kv)) return SMC_ERR_ARG;
@@ -195,6 +195,17 @@ static int32_t step_impl(const smc_params *p, const smc_step_opts *opts,
       !ancestors || !ess || !resampled) {
     return SMC_ERR_ARG;
   }
+  return SMC_OK;
+}
+
+static int32_t step_impl(const smc_params *p, const smc_step_opts *opts,
+                         const void *target_logits, const void *draft_logits,
+                         const int32_t *draft_tokens, float *log_weights, int32_t *tokens_out,
+                         int32_t *ancestors, float *ess, int32_t *resampled, const smc_kv *kv,
+                         void *workspace, size_t ws_bytes, void *stream) {
+  const int32_t arg_rc = check_step_args(p, target_logits, draft_logits, draft_tokens,
+                                         log_weights, tokens_out, ancestors, ess, resampled, kv);
+  if (arg_rc != SMC_OK) return arg_rc;
   Shape s = to_shape(p);
   if (opts) {
     if (opts->reserved[0] != 0 || opts->reserved[1] != 0) return SMC_ERR_ARG;

@@ -6,7 +6,17 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "smcsd.h"
+
 namespace smcsd {
+
+// smc_step's host-side argument checks (shape, dtype, KV struct, null
+// pointers): SMC_OK or the error code smc_step would return.
+int32_t check_step_args(const smc_params *p, const void *target_logits,
+                        const void *draft_logits, const int32_t *draft_tokens,
+                        const float *log_weights, const int32_t *tokens_out,
+                        const int32_t *ancestors, const float *ess, const int32_t *resampled,
+                        const smc_kv *kv);
 
 // Per-(row, chunk) partial of a vocabulary reduction: chunk max m, fast fp32
 // sum s of exp(l - m), and the float-float sum (shi, slo) of the sampling

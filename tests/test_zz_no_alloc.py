@@ -43,8 +43,11 @@ def _state(w, dev, steps):
     return kv, outs
 
 
-@pytest.mark.parametrize("name,B", [("tiny_v64", 3), ("single_prompt_v32000", 2)])
+@pytest.mark.parametrize("name,B", [("tiny_v64", 3), ("single_prompt_v32000", 2),
+                                    ("batched_serving_v128256", 16)])
 def test_noalloc_matches_workspace_entry_point(name, B):
+    """Two calls in a row; the serving shape (16 prompts x 16 particles, K 4,
+    V 128256) is the library's main use and must fit the fixed array."""
     w = WORKLOADS[name].with_(B=B)
     dev = "cuda"
     kv_a, out_a = _state(w, dev, 2)
@@ -52,6 +55,7 @@ def test_noalloc_matches_workspace_entry_point(name, B):
     p0 = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 7, 0)
     kv_sa = smcsd.make_kv(p0, kv_a, w.block_size)
     kv_sb = smcsd.make_kv(p0, kv_b, w.block_size)
+    assert smcsd.smc_workspace_bytes(p0, kv_sa) <= (8 << 20), "shape does not fit the array"
     ws = smcsd.alloc_workspace(p0, kv_sa, device=dev)
     status = torch.full((1,), -1, dtype=torch.int32, device=dev)
     for step in range(2):  # two calls in a row, state carried forward
@@ -74,14 +78,20 @@ def test_noalloc_matches_workspace_entry_point(name, B):
             assert torch.equal(kv_a[key], kv_b[key]), key
 
 
-def test_noalloc_rejects_shapes_beyond_its_array():
+@pytest.mark.parametrize("B,N,K,V,dtype", [(64, 256, 16, 1 << 20, "bf16"),
+                                            (128, 16, 4, 128256, "bf16"),
+                                            (8, 256, 8, 151936, "f32")])
+def test_noalloc_rejects_shapes_beyond_its_array(B, N, K, V, dtype):
+    """Shapes whose workspace exceeds the fixed array are refused with
+    SMC_ERR_WORKSPACE before anything is launched (the pointers below are
+    never touched)."""
     lib = binding.lib()
     fn = lib.smc_step_noalloc
     fn.restype = ctypes.c_int32
     fn.argtypes = [ctypes.POINTER(binding.smc_params)] + [ctypes.c_void_p] * 8 + \
         [ctypes.POINTER(binding.smc_kv), ctypes.c_void_p, ctypes.c_void_p]
-    big = smcsd.make_params(64, 256, 16, 1 << 20, "bf16")
+    big = smcsd.make_params(B, N, K, V, dtype)
     assert smcsd.smc_workspace_bytes(big) > (8 << 20)
-    fake = ctypes.c_void_p(0x1000)  # never touched: the size check fails first
+    fake = ctypes.c_void_p(0x1000)
     rc = fn(ctypes.byref(big), *[fake] * 8, None, fake, None)
     assert rc == -3, smcsd.smc_strerror(rc)
