@@ -1,8 +1,12 @@
 """GPU parity of the step's extensions against the CPU oracle: smc_step_ex
 (temperature, per-particle log-potentials, top-p nuclei), smc_draft_sample
 (the draft-side sampler) and smc_kv_usage (KV-cache accounting).  Same bar as the basic
-step: integer outputs exact except draws the oracle flags as near ties,
-log-weights within 1e-4 (fp32 logits) or 2e-3 (bf16 logits)."""
+step: integer outputs exact except draws the oracle flags as near ties, and
+no more such mismatches than 1e-4 of the draws (none, below 10^4 draws);
+log-weights within 1e-4 (fp32 logits) or 2e-3 (bf16 logits).  The tests
+built to put the nucleus boundary on ties of equal logits (tied and
+two-valued rows, vocabularies of a few tokens) require only that every
+mismatch be flagged: they sample the near-tie cases on purpose."""
 import numpy as np
 import pytest
 import torch
@@ -47,13 +51,15 @@ def test_step_ex_matches_oracle(name, B, temperature):
     steps = 6 if w.V > 1000 else 10
     t = lockstep(w, steps, seed=17, with_kv=True, temperature=temperature,
                  potential_fn=_potentials(w, 17))
-    print(f"{name} T={temperature}: draws={t.draws} flagged={t.flagged} mismatched={t.mismatched}")
+    print(f"{name} T={temperature}: {t.summary()}")
+    assert t.rate_ok()
 
 
 def test_step_ex_serving_size_one_step():
     w = WORKLOADS["batched_serving_v128256"].with_(B=4)
     t = lockstep(w, 2, seed=5, with_kv=True, temperature=1.3, potential_fn=_potentials(w, 5))
-    print(f"serving T=1.3: draws={t.draws} flagged={t.flagged} mismatched={t.mismatched}")
+    print(f"serving T=1.3: {t.summary()}")
+    assert t.rate_ok()
 
 
 def test_step_ex_unaligned_vocab_takes_the_per_chunk_path():
@@ -99,6 +105,7 @@ def test_draft_sample_matches_oracle(V, dtype, alpha):
         mism += int((g != ref).sum())
     print(f"draft sample V={V} {dtype} alpha={alpha}: draws={draws} flagged={flagged} "
           f"mismatched={mism}")
+    assert mism <= 1e-4 * draws
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
@@ -195,8 +202,8 @@ def test_step_ex_top_p_matches_oracle(name, B, top_p, temperature):
     steps = 4 if w.V > 1000 else 10
     t = lockstep(w, steps, seed=23, with_kv=True, temperature=temperature, top_p=top_p,
                  tokens_fn=_nucleus_tokens(w, top_p, temperature, 23))
-    print(f"{name} top_p={top_p} T={temperature}: draws={t.draws} flagged={t.flagged} "
-          f"mismatched={t.mismatched}")
+    print(f"{name} top_p={top_p} T={temperature}: {t.summary()}")
+    assert t.rate_ok()
 
 
 def test_step_ex_top_p_serving_size_and_unaligned():
@@ -302,10 +309,9 @@ def test_sps_verify_ex_matches_oracle(V, dtype, B, K, temperature, top_p):
     fn = _sps_nucleus_tokens(w, top_p, temperature, 17) if top_p < 1.0 else None
     t, ref, g_n = sps_lockstep(w, seed=6, step=2, temperature=temperature, top_p=top_p,
                                tokens_fn=fn)
-    print(f"sps_ex V={V} T={temperature} top_p={top_p}: draws={t.draws} flagged={t.flagged} "
-          f"mismatched={t.mismatched}")
+    print(f"sps_ex V={V} T={temperature} top_p={top_p}: {t.summary()}")
     assert (ref["n_emitted"] < K + 1).any(), "no rejection exercised"
-    assert t.mismatched <= max(1, t.draws // 1000)
+    assert t.rate_ok()
 
 
 def test_sps_verify_ex_draft_outside_nucleus_is_reported():

@@ -28,7 +28,7 @@ def _built():
 
 
 def _report(t, name):
-    print(f"{name}: draws={t.draws} flagged={t.flagged} mismatched={t.mismatched}")
+    print(f"{name}: {t.summary()}")
 
 
 # ---------------------------------------------------------------------------
@@ -37,37 +37,81 @@ def _report(t, name):
 def test_tiny_v64_ten_steps_with_kv():
     t = lockstep(WORKLOADS["tiny_v64"], steps=10)
     _report(t, "tiny")
-    assert t.mismatched == 0
+    assert t.mismatched == 0 and t.lw_checked > 0
 
 
 def test_tiny_v64_no_resampling_checks_every_weight():
     w = WORKLOADS["tiny_v64"].with_(B=3, N=16)
     t = lockstep(w, steps=6, ess_frac=0.0)
-    assert t.mismatched == 0
+    assert t.mismatched == 0 and t.lw_checked == 6 * w.B * w.N
 
 
 def test_tiny_v64_always_resample():
     w = WORKLOADS["tiny_v64"].with_(B=4, N=32, sigma_d=2.0)
     t = lockstep(w, steps=6, ess_frac=1.0)
     _report(t, "always-resample")
+    assert t.rate_ok()
 
 
 def test_single_prompt_v32000_bf16():
     t = lockstep(WORKLOADS["single_prompt_v32000"], steps=24)
     _report(t, "single prompt")
-    assert t.mismatched <= max(1, t.draws // 1000)
+    assert t.rate_ok()
 
 
 def test_power_sampling_alpha4_fp32():
     w = WORKLOADS["power_sampling_v151936"].with_(B=2, N=8)
     t = lockstep(w, steps=2)
     _report(t, "power sampling")
+    assert t.rate_ok()
 
 
 def test_serving_full_size_one_step():
     """B16 N16 K4 V128256 bf16, prefix 2048, the bench's launch configuration."""
     t = lockstep(WORKLOADS["batched_serving_v128256"], steps=1)
     _report(t, "serving")
+    assert t.rate_ok()
+
+
+def test_serving_full_size_every_log_weight(pool):
+    """B16 N16 K4 V128256 bf16 with resampling off for two steps, so that
+    every one of the B*N log-weights is compared (at 2e-3) after each step."""
+    w = WORKLOADS["batched_serving_v128256"]
+    t = lockstep(w, steps=2, ess_frac=0.0, pool=pool)
+    _report(t, "serving, every log-weight")
+    assert t.lw_checked == 2 * w.B * w.N
+    assert t.rate_ok()
+
+
+def test_power_sampling_full_size_every_log_weight(pool):
+    """B8 N32 K8 V151936 fp32, alpha = 4, resampling off: every log-weight,
+    bonus term lse(4 l) - 4 lse(l) included, compared at 1e-4."""
+    w = WORKLOADS["power_sampling_v151936"]
+    t = lockstep(w, steps=1, ess_frac=0.0, with_kv=False, pool=pool)
+    _report(t, "power sampling, every log-weight")
+    assert t.lw_checked == w.B * w.N
+    assert t.rate_ok()
+
+
+@pytest.mark.parametrize("case", ["fused_power_sampling", "tail_n64", "tail_top_p_serving"])
+def test_large_staged_kv_state(case, pool):
+    """KV tables and pools sized for long episodes, staged in dynamic shared
+    memory: 30 to 45 KB on top of the tail's static shared memory, so the
+    launch needs the opt-in above 48 KB.  Through the fused epilogue (N = 32)
+    and through the separate tail kernel (N = 64, and top-p)."""
+    from test_gpu_next import _nucleus_tokens
+    if case == "fused_power_sampling":
+        w = WORKLOADS["power_sampling_v151936"].with_(B=1)
+        t = lockstep(w, steps=2, kv_steps=128, pool=pool)
+    elif case == "tail_n64":
+        w = WORKLOADS["sweep_v128256"].with_(B=2, N=64, K=8)
+        t = lockstep(w, steps=2, kv_steps=32, pool=pool)
+    else:
+        w = WORKLOADS["batched_serving_v128256"].with_(B=2)
+        t = lockstep(w, steps=1, kv_steps=128, pool=pool, top_p=0.95,
+                     tokens_fn=_nucleus_tokens(w, 0.95, 1.0, 61))
+    _report(t, f"large staged KV ({case})")
+    assert t.rate_ok()
 
 
 @pytest.mark.parametrize("V,dtype", [(1001, "bf16"), (37, "f32"), (8193, "bf16"),
@@ -91,6 +135,7 @@ def test_max_particles_and_long_draft():
                  sigma_d=1.5, steps=3, prefix=20, block_size=8)
     t = lockstep(w, steps=3)
     _report(t, "N=256")
+    assert t.rate_ok()
 
 
 def test_misaligned_base_pointer_takes_scalar_path():
@@ -129,29 +174,16 @@ def test_repeat_call_is_bitwise_deterministic():
         assert torch.equal(a, b)
 
 
-def test_bonus_mismatch_rate_at_v128256():
+def test_bonus_mismatch_rate_at_v128256(pool):
     """Float-float sampling sums: bonus tokens at V=128256 agree with the
-    fp64 oracle except on near ties; the mismatch rate must stay below 1e-4."""
+    fp64 oracle except on near ties, and every log-weight within 2e-3;
+    resampling is off, so each of the 12 steps compares all 512 weights."""
     w = WORKLOADS["batched_serving_v128256"].with_(K=1, N=16, B=32)
-    runner = StepRunner(w, seed=11, with_kv=False, ess_frac=0.0)
-    draws = mism = flagged = 0
-    for step in range(12):
-        inp = make_step_inputs(w, 11, device="cuda", step=step)
-        runner.run(inp, step)
-        g = runner.tokens_out.cpu().numpy().reshape(w.B, w.N, 2)[:, :, 1]
-        bonus_rows = to_numpy_logits(inp["target"][:, :, 1])
-        for b in range(w.B):
-            for n in range(w.N):
-                u = osmc.philox.uniform(11, step, b * w.N + n, 1, osmc.philox.BONUS)
-                row = osmc.widen(bonus_rows[b, n], "bf16")
-                tok, margin = osmc.inverse_cdf(osmc.bonus_weights(row, 1.0), u)
-                draws += 1
-                flagged += margin < 1e-5
-                if tok != g[b, n]:
-                    mism += 1
-                    assert margin < 1e-5, (step, b, n, tok, g[b, n], margin)
-    print(f"bonus draws={draws} flagged={flagged} mismatched={mism}")
-    assert mism <= draws * 1e-4 + 1
+    t = lockstep(w, steps=12, seed=11, with_kv=False, ess_frac=0.0, pool=pool)
+    _report(t, "bonus at V=128256")
+    assert t.kinds["bonus"][0] == 12 * w.B * w.N
+    assert t.lw_checked == 12 * w.B * w.N
+    assert t.rate_ok()
 
 
 # ---------------------------------------------------------------------------
@@ -165,7 +197,7 @@ def test_sps_verify_matches_oracle(V, dtype, B, K):
     t, ref, g_n = sps_lockstep(w, seed=2, step=1)
     _report(t, f"sps V={V}")
     assert (ref["n_emitted"] < K + 1).any(), "no rejection exercised"
-    assert t.mismatched <= max(1, t.draws // 1000)
+    assert t.rate_ok()
 
 
 def test_sps_verify_draft_equals_target_accepts_all():
@@ -209,7 +241,7 @@ def test_sps_verify_residual_with_a_bulk_of_close_calls(dtype, shift):
     t, ref, g_n = sps_lockstep(w, seed=6, step=2, tokens_fn=_swapped_pair_drafts(shift))
     _report(t, f"sps close calls {dtype} shift={shift}")
     assert (ref["n_emitted"] == 1).mean() > 0.9, "position 0 should reject"
-    assert t.mismatched <= max(1, t.draws // 1000)
+    assert t.rate_ok()
 
 
 # ---------------------------------------------------------------------------

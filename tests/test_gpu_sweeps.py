@@ -10,7 +10,9 @@ in part:
 
 The bar is the one of every parity test: integer outputs identical to the
 oracle except on draws the oracle flags as near ties (the harness fails on any
-other mismatch), log-weights within 2e-3 for bf16 logits and 1e-4 for fp32.
+other mismatch), no more such mismatches than 1e-4 of each kind's draws (so
+none in a test of fewer than 10^4 draws), log-weights within 2e-3 for bf16
+logits and 1e-4 for fp32.
 """
 import pytest
 import torch
@@ -32,15 +34,15 @@ def _built():
 
 
 def _report(t, name):
-    print(f"{name}: draws={t.draws} flagged={t.flagged} mismatched={t.mismatched}")
+    print(f"{name}: {t.summary()}")
 
 
 @pytest.mark.parametrize("sigma_d", SERVING_SIGMAS)
-def test_serving_at_each_draft_noise(sigma_d):
+def test_serving_at_each_draft_noise(sigma_d, pool):
     w = WORKLOADS["batched_serving_v128256"].with_(sigma_d=sigma_d)
-    t = lockstep(w, steps=2, seed=5)
+    t = lockstep(w, steps=2, seed=5, pool=pool)
     _report(t, f"serving sigma_d={sigma_d}")
-    assert t.mismatched <= max(1, t.draws // 1000)
+    assert t.rate_ok(), t.summary()
 
 
 @pytest.mark.parametrize("K", SWEEP_K)
@@ -48,7 +50,7 @@ def test_serving_at_each_draft_noise(sigma_d):
 def test_sweep_grid(N, K):
     w = WORKLOADS["sweep_v128256"].with_(B=2, N=N, K=K)
     t = lockstep(w, steps=2, seed=7)
-    assert t.mismatched <= max(1, t.draws // 1000)
+    assert t.rate_ok(), t.summary()
 
 
 @pytest.mark.parametrize("K", SWEEP_K)
@@ -57,10 +59,10 @@ def test_sweep_sps_verify_at_n1(K):
     t, ref, g_n = sps_lockstep(w, seed=7, step=3)
     _report(t, f"sweep sps K={K}")
     assert (ref["n_emitted"] < K + 1).any(), "no rejection exercised"
-    assert t.mismatched <= max(1, t.draws // 1000)
+    assert t.rate_ok(), t.summary()
 
 
-def test_power_sampling_full_size_one_step():
-    t = lockstep(WORKLOADS["power_sampling_v151936"], steps=1, seed=9)
+def test_power_sampling_full_size_one_step(pool):
+    t = lockstep(WORKLOADS["power_sampling_v151936"], steps=1, seed=9, pool=pool)
     _report(t, "power sampling, full size")
-    assert t.mismatched <= max(1, t.draws // 1000)
+    assert t.rate_ok(), t.summary()
