@@ -23,7 +23,8 @@ size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws) 
   };
   // region that must start at zero (counters and the freed-block bitmap)
   const size_t o_status = take(sizeof(unsigned));
-  const size_t o_pt = take(sizeof(unsigned) * s.B);
+  const size_t o_wd = take(sizeof(unsigned) * s.B);
+  const size_t o_bd = take(sizeof(unsigned) * s.B);
   const size_t o_rt = take(sizeof(unsigned) * rows);
   const size_t o_sa = take(sizeof(unsigned) * s.B);
   const size_t o_sb = take(sizeof(unsigned) * s.B);
@@ -44,7 +45,8 @@ size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws) 
   if (ws && base) {
     char *p = static_cast<char *>(base);
     ws->status = reinterpret_cast<unsigned *>(p + o_status);
-    ws->prompt_ticket = reinterpret_cast<unsigned *>(p + o_pt);
+    ws->weights_done = reinterpret_cast<unsigned *>(p + o_wd);
+    ws->bonus_done = reinterpret_cast<unsigned *>(p + o_bd);
     ws->row_ticket = reinterpret_cast<unsigned *>(p + o_rt);
     ws->sps_ticket_a = reinterpret_cast<unsigned *>(p + o_sa);
     ws->sps_ticket_b = reinterpret_cast<unsigned *>(p + o_sb);

@@ -89,13 +89,6 @@ __device__ __forceinline__ ff ff_div(ff a, ff b) {
 __device__ __forceinline__ bool ff_gt(ff a, ff b) {
   return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo);
 }
-__device__ __forceinline__ double ff_to_double(ff a) {
-  return static_cast<double>(a.hi) + static_cast<double>(a.lo);
-}
-__device__ __forceinline__ ff ff_from_double(double x) {
-  const float hi = static_cast<float>(x);
-  return {hi, static_cast<float>(x - static_cast<double>(hi))};
-}
 
 // ---------------------------------------------------------------------------
 // Accurate 2^y for y = yh + yl <= ~0, as an unnormalised float pair with
@@ -133,6 +126,43 @@ __device__ __forceinline__ ff accurate_exp(float d, float dl, const float2 *tab)
   const float yh = d * kLog2eHi;
   const float yl = fmaf(d, kLog2eHi, -yh) + fmaf(d, kLog2eLo, dl * kLog2eHi);
   return accurate_exp2(yh, yl, tab);
+}
+
+// ff_add, ff_sub and ff_mul_f that pass an infinite or NaN operand through
+// as a plain float (the float-float forms would turn an infinite head into
+// NaN): -inf stays -inf, so a weight of 0 stays 0.
+__device__ __forceinline__ ff ff_add_x(ff a, ff b) {
+  return (isfinite(a.hi) && isfinite(b.hi)) ? ff_add(a, b) : ff{a.hi + b.hi, 0.f};
+}
+__device__ __forceinline__ ff ff_sub_x(ff a, ff b) { return ff_add_x(a, ff{-b.hi, -b.lo}); }
+__device__ __forceinline__ ff ff_mul_fx(ff a, float f) {
+  return isfinite(a.hi) ? ff_mul_f(a, f) : ff{a.hi * f, 0.f};
+}
+
+// log(x) of a float-float x >= 2^-100 (normalised), as a float-float value
+// about 1e-9 from the exact logarithm: y0 = logf(x.hi), then one Newton step
+// with the accurate exponential, log x = y0 + log(x e^-y0), where x e^-y0 =
+// 1 + r with |r| ~ 1e-7, so log(1 + r) = r - r^2/2 to far below the exp's
+// own 3e-10.
+__device__ __forceinline__ ff ff_log(ff x, const float2 *tab) {
+  const float y0 = logf(x.hi);
+  const ff e = accurate_exp(-y0, 0.f, tab);
+  const ff p = ff_mul(x, fast_two_sum(e.hi, e.lo));  // x e^-y0, close to 1
+  const float r = (p.hi - 1.f) + p.lo;                // p.hi - 1 is exact (Sterbenz)
+  return fast_two_sum(y0, fmaf(-0.5f * r, r, r));
+}
+__device__ __forceinline__ ff ff_log_f(float x, const float2 *tab) {
+  return ff_log(ff{x, 0.f}, tab);
+}
+
+// A row's log-sum-exp ts*M + log(S) as a float-float value, from its largest
+// logit M and S = sum exp(ts (l - M)) (S >= 1 when M is finite).  Rows with a
+// non-finite M or S (errors reported elsewhere) get the plain fp32 value.
+__device__ __forceinline__ ff row_lse(float ts, float M, float S, const float2 *tab) {
+  if (!(isfinite(M) && S >= 1.f && S < __int_as_float(0x7f800000))) {
+    return ff{ts * M + logf(S), 0.f};
+  }
+  return ff_add(two_prod(ts, M), ff_log_f(S, tab));
 }
 
 // Accumulate an unnormalised pair into a running float-float sum.
@@ -317,49 +347,6 @@ __device__ __forceinline__ ff block_ff_scan(ff v, float2 *scratch, ff *total) {
   return ff_add(base, v);
 }
 
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-__device__ __forceinline__ double warp_max_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-__device__ __forceinline__ double block_sum_d(double v, double *scratch) {
-  v = warp_sum_d(v);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __syncthreads();
-  if (lane == 0) scratch[warp] = v;
-  __syncthreads();
-  v = lane < kWarps ? scratch[lane] : 0.0;
-  return warp_sum_d(v);
-}
-__device__ __forceinline__ double block_max_d(double v, double *scratch) {
-  v = warp_max_d(v);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __syncthreads();
-  if (lane == 0) scratch[warp] = v;
-  __syncthreads();
-  v = lane < kWarps ? scratch[lane] : -__longlong_as_double(0x7ff0000000000000ll);
-  return warp_max_d(v);
-}
-// Inclusive scan of doubles in thread order.
-__device__ __forceinline__ double block_scan_d(double v, double *scratch) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double w = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += w;
-  }
-  __syncthreads();
-  if (lane == 31) scratch[warp] = v;
-  __syncthreads();
-  double base = 0.0;
-  for (int w = 0; w < warp; ++w) base += scratch[w];
-  return base + v;
-}
 // Exclusive scan of ints in thread order; *total gets the sum.
 __device__ __forceinline__ int block_excl_scan_i(int v, int *scratch, int *total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -474,6 +461,58 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
           "r"(smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// A hint to bring [p, p + bytes) into L2: the 16-byte-aligned part of the
+// range, by one bulk prefetch (no data moves to the SM; nothing to wait for).
+__device__ __forceinline__ void prefetch_l2(const void *p, size_t bytes) {
+  const unsigned long long a0 = reinterpret_cast<unsigned long long>(p);
+  const unsigned long long s = (a0 + 15ull) & ~15ull, e = (a0 + bytes) & ~15ull;
+  if (e > s) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(s),
+                 "r"(static_cast<unsigned>(e - s))
+                 : "memory");
+  }
+}
+
+// A named CTA barrier (id 1..15) over `n` threads, a multiple of 32: only
+// the warps that take part wait for one another.
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Counters that one kernel's CTAs raise and a concurrent kernel's CTAs wait
+// on (gpu scope).  add_release publishes the calling thread's earlier writes
+// with the increment; a thread whose acquire load reads the count sees them.
+__device__ __forceinline__ void add_release_gpu(unsigned *p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Waits until *p reaches `target`: at most `limit` polls, backing off to
+// about a microsecond between them.  False when it gave up.
+__device__ __forceinline__ bool wait_count(const unsigned *p, unsigned target, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (ld_acquire_gpu(p) >= target) return true;
+    __nanosleep(i < 64 ? 32 : 1024);
+  }
+  return ld_acquire_gpu(p) >= target;
+}
+
+// Asynchronous 4-byte global-to-shared copy (cp.async): issued without
+// waiting; cp_async_wait_all waits for the calling thread's copies (a CTA
+// barrier after it makes them visible to the other threads).
+__device__ __forceinline__ void cp_async4(void *smem_dst, const void *gmem_src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(smem_dst)),
+               "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // Device status word: OR in error bits (never traps, never waits).

@@ -35,7 +35,8 @@ struct KvArgs {
 // Workspace carve-up shared by every entry point.
 struct Workspace {
   unsigned *status;          // [1]  device status bits
-  unsigned *prompt_ticket;   // [B]  (unused: the tail is its own kernel)
+  unsigned *weights_done;    // [B]  particles of the prompt whose new log-weight is published
+  unsigned *bonus_done;      // [B]  particles of the prompt whose bonus token is published
   unsigned *row_ticket;      // [rows]
   unsigned *sps_ticket_a;    // [B]
   unsigned *sps_ticket_b;    // [B]

@@ -23,6 +23,7 @@
 // ticket) combines it.  smc_resample and kv_blocktable_remap run the tail's
 // pieces alone (resample_kernel, kv_remap_kernel).  With top_p < 1 the
 // nucleus kernel (topp.cu) runs between the row combine and the tail.
+#include <atomic>
 #include <cmath>
 
 #include "row_common.cuh"
@@ -42,61 +43,81 @@ int chunks_per_row(int dtype, int V) {
 // Blocks that hold `len` tokens (64-bit, so a corrupt length cannot overflow).
 // ---------------------------------------------------------------------------
 // Normalise one prompt's log-weights, compute ESS and, below the threshold,
-// resample systematically.  fp32 throughout (FP64 is a slow path on this
-// GPU, and the row statistics feeding the weights are fp32-accurate).  The
-// block version serves any N <= 256; thread i < N holds lw_i and, on return,
-// s_anc[i] holds the ancestor of particle i.
+// resample systematically.  The log-weights arrive as float-float values
+// (the fp32 state plus this step's increment, unrounded) and everything
+// stays float-float on the fp32 pipes (this GPU's fp64 rate is far lower).
+// With e_i = exp(lw_i - max) by the accurate exponential (about 3e-10),
+// S = sum e and Q = sum e^2, the normalised weights are w = e / S, so
+//   ESS = 1 / sum w^2 = S^2 / Q,  resample iff S^2 < tau N Q,
+// and ancestor a_i = min{j : C_j > (u0 + i)/N} with C the prefix of w is
+// the first j whose prefix of e exceeds (u0 + i) S / N: no division on the
+// critical path.  u0 is the step's resampling uniform of the prompt and rN
+// the float-float 1/N, both computed by the caller ahead of time.  The
+// block version serves any N <= 256; thread i < N holds lw_i and, on
+// return, s_anc[i] holds the ancestor of particle i.  `tab` is the 2^(j/64)
+// table in shared memory.
 // ---------------------------------------------------------------------------
 struct ResampleResult { bool resampled; float ess; };
 
-// Smallest j in [0, n) with c[j] > pt, clamped to n-1.
-__device__ __forceinline__ int first_above(const float *c, int n, float pt) {
+// Smallest j in [0, n) with c[j] > pt, clamped to n-1 (c as float-float).
+__device__ __forceinline__ int first_above(const float2 *c, int n, ff pt) {
   int lo = 0, hi = n - 1;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
-    if (c[mid] > pt) hi = mid; else lo = mid + 1;
+    if (ff_gt(ff{c[mid].x, c[mid].y}, pt)) hi = mid; else lo = mid + 1;
   }
   return lo;
 }
 
-__device__ __forceinline__ float block_scan_f(float v, float *scratch) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float w = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += w;
-  }
-  __syncthreads();
-  if (lane == 31) scratch[warp] = v;
-  __syncthreads();
-  float base = 0.f;
-  for (int w = 0; w < warp; ++w) base += scratch[w];
-  return base + v;
+// Weight e = exp(lw - m) of one particle (0 for -inf or invalid).
+__device__ __forceinline__ ff particle_mass(ff lw, float m, bool use, const float2 *tab) {
+  if (!use) return ff{0.f, 0.f};
+  const ff d = ff_sub(lw, ff{m, 0.f});
+  return ff_norm(accurate_exp(d.hi, d.lo, tab));
 }
 
-__device__ ResampleResult normalise_resample(int b, int N, float lw, bool valid, float ess_frac,
-                                             uint64_t seed, uint32_t step, unsigned *status,
-                                             int *s_anc, float *s_c, float *s_red) {
+// The resampling inputs that do not depend on the weights: the prompt's
+// uniform u0 and 1/N as a float-float value.
+struct ResampleKey { float u0; ff rn; };
+__device__ __forceinline__ ResampleKey resample_key(uint64_t seed, uint32_t step, int b, int N) {
+  return {philox_uniform(seed, step, b, 0, SMC_PURPOSE_RESAMPLE),
+          ff_div(ff{1.f, 0.f}, ff{static_cast<float>(N), 0.f})};
+}
+
+// ESS = S^2 / Q and the decision S^2 < tau N Q.
+__device__ __forceinline__ bool resample_decision(ff S, ff Q, float ess_frac, int N, bool ok,
+                                                  float *ess) {
+  const ff s2 = ff_mul(S, S);
+  *ess = ff_div(s2, Q).hi;
+  return ok && ff_gt(ff_mul(two_prod(ess_frac, static_cast<float>(N)), Q), s2);
+}
+
+__device__ __noinline__ ResampleResult normalise_resample(int N, ff lw, bool valid,
+                                                          float ess_frac,
+                                             ResampleKey key, unsigned *status, int *s_anc,
+                                             float2 *s_c, float2 *s_red, const float2 *tab) {
   constexpr float kInf = -kNegInf;
   unsigned bits = 0;
-  if (valid && (isnan(lw) || lw == kInf)) bits |= SMC_DEV_NONFINITE;
-  const float m = block_max(valid && !isnan(lw) ? lw : kNegInf, s_red);
+  if (valid && (isnan(lw.hi) || lw.hi == kInf)) bits |= SMC_DEV_NONFINITE;
+  const float m = block_max(valid && !isnan(lw.hi) ? lw.hi : kNegInf,
+                            reinterpret_cast<float *>(s_red));
   const bool ok = m > kNegInf && m < kInf;
   if (threadIdx.x == 0 && m == kNegInf) bits |= SMC_DEV_ALL_ZERO_WEIGHT;
   if (bits) raise_status(status, bits);
-  const float e = (valid && ok) ? expf(lw - m) : 0.f;
-  const float big_l = m + logf(block_sum_f(e, s_red));
-  const float w = (valid && ok) ? expf(lw - big_l) : 0.f;
-  const float ess = 1.f / block_sum_f(w * w, s_red);
-  const bool resample = ok && ess < ess_frac * static_cast<float>(N);
+  const ff e = particle_mass(lw, m, valid && ok, tab);
+  const ff S = block_ff_sum(e, s_red);
+  const ff Q = block_ff_sum(ff_mul(e, e), s_red);
+  float ess;
+  const bool resample = resample_decision(S, Q, ess_frac, N, ok, &ess);
   int anc = threadIdx.x;
   if (resample) {
-    const float c = block_scan_f(w, s_red);
-    if (valid) s_c[threadIdx.x] = c;
+    ff total;
+    const ff c = block_ff_scan(e, s_red, &total);
+    if (valid) s_c[threadIdx.x] = make_float2(c.hi, c.lo);
     __syncthreads();
     if (valid) {
-      const float u0 = philox_uniform(seed, step, b, 0, SMC_PURPOSE_RESAMPLE);
-      anc = first_above(s_c, N, (u0 + static_cast<float>(threadIdx.x)) / static_cast<float>(N));
+      const ff pt = ff_mul(ff_mul(two_sum(key.u0, static_cast<float>(threadIdx.x)), S), key.rn);
+      anc = first_above(s_c, N, pt);
     }
   }
   if (valid) s_anc[threadIdx.x] = anc;
@@ -105,40 +126,37 @@ __device__ ResampleResult normalise_resample(int b, int N, float lw, bool valid,
 }
 
 // The same for N <= 32, by warp 0 alone with shuffles (no CTA barrier).
-__device__ ResampleResult normalise_resample_warp(int b, int N, float lw, bool valid,
-                                                  float ess_frac, uint64_t seed, uint32_t step,
-                                                  unsigned *status, int *s_anc, float *s_c) {
+__device__ ResampleResult normalise_resample_warp(int N, ff lw, bool valid, float ess_frac,
+                                                  ResampleKey key, unsigned *status, int *s_anc,
+                                                  float2 *s_c, const float2 *tab) {
   constexpr float kInf = -kNegInf;
   const int lane = threadIdx.x & 31;
   unsigned bits = 0;
-  if (valid && (isnan(lw) || lw == kInf)) bits |= SMC_DEV_NONFINITE;
-  const float m = warp_max(valid && !isnan(lw) ? lw : kNegInf);
+  if (valid && (isnan(lw.hi) || lw.hi == kInf)) bits |= SMC_DEV_NONFINITE;
+  const float m = warp_max(valid && !isnan(lw.hi) ? lw.hi : kNegInf);
   const bool ok = m > kNegInf && m < kInf;
   if (lane == 0 && m == kNegInf) bits |= SMC_DEV_ALL_ZERO_WEIGHT;
   if (bits) raise_status(status, bits);
-  float e = (valid && ok) ? expf(lw - m) : 0.f;
+  const ff e = particle_mass(lw, m, valid && ok, tab);
+  // S = sum e and Q = sum e^2, the two butterflies interleaved
+  ff S = e, Q = ff_mul(e, e);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
-  const float big_l = m + logf(e);
-  const float w = (valid && ok) ? expf(lw - big_l) : 0.f;
-  float w2 = w * w;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) w2 += __shfl_xor_sync(0xffffffffu, w2, o);
-  const float ess = 1.f / w2;
-  const bool resample = ok && ess < ess_frac * static_cast<float>(N);
+  for (int o = 16; o > 0; o >>= 1) {
+    const ff s2{__shfl_xor_sync(0xffffffffu, S.hi, o), __shfl_xor_sync(0xffffffffu, S.lo, o)};
+    const ff q2{__shfl_xor_sync(0xffffffffu, Q.hi, o), __shfl_xor_sync(0xffffffffu, Q.lo, o)};
+    S = ff_add(S, s2);
+    Q = ff_add(Q, q2);
+  }
+  float ess;
+  const bool resample = resample_decision(S, Q, ess_frac, N, ok, &ess);
   int anc = lane;
   if (resample) {
-    float c = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float v = __shfl_up_sync(0xffffffffu, c, o);
-      if (lane >= o) c += v;
-    }
-    if (valid) s_c[lane] = c;
+    const ff c = warp_ff_incl_scan(e);
+    if (valid) s_c[lane] = make_float2(c.hi, c.lo);
     __syncwarp();
     if (valid) {
-      const float u0 = philox_uniform(seed, step, b, 0, SMC_PURPOSE_RESAMPLE);
-      anc = first_above(s_c, N, (u0 + static_cast<float>(lane)) / static_cast<float>(N));
+      const ff pt = ff_mul(ff_mul(two_sum(key.u0, static_cast<float>(lane)), S), key.rn);
+      anc = first_above(s_c, N, pt);
     }
   }
   if (valid) s_anc[lane] = anc;
@@ -214,11 +232,199 @@ __device__ void kv_copy_in(const KvArgs &kv, int b, int N, const KvScratch &sc, 
   }
 }
 
+// The staged copy-in of kv_copy_in, by asynchronous copies that the caller
+// waits for later (cp_async_wait_all, then a CTA barrier): prompt b's tables,
+// token counts and reference counts; the freed-block bitmap and the count
+// changes are cleared.  The free stack's top entries need free_top first and
+// come separately (kv_copy_stack_async).  All threads of the CTA call it.
+__device__ void kv_copy_in_async(const KvArgs &kv, int b, int N, const KvScratch &sc) {
+  const int T = kv.T, P = kv.P;
+  const int words = (P + 31) / 32;
+  const int t = threadIdx.x;
+  const int32_t *tables = kv.tables + static_cast<size_t>(b) * N * T;
+  for (int i = t; i < N * T; i += kThreads) cp_async4(sc.old_t + i, tables + i);
+  const int32_t *len = kv.seq_len + static_cast<size_t>(b) * N;
+  for (int i = t; i < N; i += kThreads) cp_async4(sc.old_l + i, len + i);
+  const int32_t *rc = kv.refcount + static_cast<size_t>(b) * P;
+  for (int i = t; i < P; i += kThreads) cp_async4(sc.rc + i, rc + i);
+  for (int w = t; w < words; w += kThreads) sc.bits[w] = 0u;
+  for (int k = t; k < P; k += kThreads) sc.delta[k] = 0;
+}
+
+// The top kStackPre entries of prompt b's free stack (stk[k] = entry k below
+// the top `top`) and the top itself, by asynchronous copies.
+__device__ void kv_copy_stack_async(const KvArgs &kv, int b, int top, const KvScratch &sc) {
+  const int P = kv.P;
+  const int32_t *stack = kv.free_list + static_cast<size_t>(b) * P;
+  if (threadIdx.x == 0) *sc.top0 = top;
+  const int n_pre = (top >= 0 && top <= P) ? min(top, kStackPre) : 0;
+  for (int k = threadIdx.x; k < n_pre; k += kThreads) cp_async4(sc.stk + k, stack + top - 1 - k);
+}
+
+// L2 prefetch of what a prompt's remap stages: tables, token counts,
+// reference counts, the free stack and its top.
+__device__ __forceinline__ void kv_prefetch_l2(const KvArgs &kv, int b, int N) {
+  const size_t nt = static_cast<size_t>(N) * kv.T, p = static_cast<size_t>(kv.P);
+  prefetch_l2(kv.tables + b * nt, nt * sizeof(int32_t));
+  prefetch_l2(kv.refcount + b * p, p * sizeof(int32_t));
+  prefetch_l2(kv.free_list + b * p, p * sizeof(int32_t));
+  prefetch_l2(kv.seq_len + static_cast<size_t>(b) * N, static_cast<size_t>(N) * sizeof(int32_t));
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(kv.free_top + b));
+}
+
+// The count update of a remap whose copy of the tables lives in workspace
+// scratch (prompts too large to stage in shared memory): global atomics, new
+// references first, so that no count touches 0 before every increment is in.
+// Out of line: shapes that stage in shared memory never run it.  Returns
+// false (with *s_flag set) when a block id lies outside the prompt's pool.
+// All threads of the CTA call it.
+__device__ __noinline__ bool kv_remap_unstaged(const KvArgs &kv, int N, const int *s_anc,
+                                               const int *s_nb, const KvScratch &sc, int lo_id,
+                                               int32_t *tables, int32_t *seq_len,
+                                               volatile int *s_flag) {
+  const int T = kv.T, P = kv.P;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  auto in_pool = [&](int blk) { return blk >= lo_id && blk < lo_id + P; };
+  for (int i = warp; i < N; i += kWarps) {
+    for (int t = lane; t < s_nb[i]; t += 32) {
+      if (!in_pool(sc.old_t[i * T + t])) *s_flag = 1;
+    }
+  }
+  __syncthreads();
+  if (*s_flag) return false;
+  for (int i = warp; i < N; i += kWarps) {
+    const int a = s_anc[i];
+    const int nb_new = s_nb[a], nb_old = s_nb[i];
+    for (int t = lane; t < nb_new; t += 32) {
+      const int blk = sc.old_t[a * T + t];
+      if (!(t < nb_old && sc.old_t[i * T + t] == blk)) atomicAdd(&kv.refcount[blk], 1);
+    }
+  }
+  __syncthreads();
+  for (int i = warp; i < N; i += kWarps) {
+    const int a = s_anc[i];
+    const int nb_new = s_nb[a], nb_old = s_nb[i];
+    for (int t = lane; t < T; t += 32) {
+      const int nv = sc.old_t[a * T + t];
+      if (t < nb_old) {
+        const int blk = sc.old_t[i * T + t];
+        if (!(t < nb_new && nv == blk)) {
+          if (atomicSub(&kv.refcount[blk], 1) == 1) {
+            const int rel = blk - lo_id;
+            atomicOr(&sc.bits[rel >> 5], 1u << (rel & 31));
+          }
+        }
+      }
+      tables[i * T + t] = nv;
+    }
+  }
+  for (int i = tid; i < N; i += kThreads) seq_len[i] = sc.old_l[s_anc[i]];
+  __syncthreads();
+  return true;
+}
+
+// Shared state of one prompt's remap (kv_prepare, kv_remap_append).
+struct KvSmem {
+  int nb[SMC_MAX_N];     // used blocks of each particle before the remap
+  int otail[SMC_MAX_N];  // its partially filled last block, -1 when it has none
+  int ntail[SMC_MAX_N];  // the same after the remap (append of more than 32 particles)
+  int ired[2 * kWarps];
+  long long ll[kWarps];
+  int bad;               // kv_prepare's findings: kBadState | kBadId | kBadTail
+  int top_old;           // free_top before the remap
+  int n_freed;           // blocks the remap pushed
+  int flag;              // the unstaged remap's error flag
+  int t_common;          // first table slot at which the particles' tables differ
+};
+constexpr int kBadState = 1;  // a token count outside [0, T*block_size] or free_top outside [0, P]
+constexpr int kBadId = 2;     // a used block outside the prompt's pool
+constexpr int kBadTail = 4;   // a partially filled last block outside the pool
+
+// What the remap and the append read of the state before the remap, by
+// threads [t0, t0 + nt) of the CTA with no barrier inside (ks.bad must be 0
+// and ks.t_common T beforehand, kv_prepare_init; the caller's barrier
+// publishes the rest): each particle's used block count and partial tail
+// block, free_top, the checks of the ids, and the first table slot at which
+// two particles differ (in the block id or in whether the slot is used).
+// Every used block of every particle is checked, so that a remap can take
+// any of them without checking again.  Below t_common every particle holds
+// the same blocks (the shared prefix), so no remap changes a table or a
+// count there.
+__device__ __forceinline__ void kv_prepare_init(KvSmem &ks, int T) {
+  ks.bad = 0;
+  ks.t_common = T;
+}
+
+__device__ void kv_prepare(const KvArgs &kv, int b, int N, const KvScratch &sc, KvSmem &ks,
+                           int t0, int nt) {
+  const int t = static_cast<int>(threadIdx.x) - t0;
+  if (t < 0 || t >= nt) return;
+  const int T = kv.T, bs = kv.block_size, P = kv.P;
+  const int lo_id = b * P;
+  const long long cap = static_cast<long long>(T) * bs;  // tokens a full table holds
+  auto in_pool = [&](int blk) { return blk >= lo_id && blk < lo_id + P; };
+  int bad = 0;
+  if (t == 0) {
+    const int top0 = sc.rc ? *sc.top0 : __ldcg(kv.free_top + b);
+    ks.top_old = top0;
+    if (top0 < 0 || top0 > P) bad |= kBadState;
+  }
+  for (int i = t; i < N; i += nt) {
+    const int len = sc.old_l[i];
+    int nb = 0, tail = -1;
+    if (len < 0 || len > cap) {
+      bad |= kBadState;
+    } else {
+      nb = static_cast<int>((static_cast<long long>(len) + bs - 1) / bs);
+      if (len % bs) {
+        tail = sc.old_t[i * T + nb - 1];
+        if (!in_pool(tail)) bad |= kBadTail;
+      }
+    }
+    ks.nb[i] = nb;
+    ks.otail[i] = tail;
+  }
+  // every slot: a warp of the group per particle, a lane per slot
+  const int lane = t & 31, nw = nt >> 5;
+  const int len0 = sc.old_l[0];
+  const long long nb0 = (len0 < 0 || len0 > cap) ? -1 : (static_cast<long long>(len0) + bs - 1) / bs;
+  for (int i = t >> 5; i < N; i += nw) {
+    const int len = sc.old_l[i];
+    if (len < 0 || len > cap) continue;  // flagged above
+    const int nb = static_cast<int>((static_cast<long long>(len) + bs - 1) / bs);
+    int first = T;
+    for (int s = lane; s < T; s += 32) {
+      const int v = sc.old_t[i * T + s];
+      if (s < nb && !in_pool(v)) bad |= kBadId;
+      if (first == T && (v != sc.old_t[s] || (s < nb) != (s < nb0))) first = s;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(0xffffffffu, first, o));
+    if (lane == 0 && first < T) atomicMin(&ks.t_common, first);
+  }
+  if (bad) atomicOr(&ks.bad, bad);
+}
+
+// Exclusive warp scan of v (all lanes); *total gets the warp's sum.
+__device__ __forceinline__ int warp_excl_scan_i(int v, int *total) {
+  const int lane = threadIdx.x & 31;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  *total = __shfl_sync(0xffffffffu, x, 31);
+  return x - v;
+}
+
+// Remap of prompt b's block tables by the ancestors s_anc (when resampled)
+// and append of n_append tokens to every particle, by the whole CTA.  With
+// `prepared`, kv_prepare has run on the staged state (all threads passed a
+// barrier since); with `copied`, the state is already in `sc`.
 __device__ void kv_remap_append(const KvArgs &kv, int b, int N, const int *s_anc, bool resampled,
-                                int n_append, const Workspace &ws, int *s_i, int *s_tail,
-                                int *s_nb, const KvScratch &sc, bool copied) {
-  __shared__ int s_flag, s_top_old, s_n_freed;
-  __shared__ long long s_ll[kWarps];
+                                int n_append, const Workspace &ws, KvSmem &ks,
+                                const KvScratch &sc, bool copied, bool prepared) {
   const int T = kv.T, bs = kv.block_size, P = kv.P;
   const int lo_id = b * P;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -227,181 +433,241 @@ __device__ void kv_remap_append(const KvArgs &kv, int b, int N, const int *s_anc
   int32_t *tables = kv.tables + static_cast<size_t>(b) * N * T;
   int32_t *seq_len = kv.seq_len + static_cast<size_t>(b) * N;
   int32_t *stack = kv.free_list + static_cast<size_t>(b) * P;
-  const long long cap = static_cast<long long>(T) * bs;  // tokens a full table holds
-  if (!copied) kv_copy_in(kv, b, N, sc, 0, kThreads);
-  if (!staged && tid == 0) {
-    const int top0 = kv.free_top[b];
-    s_top_old = top0;
-    s_flag = (top0 < 0 || top0 > P) ? 1 : 0;
-    kv.n_cow[b] = 0;
-  }
-  __syncthreads();
-  if (staged && tid == 0) {
-    const int top0 = *sc.top0;
-    s_top_old = top0;
-    s_flag = (top0 < 0 || top0 > P) ? 1 : 0;
-    kv.n_cow[b] = 0;
-  }
-  if (tid == 0) s_n_freed = 0;
-  __syncthreads();
   auto in_pool = [&](int blk) { return blk >= lo_id && blk < lo_id + P; };
   auto fail = [&]() {
     if (tid == 0) raise_status(ws.status, SMC_DEV_BAD_BLOCK);
   };
-  if (s_flag) { fail(); return; }
-  // used blocks of every (pre-remap) particle; a bad count is an error
-  for (int i = tid; i < N; i += kThreads) {
-    const int len = sc.old_l[i];
-    if (len < 0 || len > cap) {
-      s_flag = 1;
-      s_nb[i] = 0;
-    } else {
-      s_nb[i] = static_cast<int>((static_cast<long long>(len) + bs - 1) / bs);
-    }
+  if (!copied) kv_copy_in(kv, b, N, sc, 0, kThreads);
+  if (!prepared) {
+    if (tid == 0) kv_prepare_init(ks, T);
+    __syncthreads();
+    kv_prepare(kv, b, N, sc, ks, 0, kThreads);
+  }
+  if (tid == 0) {
+    kv.n_cow[b] = 0;
+    ks.n_freed = 0;
+    ks.flag = 0;
   }
   __syncthreads();
-  if (s_flag) { fail(); return; }
+  {
+    const int bad = ks.bad;
+    if ((bad & kBadState) || (bad & (resampled ? kBadId : kBadTail))) {
+      fail();
+      return;
+    }
+  }
+  const int top_old = ks.top_old;
+  // the append runs on warp 0 alone for N <= 32 (staged state)
+  const bool warp_path = N <= 32 && staged;
 
   if (resampled) {
     if (staged) {
-      // net reference-count change per block in shared memory, then one pass
-      // over the pool applies it; a count reaching 0 frees the block.  Every
-      // used slot of every old table is seen here (as ov of its particle),
-      // so the pool check of the ids happens in the same pass; a slot whose
-      // value does not change is not rewritten.
-      for (int i = warp; i < N; i += kWarps) {
-        const int a = s_anc[i];
-        const int nb_new = s_nb[a], nb_old = s_nb[i];
-        for (int t = lane; t < T; t += 32) {
-          const int nv = sc.old_t[a * T + t];
-          const int ov = sc.old_t[i * T + t];
-          const bool has_new = t < nb_new, has_old = t < nb_old;
-          if ((has_new && !in_pool(nv)) || (has_old && !in_pool(ov))) {
-            s_flag = 1;
-            continue;
+      // net reference-count change per block in shared memory: a slot whose
+      // block changes gives +1 to the new block and -1 to the old one; then
+      // a pass over the same slots applies the changes, and a count reaching
+      // 0 frees the block.  Only slots from t_common on can change.  Slot
+      // (i, t) sits at idx = t N + i, so consecutive threads take consecutive
+      // particles at one slot (blocks appended in the same step sit N ids
+      // apart along a table: a warp along one table would send its updates to
+      // two banks).  Each thread's slots advance by kThreads; their loads are
+      // issued in batches of kU before the updates.
+      constexpr int kU = 4;
+      const int tc = ks.t_common;
+      const int di = kThreads % N, dt = kThreads / N;
+      int i = tid % N, t = tc + tid / N;
+      while (t < T) {
+        int ia[kU], ta[kU], nv[kU], ov[kU];
+        bool upd[kU], hn[kU], ho[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          ia[u] = i;
+          ta[u] = t;
+          upd[u] = false;
+          if (t < T) {
+            const int anc = s_anc[i];
+            upd[u] = anc != i;  // a particle that is its own ancestor keeps its table
+            nv[u] = sc.old_t[anc * T + t];
+            ov[u] = sc.old_t[i * T + t];
+            hn[u] = t < ks.nb[anc];
+            ho[u] = t < ks.nb[i];
           }
-          if (has_new && !(has_old && ov == nv)) atomicAdd(&sc.delta[nv - lo_id], 1);
-          if (has_old && !(has_new && nv == ov)) atomicSub(&sc.delta[ov - lo_id], 1);
-          if (nv != ov) tables[i * T + t] = nv;
+          i += di;
+          t += dt;
+          if (i >= N) {
+            i -= N;
+            ++t;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          if (!upd[u]) continue;
+          if (hn[u] && !(ho[u] && ov[u] == nv[u])) atomicAdd(&sc.delta[nv[u] - lo_id], 1);
+          if (ho[u] && !(hn[u] && nv[u] == ov[u])) atomicSub(&sc.delta[ov[u] - lo_id], 1);
+          if (nv[u] != ov[u]) tables[ia[u] * T + ta[u]] = nv[u];
         }
       }
-      for (int i = tid; i < N; i += kThreads) seq_len[i] = sc.old_l[s_anc[i]];
+      for (int p = tid; p < N; p += kThreads) seq_len[p] = sc.old_l[s_anc[p]];
       __syncthreads();
-      if (s_flag) { fail(); return; }
-      for (int k = tid; k < P; k += kThreads) {
-        const int d = sc.delta[k];
-        if (d != 0) {
-          const int nr = sc.rc[k] + d;
-          kv.refcount[lo_id + k] = nr;
-          if (nr == 0) atomicOr(&sc.bits[k >> 5], 1u << (k & 31));
+      // every block whose count changed is an old block at a slot from
+      // t_common on; the first thread to reach it takes its change
+      i = tid % N;
+      t = tc + tid / N;
+      for (; t < T;) {
+        if (t < ks.nb[i]) {
+          const int k = sc.old_t[i * T + t] - lo_id;
+          const int d = atomicExch(&sc.delta[k], 0);
+          if (d != 0) {
+            const int nr = sc.rc[k] + d;
+            kv.refcount[lo_id + k] = nr;
+            if (nr == 0) atomicOr(&sc.bits[k >> 5], 1u << (k & 31));
+          }
+        }
+        i += di;
+        t += dt;
+        if (i >= N) {
+          i -= N;
+          ++t;
         }
       }
       __syncthreads();
     } else {
-      for (int i = warp; i < N; i += kWarps) {
-        for (int t = lane; t < s_nb[i]; t += 32) {
-          if (!in_pool(sc.old_t[i * T + t])) s_flag = 1;
-        }
+      if (!kv_remap_unstaged(kv, N, s_anc, ks.nb, sc, lo_id, tables, seq_len, &ks.flag)) {
+        fail();
+        return;
       }
-      __syncthreads();
-      if (s_flag) { fail(); return; }
-      // new references first, so no count touches 0 before every increment is in
-      for (int i = warp; i < N; i += kWarps) {
-        const int a = s_anc[i];
-        const int nb_new = s_nb[a], nb_old = s_nb[i];
-        for (int t = lane; t < nb_new; t += 32) {
-          const int blk = sc.old_t[a * T + t];
-          if (!(t < nb_old && sc.old_t[i * T + t] == blk)) atomicAdd(&kv.refcount[blk], 1);
-        }
-      }
-      __syncthreads();
-      for (int i = warp; i < N; i += kWarps) {
-        const int a = s_anc[i];
-        const int nb_new = s_nb[a], nb_old = s_nb[i];
-        for (int t = lane; t < T; t += 32) {
-          const int nv = sc.old_t[a * T + t];
-          if (t < nb_old) {
-            const int blk = sc.old_t[i * T + t];
-            if (!(t < nb_new && nv == blk)) {
-              if (atomicSub(&kv.refcount[blk], 1) == 1) {
-                const int rel = blk - lo_id;
-                atomicOr(&sc.bits[rel >> 5], 1u << (rel & 31));
-              }
-            }
-          }
-          tables[i * T + t] = nv;
-        }
-      }
-      for (int i = tid; i < N; i += kThreads) seq_len[i] = sc.old_l[s_anc[i]];
-      __syncthreads();
     }
-    // push freed blocks in ascending id order (staged: also list them in
+    // push the freed blocks in ascending id order (staged: also list them in
     // `delta`, whose counts are spent)
-    int top = s_top_old;
-    for (int w0 = 0; w0 < words; w0 += kThreads) {
-      const int w = w0 + tid;
-      unsigned fb = w < words ? sc.bits[w] : 0u;
-      int total;
-      int pos = top + block_excl_scan_i(__popc(fb), s_i, &total);
-      if (fb) sc.bits[w] = 0u;
-      while (fb) {
-        const int bit = __ffs(fb) - 1;
-        fb &= fb - 1;
-        if (pos < P) {
-          stack[pos] = lo_id + w * 32 + bit;
-          if (staged) sc.delta[pos - s_top_old] = lo_id + w * 32 + bit;
+    {
+      int top = top_old;
+      for (int w0 = 0; w0 < words; w0 += kThreads) {
+        const int w = w0 + tid;
+        unsigned fb = w < words ? sc.bits[w] : 0u;
+        int total;
+        int pos = top + block_excl_scan_i(__popc(fb), ks.ired, &total);
+        if (fb) sc.bits[w] = 0u;
+        while (fb) {
+          const int bit = __ffs(fb) - 1;
+          fb &= fb - 1;
+          if (pos < P) {
+            stack[pos] = lo_id + w * 32 + bit;
+            if (staged) sc.delta[pos - top_old] = lo_id + w * 32 + bit;
+          }
+          ++pos;
         }
-        ++pos;
+        top += total;
       }
-      top += total;
+      if (top > P) {  // counts did not match the tables
+        fail();
+        return;
+      }
+      if (tid == 0) {
+        kv.free_top[b] = top;
+        ks.n_freed = top - top_old;
+      }
+      __syncthreads();
     }
-    if (top > P) s_flag = 1;  // counts did not match the tables
-    __syncthreads();
-    if (tid == 0) {
-      kv.free_top[b] = min(top, P);
-      s_n_freed = min(top, P) - s_top_old;
-    }
-    if (s_flag) { fail(); return; }
-    __syncthreads();
   }
-  if (n_append <= 0) return;
 
-  // ---- append: particle i's table is now row src(i) of the copy -----------
+  if (warp_path) {
+    if (warp != 0) return;
+    // ---- warp 0: the append ------------------------------------------------
+    const int n_freed = ks.n_freed;
+    if (n_append <= 0) return;
+    const bool valid = lane < N;
+    const int src = valid ? (resampled ? s_anc[lane] : lane) : 0;
+    const int len = valid ? sc.old_l[src] : 0;
+    const int nb = valid ? ks.nb[src] : 0;
+    const int tail = valid ? ks.otail[src] : -1;
+    // a shared partial tail stays with its lowest particle; the others fork
+    const unsigned peers = __match_any_sync(0xffffffffu, tail >= 0 ? tail : -1 - lane);
+    const int fork = (tail >= 0 && __ffs(peers) - 1 != lane) ? 1 : 0;
+    const long long nb2 = valid ? (static_cast<long long>(len) + n_append + bs - 1) / bs : 0;
+    if (__any_sync(0xffffffffu, nb2 > T)) {
+      if (lane == 0) raise_status(ws.status, SMC_DEV_TABLE_OVERFLOW);
+      return;
+    }
+    const int grow = valid ? static_cast<int>(nb2) - nb : 0;
+    int n_forks, total_pops;
+    const int cidx = warp_excl_scan_i(fork, &n_forks);
+    const int off = warp_excl_scan_i(fork + grow, &total_pops);
+    const int top = top_old + n_freed;
+    if (total_pops > top) {
+      if (lane == 0) raise_status(ws.status, SMC_DEV_POOL_EXHAUSTED);
+      return;
+    }
+    auto pop = [&](int k) -> int {
+      if (k < n_freed) return sc.delta[n_freed - 1 - k];
+      const int j = k - n_freed;
+      return j < kStackPre ? sc.stk[j] : stack[top_old - 1 - j];
+    };
+    if (valid) {
+      int k = off;
+      if (fork) {
+        const int d = pop(k);
+        ++k;
+        if (in_pool(d)) {
+          int32_t *pair = kv.cow_pairs + (static_cast<size_t>(b) * N + cidx) * 2;
+          pair[0] = tail;
+          pair[1] = d;
+          tables[lane * T + nb - 1] = d;
+          kv.refcount[d] = 1;
+          atomicSub(&kv.refcount[tail], 1);
+        } else {
+          raise_status(ws.status, SMC_DEV_BAD_BLOCK);
+        }
+      }
+      for (int g = 0; g < grow; ++g) {
+        const int d = pop(k);
+        ++k;
+        if (in_pool(d)) {
+          tables[lane * T + nb + g] = d;
+          kv.refcount[d] = 1;
+        } else {
+          raise_status(ws.status, SMC_DEV_BAD_BLOCK);
+        }
+      }
+      seq_len[lane] = static_cast<int>(len + n_append);
+    }
+    if (lane == 0) {
+      kv.free_top[b] = top - total_pops;
+      kv.n_cow[b] = n_forks;
+    }
+    return;
+  }
+
+  if (n_append <= 0) return;
+  // ---- append by the whole CTA: particle i's table is now row src(i) ------
   const bool valid = tid < N;
   const int src = valid ? (resampled ? s_anc[tid] : tid) : 0;
   int len = 0, nb = 0, tail = -1;
   if (valid) {
     len = sc.old_l[src];
-    nb = s_nb[src];
-    if (len % bs) {
-      tail = sc.old_t[src * T + nb - 1];
-      if (!in_pool(tail)) s_flag = 1;
-    }
-    s_tail[tid] = tail;
+    nb = ks.nb[src];
+    tail = ks.otail[src];
+    ks.ntail[tid] = tail;
   }
   __syncthreads();
-  if (s_flag) { fail(); return; }
   int fork = 0;
   if (valid && tail >= 0) {
     for (int i2 = 0; i2 < tid; ++i2) {
-      if (s_tail[i2] == tail) { fork = 1; break; }
+      if (ks.ntail[i2] == tail) { fork = 1; break; }
     }
   }
   const long long nb2 = valid ? (static_cast<long long>(len) + n_append + bs - 1) / bs : 0;
-  if (valid && nb2 > T) s_flag = 2;
-  const int grow = (valid && nb2 <= T) ? static_cast<int>(nb2) - nb : 0;
+  const bool overflow = __syncthreads_or(valid && nb2 > T) != 0;
+  const int grow = (valid && !overflow) ? static_cast<int>(nb2) - nb : 0;
   // one scan of (forks, pops) packed in 64 bits: forks high, pops low
   long long both_total;
   const long long both = block_excl_scan_ll((static_cast<long long>(fork) << 32) | (fork + grow),
-                                            s_ll, &both_total);
+                                            ks.ll, &both_total);
   const int off = static_cast<int>(both & 0xffffffffll);
   const int cidx = static_cast<int>(both >> 32);
   const int total_pops = static_cast<int>(both_total & 0xffffffffll);
   const int n_forks = static_cast<int>(both_total >> 32);
-  const int n_freed = s_n_freed, top_old = s_top_old;
+  const int n_freed = ks.n_freed;
   const int top = top_old + n_freed;
-  __syncthreads();
-  if (s_flag == 2) {
+  if (overflow) {
     if (tid == 0) raise_status(ws.status, SMC_DEV_TABLE_OVERFLOW);
     return;
   }
@@ -486,63 +752,79 @@ constexpr int kTailTokens = 2048;  // drafted tokens of a prompt staged in share
 
 struct TailSmem {
   int tok[kTailTokens];
-  float c[SMC_MAX_N];
-  float red[2 * kWarps];
+  float2 c[SMC_MAX_N];
+  float2 red[2 * kWarps];
+  float2 tab[64];
   int anc[SMC_MAX_N];
   int bonus[SMC_MAX_N];
-  int tail[SMC_MAX_N];
-  int nb[SMC_MAX_N];
   int ired[2 * kWarps];
+  KvSmem ks;
 };
 
-// Runs in tail_kernel, launched with programmatic dependent launch while the
-// finish kernel still runs.  The KV state, the incoming log-weights and the
-// drafted tokens were all written before this step's first kernel, so they
-// are read before waiting for the finish kernel; only the row results are
-// read after.
-__device__ void smc_tail(const StepArgs &a, int b, TailSmem &sm, int *dyn, bool kv_staged) {
-  const int N = a.N, K = a.K, rpp = 2 * K + 1;
+// Stages what a prompt's tail reads that no kernel of this step writes: the
+// KV state (in shared memory when `sc` is staged, else in workspace scratch),
+// the drafted tokens and the incoming log-weight of particle tid (returned);
+// *top receives the prompt's free_top.  Called before the wait on the row
+// kernels.  Staged copies are asynchronous: the caller issues the stack's
+// copy (tail_prefetch_stack, once *top has arrived) and waits for them all
+// (cp_async_wait_all) before prompt_tail.
+__device__ float tail_prefetch(const StepArgs &a, int b, TailSmem &sm, const KvScratch &sc,
+                               int *top) {
+  const int N = a.N, K = a.K;
+  const int tid = threadIdx.x;
+  stage_exp2_table(sm.tab);
+  *top = 0;
+  if (a.use_kv) {
+    if (sc.rc) {
+      kv_copy_in_async(a.kv, b, N, sc);
+      *top = __ldcg(a.kv.free_top + b);
+    } else {
+      kv_copy_in(a.kv, b, N, sc, 0, kThreads);
+    }
+  }
+  if (N * K <= kTailTokens) {
+    const int32_t *tok = a.tokens + static_cast<size_t>(b) * N * K;
+    for (int i = tid; i < N * K; i += kThreads) cp_async4(sm.tok + i, tok + i);
+  }
+  return tid < N ? __ldcg(a.out.log_weights + static_cast<size_t>(b) * N + tid) : 0.f;
+}
+
+__device__ __forceinline__ void tail_prefetch_stack(const StepArgs &a, int b, int top,
+                                                    const KvScratch &sc) {
+  if (a.use_kv && sc.rc) kv_copy_stack_async(a.kv, b, top, sc);
+}
+
+// A prompt's weights once every particle's increment is known: thread i < N
+// holds lwf = the incoming log-weight plus this step's increment (float-float,
+// unrounded); sm.tab holds the 2^(j/64) table; key = resample_key(seed, step,
+// b, N).  Normalisation, ESS, systematic resampling (ancestors in sm.anc) and
+// the emission of each particle's K drafted tokens, taken from its ancestor;
+// the bonus slot of each output is the caller's.  With `sc` (the staged KV
+// state), kv_prepare also runs: on warps 1.. while warp 0 takes the weights
+// (N <= 32), else after them.  All threads of the CTA call it, after
+// tail_prefetch; all get whether the prompt resampled.
+__device__ bool prompt_weights(const StepArgs &a, int b, TailSmem &sm, ff lwf, ResampleKey key,
+                               const KvScratch *sc) {
+  const int N = a.N, K = a.K;
   const int tid = threadIdx.x;
   const bool small = N <= 32;
-  __shared__ int s_res;
-  const KvScratch sc = a.use_kv ? kv_scratch(a.kv, b, N, a.ws, dyn, kv_staged) : KvScratch{};
-  if (a.use_kv) kv_copy_in(a.kv, b, N, sc, 0, kThreads);
   const bool tok_staged = N * K <= kTailTokens;
-  if (tok_staged) {
-    copy_batched(sm.tok, a.tokens + static_cast<size_t>(b) * N * K, N * K, tid, kThreads);
-  }
+  __shared__ int s_res;
   const bool valid = tid < N;
   const int part = b * N + tid;
-  const float lw0 = valid ? __ldcg(a.out.log_weights + part) : 0.f;
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (tok_staged) __syncthreads();  // sm.tok complete
+  if (tid == 0) kv_prepare_init(sm.ks, a.use_kv ? a.kv.T : 0);
+  cp_async_wait_all();  // this thread's staged copies
+  __syncthreads();      // everyone's: sm.tok, the KV stage; and sm.tab
   // with N <= 32, warp 0 alone does the weights (shuffles, no CTA barrier)
-  const bool weights_thread = small ? tid < 32 : true;
-  if (weights_thread) {
-    float lwf = 0.f;
-    if (valid) {
-      const RowResult *r = a.ws.results + static_cast<size_t>(part) * rpp;
-      const float4 rb = __ldcg(reinterpret_cast<const float4 *>(r + K));
-      float delta = 0.f;
-#pragma unroll 4
-      for (int k = 0; k < K; ++k) {
-        const float4 rp = __ldcg(reinterpret_cast<const float4 *>(r + k));
-        const float4 rq = __ldcg(reinterpret_cast<const float4 *>(r + K + 1 + k));
-        delta += a.alpha * (rp.y - rp.x) - (rq.y - rq.x);
-      }
-      if (a.alpha != 1.f) delta += rb.z - a.alpha * rb.x;
-      if (a.potential) delta += __ldcg(a.potential + part);
-      sm.bonus[tid] = __float_as_int(rb.w);
-      lwf = lw0 + delta;
-    }
+  if (small ? tid < 32 : true) {
     const ResampleResult rr =
-        small ? normalise_resample_warp(b, N, lwf, valid, a.ess_frac, a.seed, a.step, a.ws.status,
-                                        sm.anc, sm.c)
-              : normalise_resample(b, N, lwf, valid, a.ess_frac, a.seed, a.step, a.ws.status,
-                                   sm.anc, sm.c, sm.red);
+        small ? normalise_resample_warp(N, lwf, valid, a.ess_frac, key, a.ws.status, sm.anc, sm.c,
+                                        sm.tab)
+              : normalise_resample(N, lwf, valid, a.ess_frac, key, a.ws.status, sm.anc, sm.c,
+                                   sm.red, sm.tab);
     if (valid) {
       const int anc = sm.anc[tid];
-      a.out.log_weights[part] = rr.resampled ? 0.f : lwf;
+      a.out.log_weights[part] = rr.resampled ? 0.f : lwf.hi;
       a.out.ancestors[part] = anc;
       int32_t *dst = a.out.tokens_out + static_cast<size_t>(part) * (K + 1);
       if (tok_staged) {
@@ -554,19 +836,72 @@ __device__ void smc_tail(const StepArgs &a, int b, TailSmem &sm, int *dyn, bool 
 #pragma unroll 4
         for (int k = 0; k < K; ++k) dst[k] = srcp[k];
       }
-      dst[K] = sm.bonus[anc];
     }
     if (tid == 0) {
       a.out.ess[b] = rr.ess;
       a.out.resampled[b] = rr.resampled ? 1 : 0;
       s_res = rr.resampled ? 1 : 0;
     }
+  } else if (sc) {
+    kv_prepare(a.kv, b, N, *sc, sm.ks, 32, kThreads - 32);
   }
   __syncthreads();
-  if (a.use_kv) {
-    kv_remap_append(a.kv, b, N, sm.anc, s_res != 0, K + 1, a.ws, sm.ired, sm.tail, sm.nb, sc,
-                    true);
+  if (!small && sc) kv_prepare(a.kv, b, N, *sc, sm.ks, 0, kThreads);  // published by the remap's barrier
+  return s_res != 0;
+}
+
+// The prompt's tail with every particle's weight and bonus token known
+// (sm.bonus[i]: particle i's): prompt_weights, the bonus slots, and the KV
+// remap with append.
+__device__ void prompt_tail(const StepArgs &a, int b, TailSmem &sm, ff lwf, ResampleKey key,
+                            const KvScratch &sc) {
+  const int N = a.N, K = a.K;
+  const int tid = threadIdx.x;
+  const bool res = prompt_weights(a, b, sm, lwf, key, a.use_kv ? &sc : nullptr);
+  if (tid < N) {
+    a.out.tokens_out[static_cast<size_t>(b * N + tid) * (K + 1) + K] = sm.bonus[sm.anc[tid]];
   }
+  if (a.use_kv) kv_remap_append(a.kv, b, N, sm.anc, res, K + 1, a.ws, sm.ks, sc, true, true);
+}
+
+// Runs in tail_kernel, launched with programmatic dependent launch while the
+// row combine still runs.  The KV state, the incoming log-weights and the
+// drafted tokens were all written before this step's first kernel, so they
+// are read before waiting for the combine; only the row results are read
+// after.  The increment is summed in float-float from the rows' results (a
+// log-sum-exp row's result holds its value as a float pair, head and tail).
+__device__ void smc_tail(const StepArgs &a, int b, TailSmem &sm, int *dyn, bool kv_staged) {
+  const int N = a.N, K = a.K, rpp = 2 * K + 1;
+  const int tid = threadIdx.x;
+  const KvScratch sc = a.use_kv ? kv_scratch(a.kv, b, N, a.ws, dyn, kv_staged) : KvScratch{};
+  int top = 0;
+  const float lw0 = tail_prefetch(a, b, sm, sc, &top);
+  tail_prefetch_stack(a, b, top, sc);
+  const ResampleKey key = resample_key(a.seed, a.step, b, N);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the next step's rows
+  ff lwf{0.f, 0.f};
+  if (tid < N) {
+    const int part = b * N + tid;
+    const RowResult *r = a.ws.results + static_cast<size_t>(part) * rpp;
+    const float4 rb = __ldcg(reinterpret_cast<const float4 *>(r + K));
+    ff delta{0.f, 0.f};
+#pragma unroll 4
+    for (int k = 0; k < K; ++k) {
+      const float4 rp = __ldcg(reinterpret_cast<const float4 *>(r + k));
+      const float4 rq = __ldcg(reinterpret_cast<const float4 *>(r + K + 1 + k));
+      const ff lp = ff_sub_x(ff{rp.y, 0.f}, ff{rp.x, rp.z});  // log p of the drafted token
+      const ff lq = ff_sub_x(ff{rq.y, 0.f}, ff{rq.x, rq.z});  // log q of it
+      delta = ff_add_x(delta, ff_sub_x(ff_mul_fx(lp, a.alpha), lq));
+    }
+    if (a.alpha != 1.f) {
+      delta = ff_add_x(delta, ff_sub_x(ff{rb.z, 0.f}, ff_mul_fx(ff{rb.x, 0.f}, a.alpha)));
+    }
+    if (a.potential) delta = ff_add_x(delta, ff{__ldcg(a.potential + part), 0.f});
+    sm.bonus[tid] = __float_as_int(rb.w);
+    lwf = ff_add_x(ff{lw0, 0.f}, delta);
+  }
+  prompt_tail(a, b, sm, lwf, key, sc);
 }
 
 __device__ void sps_tail(const StepArgs &a, int b, TailSmem &sm) {
@@ -633,7 +968,7 @@ __global__ void __launch_bounds__(kThreads, 4) step_rows_kernel(const StepArgs a
   // ---- stream the chunk and reduce it -------------------------------------
   float x[EPT];
   load_chunk<T, VEC>(rowp + c0 * ESZ, n_valid, x);
-  if (is_bonus) stage_exp2_table(s_tab);
+  stage_exp2_table(s_tab);  // read by the bonus sums and by the row combine
 
   float m = kNegInf;
 #pragma unroll
@@ -707,13 +1042,13 @@ __global__ void __launch_bounds__(kThreads, 4) step_rows_kernel(const StepArgs a
         float g = __int_as_float(0x7fc00000);
         if (M == kNegInf) bits |= SMC_DEV_EMPTY_ROW;
         else if (!(sum < -kNegInf) || M == -kNegInf) bits |= SMC_DEV_NONFINITE;
-        const float lse = a.tscale * M + logf(sum);
+        const ff lse = row_lse(a.tscale, M, sum, s_tab);
         const int k = j < a.K ? j : j - a.K - 1;
         const int tok = a.tokens[static_cast<size_t>(part) * a.K + k];
         if (tok < 0 || tok >= a.V) bits |= SMC_DEV_BAD_TOKEN;
         else g = a.tscale * Tr::scalar(rowp, tok);
         if (bits) raise_status(a.ws.status, bits);
-        a.ws.results[row] = RowResult{lse, g, 0.f, -1};
+        a.ws.results[row] = RowResult{lse.hi, g, lse.lo, -1};  // lse as head and tail
       }
     }
   } else {
@@ -755,9 +1090,8 @@ __global__ void __launch_bounds__(kThreads, 4) step_rows_kernel(const StepArgs a
         s_target = rem;
         float lse, lse_alpha;
         if (ok) {
-          const double lt = log(ff_to_double(total));
-          lse_alpha = static_cast<float>(static_cast<double>(alpha) * M + lt);
-          lse = a.bonus_lse ? a.tscale * M + logf(fast) : lse_alpha;
+          lse_alpha = ff_add(two_prod(alpha, M), ff_log(total, s_tab)).hi;
+          lse = a.bonus_lse ? row_lse(a.tscale, M, fast, s_tab).hi : lse_alpha;
         } else {
           lse = lse_alpha = M == kNegInf ? kNegInf : __int_as_float(0x7fc00000);
           raise_status(a.ws.status, M == kNegInf ? SMC_DEV_EMPTY_ROW : SMC_DEV_NONFINITE);
@@ -811,7 +1145,9 @@ constexpr uint32_t kWaitLimit = 1u << 18;  // polls; each may suspend up to 20 u
 
 enum : int { kSlotFirst = 1, kSlotLast = 2, kSlotEnd = 4 };
 
-struct SlotMeta { int row, part, j, chunk, n, flags, pad0, pad1; };
+// item: the index, within its row, of the work item the chunk belongs to
+// (where the item's partials go); for bonus rows, the chunk itself.
+struct SlotMeta { int row, part, j, chunk, n, flags, item, pad; };
 
 // Logits per ring slot and per 16-byte vector of the streaming kernel.
 template <typename T> struct StreamGeom {
@@ -821,15 +1157,27 @@ template <typename T> struct StreamGeom {
   static constexpr int kWCH = kCH / kConsumerWarps;  // logits of one consumer warp's range
 };
 
+// Non-bonus rows are numbered rf = particle * 2K + (target positions 0..K-1,
+// then draft positions 0..K-1).  Rows rf < R1 are cut into ipr items of G
+// chunks; the last rows, rf >= R1, into single-chunk items, so that the work
+// queue ends in small pieces and the CTAs run out of work at nearly the same
+// time.
 struct StreamArgs {
   StepArgs a;
   int snch;           // ring-slot chunks per row: ceil(V / StreamGeom<T>::kCH)
   float wspan;        // 40 / balpha: logits further below a range's max weigh e^-40
-  int G;              // chunks per work item of a non-bonus row
-  int ipr;            // work items per non-bonus row
-  int n_fast_items;   // non-bonus rows * ipr
+  int G;              // chunks per work item of a non-bonus row rf < R1
+  int ipr;            // work items per non-bonus row rf < R1
+  int R1;             // non-bonus rows cut into G-chunk items
+  int n_items1;       // R1 * ipr: the queue's G-chunk items come first
+  int n_fast_items;   // all non-bonus items
   int n_bonus_items;  // bonus rows * snch (one chunk per item)
 };
+
+// Partial slots (work items) of non-bonus row rf.
+__host__ __device__ __forceinline__ int items_of_row(const StreamArgs &sa, int rf) {
+  return rf < sa.R1 ? sa.ipr : sa.snch;
+}
 
 constexpr size_t stream_dyn_smem() {
   return static_cast<size_t>(kStages) * kChunkBytes + 2 * kStages * sizeof(uint64_t) +
@@ -859,6 +1207,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rpp = 2 * a.K + 1;
 
+  // launched with programmatic dependent launch: nothing before this line
+  // touches global memory that an earlier kernel may still write
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -879,8 +1230,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
   if (warp == kConsumerWarps) {
     if (lane == 0) {
       const int rest = rpp - 1;  // non-bonus rows per particle
-      int row = 0, first = 0, chunk = 0, end = 0;
-      int n_fast = 0, n_bonus = 0;
+      int row = 0, first = 0, chunk = 0, end = 0, item = 0;
+      int fast_chunks = 0, n_bonus = 0;
       bool have = false, fast_done = sa.n_fast_items == 0, bonus_done = sa.n_bonus_items == 0;
       // each queue's next claim is issued one item ahead, so that the
       // atomic's round trip overlaps the copies of the current item
@@ -898,7 +1249,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
           have = false;
           if (fast_done && bonus_done) break;
           const bool take_bonus =
-              !bonus_done && (fast_done || n_bonus * 2 * a.K < n_fast * sa.G);
+              !bonus_done && (fast_done || n_bonus * 2 * a.K < fast_chunks);
           if (take_bonus) {
             const unsigned id = next_bonus;
             if (id >= static_cast<unsigned>(sa.n_bonus_items)) { bonus_done = true; continue; }
@@ -908,17 +1259,27 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
             row = part * rpp + a.K;
             first = static_cast<int>(id) - part * sa.snch;
             end = first + 1;
+            item = first;
           } else {
             const unsigned id = next_fast;
             if (id >= static_cast<unsigned>(sa.n_fast_items)) { fast_done = true; continue; }
             next_fast = atomicAdd(&a.ws.work_counter[0], 1u);
-            ++n_fast;
-            const int rf = static_cast<int>(id) / sa.ipr;
-            const int g = static_cast<int>(id) - rf * sa.ipr;
-            const int part = rf / rest, jj = rf - (rf / rest) * rest;
+            int rf;
+            if (static_cast<int>(id) < sa.n_items1) {
+              rf = static_cast<int>(id) / sa.ipr;
+              item = static_cast<int>(id) - rf * sa.ipr;
+              first = item * sa.G;
+              end = min(first + sa.G, sa.snch);
+            } else {
+              const int i2 = static_cast<int>(id) - sa.n_items1;
+              const int r2 = i2 / sa.snch;
+              rf = sa.R1 + r2;
+              item = first = i2 - r2 * sa.snch;
+              end = first + 1;
+            }
+            fast_chunks += end - first;
+            const int part = rf / rest, jj = rf - part * rest;
             row = part * rpp + (jj < a.K ? jj : jj + 1);
-            first = g * sa.G;
-            end = min(first + sa.G, sa.snch);
           }
           chunk = first;
           have = true;
@@ -927,6 +1288,13 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
           SlotMeta &mt = meta[slot];
           mt.row = -1; mt.part = 0; mt.j = 0; mt.chunk = 0; mt.n = 0; mt.flags = kSlotEnd;
           mbar_arrive(&full[slot]);
+          // the queues are drained, so the step's tail comes within a few
+          // microseconds: bring a prompt's KV state into L2 for it
+          if (a.mode == 0 && a.use_kv) {
+            for (int b = static_cast<int>(blockIdx.x); b < a.B; b += static_cast<int>(gridDim.x)) {
+              kv_prefetch_l2(a.kv, b, a.N);
+            }
+          }
           break;
         }
         const int64_t c0 = static_cast<int64_t>(chunk) * CH;
@@ -938,6 +1306,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
         mt.chunk = chunk;
         mt.n = n;
         mt.flags = (chunk == first ? kSlotFirst : 0) | (chunk + 1 == end ? kSlotLast : 0);
+        mt.item = item;
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(n * ESZ));
         bulk_copy_g2s(bufs + static_cast<size_t>(slot) * (kChunkBytes / 16),
@@ -1094,8 +1463,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) contrib += __shfl_xor_sync(0xffffffffu, contrib, o);
       if (lane == 0) {
-        const int g = is_bonus ? mt.chunk : mt.chunk / sa.G;
-        a.ws.item_part[(static_cast<size_t>(row) * sa.snch + g) * kConsumerWarps + warp] =
+        a.ws.item_part[(static_cast<size_t>(row) * sa.snch + mt.item) * kConsumerWarps + warp] =
             make_float2(M, contrib);
       }
     }
@@ -1182,40 +1550,265 @@ __device__ int block_select_fixed(const char *rowp, int64_t r0, int len, long lo
 }
 
 // ---------------------------------------------------------------------------
+// A row's log-sum-exp pieces from the streaming kernel's (item, warp)
+// partials, by an aligned group of G lanes: M the row's largest logit and S
+// the fp32 sum of exp(tscale (l - M)) (NaN marks a NaN or +inf logit).  Every
+// lane of the group gets both; all 32 lanes of the warp must call it (each
+// group on its own row, or with act false).  rf: the row's non-bonus number,
+// or -1 for a bonus row (one item a chunk).
+// ---------------------------------------------------------------------------
+template <int G>
+__device__ __forceinline__ void group_row_stats(const StreamArgs &sa, int row, int rf, bool act,
+                                                float *out_m, float *out_s) {
+  constexpr float kInf = -kNegInf;
+  const StepArgs &a = sa.a;
+  const int sub = threadIdx.x & (G - 1);
+  float lm = kNegInf, ls = 0.f;
+  if (act) {
+    const float2 *ip = a.ws.item_part + static_cast<size_t>(row) * sa.snch * kConsumerWarps;
+    const int n_ip = (rf < 0 ? sa.snch : items_of_row(sa, rf)) * kConsumerWarps;
+#pragma unroll 4
+    for (int c = sub; c < n_ip; c += G) {
+      const float2 pv = __ldcg(ip + c);
+      if (pv.x > lm) {
+        if (lm > kNegInf && pv.x < kInf) ls *= expf(a.tscale * (lm - pv.x));
+        else if (pv.x == kInf) ls = 0.f;
+        lm = pv.x;
+      }
+      if (pv.x > kNegInf && lm < kInf) ls += pv.y * expf(a.tscale * (pv.x - lm));
+      else if (pv.y != 0.f) ls += pv.y;  // NaN marker
+    }
+  }
+  float fM = lm;
+#pragma unroll
+  for (int o = G / 2; o > 0; o >>= 1) fM = fmaxf(fM, __shfl_xor_sync(0xffffffffu, fM, o));
+  float fS = (lm > kNegInf && fM < kInf) ? ls * expf(a.tscale * (lm - fM)) : ls;
+#pragma unroll
+  for (int o = G / 2; o > 0; o >>= 1) fS += __shfl_xor_sync(0xffffffffu, fS, o);
+  *out_m = fM;
+  *out_s = fS;
+}
+
+__device__ __forceinline__ void fast_row_stats(const StreamArgs &sa, int row, int rf,
+                                               float *out_m, float *out_s) {
+  group_row_stats<32>(sa, row, rf, true, out_m, out_s);
+}
+
+// Where a bonus row's inverse-CDF draw falls, found by bonus_select_warp: the
+// unit (-1 when the row has no mass), the remaining target inside it in the
+// unit's own fixed-point scale, the unit's reference logit, and the row's
+// log-sum-exps of tscale*l (lse) and of balpha*l (lse_alpha).
+struct BonusSel { long long target; int sel; float ref; ff lse, lse_alpha; };
+
+// Units whose largest logit was too large for the streaming kernel's clamp
+// (flag set) are summed here instead, in exact fixed point, by one warp.
+// Rare, so kept out of line: the draw's usual path stays short.
+template <typename T>
+__device__ __noinline__ void bonus_resum_flagged(const StreamArgs &sa, const char *rowp,
+                                                 int4 *bp, int n_units, const float2 *tab) {
+  using Tr = LogitTraits<T>;
+  constexpr int CH = StreamGeom<T>::kCH;
+  constexpr int WCH = StreamGeom<T>::kWCH;
+  const int lane = threadIdx.x & 31;
+  for (int q = 0; q < n_units; ++q) {
+    const int4 pv = bp[q];
+    if (pv.w == 0) continue;
+    const float ref = __int_as_float(pv.x);
+    const int c = q / kConsumerWarps, w = q - c * kConsumerWarps;
+    const int64_t r0 = static_cast<int64_t>(c) * CH + static_cast<int64_t>(w) * WCH;
+    const int len = static_cast<int>(min(static_cast<int64_t>(WCH), sa.a.V - r0));
+    long long sum = 0;
+    for (int i = lane; i < len; i += 32) {
+      sum += weight_fixed(Tr::scalar(rowp, r0 + i), ref, sa.a.balpha, tab);
+    }
+    const ff v = fixed_to_ff(warp_sum_ll(sum));
+    __syncwarp();
+    if (lane == 0) bp[q] = make_int4(pv.x, __float_as_int(v.hi), __float_as_int(v.lo), 0);
+    __syncwarp();
+  }
+  __threadfence_block();
+}
+
+// Unit selection for rows of more than 64 units, by one warp: masses
+// computed on demand in blocks of 32, the total first, then the scan
+// (warp_find_chunk).  Out of line, like the rare paths.
+__device__ __noinline__ void bonus_select_long(const StreamArgs &sa, const int4 *bp,
+                                               int n_units, float u, const float2 *tab, int *sel,
+                                               float *out_m, ff *out_total, ff *rem) {
+  constexpr float kInf = -kNegInf;
+  const int lane = threadIdx.x & 31;
+  const float alpha = sa.a.balpha;
+  float M = kNegInf;
+  for (int q = lane; q < n_units; q += 32) M = fmaxf(M, __int_as_float(bp[q].x));
+  M = warp_max(M);
+  const bool ok = M > kNegInf && M < kInf;
+  auto unit_mass = [&](int q, ff *val, ff *f) {
+    const int4 pv = bp[q];
+    const float ref = __int_as_float(pv.x);
+    if (ok && ref > kNegInf) {
+      *f = ff_norm(weight_term(ref, M, alpha, tab));  // exp(alpha (ref - M))
+      *val = ff_mul(ff{__int_as_float(pv.y), __int_as_float(pv.z)}, *f);
+    }
+  };
+  ff total{0.f, 0.f};
+  for (int q0 = 0; q0 < n_units; q0 += 32) {
+    ff val{0.f, 0.f}, f{1.f, 0.f};
+    if (q0 + lane < n_units) unit_mass(q0 + lane, &val, &f);
+    total = ff_add(total, warp_ff_sum(val));
+  }
+  *sel = ok ? warp_find_chunk(n_units, ff_mul_f(total, u), unit_mass, rem) : -1;
+  *out_m = M;
+  *out_total = total;
+}
+
+// Stage 1 of a bonus-row draw, by one full warp (no CTA barrier), from the
+// streaming kernel's unit sums: units are (chunk, warp) ranges of WCH
+// logits in vocabulary order, each with its largest logit as reference and
+// the float-float sum of its weights exp(balpha (l - ref)).  Which unit holds
+// u times the total comes from a float-float scan of the units' masses (two
+// units a lane for rows of at most 64 units, else bonus_select_long).  u is
+// the draw's uniform (bonus_uniform).  fM and fS are the row's fast
+// log-sum-exp pieces (used when alpha != 1).  With need_lse the row's
+// log-sum-exps go to out->lse and out->lse_alpha.  Lane 0 writes *out.
+__device__ __forceinline__ float bonus_uniform(const StepArgs &a, int part) {
+  return philox_uniform(a.seed, a.step, part, a.bonus_position, a.bonus_purpose);
+}
+
+template <typename T>
+__device__ void bonus_select_warp(const StreamArgs &sa, int part, const char *rowp, float u,
+                                  float fM, float fS, bool need_lse, const float2 *tab,
+                                  BonusSel *out) {
+  constexpr float kInf = -kNegInf;
+  constexpr unsigned kAll = 0xffffffffu;
+  const StepArgs &a = sa.a;
+  const int lane = threadIdx.x & 31;
+  const float alpha = a.balpha;
+  int4 *bp = a.ws.bonus_part + static_cast<size_t>(part) * sa.snch * kConsumerWarps;
+  const int n_units = sa.snch * kConsumerWarps;
+  int sel = -1;
+  float M = kNegInf, ref = 0.f;
+  ff total{0.f, 0.f}, rem{0.f, 0.f};
+  if (n_units <= 64) {
+    // units 2*lane and 2*lane + 1, adjacent in vocabulary order
+    const int q0 = 2 * lane, q1 = q0 + 1;
+    const int4 neg = make_int4(__float_as_int(kNegInf), 0, 0, 0);
+    int4 p0 = q0 < n_units ? bp[q0] : neg, p1 = q1 < n_units ? bp[q1] : neg;
+    if (__any_sync(kAll, (p0.w | p1.w) != 0)) {
+      bonus_resum_flagged<T>(sa, rowp, bp, n_units, tab);
+      p0 = q0 < n_units ? bp[q0] : neg;
+      p1 = q1 < n_units ? bp[q1] : neg;
+    }
+    const float r0 = __int_as_float(p0.x), r1 = __int_as_float(p1.x);
+    M = warp_max(fmaxf(r0, r1));
+    const bool ok = M > kNegInf && M < kInf;
+    ff v0{0.f, 0.f}, v1{0.f, 0.f}, f0{1.f, 0.f}, f1{1.f, 0.f};
+    if (ok && r0 > kNegInf) {
+      f0 = ff_norm(weight_term(r0, M, alpha, tab));  // exp(alpha (ref - M))
+      v0 = ff_mul(ff{__int_as_float(p0.y), __int_as_float(p0.z)}, f0);
+    }
+    if (ok && r1 > kNegInf) {
+      f1 = ff_norm(weight_term(r1, M, alpha, tab));
+      v1 = ff_mul(ff{__int_as_float(p1.y), __int_as_float(p1.z)}, f1);
+    }
+    const ff pair = ff_add(v0, v1);
+    const ff incl = warp_ff_incl_scan(pair);  // through unit q1
+    total = shfl_ff(incl, 31);
+    const ff excl = ff_sub(incl, pair);       // before unit q0
+    const ff c0 = ff_add(excl, v0);           // through unit q0
+    const ff target = ff_mul_f(total, u);
+    const bool pos0 = v0.hi > 0.f, pos1 = v1.hi > 0.f;
+    const bool hit0 = pos0 && ff_gt(c0, target), hit1 = pos1 && ff_gt(incl, target);
+    const unsigned hits = __ballot_sync(kAll, hit0 || hit1);
+    const unsigned any = __ballot_sync(kAll, pos0 || pos1);
+    if (ok && any) {
+      // the first unit whose prefix exceeds the target; past the total
+      // (rounding), the last unit with mass, taken whole
+      const int src = hits ? __ffs(hits) - 1 : 31 - __clz(any);
+      const bool first_half = hits ? hit0 : !pos1;
+      const bool h0 = __shfl_sync(kAll, first_half, src);
+      const ff ex = h0 ? excl : c0;  // the chosen unit's exclusive prefix
+      const ff val = h0 ? v0 : v1, f = h0 ? f0 : f1;
+      const ff l_rem = hits ? ff_div(ff_sub(target, ex), f) : ff_div(val, f);
+      rem = shfl_ff(l_rem, src);
+      ref = __shfl_sync(kAll, h0 ? r0 : r1, src);
+      sel = 2 * src + (h0 ? 0 : 1);
+    }
+  } else {
+    bool flagged = false;
+    for (int q = lane; q < n_units; q += 32) flagged |= bp[q].w != 0;
+    if (__any_sync(kAll, flagged)) bonus_resum_flagged<T>(sa, rowp, bp, n_units, tab);
+    bonus_select_long(sa, bp, n_units, u, tab, &sel, &M, &total, &rem);
+    if (sel >= 0) ref = __int_as_float(bp[sel].x);
+  }
+  if (lane == 0) {
+    const bool ok = M > kNegInf && M < kInf;
+    out->sel = sel;
+    out->target = ff_to_fixed(rem);
+    out->ref = ref;
+    if (!need_lse) {
+      out->lse = out->lse_alpha = ff{0.f, 0.f};
+      if (!ok) raise_status(a.ws.status, M == kNegInf ? SMC_DEV_EMPTY_ROW : SMC_DEV_NONFINITE);
+    } else if (ok) {
+      out->lse_alpha = ff_add(two_prod(alpha, M), ff_log(total, tab));
+      out->lse = a.bonus_lse ? row_lse(a.tscale, fM, fS, tab) : out->lse_alpha;
+    } else {
+      const float v = M == kNegInf ? kNegInf : __int_as_float(0x7fc00000);
+      out->lse = out->lse_alpha = ff{v, 0.f};
+      raise_status(a.ws.status, M == kNegInf ? SMC_DEV_EMPTY_ROW : SMC_DEV_NONFINITE);
+    }
+  }
+}
+
+// Stage 2, by the whole CTA: the element of the selected unit, by an exact
+// fixed-point rescan of its WCH logits (block_select_fixed); -1 when the row
+// has no mass.  All threads must call it, with `s` visible to every thread;
+// every thread gets the token.
+template <typename T>
+__device__ __forceinline__ int bonus_rescan(const StreamArgs &sa, const char *rowp,
+                                            const BonusSel &s, const float2 *tab,
+                                            long long *s_ll, int *s_i) {
+  constexpr int CH = StreamGeom<T>::kCH;
+  constexpr int WCH = StreamGeom<T>::kWCH;
+  const int sel = s.sel;
+  if (sel < 0) return -1;  // uniform across the CTA
+  const int c = sel / kConsumerWarps, w = sel - c * kConsumerWarps;
+  const int64_t r0 = static_cast<int64_t>(c) * CH + static_cast<int64_t>(w) * WCH;
+  const int len = static_cast<int>(max(static_cast<int64_t>(0),
+                                       min(static_cast<int64_t>(WCH), sa.a.V - r0)));
+  return block_select_fixed<T, WCH / kThreads>(rowp, r0, len, s.target, s.ref, sa.a.balpha, tab,
+                                               s_ll, s_i);
+}
+
+// ---------------------------------------------------------------------------
 // Row combine after the streaming kernel, launched with programmatic
 // dependent launch (it waits for the streaming kernel before reading its
 // partials).  The first n_fast_ctas CTAs take the log-sum-exp rows, one warp
 // per row: the row's log-sum-exp from its (item, warp) partials and the
-// drafted token's logit.  Each further CTA takes one bonus row: warp 0 finds
-// which (chunk, warp) unit holds u times the total from the units'
-// float-float sums, then the whole CTA rescans that unit in exact fixed
-// point to find the element (inverse CDF in vocabulary order).
+// drafted token's logit.  Each further CTA takes one bonus row: warp 0
+// finds the unit (bonus_select_warp), then the whole CTA the element
+// (bonus_rescan).  Used by the verify, the draft sampler and the nucleus
+// path; the plain SMC step takes particle_kernel and prompt_kernel instead.
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa, int n_fast_ctas) {
   using Tr = LogitTraits<T>;
-  constexpr int CH = StreamGeom<T>::kCH;
-  constexpr int WCH = StreamGeom<T>::kWCH;
   constexpr float kInf = -kNegInf;
   const StepArgs &a = sa.a;
   __shared__ float2 s_tab[64];
+  __shared__ BonusSel s_sel;
   __shared__ long long s_ll[kWarps];
   __shared__ int s_i[2 * kWarps];
-  __shared__ long long s_target;
-  __shared__ int s_sel;
-  __shared__ float s_ref;
-  __shared__ float s_red[2 * kWarps];
-  __shared__ float2 s_f2[kWarps];
   stage_exp2_table(s_tab);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int rpp = 2 * a.K + 1;
   const bool bonus_cta = static_cast<int>(blockIdx.x) >= n_fast_ctas;
-  int row, part, j;
+  int row, part, j, rfi = -1;
   bool live = true;
   if (!bonus_cta) {
     const long long n_fast_rows = static_cast<long long>(a.B) * a.N * 2 * a.K;
     const long long rf = static_cast<long long>(blockIdx.x) * kWarps + warp;
     live = rf < n_fast_rows;
+    rfi = live ? static_cast<int>(rf) : 0;
     part = live ? static_cast<int>(rf / (2 * a.K)) : 0;
     const int jj = live ? static_cast<int>(rf - static_cast<long long>(part) * 2 * a.K) : 0;
     j = jj < a.K ? jj : jj + 1;
@@ -1230,7 +1823,8 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa, i
   // the drafted token and its logit are inputs of the step: gathered while
   // the streaming kernel still runs
   int gtok = 0;
-  float gv = 0.f;
+  float gv = 0.f, u = 0.f;
+  if (is_bonus && warp == 0) u = bonus_uniform(a, part);
   if (!is_bonus && live && lane == 0) {
     gtok = a.tokens[static_cast<size_t>(part) * a.K + (j < a.K ? j : j - a.K - 1)];
     gv = (gtok < 0 || gtok >= a.V) ? __int_as_float(0x7fc00000) : a.tscale * Tr::scalar(rowp, gtok);
@@ -1240,170 +1834,204 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa, i
   __syncthreads();
   if (!live) return;
 
-  // fast log-sum-exp pieces of the row (every warp of a bonus CTA computes
-  // them; only warp 0's are used)
+  // fast log-sum-exp pieces of the row (for a bonus row, warp 0's are used)
   float fM = kNegInf, fS = 0.f;
-  if (fast) {
-    const float2 *ip = a.ws.item_part + static_cast<size_t>(row) * sa.snch * kConsumerWarps;
-    const int n_ip = (is_bonus ? sa.snch : sa.ipr) * kConsumerWarps;
-    float lm = kNegInf, ls = 0.f;
-#pragma unroll 4
-    for (int c = lane; c < n_ip; c += 32) {
-      const float2 pv = ip[c];
-      if (pv.x > lm) {
-        if (lm > kNegInf && pv.x < kInf) ls *= expf(a.tscale * (lm - pv.x));
-        else if (pv.x == kInf) ls = 0.f;
-        lm = pv.x;
-      }
-      if (pv.x > kNegInf && lm < kInf) ls += pv.y * expf(a.tscale * (pv.x - lm));
-      else if (pv.y != 0.f) ls += pv.y;  // NaN marker
-    }
-    fM = warp_max(lm);
-    fS = (lm > kNegInf && fM < kInf) ? ls * expf(a.tscale * (lm - fM)) : ls;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) fS += __shfl_xor_sync(0xffffffffu, fS, o);
-  }
+  if (fast && (!is_bonus || warp == 0)) fast_row_stats(sa, row, is_bonus ? -1 : rfi, &fM, &fS);
   if (!is_bonus) {
     if (lane == 0) {
       unsigned bits = 0;
       if (fM == kNegInf) bits |= SMC_DEV_EMPTY_ROW;
       else if (!(fS < kInf) || fM == kInf) bits |= SMC_DEV_NONFINITE;
-      const float lse = a.tscale * fM + logf(fS);
+      const ff lse = row_lse(a.tscale, fM, fS, s_tab);
       if (gtok < 0 || gtok >= a.V) bits |= SMC_DEV_BAD_TOKEN;
       if (bits) raise_status(a.ws.status, bits);
-      a.ws.results[row] = RowResult{lse, gv, 0.f, -1};
+      a.ws.results[row] = RowResult{lse.hi, gv, lse.lo, -1};  // lse as head and tail
     }
     return;
   }
-
-  // ---- bonus row: units are (chunk, warp) ranges of WCH logits in vocabulary
-  // order, each with its max as reference and the float-float sum of its
-  // weights relative to it
-  const float alpha = a.balpha;
-  int4 *bp = a.ws.bonus_part + static_cast<size_t>(part) * sa.snch * kConsumerWarps;
-  const int n_units = sa.snch * kConsumerWarps;
-  // rows of up to kThreads units: thread q holds unit q from here on
-  int4 pv_own = threadIdx.x < n_units ? bp[threadIdx.x]
-                                      : make_int4(__float_as_int(kNegInf), 0, 0, 0);
-  bool flagged = pv_own.w != 0;
-  for (int q = kThreads + threadIdx.x; q < n_units; q += kThreads) flagged |= bp[q].w != 0;
-  if (__syncthreads_or(flagged)) {
-    // a unit whose max was too large for the streaming kernel's clamp (flag
-    // set) is summed here instead, in exact fixed point (rare)
-    if (warp == 0) {
-      for (int q = 0; q < n_units; ++q) {
-        const int4 pv = bp[q];
-        if (pv.w == 0) continue;
-        const float ref = __int_as_float(pv.x);
-        const int c = q / kConsumerWarps, w = q - c * kConsumerWarps;
-        const int64_t r0 = static_cast<int64_t>(c) * CH + static_cast<int64_t>(w) * WCH;
-        const int len = static_cast<int>(min(static_cast<int64_t>(WCH), a.V - r0));
-        long long sum = 0;
-        for (int i = lane; i < len; i += 32) sum += weight_fixed(Tr::scalar(rowp, r0 + i), ref, alpha, s_tab);
-        const ff v = fixed_to_ff(warp_sum_ll(sum));
-        __syncwarp();
-        if (lane == 0) bp[q] = make_int4(pv.x, __float_as_int(v.hi), __float_as_int(v.lo), 0);
-        __syncwarp();
-      }
-    }
-    __syncthreads();
-    if (threadIdx.x < n_units) pv_own = bp[threadIdx.x];
+  if (warp == 0) bonus_select_warp<T>(sa, part, rowp, u, fM, fS, true, s_tab, &s_sel);
+  __syncthreads();
+  const int tok = bonus_rescan<T>(sa, rowp, s_sel, s_tab, s_ll, s_i);
+  if (threadIdx.x == 0) {
+    a.ws.results[row] = RowResult{s_sel.lse.hi, 0.f, s_sel.lse_alpha.hi, tok};
+    if (a.mode == 2) a.out.tokens_out[part] = tok;
   }
-  const float u = philox_uniform(a.seed, a.step, part, a.bonus_position, a.bonus_purpose);
-  if (n_units <= kThreads) {
-    // one unit per thread: its mass relative to the row's largest reference
-    // M, a CTA-wide inclusive prefix, and the first unit whose prefix exceeds
-    // u times the total
-    const int q = threadIdx.x;
-    const int4 pv = pv_own;
-    const float ref = __int_as_float(pv.x);
-    const float M = block_max(ref, s_red);
-    const bool ok = M > kNegInf && M < kInf;
-    ff val{0.f, 0.f}, f{1.f, 0.f};
-    if (ok && ref > kNegInf) {
-      f = ff_norm(weight_term(ref, M, alpha, s_tab));  // exp(alpha (ref - M))
-      val = ff_mul(ff{__int_as_float(pv.y), __int_as_float(pv.z)}, f);
-    }
-    ff total;
-    const ff incl = block_ff_scan(val, s_f2, &total);
-    const ff target = ff_mul_f(total, u);
-    const bool pos = val.hi > 0.f;
-    const bool hit = pos && ff_gt(incl, target);
-    const int first = block_min_i(hit ? q : 0x7fffffff, s_i);
-    const int last = -block_min_i(pos ? -q : 1, s_i);  // largest positive unit, or -1
-    const int sel = !ok ? -1 : (first != 0x7fffffff ? first : last);
-    if (q == sel) {
-      // the remaining target in the unit's own units; past the total
-      // (rounding), the unit's whole mass
-      const ff rem = first != 0x7fffffff ? ff_div(ff_sub(target, ff_sub(incl, val)), f)
-                                         : ff_div(val, f);
-      s_target = ff_to_fixed(rem);
-      s_ref = ref;
-    }
-    if (q == 0) {
-      s_sel = sel;
-      float lse, lse_alpha;
-      if (ok) {
-        lse_alpha = alpha * M + (logf(total.hi) + total.lo / total.hi);
-        lse = a.bonus_lse ? a.tscale * fM + logf(fS) : lse_alpha;
-      } else {
-        lse = lse_alpha = M == kNegInf ? kNegInf : __int_as_float(0x7fc00000);
-        raise_status(a.ws.status, M == kNegInf ? SMC_DEV_EMPTY_ROW : SMC_DEV_NONFINITE);
+}
+
+// ---------------------------------------------------------------------------
+// Epilogue of a plain SMC step on the streaming path: particle_kernel (one CTA
+// per particle) and prompt_kernel (one CTA per prompt) run side by side.
+//
+// particle_kernel, launched with programmatic dependent launch after the
+// streaming kernel, waits for it, then: warps 1.. combine the particle's 2K
+// log-sum-exp rows from their (item, warp) partials and sum its weight
+// increment in float-float, while warp 0 locates the bonus draw
+// (bonus_select_warp); then the whole CTA rescans the unit (bonus_rescan).
+// The particle's new log-weight (incoming plus increment, as a float pair) goes
+// to its first row result and its bonus token to its bonus row's result, each
+// followed by a release increment of the prompt's counter (weights_done, then
+// bonus_done).  With alpha != 1 the increment also takes the bonus row's
+// log-sum-exps, so the weight is published after warp 0's search.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kCountWaitLimit = 1u << 20;  // polls of about 1 us: about a second
+
+__device__ __forceinline__ void publish_weight(const StepArgs &a, int part, const float2 *s_d,
+                                               ff extra, float lw0) {
+  ff d = extra;
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) d = ff_add_x(d, ff{s_d[w].x, s_d[w].y});
+  const ff lwf = ff_add_x(ff{lw0, 0.f}, d);
+  RowResult *r = a.ws.results + static_cast<size_t>(part) * (2 * a.K + 1);
+  *reinterpret_cast<float2 *>(r) = make_float2(lwf.hi, lwf.lo);
+  add_release_gpu(a.ws.weights_done + part / a.N, 1u);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) particle_kernel(const StreamArgs sa) {
+  using Tr = LogitTraits<T>;
+  constexpr float kInf = -kNegInf;
+  constexpr unsigned kAll = 0xffffffffu;
+  const StepArgs &a = sa.a;
+  __shared__ float2 s_tab[64];
+  __shared__ BonusSel s_sel;
+  __shared__ long long s_ll[kWarps];
+  __shared__ int s_i[2 * kWarps];
+  __shared__ float2 s_d[kWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int part = blockIdx.x;
+  const int K = a.K, rpp = 2 * K + 1, nr = 2 * K;
+  const char *bonus_rowp = row_base<T>(a, part * rpp + K);
+  // the prompt kernel may launch once every particle CTA has started
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  stage_exp2_table(s_tab);
+  // the log-sum-exp rows go to groups of kG lanes of warps 1..: group
+  // g = (w - 1) 32/kG + lane/kG takes rows g, g + n_grp, ...
+  constexpr int kG = 8, kGpw = 32 / kG;
+  constexpr int n_grp = (kWarps - 1) * kGpw;
+  const int grp = (warp - 1) * kGpw + lane / kG, sub = lane & (kG - 1);
+  // inputs of the step, read while the streaming kernel still runs: the
+  // drafted tokens and their logits (lane q kG + r of warp w >= 1 holds row
+  // (w - 1) kGpw + q + n_grp r), the incoming log-weight and the potential
+  const int jj_l = (warp - 1) * kGpw + lane / kG + n_grp * sub;
+  int gtok = 0;
+  float gv = 0.f;
+  if (warp > 0 && jj_l < nr) {
+    const int j = jj_l < K ? jj_l : jj_l + 1;
+    gtok = a.tokens[static_cast<size_t>(part) * K + (jj_l < K ? jj_l : jj_l - K)];
+    gv = (gtok < 0 || gtok >= a.V) ? __int_as_float(0x7fc00000)
+                                   : a.tscale * Tr::scalar(row_base<T>(a, part * rpp + j), gtok);
+  }
+  const int publisher = a.bonus_lse ? 0 : 32;
+  const float u = warp == 0 ? bonus_uniform(a, part) : 0.f;
+  float lw0 = 0.f, pot = 0.f;
+  if (static_cast<int>(threadIdx.x) == publisher) {
+    lw0 = __ldcg(a.out.log_weights + part);
+    if (a.potential) pot = __ldcg(a.potential + part);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  if (warp == 0) {
+    float fM = kNegInf, fS = 0.f;
+    if (a.bonus_lse) fast_row_stats(sa, part * rpp + K, -1, &fM, &fS);
+    bonus_select_warp<T>(sa, part, bonus_rowp, u, fM, fS, a.bonus_lse, s_tab, &s_sel);
+  } else {
+    ff d{0.f, 0.f};
+    unsigned bits = 0;
+#pragma unroll 1
+    for (int r = 0; (warp - 1) * kGpw + n_grp * r < nr; ++r) {  // uniform across the warp
+      const int jj = grp + n_grp * r;
+      const bool act = jj < nr;
+      const int j = jj < K ? jj : jj + 1;
+      float fM, fS;
+      group_row_stats<kG>(sa, part * rpp + j, part * nr + jj, act, &fM, &fS);
+      const int src = (lane & ~(kG - 1)) + r;
+      const int t = __shfl_sync(kAll, gtok, src);
+      const float g = __shfl_sync(kAll, gv, src);
+      if (act && sub == 0) {
+        if (fM == kNegInf) bits |= SMC_DEV_EMPTY_ROW;
+        else if (!(fS < kInf) || fM == kInf) bits |= SMC_DEV_NONFINITE;
+        if (t < 0 || t >= a.V) bits |= SMC_DEV_BAD_TOKEN;
+        const ff l = ff_sub_x(ff{g, 0.f}, row_lse(a.tscale, fM, fS, s_tab));  // log p or log q
+        d = jj < K ? ff_add_x(d, ff_mul_fx(l, a.alpha)) : ff_sub_x(d, l);
       }
-      a.ws.results[row] = RowResult{lse, 0.f, lse_alpha, -1};
     }
-  } else if (warp == 0) {
-    // longer rows: warp 0 computes unit masses on demand
-    float M = kNegInf;
-    for (int q = lane; q < n_units; q += 32) M = fmaxf(M, __int_as_float(bp[q].x));
-    M = warp_max(M);
-    const bool ok = M > kNegInf && M < kInf;
-    auto unit_mass = [&](int q, ff *val, ff *f) {
-      const int4 pv = bp[q];
-      const float ref = __int_as_float(pv.x);
-      if (ok && ref > kNegInf) {
-        *f = ff_norm(weight_term(ref, M, alpha, s_tab));  // exp(alpha (ref - M))
-        *val = ff_mul(ff{__int_as_float(pv.y), __int_as_float(pv.z)}, *f);
-      }
-    };
-    ff total{0.f, 0.f};
-    for (int q0 = 0; q0 < n_units; q0 += 32) {
-      ff val{0.f, 0.f}, f{1.f, 0.f};
-      if (q0 + lane < n_units) unit_mass(q0 + lane, &val, &f);
-      total = ff_add(total, warp_ff_sum(val));
+    // the warp's groups, summed into lane 0 (other lanes hold zeros)
+#pragma unroll
+    for (int o = kG; o < 32; o <<= 1) {
+      d = ff_add_x(d, ff{__shfl_xor_sync(kAll, d.hi, o), __shfl_xor_sync(kAll, d.lo, o)});
     }
-    ff rem{0.f, 0.f};
-    const int sel = ok ? warp_find_chunk(n_units, ff_mul_f(total, u), unit_mass, &rem) : -1;
-    if (lane == 0) {
-      s_sel = sel;
-      s_target = ff_to_fixed(rem);
-      s_ref = sel >= 0 ? __int_as_float(bp[sel].x) : 0.f;
-      float lse, lse_alpha;
-      if (ok) {
-        lse_alpha = alpha * M + (logf(total.hi) + total.lo / total.hi);
-        lse = a.bonus_lse ? a.tscale * fM + logf(fS) : lse_alpha;
-      } else {
-        lse = lse_alpha = M == kNegInf ? kNegInf : __int_as_float(0x7fc00000);
-        raise_status(a.ws.status, M == kNegInf ? SMC_DEV_EMPTY_ROW : SMC_DEV_NONFINITE);
-      }
-      a.ws.results[row] = RowResult{lse, 0.f, lse_alpha, -1};
+    if (bits) raise_status(a.ws.status, bits);
+    if (lane == 0) s_d[warp] = make_float2(d.hi, d.lo);
+    if (!a.bonus_lse) {
+      named_bar_sync(1, (kWarps - 1) * 32);
+      if (static_cast<int>(threadIdx.x) == publisher) publish_weight(a, part, s_d, ff{pot, 0.f}, lw0);
     }
   }
   __syncthreads();
-  const int sel = s_sel;
-  if (sel < 0) {  // uniform across the CTA
-    if (a.mode == 2 && threadIdx.x == 0) a.out.tokens_out[part] = -1;
+  if (a.bonus_lse && static_cast<int>(threadIdx.x) == publisher) {
+    // alpha != 1: the bonus row's log-sum-exps enter the increment
+    const ff extra = ff_add_x(ff_sub_x(s_sel.lse_alpha, ff_mul_fx(s_sel.lse, a.alpha)),
+                              ff{pot, 0.f});
+    publish_weight(a, part, s_d, extra, lw0);
+  }
+  const int tok = bonus_rescan<T>(sa, bonus_rowp, s_sel, s_tab, s_ll, s_i);
+  if (threadIdx.x == 0) {
+    a.ws.results[static_cast<size_t>(part) * rpp + K].tok = tok;
+    add_release_gpu(a.ws.bonus_done + part / a.N, 1u);
+  }
+}
+
+// prompt_kernel, launched with programmatic dependent launch after
+// particle_kernel, never waits for that grid to finish: it stages the KV
+// state and the drafted tokens, waits (bounded) until all N particles of its
+// prompt have published their weights, normalises, resamples and remaps the
+// KV state, and only then waits for their bonus tokens to emit them.  It
+// resets its prompt's counters for the next step.  A wait that gives up
+// raises SMC_DEV_TIMEOUT and leaves the prompt's outputs unwritten.
+__global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const StepArgs a, int kv_staged) {
+  __shared__ TailSmem sm;
+  __shared__ int s_ok;
+  extern __shared__ int dyn_i[];
+  const int b = blockIdx.x, N = a.N, K = a.K, rpp = 2 * K + 1;
+  const int tid = threadIdx.x;
+  const KvScratch sc = a.use_kv ? kv_scratch(a.kv, b, N, a.ws, dyn_i, kv_staged != 0) : KvScratch{};
+  int top = 0;
+  tail_prefetch(a, b, sm, sc, &top);
+  tail_prefetch_stack(a, b, top, sc);
+  const ResampleKey key = resample_key(a.seed, a.step, b, N);
+  if (tid == 0) s_ok = wait_count(a.ws.weights_done + b, static_cast<unsigned>(N), kCountWaitLimit);
+  __syncthreads();
+  if (!s_ok) {
+    if (tid == 0) raise_status(a.ws.status, SMC_DEV_TIMEOUT);
+    cp_async_wait_all();
     return;
   }
-  const int c = sel / kConsumerWarps, w = sel - c * kConsumerWarps;
-  const int64_t r0 = static_cast<int64_t>(c) * CH + static_cast<int64_t>(w) * WCH;
-  const int len = static_cast<int>(max(static_cast<int64_t>(0),
-                                       min(static_cast<int64_t>(WCH), a.V - r0)));
-  const int tok = block_select_fixed<T, WCH / kThreads>(rowp, r0, len, s_target, s_ref, alpha,
-                                                         s_tab, s_ll, s_i);
-  if (threadIdx.x == 0) {
-    a.ws.results[row].tok = tok;
-    if (a.mode == 2) a.out.tokens_out[part] = tok;
+  const RowResult *res = a.ws.results + static_cast<size_t>(b) * N * rpp;
+  ff lwf{0.f, 0.f};
+  if (tid < N) {
+    const float2 v = __ldcg(reinterpret_cast<const float2 *>(res + static_cast<size_t>(tid) * rpp));
+    lwf = ff{v.x, v.y};
+  }
+  const bool resampled = prompt_weights(a, b, sm, lwf, key, a.use_kv ? &sc : nullptr);
+  if (a.use_kv) kv_remap_append(a.kv, b, N, sm.anc, resampled, K + 1, a.ws, sm.ks, sc, true, true);
+  if (tid == 0) s_ok = wait_count(a.ws.bonus_done + b, static_cast<unsigned>(N), kCountWaitLimit);
+  __syncthreads();
+  // the next step's streaming kernel may launch now (it waits for this grid
+  // to end).  Not earlier: its CTAs, made resident while particle CTAs still
+  // occupy the SMs, were measured to stream about 10 % slower.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (!s_ok) {
+    if (tid == 0) raise_status(a.ws.status, SMC_DEV_TIMEOUT);
+    return;
+  }
+  if (tid < N) {
+    const int anc = sm.anc[tid];
+    a.out.tokens_out[static_cast<size_t>(b * N + tid) * (K + 1) + K] =
+        __ldcg(&res[static_cast<size_t>(anc) * rpp + K].tok);
+  }
+  if (tid == 0) {
+    a.ws.weights_done[b] = 0u;
+    a.ws.bonus_done[b] = 0u;
   }
 }
 
@@ -1435,8 +2063,11 @@ resample_kernel(int N, float ess_frac, uint64_t seed, uint32_t step, float *log_
   const int tid = threadIdx.x;
   const bool valid = tid < N;
   const float lwf = valid ? log_weights[static_cast<size_t>(b) * N + tid] : 0.f;
-  const ResampleResult rr = normalise_resample(b, N, lwf, valid, ess_frac, seed, step, status,
-                                               sm.anc, sm.c, sm.red);
+  stage_exp2_table(sm.tab);
+  __syncthreads();
+  const ResampleResult rr = normalise_resample(N, ff{lwf, 0.f}, valid, ess_frac,
+                                               resample_key(seed, step, b, N), status, sm.anc,
+                                               sm.c, sm.red, sm.tab);
   if (valid) {
     log_weights[static_cast<size_t>(b) * N + tid] = rr.resampled ? 0.f : lwf;
     ancestors[static_cast<size_t>(b) * N + tid] = sm.anc[tid];
@@ -1464,8 +2095,8 @@ kv_remap_kernel(int N, KvArgs kv, const int32_t *ancestors, const int32_t *resam
     sm.anc[tid] = a;
   }
   __syncthreads();
-  kv_remap_append(kv, b, N, sm.anc, res, n_append, ws, sm.ired, sm.tail, sm.nb,
-                  kv_scratch(kv, b, N, ws, dyn_i, kv_staged != 0), false);
+  kv_remap_append(kv, b, N, sm.anc, res, n_append, ws, sm.ks,
+                  kv_scratch(kv, b, N, ws, dyn_i, kv_staged != 0), false, false);
 }
 
 // ---------------------------------------------------------------------------
@@ -1507,8 +2138,96 @@ void set_row_timing_events(cudaEvent_t begin, cudaEvent_t end) {
   g_rows_end = end;
 }
 
+// Dynamic shared memory for a staged KV remap, or 0 when it does not fit.
+static size_t kv_stage_bytes(int N, const KvArgs *kv) {
+  if (!kv) return 0;
+  const size_t bytes = kv_stage_words(N, kv->T, kv->P) * sizeof(int);
+  return bytes <= kKvStageMaxBytes ? bytes : 0;
+}
+
+// The kernels that stage a KV remap in dynamic shared memory take up to
+// kKvStageMaxBytes of it on top of their static shared memory; they are
+// opted into that maximum once per device, so that every staged size fits
+// (and concurrent launches never lower the limit under one another).
+//
+// The epilogue kernels also ask for the largest shared-memory carveout.  An
+// SM changes its L1/shared split only when it is idle, so a small-footprint
+// kernel given a small carveout would keep the next kernel's large-footprint
+// CTAs (the prompt tails, the next step's streaming CTAs) off every SM it
+// occupies until it drains.
+static cudaError_t configure_kernels() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<bool> done[kMaxDev];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < kMaxDev && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  const int bytes = static_cast<int>(kKvStageMaxBytes);
+  const cudaFuncAttribute attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  if ((e = cudaFuncSetAttribute(tail_kernel, attr, bytes)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(kv_remap_kernel, attr, bytes)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(prompt_kernel, attr, bytes)) != cudaSuccess) return e;
+  const cudaFuncAttribute co = cudaFuncAttributePreferredSharedMemoryCarveout;
+  const int full = cudaSharedmemCarveoutMaxShared;
+  const void *epilogue[] = {
+      reinterpret_cast<const void *>(tail_kernel),
+      reinterpret_cast<const void *>(prompt_kernel),
+      reinterpret_cast<const void *>(particle_kernel<float>),
+      reinterpret_cast<const void *>(particle_kernel<bf16_tag>),
+      reinterpret_cast<const void *>(finish_kernel<float>),
+      reinterpret_cast<const void *>(finish_kernel<bf16_tag>),
+      reinterpret_cast<const void *>(row_stream_kernel<float>),
+      reinterpret_cast<const void *>(row_stream_kernel<bf16_tag>)};
+  for (const void *f : epilogue) {
+    if ((e = cudaFuncSetAttribute(f, co, full)) != cudaSuccess) return e;
+  }
+  if (dev < kMaxDev) done[dev].store(true, std::memory_order_release);
+  return cudaSuccess;
+}
+
+// A launch with programmatic stream serialisation: the kernel may start
+// before the one ahead of it in the stream has finished, and waits
+// (griddepcontrol.wait, or on workspace counters) before reading its results.
+// Used in place: cfg points at attr.
+struct PdlLaunch {
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  PdlLaunch(unsigned grid, unsigned block, size_t dyn, cudaStream_t stream) {
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = dyn;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  PdlLaunch(const PdlLaunch &) = delete;
+};
+
+// The plain SMC step's epilogue: particle_kernel, then prompt_kernel, which
+// runs alongside it.
 template <typename T>
-static cudaError_t launch_stream(const StepArgs &a, long long rows, cudaStream_t stream) {
+static cudaError_t launch_particle_epilogue(const StreamArgs &sa, cudaStream_t stream) {
+  const StepArgs &a = sa.a;
+  const size_t dyn = a.use_kv ? kv_stage_bytes(a.N, &a.kv) : 0;
+  cudaError_t e = configure_kernels();
+  if (e != cudaSuccess) return e;
+  {
+    PdlLaunch l(static_cast<unsigned>(a.B * a.N), kThreads, 0, stream);
+    e = cudaLaunchKernelEx(&l.cfg, particle_kernel<T>, sa);
+    if (e != cudaSuccess) return e;
+  }
+  PdlLaunch l(static_cast<unsigned>(a.B), kThreads, dyn, stream);
+  return cudaLaunchKernelEx(&l.cfg, prompt_kernel, a, dyn > 0 ? 1 : 0);
+}
+
+// The streaming kernel, then either the plain step's epilogue (when
+// `fuse_tail` is set; *tail_done is then set) or the row combine
+// (finish_kernel), after which the caller launches the tail.
+template <typename T>
+static cudaError_t launch_stream(const StepArgs &a, long long rows, cudaStream_t stream,
+                                 bool fuse_tail, bool *tail_done) {
   int sms = 0, per_sm = 0;
   cudaError_t e = stream_geometry<T>(&sms, &per_sm);
   if (e != cudaSuccess) return e;
@@ -1526,68 +2245,64 @@ static cudaError_t launch_stream(const StepArgs &a, long long rows, cudaStream_t
   sa.ipr = (sa.snch + g0 - 1) / g0;
   sa.G = (sa.snch + sa.ipr - 1) / sa.ipr;
   const long long parts = rows / (2 * a.K + 1);
-  sa.n_fast_items = static_cast<int>(parts * 2 * a.K * sa.ipr);
+  const long long fast_rows = parts * 2 * a.K;
+  // the queue's last non-bonus rows go in single-chunk items: about five
+  // halves of a chunk per resident CTA at the end
+  long long r2 = sa.G > 1 ? (5 * grid_max / 2 + sa.snch - 1) / sa.snch : 0;
+  if (r2 > fast_rows) r2 = fast_rows;
+  sa.R1 = static_cast<int>(fast_rows - r2);
+  sa.n_items1 = sa.R1 * sa.ipr;
+  sa.n_fast_items = static_cast<int>(sa.n_items1 + r2 * sa.snch);
   sa.n_bonus_items = static_cast<int>(parts * sa.snch);
   const long long n_items = static_cast<long long>(sa.n_fast_items) + sa.n_bonus_items;
   const long long grid = grid_max < n_items ? grid_max : n_items;
   if (g_rows_begin && (e = cudaEventRecord(g_rows_begin, stream)) != cudaSuccess) return e;
-  row_stream_kernel<T><<<static_cast<unsigned>(grid), kStreamThreads, stream_dyn_smem(), stream>>>(sa);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  {
+    // programmatic dependent launch: when the kernel before it in the stream
+    // lets its dependents start early (the step's own epilogue or tail does),
+    // the CTAs become resident while it runs and wait at their first
+    // instruction for its completion, so no launch gap separates two steps
+    PdlLaunch l(static_cast<unsigned>(grid), kStreamThreads, stream_dyn_smem(), stream);
+    e = cudaLaunchKernelEx(&l.cfg, row_stream_kernel<T>, sa);
+    if (e != cudaSuccess) return e;
+  }
   if (g_rows_end && (e = cudaEventRecord(g_rows_end, stream)) != cudaSuccess) return e;
+  if (fuse_tail) {
+    *tail_done = true;
+    return launch_particle_epilogue<T>(sa, stream);
+  }
   // log-sum-exp rows: one warp each; bonus rows: one CTA each
-  const long long fast_rows = parts * 2 * a.K;
   const int n_fast_ctas = static_cast<int>((fast_rows + kWarps - 1) / kWarps);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(n_fast_ctas + parts));
-  cfg.blockDim = dim3(kThreads);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, finish_kernel<T>, sa, n_fast_ctas);
-}
-
-// The per-prompt tail, launched with programmatic dependent launch so that it
-// can be scheduled while the row kernel drains.
-// Dynamic shared memory for a staged KV remap, or 0 when it does not fit.
-static size_t kv_stage_bytes(int N, const KvArgs *kv) {
-  if (!kv) return 0;
-  const size_t bytes = kv_stage_words(N, kv->T, kv->P) * sizeof(int);
-  return bytes <= kKvStageMaxBytes ? bytes : 0;
+  PdlLaunch l(static_cast<unsigned>(n_fast_ctas + parts), kThreads, 0, stream);
+  return cudaLaunchKernelEx(&l.cfg, finish_kernel<T>, sa, n_fast_ctas);
 }
 
 
 static cudaError_t launch_tail(const StepArgs &a, cudaStream_t stream) {
   const size_t dyn = a.use_kv ? kv_stage_bytes(a.N, &a.kv) : 0;
-  cudaError_t e = allow_dyn_smem(tail_kernel, dyn);
+  cudaError_t e = configure_kernels();
   if (e != cudaSuccess) return e;
-  const int staged = dyn > 0 ? 1 : 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.B);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = dyn;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tail_kernel, a, staged);
+  PdlLaunch l(static_cast<unsigned>(a.B), kThreads, dyn, stream);
+  return cudaLaunchKernelEx(&l.cfg, tail_kernel, a, dyn > 0 ? 1 : 0);
 }
 
-// The row pass (streaming or per-chunk kernel, then the row combine).
-static cudaError_t launch_rows(const StepArgs &a, int dtype, long long rows, cudaStream_t stream) {
+// The row pass (streaming or per-chunk kernel, then the row combine).  With
+// `fuse_tail`, the streaming path may also run the per-prompt tail
+// (*tail_done is then set).
+static cudaError_t launch_rows(const StepArgs &a, int dtype, long long rows, cudaStream_t stream,
+                               bool fuse_tail = false, bool *tail_done = nullptr) {
+  bool dummy = false;
+  if (!tail_done) tail_done = &dummy;
+  *tail_done = false;
+  cudaError_t e = configure_kernels();
+  if (e != cudaSuccess) return e;
   const int esz = dtype == SMC_BF16 ? 2 : 4;
   // bulk copies need 16-byte aligned rows and chunk sizes: aligned bases and V*esz % 16 == 0
   const bool vec = aligned16(a.target) && aligned16(a.draft) &&
                    (static_cast<long long>(a.V) * esz) % 16 == 0;
-  cudaError_t e;
   if (vec) {
-    e = dtype == SMC_BF16 ? launch_stream<bf16_tag>(a, rows, stream)
-                          : launch_stream<float>(a, rows, stream);
+    e = dtype == SMC_BF16 ? launch_stream<bf16_tag>(a, rows, stream, fuse_tail, tail_done)
+                          : launch_stream<float>(a, rows, stream, fuse_tail, tail_done);
   } else {
     const long long grid = rows * a.nch;
     dim3 g(static_cast<unsigned>(grid)), blk(kThreads);
@@ -1627,8 +2342,10 @@ cudaError_t launch_step_rows(const Shape &s, int mode, const void *target, const
   a.use_kv = kv != nullptr;
   if (kv) a.kv = *kv;
   const long long rows = static_cast<long long>(s.B) * s.N * (2 * s.K + 1);
-  cudaError_t e = launch_rows(a, s.dtype, rows, stream);
+  bool tail_done = false;
+  cudaError_t e = launch_rows(a, s.dtype, rows, stream, mode == 0 && s.top_p >= 1.f, &tail_done);
   if (e != cudaSuccess) return e;
+  if (tail_done) return cudaGetLastError();
   if (s.top_p < 1.f) {
     e = launch_topp(a, s.dtype, s.top_p, rows, stream);
     if (e != cudaSuccess) return e;
@@ -1693,7 +2410,7 @@ cudaError_t launch_kv_remap(const Shape &s, const KvArgs &kv, const int32_t *anc
                             const int32_t *resampled, int n_append, const Workspace &ws,
                             cudaStream_t stream) {
   const size_t dyn = kv_stage_bytes(s.N, &kv);
-  cudaError_t e = allow_dyn_smem(kv_remap_kernel, dyn);
+  cudaError_t e = configure_kernels();
   if (e != cudaSuccess) return e;
   kv_remap_kernel<<<s.B, kThreads, dyn, stream>>>(s.N, kv, ancestors, resampled, n_append, ws,
                                                    dyn > 0 ? 1 : 0);

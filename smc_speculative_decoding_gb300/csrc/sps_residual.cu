@@ -116,9 +116,10 @@ __global__ void __launch_bounds__(kThreads) sps_stats_kernel(const SpsArgs a) {
         }
         tot = ff_add(tot, warp_ff_sum(val));
       }
-      // log of the (kept) mass of exp(s l): s M + log(total), s M exact in double
-      const ff l = ff_from_double(static_cast<double>(a.tscale) * static_cast<double>(M) +
-                                  log(ff_to_double(tot)));
+      // log of the (kept) mass of exp(s l): s M (exact, as a pair) + log(total)
+      const ff l = (M > kNegInf && tot.hi > 0.f)
+                       ? ff_add(two_prod(a.tscale, M), ff_log(ff_norm(tot), s_tab))
+                       : ff{kNegInf, 0.f};
       lse[r][0] = l.hi;
       lse[r][1] = l.lo;
     }

@@ -42,10 +42,12 @@ __device__ __forceinline__ const char *row_base(const StepArgs &a, int row) {
 
 static inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Opts a kernel into more than 48 KB of dynamic shared memory.
+// Opts a kernel into `bytes` of dynamic shared memory.  A launch whose static
+// plus dynamic shared memory exceeds 48 KB needs this even when the dynamic
+// part alone does not, so it is set whenever a kernel takes any.
 template <typename K>
 static inline cudaError_t allow_dyn_smem(K kernel, size_t bytes) {
-  if (bytes <= 48 * 1024) return cudaSuccess;
+  if (bytes == 0) return cudaSuccess;
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(bytes));
 }

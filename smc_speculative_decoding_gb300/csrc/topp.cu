@@ -458,7 +458,10 @@ __device__ __forceinline__ void topp_finish_fast(const StepArgs &a, int row, int
     if (j < a.K) r.g = kNegInf;                         // outside the target's nucleus
     else raise_status(a.ws.status, SMC_DEV_BAD_TOKEN);  // could not have been drafted
   }
-  r.lse += log_z;
+  // a log-sum-exp row's result holds its value as a float pair (lse, lse_alpha)
+  const ff lse = ff_add(ff{r.lse, r.lse_alpha}, ff{log_z, 0.f});
+  r.lse = lse.hi;
+  r.lse_alpha = lse.lo;
   a.ws.results[row] = r;
 }
 
