@@ -17,10 +17,22 @@ Inputs are resident in HBM before timing; each step reads 591 MB of logits,
 more than the 129 MB L2, from a ring of two distinct step inputs, so no step
 finds its logits in L2.  The KV state and weights are reset every 128 steps
 (the workload's episode length), outside the timed region.
+
+Besides the headline line's own numbers, the JSON carries:
+  * ``extensions``: the draft sampler, smc_step_ex (temperature, potentials,
+    top-p), sps_verify on the serving rows with sampled and with argmax
+    drafts, and the KV-cache saving over a 128-step serving episode;
+  * ``workloads``: every other workload the method is described on (power
+    sampling, the serving draft-noise sweep, the single-prompt latency case,
+    the batch-32 (N, K) sweep), each timed the same way, with its row-pass and
+    whole-step roofline fractions and the oracle timed on a sample of it;
+  * ``parity_sample``: the headline's first steps checked against the CPU
+    oracle (part of the oracle leg), with flagged and mismatched draw counts.
 """
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -41,6 +53,8 @@ KERNEL = "row_stream_kernel"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "row_stream_kernel_batched_serving_v128256.md")
 KERNEL_SOURCES = ["smc_step.cu", "step_args.cuh", "row_common.cuh", "device_common.cuh",
                   "exp2_table.cuh"]
+L2_BYTES = 129 * 2 ** 20
+RING_MIN_BYTES = 4 * L2_BYTES   # a ring of distinct step inputs at least this large
 
 
 def parse_args():
@@ -61,6 +75,10 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the secondary measurements of the step's extensions")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads (power sampling, sweeps, latency case)")
+    ap.add_argument("--sweep", choices=["full", "corners", "none"], default="full",
+                    help="points of the batch-32 (N, K) sweep to time")
     return ap.parse_args()
 
 
@@ -109,16 +127,26 @@ def workload(args):
     return w
 
 
+def logit_bytes(w):
+    return w.B * w.N * (2 * w.K + 1) * w.V * w.bytes_per_logit
+
+
 def algorithmic_bytes(w, T, resampled_prompts):
     """Bytes one step must move: every logit once, the particle state, and the
     block tables of prompts that resampled (read + write)."""
-    logits = w.B * w.N * (2 * w.K + 1) * w.V * w.bytes_per_logit
     particle = w.B * w.N * (4 * w.K        # drafted tokens read
                             + 8             # log-weight read + write
                             + 4 * (w.K + 1)  # emitted tokens
                             + 4)            # ancestor
     tables = resampled_prompts * w.N * (T * 4 * 2 + 8)
-    return logits + particle + tables
+    return logit_bytes(w) + particle + tables
+
+
+def kernels_per_step(w):
+    """Kernels one plain smc_step launches: the streaming row pass, the
+    per-particle epilogue and the per-prompt tail when a row's bytes are a
+    multiple of 16; else the per-chunk row kernel and the tail."""
+    return 3 if (w.V * w.bytes_per_logit) % 16 == 0 else 2
 
 
 def measured_peak():
@@ -204,112 +232,165 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+class StepBench:
+    """Device state of smc_step on one workload: a ring of distinct step
+    inputs (at least RING_MIN_BYTES, so no step finds its logits in L2), the
+    particle outputs and, with KV tables, the paged KV state of an episode."""
+
+    def __init__(self, smcsd, w, dev, seed, episode, with_kv=True, ring_min=RING_MIN_BYTES):
+        from smc_speculative_decoding_gb300.workloads import make_step_inputs, make_kv_state
+        self.smcsd, self.w, self.dev, self.episode = smcsd, w, dev, episode
+        n_ring = max(2, math.ceil(ring_min / logit_bytes(w)))
+        self.ring = [make_step_inputs(w, seed, device=dev, step=s) for s in range(n_ring)]
+        self.T, self.P = w.kv_dims(episode)
+        p0 = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, 0)
+        self.kv0 = self.kv = self.kv_s = None
+        if with_kv:
+            self.kv0 = make_kv_state(w.B, w.N, w.prefix, w.block_size, self.T, self.P, device=dev)
+            self.kv = {k: v.clone() for k, v in self.kv0.items()}
+            self.kv_s = smcsd.make_kv(p0, self.kv, w.block_size)
+        self.ws = smcsd.alloc_workspace(p0, self.kv_s, device=dev)
+        self.lw = torch.zeros(w.B * w.N, device=dev)
+        self.tok = torch.empty(w.B * w.N * (w.K + 1), dtype=torch.int32, device=dev)
+        self.anc = torch.empty(w.B * w.N, dtype=torch.int32, device=dev)
+        self.ess = torch.empty(w.B, device=dev)
+        self.res = torch.empty(w.B, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.current_stream()
+
+    def reset(self):
+        if self.kv is not None:
+            for k in self.kv:
+                self.kv[k].copy_(self.kv0[k])
+        self.lw.zero_()
+
+    def step(self, s):
+        """One smc_step; s is the global step counter (the Philox counter)."""
+        w, inp = self.w, self.ring[s % len(self.ring)]
+        p = self.smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, s)
+        self.smcsd.smc_step(p, inp["target"], inp["draft"], inp["draft_tokens"], self.lw,
+                            self.tok, self.anc, self.ess, self.res, kv=self.kv_s,
+                            workspace=self.ws, stream=self.stream)
+
+    def time_steps(self, n_steps, s0):
+        """Episodes of `episode` steps, the state reset between them (untimed);
+        every step bracketed by CUDA events and nothing else launched in
+        between.  Returns (total ms, per-step ms)."""
+        total, per, done = 0.0, [], 0
+        while done < n_steps:
+            self.reset()
+            n = min(self.episode, n_steps - done)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+            ev[0].record(self.stream)
+            for i in range(n):
+                self.step(s0 + done + i)
+                ev[i + 1].record(self.stream)
+            torch.cuda.synchronize()
+            total += ev[0].elapsed_time(ev[n])
+            per += [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+            done += n
+        return total, per
+
+    def time_rows(self, n_steps, s0):
+        """The same steps again with the library's row-timing hook recording
+        CUDA events around the streaming row kernel; also keeps each step's
+        ESS and resampling flags (copied on the device, outside any timing).
+        Returns (row ms per step, ess [n, B], resampled [n, B])."""
+        w = self.w
+        ess_buf = torch.empty(n_steps, w.B, device=self.dev)
+        res_buf = torch.empty(n_steps, w.B, dtype=torch.int32, device=self.dev)
+        row_ms, done = [], 0
+        while done < n_steps:
+            self.reset()
+            n = min(self.episode, n_steps - done)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n)]
+            for i in range(n):
+                self.smcsd.smc_set_row_timing_events(*evs[i])
+                self.step(s0 + done + i)
+                ess_buf[done + i].copy_(self.ess)
+                res_buf[done + i].copy_(self.res)
+            self.smcsd.smc_set_row_timing_events(None, None)
+            torch.cuda.synchronize()
+            row_ms += [b.elapsed_time(e) for b, e in evs]
+            done += n
+        return row_ms, ess_buf.cpu().numpy(), res_buf.cpu().numpy()
+
+    def status(self):
+        return self.smcsd.smc_device_status(self.ws, clear=True)
+
+
+def step_figures(w, total_ms, per_ms, n_steps, row_ms, ess, res, T, peak, world=1):
+    """The numbers of one workload's timing: throughput, per-step spread, the
+    row pass against the HBM peak, the whole step against it."""
+    ms = total_ms / n_steps
+    resampled = float(res.sum()) / max(1, res.shape[0])
+    row_launch_ms = float(np.mean(row_ms))
+    row_gbs = logit_bytes(w) / (row_launch_ms / 1e3) / 1e9
+    step_bytes = algorithmic_bytes(w, T, resampled)
+    step_gbs = step_bytes / (ms / 1e3) / 1e9
+    return {
+        "ms_per_step": ms, "ms_per_step_median": float(np.median(per_ms)),
+        "ms_per_step_min": float(np.min(per_ms)),
+        "particle_tokens_per_s": w.particle_tokens * n_steps * world / (total_ms / 1e3),
+        "steps_per_s": n_steps * world / (total_ms / 1e3),
+        "row_pass": {"ms": row_launch_ms, "gbs": row_gbs, "frac": row_gbs / peak,
+                     "bytes": logit_bytes(w)},
+        "step": {"gbs": step_gbs, "frac": step_gbs / peak, "bytes": step_bytes},
+        "resampled_prompts_per_step": resampled, "mean_ess": float(np.mean(ess)),
+        "mean_ess_over_n": float(np.mean(ess)) / w.N,
+    }
+
+
 def run_ours(args, world, rank, local):
     import smc_speculative_decoding_gb300 as smcsd
     from smc_speculative_decoding_gb300 import build
-    from smc_speculative_decoding_gb300.workloads import make_step_inputs, make_kv_state
 
     build.build()
     dev = f"cuda:{local}"
     w = workload(args)
-    T, P = w.kv_dims(args.episode)
-    ring = [make_step_inputs(w, input_seed(rank), device=dev, step=s) for s in range(2)]
-    kv0 = make_kv_state(w.B, w.N, w.prefix, w.block_size, T, P, device=dev)
-    kv = {k: v.clone() for k, v in kv0.items()}
-    p0 = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, 0)
-    kv_s = smcsd.make_kv(p0, kv, w.block_size)
-    ws = smcsd.alloc_workspace(p0, kv_s, device=dev)
-    lw = torch.zeros(w.B * w.N, device=dev)
-    tok = torch.empty(w.B * w.N * (w.K + 1), dtype=torch.int32, device=dev)
-    anc = torch.empty(w.B * w.N, dtype=torch.int32, device=dev)
-    ess = torch.empty(w.B, device=dev)
-    res = torch.empty(w.B, dtype=torch.int32, device=dev)
-    res_count = torch.zeros(w.B, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream()
+    sb = StepBench(smcsd, w, dev, input_seed(rank), args.episode, ring_min=0)
 
-    def reset():
-        for k in kv:
-            kv[k].copy_(kv0[k])
-        lw.zero_()
-
-    def step(s, count=False):
-        # s is the global step counter (the Philox counter of the step)
-        inp = ring[s % 2]
-        p = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, s)
-        smcsd.smc_step(p, inp["target"], inp["draft"], inp["draft_tokens"],
-                       lw, tok, anc, ess, res, kv=kv_s, workspace=ws, stream=stream)
-        if count:
-            res_count.add_(res)
-
-    # warm-up
-    reset()
-    for s in range(args.warmup):
-        step(s)
-        if (s + 1) % args.episode == 0:
-            reset()
-    torch.cuda.synchronize()
-    assert smcsd.smc_device_status(ws, clear=True) == 0
-
-    # timed region: episodes of `episode` steps, KV reset between them (untimed)
+    # the clock sampler starts first, so that the timed steps follow the
+    # warm-up with no idle gap (an idle GPU drops its clocks, and the first
+    # step after a pause then runs several times slower)
     clocks = ClockSampler(local)
     clocks.start()
+    sb.reset()
+    for s in range(args.warmup):
+        sb.step(s)
+        if (s + 1) % args.episode == 0:
+            sb.reset()
+    assert sb.status() == 0  # synchronises
+
+    # timed region: episodes of `episode` steps, KV reset between them (untimed)
     barrier(world)
     torch.cuda.synchronize()
-    total_ms = 0.0
-    launch_ms = []
-    done = 0
-    while done < args.steps:
-        reset()
-        n = min(args.episode, args.steps - done)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
-        ev[0].record(stream)
-        for s in range(n):
-            step(args.warmup + done + s, count=True)
-            ev[s + 1].record(stream)
-        torch.cuda.synchronize()
-        total_ms += ev[0].elapsed_time(ev[n])
-        launch_ms += [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
-        done += n
+    total_ms, per_ms = sb.time_steps(args.steps, args.warmup)
     barrier(world)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    bits = smcsd.smc_device_status(ws, clear=True)
+    bits = sb.status()
     if bits:
         raise RuntimeError(f"device status during timing: {smcsd.status_names(bits)}")
     total_ms = max_over_ranks(total_ms, world)
-    resampled_prompts = float(res_count.sum().item()) / args.steps
 
     # the row pass alone: a second run of the same steps with the library's
     # row-timing hook recording CUDA events around the streaming kernel
-    row_ms = []
-    done = 0
     n_rows_steps = min(args.steps, args.row_steps)
-    while done < n_rows_steps:
-        reset()
-        n = min(args.episode, n_rows_steps - done)
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(n)]
-        for s in range(n):
-            smcsd.smc_set_row_timing_events(*evs[s])
-            step(args.warmup + done + s)
-        smcsd.smc_set_row_timing_events(None, None)
-        torch.cuda.synchronize()
-        row_ms += [b.elapsed_time(e) for b, e in evs]
-        done += n
+    row_ms, ess, res = sb.time_rows(n_rows_steps, args.warmup)
+    assert sb.status() == 0
     row_launch_ms = max_over_ranks(float(np.mean(row_ms)), world)
-
-    ptok = w.particle_tokens * args.steps * world
-    value = ptok / (total_ms / 1e3)
-    avg_launch_ms = float(np.mean(launch_ms))
-    bytes_step = algorithmic_bytes(w, T, resampled_prompts)
-    step_gbs = bytes_step / (avg_launch_ms / 1e3) / 1e9
-    row_bytes = w.B * w.N * (2 * w.K + 1) * w.V * w.bytes_per_logit
-    achieved = row_bytes / (row_launch_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak()
+    fig = step_figures(w, total_ms, per_ms, args.steps, [row_launch_ms], ess, res, sb.T, peak,
+                       world)
+    row_bytes = logit_bytes(w)
+    achieved = row_bytes / (row_launch_ms / 1e3) / 1e9
 
     out = {
-        "metric": METRIC, "value": value, "unit": "particle-tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "metric": METRIC, "value": fig["particle_tokens_per_s"], "unit": "particle-tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps,
+        "ms_per_step_median": fig["ms_per_step_median"], "ms_per_step_min": fig["ms_per_step_min"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "N": w.N, "K": w.K, "V": w.V,
@@ -319,8 +400,9 @@ def run_ours(args, world, rank, local):
                    "parallelism": f"prompt-sharded x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2: 591 MB of logits per step from a ring of "
                          "2 distinct steps (129 MB L2)"},
-        "steps_per_s": args.steps * world / (total_ms / 1e3),
-        "resampled_prompts_per_step": resampled_prompts,
+        "steps_per_s": fig["steps_per_s"],
+        "resampled_prompts_per_step": fig["resampled_prompts_per_step"],
+        "mean_ess": fig["mean_ess"], "mean_ess_over_n": fig["mean_ess_over_n"],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(),
                      "kernel": KERNEL, "algorithmic_bytes_per_launch": row_bytes,
@@ -328,28 +410,61 @@ def run_ours(args, world, rank, local):
                      "launch_timing": f"CUDA events around the row pass (library hook), "
                                       f"{len(row_ms)} steps after the timed region",
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
-        "step_roofline": {"achieved": step_gbs, "frac": step_gbs / peak, "unit": "GB/s",
-                          "algorithmic_bytes_per_step": bytes_step,
-                          "avg_step_ms": avg_launch_ms,
-                          "kernels": ["row_stream_kernel", "finish_kernel", "tail_kernel"]},
-        # each smc_step launches row_stream_kernel, finish_kernel and tail_kernel
-        "gpu_launches": 3 * args.steps,
+        "step_roofline": {"achieved": fig["step"]["gbs"], "frac": fig["step"]["frac"],
+                          "unit": "GB/s", "algorithmic_bytes_per_step": fig["step"]["bytes"],
+                          "avg_step_ms": total_ms / args.steps,
+                          "kernels": ["row_stream_kernel", "particle_kernel", "prompt_kernel"]
+                          if kernels_per_step(w) == 3 else
+                          ["step_rows_kernel", "tail_kernel"]},
+        "gpu_launches": kernels_per_step(w) * args.steps,
         "clocks": clk,
     }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["_parity_inputs"] = gpu_parity_sample(sb, n_steps=2, s0=args.warmup + args.steps)
+    del sb
+    torch.cuda.empty_cache()
     if not args.no_e2e:
         out["e2e"] = run_e2e(args, w, dev, smcsd, world)
     if not args.no_extras:
-        out["extensions"] = run_extensions(w, dev, smcsd, ring)
+        out["extensions"] = run_extensions(w, dev, smcsd)
+    if not args.no_workloads and rank == 0:
+        out["workloads"] = run_workloads(args, dev, smcsd, peak, with_cpu=not args.no_cpu_baseline)
     return out
 
 
-def run_extensions(w, dev, smcsd, ring, reps=50):
-    """Secondary measurements, not part of the step's line: the draft-side
-    sampler on one position of every particle (B*N rows of V), and smc_step_ex
-    at temperature 0.8 with log-potentials (the same step as the headline,
-    with the extensions on)."""
-    import torch
+def gpu_parity_sample(sb, n_steps, s0):
+    """The headline's first steps of a fresh episode, with each step's inputs
+    and the GPU's state before and after, copied to the host for the oracle
+    leg to check (the oracle runs in cpu_baseline, not here)."""
+    w = sb.w
+    sb.reset()
+    samples = []
+    for i in range(n_steps):
+        inp = sb.ring[(s0 + i) % len(sb.ring)]
+        lw_in = sb.lw.cpu().numpy().reshape(w.B, w.N).astype(np.float64)
+        sb.step(s0 + i)
+        torch.cuda.synchronize()
+        samples.append(dict(
+            step=s0 + i, lw_in=lw_in,
+            target=inp["target"].cpu(), draft=inp["draft"].cpu(),
+            x=inp["draft_tokens"].cpu().numpy().astype(np.int64),
+            lw=sb.lw.cpu().numpy().reshape(w.B, w.N).astype(np.float64),
+            tok=sb.tok.cpu().numpy().reshape(w.B, w.N, w.K + 1),
+            anc=sb.anc.cpu().numpy().reshape(w.B, w.N),
+            ess=sb.ess.cpu().numpy().astype(np.float64),
+            res=sb.res.cpu().numpy().astype(bool)))
+    assert sb.status() == 0
+    return samples
+
+
+def run_extensions(w, dev, smcsd, reps=50):
+    """Secondary measurements on the headline workload's rows: the draft-side
+    sampler, smc_step_ex at temperature 0.8 with log-potentials and at top-p
+    0.9, sps_verify on the same rows, and the KV-cache saving of an episode."""
+    from smc_speculative_decoding_gb300.workloads import make_step_inputs, make_kv_state
+    peak = measured_peak()[0]
     res = {}
+    ring = [make_step_inputs(w, 1000, device=dev, step=s) for s in range(2)]
     params = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, 1.0, w.ess_frac, 0, 0)
     ws = smcsd.alloc_workspace(params)
     rows = ring[0]["draft"][:, :, 0].contiguous()
@@ -371,11 +486,12 @@ def run_extensions(w, dev, smcsd, ring, reps=50):
     res["draft_sample"] = {"rows": w.B * w.N, "V": w.V, "ms_per_call": med,
                            "tokens_per_s": w.B * w.N / (med / 1e3),
                            "achieved_gbs": bytes_call / (med / 1e3) / 1e9,
-                           "frac_of_hbm_peak": bytes_call / (med / 1e3) / 1e9 / measured_peak()[0],
+                           "frac_of_hbm_peak": bytes_call / (med / 1e3) / 1e9 / peak,
                            "l2": "256 MB buffer written between calls"}
+    del rows, flush
     T, P = w.kv_dims(64)
-    from smc_speculative_decoding_gb300.workloads import make_kv_state
-    kv = make_kv_state(w.B, w.N, w.prefix, w.block_size, T, P, device=dev)
+    kv0 = make_kv_state(w.B, w.N, w.prefix, w.block_size, T, P, device=dev)
+    kv = {k: v.clone() for k, v in kv0.items()}
     kv_s = smcsd.make_kv(params, kv, w.block_size)
     ws2 = smcsd.alloc_workspace(params, kv_s)
     lw = torch.zeros(w.B * w.N, device=dev)
@@ -383,87 +499,167 @@ def run_extensions(w, dev, smcsd, ring, reps=50):
                 anc=torch.empty(w.B * w.N, dtype=torch.int32, device=dev),
                 ess=torch.empty(w.B, device=dev), res=torch.empty(w.B, dtype=torch.int32, device=dev))
     phi = torch.zeros(w.B * w.N, device=dev)
-    n = 48
-    for s in range(3):
-        p = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, s)
-        smcsd.smc_step_ex(p, ring[s % 2]["target"], ring[s % 2]["draft"], ring[s % 2]["draft_tokens"],
-                          lw, outs["tok"], outs["anc"], outs["ess"], outs["res"], kv=kv_s,
-                          workspace=ws2, temperature=0.8, log_potential=phi)
-    torch.cuda.synchronize()
-    e0.record()
-    for s in range(n):
-        p = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, 3 + s)
-        smcsd.smc_step_ex(p, ring[s % 2]["target"], ring[s % 2]["draft"], ring[s % 2]["draft_tokens"],
-                          lw, outs["tok"], outs["anc"], outs["ess"], outs["res"], kv=kv_s,
-                          workspace=ws2, temperature=0.8, log_potential=phi)
-    e1.record()
-    torch.cuda.synchronize()
-    assert smcsd.smc_device_status(ws2, clear=True) == 0
-    ms_step = e0.elapsed_time(e1) / n
+
+    def reset():
+        for k in kv:
+            kv[k].copy_(kv0[k])
+        lw.zero_()
+
+    def ex_steps(n, s0, ring_, **kw):
+        for s in range(n):
+            p = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, s0 + s)
+            r = ring_[s % 2]
+            smcsd.smc_step_ex(p, r["target"], r["draft"], r["draft_tokens"], lw, outs["tok"],
+                              outs["anc"], outs["ess"], outs["res"], kv=kv_s, workspace=ws2, **kw)
+
+    def timed(n, ring_, **kw):
+        reset()
+        ex_steps(3, 0, ring_, **kw)
+        torch.cuda.synchronize()
+        e0.record()
+        ex_steps(n, 3, ring_, **kw)
+        e1.record()
+        torch.cuda.synchronize()
+        assert smcsd.smc_device_status(ws2, clear=True) == 0
+        return e0.elapsed_time(e1) / n
+
+    ms_step = timed(48, ring, temperature=0.8, log_potential=phi)
     res["step_ex_temperature_potential"] = {"ms_per_step": ms_step,
                                             "particle_tokens_per_s": w.particle_tokens / (ms_step / 1e3),
-                                            "temperature": 0.8, "steps": n}
+                                            "temperature": 0.8, "steps": 48}
     # top-p 0.9: drafted tokens are each draft row's argmax, always inside its nucleus
     ring_tp = [dict(r, draft_tokens=r["draft"].float().argmax(-1).to(torch.int32).contiguous())
                for r in ring]
-    for k in kv:
-        kv[k].copy_(make_kv_state(w.B, w.N, w.prefix, w.block_size, T, P, device=dev)[k])
-    lw.zero_()
-
-    def tp_step(s):
-        p = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, s)
-        smcsd.smc_step_ex(p, ring_tp[s % 2]["target"], ring_tp[s % 2]["draft"],
-                          ring_tp[s % 2]["draft_tokens"], lw, outs["tok"], outs["anc"], outs["ess"],
-                          outs["res"], kv=kv_s, workspace=ws2, top_p=0.9)
-    for s in range(3):
-        tp_step(s)
-    torch.cuda.synchronize()
-    n_tp = 16
-    e0.record()
-    for s in range(n_tp):
-        tp_step(3 + s)
-    e1.record()
-    torch.cuda.synchronize()
-    assert smcsd.smc_device_status(ws2, clear=True) == 0
-    ms_tp = e0.elapsed_time(e1) / n_tp
-    res["step_ex_top_p"] = {"ms_per_step": ms_tp, "top_p": 0.9, "steps": n_tp,
+    ms_tp = timed(16, ring_tp, top_p=0.9)
+    res["step_ex_top_p"] = {"ms_per_step": ms_tp, "top_p": 0.9, "steps": 16,
                             "particle_tokens_per_s": w.particle_tokens / (ms_tp / 1e3),
-                            "note": "the nucleus kernel reads every row once more from HBM and again from L2 (mass bins, then the threshold bin)"}
+                            "note": "the nucleus kernel reads every row once more from HBM "
+                                    "and again from L2 (mass bins, then the threshold bin)"}
     # speculative-sampling verify on the same rows, one particle per prompt
-    # (B*N prompts), plain and under temperature 0.8 with top-p 0.9
+    # (B*N prompts): drafted tokens sampled from the draft rows (the
+    # workload's own, as speculative sampling draws them), and each draft
+    # row's argmax (few rejections); then under temperature 0.8 and top-p 0.9
     nb = w.B * w.N
     ps = smcsd.make_params(nb, 1, w.K, w.V, w.dtype, 1.0, 0.5, 0, 0)
     ws3 = smcsd.alloc_workspace(ps)
     s_tok = torch.empty(nb * (w.K + 1), dtype=torch.int32, device=dev)
     s_n = torch.empty(nb, dtype=torch.int32, device=dev)
-    views = [(r["target"].view(nb, w.K + 1, w.V), r["draft"].view(nb, w.K, w.V), r["draft_tokens"].view(nb, w.K))
-             for r in ring_tp]
+    bytes_call = nb * (2 * w.K + 1) * w.V * w.bytes_per_logit
 
-    def sps_time(**kw):
+    def sps_time(ring_, **kw):
+        views = [(r["target"].view(nb, w.K + 1, w.V), r["draft"].view(nb, w.K, w.V),
+                  r["draft_tokens"].view(nb, w.K)) for r in ring_]
         fn = smcsd.sps_verify_ex if kw else smcsd.sps_verify
         for s in range(3):
             fn(ps, *views[s % 2], s_tok, s_n, ws3, **kw)
         torch.cuda.synchronize()
-        n_sps, emitted = 16, 0
+        n_sps = 16
         e0.record()
         for s in range(n_sps):
             fn(ps, *views[s % 2], s_tok, s_n, ws3, **kw)
         e1.record()
         torch.cuda.synchronize()
         assert smcsd.smc_device_status(ws3, clear=True) == 0
-        emitted = int(s_n.sum().item())
-        return e0.elapsed_time(e1) / n_sps, emitted
-    ms_s, em = sps_time()
-    bytes_call = nb * (2 * w.K + 1) * w.V * w.bytes_per_logit
-    res["sps_verify"] = {"prompts": nb, "ms_per_call": ms_s,
-                         "tokens_per_s_last_call": em / (ms_s / 1e3),
-                         "achieved_gbs": bytes_call / (ms_s / 1e3) / 1e9,
-                         "frac_of_hbm_peak": bytes_call / (ms_s / 1e3) / 1e9 / measured_peak()[0],
-                         "bytes": "every row once; a rejection reads two rows again"}
-    ms_s2, em2 = sps_time(temperature=0.8, top_p=0.9)
-    res["sps_verify_ex_top_p"] = {"prompts": nb, "ms_per_call": ms_s2, "temperature": 0.8,
-                                  "top_p": 0.9, "tokens_per_s_last_call": em2 / (ms_s2 / 1e3)}
+        m = e0.elapsed_time(e1) / n_sps
+        em = int(s_n.sum().item())
+        return {"prompts": nb, "ms_per_call": m, "tokens_per_s_last_call": em / (m / 1e3),
+                "rejected_prompts_last_call": int((s_n <= w.K).sum().item()),
+                "achieved_gbs": bytes_call / (m / 1e3) / 1e9,
+                "frac_of_hbm_peak": bytes_call / (m / 1e3) / 1e9 / peak,
+                "bytes": "every row once; a rejected prompt's rows p_j and q_j again"}
+
+    res["sps_verify"] = dict(sps_time(ring), drafts="sampled from the draft rows")
+    res["sps_verify_argmax_drafts"] = dict(sps_time(ring_tp), drafts="each draft row's argmax")
+    r2 = sps_time(ring_tp, temperature=0.8, top_p=0.9)
+    res["sps_verify_ex_top_p"] = {k: r2[k] for k in ("prompts", "ms_per_call",
+                                                      "tokens_per_s_last_call")}
+    res["sps_verify_ex_top_p"].update(temperature=0.8, top_p=0.9, drafts="argmax")
+    del ring_tp
+    res["kv_saving"] = kv_saving_episode(w, dev, smcsd, ring)
     return res
+
+
+def kv_saving_episode(w, dev, smcsd, ring, steps=128):
+    """The KV cache of one serving episode: every step appends K+1 tokens,
+    resampling shares blocks by pointer; smc_kv_usage after each step gives
+    the blocks in use and the blocks N unshared copies would hold."""
+    from smc_speculative_decoding_gb300.workloads import make_kv_state
+    T, P = w.kv_dims(steps)
+    params = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, 0)
+    kv = make_kv_state(w.B, w.N, w.prefix, w.block_size, T, P, device=dev)
+    kv_s = smcsd.make_kv(params, kv, w.block_size)
+    ws = smcsd.alloc_workspace(params, kv_s)
+    lw = torch.zeros(w.B * w.N, device=dev)
+    tok = torch.empty(w.B * w.N * (w.K + 1), dtype=torch.int32, device=dev)
+    anc = torch.empty(w.B * w.N, dtype=torch.int32, device=dev)
+    ess = torch.empty(w.B, device=dev)
+    res = torch.empty(w.B, dtype=torch.int32, device=dev)
+    used = torch.empty(steps, w.B, dtype=torch.int32, device=dev)
+    unshared = torch.empty(steps, w.B, dtype=torch.int32, device=dev)
+    for s in range(steps):
+        p = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, w.alpha, w.ess_frac, 0, s)
+        r = ring[s % len(ring)]
+        smcsd.smc_step(p, r["target"], r["draft"], r["draft_tokens"], lw, tok, anc, ess, res,
+                       kv=kv_s, workspace=ws)
+        smcsd.smc_kv_usage(params, kv_s, used[s], unshared[s])
+    torch.cuda.synchronize()
+    assert smcsd.smc_device_status(ws) == 0
+    u = used.cpu().numpy().sum(1).astype(np.float64)
+    x = unshared.cpu().numpy().sum(1).astype(np.float64)
+    saving = 1.0 - u / x
+    return {"steps": steps, "prefix": w.prefix, "block_size": w.block_size,
+            "used_blocks_final": int(u[-1]), "unshared_blocks_final": int(x[-1]),
+            "saving_final": float(saving[-1]), "saving_mean": float(saving.mean()),
+            "saving_first_step": float(saving[0]),
+            "context": "the pages report 72.3 % less KV cache for SMC-SD on their models; "
+                       "this is the same ratio on synthetic logits"}
+
+
+def run_workloads(args, dev, smcsd, peak, with_cpu):
+    """Every other workload of the method, timed like the headline: power
+    sampling (alpha = 4), the serving draft-noise sweep, the single-prompt
+    latency case and the batch-32 (N, K) sweep."""
+    from smc_speculative_decoding_gb300.workloads import (WORKLOADS, SERVING_SIGMAS, SWEEP_N,
+                                                          SWEEP_K)
+    out = {}
+    cases = [("power_sampling_v151936", WORKLOADS["power_sampling_v151936"], 16)]
+    for sig in SERVING_SIGMAS:
+        if sig != WORKLOADS[WORKLOAD].sigma_d:
+            cases.append((f"batched_serving_v128256_sigma_d{sig:g}",
+                          WORKLOADS[WORKLOAD].with_(sigma_d=sig), 16))
+    cases.append(("single_prompt_v32000", WORKLOADS["single_prompt_v32000"], 64))
+    if args.sweep != "none":
+        pts = [(n, k) for n in SWEEP_N for k in SWEEP_K]
+        if args.sweep == "corners":
+            pts = [(1, 2), (8, 4), (64, 8)]
+        for n, k in pts:
+            cases.append((f"sweep_v128256_N{n}_K{k}", WORKLOADS["sweep_v128256"].with_(N=n, K=k), 12))
+    for name, w, n_steps in cases:
+        sb = StepBench(smcsd, w, dev, 1000, max(128, n_steps))
+        sb.reset()
+        for s in range(3):
+            sb.step(s)
+        torch.cuda.synchronize()
+        total, per = sb.time_steps(n_steps, 3)
+        assert sb.status() == 0
+        row_ms, ess, res = sb.time_rows(min(n_steps, 8), 3)
+        fig = step_figures(w, total, per, n_steps, row_ms, ess, res, sb.T, peak)
+        fig["config"] = {"B": w.B, "N": w.N, "K": w.K, "V": w.V, "logits": w.dtype,
+                         "alpha": w.alpha, "sigma_d": w.sigma_d, "prefix": w.prefix,
+                         "steps": n_steps, "ring_inputs": len(sb.ring),
+                         "ring_bytes": len(sb.ring) * logit_bytes(w)}
+        fig["us_per_step"] = 1e3 * fig["ms_per_step"]
+        fig["gpu_launches_per_step"] = kernels_per_step(w)
+        del sb
+        torch.cuda.empty_cache()
+        if with_cpu:
+            n, el = oracle_prompt_steps(w, 0.5 if name.startswith("sweep") else 2.0, max_steps=2)
+            fig["cpu_baseline"] = {"value": n * w.N * (w.K + 1) / el, "unit": "particle-tokens/s",
+                                   "cores": 1, "kind": "oracle",
+                                   "sample": f"{n} prompt-steps of 1 x {w.N} particles, "
+                                             f"{2 * w.K + 1} rows of V={w.V}, in {el:.2f} s"}
+        out[name] = fig
+    return out
 
 
 def run_e2e(args, w, dev, smcsd, world):
@@ -609,14 +805,56 @@ def oracle_all_cores(w, budget_s):
             "sample": f"{n} prompt-steps over {cores} processes in {el:.1f} s"}
 
 
-def cpu_baseline(w, budget_s):
+def oracle_parity(w, samples):
+    """The oracle on the GPU's parity sample (inputs and the GPU's incoming
+    log-weights, step by step): draws compared, flagged as near ties
+    (|u S - C| < 1e-5 S), mismatched; log-weights compared where no
+    resampling reset them."""
+    from smc_speculative_decoding_gb300.workloads import to_numpy_logits
+    from oracle import smc as osmc
+    tol = 2e-3 if w.dtype == "bf16" else 1e-4
+    c = {"prompt_steps": 0, "draws": 0, "flagged": 0, "mismatched": 0, "unflagged_mismatched": 0,
+         "lw_checked": 0, "lw_err_max": 0.0, "lw_out_of_tolerance": 0}
+    t0 = time.perf_counter()
+    for smp in samples:
+        tgt, dft = to_numpy_logits(smp["target"]), to_numpy_logits(smp["draft"])
+        r = osmc.smc_step(tgt, dft, smp["x"], smp["lw_in"], alpha=w.alpha, ess_frac=w.ess_frac,
+                          seed=0, step=smp["step"], dtype=w.dtype)
+        c["prompt_steps"] += w.B
+
+        def add(n, flag, miss):
+            c["draws"] += int(n)
+            c["flagged"] += int(np.sum(flag))
+            c["mismatched"] += int(np.sum(miss))
+            c["unflagged_mismatched"] += int(np.sum(miss & ~flag))
+        add(w.B, r["ess_margin"] < 1e-5, smp["res"] != r["resampled"])
+        for b in range(w.B):
+            if smp["res"][b] != r["resampled"][b]:
+                continue
+            a = smp["anc"][b]
+            if smp["res"][b]:
+                add(w.N, r["resample_margin"][b] < 1e-5, a != r["ancestors"][b])
+            else:
+                err = np.abs(smp["lw"][b] - r["log_weights_pre"][b])
+                c["lw_checked"] += w.N
+                c["lw_err_max"] = max(c["lw_err_max"], float(err.max()))
+                c["lw_out_of_tolerance"] += int((err > tol).sum())
+            add(w.N, r["bonus_margin"][b, a] < 1e-5, smp["tok"][b, :, w.K] != r["bonus"][b, a])
+    c["oracle_seconds"] = time.perf_counter() - t0
+    return c
+
+
+def cpu_baseline(w, budget_s, parity_samples=None):
     n, el = oracle_prompt_steps(w, budget_s)
-    return {"value": n * w.N * (w.K + 1) / el, "unit": "particle-tokens/s", "cores": 1,
-            "kind": "oracle",
-            "sample": f"{n} prompt-steps of {w.name} (1 prompt x {w.N} particles x "
-                      f"{2 * w.K + 1} rows of V={w.V}, tail and KV remap) in {el:.1f} s, "
-                      f"numpy fp64, single thread",
-            "all_cores": oracle_all_cores(w, budget_s)}
+    out = {"value": n * w.N * (w.K + 1) / el, "unit": "particle-tokens/s", "cores": 1,
+           "kind": "oracle",
+           "sample": f"{n} prompt-steps of {w.name} (1 prompt x {w.N} particles x "
+                     f"{2 * w.K + 1} rows of V={w.V}, tail and KV remap) in {el:.1f} s, "
+                     f"numpy fp64, single thread",
+           "all_cores": oracle_all_cores(w, budget_s)}
+    if parity_samples:
+        out["parity_sample"] = oracle_parity(w, parity_samples)
+    return out
 
 
 def run_reference(args, world, rank):
@@ -655,9 +893,11 @@ def main():
         return 0
     world, rank, local = dist_setup(args.gpus)
     out = run_ours(args, world, rank, local)
+    samples = out.pop("_parity_inputs", None)
     if rank == 0:
         if not args.no_cpu_baseline:
-            out["cpu_baseline"] = cpu_baseline(workload(args), args.cpu_seconds)
+            out["cpu_baseline"] = cpu_baseline(workload(args), args.cpu_seconds, samples)
+            out["parity_sample"] = out["cpu_baseline"].pop("parity_sample", None)
         print(json.dumps(out), flush=True)
     if world > 1:
         import torch.distributed as dist
