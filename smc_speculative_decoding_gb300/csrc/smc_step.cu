@@ -359,9 +359,10 @@ __device__ void kv_prepare(const KvArgs &kv, int b, int N, const KvScratch &sc, 
                            int t0, int nt) {
   const int t = static_cast<int>(threadIdx.x) - t0;
   if (t < 0 || t >= nt) return;
-  const int T = kv.T, bs = kv.block_size, P = kv.P;
+  const int T = kv.T, P = kv.P;
+  const unsigned bs = static_cast<unsigned>(kv.block_size);
   const int lo_id = b * P;
-  const long long cap = static_cast<long long>(T) * bs;  // tokens a full table holds
+  const long long cap = static_cast<long long>(T) * kv.block_size;  // tokens a full table holds
   auto in_pool = [&](int blk) { return blk >= lo_id && blk < lo_id + P; };
   int bad = 0;
   if (t == 0) {
@@ -375,8 +376,8 @@ __device__ void kv_prepare(const KvArgs &kv, int b, int N, const KvScratch &sc, 
     if (len < 0 || len > cap) {
       bad |= kBadState;
     } else {
-      nb = static_cast<int>((static_cast<long long>(len) + bs - 1) / bs);
-      if (len % bs) {
+      nb = static_cast<int>((static_cast<unsigned>(len) + bs - 1u) / bs);
+      if (static_cast<unsigned>(len) % bs) {
         tail = sc.old_t[i * T + nb - 1];
         if (!in_pool(tail)) bad |= kBadTail;
       }
@@ -384,24 +385,28 @@ __device__ void kv_prepare(const KvArgs &kv, int b, int N, const KvScratch &sc, 
     ks.nb[i] = nb;
     ks.otail[i] = tail;
   }
-  // every slot: a warp of the group per particle, a lane per slot
-  const int lane = t & 31, nw = nt >> 5;
-  const int len0 = sc.old_l[0];
-  const long long nb0 = (len0 < 0 || len0 > cap) ? -1 : (static_cast<long long>(len0) + bs - 1) / bs;
-  for (int i = t >> 5; i < N; i += nw) {
-    const int len = sc.old_l[i];
-    if (len < 0 || len > cap) continue;  // flagged above
-    const int nb = static_cast<int>((static_cast<long long>(len) + bs - 1) / bs);
-    int first = T;
-    for (int s = lane; s < T; s += 32) {
-      const int v = sc.old_t[i * T + s];
-      if (s < nb && !in_pool(v)) bad |= kBadId;
-      if (first == T && (v != sc.old_t[s] || (s < nb) != (s < nb0))) first = s;
+  named_bar_sync(2, nt);  // ks.nb of every particle
+  // every slot (i, s): consecutive threads on consecutive particles at one
+  // slot, each thread's pairs kept apart by nt; the first slot at which a
+  // particle differs from particle 0 bounds t_common
+  const int nb0 = ks.nb[0];
+  const int di = nt % N, ds = nt / N;
+  int i = t % N, s = t / N, first = T;
+  while (s < T) {
+    const int v = sc.old_t[i * T + s];
+    const bool used = s < ks.nb[i];
+    if (used && !in_pool(v)) bad |= kBadId;
+    if (s < first && (v != sc.old_t[s] || used != (s < nb0))) first = s;
+    i += di;
+    s += ds;
+    if (i >= N) {
+      i -= N;
+      ++s;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(0xffffffffu, first, o));
-    if (lane == 0 && first < T) atomicMin(&ks.t_common, first);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(0xffffffffu, first, o));
+  if ((t & 31) == 0 && first < T) atomicMin(&ks.t_common, first);
   if (bad) atomicOr(&ks.bad, bad);
 }
 
@@ -418,10 +423,25 @@ __device__ __forceinline__ int warp_excl_scan_i(int v, int *total) {
   return x - v;
 }
 
+// ceil(a / b) for a >= 0, b >= 1, by a 32-bit division when the operands
+// allow (a 64-bit division costs several hundred cycles).
+__device__ __forceinline__ long long ceil_div_nonneg(long long a, int b) {
+  const unsigned long long n = static_cast<unsigned long long>(a) + static_cast<unsigned>(b) - 1ull;
+  if (n < 4294967296ull) return static_cast<unsigned>(n) / static_cast<unsigned>(b);
+  return static_cast<long long>(n / static_cast<unsigned long long>(b));
+}
+
 // Remap of prompt b's block tables by the ancestors s_anc (when resampled)
 // and append of n_append tokens to every particle, by the whole CTA.  With
 // `prepared`, kv_prepare has run on the staged state (all threads passed a
 // barrier since); with `copied`, the state is already in `sc`.
+//
+// Staged state: the pushed blocks are listed in shared memory and go back as
+// one range, and each remapped table goes back as one contiguous row segment
+// (past the shared prefix).  Global stores are the expensive part of this
+// latency-bound code (on GB300 each warp-wide store instruction occupies the
+// SM for about 40 cycles, coalesced or not), so only changed counts are
+// stored.
 __device__ void kv_remap_append(const KvArgs &kv, int b, int N, const int *s_anc, bool resampled,
                                 int n_append, const Workspace &ws, KvSmem &ks,
                                 const KvScratch &sc, bool copied, bool prepared) {
@@ -457,8 +477,6 @@ __device__ void kv_remap_append(const KvArgs &kv, int b, int N, const int *s_anc
     }
   }
   const int top_old = ks.top_old;
-  // the append runs on warp 0 alone for N <= 32 (staged state)
-  const bool warp_path = N <= 32 && staged;
 
   if (resampled) {
     if (staged) {
@@ -476,12 +494,10 @@ __device__ void kv_remap_append(const KvArgs &kv, int b, int N, const int *s_anc
       const int di = kThreads % N, dt = kThreads / N;
       int i = tid % N, t = tc + tid / N;
       while (t < T) {
-        int ia[kU], ta[kU], nv[kU], ov[kU];
+        int nv[kU], ov[kU];
         bool upd[kU], hn[kU], ho[kU];
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-          ia[u] = i;
-          ta[u] = t;
           upd[u] = false;
           if (t < T) {
             const int anc = s_anc[i];
@@ -503,8 +519,13 @@ __device__ void kv_remap_append(const KvArgs &kv, int b, int N, const int *s_anc
           if (!upd[u]) continue;
           if (hn[u] && !(ho[u] && ov[u] == nv[u])) atomicAdd(&sc.delta[nv[u] - lo_id], 1);
           if (ho[u] && !(hn[u] && nv[u] == ov[u])) atomicSub(&sc.delta[ov[u] - lo_id], 1);
-          if (nv[u] != ov[u]) tables[ia[u] * T + ta[u]] = nv[u];
         }
+      }
+      // the new tables: row segments [t_common, T) of the ancestors, a warp a row
+      for (int p = warp; p < N; p += kWarps) {
+        const int anc = s_anc[p];
+        if (anc == p) continue;
+        for (int s2 = tc + lane; s2 < T; s2 += 32) tables[p * T + s2] = sc.old_t[anc * T + s2];
       }
       for (int p = tid; p < N; p += kThreads) seq_len[p] = sc.old_l[s_anc[p]];
       __syncthreads();
@@ -536,155 +557,54 @@ __device__ void kv_remap_append(const KvArgs &kv, int b, int N, const int *s_anc
         return;
       }
     }
-    // push the freed blocks in ascending id order (staged: also list them in
-    // `delta`, whose counts are spent)
-    {
-      int top = top_old;
-      for (int w0 = 0; w0 < words; w0 += kThreads) {
-        const int w = w0 + tid;
-        unsigned fb = w < words ? sc.bits[w] : 0u;
-        int total;
-        int pos = top + block_excl_scan_i(__popc(fb), ks.ired, &total);
-        if (fb) sc.bits[w] = 0u;
-        while (fb) {
-          const int bit = __ffs(fb) - 1;
-          fb &= fb - 1;
-          if (pos < P) {
-            stack[pos] = lo_id + w * 32 + bit;
-            if (staged) sc.delta[pos - top_old] = lo_id + w * 32 + bit;
-          }
-          ++pos;
+    // push the freed blocks in ascending id order: staged, listed in `delta`
+    // (whose counts are spent) and written back as one range; else straight
+    // to the stack
+    int top = top_old;
+    for (int w0 = 0; w0 < words; w0 += kThreads) {
+      const int w = w0 + tid;
+      unsigned fb = w < words ? sc.bits[w] : 0u;
+      int total;
+      int pos = top + block_excl_scan_i(__popc(fb), ks.ired, &total);
+      if (fb) sc.bits[w] = 0u;
+      while (fb) {
+        const int bit = __ffs(fb) - 1;
+        fb &= fb - 1;
+        if (pos < P) {
+          if (staged) sc.delta[pos - top_old] = lo_id + w * 32 + bit;
+          else stack[pos] = lo_id + w * 32 + bit;
         }
-        top += total;
+        ++pos;
       }
-      if (top > P) {  // counts did not match the tables
-        fail();
-        return;
-      }
-      if (tid == 0) {
-        kv.free_top[b] = top;
-        ks.n_freed = top - top_old;
-      }
-      __syncthreads();
+      top += total;
+    }
+    if (top > P) {  // counts did not match the tables
+      fail();
+      return;
+    }
+    if (tid == 0) {
+      kv.free_top[b] = top;
+      ks.n_freed = top - top_old;
+    }
+    __syncthreads();
+    if (staged) {
+      for (int k = tid; k < top - top_old; k += kThreads) stack[top_old + k] = sc.delta[k];
     }
   }
 
-  if (warp_path) {
-    if (warp != 0) return;
-    // ---- warp 0: the append ------------------------------------------------
-    const int n_freed = ks.n_freed;
-    if (n_append <= 0) return;
-    const bool valid = lane < N;
-    const int src = valid ? (resampled ? s_anc[lane] : lane) : 0;
-    const int len = valid ? sc.old_l[src] : 0;
-    const int nb = valid ? ks.nb[src] : 0;
-    const int tail = valid ? ks.otail[src] : -1;
-    // a shared partial tail stays with its lowest particle; the others fork
-    const unsigned peers = __match_any_sync(0xffffffffu, tail >= 0 ? tail : -1 - lane);
-    const int fork = (tail >= 0 && __ffs(peers) - 1 != lane) ? 1 : 0;
-    const long long nb2 = valid ? (static_cast<long long>(len) + n_append + bs - 1) / bs : 0;
-    if (__any_sync(0xffffffffu, nb2 > T)) {
-      if (lane == 0) raise_status(ws.status, SMC_DEV_TABLE_OVERFLOW);
-      return;
-    }
-    const int grow = valid ? static_cast<int>(nb2) - nb : 0;
-    int n_forks, total_pops;
-    const int cidx = warp_excl_scan_i(fork, &n_forks);
-    const int off = warp_excl_scan_i(fork + grow, &total_pops);
-    const int top = top_old + n_freed;
-    if (total_pops > top) {
-      if (lane == 0) raise_status(ws.status, SMC_DEV_POOL_EXHAUSTED);
-      return;
-    }
-    auto pop = [&](int k) -> int {
-      if (k < n_freed) return sc.delta[n_freed - 1 - k];
-      const int j = k - n_freed;
-      return j < kStackPre ? sc.stk[j] : stack[top_old - 1 - j];
-    };
-    if (valid) {
-      int k = off;
-      if (fork) {
-        const int d = pop(k);
-        ++k;
-        if (in_pool(d)) {
-          int32_t *pair = kv.cow_pairs + (static_cast<size_t>(b) * N + cidx) * 2;
-          pair[0] = tail;
-          pair[1] = d;
-          tables[lane * T + nb - 1] = d;
-          kv.refcount[d] = 1;
-          atomicSub(&kv.refcount[tail], 1);
-        } else {
-          raise_status(ws.status, SMC_DEV_BAD_BLOCK);
-        }
-      }
-      for (int g = 0; g < grow; ++g) {
-        const int d = pop(k);
-        ++k;
-        if (in_pool(d)) {
-          tables[lane * T + nb + g] = d;
-          kv.refcount[d] = 1;
-        } else {
-          raise_status(ws.status, SMC_DEV_BAD_BLOCK);
-        }
-      }
-      seq_len[lane] = static_cast<int>(len + n_append);
-    }
-    if (lane == 0) {
-      kv.free_top[b] = top - total_pops;
-      kv.n_cow[b] = n_forks;
-    }
-    return;
-  }
-
-  if (n_append <= 0) return;
-  // ---- append by the whole CTA: particle i's table is now row src(i) ------
-  const bool valid = tid < N;
-  const int src = valid ? (resampled ? s_anc[tid] : tid) : 0;
-  int len = 0, nb = 0, tail = -1;
-  if (valid) {
-    len = sc.old_l[src];
-    nb = ks.nb[src];
-    tail = ks.otail[src];
-    ks.ntail[tid] = tail;
-  }
-  __syncthreads();
-  int fork = 0;
-  if (valid && tail >= 0) {
-    for (int i2 = 0; i2 < tid; ++i2) {
-      if (ks.ntail[i2] == tail) { fork = 1; break; }
-    }
-  }
-  const long long nb2 = valid ? (static_cast<long long>(len) + n_append + bs - 1) / bs : 0;
-  const bool overflow = __syncthreads_or(valid && nb2 > T) != 0;
-  const int grow = (valid && !overflow) ? static_cast<int>(nb2) - nb : 0;
-  // one scan of (forks, pops) packed in 64 bits: forks high, pops low
-  long long both_total;
-  const long long both = block_excl_scan_ll((static_cast<long long>(fork) << 32) | (fork + grow),
-                                            ks.ll, &both_total);
-  const int off = static_cast<int>(both & 0xffffffffll);
-  const int cidx = static_cast<int>(both >> 32);
-  const int total_pops = static_cast<int>(both_total & 0xffffffffll);
-  const int n_forks = static_cast<int>(both_total >> 32);
+  // ---- append: particle i's table is now row src(i) of the copy ----------
+  // (errors go to ks.flag: 1 bad block, 2 table overflow, 4 pool exhausted)
   const int n_freed = ks.n_freed;
   const int top = top_old + n_freed;
-  if (overflow) {
-    if (tid == 0) raise_status(ws.status, SMC_DEV_TABLE_OVERFLOW);
-    return;
-  }
-  if (total_pops > top) {
-    if (tid == 0) raise_status(ws.status, SMC_DEV_POOL_EXHAUSTED);
-    return;
-  }
-  // the k-th pop from the top: this remap's freed blocks first (the last
-  // pushed on top), then the stack as it was
   auto pop = [&](int k) -> int {
     if (!staged) return stack[top - 1 - k];
     if (k < n_freed) return sc.delta[n_freed - 1 - k];
     const int j = k - n_freed;
     return j < kStackPre ? sc.stk[j] : stack[top_old - 1 - j];
   };
-  if (valid) {
-    int k = off;
+  // particle p's part of the append; k = its first pop, cidx its fork's pair
+  auto append_one = [&](int p, int src, int len, int nb, int tail, int fork, int grow, int k,
+                        int cidx) {
     if (fork) {
       const int d = pop(k);
       ++k;
@@ -692,28 +612,101 @@ __device__ void kv_remap_append(const KvArgs &kv, int b, int N, const int *s_anc
         int32_t *pair = kv.cow_pairs + (static_cast<size_t>(b) * N + cidx) * 2;
         pair[0] = tail;
         pair[1] = d;
-        tables[tid * T + nb - 1] = d;
+        tables[p * T + nb - 1] = d;
         kv.refcount[d] = 1;
         atomicSub(&kv.refcount[tail], 1);
       } else {
-        raise_status(ws.status, SMC_DEV_BAD_BLOCK);
+        atomicOr(&ks.flag, 1);
       }
     }
     for (int g = 0; g < grow; ++g) {
       const int d = pop(k);
       ++k;
       if (in_pool(d)) {
-        tables[tid * T + nb + g] = d;
+        tables[p * T + nb + g] = d;
         kv.refcount[d] = 1;
       } else {
-        raise_status(ws.status, SMC_DEV_BAD_BLOCK);
+        atomicOr(&ks.flag, 1);
       }
     }
-    seq_len[tid] = static_cast<int>(len + n_append);
+    seq_len[p] = static_cast<int>(len + n_append);
+  };
+  const bool warp_append = N <= 32 && staged;
+  if (n_append > 0 && warp_append) {
+    // one warp: no CTA barrier
+    if (warp == 0) {
+      const bool valid = lane < N;
+      const int src = valid ? (resampled ? s_anc[lane] : lane) : 0;
+      const int len = valid ? sc.old_l[src] : 0;
+      const int nb = valid ? ks.nb[src] : 0;
+      const int tail = valid ? ks.otail[src] : -1;
+      // a shared partial tail stays with its lowest particle; the others fork
+      const unsigned peers = __match_any_sync(0xffffffffu, tail >= 0 ? tail : -1 - lane);
+      const int fork = (tail >= 0 && __ffs(peers) - 1 != lane) ? 1 : 0;
+      const long long nb2 = valid ? ceil_div_nonneg(static_cast<long long>(len) + n_append, bs) : 0;
+      int n_forks, total_pops;
+      const int grow = (valid && nb2 <= T) ? static_cast<int>(nb2) - nb : 0;
+      const int cidx = warp_excl_scan_i(fork, &n_forks);
+      const int off = warp_excl_scan_i(fork + grow, &total_pops);
+      if (__any_sync(0xffffffffu, nb2 > T)) {
+        if (lane == 0) ks.flag = 2;
+      } else if (total_pops > top) {
+        if (lane == 0) ks.flag = 4;
+      } else {
+        if (valid) append_one(lane, src, len, nb, tail, fork, grow, off, cidx);
+        if (lane == 0) {
+          kv.free_top[b] = top - total_pops;
+          kv.n_cow[b] = n_forks;
+        }
+      }
+    }
+    __syncthreads();
+  } else if (n_append > 0) {
+    const bool valid = tid < N;
+    const int src = valid ? (resampled ? s_anc[tid] : tid) : 0;
+    int len = 0, nb = 0, tail = -1;
+    if (valid) {
+      len = sc.old_l[src];
+      nb = ks.nb[src];
+      tail = ks.otail[src];
+      ks.ntail[tid] = tail;
+    }
+    __syncthreads();
+    int fork = 0;
+    if (valid && tail >= 0) {
+      for (int i2 = 0; i2 < tid; ++i2) {
+        if (ks.ntail[i2] == tail) { fork = 1; break; }
+      }
+    }
+    const long long nb2 = valid ? ceil_div_nonneg(static_cast<long long>(len) + n_append, bs) : 0;
+    const bool overflow = __syncthreads_or(valid && nb2 > T) != 0;
+    const int grow = (valid && !overflow) ? static_cast<int>(nb2) - nb : 0;
+    // one scan of (forks, pops) packed in 64 bits: forks high, pops low
+    long long both_total;
+    const long long both = block_excl_scan_ll((static_cast<long long>(fork) << 32) | (fork + grow),
+                                              ks.ll, &both_total);
+    const int off = static_cast<int>(both & 0xffffffffll);
+    const int cidx = static_cast<int>(both >> 32);
+    const int total_pops = static_cast<int>(both_total & 0xffffffffll);
+    const int n_forks = static_cast<int>(both_total >> 32);
+    if (overflow) {
+      if (tid == 0) ks.flag = 2;
+    } else if (total_pops > top) {
+      if (tid == 0) ks.flag = 4;
+    } else {
+      if (valid) append_one(tid, src, len, nb, tail, fork, grow, off, cidx);
+      if (tid == 0) {
+        kv.free_top[b] = top - total_pops;
+        kv.n_cow[b] = n_forks;
+      }
+    }
+    __syncthreads();
   }
-  if (tid == 0) {
-    kv.free_top[b] = top - total_pops;
-    kv.n_cow[b] = n_forks;
+  if (tid == 0 && n_append > 0) {
+    const int f = ks.flag;
+    if (f & 1) raise_status(ws.status, SMC_DEV_BAD_BLOCK);
+    if (f & 2) raise_status(ws.status, SMC_DEV_TABLE_OVERFLOW);
+    if (f & 4) raise_status(ws.status, SMC_DEV_POOL_EXHAUSTED);
   }
 }
 
