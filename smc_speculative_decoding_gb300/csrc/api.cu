@@ -38,8 +38,9 @@ size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws) 
   const size_t o_res = take(sizeof(RowResult) * rows);
   const size_t o_rej = take(sizeof(int32_t) * s.B);
   const size_t o_sst = take(sizeof(float4) * s.B);
-  const size_t o_spq = take(sizeof(float4) * s.B * nch * 2);
-  const size_t o_spr = take(sizeof(float2) * s.B * nch);
+  const size_t snch = static_cast<size_t>(sps_chunks_per_row(s.dtype, s.V));
+  const size_t o_spq = take(sizeof(float4) * s.B * snch * 2);
+  const size_t o_spr = take(sizeof(float2) * s.B * snch);
   const size_t o_kt = take(sizeof(int32_t) * static_cast<size_t>(s.B) * s.N * (T > 0 ? T : 0));
   const size_t o_kl = take(sizeof(int32_t) * static_cast<size_t>(s.B) * s.N);
   if (ws && base) {

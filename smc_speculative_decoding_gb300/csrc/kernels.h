@@ -50,8 +50,8 @@ struct Workspace {
   RowResult *results;        // [rows]
   int32_t *sps_rej;          // [B]  first rejected position, -1 if none
   float4 *sps_stats;         // [B]  precise (lse_p hi, lo, lse_q hi, lo) of row j
-  float4 *sps_part_pq;       // [B * nch * 2]  per-chunk stats of rows p_j, q_j
-  float2 *sps_part_r;        // [B * nch]      per-chunk residual mass
+  float4 *sps_part_pq;       // [B * snch * 2] per-chunk stats of rows p_j, q_j (SpS chunks)
+  float2 *sps_part_r;        // [B * snch]     per-chunk residual mass
   int32_t *kv_old_tables;    // [B * N * T]
   int32_t *kv_old_len;       // [B * N]
   size_t zero_bytes;         // bytes from the start that must start at zero
@@ -70,6 +70,7 @@ struct Shape {
 // Elements per chunk of the row reductions for a dtype.
 int chunk_elems(int dtype);
 int chunks_per_row(int dtype, int V);
+int sps_chunks_per_row(int dtype, int V);  // chunks of the SpS residual kernels
 
 // Lays out `base` for the shape; returns the bytes needed (base may be null).
 size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws);

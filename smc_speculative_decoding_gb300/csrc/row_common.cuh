@@ -21,29 +21,30 @@ template <typename T> struct ChunkGeom {
 // requires a 16-byte aligned base and n_valid a multiple of the vector width.
 // Element x[i*EPV + e] is logit (i*kThreads + tid)*EPV + e of the chunk (VEC)
 // or logit i*kThreads + tid (scalar path); order does not matter to callers.
-template <typename T, bool VEC>
+// NV: 16-byte vectors per thread (the chunk holds kThreads * NV of them).
+template <typename T, bool VEC, int NV = kNV>
 __device__ __forceinline__ void load_chunk(const char *chunk_base, int n_valid,
-                                           float (&x)[ChunkGeom<T>::kEPT]) {
+                                           float (&x)[NV * LogitTraits<T>::kPerVec]) {
   using Tr = LogitTraits<T>;
   constexpr int EPV = ChunkGeom<T>::kEPV;
   const int tid = threadIdx.x;
   if (VEC) {
     const uint4 *base = reinterpret_cast<const uint4 *>(chunk_base);
-    uint4 v[kNV];
+    uint4 v[NV];
 #pragma unroll
-    for (int i = 0; i < kNV; ++i) {
+    for (int i = 0; i < NV; ++i) {
       const int vi = i * kThreads + tid;
       v[i] = vi * EPV < n_valid ? ld_stream16(base + vi) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
-    for (int i = 0; i < kNV; ++i) {
+    for (int i = 0; i < NV; ++i) {
       const bool ok = (i * kThreads + tid) * EPV < n_valid;
 #pragma unroll
       for (int e = 0; e < EPV; ++e) x[i * EPV + e] = ok ? Tr::at(v[i], e) : kNegInf;
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < ChunkGeom<T>::kEPT; ++i) {
+    for (int i = 0; i < NV * EPV; ++i) {
       const int idx = i * kThreads + tid;
       x[i] = idx < n_valid ? Tr::scalar(chunk_base, idx) : kNegInf;
     }
@@ -203,6 +204,72 @@ struct BonusPairSum {
     e.lo += l0;
     o.lo += l1;
     return ff_add(ff_norm(e), ff_norm(o));
+  }
+};
+
+// ---------------------------------------------------------------------------
+// exp(s x - L) for two logits at a time on the packed fp32x2 pipes, for a
+// scale s > 0 and a float-float L shared by both (a row's log-sum-exp, so
+// that the result is a probability): the method of BonusPairSum::add with
+// the offset L in place of a float reference.  s x is taken exactly
+// (two-product), s x - L.hi exactly (two-sum), L.lo joins the tail, y =
+// (s x - L) log2(e) as a float pair, and 2^y = 2^n 2^(j/64) 2^r, about 3e-10
+// relative.  The result is a float pair per logit, head and tail packed,
+// unnormalised.  Logits with s x - L below -59 (also -inf and NaN) are raised
+// to that bound, so they weigh about e^-59 instead of less: masking a logit
+// to 0 is the caller's.
+// ---------------------------------------------------------------------------
+struct ShiftedExp {
+  unsigned long long s2, ns2, nlh, nll;
+  float lbx;
+  bool s1;
+
+  __device__ __forceinline__ void init(float s, ff big_l) {
+    s1 = s == 1.f;
+    s2 = f2dup(s);
+    ns2 = f2dup(-s);
+    nlh = f2dup(-big_l.hi);
+    nll = f2dup(-big_l.lo);
+    lbx = (big_l.hi - 59.f) / s;
+  }
+
+  __device__ __forceinline__ void eval(float x0, float x1, const float *th, const float *tl,
+                                       unsigned long long *out_h, unsigned long long *out_l) const {
+    constexpr float kShift = 12582912.f;  // 1.5 * 2^23: rounds 64 y into the low bits
+    const unsigned long long X = f2pack(fmaxf(x0, lbx), fmaxf(x1, lbx));
+    // s x as SH - NSE, exactly
+    unsigned long long SH = X, NSE = 0ull;
+    if (!s1) {
+      SH = mul2(s2, X);
+      NSE = fma2(ns2, X, SH);
+    }
+    // d = s x - L as DH + DL: two-sum of SH and -L.hi, then the tails
+    const unsigned long long DH = add2(SH, nlh);
+    const unsigned long long BB = sub2(DH, SH);
+    const unsigned long long DE = add2(sub2(SH, sub2(DH, BB)), sub2(nlh, BB));
+    const unsigned long long DL = add2(sub2(DE, NSE), nll);
+    // y = d log2(e) as YH - NYL
+    const unsigned long long YH = mul2(DH, f2dup(kLog2eHi));
+    const unsigned long long NYE = fma2(DH, f2dup(-kLog2eHi), YH);
+    const unsigned long long NYL =
+        fma2(DH, f2dup(-kLog2eLo), fma2(DL, f2dup(-kLog2eHi), NYE));
+    // y = ki/64 + r
+    const unsigned long long T = fma2(YH, f2dup(64.f), f2dup(kShift));
+    const unsigned long long K = sub2(T, f2dup(kShift));
+    const unsigned long long R = sub2(fma2(K, f2dup(-0.015625f), YH), NYL);
+    unsigned long long Q = fma2(R, f2dup(kC3), f2dup(kC2));
+    Q = fma2(R, Q, f2dup(kC1Lo));
+    const unsigned long long P = fma2(R, f2dup(kC1Hi), mul2(R, Q));  // 2^r - 1
+    float t0, t1;
+    f2unpack(T, t0, t1);
+    const int k0 = __float_as_int(t0) - 0x4B400000, k1 = __float_as_int(t1) - 0x4B400000;
+    const int j0 = k0 & 63, j1 = k1 & 63;
+    const unsigned long long TH = f2pack(th[j0], th[j1]), TL = f2pack(tl[j0], tl[j1]);
+    const unsigned long long LO = fma2(TH, P, fma2(TL, P, TL));  // 2^(j/64) 2^r - head
+    const unsigned long long SC = f2pack(__int_as_float(((k0 >> 6) + 127) << 23),
+                                         __int_as_float(((k1 >> 6) + 127) << 23));
+    *out_h = mul2(TH, SC);
+    *out_l = mul2(LO, SC);
   }
 };
 

@@ -22,6 +22,22 @@
 
 namespace smcsd {
 
+// The residual kernels' chunk: kSpsNV 16-byte vectors per thread (half the
+// row kernels' chunk), so that both rows' chunks fit in few registers and
+// four CTAs share an SM.
+constexpr int kSpsNV = 2;
+template <typename T> struct SpsGeom {
+  static constexpr int kEPV = LogitTraits<T>::kPerVec;
+  static constexpr int kEPT = kSpsNV * kEPV;
+  static constexpr int kCH = kThreads * kEPT;
+  static constexpr int kESZ = sizeof(T) == 4 ? 4 : 2;
+};
+
+int sps_chunks_per_row(int dtype, int V) {
+  const int ch = dtype == SMC_BF16 ? SpsGeom<bf16_tag>::kCH : SpsGeom<float>::kCH;
+  return (V + ch - 1) / ch;
+}
+
 struct SpsArgs {
   const char *target, *draft;
   int B, K, V, nch;
@@ -51,17 +67,59 @@ __device__ __forceinline__ ff prob_term_s(float x, float s, ff big_l, const floa
   return accurate_exp(d.hi, d.lo + (sx.lo - big_l.lo), tab);
 }
 
+// One row's chunk sum of exp(s (x - mc)) over the kept logits x[], mc their
+// maximum: two logits at a time on the packed pipes (BonusPairSum), or, when
+// mc is too large for the pair path's lower bound, by scalar terms.
+template <typename T, int EPT>
+__device__ __forceinline__ ff chunk_weight_sum(const float (&x)[EPT], float mc, float s,
+                                               const float *th, const float *tl,
+                                               const float2 *tab) {
+  constexpr float kInf = -kNegInf;
+  if (!(mc > kNegInf && mc < kInf)) return {0.f, 0.f};
+  BonusPairSum ps;
+  if (ps.init(mc, s, 40.f / s)) {
+    const bool fast = sizeof(T) == 2 && BonusPairSum::fast_diff_ok(mc, 40.f / s);
+    if (s == 1.f) {
+      if (fast) {
+#pragma unroll
+        for (int e = 0; e < EPT; e += 2) ps.add<true, true>(x[e], x[e + 1], th, tl);
+      } else {
+#pragma unroll
+        for (int e = 0; e < EPT; e += 2) ps.add<true, false>(x[e], x[e + 1], th, tl);
+      }
+    } else {
+      if (fast) {
+#pragma unroll
+        for (int e = 0; e < EPT; e += 2) ps.add<false, true>(x[e], x[e + 1], th, tl);
+      } else {
+#pragma unroll
+        for (int e = 0; e < EPT; e += 2) ps.add<false, false>(x[e], x[e + 1], th, tl);
+      }
+    }
+    return ps.total();
+  }
+  ff S0{0.f, 0.f}, S1{0.f, 0.f};
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    if (e & 1) ff_accum(S1, weight_term(x[e], mc, s, tab));
+    else ff_accum(S0, weight_term(x[e], mc, s, tab));
+  }
+  return ff_add(ff_norm(S0), ff_norm(S1));
+}
+
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kThreads) sps_stats_kernel(const SpsArgs a) {
-  using G = ChunkGeom<T>;
+  using G = SpsGeom<T>;
   __shared__ float s_red[2 * kWarps];
   __shared__ float2 s_ff[kWarps];
   __shared__ float2 s_tab[64];
+  __shared__ float s_th[64], s_tl[64];
   __shared__ int s_last;
   const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
   const int jr = a.ws.sps_rej[b];
   if (jr < 0) return;
   stage_exp2_table(s_tab);
+  stage_exp2_split(s_th, s_tl);
   const int64_t c0 = static_cast<int64_t>(c) * G::kCH;
   const int n_valid = static_cast<int>(min(static_cast<int64_t>(G::kCH), a.V - c0));
   const char *rows[2] = {
@@ -69,25 +127,26 @@ __global__ void __launch_bounds__(kThreads) sps_stats_kernel(const SpsArgs a) {
       a.draft + (static_cast<size_t>(b) * a.K + jr) * static_cast<size_t>(a.V) * G::kESZ};
   float thr[2];
   sps_thresholds(a, b, jr, &thr[0], &thr[1]);
+  // both rows' chunks in flight at once; logits outside a nucleus weigh 0
+  float x[2][G::kEPT];
+  load_chunk<T, VEC, kSpsNV>(rows[0] + c0 * G::kESZ, n_valid, x[0]);
+  load_chunk<T, VEC, kSpsNV>(rows[1] + c0 * G::kESZ, n_valid, x[1]);
+  float m[2] = {kNegInf, kNegInf};
+#pragma unroll
   for (int r = 0; r < 2; ++r) {
-    float x[G::kEPT];
-    load_chunk<T, VEC>(rows[r] + c0 * G::kESZ, n_valid, x);
-    float m = kNegInf;
 #pragma unroll
-    for (int e = 0; e < G::kEPT; ++e) m = fmaxf(m, x[e]);
-    const float mc = block_max(m, s_red);
-    // two running sums, so that consecutive additions do not wait on each other
-    ff S0{0.f, 0.f}, S1{0.f, 0.f};
-    if (mc > kNegInf && mc < -kNegInf) {
-#pragma unroll
-      for (int e = 0; e < G::kEPT; ++e) {
-        if (x[e] >= thr[r]) {
-          if (e & 1) ff_accum(S1, weight_term(x[e], mc, a.tscale, s_tab));
-          else ff_accum(S0, weight_term(x[e], mc, a.tscale, s_tab));
-        }
-      }
+    for (int e = 0; e < G::kEPT; ++e) {
+      if (!(x[r][e] >= thr[r])) x[r][e] = kNegInf;
+      m[r] = fmaxf(m[r], x[r][e]);
     }
-    const ff S = block_ff_sum(ff_add(ff_norm(S0), ff_norm(S1)), s_ff);
+  }
+  const float mcp = block_max(m[0], s_red);
+  const float mcq = block_max(m[1], s_red);  // (the table is staged: block_max has barriers)
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const float mc = r == 0 ? mcp : mcq;
+    const ff S = block_ff_sum(chunk_weight_sum<T, G::kEPT>(x[r], mc, a.tscale, s_th, s_tl, s_tab),
+                              s_ff);
     if (tid == 0) a.ws.sps_part_pq[(static_cast<size_t>(b) * a.nch + c) * 2 + r] = make_float4(mc, S.hi, S.lo, 0.f);
   }
   if (tid == 0) {
@@ -142,10 +201,11 @@ __device__ __forceinline__ ff residual_of(float xp, float xq, float s, ff lp, ff
 
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kThreads) sps_residual_kernel(const SpsArgs a) {
-  using G = ChunkGeom<T>;
+  using G = SpsGeom<T>;
   using Tr = LogitTraits<T>;
   __shared__ float2 s_ff[kWarps];
   __shared__ float2 s_tab[64];
+  __shared__ float s_th[64], s_tl[64];
   __shared__ int s_int[2 * kWarps];
   __shared__ int s_last;
   __shared__ int s_sel;
@@ -156,6 +216,7 @@ __global__ void __launch_bounds__(kThreads) sps_residual_kernel(const SpsArgs a)
   const int jr = a.ws.sps_rej[b];
   if (jr < 0) return;
   stage_exp2_table(s_tab);
+  stage_exp2_split(s_th, s_tl);
   const float4 st = a.ws.sps_stats[b];
   const ff lp{st.x, st.y}, lq{st.z, st.w};
   float thr_p, thr_q;
@@ -165,16 +226,60 @@ __global__ void __launch_bounds__(kThreads) sps_residual_kernel(const SpsArgs a)
   const char *prow = a.target + (static_cast<size_t>(b) * (a.K + 1) + jr) * static_cast<size_t>(a.V) * G::kESZ;
   const char *qrow = a.draft + (static_cast<size_t>(b) * a.K + jr) * static_cast<size_t>(a.V) * G::kESZ;
   float xp[G::kEPT], xq[G::kEPT];
-  load_chunk<T, VEC>(prow + c0 * G::kESZ, n_valid, xp);
-  load_chunk<T, VEC>(qrow + c0 * G::kESZ, n_valid, xq);
-  __syncthreads();  // table staged
+  load_chunk<T, VEC, kSpsNV>(prow + c0 * G::kESZ, n_valid, xp);
+  load_chunk<T, VEC, kSpsNV>(qrow + c0 * G::kESZ, n_valid, xq);
+  __syncthreads();  // tables staged
+  // p and q two logits at a time on the packed pipes, and the residual
+  // max(0, p - q) of each in float-float as residual_of takes it: logits
+  // outside a nucleus are set to -inf first (they then weigh about e^-59
+  // instead of 0, far below what can move a draw); the running sums start at
+  // 2, above any residual (<= 1), so the fast two-sum is exact at every
+  // addition
+  ShiftedExp ep, eq;
+  ep.init(a.tscale, lp);
+  eq.init(a.tscale, lq);
+  const bool live = lp.hi > kNegInf && lq.hi > kNegInf;
   ff R0{0.f, 0.f}, R1{0.f, 0.f};
+  if (live) {
+    unsigned long long acc = f2dup(2.f), alo = 0ull;
 #pragma unroll
-  for (int e = 0; e < G::kEPT; ++e) {
-    const ff d = residual_of(xp[e], xq[e], a.tscale, lp, lq, thr_p, thr_q, s_tab);
-    if (d.hi > 0.f) {
-      if (e & 1) ff_accum(R1, d);
-      else ff_accum(R0, d);
+    for (int e = 0; e < G::kEPT; e += 2) {
+      unsigned long long PH, PL, QH, QL;
+      ep.eval(xp[e] >= thr_p ? xp[e] : kNegInf, xp[e + 1] >= thr_p ? xp[e + 1] : kNegInf, s_th,
+              s_tl, &PH, &PL);
+      eq.eval(xq[e] >= thr_q ? xq[e] : kNegInf, xq[e + 1] >= thr_q ? xq[e + 1] : kNegInf, s_th,
+              s_tl, &QH, &QL);
+      // d = p - q: two-sum of the heads, the tails after, then normalised
+      const unsigned long long DH = sub2(PH, QH);
+      const unsigned long long BB = sub2(DH, PH);
+      const unsigned long long DE = sub2(sub2(PH, sub2(DH, BB)), add2(QH, BB));
+      const unsigned long long DL = add2(DE, sub2(PL, QL));
+      const unsigned long long NH = add2(DH, DL);
+      const unsigned long long NL = sub2(DL, sub2(NH, DH));
+      float h0, h1, l0, l1;
+      f2unpack(NH, h0, h1);
+      f2unpack(NL, l0, l1);
+      const unsigned long long RH = f2pack(h0 > 0.f ? h0 : 0.f, h1 > 0.f ? h1 : 0.f);
+      const unsigned long long RL = f2pack(h0 > 0.f ? l0 : 0.f, h1 > 0.f ? l1 : 0.f);
+      const unsigned long long S2 = add2(acc, RH);
+      alo = add2(alo, add2(sub2(RH, sub2(S2, acc)), RL));
+      acc = S2;
+    }
+    float a0, a1, o0, o1;
+    f2unpack(acc, a0, a1);
+    f2unpack(alo, o0, o1);
+    R0 = two_sum(a0, -2.f);
+    R1 = two_sum(a1, -2.f);
+    R0.lo += o0;
+    R1.lo += o1;
+  } else {
+#pragma unroll
+    for (int e = 0; e < G::kEPT; ++e) {
+      const ff d = residual_of(xp[e], xq[e], a.tscale, lp, lq, thr_p, thr_q, s_tab);
+      if (d.hi > 0.f) {
+        if (e & 1) ff_accum(R1, d);
+        else ff_accum(R0, d);
+      }
     }
   }
   const ff R = block_ff_sum(ff_add(ff_norm(R0), ff_norm(R1)), s_ff);
@@ -274,7 +379,7 @@ cudaError_t launch_sps_residual(const Shape &s, const void *target, const void *
   a.target = static_cast<const char *>(target);
   a.draft = static_cast<const char *>(draft);
   a.B = s.B; a.K = s.K; a.V = s.V;
-  a.nch = chunks_per_row(s.dtype, s.V);
+  a.nch = sps_chunks_per_row(s.dtype, s.V);
   a.tscale = s.tscale;
   a.topp = s.top_p < 1.f;
   a.seed = s.seed; a.step = s.step;
