@@ -1200,9 +1200,11 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rpp = 2 * a.K + 1;
 
-  // launched with programmatic dependent launch: nothing before this line
-  // touches global memory that an earlier kernel may still write
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Launched with programmatic dependent launch.  The producer reads only the
+  // logits and claims work from the queue counters, which no kernel of this
+  // library writes while a dependent may run, so it starts its copies at
+  // once; the consumers wait (griddepcontrol.wait below) before they write
+  // the partials that the previous step's kernels read.
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -1217,9 +1219,11 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
   // ---- producer warp -----------------------------------------------------------
   // Work comes from two queues: items of G chunks of the non-bonus rows, and
   // single chunks of the bonus rows (whose weights cost far more to compute).
-  // The producer interleaves them in the proportion of the whole step (2K
-  // non-bonus chunks per bonus chunk), so that every CTA, all through the
-  // kernel, mixes streaming-bound and arithmetic-bound chunks evenly.
+  // The producer interleaves them in about the proportion of the whole step
+  // (2K non-bonus chunks per bonus chunk), so that every CTA mixes
+  // streaming-bound and arithmetic-bound chunks evenly; bonus chunks are
+  // taken 8/7 as often, so that their queue drains before the other and the
+  // kernel ends on cheap chunks.
   if (warp == kConsumerWarps) {
     if (lane == 0) {
       const int rest = rpp - 1;  // non-bonus rows per particle
@@ -1242,7 +1246,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
           have = false;
           if (fast_done && bonus_done) break;
           const bool take_bonus =
-              !bonus_done && (fast_done || n_bonus * 2 * a.K < fast_chunks);
+              !bonus_done && (fast_done || n_bonus * 2 * a.K * 7 < fast_chunks * 8);
           if (take_bonus) {
             const unsigned id = next_bonus;
             if (id >= static_cast<unsigned>(sa.n_bonus_items)) { bonus_done = true; continue; }
@@ -1311,6 +1315,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
   }
 
   // ---- consumer warps --------------------------------------------------------
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const float l2s = a.tscale * kLog2e;  // log2(e) of the scaled logits
   float m_t = kNegInf, s_t = 0.f;  // this lane's running (max, sum exp) over the item
   for (int i = 0;; ++i) {
