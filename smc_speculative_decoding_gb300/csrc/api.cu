@@ -29,7 +29,7 @@ size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws) 
   const size_t o_sa = take(sizeof(unsigned) * s.B);
   const size_t o_sb = take(sizeof(unsigned) * s.B);
   const size_t o_bm = take(sizeof(unsigned) * s.B * words);
-  const size_t o_wc = take(sizeof(unsigned) * 4);
+  const size_t o_wc = take(sizeof(unsigned) * 8);
   const size_t zero_bytes = off;
   // scratch that every call overwrites before reading
   const size_t o_part = take(sizeof(RowPartial) * rows * nch);
@@ -54,6 +54,8 @@ size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws) 
     ws->kv_bitmap = reinterpret_cast<unsigned *>(p + o_bm);
     ws->work_counter = reinterpret_cast<unsigned *>(p + o_wc);
     ws->exit_counter = ws->work_counter + 2;
+    ws->rows_done = ws->work_counter + 3;
+    ws->tail_ticket = ws->work_counter + 4;
     ws->partials = reinterpret_cast<RowPartial *>(p + o_part);
     ws->item_part = reinterpret_cast<float2 *>(p + o_ip);
     ws->bonus_part = reinterpret_cast<int4 *>(p + o_bp);

@@ -488,6 +488,17 @@ __device__ __forceinline__ void named_bar_sync(int id, int n) {
 __device__ __forceinline__ void add_release_gpu(unsigned *p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// atomicAdd on a shared counter with acquire-release semantics at CTA scope:
+// the calling thread's earlier writes (global ones too) happen before any
+// later add's observer, and this add sees what earlier adders published.
+__device__ __forceinline__ unsigned atom_add_acq_rel_cta(unsigned *p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "r"(static_cast<unsigned>(__cvta_generic_to_shared(p))), "r"(v)
+               : "memory");
+  return old;
+}
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

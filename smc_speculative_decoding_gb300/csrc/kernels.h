@@ -43,6 +43,8 @@ struct Workspace {
   unsigned *kv_bitmap;       // [B * ceil(P/32)]
   unsigned *work_counter;    // [2]  next fast-row item, next bonus chunk (streaming kernel)
   unsigned *exit_counter;    // [1]  CTAs of the streaming kernel that finished
+  unsigned *rows_done;       // [1]  streaming CTAs whose partials are published (plain step)
+  unsigned *tail_ticket;     // [1]  prompt CTAs past their waits (plain step)
   RowPartial *partials;      // [rows * nch]  (per-chunk kernel)
   float2 *item_part;         // [rows * nch * 8]  (m, s) per work item and warp (streaming kernel)
   int4 *bonus_part;          // [B * N * nch * 8] (ref bits, fixed-point sum lo, hi, -)

@@ -1165,6 +1165,8 @@ struct StreamArgs {
   int n_items1;       // R1 * ipr: the queue's G-chunk items come first
   int n_fast_items;   // all non-bonus items
   int n_bonus_items;  // bonus rows * snch (one chunk per item)
+  int signal_rows;    // nonzero: each CTA adds 1 to ws.rows_done once its partials are out
+  int row_grid;       // CTAs of the streaming kernel
 };
 
 // Partial slots (work items) of non-bonus row rf.
@@ -1195,7 +1197,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
   uint64_t *empty = full + kStages;
   SlotMeta *meta = reinterpret_cast<SlotMeta *>(empty + kStages);
   __shared__ float s_th[64], s_tl[64];
-  __shared__ int s_exited;
+  __shared__ unsigned s_exited;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rpp = 2 * a.K + 1;
@@ -1211,7 +1213,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
       mbar_init(&empty[s], kConsumerWarps);
     }
     mbar_init_fence();
-    s_exited = 0;
+    s_exited = 0u;
   }
   stage_exp2_split(s_th, s_tl);
   __syncthreads();  // the only CTA-wide barrier
@@ -1285,6 +1287,11 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
           SlotMeta &mt = meta[slot];
           mt.row = -1; mt.part = 0; mt.j = 0; mt.chunk = 0; mt.n = 0; mt.flags = kSlotEnd;
           mbar_arrive(&full[slot]);
+          // the queues are drained: the dependent kernel may launch, so that its
+          // CTAs take SMs as this kernel's CTAs leave them.  (After this grid's
+          // own wait, so that it never launches before the previous step ends.)
+          asm volatile("griddepcontrol.wait;" ::: "memory");
+          asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
           // the queues are drained, so the step's tail comes within a few
           // microseconds: bring a prompt's KV state into L2 for it
           if (a.mode == 0 && a.use_kv) {
@@ -1467,9 +1474,13 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
     }
   }
 
-  // ---- consumer exit: let the finish kernel launch; reset the work counters ---
+  // ---- consumer exit: publish the CTA's partials; reset the work counters ----
+  // Each warp's lane 0 wrote the warp's partials; the CTA-scope acquire-release
+  // adds order them before the last warp's gpu-scope release of rows_done,
+  // which the plain step's particle kernel waits on.
   if (lane == 0) {
-    if (atomicAdd(&s_exited, 1) == kConsumerWarps - 1) {
+    if (atom_add_acq_rel_cta(&s_exited, 1u) == kConsumerWarps - 1) {
+      if (sa.signal_rows) add_release_gpu(a.ws.rows_done, 1u);
       asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
       __threadfence();
       if (atomicAdd(a.ws.exit_counter, 1u) == gridDim.x - 1) {
@@ -1926,7 +1937,17 @@ __global__ void __launch_bounds__(kThreads) particle_kernel(const StreamArgs sa)
     lw0 = __ldcg(a.out.log_weights + part);
     if (a.potential) pot = __ldcg(a.potential + part);
   }
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // every streaming CTA's partials are out once rows_done reaches the grid
+  // (bounded; this grid launches only after every streaming CTA has started)
+  __shared__ int s_rows_ok;
+  if (threadIdx.x == 0) {
+    s_rows_ok = wait_count(a.ws.rows_done, static_cast<unsigned>(sa.row_grid), kCountWaitLimit);
+  }
+  __syncthreads();
+  if (!s_rows_ok) {
+    if (threadIdx.x == 0) raise_status(a.ws.status, SMC_DEV_TIMEOUT);
+    return;
+  }
 
   if (warp == 0) {
     float fM = kNegInf, fS = 0.f;
@@ -2030,6 +2051,12 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const StepArgs a, i
   if (tid == 0) {
     a.ws.weights_done[b] = 0u;
     a.ws.bonus_done[b] = 0u;
+    // the last prompt CTA past its waits: every particle CTA has passed its
+    // wait on rows_done, which can start again from 0
+    if (atomicAdd(a.ws.tail_ticket, 1u) == gridDim.x - 1) {
+      *a.ws.rows_done = 0u;
+      *a.ws.tail_ticket = 0u;
+    }
   }
 }
 
@@ -2254,6 +2281,8 @@ static cudaError_t launch_stream(const StepArgs &a, long long rows, cudaStream_t
   sa.n_bonus_items = static_cast<int>(parts * sa.snch);
   const long long n_items = static_cast<long long>(sa.n_fast_items) + sa.n_bonus_items;
   const long long grid = grid_max < n_items ? grid_max : n_items;
+  sa.signal_rows = fuse_tail ? 1 : 0;
+  sa.row_grid = static_cast<int>(grid);
   if (g_rows_begin && (e = cudaEventRecord(g_rows_begin, stream)) != cudaSuccess) return e;
   {
     // programmatic dependent launch: when the kernel before it in the stream
