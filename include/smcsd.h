@@ -158,6 +158,21 @@ int32_t smc_device_status(void *workspace, int32_t clear, int32_t *out_bits,
  * exactly one of the two is NULL. */
 int32_t smc_set_row_timing_events(void *rows_begin, void *rows_end);
 
+/* Measurement hook with no counterpart in the pages: a device-side clock of
+ * step starts.  When `stamps` is not NULL, every later call's streaming row
+ * kernel takes k = (*counter)++ once the kernel before it in the stream has
+ * finished, and writes the GPU's global nanosecond timer to stamps[k] if
+ * k < capacity.  So consecutive stamps of back-to-back steps differ by the
+ * step's period, measured without putting any stream operation between the
+ * steps (an event recorded between two steps delays the second one's
+ * launch).  `stamps` (uint64 [capacity]) and `counter` (one uint32, set to 0
+ * by the caller) are device memory owned by the caller; NULL turns the hook
+ * off.  Only the streaming row kernel writes stamps (rows 16-byte aligned
+ * with V * element size a multiple of 16).  One process-wide setting; set it
+ * from the thread that makes the calls.  Returns SMC_OK, or SMC_ERR_ARG when
+ * `stamps` is not NULL and `counter` is NULL or capacity < 1. */
+int32_t smc_set_step_clock(uint64_t *stamps, uint32_t *counter, int32_t capacity);
+
 /* One SMC-SD step for B prompts x N particles ([SMC] section 2).
  *
  * target_logits [B, N, K+1, V]  row k < K scores drafted token k, row K is the

@@ -73,6 +73,7 @@ _SIGS = {
                       [ctypes.POINTER(smc_step_opts), ctypes.c_void_p, ctypes.c_size_t,
                        ctypes.c_void_p]),
     "smc_set_row_timing_events": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_void_p]),
+    "smc_set_step_clock": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]),
     "smc_step_ex": (ctypes.c_int32, [ctypes.POINTER(smc_params), ctypes.POINTER(smc_step_opts)] +
                     [ctypes.c_void_p] * 8 +
                     [ctypes.POINTER(smc_kv), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
@@ -201,6 +202,22 @@ def smc_set_row_timing_events(rows_begin=None, rows_end=None):
         return ctypes.c_void_p(ev.cuda_event)
     _check("smc_set_row_timing_events",
            lib().smc_set_row_timing_events(handle(rows_begin), handle(rows_end)))
+
+
+def smc_set_step_clock(stamps=None, counter=None):
+    """Device-side step clock: `stamps` (int64 CUDA tensor) receives the GPU
+    timer (ns) as each later step's row pass starts, at index counter[0]++
+    (`counter`: int32 CUDA tensor of one element, zeroed by the caller).
+    None turns it off."""
+    if stamps is None:
+        _check("smc_set_step_clock", lib().smc_set_step_clock(None, None, 0))
+        return
+    if not (stamps.is_cuda and stamps.dtype == torch.int64 and counter is not None
+            and counter.is_cuda and counter.dtype == torch.int32 and counter.numel() >= 1):
+        raise TypeError("stamps: int64 CUDA tensor; counter: int32 CUDA tensor")
+    _check("smc_set_step_clock",
+           lib().smc_set_step_clock(ctypes.c_void_p(stamps.data_ptr()),
+                                    ctypes.c_void_p(counter.data_ptr()), stamps.numel()))
 
 
 def status_names(bits):

@@ -184,6 +184,12 @@ int32_t smc_set_row_timing_events(void *rows_begin, void *rows_end) {
   return SMC_OK;
 }
 
+int32_t smc_set_step_clock(uint64_t *stamps, uint32_t *counter, int32_t capacity) {
+  if (stamps && (!counter || capacity < 1)) return SMC_ERR_ARG;
+  set_step_clock(reinterpret_cast<unsigned long long *>(stamps), counter, stamps ? capacity : 0);
+  return SMC_OK;
+}
+
 }  // extern "C"
 
 namespace smcsd {

@@ -476,6 +476,13 @@ __device__ __forceinline__ void prefetch_l2(const void *p, size_t bytes) {
   }
 }
 
+// The GPU's global timer, in nanoseconds.
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 // A named CTA barrier (id 1..15) over `n` threads, a multiple of 32: only
 // the warps that take part wait for one another.
 __device__ __forceinline__ void named_bar_sync(int id, int n) {

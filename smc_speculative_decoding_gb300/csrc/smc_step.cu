@@ -1167,6 +1167,9 @@ struct StreamArgs {
   int n_bonus_items;  // bonus rows * snch (one chunk per item)
   int signal_rows;    // nonzero: each CTA adds 1 to ws.rows_done once its partials are out
   int row_grid;       // CTAs of the streaming kernel
+  unsigned long long *clk;  // step-clock hook (smc_set_step_clock), or null
+  unsigned *clk_ctr;
+  int clk_cap;
 };
 
 // Partial slots (work items) of non-bonus row rf.
@@ -1323,6 +1326,10 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
 
   // ---- consumer warps --------------------------------------------------------
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (sa.clk && blockIdx.x == 0 && tid == 0) {  // the step-clock hook: this step starts
+    const unsigned k = atomicAdd(sa.clk_ctr, 1u);
+    if (k < static_cast<unsigned>(sa.clk_cap)) sa.clk[k] = global_timer_ns();
+  }
   const float l2s = a.tscale * kLog2e;  // log2(e) of the scaled logits
   float m_t = kNegInf, s_t = 0.f;  // this lane's running (max, sum exp) over the item
   for (int i = 0;; ++i) {
@@ -2157,6 +2164,15 @@ static cudaError_t stream_geometry(int *sms, int *per_sm) {
 }
 
 static cudaEvent_t g_rows_begin = nullptr, g_rows_end = nullptr;
+static unsigned long long *g_clk = nullptr;
+static unsigned *g_clk_ctr = nullptr;
+static int g_clk_cap = 0;
+
+void set_step_clock(unsigned long long *stamps, unsigned *counter, int capacity) {
+  g_clk = stamps;
+  g_clk_ctr = counter;
+  g_clk_cap = capacity;
+}
 
 void set_row_timing_events(cudaEvent_t begin, cudaEvent_t end) {
   g_rows_begin = begin;
@@ -2283,6 +2299,9 @@ static cudaError_t launch_stream(const StepArgs &a, long long rows, cudaStream_t
   const long long grid = grid_max < n_items ? grid_max : n_items;
   sa.signal_rows = fuse_tail ? 1 : 0;
   sa.row_grid = static_cast<int>(grid);
+  sa.clk = g_clk;
+  sa.clk_ctr = g_clk_ctr;
+  sa.clk_cap = g_clk_cap;
   if (g_rows_begin && (e = cudaEventRecord(g_rows_begin, stream)) != cudaSuccess) return e;
   {
     // programmatic dependent launch: when the kernel before it in the stream

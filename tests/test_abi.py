@@ -152,6 +152,11 @@ def test_host_validation_without_gpu(lib):
     assert lib.smc_set_row_timing_events(fake, None) == -1
     assert lib.smc_set_row_timing_events(None, fake) == -1
     assert lib.smc_set_row_timing_events(None, None) == 0
+    # the step clock needs a counter and a positive capacity with its stamps
+    lib.smc_set_step_clock.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]
+    assert lib.smc_set_step_clock(fake, None, 4) == -1
+    assert lib.smc_set_step_clock(fake, fake, 0) == -1
+    assert lib.smc_set_step_clock(None, None, 0) == 0
 
 
 def test_oracle_and_cuda_path_share_no_code():
