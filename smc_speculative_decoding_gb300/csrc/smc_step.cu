@@ -1239,6 +1239,11 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
       // atomic's round trip overlaps the copies of the current item
       unsigned next_fast = fast_done ? 0u : atomicAdd(&a.ws.work_counter[0], 1u);
       unsigned next_bonus = bonus_done ? 0u : atomicAdd(&a.ws.work_counter[1], 1u);
+      // near the end of the queues (bonus queue empty, under two fast items
+      // per CTA left) at most two chunks stay in flight: the last items go to
+      // whichever CTAs are ready, and each CTA has less queued when they run dry
+      const unsigned tail_from = static_cast<unsigned>(
+          max(0, sa.n_fast_items - 2 * static_cast<int>(gridDim.x)));
       for (int i = 0;; ++i) {
         const int slot = i % kStages;
         if (i >= kStages &&
@@ -1246,6 +1251,17 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
           raise_status(a.ws.status, SMC_DEV_TIMEOUT);
           meta[slot].flags = kSlotEnd;  // consumers time out on this slot too
           break;
+        }
+        if (i >= 2 && bonus_done && next_fast >= tail_from) {
+          // the chunk issued two iterations ago has been consumed (its slot is
+          // not refilled before the next iteration, so the parity is exact)
+          const int i2 = i - 2;
+          if (!mbar_wait(&empty[i2 % kStages], static_cast<uint32_t>(i2 / kStages) & 1u,
+                         kWaitLimit)) {
+            raise_status(a.ws.status, SMC_DEV_TIMEOUT);
+            meta[slot].flags = kSlotEnd;
+            break;
+          }
         }
         while (!have || chunk >= end) {
           have = false;
