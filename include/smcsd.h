@@ -173,6 +173,20 @@ int32_t smc_set_row_timing_events(void *rows_begin, void *rows_end);
  * `stamps` is not NULL and `counter` is NULL or capacity < 1. */
 int32_t smc_set_step_clock(uint64_t *stamps, uint32_t *counter, int32_t capacity);
 
+/* Self-test of failure detection, with no counterpart in the pages: runs one
+ * of the library's bounded waits against a condition that nothing satisfies,
+ * so that it gives up after `poll_limit` polls and raises SMC_DEV_TIMEOUT in
+ * the status word, as a real wait that times out does.  kind 0: the counter
+ * wait of the step's epilogue kernels (each poll backs off up to about a
+ * microsecond); kind 1: the mbarrier wait of the streaming kernel's ring.
+ * `workspace` is device memory of at least 8 bytes, zeroed beforehand
+ * (smc_workspace_init): its first word is the status word read by
+ * smc_device_status, its second a counter that stays 0.  No kernel traps
+ * or faults; the context stays usable.  Returns SMC_OK once queued,
+ * SMC_ERR_ARG on a bad argument, SMC_ERR_LAUNCH if the launch fails. */
+int32_t smc_selftest_bounded_wait(void *workspace, size_t ws_bytes, int32_t kind,
+                                  int32_t poll_limit, void *stream);
+
 /* One SMC-SD step for B prompts x N particles ([SMC] section 2).
  *
  * target_logits [B, N, K+1, V]  row k < K scores drafted token k, row K is the

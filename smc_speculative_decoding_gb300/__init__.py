@@ -9,7 +9,8 @@ from .binding import (  # noqa: F401
     SmcError, smc_params, smc_kv, make_params, make_kv, alloc_workspace,
     smc_abi_version, smc_strerror, smc_workspace_bytes, smc_workspace_init,
     smc_device_status, status_names, smc_step, smc_resample, kv_blocktable_remap,
-    sps_verify, sps_verify_ex, smc_set_row_timing_events, smc_set_step_clock, smc_step_ex,
+    sps_verify, sps_verify_ex, smc_set_row_timing_events, smc_set_step_clock,
+    smc_selftest_bounded_wait, smc_step_ex,
     smc_draft_sample,
     smc_kv_usage,
     smc_step_opts, SMC_F32, SMC_BF16,
@@ -20,6 +21,7 @@ __all__ = [
     "smc_abi_version", "smc_strerror", "smc_workspace_bytes", "smc_workspace_init",
     "smc_device_status", "status_names", "smc_step", "smc_resample", "kv_blocktable_remap",
     "sps_verify", "sps_verify_ex", "smc_set_row_timing_events", "smc_set_step_clock",
+    "smc_selftest_bounded_wait",
     "smc_step_ex", "smc_draft_sample",
     "smc_kv_usage", "smc_step_opts", "SMC_F32", "SMC_BF16",
 ]

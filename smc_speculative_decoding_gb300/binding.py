@@ -74,6 +74,8 @@ _SIGS = {
                        ctypes.c_void_p]),
     "smc_set_row_timing_events": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_void_p]),
     "smc_set_step_clock": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]),
+    "smc_selftest_bounded_wait": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32,
+                                                   ctypes.c_int32, ctypes.c_void_p]),
     "smc_step_ex": (ctypes.c_int32, [ctypes.POINTER(smc_params), ctypes.POINTER(smc_step_opts)] +
                     [ctypes.c_void_p] * 8 +
                     [ctypes.POINTER(smc_kv), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
@@ -218,6 +220,16 @@ def smc_set_step_clock(stamps=None, counter=None):
     _check("smc_set_step_clock",
            lib().smc_set_step_clock(ctypes.c_void_p(stamps.data_ptr()),
                                     ctypes.c_void_p(counter.data_ptr()), stamps.numel()))
+
+
+def smc_selftest_bounded_wait(workspace, kind, poll_limit=1000, stream=None):
+    """Run one of the library's bounded waits (kind 0: counter, 1: mbarrier)
+    against a condition nothing satisfies; it raises the timeout status bit
+    in `workspace` (a zeroed uint8 CUDA tensor of at least 8 bytes)."""
+    _check("smc_selftest_bounded_wait",
+           lib().smc_selftest_bounded_wait(ctypes.c_void_p(workspace.data_ptr()),
+                                           workspace.numel() * workspace.element_size(),
+                                           kind, poll_limit, _stream(stream)))
 
 
 def status_names(bits):

@@ -184,6 +184,20 @@ int32_t smc_set_row_timing_events(void *rows_begin, void *rows_end) {
   return SMC_OK;
 }
 
+int32_t smc_selftest_bounded_wait(void *workspace, size_t ws_bytes, int32_t kind,
+                                  int32_t poll_limit, void *stream) {
+  if (!workspace || ws_bytes < 2 * sizeof(unsigned) || (kind != 0 && kind != 1) ||
+      poll_limit < 1) {
+    return SMC_ERR_ARG;
+  }
+  if (launch_selftest_wait(static_cast<unsigned *>(workspace), kind,
+                           static_cast<unsigned>(poll_limit),
+                           static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    return SMC_ERR_LAUNCH;
+  }
+  return SMC_OK;
+}
+
 int32_t smc_set_step_clock(uint64_t *stamps, uint32_t *counter, int32_t capacity) {
   if (stamps && (!counter || capacity < 1)) return SMC_ERR_ARG;
   set_step_clock(reinterpret_cast<unsigned long long *>(stamps), counter, stamps ? capacity : 0);

@@ -104,6 +104,7 @@ cudaError_t launch_kv_remap(const Shape &s, const KvArgs &kv, const int32_t *anc
 // Events recorded around the row pass of every later step (null: none).
 void set_row_timing_events(cudaEvent_t begin, cudaEvent_t end);
 void set_step_clock(unsigned long long *stamps, unsigned *counter, int capacity);
+cudaError_t launch_selftest_wait(unsigned *words, int kind, unsigned limit, cudaStream_t stream);
 
 cudaError_t launch_sps_residual(const Shape &s, const void *target, const void *draft,
                                 int32_t *tokens_out, const Workspace &ws, cudaStream_t stream);

@@ -2419,6 +2419,32 @@ cudaError_t launch_step_rows(const Shape &s, int mode, const void *target, const
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Self-test of the bounded waits: one thread runs the counter wait
+// (wait_count, as the epilogue kernels use it) or the mbarrier wait
+// (mbar_wait, as the streaming kernel's ring uses it) against a condition
+// nothing satisfies, for `limit` polls, and raises SMC_DEV_TIMEOUT.
+// words[0] is the status word; words[1] the counter (0, never raised).
+// ---------------------------------------------------------------------------
+__global__ void selftest_wait_kernel(unsigned *words, int kind, unsigned limit) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  bool ok;
+  if (kind == 0) {
+    ok = wait_count(words + 1, 1u, limit);
+  } else {
+    mbar_init(&bar, 1);
+    mbar_init_fence();
+    ok = mbar_wait(&bar, 0u, limit);  // phase 0 never completes: nothing arrives
+  }
+  if (!ok) raise_status(words, SMC_DEV_TIMEOUT);
+}
+
+cudaError_t launch_selftest_wait(unsigned *words, int kind, unsigned limit, cudaStream_t stream) {
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(words, kind, limit);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_draft_sample(const Shape &s, const void *logits, int position,
                                 int32_t *tokens_out, const Workspace &ws, cudaStream_t stream) {
   Shape s0 = s;

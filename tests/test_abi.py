@@ -157,6 +157,13 @@ def test_host_validation_without_gpu(lib):
     assert lib.smc_set_step_clock(fake, None, 4) == -1
     assert lib.smc_set_step_clock(fake, fake, 0) == -1
     assert lib.smc_set_step_clock(None, None, 0) == 0
+    # the wait self-test: a buffer of two words, kind 0 or 1, a positive limit
+    lib.smc_selftest_bounded_wait.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32,
+                                              ctypes.c_int32, ctypes.c_void_p]
+    assert lib.smc_selftest_bounded_wait(None, 64, 0, 10, None) == -1
+    assert lib.smc_selftest_bounded_wait(fake, 4, 0, 10, None) == -1
+    assert lib.smc_selftest_bounded_wait(fake, 64, 2, 10, None) == -1
+    assert lib.smc_selftest_bounded_wait(fake, 64, 1, 0, None) == -1
 
 
 def test_oracle_and_cuda_path_share_no_code():

@@ -1,7 +1,9 @@
-"""The library's measurement hooks on the GPU: the device step clock
-(smc_set_step_clock) stamps each step's row pass once, in order, within its
-capacity, and nothing once it is turned off; turning it on changes no
-output."""
+"""The library's measurement and self-test hooks on the GPU: the device step
+clock (smc_set_step_clock) stamps each step's row pass once, in order,
+within its capacity, and nothing once it is turned off; turning it on
+changes no output.  The bounded waits give up with SMC_DEV_TIMEOUT when
+nothing satisfies them (smc_selftest_bounded_wait), and the context stays
+usable."""
 import numpy as np
 import pytest
 import torch
@@ -71,3 +73,18 @@ def test_step_clock_changes_no_output():
                       r.kv["tables"], r.kv["refcount"], r.kv["seq_len"])])
     for a, b in zip(*outs):
         assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("kind", [0, 1])
+def test_bounded_wait_gives_up_with_the_timeout_status(kind):
+    buf = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    smcsd.smc_selftest_bounded_wait(buf, kind, poll_limit=2000)
+    torch.cuda.synchronize()
+    bits = int(buf[:4].view(torch.int32).item())
+    assert "timeout" in smcsd.status_names(bits)
+    # the context still runs a step, and its own status is clean
+    w = WORKLOADS["tiny_v64"]
+    r = StepRunner(w, seed=2, with_kv=True, steps=4)
+    _run(r, w, 2)
+    torch.cuda.synchronize()
+    assert smcsd.smc_device_status(r.workspace, clear=True) == 0
