@@ -23,7 +23,7 @@ size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws) 
   };
   // region that must start at zero (counters and the freed-block bitmap)
   const size_t o_status = take(sizeof(unsigned));
-  const size_t o_wd = take(sizeof(unsigned) * s.B);
+  const size_t o_wr = take(sizeof(unsigned long long) * s.B * s.N * kWrecPerParticle);
   const size_t o_bd = take(sizeof(unsigned) * s.B);
   const size_t o_rt = take(sizeof(unsigned) * rows);
   const size_t o_sa = take(sizeof(unsigned) * s.B);
@@ -46,7 +46,7 @@ size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws) 
   if (ws && base) {
     char *p = static_cast<char *>(base);
     ws->status = reinterpret_cast<unsigned *>(p + o_status);
-    ws->weights_done = reinterpret_cast<unsigned *>(p + o_wd);
+    ws->wrec = reinterpret_cast<unsigned long long *>(p + o_wr);
     ws->bonus_done = reinterpret_cast<unsigned *>(p + o_bd);
     ws->row_ticket = reinterpret_cast<unsigned *>(p + o_rt);
     ws->sps_ticket_a = reinterpret_cast<unsigned *>(p + o_sa);

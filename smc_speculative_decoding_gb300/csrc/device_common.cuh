@@ -476,6 +476,18 @@ __device__ __forceinline__ void prefetch_l2(const void *p, size_t bytes) {
   }
 }
 
+// 64-bit stores and loads at gpu scope.  An aligned 64-bit access is single-
+// copy atomic, so a value and its tag written in one such store are seen
+// together or not at all, with no fence.
+__device__ __forceinline__ void st_relaxed_gpu_u64(unsigned long long *p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // The GPU's global timer, in nanoseconds.
 __device__ __forceinline__ unsigned long long global_timer_ns() {
   unsigned long long t;

@@ -33,9 +33,12 @@ struct KvArgs {
 };
 
 // Workspace carve-up shared by every entry point.
+constexpr int kWrecPerParticle = 16;  // two 64-bit records for each of 8 warps
+
 struct Workspace {
   unsigned *status;          // [1]  device status bits
-  unsigned *weights_done;    // [B]  particles of the prompt whose new log-weight is published
+  unsigned long long *wrec;  // [B*N * kWrecPerParticle] tagged weight records (plain step):
+                             // (call tag << 32) | float bits, head and tail per warp
   unsigned *bonus_done;      // [B]  particles of the prompt whose bonus token is published
   unsigned *row_ticket;      // [rows]
   unsigned *sps_ticket_a;    // [B]

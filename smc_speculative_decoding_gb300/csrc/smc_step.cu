@@ -1899,23 +1899,24 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const StreamArgs sa, i
 // log-sum-exp rows from their (item, warp) partials and sum its weight
 // increment in float-float, while warp 0 locates the bonus draw
 // (bonus_select_warp); then the whole CTA rescans the unit (bonus_rescan).
-// The particle's new log-weight (incoming plus increment, as a float pair) goes
-// to its first row result and its bonus token to its bonus row's result, each
-// followed by a release increment of the prompt's counter (weights_done, then
-// bonus_done).  With alpha != 1 the increment also takes the bonus row's
-// log-sum-exps, so the weight is published after warp 0's search.
+// Each warp's part of the increment goes out at once as tagged 64-bit records
+// (publish_part; warp 0's part, the bonus row's log-sum-exps, only with
+// alpha != 1): prompt_kernel's thread i polls particle i's records until all
+// carry the call's tag and adds the incoming log-weight and the potential
+// itself, so no barrier or fence sits between a warp's rows and the prompt.
+// The bonus token goes to the bonus row's result, followed by a release
+// increment of the prompt's bonus_done counter.
 // ---------------------------------------------------------------------------
 constexpr uint32_t kCountWaitLimit = 1u << 20;  // polls of about 1 us: about a second
 
-__device__ __forceinline__ void publish_weight(const StepArgs &a, int part, const float2 *s_d,
-                                               ff extra, float lw0) {
-  ff d = extra;
-#pragma unroll
-  for (int w = 1; w < kWarps; ++w) d = ff_add_x(d, ff{s_d[w].x, s_d[w].y});
-  const ff lwf = ff_add_x(ff{lw0, 0.f}, d);
-  RowResult *r = a.ws.results + static_cast<size_t>(part) * (2 * a.K + 1);
-  *reinterpret_cast<float2 *>(r) = make_float2(lwf.hi, lwf.lo);
-  add_release_gpu(a.ws.weights_done + part / a.N, 1u);
+// A warp's part of a particle's weight increment, stored as two tagged 64-bit
+// records (head, tail) that prompt_kernel polls: a value and its call's tag in
+// one single-copy-atomic store, so no fence is needed.
+__device__ __forceinline__ void publish_part(const StepArgs &a, int part, int warp, ff d) {
+  unsigned long long *rec = a.ws.wrec + static_cast<size_t>(part) * kWrecPerParticle + 2 * warp;
+  const unsigned long long tag = static_cast<unsigned long long>(a.call_tag) << 32;
+  st_relaxed_gpu_u64(rec, tag | __float_as_uint(d.hi));
+  st_relaxed_gpu_u64(rec + 1, tag | __float_as_uint(d.lo));
 }
 
 template <typename T>
@@ -1928,7 +1929,6 @@ __global__ void __launch_bounds__(kThreads) particle_kernel(const StreamArgs sa)
   __shared__ BonusSel s_sel;
   __shared__ long long s_ll[kWarps];
   __shared__ int s_i[2 * kWarps];
-  __shared__ float2 s_d[kWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int part = blockIdx.x;
   const int K = a.K, rpp = 2 * K + 1, nr = 2 * K;
@@ -1953,13 +1953,7 @@ __global__ void __launch_bounds__(kThreads) particle_kernel(const StreamArgs sa)
     gv = (gtok < 0 || gtok >= a.V) ? __int_as_float(0x7fc00000)
                                    : a.tscale * Tr::scalar(row_base<T>(a, part * rpp + j), gtok);
   }
-  const int publisher = a.bonus_lse ? 0 : 32;
   const float u = warp == 0 ? bonus_uniform(a, part) : 0.f;
-  float lw0 = 0.f, pot = 0.f;
-  if (static_cast<int>(threadIdx.x) == publisher) {
-    lw0 = __ldcg(a.out.log_weights + part);
-    if (a.potential) pot = __ldcg(a.potential + part);
-  }
   // every streaming CTA's partials are out once rows_done reaches the grid
   // (bounded; this grid launches only after every streaming CTA has started)
   __shared__ int s_rows_ok;
@@ -1976,6 +1970,10 @@ __global__ void __launch_bounds__(kThreads) particle_kernel(const StreamArgs sa)
     float fM = kNegInf, fS = 0.f;
     if (a.bonus_lse) fast_row_stats(sa, part * rpp + K, -1, &fM, &fS);
     bonus_select_warp<T>(sa, part, bonus_rowp, u, fM, fS, a.bonus_lse, s_tab, &s_sel);
+    if (a.bonus_lse && lane == 0) {
+      // alpha != 1: the bonus row's log-sum-exps enter the increment
+      publish_part(a, part, 0, ff_sub_x(s_sel.lse_alpha, ff_mul_fx(s_sel.lse, a.alpha)));
+    }
   } else {
     ff d{0.f, 0.f};
     unsigned bits = 0;
@@ -2003,19 +2001,9 @@ __global__ void __launch_bounds__(kThreads) particle_kernel(const StreamArgs sa)
       d = ff_add_x(d, ff{__shfl_xor_sync(kAll, d.hi, o), __shfl_xor_sync(kAll, d.lo, o)});
     }
     if (bits) raise_status(a.ws.status, bits);
-    if (lane == 0) s_d[warp] = make_float2(d.hi, d.lo);
-    if (!a.bonus_lse) {
-      named_bar_sync(1, (kWarps - 1) * 32);
-      if (static_cast<int>(threadIdx.x) == publisher) publish_weight(a, part, s_d, ff{pot, 0.f}, lw0);
-    }
+    if (lane == 0) publish_part(a, part, warp, d);
   }
   __syncthreads();
-  if (a.bonus_lse && static_cast<int>(threadIdx.x) == publisher) {
-    // alpha != 1: the bonus row's log-sum-exps enter the increment
-    const ff extra = ff_add_x(ff_sub_x(s_sel.lse_alpha, ff_mul_fx(s_sel.lse, a.alpha)),
-                              ff{pot, 0.f});
-    publish_weight(a, part, s_d, extra, lw0);
-  }
   const int tok = bonus_rescan<T>(sa, bonus_rowp, s_sel, s_tab, s_ll, s_i);
   if (threadIdx.x == 0) {
     a.ws.results[static_cast<size_t>(part) * rpp + K].tok = tok;
@@ -2038,22 +2026,49 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const StepArgs a, i
   const int tid = threadIdx.x;
   const KvScratch sc = a.use_kv ? kv_scratch(a.kv, b, N, a.ws, dyn_i, kv_staged != 0) : KvScratch{};
   int top = 0;
-  tail_prefetch(a, b, sm, sc, &top);
+  const float lw0 = tail_prefetch(a, b, sm, sc, &top);
   tail_prefetch_stack(a, b, top, sc);
+  const float pot = (a.potential && tid < N) ? __ldcg(a.potential + b * N + tid) : 0.f;
   const ResampleKey key = resample_key(a.seed, a.step, b, N);
-  if (tid == 0) s_ok = wait_count(a.ws.weights_done + b, static_cast<unsigned>(N), kCountWaitLimit);
-  __syncthreads();
-  if (!s_ok) {
+  // thread i < N polls particle i's weight records until every one carries
+  // this call's tag (bounded), and sums them with the incoming log-weight
+  ff lwf{0.f, 0.f};
+  bool ok = true;
+  if (tid < N) {
+    const unsigned long long *rec =
+        a.ws.wrec + static_cast<size_t>(b * N + tid) * kWrecPerParticle;
+    const int w0 = a.bonus_lse ? 0 : 1;
+    ok = false;
+    for (uint32_t it = 0; it < kCountWaitLimit; ++it) {
+      unsigned long long v[kWrecPerParticle];
+      bool all = true;
+#pragma unroll
+      for (int k = 0; k < kWrecPerParticle; ++k) {
+        v[k] = k >= 2 * w0 ? ld_relaxed_gpu_u64(rec + k) : 0ull;
+        if (k >= 2 * w0 && static_cast<uint32_t>(v[k] >> 32) != a.call_tag) all = false;
+      }
+      if (all) {
+        ff d{0.f, 0.f};
+#pragma unroll
+        for (int w = 0; w < kWrecPerParticle / 2; ++w) {
+          if (w >= w0) {
+            d = ff_add_x(d, ff{__uint_as_float(static_cast<uint32_t>(v[2 * w])),
+                               __uint_as_float(static_cast<uint32_t>(v[2 * w + 1]))});
+          }
+        }
+        lwf = ff_add_x(ff{lw0, 0.f}, ff_add_x(d, ff{pot, 0.f}));
+        ok = true;
+        break;
+      }
+      __nanosleep(it < 64 ? 32 : 1024);
+    }
+  }
+  if (__syncthreads_or(!ok)) {
     if (tid == 0) raise_status(a.ws.status, SMC_DEV_TIMEOUT);
     cp_async_wait_all();
     return;
   }
   const RowResult *res = a.ws.results + static_cast<size_t>(b) * N * rpp;
-  ff lwf{0.f, 0.f};
-  if (tid < N) {
-    const float2 v = __ldcg(reinterpret_cast<const float2 *>(res + static_cast<size_t>(tid) * rpp));
-    lwf = ff{v.x, v.y};
-  }
   const bool resampled = prompt_weights(a, b, sm, lwf, key, a.use_kv ? &sc : nullptr);
   if (a.use_kv) kv_remap_append(a.kv, b, N, sm.anc, resampled, K + 1, a.ws, sm.ks, sc, true, true);
   if (tid == 0) s_ok = wait_count(a.ws.bonus_done + b, static_cast<unsigned>(N), kCountWaitLimit);
@@ -2072,7 +2087,6 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const StepArgs a, i
         __ldcg(&res[static_cast<size_t>(anc) * rpp + K].tok);
   }
   if (tid == 0) {
-    a.ws.weights_done[b] = 0u;
     a.ws.bonus_done[b] = 0u;
     // the last prompt CTA past its waits: every particle CTA has passed its
     // wait on rows_done, which can start again from 0
@@ -2377,8 +2391,17 @@ static cudaError_t launch_rows(const StepArgs &a, int dtype, long long rows, cud
   return e;
 }
 
+// A tag for each call, never 0 (so zeroed records never match).
+static uint32_t next_call_tag() {
+  static std::atomic<uint32_t> counter{0};
+  uint32_t t = counter.fetch_add(1u, std::memory_order_relaxed) + 1u;
+  if (t == 0u) t = counter.fetch_add(1u, std::memory_order_relaxed) + 1u;
+  return t;
+}
+
 static StepArgs step_args(const Shape &s, int mode, const Workspace &ws) {
   StepArgs a{};
+  a.call_tag = next_call_tag();
   a.B = s.B; a.N = s.N; a.K = s.K; a.V = s.V;
   a.nch = chunks_per_row(s.dtype, s.V);
   a.mode = mode;

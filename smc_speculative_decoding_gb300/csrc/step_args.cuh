@@ -22,6 +22,7 @@ struct StepArgs {
   const float *potential;     // [B*N] log-potential increments, or null
   uint64_t seed;
   uint32_t step;
+  uint32_t call_tag;          // nonzero, different for every call (tags the weight records)
   Workspace ws;
   StepOutputs out;
   KvArgs kv;
