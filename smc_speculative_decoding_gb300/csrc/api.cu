@@ -41,6 +41,7 @@ size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws) 
   const size_t snch = static_cast<size_t>(sps_chunks_per_row(s.dtype, s.V));
   const size_t o_spq = take(sizeof(float4) * s.B * snch * 2);
   const size_t o_spr = take(sizeof(float2) * s.B * snch);
+  const size_t o_srt = take(sizeof(int32_t) * s.B);
   const size_t o_kt = take(sizeof(int32_t) * static_cast<size_t>(s.B) * s.N * (T > 0 ? T : 0));
   const size_t o_kl = take(sizeof(int32_t) * static_cast<size_t>(s.B) * s.N);
   if (ws && base) {
@@ -56,6 +57,8 @@ size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws) 
     ws->exit_counter = ws->work_counter + 2;
     ws->rows_done = ws->work_counter + 3;
     ws->tail_ticket = ws->work_counter + 4;
+    ws->sps_retry_n = ws->work_counter + 5;
+    ws->sps_retry_done = ws->work_counter + 6;
     ws->partials = reinterpret_cast<RowPartial *>(p + o_part);
     ws->item_part = reinterpret_cast<float2 *>(p + o_ip);
     ws->bonus_part = reinterpret_cast<int4 *>(p + o_bp);
@@ -64,6 +67,7 @@ size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws) 
     ws->sps_stats = reinterpret_cast<float4 *>(p + o_sst);
     ws->sps_part_pq = reinterpret_cast<float4 *>(p + o_spq);
     ws->sps_part_r = reinterpret_cast<float2 *>(p + o_spr);
+    ws->sps_retry = reinterpret_cast<int32_t *>(p + o_srt);
     ws->kv_old_tables = reinterpret_cast<int32_t *>(p + o_kt);
     ws->kv_old_len = reinterpret_cast<int32_t *>(p + o_kl);
     ws->zero_bytes = zero_bytes;

@@ -48,6 +48,9 @@ struct Workspace {
   unsigned *exit_counter;    // [1]  CTAs of the streaming kernel that finished
   unsigned *rows_done;       // [1]  streaming CTAs whose partials are published (plain step)
   unsigned *tail_ticket;     // [1]  prompt CTAs past their waits (plain step)
+  unsigned *sps_retry_n;     // [1]  prompts queued for the SpS retry pass
+  unsigned *sps_retry_done;  // [1]  retry-pass CTAs that finished
+  int32_t *sps_retry;        // [B]  the queued prompts
   RowPartial *partials;      // [rows * nch]  (per-chunk kernel)
   float2 *item_part;         // [rows * nch * 8]  (m, s) per work item and warp (streaming kernel)
   int4 *bonus_part;          // [B * N * nch * 8] (ref bits, fixed-point sum lo, hi, -)

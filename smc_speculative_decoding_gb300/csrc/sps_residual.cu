@@ -4,7 +4,14 @@
 // from max(0, p_j - q_j) normalised, by inverse CDF in vocabulary order.
 //
 // Runs after the row kernel in SpS mode, which wrote the first rejected
-// position of every prompt (or -1).  Two launches over (chunk, prompt):
+// position of every prompt (or -1) and each row's log-sum-exp to about 1e-7.
+// Without top-p, one launch over (chunk, prompt), sps_onepass_kernel: each
+// CTA sums p_v and q_v against the row kernel's log-sum-exps (provisional
+// shifts) and the residual at ratio 1, all in float-float; the last CTA of
+// the prompt turns those into the exact normalisers and chunk masses, picks
+// the chunk and the element.  Where the shifts' ratio or the close calls
+// (|p_v - q_v| <= tau q_v) could move the masses by more than 1e-10, that CTA
+// takes the two-pass route below alone.  With top-p, two launches:
 //   sps_stats_kernel:    float-float log-sum-exp of rows p_j and q_j, so that
 //                        p_v and q_v are known to ~1e-10 relative;
 //   sps_residual_kernel: per-chunk residual mass; the last CTA of the prompt
@@ -107,26 +114,40 @@ __device__ __forceinline__ ff chunk_weight_sum(const float (&x)[EPT], float mc, 
   return ff_add(ff_norm(S0), ff_norm(S1));
 }
 
+
+// Shared memory of the SpS kernels.
+struct SpsSmem {
+  float2 tab[64];
+  float th[64], tl[64];
+  float red[2 * kWarps];
+  float2 ffs[kWarps];
+  float4 rec[2 * kWarps];
+  int ints[2 * kWarps];
+  int last, sel, mode, fast;
+  float sel_m;
+  ff rem, lp, lq, total;
+};
+
+// Rows p_j and q_j of prompt b, element size esz.
+__device__ __forceinline__ void sps_rows(const SpsArgs &a, int b, int jr, int esz,
+                                         const char **prow, const char **qrow) {
+  *prow = a.target + (static_cast<size_t>(b) * (a.K + 1) + jr) * static_cast<size_t>(a.V) * esz;
+  *qrow = a.draft + (static_cast<size_t>(b) * a.K + jr) * static_cast<size_t>(a.V) * esz;
+}
+
+// Chunk c of rows p_j and q_j: each row's kept maximum mc and float-float sum
+// of exp(s (x - mc)) over its kept logits, to sps_part_pq[(b nch + c) 2 + r]
+// (r = 0: p, 1: q) as (mc, sum hi, sum lo, 0).  All threads call it.
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(kThreads) sps_stats_kernel(const SpsArgs a) {
+__device__ void stats_chunk(const SpsArgs &a, int b, int jr, int c, float thr_p, float thr_q,
+                            SpsSmem &sm) {
   using G = SpsGeom<T>;
-  __shared__ float s_red[2 * kWarps];
-  __shared__ float2 s_ff[kWarps];
-  __shared__ float2 s_tab[64];
-  __shared__ float s_th[64], s_tl[64];
-  __shared__ int s_last;
-  const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
-  const int jr = a.ws.sps_rej[b];
-  if (jr < 0) return;
-  stage_exp2_table(s_tab);
-  stage_exp2_split(s_th, s_tl);
+  const int tid = threadIdx.x;
   const int64_t c0 = static_cast<int64_t>(c) * G::kCH;
   const int n_valid = static_cast<int>(min(static_cast<int64_t>(G::kCH), a.V - c0));
-  const char *rows[2] = {
-      a.target + (static_cast<size_t>(b) * (a.K + 1) + jr) * static_cast<size_t>(a.V) * G::kESZ,
-      a.draft + (static_cast<size_t>(b) * a.K + jr) * static_cast<size_t>(a.V) * G::kESZ};
-  float thr[2];
-  sps_thresholds(a, b, jr, &thr[0], &thr[1]);
+  const char *rows[2];
+  sps_rows(a, b, jr, G::kESZ, &rows[0], &rows[1]);
+  const float thr[2] = {thr_p, thr_q};
   // both rows' chunks in flight at once; logits outside a nucleus weigh 0
   float x[2][G::kEPT];
   load_chunk<T, VEC, kSpsNV>(rows[0] + c0 * G::kESZ, n_valid, x[0]);
@@ -140,53 +161,51 @@ __global__ void __launch_bounds__(kThreads) sps_stats_kernel(const SpsArgs a) {
       m[r] = fmaxf(m[r], x[r][e]);
     }
   }
-  const float mcp = block_max(m[0], s_red);
-  const float mcq = block_max(m[1], s_red);  // (the table is staged: block_max has barriers)
+  const float mcp = block_max(m[0], sm.red);
+  const float mcq = block_max(m[1], sm.red);  // (block_max's barriers also cover the tables)
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     const float mc = r == 0 ? mcp : mcq;
-    const ff S = block_ff_sum(chunk_weight_sum<T, G::kEPT>(x[r], mc, a.tscale, s_th, s_tl, s_tab),
-                              s_ff);
-    if (tid == 0) a.ws.sps_part_pq[(static_cast<size_t>(b) * a.nch + c) * 2 + r] = make_float4(mc, S.hi, S.lo, 0.f);
-  }
-  if (tid == 0) {
-    __threadfence();
-    s_last = atomicAdd(&a.ws.sps_ticket_a[b], 1u) == static_cast<unsigned>(a.nch - 1);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (tid < 32) {
-    const int lane = tid;
-    float lse[2][2];
-    for (int r = 0; r < 2; ++r) {
-      float M = kNegInf;
-      for (int cc = lane; cc < a.nch; cc += 32) {
-        M = fmaxf(M, __ldcg(&a.ws.sps_part_pq[(static_cast<size_t>(b) * a.nch + cc) * 2 + r].x));
-      }
-      M = warp_max(M);
-      ff tot{0.f, 0.f};
-      for (int c0w = 0; c0w < a.nch; c0w += 32) {
-        const int cc = c0w + lane;
-        ff val{0.f, 0.f};
-        if (cc < a.nch && M > kNegInf) {
-          const float4 q = __ldcg(&a.ws.sps_part_pq[(static_cast<size_t>(b) * a.nch + cc) * 2 + r]);
-          if (q.x > kNegInf) val = ff_mul(ff{q.y, q.z}, ff_norm(weight_term(q.x, M, a.tscale, s_tab)));
-        }
-        tot = ff_add(tot, warp_ff_sum(val));
-      }
-      // log of the (kept) mass of exp(s l): s M (exact, as a pair) + log(total)
-      const ff l = (M > kNegInf && tot.hi > 0.f)
-                       ? ff_add(two_prod(a.tscale, M), ff_log(ff_norm(tot), s_tab))
-                       : ff{kNegInf, 0.f};
-      lse[r][0] = l.hi;
-      lse[r][1] = l.lo;
-    }
-    if (lane == 0) {
-      a.ws.sps_stats[b] = make_float4(lse[0][0], lse[0][1], lse[1][0], lse[1][1]);
-      a.ws.sps_ticket_a[b] = 0u;
+    const ff S = block_ff_sum(
+        chunk_weight_sum<T, G::kEPT>(x[r], mc, a.tscale, sm.th, sm.tl, sm.tab), sm.ffs);
+    if (tid == 0) {
+      a.ws.sps_part_pq[(static_cast<size_t>(b) * a.nch + c) * 2 + r] = make_float4(mc, S.hi, S.lo, 0.f);
     }
   }
+}
+
+// Run by one full warp once every chunk's stats_chunk is visible: the
+// float-float log-sum-exps of the kept parts of rows p_j and q_j (-inf for an
+// empty one), to sps_stats[b] and returned.
+__device__ void stats_combine(const SpsArgs &a, int b, const float2 *tab, ff *lp, ff *lq) {
+  const int lane = threadIdx.x & 31;
+  float lse[2][2];
+  for (int r = 0; r < 2; ++r) {
+    float M = kNegInf;
+    for (int cc = lane; cc < a.nch; cc += 32) {
+      M = fmaxf(M, __ldcg(&a.ws.sps_part_pq[(static_cast<size_t>(b) * a.nch + cc) * 2 + r].x));
+    }
+    M = warp_max(M);
+    ff tot{0.f, 0.f};
+    for (int c0w = 0; c0w < a.nch; c0w += 32) {
+      const int cc = c0w + lane;
+      ff val{0.f, 0.f};
+      if (cc < a.nch && M > kNegInf) {
+        const float4 q = __ldcg(&a.ws.sps_part_pq[(static_cast<size_t>(b) * a.nch + cc) * 2 + r]);
+        if (q.x > kNegInf) val = ff_mul(ff{q.y, q.z}, ff_norm(weight_term(q.x, M, a.tscale, tab)));
+      }
+      tot = ff_add(tot, warp_ff_sum(val));
+    }
+    // log of the (kept) mass of exp(s l): s M (exact, as a pair) + log(total)
+    const ff l = (M > kNegInf && tot.hi > 0.f)
+                     ? ff_add(two_prod(a.tscale, M), ff_log(ff_norm(tot), tab))
+                     : ff{kNegInf, 0.f};
+    lse[r][0] = l.hi;
+    lse[r][1] = l.lo;
+  }
+  if (lane == 0) a.ws.sps_stats[b] = make_float4(lse[0][0], lse[0][1], lse[1][0], lse[1][1]);
+  *lp = ff{lse[0][0], lse[0][1]};
+  *lq = ff{lse[1][0], lse[1][1]};
 }
 
 // max(0, p_v - q_v) for logits xp, xq, each probability zero outside its
@@ -199,107 +218,127 @@ __device__ __forceinline__ ff residual_of(float xp, float xq, float s, ff lp, ff
   return d.hi > 0.f ? d : ff{0.f, 0.f};
 }
 
+// Running float-float sums of nonnegative packed pairs: the heads start at 2,
+// above any single addend, so the fast two-sum is exact at every addition.
+struct PairAcc {
+  unsigned long long h, l;
+  __device__ __forceinline__ void init() {
+    h = f2dup(2.f);
+    l = 0ull;
+  }
+  __device__ __forceinline__ void add(unsigned long long xh, unsigned long long xl) {
+    const unsigned long long s2 = add2(h, xh);
+    l = add2(l, add2(sub2(xh, sub2(s2, h)), xl));
+    h = s2;
+  }
+  __device__ __forceinline__ ff total() const {
+    float a0, a1, o0, o1;
+    f2unpack(h, a0, a1);
+    f2unpack(l, o0, o1);
+    ff r0 = two_sum(a0, -2.f), r1 = two_sum(a1, -2.f);
+    r0.lo += o0;
+    r1.lo += o1;
+    return ff_add(ff_norm(r0), ff_norm(r1));
+  }
+};
+
+// d = p - q of packed float-float pairs, normalised (NH, NL).
+__device__ __forceinline__ void packed_diff(unsigned long long PH, unsigned long long PL,
+                                            unsigned long long QH, unsigned long long QL,
+                                            unsigned long long *NH, unsigned long long *NL) {
+  const unsigned long long DH = sub2(PH, QH);
+  const unsigned long long BB = sub2(DH, PH);
+  const unsigned long long DE = sub2(sub2(PH, sub2(DH, BB)), add2(QH, BB));
+  const unsigned long long DL = add2(DE, sub2(PL, QL));
+  *NH = add2(DH, DL);
+  *NL = sub2(DL, sub2(*NH, DH));
+}
+
+// Chunk c's residual mass sum_v max(0, p_v - q_v) in float-float, for exact
+// log-sum-exps lp, lq of the kept rows, to sps_part_r[b nch + c].  All threads
+// call it (the tables staged).
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(kThreads) sps_residual_kernel(const SpsArgs a) {
+__device__ void residual_chunk(const SpsArgs &a, int b, int jr, int c, ff lp, ff lq,
+                               float thr_p, float thr_q, SpsSmem &sm) {
   using G = SpsGeom<T>;
-  using Tr = LogitTraits<T>;
-  __shared__ float2 s_ff[kWarps];
-  __shared__ float2 s_tab[64];
-  __shared__ float s_th[64], s_tl[64];
-  __shared__ int s_int[2 * kWarps];
-  __shared__ int s_last;
-  __shared__ int s_sel;
-  __shared__ int s_mode;
-  __shared__ float s_sel_m;
-  __shared__ ff s_rem;
-  const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
-  const int jr = a.ws.sps_rej[b];
-  if (jr < 0) return;
-  stage_exp2_table(s_tab);
-  stage_exp2_split(s_th, s_tl);
-  const float4 st = a.ws.sps_stats[b];
-  const ff lp{st.x, st.y}, lq{st.z, st.w};
-  float thr_p, thr_q;
-  sps_thresholds(a, b, jr, &thr_p, &thr_q);
+  const int tid = threadIdx.x;
   const int64_t c0 = static_cast<int64_t>(c) * G::kCH;
   const int n_valid = static_cast<int>(min(static_cast<int64_t>(G::kCH), a.V - c0));
-  const char *prow = a.target + (static_cast<size_t>(b) * (a.K + 1) + jr) * static_cast<size_t>(a.V) * G::kESZ;
-  const char *qrow = a.draft + (static_cast<size_t>(b) * a.K + jr) * static_cast<size_t>(a.V) * G::kESZ;
+  const char *prow, *qrow;
+  sps_rows(a, b, jr, G::kESZ, &prow, &qrow);
   float xp[G::kEPT], xq[G::kEPT];
   load_chunk<T, VEC, kSpsNV>(prow + c0 * G::kESZ, n_valid, xp);
   load_chunk<T, VEC, kSpsNV>(qrow + c0 * G::kESZ, n_valid, xq);
-  __syncthreads();  // tables staged
   // p and q two logits at a time on the packed pipes, and the residual
   // max(0, p - q) of each in float-float as residual_of takes it: logits
   // outside a nucleus are set to -inf first (they then weigh about e^-59
-  // instead of 0, far below what can move a draw); the running sums start at
-  // 2, above any residual (<= 1), so the fast two-sum is exact at every
-  // addition
+  // instead of 0, far below what can move a draw)
   ShiftedExp ep, eq;
   ep.init(a.tscale, lp);
   eq.init(a.tscale, lq);
   const bool live = lp.hi > kNegInf && lq.hi > kNegInf;
-  ff R0{0.f, 0.f}, R1{0.f, 0.f};
+  ff R{0.f, 0.f};
   if (live) {
-    unsigned long long acc = f2dup(2.f), alo = 0ull;
+    PairAcc acc;
+    acc.init();
 #pragma unroll
     for (int e = 0; e < G::kEPT; e += 2) {
-      unsigned long long PH, PL, QH, QL;
-      ep.eval(xp[e] >= thr_p ? xp[e] : kNegInf, xp[e + 1] >= thr_p ? xp[e + 1] : kNegInf, s_th,
-              s_tl, &PH, &PL);
-      eq.eval(xq[e] >= thr_q ? xq[e] : kNegInf, xq[e + 1] >= thr_q ? xq[e + 1] : kNegInf, s_th,
-              s_tl, &QH, &QL);
-      // d = p - q: two-sum of the heads, the tails after, then normalised
-      const unsigned long long DH = sub2(PH, QH);
-      const unsigned long long BB = sub2(DH, PH);
-      const unsigned long long DE = sub2(sub2(PH, sub2(DH, BB)), add2(QH, BB));
-      const unsigned long long DL = add2(DE, sub2(PL, QL));
-      const unsigned long long NH = add2(DH, DL);
-      const unsigned long long NL = sub2(DL, sub2(NH, DH));
+      unsigned long long PH, PL, QH, QL, NH, NL;
+      ep.eval(xp[e] >= thr_p ? xp[e] : kNegInf, xp[e + 1] >= thr_p ? xp[e + 1] : kNegInf, sm.th,
+              sm.tl, &PH, &PL);
+      eq.eval(xq[e] >= thr_q ? xq[e] : kNegInf, xq[e + 1] >= thr_q ? xq[e + 1] : kNegInf, sm.th,
+              sm.tl, &QH, &QL);
+      packed_diff(PH, PL, QH, QL, &NH, &NL);
       float h0, h1, l0, l1;
       f2unpack(NH, h0, h1);
       f2unpack(NL, l0, l1);
-      const unsigned long long RH = f2pack(h0 > 0.f ? h0 : 0.f, h1 > 0.f ? h1 : 0.f);
-      const unsigned long long RL = f2pack(h0 > 0.f ? l0 : 0.f, h1 > 0.f ? l1 : 0.f);
-      const unsigned long long S2 = add2(acc, RH);
-      alo = add2(alo, add2(sub2(RH, sub2(S2, acc)), RL));
-      acc = S2;
+      acc.add(f2pack(h0 > 0.f ? h0 : 0.f, h1 > 0.f ? h1 : 0.f),
+              f2pack(h0 > 0.f ? l0 : 0.f, h1 > 0.f ? l1 : 0.f));
     }
-    float a0, a1, o0, o1;
-    f2unpack(acc, a0, a1);
-    f2unpack(alo, o0, o1);
-    R0 = two_sum(a0, -2.f);
-    R1 = two_sum(a1, -2.f);
-    R0.lo += o0;
-    R1.lo += o1;
+    R = acc.total();
   } else {
+    ff R0{0.f, 0.f}, R1{0.f, 0.f};
 #pragma unroll
     for (int e = 0; e < G::kEPT; ++e) {
-      const ff d = residual_of(xp[e], xq[e], a.tscale, lp, lq, thr_p, thr_q, s_tab);
+      const ff d = residual_of(xp[e], xq[e], a.tscale, lp, lq, thr_p, thr_q, sm.tab);
       if (d.hi > 0.f) {
         if (e & 1) ff_accum(R1, d);
         else ff_accum(R0, d);
       }
     }
+    R = ff_add(ff_norm(R0), ff_norm(R1));
   }
-  const ff R = block_ff_sum(ff_add(ff_norm(R0), ff_norm(R1)), s_ff);
-  if (tid == 0) {
-    a.ws.sps_part_r[static_cast<size_t>(b) * a.nch + c] = make_float2(R.hi, R.lo);
-    __threadfence();
-    s_last = atomicAdd(&a.ws.sps_ticket_b[b], 1u) == static_cast<unsigned>(a.nch - 1);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
+  R = block_ff_sum(R, sm.ffs);
+  if (tid == 0) a.ws.sps_part_r[static_cast<size_t>(b) * a.nch + c] = make_float2(R.hi, R.lo);
+}
+
+// The draw once every chunk's residual mass is in sps_part_r (and, for the
+// fallback below, every chunk's stats_chunk in sps_part_pq), run by the whole
+// CTA: u from Philox (purpose RESIDUAL) picks the chunk by the chunk masses,
+// then the element by a rescan of the chunk with exact residuals.  With no
+// residual mass (p_j == q_j up to rounding) the token is drawn from p_j.
+// Writes the token; `total` is the residual mass when already summed, else
+// negative.
+template <typename T>
+__device__ void residual_select(const SpsArgs &a, int b, int jr, ff lp, ff lq, float thr_p,
+                                float thr_q, ff total_in, SpsSmem &sm) {
+  using G = SpsGeom<T>;
+  using Tr = LogitTraits<T>;
+  const int tid = threadIdx.x;
+  const char *prow, *qrow;
+  sps_rows(a, b, jr, G::kESZ, &prow, &qrow);
   if (tid < 32) {
     const int lane = tid;
     const float2 *pr = a.ws.sps_part_r + static_cast<size_t>(b) * a.nch;
-    ff total{0.f, 0.f};
-    for (int c0w = 0; c0w < a.nch; c0w += 32) {
-      const int cc = c0w + lane;
-      ff val{0.f, 0.f};
-      if (cc < a.nch) val = ff{__ldcg(&pr[cc].x), __ldcg(&pr[cc].y)};
-      total = ff_add(total, warp_ff_sum(val));
+    ff total = total_in;
+    if (!(total.hi >= 0.f)) {
+      total = ff{0.f, 0.f};
+      for (int c0w = 0; c0w < a.nch; c0w += 32) {
+        const int cc = c0w + lane;
+        ff val{0.f, 0.f};
+        if (cc < a.nch) val = ff{__ldcg(&pr[cc].x), __ldcg(&pr[cc].y)};
+        total = ff_add(total, warp_ff_sum(val));
+      }
     }
     const float u = philox_uniform(a.seed, a.step, b, jr, SMC_PURPOSE_RESIDUAL);
     ff rem{0.f, 0.f};
@@ -321,7 +360,7 @@ __global__ void __launch_bounds__(kThreads) sps_residual_kernel(const SpsArgs a)
       auto chunk_mass = [&](int cc, ff *val, ff *f) {
         const float4 q = __ldcg(&pq[cc * 2]);
         if (q.x > kNegInf) {
-          *f = ff_norm(weight_term(q.x, M, a.tscale, s_tab));
+          *f = ff_norm(weight_term(q.x, M, a.tscale, sm.tab));
           *val = ff_mul(ff{q.y, q.z}, *f);
         }
       };
@@ -336,42 +375,337 @@ __global__ void __launch_bounds__(kThreads) sps_residual_kernel(const SpsArgs a)
       if (sel >= 0) sel_m = __ldcg(&pq[sel * 2].x);
     }
     if (lane == 0) {
-      s_sel = sel;
-      s_mode = mode;
-      s_sel_m = sel_m;
-      s_rem = rem;
-      a.ws.sps_ticket_b[b] = 0u;
+      sm.sel = sel;
+      sm.mode = mode;
+      sm.sel_m = sel_m;
+      sm.rem = rem;
     }
   }
   __syncthreads();
-  const int sel = s_sel;
+  const int sel = sm.sel;
   int tok = -1;
   if (sel >= 0) {
     const int64_t sc0 = static_cast<int64_t>(sel) * G::kCH;
     const int len = static_cast<int>(min(static_cast<int64_t>(G::kCH), a.V - sc0));
-    if (s_mode == 0) {
+    if (sm.mode == 0) {
       tok = block_select_in_chunk(
-          sc0, len, s_rem,
+          sc0, len, sm.rem,
           [&](int64_t i) {
             return residual_of(Tr::scalar(prow, i), Tr::scalar(qrow, i), a.tscale, lp, lq, thr_p,
-                               thr_q, s_tab);
+                               thr_q, sm.tab);
           },
-          s_ff, s_int);
+          sm.ffs, sm.ints);
     } else {
-      const float cm = s_sel_m;
+      const float cm = sm.sel_m;
       tok = block_select_in_chunk(
-          sc0, len, s_rem,
+          sc0, len, sm.rem,
           [&](int64_t i) {
             const float x = Tr::scalar(prow, i);
-            return x >= thr_p ? weight_term(x, cm, a.tscale, s_tab) : ff{0.f, 0.f};
+            return x >= thr_p ? weight_term(x, cm, a.tscale, sm.tab) : ff{0.f, 0.f};
           },
-          s_ff, s_int);
+          sm.ffs, sm.ints);
     }
   }
   if (tid == 0) a.tokens_out[static_cast<size_t>(b) * (a.K + 1) + jr] = tok;
 }
 
+// The two-pass route for one prompt, run by one whole CTA: stats_chunk over
+// every chunk, the exact log-sum-exps, residual_chunk over every chunk, the
+// draw.
+template <typename T, bool VEC>
+__device__ void sps_two_pass_one_cta(const SpsArgs &a, int b, int jr, float thr_p, float thr_q,
+                                     SpsSmem &sm) {
+  for (int cc = 0; cc < a.nch; ++cc) stats_chunk<T, VEC>(a, b, jr, cc, thr_p, thr_q, sm);
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    ff lp, lq;
+    stats_combine(a, b, sm.tab, &lp, &lq);
+    if (threadIdx.x == 0) {
+      sm.lp = lp;
+      sm.lq = lq;
+    }
+  }
+  __syncthreads();
+  const ff lp = sm.lp, lq = sm.lq;
+  for (int cc = 0; cc < a.nch; ++cc) residual_chunk<T, VEC>(a, b, jr, cc, lp, lq, thr_p, thr_q, sm);
+  __syncthreads();
+  residual_select<T>(a, b, jr, lp, lq, thr_p, thr_q, ff{-1.f, 0.f}, sm);
+}
+
+__device__ __forceinline__ void sps_stage_tables(SpsSmem &sm) {
+  stage_exp2_table(sm.tab);
+  stage_exp2_split(sm.th, sm.tl);
+}
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kThreads) sps_stats_kernel(const SpsArgs a) {
+  __shared__ SpsSmem sm;
+  const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
+  const int jr = a.ws.sps_rej[b];
+  if (jr < 0) return;
+  sps_stage_tables(sm);
+  float thr_p, thr_q;
+  sps_thresholds(a, b, jr, &thr_p, &thr_q);
+  stats_chunk<T, VEC>(a, b, jr, c, thr_p, thr_q, sm);
+  if (tid == 0) {
+    __threadfence();
+    sm.last = atomicAdd(&a.ws.sps_ticket_a[b], 1u) == static_cast<unsigned>(a.nch - 1);
+  }
+  __syncthreads();
+  if (!sm.last) return;
+  __threadfence();
+  if (tid < 32) {
+    ff lp, lq;
+    stats_combine(a, b, sm.tab, &lp, &lq);
+    if (tid == 0) a.ws.sps_ticket_a[b] = 0u;
+  }
+}
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kThreads) sps_residual_kernel(const SpsArgs a) {
+  __shared__ SpsSmem sm;
+  const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
+  const int jr = a.ws.sps_rej[b];
+  if (jr < 0) return;
+  sps_stage_tables(sm);
+  const float4 st = a.ws.sps_stats[b];
+  const ff lp{st.x, st.y}, lq{st.z, st.w};
+  float thr_p, thr_q;
+  sps_thresholds(a, b, jr, &thr_p, &thr_q);
+  __syncthreads();  // tables staged
+  residual_chunk<T, VEC>(a, b, jr, c, lp, lq, thr_p, thr_q, sm);
+  if (tid == 0) {
+    __threadfence();
+    sm.last = atomicAdd(&a.ws.sps_ticket_b[b], 1u) == static_cast<unsigned>(a.nch - 1);
+  }
+  __syncthreads();
+  if (!sm.last) return;
+  __threadfence();
+  if (tid == 0) a.ws.sps_ticket_b[b] = 0u;
+  residual_select<T>(a, b, jr, lp, lq, thr_p, thr_q, ff{-1.f, 0.f}, sm);
+}
+
+// The one-pass route's tolerances.  tau bounds the ratio error it accepts
+// (|rho - 1| <= tau / 2) and sets the close-call band |p_v - q_v| <= tau q_v;
+// the chunk masses may move by at most kSpsMassBound of the residual mass.
+// The first pass shifts by the row kernel's log-sum-exps (about 1e-7); the
+// retry pass by exact ones.
+constexpr float kSpsTauFirst = 4e-6f;
+constexpr float kSpsTauRetry = 1e-8f;
+constexpr float kSpsMassBound = 2e-10f;
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Chunk c of prompt b without top-p, with P_v = exp(s x_v - lp0) and
+// Q_v = exp(s y_v - lq0) for shifts lp0, lq0 near the rows' log-sum-exps
+// (p_v = P_v / sum P, q_v = Q_v / sum Q): the float-float sums of P and Q,
+// the residual at ratio 1, R1 = sum max(0, P - Q), the Q-mass where P > Q
+// (AQ) and the Q-mass of the close calls (CQ), to
+// sps_part_pq[(b nch + c) 2 + {0, 1}].  The prompt's last CTA (ticket) sets
+// cp = 1 / sum P, cq = 1 / sum Q; chunk c's residual mass is
+// cp R1 + (cp - cq) AQ, exact but for close calls, which move it by at most
+// |cp - cq| CQ.  If that bound or the ratio is out of range: on the first
+// pass the prompt is queued for the retry pass with the exact log-sum-exps
+// (sps_stats); on the retry pass, or when no residual is left or a shift is
+// not finite, the CTA takes the two-pass route alone.
+template <typename T, bool VEC>
+__device__ void onepass_chunk(const SpsArgs &a, int b, int jr, int c, ff lp0, ff lq0, bool retry,
+                              unsigned *ticket, SpsSmem &sm) {
+  using G = SpsGeom<T>;
+  constexpr float kInf = -kNegInf;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float tau = retry ? kSpsTauRetry : kSpsTauFirst;
+  const bool live = fabsf(lp0.hi) < kInf && fabsf(lq0.hi) < kInf;
+  const int64_t c0 = static_cast<int64_t>(c) * G::kCH;
+  const int n_valid = static_cast<int>(min(static_cast<int64_t>(G::kCH), a.V - c0));
+  const char *prow, *qrow;
+  sps_rows(a, b, jr, G::kESZ, &prow, &qrow);
+  float xp[G::kEPT], xq[G::kEPT];
+  load_chunk<T, VEC, kSpsNV>(prow + c0 * G::kESZ, n_valid, xp);
+  load_chunk<T, VEC, kSpsNV>(qrow + c0 * G::kESZ, n_valid, xq);
+  __syncthreads();  // tables staged; the previous prompt's shared state read
+  ff sp{0.f, 0.f}, sq{0.f, 0.f}, r1{0.f, 0.f};
+  float aq = 0.f, cq = 0.f;
+  if (live) {
+    ShiftedExp ep, eq;
+    ep.init(a.tscale, lp0);
+    eq.init(a.tscale, lq0);
+    PairAcc accp, accq, accr;
+    accp.init();
+    accq.init();
+    accr.init();
+    unsigned long long aq2 = 0ull, cq2 = 0ull;
+#pragma unroll
+    for (int e = 0; e < G::kEPT; e += 2) {
+      unsigned long long PH, PL, QH, QL, NH, NL;
+      ep.eval(xp[e], xp[e + 1], sm.th, sm.tl, &PH, &PL);
+      eq.eval(xq[e], xq[e + 1], sm.th, sm.tl, &QH, &QL);
+      accp.add(PH, PL);
+      accq.add(QH, QL);
+      packed_diff(PH, PL, QH, QL, &NH, &NL);
+      float h0, h1, l0, l1, q0, q1;
+      f2unpack(NH, h0, h1);
+      f2unpack(NL, l0, l1);
+      f2unpack(QH, q0, q1);
+      accr.add(f2pack(h0 > 0.f ? h0 : 0.f, h1 > 0.f ? h1 : 0.f),
+               f2pack(h0 > 0.f ? l0 : 0.f, h1 > 0.f ? l1 : 0.f));
+      aq2 = add2(aq2, f2pack(h0 > 0.f ? q0 : 0.f, h1 > 0.f ? q1 : 0.f));
+      cq2 = add2(cq2, f2pack(fabsf(h0) <= tau * q0 ? q0 : 0.f, fabsf(h1) <= tau * q1 ? q1 : 0.f));
+    }
+    sp = accp.total();
+    sq = accq.total();
+    r1 = accr.total();
+    float a0, a1;
+    f2unpack(aq2, a0, a1);
+    aq = a0 + a1;
+    f2unpack(cq2, a0, a1);
+    cq = a0 + a1;
+  }
+  // the CTA's sums: warps by shuffles, then thread 0 over the warps
+  sp = warp_ff_sum(sp);
+  sq = warp_ff_sum(sq);
+  r1 = warp_ff_sum(r1);
+  aq = warp_sum_f(aq);
+  cq = warp_sum_f(cq);
+  if (lane == 0) {
+    sm.rec[2 * warp] = make_float4(sp.hi, sp.lo, sq.hi, sq.lo);
+    sm.rec[2 * warp + 1] = make_float4(r1.hi, r1.lo, aq, cq);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    ff tsp{0.f, 0.f}, tsq{0.f, 0.f}, tr1{0.f, 0.f};
+    float taq = 0.f, tcq = 0.f;
+    for (int w = 0; w < kWarps; ++w) {
+      const float4 u0 = sm.rec[2 * w], u1 = sm.rec[2 * w + 1];
+      tsp = ff_add(tsp, ff{u0.x, u0.y});
+      tsq = ff_add(tsq, ff{u0.z, u0.w});
+      tr1 = ff_add(tr1, ff{u1.x, u1.y});
+      taq += u1.z;
+      tcq += u1.w;
+    }
+    float4 *rec = a.ws.sps_part_pq + (static_cast<size_t>(b) * a.nch + c) * 2;
+    rec[0] = make_float4(tsp.hi, tsp.lo, tsq.hi, tsq.lo);
+    rec[1] = make_float4(tr1.hi, tr1.lo, taq, tcq);
+    __threadfence();
+    sm.last = atomicAdd(ticket + b, 1u) == static_cast<unsigned>(a.nch - 1);
+  }
+  __syncthreads();
+  if (!sm.last) return;
+  __threadfence();
+  if (tid < 32) {
+    const float4 *rec = a.ws.sps_part_pq + static_cast<size_t>(b) * a.nch * 2;
+    ff tp{0.f, 0.f}, tq{0.f, 0.f};
+    float cqs = 0.f;
+    for (int cc = lane; cc < a.nch; cc += 32) {
+      const float4 u0 = __ldcg(rec + 2 * cc), u1 = __ldcg(rec + 2 * cc + 1);
+      tp = ff_add(tp, ff{u0.x, u0.y});
+      tq = ff_add(tq, ff{u0.z, u0.w});
+      cqs += u1.w;
+    }
+    tp = warp_ff_sum(tp);
+    tq = warp_ff_sum(tq);
+    cqs = warp_sum_f(cqs);
+    const bool shifts_ok = live && tp.hi > 0.f && tp.hi < kInf && tq.hi > 0.f && tq.hi < kInf;
+    bool fast = false;
+    ff total{0.f, 0.f};
+    if (shifts_ok) {
+      const ff cp = ff_div(ff{1.f, 0.f}, tp), cqn = ff_div(ff{1.f, 0.f}, tq);
+      const ff dc = ff_sub(cp, cqn);
+      float2 *pr = a.ws.sps_part_r + static_cast<size_t>(b) * a.nch;
+      for (int cc = lane; cc < a.nch; cc += 32) {
+        const float4 u1 = __ldcg(rec + 2 * cc + 1);
+        ff rc = ff_add(ff_mul(cp, ff{u1.x, u1.y}), ff_mul_f(dc, u1.z));
+        if (!(rc.hi > 0.f)) rc = ff{0.f, 0.f};
+        pr[cc] = make_float2(rc.hi, rc.lo);
+        total = ff_add(total, rc);
+      }
+      total = warp_ff_sum(total);
+      const float rho_m1 = ff_sub(ff_div(tp, tq), ff{1.f, 0.f}).hi;
+      fast = fabsf(rho_m1) <= 0.5f * tau && total.hi > 0.f && total.hi < kInf &&
+             fabsf(dc.hi) * cqs <= kSpsMassBound * total.hi;
+      __syncwarp();
+    }
+    if (lane == 0) {
+      const ff lp = ff_add(lp0, ff_log(tp, sm.tab)), lq = ff_add(lq0, ff_log(tq, sm.tab));
+      // 0: draw now; 1: queue for the retry pass; 2: two-pass route here
+      sm.mode = fast ? 0 : (!retry && shifts_ok && total.hi > 0.f) ? 1 : 2;
+      sm.total = total;
+      sm.lp = lp;
+      sm.lq = lq;
+      ticket[b] = 0u;
+      if (sm.mode == 1) {
+        a.ws.sps_stats[b] = make_float4(lp.hi, lp.lo, lq.hi, lq.lo);
+        a.ws.sps_retry[atomicAdd(a.ws.sps_retry_n, 1u)] = b;
+      }
+    }
+  }
+  __syncthreads();
+  const int mode = sm.mode;
+  if (mode == 0) {
+    residual_select<T>(a, b, jr, sm.lp, sm.lq, kNegInf, kNegInf, sm.total, sm);
+  } else if (mode == 2) {
+    sps_two_pass_one_cta<T, VEC>(a, b, jr, kNegInf, kNegInf, sm);
+  }
+}
+
+// First pass, one CTA per (chunk, prompt), shifts from the row kernel.
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kThreads) sps_onepass_kernel(const SpsArgs a) {
+  __shared__ SpsSmem sm;
+  const int b = blockIdx.y;
+  const int jr = a.ws.sps_rej[b];
+  if (jr < 0) return;
+  sps_stage_tables(sm);
+  const RowResult *res = a.ws.results + static_cast<size_t>(b) * (2 * a.K + 1);
+  const float4 rp = __ldcg(reinterpret_cast<const float4 *>(res + jr));
+  const float4 rq = __ldcg(reinterpret_cast<const float4 *>(res + a.K + 1 + jr));
+  onepass_chunk<T, VEC>(a, b, jr, blockIdx.x, ff{rp.x, rp.z}, ff{rq.x, rq.z}, false,
+                        a.ws.sps_ticket_a, sm);
+}
+
+// Retry pass over the queued prompts, shifts exact: CTA (c, k) takes chunk c
+// of queue entries k, k + gridDim.y, ...  The grid's last CTA clears the
+// queue.
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kThreads) sps_retry_kernel(const SpsArgs a) {
+  __shared__ SpsSmem sm;
+  const unsigned n = __ldcg(a.ws.sps_retry_n);
+  if (n > 0u) sps_stage_tables(sm);
+  for (unsigned k = blockIdx.y; k < n; k += gridDim.y) {
+    const int b = __ldcg(a.ws.sps_retry + k);
+    const int jr = a.ws.sps_rej[b];
+    const float4 st = __ldcg(a.ws.sps_stats + b);
+    onepass_chunk<T, VEC>(a, b, jr, blockIdx.x, ff{st.x, st.y}, ff{st.z, st.w}, true,
+                          a.ws.sps_ticket_b, sm);
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.ws.sps_retry_done, 1u) == gridDim.x * gridDim.y - 1u) {
+      *a.ws.sps_retry_n = 0u;
+      *a.ws.sps_retry_done = 0u;
+    }
+  }
+}
+
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kSpsRetryCtas = 8;  // queue entries the retry grid takes at once
+
+template <typename T, bool VEC>
+static void launch_sps_kernels(const SpsArgs &a, bool topp, dim3 g, cudaStream_t stream) {
+  if (topp) {
+    sps_stats_kernel<T, VEC><<<g, kThreads, 0, stream>>>(a);
+    sps_residual_kernel<T, VEC><<<g, kThreads, 0, stream>>>(a);
+  } else {
+    sps_onepass_kernel<T, VEC><<<g, kThreads, 0, stream>>>(a);
+    sps_retry_kernel<T, VEC><<<dim3(g.x, min(static_cast<int>(g.y), kSpsRetryCtas)), kThreads, 0,
+                               stream>>>(a);
+  }
+}
 
 cudaError_t launch_sps_residual(const Shape &s, const void *target, const void *draft,
                                 int32_t *tokens_out, const Workspace &ws, cudaStream_t stream) {
@@ -387,23 +721,13 @@ cudaError_t launch_sps_residual(const Shape &s, const void *target, const void *
   a.ws = ws;
   const int esz = s.dtype == SMC_BF16 ? 2 : 4;
   const bool vec = aligned16(target) && aligned16(draft) && (static_cast<long long>(s.V) * esz) % 16 == 0;
-  dim3 g(a.nch, s.B), blk(kThreads);
+  const dim3 g(a.nch, s.B);
   if (s.dtype == SMC_BF16) {
-    if (vec) {
-      sps_stats_kernel<bf16_tag, true><<<g, blk, 0, stream>>>(a);
-      sps_residual_kernel<bf16_tag, true><<<g, blk, 0, stream>>>(a);
-    } else {
-      sps_stats_kernel<bf16_tag, false><<<g, blk, 0, stream>>>(a);
-      sps_residual_kernel<bf16_tag, false><<<g, blk, 0, stream>>>(a);
-    }
+    if (vec) launch_sps_kernels<bf16_tag, true>(a, a.topp != 0, g, stream);
+    else launch_sps_kernels<bf16_tag, false>(a, a.topp != 0, g, stream);
   } else {
-    if (vec) {
-      sps_stats_kernel<float, true><<<g, blk, 0, stream>>>(a);
-      sps_residual_kernel<float, true><<<g, blk, 0, stream>>>(a);
-    } else {
-      sps_stats_kernel<float, false><<<g, blk, 0, stream>>>(a);
-      sps_residual_kernel<float, false><<<g, blk, 0, stream>>>(a);
-    }
+    if (vec) launch_sps_kernels<float, true>(a, a.topp != 0, g, stream);
+    else launch_sps_kernels<float, false>(a, a.topp != 0, g, stream);
   }
   return cudaGetLastError();
 }
