@@ -2110,6 +2110,8 @@ __global__ void __launch_bounds__(kThreads, 1) tail_kernel(const StepArgs a, int
     smc_tail(a, blockIdx.x, sm, dyn_i, kv_staged != 0);  // waits inside
   } else {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the residual pass may launch now; it waits for this grid to finish
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     sps_tail(a, blockIdx.x, sm);
   }
 }

@@ -594,6 +594,8 @@ __device__ void onepass_chunk(const SpsArgs &a, int b, int jr, int c, ff lp0, ff
     sm.last = atomicAdd(ticket + b, 1u) == static_cast<unsigned>(a.nch - 1);
   }
   __syncthreads();
+  // the retry pass may launch now; it waits for this grid to finish
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (!sm.last) return;
   __threadfence();
   if (tid < 32) {
@@ -657,8 +659,12 @@ template <typename T, bool VEC>
 __global__ void __launch_bounds__(kThreads) sps_onepass_kernel(const SpsArgs a) {
   __shared__ SpsSmem sm;
   const int b = blockIdx.y;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the acceptance scan's results
   const int jr = a.ws.sps_rej[b];
-  if (jr < 0) return;
+  if (jr < 0) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    return;
+  }
   sps_stage_tables(sm);
   const RowResult *res = a.ws.results + static_cast<size_t>(b) * (2 * a.K + 1);
   const float4 rp = __ldcg(reinterpret_cast<const float4 *>(res + jr));
@@ -673,6 +679,7 @@ __global__ void __launch_bounds__(kThreads) sps_onepass_kernel(const SpsArgs a) 
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kThreads) sps_retry_kernel(const SpsArgs a) {
   __shared__ SpsSmem sm;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the first pass's queue
   const unsigned n = __ldcg(a.ws.sps_retry_n);
   if (n > 0u) sps_stage_tables(sm);
   for (unsigned k = blockIdx.y; k < n; k += gridDim.y) {
@@ -701,9 +708,19 @@ static void launch_sps_kernels(const SpsArgs &a, bool topp, dim3 g, cudaStream_t
     sps_stats_kernel<T, VEC><<<g, kThreads, 0, stream>>>(a);
     sps_residual_kernel<T, VEC><<<g, kThreads, 0, stream>>>(a);
   } else {
-    sps_onepass_kernel<T, VEC><<<g, kThreads, 0, stream>>>(a);
-    sps_retry_kernel<T, VEC><<<dim3(g.x, min(static_cast<int>(g.y), kSpsRetryCtas)), kThreads, 0,
-                               stream>>>(a);
+    // both with programmatic dependent launch: each waits for the grid before
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = g;
+    if (cudaLaunchKernelEx(&cfg, sps_onepass_kernel<T, VEC>, a) != cudaSuccess) return;
+    cfg.gridDim = dim3(g.x, min(static_cast<int>(g.y), kSpsRetryCtas));
+    (void)cudaLaunchKernelEx(&cfg, sps_retry_kernel<T, VEC>, a);
   }
 }
 
