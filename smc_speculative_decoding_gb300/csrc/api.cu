@@ -3,6 +3,8 @@
 // except in smc_device_status.
 #include <cmath>
 #include <cstring>
+#include <mutex>
+#include <unordered_map>
 
 #include "kernels.h"
 #include "smcsd.h"
@@ -29,12 +31,13 @@ size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws) 
   const size_t o_sa = take(sizeof(unsigned) * s.B);
   const size_t o_sb = take(sizeof(unsigned) * s.B);
   const size_t o_bm = take(sizeof(unsigned) * s.B * words);
-  const size_t o_wc = take(sizeof(unsigned) * 8);
+  const size_t o_wc = take(sizeof(unsigned) * 2 * kCounterWords);
   const size_t zero_bytes = off;
   // scratch that every call overwrites before reading
   const size_t o_part = take(sizeof(RowPartial) * rows * nch);
   const size_t o_ip = take(sizeof(float2) * rows * nch * 8);
-  const size_t o_bp = take(sizeof(int4) * static_cast<size_t>(s.B) * s.N * nch * 8);
+  const size_t bp_half = static_cast<size_t>(s.B) * s.N * nch * 8;
+  const size_t o_bp = take(sizeof(int4) * 2 * bp_half);
   const size_t o_res = take(sizeof(RowResult) * rows);
   const size_t o_rej = take(sizeof(int32_t) * s.B);
   const size_t o_sst = take(sizeof(float4) * s.B);
@@ -71,8 +74,29 @@ size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws) 
     ws->kv_old_tables = reinterpret_cast<int32_t *>(p + o_kt);
     ws->kv_old_len = reinterpret_cast<int32_t *>(p + o_kl);
     ws->zero_bytes = zero_bytes;
+    ws->bonus_part_half = bp_half;
   }
   return off;
+}
+
+void use_workspace_copy(Workspace *ws, unsigned which) {
+  if (!which) return;
+  ws->work_counter += kCounterWords;
+  ws->exit_counter += kCounterWords;
+  ws->rows_done += kCounterWords;
+  ws->tail_ticket += kCounterWords;
+  ws->sps_retry_n += kCounterWords;
+  ws->sps_retry_done += kCounterWords;
+  ws->bonus_part += ws->bonus_part_half;
+}
+
+// Consecutive steps on one workspace take alternate copies, so that a step's
+// row pass may start while the previous step's tail still reads its own.
+unsigned next_workspace_copy(const void *base) {
+  static std::mutex mu;
+  static std::unordered_map<const void *, unsigned> calls;
+  std::lock_guard<std::mutex> lock(mu);
+  return calls[base]++ & 1u;
 }
 
 static bool shape_ok(const smc_params *p) {
@@ -123,6 +147,7 @@ static int32_t prepare_ws(const smc_params *p, const smc_kv *kv, void *workspace
   const size_t need = carve_workspace(s, kv ? kv->T : 0, kv ? kv->P : 0, nullptr, nullptr);
   if (ws_bytes < need) return SMC_ERR_WORKSPACE;
   carve_workspace(s, kv ? kv->T : 0, kv ? kv->P : 0, workspace, ws);
+  use_workspace_copy(ws, next_workspace_copy(workspace));
   return SMC_OK;
 }
 

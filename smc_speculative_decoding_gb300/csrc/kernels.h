@@ -34,6 +34,7 @@ struct KvArgs {
 
 // Workspace carve-up shared by every entry point.
 constexpr int kWrecPerParticle = 16;  // two 64-bit records for each of 8 warps
+constexpr int kCounterWords = 8;      // one copy of the counters, work_counter[0] on
 
 struct Workspace {
   unsigned *status;          // [1]  device status bits
@@ -63,6 +64,7 @@ struct Workspace {
   int32_t *kv_old_tables;    // [B * N * T]
   int32_t *kv_old_len;       // [B * N]
   size_t zero_bytes;         // bytes from the start that must start at zero
+  size_t bonus_part_half;    // int4s in one of the two bonus_part buffers
 };
 
 struct Shape {
@@ -81,7 +83,12 @@ int chunks_per_row(int dtype, int V);
 int sps_chunks_per_row(int dtype, int V);  // chunks of the SpS residual kernels
 
 // Lays out `base` for the shape; returns the bytes needed (base may be null).
+// The counters (work_counter .. sps_retry_done) and bonus_part come twice; the
+// carve points at the first copy, use_workspace_copy(ws, 1) at the second.
 size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws);
+void use_workspace_copy(Workspace *ws, unsigned which);
+// Alternates 0, 1, 0, ... over the calls that use the workspace at `base`.
+unsigned next_workspace_copy(const void *base);
 
 struct StepOutputs {
   float *log_weights;

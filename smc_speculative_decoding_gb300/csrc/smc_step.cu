@@ -1341,11 +1341,18 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
   }
 
   // ---- consumer warps --------------------------------------------------------
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (sa.clk && blockIdx.x == 0 && tid == 0) {  // the step-clock hook: this step starts
     const unsigned k = atomicAdd(sa.clk_ctr, 1u);
     if (k < static_cast<unsigned>(sa.clk_cap)) sa.clk[k] = global_timer_ns();
   }
+  // In the plain step the consumers write only what the previous step's
+  // kernels have finished reading once the previous prompt kernel let this
+  // grid launch: the (item, warp) partials (read before the particles publish
+  // their weights) and this call's copy of the bonus partials and counters
+  // (consecutive calls alternate copies).  So they stream at once, and wait
+  // for the previous step only before they let the next kernels launch.
+  // Elsewhere they wait first.
+  if (!sa.signal_rows) asm volatile("griddepcontrol.wait;" ::: "memory");
   const float l2s = a.tscale * kLog2e;  // log2(e) of the scaled logits
   float m_t = kNegInf, s_t = 0.f;  // this lane's running (max, sum exp) over the item
   for (int i = 0;; ++i) {
@@ -1503,7 +1510,10 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
   // which the plain step's particle kernel waits on.
   if (lane == 0) {
     if (atom_add_acq_rel_cta(&s_exited, 1u) == kConsumerWarps - 1) {
-      if (sa.signal_rows) add_release_gpu(a.ws.rows_done, 1u);
+      if (sa.signal_rows) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous step has ended
+        add_release_gpu(a.ws.rows_done, 1u);
+      }
       asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
       __threadfence();
       if (atomicAdd(a.ws.exit_counter, 1u) == gridDim.x - 1) {
@@ -2068,15 +2078,17 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const StepArgs a, i
     cp_async_wait_all();
     return;
   }
+  // Every particle of this prompt has read its row partials.  The next
+  // step's streaming kernel may launch now and stream beside this tail: it
+  // writes nothing this step's kernels still read (the bonus partials and
+  // counters alternate between calls), and it lets its own dependents launch
+  // only after this grid has ended.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const RowResult *res = a.ws.results + static_cast<size_t>(b) * N * rpp;
   const bool resampled = prompt_weights(a, b, sm, lwf, key, a.use_kv ? &sc : nullptr);
   if (a.use_kv) kv_remap_append(a.kv, b, N, sm.anc, resampled, K + 1, a.ws, sm.ks, sc, true, true);
   if (tid == 0) s_ok = wait_count(a.ws.bonus_done + b, static_cast<unsigned>(N), kCountWaitLimit);
   __syncthreads();
-  // the next step's streaming kernel may launch now (it waits for this grid
-  // to end).  Not earlier: its CTAs, made resident while particle CTAs still
-  // occupy the SMs, were measured to stream about 10 % slower.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (!s_ok) {
     if (tid == 0) raise_status(a.ws.status, SMC_DEV_TIMEOUT);
     return;
