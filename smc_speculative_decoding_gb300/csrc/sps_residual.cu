@@ -312,6 +312,97 @@ __device__ void residual_chunk(const SpsArgs &a, int b, int jr, int c, ff lp, ff
   if (tid == 0) a.ws.sps_part_r[static_cast<size_t>(b) * a.nch + c] = make_float2(R.hi, R.lo);
 }
 
+// The residual draw inside chunk [c0, c0 + len) of rows p_j and q_j, by the
+// whole CTA, with exact log-sum-exps lp, lq: thread t takes the kEPT
+// consecutive elements from t kEPT, evaluates their residuals
+// max(0, p - q) two at a time on the packed pipes and keeps them in
+// registers; a block scan of the threads' sums finds the thread whose run
+// passes `target` (in the chunk's absolute units), which walks its own terms.
+// Past the chunk's total (rounding), the last element with a residual.
+// Elements whose p is zero (outside p's nucleus, -inf, past the row) weigh 0.
+template <typename T, bool VEC>
+__device__ __noinline__ int select_residual_in_chunk(const SpsArgs &a, const char *prow, const char *qrow,
+                                        int64_t c0, int len, ff target, ff lp, ff lq,
+                                        float thr_p, float thr_q, SpsSmem &sm) {
+  using G = SpsGeom<T>;
+  using Tr = LogitTraits<T>;
+  constexpr int E = G::kEPT;
+  const int tid = threadIdx.x;
+  const int beg = tid * E;
+  float xp[E], xq[E];
+  if (VEC && beg + E <= len) {
+    const uint4 *vp = reinterpret_cast<const uint4 *>(prow + (c0 + beg) * G::kESZ);
+    const uint4 *vq = reinterpret_cast<const uint4 *>(qrow + (c0 + beg) * G::kESZ);
+#pragma unroll
+    for (int i = 0; i < kSpsNV; ++i) {
+      const uint4 up = __ldcg(vp + i), uq = __ldcg(vq + i);
+#pragma unroll
+      for (int e = 0; e < G::kEPV; ++e) {
+        xp[i * G::kEPV + e] = Tr::at(up, e);
+        xq[i * G::kEPV + e] = Tr::at(uq, e);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const bool in = beg + e < len;
+      xp[e] = in ? Tr::scalar(prow, c0 + beg + e) : kNegInf;
+      xq[e] = in ? Tr::scalar(qrow, c0 + beg + e) : kNegInf;
+    }
+  }
+  ShiftedExp ep, eq;
+  ep.init(a.tscale, lp);
+  eq.init(a.tscale, lq);
+  unsigned long long rh[E / 2], rl[E / 2];
+  ff part{0.f, 0.f};
+#pragma unroll
+  for (int e = 0; e < E; e += 2) {
+    unsigned long long PH, PL, QH, QL, NH, NL;
+    const bool k0 = xp[e] >= thr_p && xp[e] > kNegInf, k1 = xp[e + 1] >= thr_p && xp[e + 1] > kNegInf;
+    ep.eval(k0 ? xp[e] : kNegInf, k1 ? xp[e + 1] : kNegInf, sm.th, sm.tl, &PH, &PL);
+    eq.eval(xq[e] >= thr_q ? xq[e] : kNegInf, xq[e + 1] >= thr_q ? xq[e + 1] : kNegInf, sm.th,
+            sm.tl, &QH, &QL);
+    packed_diff(PH, PL, QH, QL, &NH, &NL);
+    float h0, h1, l0, l1;
+    f2unpack(NH, h0, h1);
+    f2unpack(NL, l0, l1);
+    const bool p0 = k0 && h0 > 0.f, p1 = k1 && h1 > 0.f;
+    rh[e / 2] = f2pack(p0 ? h0 : 0.f, p1 ? h1 : 0.f);
+    rl[e / 2] = f2pack(p0 ? l0 : 0.f, p1 ? l1 : 0.f);
+    part = ff_add(part, ff_norm(ff{p0 ? h0 : 0.f, p0 ? l0 : 0.f}));
+    part = ff_add(part, ff_norm(ff{p1 ? h1 : 0.f, p1 ? l1 : 0.f}));
+  }
+  ff total;
+  const ff incl = block_ff_scan(part, sm.ffs, &total);
+  const ff excl = ff_sub(incl, part);
+  int cand = 0x7fffffff, last_pos = -1, first_pos = -1;
+  ff run = excl;
+#pragma unroll
+  for (int e = 0; e < E; e += 2) {
+    float h0, h1, l0, l1;
+    f2unpack(rh[e / 2], h0, h1);
+    f2unpack(rl[e / 2], l0, l1);
+    if (h0 > 0.f) {
+      last_pos = beg + e;
+      if (first_pos < 0) first_pos = beg + e;
+      run = ff_add(run, ff_norm(ff{h0, l0}));
+      if (cand == 0x7fffffff && ff_gt(run, target)) cand = beg + e;
+    }
+    if (h1 > 0.f) {
+      last_pos = beg + e + 1;
+      if (first_pos < 0) first_pos = beg + e + 1;
+      run = ff_add(run, ff_norm(ff{h1, l1}));
+      if (cand == 0x7fffffff && ff_gt(run, target)) cand = beg + e + 1;
+    }
+  }
+  // a thread whose run starts past the target (rounding) takes its first term
+  if (part.hi > 0.f && ff_gt(excl, target)) cand = first_pos;
+  if (!(part.hi > 0.f)) cand = 0x7fffffff;
+  cand = block_min_i(cand, sm.ints);
+  if (cand == 0x7fffffff) cand = -block_min_i(-last_pos, sm.ints);  // max over threads
+  return cand < 0 ? -1 : static_cast<int>(c0 + cand);
+}
+
 // The draw once every chunk's residual mass is in sps_part_r (and, for the
 // fallback below, every chunk's stats_chunk in sps_part_pq), run by the whole
 // CTA: u from Philox (purpose RESIDUAL) picks the chunk by the chunk masses,
@@ -319,8 +410,8 @@ __device__ void residual_chunk(const SpsArgs &a, int b, int jr, int c, ff lp, ff
 // residual mass (p_j == q_j up to rounding) the token is drawn from p_j.
 // Writes the token; `total` is the residual mass when already summed, else
 // negative.
-template <typename T>
-__device__ void residual_select(const SpsArgs &a, int b, int jr, ff lp, ff lq, float thr_p,
+template <typename T, bool VEC>
+__device__ __noinline__ void residual_select(const SpsArgs &a, int b, int jr, ff lp, ff lq, float thr_p,
                                 float thr_q, ff total_in, SpsSmem &sm) {
   using G = SpsGeom<T>;
   using Tr = LogitTraits<T>;
@@ -388,13 +479,8 @@ __device__ void residual_select(const SpsArgs &a, int b, int jr, ff lp, ff lq, f
     const int64_t sc0 = static_cast<int64_t>(sel) * G::kCH;
     const int len = static_cast<int>(min(static_cast<int64_t>(G::kCH), a.V - sc0));
     if (sm.mode == 0) {
-      tok = block_select_in_chunk(
-          sc0, len, sm.rem,
-          [&](int64_t i) {
-            return residual_of(Tr::scalar(prow, i), Tr::scalar(qrow, i), a.tscale, lp, lq, thr_p,
-                               thr_q, sm.tab);
-          },
-          sm.ffs, sm.ints);
+      tok = select_residual_in_chunk<T, VEC>(a, prow, qrow, sc0, len, sm.rem, lp, lq, thr_p,
+                                             thr_q, sm);
     } else {
       const float cm = sm.sel_m;
       tok = block_select_in_chunk(
@@ -413,7 +499,7 @@ __device__ void residual_select(const SpsArgs &a, int b, int jr, ff lp, ff lq, f
 // every chunk, the exact log-sum-exps, residual_chunk over every chunk, the
 // draw.
 template <typename T, bool VEC>
-__device__ void sps_two_pass_one_cta(const SpsArgs &a, int b, int jr, float thr_p, float thr_q,
+__device__ __noinline__ void sps_two_pass_one_cta(const SpsArgs &a, int b, int jr, float thr_p, float thr_q,
                                      SpsSmem &sm) {
   for (int cc = 0; cc < a.nch; ++cc) stats_chunk<T, VEC>(a, b, jr, cc, thr_p, thr_q, sm);
   __syncthreads();
@@ -429,7 +515,7 @@ __device__ void sps_two_pass_one_cta(const SpsArgs &a, int b, int jr, float thr_
   const ff lp = sm.lp, lq = sm.lq;
   for (int cc = 0; cc < a.nch; ++cc) residual_chunk<T, VEC>(a, b, jr, cc, lp, lq, thr_p, thr_q, sm);
   __syncthreads();
-  residual_select<T>(a, b, jr, lp, lq, thr_p, thr_q, ff{-1.f, 0.f}, sm);
+  residual_select<T, VEC>(a, b, jr, lp, lq, thr_p, thr_q, ff{-1.f, 0.f}, sm);
 }
 
 __device__ __forceinline__ void sps_stage_tables(SpsSmem &sm) {
@@ -482,7 +568,7 @@ __global__ void __launch_bounds__(kThreads) sps_residual_kernel(const SpsArgs a)
   if (!sm.last) return;
   __threadfence();
   if (tid == 0) a.ws.sps_ticket_b[b] = 0u;
-  residual_select<T>(a, b, jr, lp, lq, thr_p, thr_q, ff{-1.f, 0.f}, sm);
+  residual_select<T, VEC>(a, b, jr, lp, lq, thr_p, thr_q, ff{-1.f, 0.f}, sm);
 }
 
 // The one-pass route's tolerances.  tau bounds the ratio error it accepts
@@ -648,7 +734,7 @@ __device__ void onepass_chunk(const SpsArgs &a, int b, int jr, int c, ff lp0, ff
   __syncthreads();
   const int mode = sm.mode;
   if (mode == 0) {
-    residual_select<T>(a, b, jr, sm.lp, sm.lq, kNegInf, kNegInf, sm.total, sm);
+    residual_select<T, VEC>(a, b, jr, sm.lp, sm.lq, kNegInf, kNegInf, sm.total, sm);
   } else if (mode == 2) {
     sps_two_pass_one_cta<T, VEC>(a, b, jr, kNegInf, kNegInf, sm);
   }
@@ -656,7 +742,7 @@ __device__ void onepass_chunk(const SpsArgs &a, int b, int jr, int c, ff lp0, ff
 
 // First pass, one CTA per (chunk, prompt), shifts from the row kernel.
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(kThreads) sps_onepass_kernel(const SpsArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) sps_onepass_kernel(const SpsArgs a) {
   __shared__ SpsSmem sm;
   const int b = blockIdx.y;
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the acceptance scan's results

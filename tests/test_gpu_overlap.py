@@ -1,0 +1,53 @@
+"""Steps issued back to back, where each step's row pass streams beside the
+previous step's epilogue (the prompt kernel lets it launch once the weights
+are in, and consecutive calls alternate between two copies of the workspace's
+counters and bonus partials), leave the same state, bit for bit, as the same
+steps with the host waiting for each step to end (no overlap).  Every
+reduction on the path has a fixed order, so scheduling must not change a bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+from smc_speculative_decoding_gb300.workloads import WORKLOADS, make_step_inputs
+
+from gpu_harness import StepRunner
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from smc_speculative_decoding_gb300 import build
+    build.build()
+
+
+def _final_state(r):
+    kv = r.kv
+    return [t.cpu().numpy().copy() for t in
+            (r.log_weights, r.tokens_out, r.ancestors, r.ess, r.resampled, kv["tables"],
+             kv["refcount"], kv["seq_len"], kv["free_list"], kv["free_top"], kv["cow_pairs"],
+             kv["n_cow"])]
+
+
+@pytest.mark.parametrize("name,B,steps", [("batched_serving_v128256", 16, 10),
+                                          ("single_prompt_v32000", 4, 12),
+                                          ("tiny_v64", 3, 16)])
+def test_back_to_back_steps_match_serialised_steps(name, B, steps):
+    w = WORKLOADS[name].with_(B=B)
+    inputs = [make_step_inputs(w, 21, device="cuda", step=s) for s in range(steps)]
+    states = []
+    for serial in (True, False):
+        r = StepRunner(w, seed=9, with_kv=True, steps=steps)
+        torch.cuda.synchronize()
+        for s in range(steps):
+            r.run(inputs[s], s)
+            if serial:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        assert r.status() == 0
+        states.append(_final_state(r))
+    for got, want in zip(states[1], states[0]):
+        assert np.array_equal(got, want)
