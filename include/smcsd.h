@@ -29,8 +29,13 @@
  *     `workspace`, sized by smc_workspace_bytes(), 256-byte aligned, and
  *     zero-filled once before first use (smc_workspace_init).  Each call
  *     leaves the workspace's counters zero again, so it can be reused by the
- *     next call on the same stream without clearing.  Two calls that run
- *     concurrently must not share a workspace.
+ *     next call on the same stream without clearing, by calls of the same
+ *     entry point and shape (the layout depends on both; another shape or
+ *     entry point takes its own workspace, or smc_workspace_init first).  Two
+ *     calls that run concurrently must not share a workspace.  Consecutive
+ *     steps on one workspace may overlap on the GPU (a step's first kernel
+ *     starts while the previous step's last kernel finishes); the library
+ *     orders everything they share.
  *   - Return value: SMC_OK or a negative SMC_ERR_* code for a host-side
  *     failure (nothing was launched).  Conditions only the GPU can see (a bad
  *     token id, a non-finite logit, an exhausted block pool ...) set bits of a
