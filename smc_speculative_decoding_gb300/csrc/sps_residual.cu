@@ -123,7 +123,7 @@ struct SpsSmem {
   float2 ffs[kWarps];
   float4 rec[2 * kWarps];
   int ints[2 * kWarps];
-  int last, sel, mode, fast;
+  int last, sel, mode;
   float sel_m;
   ff rem, lp, lq, total;
 };

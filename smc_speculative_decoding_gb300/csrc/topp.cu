@@ -1,6 +1,7 @@
 // Top-p (nucleus) restriction of the step's rows for sm_103a: the kernel
 // smc_step_ex runs after the row combine when top_p < 1.
 #include <cmath>
+#include <type_traits>
 
 #include <cuda_bf16.h>
 
@@ -121,11 +122,22 @@ __device__ __forceinline__ float block_max_nt(float v, float *scratch) {
 // in units of 2^-(26 + qb), exact integers throughout, so every sum is
 // order-independent.  A scan over the bins finds the threshold bin b*: the
 // lowest non-empty bin whose mass above stays below top_p times the total.
-// The second pass (from L2) copies the keys and q of b*'s logits into
-// shared memory, and a radix select over those keys, 8 bits at a time from
-// their highest differing bit, finds v* inside b*.  A threshold bin with
-// more than kToppListCap logits, or rows long enough that qb would fall
-// below 18, take the exact path instead.
+// The second pass copies the keys and q of b*'s logits into shared memory,
+// and a radix select over those keys, 8 bits at a time from their highest
+// differing bit, finds v* inside b*.  A threshold bin with more than
+// kToppListCap logits, or rows long enough that qb would fall below 18, take
+// the exact path instead.
+//
+// The first pass is tried first on the likely logits only: those with
+// pi >= 2^-16, which fill bins 0 .. kToppHighBins - 1 completely, while a
+// 16-byte group without one costs four packed compares.  They are also
+// listed in shared memory (each thread its own, up to kToppHighBytes in all),
+// and the total is taken as 1
+// (the row's log-sum-exp, right to about 1e-7, well inside the 1e-5 near-tie
+// margin of the nucleus).  If those bins already hold top_p of the mass, b*
+// is among them and the second pass reads the list instead of the row;
+// otherwise the full first pass runs, and the second pass reads the row
+// again (mostly from L2).
 //
 // Exact path (radix select over the whole row).  Radix digits of 12 bits
 // then 4 (bf16) or 10 + 10 (fp32) over the keys; each pass histograms the
@@ -151,6 +163,9 @@ constexpr int kToppMassBins = 384;   // mass bins: pi from 1 down to 2^-48
 constexpr int kToppListCap = 2048;   // logits of the threshold bin held in shared memory
 constexpr int kToppBins = 4096;      // exact path: bins of the first radix digit (12 bits)
 constexpr int kToppEntries = 4096;   // runs of a bonus row summed in the first pass
+constexpr int kToppHighBins = 128;   // mass bins of pi >= 2^-16, which the first attempt fills
+constexpr int kToppHighBytes = 32768;  // shared memory of the list of those bins' logits
+constexpr int kToppQueue = 64;         // 16-byte groups each warp queues for them
 
 // 2^(26 - j/8) rounded to an integer, j = 0..7: the fractional part of a
 // mass bin's scale.
@@ -161,7 +176,7 @@ struct ToppScalars {
   unsigned long long above, kept, base, bin_above, in_above, in_kept;
   long long tok;
   uint32_t prefix;
-  int sel, n;
+  int sel, n, nh_over;
   float xlo, xhi;
   uint32_t lo2, hi2;
   int klo, nk;  // direct mode: the 16-bit keys klo .. klo + nk - 1 of bf16 bin b*
@@ -177,6 +192,11 @@ struct ToppShared {
   unsigned frac[8];
   ToppScalars s;
 };
+// Dynamic shared memory: ToppShared, then the first attempt's list of logits
+// (kToppHighBytes), then the warps' queues of 16-byte groups.
+constexpr size_t kToppHighOff = (sizeof(ToppShared) + 15) / 16 * 16;
+constexpr size_t kToppQueueOff = kToppHighOff + kToppHighBytes;
+constexpr size_t kToppSmemBytes = kToppQueueOff + sizeof(uint4) * kToppQueue * kToppWarps;
 static_assert(sizeof(uint32_t) * kToppMassBins * 32 >= sizeof(unsigned long long) * kToppBins,
               "the exact path's histogram and runs fit in the cells");
 static_assert(kToppMassBins * 32 >= 2 * kToppListCap, "the list fits in the cells");
@@ -468,7 +488,8 @@ __device__ __forceinline__ void topp_finish_fast(const StepArgs &a, int row, int
 // Main path; returns false (and writes nothing) when the row needs the exact
 // path.  The return value is the same in every thread.
 template <typename T, bool VEC>
-__device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb, ToppShared &sh) {
+__device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb, ToppShared &sh,
+                               unsigned char *hlist, uint4 *queue) {
   constexpr int NT = kToppThreads;
   const int tid = threadIdx.x, lane = tid & 31;
   const int row = topp_row(a);
@@ -481,10 +502,7 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
   // rn(r 2^qb) (r 2^qb < 2^23), since fp32 arithmetic here keeps subnormals
   const float qsc = __int_as_float(1 << qb);
   uint32_t *const cell = sh.cell;
-  for (int i = tid; i < kToppMassBins * 32; i += NT) cell[i] = 0u;
   if (tid < 8) sh.frac[tid] = kToppFrac[tid];
-  if (tid == 0) sh.s.n = 0;
-  __syncthreads();
   // Logits are first clamped to [x_lo, x_hi]: x_lo puts log2 pi at -47.5 or
   // above (-inf, NaN and the far tail then weigh about 2^-47.5, negligible),
   // x_hi at 1/32 or below.  Every finite logit lies below x_hi, since it is
@@ -514,55 +532,160 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
   };
 
   // ---- pass 1 (HBM): the (bin, lane) cells ----------------------------------
-  // the same arithmetic as mass_bin and quantise, two logits at a time on the
-  // packed fp32x2 pipes (bf16 pairs clamped with packed bf16 min / max)
+  // First attempt: only the logits with pi >= 2^-16 (x >= x_c) are binned and
+  // listed in shared memory; every logit of bins 0 .. kToppHighBins - 1 is
+  // among them, and the total is 1 (the row's log-sum-exp).  Most 16-byte
+  // groups hold no such logit and cost four packed compares.  If those bins
+  // hold less than top_p of the mass, the full pass below bins every logit.
+  float x_c = (l2lse - 16.f) / l2s;
+  if (sizeof(T) != 4) x_c = __bfloat162float(__float2bfloat16_rd(x_c));
+  const uint32_t c16 = __float_as_uint(x_c) >> 16;
+  const uint32_t XC2 = c16 | (c16 << 16), INF2 = 0x7f807f80u;
+  auto clear_cells = [&]() {
+    for (int i = tid; i < kToppMassBins * 32; i += NT) cell[i] = 0u;
+    if (tid == 0) { sh.s.n = 0; sh.s.nh_over = 0; }
+    __syncthreads();
+  };
+  clear_cells();
+  using HighT = typename std::conditional<sizeof(T) == 4, uint32_t, uint16_t>::type;
+  constexpr int kHighPerThread = kToppHighBytes / (NT * static_cast<int>(sizeof(HighT)));
+  HighT *const hstore = reinterpret_cast<HighT *>(hlist);
+  auto high_bits = [](float x) -> HighT {
+    return static_cast<HighT>(sizeof(T) == 4 ? __float_as_uint(x) : __float_as_uint(x) >> 16);
+  };
+  auto high_value = [](HighT u) -> float {
+    return __uint_as_float(sizeof(T) == 4 ? static_cast<uint32_t>(u) : static_cast<uint32_t>(u) << 16);
+  };
+  int n_high = 0;
   {
-    const unsigned long long L2S = f2dup(l2s), NL2LSE = f2dup(-l2lse), M8 = f2dup(-8.f),
-                             MB = f2dup(kMagicB), EIGHTH = f2dup(0.125f), QSC = f2dup(qsc);
-    // cell index of bin b for this lane, b 32 + lane, from t's bits directly
-    // (modulo 2^32: the bias cancels)
-    const uint32_t lane_bias = static_cast<uint32_t>(lane) - (0x4B400000u << 5);
-    auto add_pair = [&](float x0, float x1) {
-      const unsigned long long Y = fma2(f2pack(x0, x1), L2S, NL2LSE);
-      const unsigned long long Tt = fma2(Y, M8, MB);
-      float t0, t1;
-      f2unpack(Tt, t0, t1);
-      float e0, e1;
-      f2unpack(fma2(sub2(Tt, MB), EIGHTH, Y), e0, e1);
-      float q0, q1;
-      f2unpack(mul2(f2pack(fast_exp2(e0), fast_exp2(e1)), QSC), q0, q1);
-      atomicAdd(&cell[(__float_as_uint(t0) << 5) + lane_bias], __float_as_uint(q0));
-      atomicAdd(&cell[(__float_as_uint(t1) << 5) + lane_bias], __float_as_uint(q1));
-    };
-    if (sizeof(T) == 4) {
-      topp_for_each_pair<T, VEC>(rowp, a.V, [&](float x0, float x1) {
-        add_pair(fminf(fmaxf(x0, x_lo), x_hi), fminf(fmaxf(x1, x_lo), x_hi));
-      });
-    } else {
-      const uint32_t lo16 = __float_as_uint(x_lo) >> 16, hi16 = __float_as_uint(x_hi) >> 16;
-      const uint32_t LO2 = lo16 | (lo16 << 16), HI2 = hi16 | (hi16 << 16);
-      topp_for_each_group<T, VEC>(rowp, a.V, [&](const uint4 &v) {
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    // A group that holds such a logit is queued in its warp's shared-memory
+    // queue (positions from a ballot; every lane runs every iteration, groups
+    // past the row being empty), and 32 queued groups are binned at a time, one
+    // per lane, so that the warp's instructions are spent on full groups.
+    // Each thread lists the logits it bins, entry k at k NT + tid (bf16 rows
+    // keep the 16-bit values); a thread with more than kHighPerThread of them
+    // marks the list incomplete.
+    const int warp = tid >> 5;
+    uint4 *const wq = queue + warp * kToppQueue;
+    constexpr int E = LogitTraits<T>::kPerVec;
+    const int ng = (a.V + E - 1) / E;
+    const float kInfF = __int_as_float(0x7f800000);
+    auto bin_queued = [&](int count) {  // lanes below count take slots 0 .. count - 1
+      __syncwarp();
+      if (lane < count) {
+        const uint4 g = wq[lane];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t c = bmin2(bmax2(w[k], LO2), HI2);  // NaN takes the bound
-          add_pair(bf16_lo(c), bf16_hi(c));
+        for (int e = 0; e < E; ++e) {
+          const float x = LogitTraits<T>::at(g, e);
+          if (x >= x_c) {
+            float y, t;
+            const uint32_t b = mass_bin(x, y, t);
+            atomicAdd(&cell[(b << 5) + lane], quantise(y, t));
+            if (n_high < kHighPerThread) hstore[n_high * NT + tid] = high_bits(x);
+            ++n_high;
+          }
         }
-      });
+      }
+      __syncwarp();
+    };
+    int qn = 0;  // groups in the queue, the same in every lane
+    for (int g0 = 0; g0 < ng; g0 += NT * kToppUnroll) {
+      uint4 v[kToppUnroll];
+      bool in[kToppUnroll];
+#pragma unroll
+      for (int u = 0; u < kToppUnroll; ++u) {
+        const int g = g0 + u * NT + tid;
+        in[u] = g < ng;
+        if (in[u]) v[u] = topp_group<T, VEC>(rowp, g, a.V);
+      }
+#pragma unroll
+      for (int u = 0; u < kToppUnroll; ++u) {
+        const bool hit = in[u] && group_hits<T>(v[u], x_c, kInfF, XC2, INF2);
+        const unsigned bal = __ballot_sync(0xffffffffu, hit);
+        if (hit) wq[qn + __popc(bal & ((1u << lane) - 1u))] = v[u];
+        qn += __popc(bal);
+        if (qn >= 32) {
+          bin_queued(32);
+          if (lane < qn - 32) wq[lane] = wq[32 + lane];
+          qn -= 32;
+        }
+      }
+    }
+    bin_queued(qn);
+    if (n_high > kHighPerThread) sh.s.nh_over = 1;
+  }
+  __syncthreads();
+  bool high = true;
+  {
+    // the high bins' mass against top_p of the total (1)
+    unsigned long long Qh = 0, mh = 0;
+    if (tid < kToppHighBins) {
+#pragma unroll 8
+      for (int l = 0; l < 32; ++l) Qh += cell[tid * 32 + ((l + lane) & 31)];
+      mh = (Qh * sh.frac[tid & 7]) >> (tid >> 3);
+    }
+    unsigned long long high_mass;
+    block_excl_scan_u64<NT>(mh, sh.u64s, &high_mass);
+    const unsigned long long one = 1ull << (26 + qb);
+    high = high_mass >= __umul64hi(one, p64);
+  }
+  if (!high) {
+    // the full pass: every logit, with the same arithmetic as mass_bin and
+    // quantise, two logits at a time on the packed fp32x2 pipes (bf16 pairs
+    // clamped with packed bf16 min / max)
+    clear_cells();
+    {
+      const unsigned long long L2S = f2dup(l2s), NL2LSE = f2dup(-l2lse), M8 = f2dup(-8.f),
+                               MB = f2dup(kMagicB), EIGHTH = f2dup(0.125f), QSC = f2dup(qsc);
+      // cell index of bin b for this lane, b 32 + lane, from t's bits directly
+      // (modulo 2^32: the bias cancels)
+      const uint32_t lane_bias = static_cast<uint32_t>(lane) - (0x4B400000u << 5);
+      auto add_pair = [&](float x0, float x1) {
+        const unsigned long long Y = fma2(f2pack(x0, x1), L2S, NL2LSE);
+        const unsigned long long Tt = fma2(Y, M8, MB);
+        float t0, t1;
+        f2unpack(Tt, t0, t1);
+        float e0, e1;
+        f2unpack(fma2(sub2(Tt, MB), EIGHTH, Y), e0, e1);
+        float q0, q1;
+        f2unpack(mul2(f2pack(fast_exp2(e0), fast_exp2(e1)), QSC), q0, q1);
+        atomicAdd(&cell[(__float_as_uint(t0) << 5) + lane_bias], __float_as_uint(q0));
+        atomicAdd(&cell[(__float_as_uint(t1) << 5) + lane_bias], __float_as_uint(q1));
+      };
+      if (sizeof(T) == 4) {
+        topp_for_each_pair<T, VEC>(rowp, a.V, [&](float x0, float x1) {
+          add_pair(fminf(fmaxf(x0, x_lo), x_hi), fminf(fmaxf(x1, x_lo), x_hi));
+        });
+      } else {
+        const uint32_t lo16 = __float_as_uint(x_lo) >> 16, hi16 = __float_as_uint(x_hi) >> 16;
+        const uint32_t LO2 = lo16 | (lo16 << 16), HI2 = hi16 | (hi16 << 16);
+        topp_for_each_group<T, VEC>(rowp, a.V, [&](const uint4 &v) {
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t c = bmin2(bmax2(w[k], LO2), HI2);  // NaN takes the bound
+            add_pair(bf16_lo(c), bf16_hi(c));
+          }
+        });
+      }
     }
   }
   __syncthreads();
   // bin masses in units of 2^-(26 + qb), in decreasing order of the logit
+  // (in the first attempt only bins 0 .. kToppHighBins - 1 are complete, and
+  // the total is 1)
+  const int n_bins = high ? kToppHighBins : kToppMassBins;
   unsigned long long Q = 0, m = 0;
-  if (tid < kToppMassBins) {
+  if (tid < n_bins) {
 #pragma unroll 8
     for (int l = 0; l < 32; ++l) Q += cell[tid * 32 + ((l + lane) & 31)];
     m = (Q * sh.frac[tid & 7]) >> (tid >> 3);
   }
   unsigned long long total;
   const unsigned long long above = block_excl_scan_u64<NT>(m, sh.u64s, &total);
+  if (high) total = 1ull << (26 + qb);
   const unsigned long long limit = __umul64hi(total, p64);  // floor(top_p total)
-  const bool cand = tid < kToppMassBins && Q > 0 && above < limit;
+  const bool cand = tid < n_bins && Q > 0 && above < limit;
   const int bstar = block_max_int<NT>(cand ? tid : -1, sh.ints);
   if (bstar < 0) return false;  // an empty or non-finite row: the exact path reports it
   if (tid == bstar) sh.s.bin_above = above;
@@ -594,38 +717,44 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
   if (tid < 256) { sh.hq[tid] = 0u; sh.hc[tid] = 0u; sh.hh[tid] = 0u; }
   __syncthreads();  // every cell has been read: they hold the list from here on
 
-  // ---- pass 2 (L2): the threshold bin's keys and quantised masses -----------
+  // ---- pass 2: the threshold bin's keys and quantised masses ----------------
   uint32_t *const lkey = cell;
   uint32_t *const lq = cell + kToppListCap;
   const float xlo = sh.s.xlo, xhi = sh.s.xhi;
   const uint32_t lo2 = sh.s.lo2, hi2 = sh.s.hi2;
   const bool last_bin = sh.s.last_bin;
   const int klo = sh.s.klo, nk = sh.s.nk;
-  topp_for_each_group<T, VEC>(rowp, a.V, [&](const uint4 &v) {
-    // almost no group holds a logit of the interval
-    if (!last_bin && !group_hits<T>(v, xlo, xhi, lo2, hi2)) return;
-#pragma unroll
-    for (int e = 0; e < LogitTraits<T>::kPerVec; ++e) {
-      const float x = LogitTraits<T>::at(v, e);
-      float y, t;
-      if ((last_bin || (x >= xlo && x <= xhi)) && mass_bin(x, y, t) == static_cast<uint32_t>(bstar)) {
-        const uint32_t q = quantise(y, t);
-        if (nk > 0) {
-          // x lies in [xlo, xhi], so its key lies in [klo, klo + nk)
-          const int d = static_cast<int>(order_key(x) >> 16) - klo;
-          const uint32_t old = atomicAdd(&sh.hq[d], q);
-          if (old + q < q) atomicAdd(&sh.hh[d], 1u);  // the carry out of the low word
-          atomicAdd(&sh.hc[d], 1u);
-        } else {
-          const int idx = atomicAdd(&sh.s.n, 1);
-          if (idx < kToppListCap) {
-            lkey[idx] = order_key(x);
-            lq[idx] = q;
-          }
+  // the threshold bin's logits, from the list of the first attempt when it
+  // holds them all, else from the row (L2)
+  auto take = [&](float x) {
+    float y, t;
+    if ((last_bin || (x >= xlo && x <= xhi)) && mass_bin(x, y, t) == static_cast<uint32_t>(bstar)) {
+      const uint32_t q = quantise(y, t);
+      if (nk > 0) {
+        // x lies in [xlo, xhi], so its key lies in [klo, klo + nk)
+        const int d = static_cast<int>(order_key(x) >> 16) - klo;
+        const uint32_t old = atomicAdd(&sh.hq[d], q);
+        if (old + q < q) atomicAdd(&sh.hh[d], 1u);  // the carry out of the low word
+        atomicAdd(&sh.hc[d], 1u);
+      } else {
+        const int idx = atomicAdd(&sh.s.n, 1);
+        if (idx < kToppListCap) {
+          lkey[idx] = order_key(x);
+          lq[idx] = q;
         }
       }
     }
-  });
+  };
+  if (high && !sh.s.nh_over) {
+    for (int k = 0; k < n_high; ++k) take(high_value(hstore[k * NT + tid]));
+  } else {
+    topp_for_each_group<T, VEC>(rowp, a.V, [&](const uint4 &v) {
+      // almost no group holds a logit of the interval
+      if (!last_bin && !group_hits<T>(v, xlo, xhi, lo2, hi2)) return;
+#pragma unroll
+      for (int e = 0; e < LogitTraits<T>::kPerVec; ++e) take(LogitTraits<T>::at(v, e));
+    });
+  }
   __syncthreads();
   const unsigned long long bin_above = sh.s.bin_above;
   const unsigned fr = sh.frac[bstar & 7];
@@ -863,7 +992,10 @@ topp_kernel(const StepArgs a, unsigned long long p64, int qb) {
   extern __shared__ __align__(16) unsigned char topp_smem[];
   ToppShared &sh = *reinterpret_cast<ToppShared *>(topp_smem);
   if (qb > 0) {
-    if (topp_mass_bins<T, VEC>(a, p64, qb, sh)) return;
+    if (topp_mass_bins<T, VEC>(a, p64, qb, sh, topp_smem + kToppHighOff,
+                               reinterpret_cast<uint4 *>(topp_smem + kToppQueueOff))) {
+      return;
+    }
     __syncthreads();
   }
   topp_exact<T, VEC>(a, p64, sh);
@@ -884,7 +1016,7 @@ static cudaError_t launch_topp_t(const StepArgs &a, float top_p, long long rows,
   if (qb < 18) qb = 0;
   const unsigned long long p64 =
       static_cast<unsigned long long>(std::ldexp(static_cast<double>(top_p), 64));
-  const size_t smem = sizeof(ToppShared);
+  const size_t smem = kToppSmemBytes;
   cudaError_t e = allow_dyn_smem(topp_kernel<T, VEC>, smem);
   if (e != cudaSuccess) return e;
   topp_kernel<T, VEC><<<static_cast<unsigned>(rows), kToppThreads, smem, stream>>>(a, p64, qb);

@@ -214,6 +214,20 @@ def test_step_ex_top_p_serving_size_and_unaligned():
     lockstep(w, 3, seed=30, with_kv=False, top_p=0.6, tokens_fn=_nucleus_tokens(w, 0.6, 1.0, 30))
 
 
+@pytest.mark.parametrize("sigma_t,top_m,top_p", [(1.0, 0, 0.9), (0.05, 0, 0.5), (3.0, 50, 0.99)])
+def test_step_ex_top_p_threshold_below_the_first_attempt(sigma_t, top_m, top_p):
+    """Serving-size rows whose nucleus threshold lies below pi = 2^-16 (sigma 1:
+    about 2^-18; sigma 0.05: every pi near 1/V; top_p 0.99 on the serving
+    logits), so the nucleus kernel's first attempt, which bins only the
+    logits above 2^-16, falls short of top_p and the full pass runs."""
+    w = WORKLOADS["batched_serving_v128256"].with_(B=2, N=4, sigma_t=sigma_t, top_m=top_m)
+    t = lockstep(w, 2, seed=61, with_kv=False, top_p=top_p,
+                 tokens_fn=_nucleus_tokens(w, top_p, 1.0, 61))
+    print(f"sigma={sigma_t} top_p={top_p}: draws={t.draws} flagged={t.flagged} "
+          f"mismatched={t.mismatched}")
+    assert t.rate_ok()
+
+
 @pytest.mark.parametrize("dtype,V", [("f32", 600_001), ("bf16", 1_100_000)])
 def test_step_ex_top_p_long_rows(dtype, V):
     """Rows long enough that a bonus row's runs span several warp reads, and
