@@ -541,12 +541,12 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
   if (sizeof(T) != 4) x_c = __bfloat162float(__float2bfloat16_rd(x_c));
   const uint32_t c16 = __float_as_uint(x_c) >> 16;
   const uint32_t XC2 = c16 | (c16 << 16), INF2 = 0x7f807f80u;
-  auto clear_cells = [&]() {
-    for (int i = tid; i < kToppMassBins * 32; i += NT) cell[i] = 0u;
+  auto clear_cells = [&](int n_bins) {
+    for (int i = tid; i < n_bins * 32; i += NT) cell[i] = 0u;
     if (tid == 0) { sh.s.n = 0; sh.s.nh_over = 0; }
     __syncthreads();
   };
-  clear_cells();
+  clear_cells(kToppHighBins + 8);  // the first attempt's logits reach bin 129 at most
   using HighT = typename std::conditional<sizeof(T) == 4, uint32_t, uint16_t>::type;
   constexpr int kHighPerThread = kToppHighBytes / (NT * static_cast<int>(sizeof(HighT)));
   HighT *const hstore = reinterpret_cast<HighT *>(hlist);
@@ -615,25 +615,28 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
     if (n_high > kHighPerThread) sh.s.nh_over = 1;
   }
   __syncthreads();
-  bool high = true;
-  {
-    // the high bins' mass against top_p of the total (1)
-    unsigned long long Qh = 0, mh = 0;
-    if (tid < kToppHighBins) {
+  // bin masses in units of 2^-(26 + qb), in decreasing order of the logit;
+  // first those of the first attempt's bins, against a total of 1
+  auto bin_masses = [&](int n_bins, unsigned long long *Q, unsigned long long *m) {
+    *Q = 0;
+    *m = 0;
+    if (tid < n_bins) {
 #pragma unroll 8
-      for (int l = 0; l < 32; ++l) Qh += cell[tid * 32 + ((l + lane) & 31)];
-      mh = (Qh * sh.frac[tid & 7]) >> (tid >> 3);
+      for (int l = 0; l < 32; ++l) *Q += cell[tid * 32 + ((l + lane) & 31)];
+      *m = (*Q * sh.frac[tid & 7]) >> (tid >> 3);
     }
-    unsigned long long high_mass;
-    block_excl_scan_u64<NT>(mh, sh.u64s, &high_mass);
-    const unsigned long long one = 1ull << (26 + qb);
-    high = high_mass >= __umul64hi(one, p64);
-  }
-  if (!high) {
+  };
+  unsigned long long Q, m, total;
+  bin_masses(kToppHighBins, &Q, &m);
+  unsigned long long above = block_excl_scan_u64<NT>(m, sh.u64s, &total);
+  const bool high = total >= __umul64hi(1ull << (26 + qb), p64);
+  if (high) {
+    total = 1ull << (26 + qb);
+  } else {
     // the full pass: every logit, with the same arithmetic as mass_bin and
     // quantise, two logits at a time on the packed fp32x2 pipes (bf16 pairs
     // clamped with packed bf16 min / max)
-    clear_cells();
+    clear_cells(kToppMassBins);
     {
       const unsigned long long L2S = f2dup(l2s), NL2LSE = f2dup(-l2lse), M8 = f2dup(-8.f),
                                MB = f2dup(kMagicB), EIGHTH = f2dup(0.125f), QSC = f2dup(qsc);
@@ -669,21 +672,12 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
         });
       }
     }
+    __syncthreads();
+    bin_masses(kToppMassBins, &Q, &m);
+    above = block_excl_scan_u64<NT>(m, sh.u64s, &total);
   }
-  __syncthreads();
-  // bin masses in units of 2^-(26 + qb), in decreasing order of the logit
-  // (in the first attempt only bins 0 .. kToppHighBins - 1 are complete, and
-  // the total is 1)
+  // (in the first attempt only bins 0 .. kToppHighBins - 1 are complete)
   const int n_bins = high ? kToppHighBins : kToppMassBins;
-  unsigned long long Q = 0, m = 0;
-  if (tid < n_bins) {
-#pragma unroll 8
-    for (int l = 0; l < 32; ++l) Q += cell[tid * 32 + ((l + lane) & 31)];
-    m = (Q * sh.frac[tid & 7]) >> (tid >> 3);
-  }
-  unsigned long long total;
-  const unsigned long long above = block_excl_scan_u64<NT>(m, sh.u64s, &total);
-  if (high) total = 1ull << (26 + qb);
   const unsigned long long limit = __umul64hi(total, p64);  // floor(top_p total)
   const bool cand = tid < n_bins && Q > 0 && above < limit;
   const int bstar = block_max_int<NT>(cand ? tid : -1, sh.ints);
