@@ -166,6 +166,7 @@ constexpr int kToppEntries = 4096;   // runs of a bonus row summed in the first 
 constexpr int kToppHighBins = 128;   // mass bins of pi >= 2^-16, which the first attempt fills
 constexpr int kToppHighBytes = 32768;  // shared memory of the list of those bins' logits
 constexpr int kToppQueue = 64;         // 16-byte groups each warp queues for them
+constexpr int kToppPrefetchAhead = 2;  // iterations of that pass brought into L2 ahead
 
 // 2^(26 - j/8) rounded to an integer, j = 0..7: the fractional part of a
 // mass bin's scale.
@@ -589,7 +590,19 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
       __syncwarp();
     };
     int qn = 0;  // groups in the queue, the same in every lane
-    for (int g0 = 0; g0 < ng; g0 += NT * kToppUnroll) {
+    // the row's next groups go into L2 kToppPrefetchAhead iterations ahead
+    // (one bulk prefetch per iteration, by thread 0), so that the loads below
+    // meet L2 latency rather than HBM's
+    constexpr int kIt = NT * kToppUnroll;  // groups per iteration
+    auto prefetch_groups = [&](int g_from) {
+      if (VEC && tid == 0 && g_from < ng) {
+        prefetch_l2(rowp + static_cast<size_t>(g_from) * 16,
+                    static_cast<size_t>(min(kIt, ng - g_from)) * 16);
+      }
+    };
+    for (int k = 0; k < kToppPrefetchAhead; ++k) prefetch_groups(k * kIt);
+    for (int g0 = 0; g0 < ng; g0 += kIt) {
+      prefetch_groups(g0 + kToppPrefetchAhead * kIt);
       uint4 v[kToppUnroll];
       bool in[kToppUnroll];
 #pragma unroll
