@@ -336,6 +336,26 @@ __device__ __forceinline__ bool group_hits(const uint4 &v, float lo, float hi, u
   return m != 0u;
 }
 
+// Whether any logit of a group is at least lo (lo2: lo as a packed bf16 pair,
+// for bf16 groups two packed compares per word); NaN is never.
+template <typename T>
+__device__ __forceinline__ bool group_any_ge(const uint4 &v, float lo, uint32_t lo2) {
+  if (sizeof(T) == 4) {
+    return __uint_as_float(v.x) >= lo || __uint_as_float(v.y) >= lo ||
+           __uint_as_float(v.z) >= lo || __uint_as_float(v.w) >= lo;
+  }
+  uint32_t m = 0, ge;
+  asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(ge) : "r"(v.x), "r"(lo2));
+  m |= ge;
+  asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(ge) : "r"(v.y), "r"(lo2));
+  m |= ge;
+  asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(ge) : "r"(v.z), "r"(lo2));
+  m |= ge;
+  asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(ge) : "r"(v.w), "r"(lo2));
+  m |= ge;
+  return m != 0u;
+}
+
 // The bonus row's draw over the kept logits {x >= thr} (none unless live):
 // the first whose inclusive prefix of weight(x) (exact integers) exceeds
 // floor(u total); -1 with no weight.  The row is cut into runs of 128 G
@@ -541,7 +561,7 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
   float x_c = (l2lse - 16.f) / l2s;
   if (sizeof(T) != 4) x_c = __bfloat162float(__float2bfloat16_rd(x_c));
   const uint32_t c16 = __float_as_uint(x_c) >> 16;
-  const uint32_t XC2 = c16 | (c16 << 16), INF2 = 0x7f807f80u;
+  const uint32_t XC2 = c16 | (c16 << 16);
   auto clear_cells = [&](int n_bins) {
     for (int i = tid; i < n_bins * 32; i += NT) cell[i] = 0u;
     if (tid == 0) { sh.s.n = 0; sh.s.nh_over = 0; }
@@ -570,7 +590,6 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
     uint4 *const wq = queue + warp * kToppQueue;
     constexpr int E = LogitTraits<T>::kPerVec;
     const int ng = (a.V + E - 1) / E;
-    const float kInfF = __int_as_float(0x7f800000);
     auto bin_queued = [&](int count) {  // lanes below count take slots 0 .. count - 1
       __syncwarp();
       if (lane < count) {
@@ -613,7 +632,7 @@ __device__ bool topp_mass_bins(const StepArgs &a, unsigned long long p64, int qb
       }
 #pragma unroll
       for (int u = 0; u < kToppUnroll; ++u) {
-        const bool hit = in[u] && group_hits<T>(v[u], x_c, kInfF, XC2, INF2);
+        const bool hit = in[u] && group_any_ge<T>(v[u], x_c, XC2);
         const unsigned bal = __ballot_sync(0xffffffffu, hit);
         if (hit) wq[qn + __popc(bal & ((1u << lane) - 1u))] = v[u];
         qn += __popc(bal);
