@@ -214,13 +214,20 @@ def test_step_ex_top_p_serving_size_and_unaligned():
     lockstep(w, 3, seed=30, with_kv=False, top_p=0.6, tokens_fn=_nucleus_tokens(w, 0.6, 1.0, 30))
 
 
-@pytest.mark.parametrize("sigma_t,top_m,top_p", [(1.0, 0, 0.9), (0.05, 0, 0.5), (3.0, 50, 0.99)])
-def test_step_ex_top_p_threshold_below_the_first_attempt(sigma_t, top_m, top_p):
+@pytest.mark.parametrize("sigma_t,top_m,top_p,sigma_d", [(1.0, 0, 0.9, 1.0), (0.05, 0, 0.5, 1.0),
+                                                         (3.0, 50, 0.99, 1.0), (2.0, 0, 0.5, 0.0)])
+def test_step_ex_top_p_threshold_below_the_first_attempt(sigma_t, top_m, top_p, sigma_d):
     """Serving-size rows whose nucleus threshold lies below pi = 2^-16 (sigma 1:
     about 2^-18; sigma 0.05: every pi near 1/V; top_p 0.99 on the serving
     logits), so the nucleus kernel's first attempt, which bins only the
-    logits above 2^-16, falls short of top_p and the full pass runs."""
-    w = WORKLOADS["batched_serving_v128256"].with_(B=2, N=4, sigma_t=sigma_t, top_m=top_m)
+    logits above 2^-16, falls short of top_p and the full pass runs.  With
+    sigma 2 and top_p 0.5 the threshold lies near 2^-14, inside the first
+    attempt, but about 12000 logits of a row lie above 2^-16: some threads'
+    slices of the shared-memory list overflow, and the threshold bin's logits
+    are read from the row again (draft rows equal to the target rows, so that
+    the drafted tokens lie in the target's nucleus at so small a top_p)."""
+    w = WORKLOADS["batched_serving_v128256"].with_(B=2, N=4, sigma_t=sigma_t, top_m=top_m,
+                                                   sigma_d=sigma_d)
     t = lockstep(w, 2, seed=61, with_kv=False, top_p=top_p,
                  tokens_fn=_nucleus_tokens(w, top_p, 1.0, 61))
     print(f"sigma={sigma_t} top_p={top_p}: draws={t.draws} flagged={t.flagged} "
