@@ -206,6 +206,17 @@ def test_step_ex_top_p_matches_oracle(name, B, top_p, temperature):
     assert t.rate_ok()
 
 
+@pytest.mark.parametrize("V,top_p", [(32000, 0.9), (151936, 0.8)])
+def test_step_ex_top_p_fp32_rows(V, top_p):
+    """fp32 logits: the nucleus kernel's first attempt keeps 32-bit values in its
+    list (16 a thread) and tests groups of four logits."""
+    w = WORKLOADS["single_prompt_v32000"].with_(B=2, N=4, V=V, dtype="f32")
+    t = lockstep(w, 2, seed=67, with_kv=False, top_p=top_p,
+                 tokens_fn=_nucleus_tokens(w, top_p, 1.0, 67))
+    print(f"fp32 V={V} top_p={top_p}: {t.summary()}")
+    assert t.rate_ok()
+
+
 def test_step_ex_top_p_serving_size_and_unaligned():
     w = WORKLOADS["batched_serving_v128256"].with_(B=2, N=8)
     lockstep(w, 2, seed=29, with_kv=True, top_p=0.95,
