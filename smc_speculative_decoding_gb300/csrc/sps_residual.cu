@@ -122,6 +122,7 @@ struct SpsSmem {
   float red[2 * kWarps];
   float2 ffs[kWarps];
   float4 rec[2 * kWarps];
+  float tred[8][kThreads];  // the one-pass CTA's per-thread sums, for warp 0 to add
   int ints[2 * kWarps];
   int last, sel, mode;
   float sel_m;
@@ -651,33 +652,41 @@ __device__ void onepass_chunk(const SpsArgs &a, int b, int jr, int c, ff lp0, ff
     f2unpack(cq2, a0, a1);
     cq = a0 + a1;
   }
-  // the CTA's sums: warps by shuffles, then thread 0 over the warps
-  sp = warp_ff_sum(sp);
-  sq = warp_ff_sum(sq);
-  r1 = warp_ff_sum(r1);
-  aq = warp_sum_f(aq);
-  cq = warp_sum_f(cq);
-  if (lane == 0) {
-    sm.rec[2 * warp] = make_float4(sp.hi, sp.lo, sq.hi, sq.lo);
-    sm.rec[2 * warp + 1] = make_float4(r1.hi, r1.lo, aq, cq);
-  }
+  // the CTA's sums, by warp 0 alone: each lane adds kWarps threads' values
+  // from shared memory, then the warp's lanes by shuffles
+  sm.tred[0][tid] = sp.hi;
+  sm.tred[1][tid] = sp.lo;
+  sm.tred[2][tid] = sq.hi;
+  sm.tred[3][tid] = sq.lo;
+  sm.tred[4][tid] = r1.hi;
+  sm.tred[5][tid] = r1.lo;
+  sm.tred[6][tid] = aq;
+  sm.tred[7][tid] = cq;
   __syncthreads();
-  if (tid == 0) {
+  if (warp == 0) {
     ff tsp{0.f, 0.f}, tsq{0.f, 0.f}, tr1{0.f, 0.f};
     float taq = 0.f, tcq = 0.f;
+#pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      const float4 u0 = sm.rec[2 * w], u1 = sm.rec[2 * w + 1];
-      tsp = ff_add(tsp, ff{u0.x, u0.y});
-      tsq = ff_add(tsq, ff{u0.z, u0.w});
-      tr1 = ff_add(tr1, ff{u1.x, u1.y});
-      taq += u1.z;
-      tcq += u1.w;
+      const int t = lane + 32 * w;
+      tsp = ff_add(tsp, ff{sm.tred[0][t], sm.tred[1][t]});
+      tsq = ff_add(tsq, ff{sm.tred[2][t], sm.tred[3][t]});
+      tr1 = ff_add(tr1, ff{sm.tred[4][t], sm.tred[5][t]});
+      taq += sm.tred[6][t];
+      tcq += sm.tred[7][t];
     }
-    float4 *rec = a.ws.sps_part_pq + (static_cast<size_t>(b) * a.nch + c) * 2;
-    rec[0] = make_float4(tsp.hi, tsp.lo, tsq.hi, tsq.lo);
-    rec[1] = make_float4(tr1.hi, tr1.lo, taq, tcq);
-    __threadfence();
-    sm.last = atomicAdd(ticket + b, 1u) == static_cast<unsigned>(a.nch - 1);
+    tsp = warp_ff_sum(tsp);
+    tsq = warp_ff_sum(tsq);
+    tr1 = warp_ff_sum(tr1);
+    taq = warp_sum_f(taq);
+    tcq = warp_sum_f(tcq);
+    if (lane == 0) {
+      float4 *rec = a.ws.sps_part_pq + (static_cast<size_t>(b) * a.nch + c) * 2;
+      rec[0] = make_float4(tsp.hi, tsp.lo, tsq.hi, tsq.lo);
+      rec[1] = make_float4(tr1.hi, tr1.lo, taq, tcq);
+      __threadfence();
+      sm.last = atomicAdd(ticket + b, 1u) == static_cast<unsigned>(a.nch - 1);
+    }
   }
   __syncthreads();
   // the retry pass may launch now; it waits for this grid to finish
