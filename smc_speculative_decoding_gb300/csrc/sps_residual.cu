@@ -5,13 +5,16 @@
 //
 // Runs after the row kernel in SpS mode, which wrote the first rejected
 // position of every prompt (or -1) and each row's log-sum-exp to about 1e-7.
-// Without top-p, one launch over (chunk, prompt), sps_onepass_kernel: each
-// CTA sums p_v and q_v against the row kernel's log-sum-exps (provisional
+// Without top-p, sps_onepass_kernel, one CTA per (chunk, prompt): each CTA
+// sums p_v and q_v against the row kernel's log-sum-exps (provisional
 // shifts) and the residual at ratio 1, all in float-float; the last CTA of
 // the prompt turns those into the exact normalisers and chunk masses, picks
 // the chunk and the element.  Where the shifts' ratio or the close calls
-// (|p_v - q_v| <= tau q_v) could move the masses by more than 1e-10, that CTA
-// takes the two-pass route below alone.  With top-p, two launches:
+// (|p_v - q_v| <= tau q_v) could move the masses by more than 2e-10 of the
+// residual mass, the prompt is queued for sps_retry_kernel, the same pass
+// with the exact log-sum-exps as shifts; a prompt with no residual mass or a
+// non-finite row takes the two-pass route below in one CTA.  With top-p, two
+// launches:
 //   sps_stats_kernel:    float-float log-sum-exp of rows p_j and q_j, so that
 //                        p_v and q_v are known to ~1e-10 relative;
 //   sps_residual_kernel: per-chunk residual mass; the last CTA of the prompt
