@@ -1206,10 +1206,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
   const int rpp = 2 * a.K + 1;
 
   // Launched with programmatic dependent launch.  The producer reads only the
-  // logits and claims work from the queue counters, which no kernel of this
-  // library writes while a dependent may run, so it starts its copies at
-  // once; the consumers wait (griddepcontrol.wait below) before they write
-  // the partials that the previous step's kernels read.
+  // logits and claims work from this call's copy of the queue counters, so it
+  // starts its copies at once; the consumers start at once in the plain step
+  // and wait for the previous grid elsewhere (see below).
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -2024,10 +2023,10 @@ __global__ void __launch_bounds__(kThreads) particle_kernel(const StreamArgs sa)
 // prompt_kernel, launched with programmatic dependent launch after
 // particle_kernel, never waits for that grid to finish: it stages the KV
 // state and the drafted tokens, waits (bounded) until all N particles of its
-// prompt have published their weights, normalises, resamples and remaps the
-// KV state, and only then waits for their bonus tokens to emit them.  It
-// resets its prompt's counters for the next step.  A wait that gives up
-// raises SMC_DEV_TIMEOUT and leaves the prompt's outputs unwritten.
+// prompt have published their weights, lets the next step's row pass launch,
+// normalises, resamples and remaps the KV state, and only then waits for the
+// bonus tokens to emit them.  It resets its prompt's counters.  A wait that
+// gives up raises SMC_DEV_TIMEOUT and leaves the prompt's outputs unwritten.
 __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const StepArgs a, int kv_staged) {
   __shared__ TailSmem sm;
   __shared__ int s_ok;
