@@ -36,6 +36,13 @@
  *     steps on one workspace may overlap on the GPU (a step's first kernel
  *     starts while the previous step's last kernel finishes); the library
  *     orders everything they share.
+ *   - The library's kernels are launched with programmatic dependent launch,
+ *     and the row pass reads its logits as soon as it starts.  So the kernel
+ *     before a call in the stream must not let its dependents start before
+ *     it has written the inputs (griddepcontrol.launch_dependents /
+ *     cudaTriggerProgrammaticLaunchCompletion ahead of its last stores): put
+ *     an event wait or any ordinary launch between them if it does.  Kernels
+ *     that never trigger early (the default) are waited for in full.
  *   - Return value: SMC_OK or a negative SMC_ERR_* code for a host-side
  *     failure (nothing was launched).  Conditions only the GPU can see (a bad
  *     token id, a non-finite logit, an exhausted block pool ...) set bits of a
