@@ -32,18 +32,26 @@ def _final_state(r):
              kv["n_cow"])]
 
 
-@pytest.mark.parametrize("name,B,steps", [("batched_serving_v128256", 16, 10),
-                                          ("single_prompt_v32000", 4, 12),
-                                          ("tiny_v64", 3, 16)])
-def test_back_to_back_steps_match_serialised_steps(name, B, steps):
+@pytest.mark.parametrize("name,B,steps,top_p", [("batched_serving_v128256", 16, 10, 1.0),
+                                                ("single_prompt_v32000", 4, 12, 1.0),
+                                                ("tiny_v64", 3, 16, 1.0),
+                                                ("batched_serving_v128256", 4, 8, 0.9),
+                                                ("single_prompt_v32000", 4, 8, 0.8)])
+def test_back_to_back_steps_match_serialised_steps(name, B, steps, top_p):
+    """top_p < 1: the nucleus path, whose tail lets the next step's row pass
+    stream beside it."""
     w = WORKLOADS[name].with_(B=B)
     inputs = [make_step_inputs(w, 21, device="cuda", step=s) for s in range(steps)]
+    if top_p < 1.0:
+        # drafted tokens inside the draft's nucleus: each draft row's argmax
+        for inp in inputs:
+            inp["draft_tokens"].copy_(inp["draft"].float().argmax(-1).to(torch.int32))
     states = []
     for serial in (True, False):
         r = StepRunner(w, seed=9, with_kv=True, steps=steps)
         torch.cuda.synchronize()
         for s in range(steps):
-            r.run(inputs[s], s)
+            r.run(inputs[s], s, top_p=top_p)
             if serial:
                 torch.cuda.synchronize()
         torch.cuda.synchronize()
