@@ -692,8 +692,6 @@ __device__ void onepass_chunk(const SpsArgs &a, int b, int jr, int c, ff lp0, ff
     }
   }
   __syncthreads();
-  // the retry pass may launch now; it waits for this grid to finish
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (!sm.last) return;
   __threadfence();
   if (tid < 32) {
@@ -758,11 +756,11 @@ __global__ void __launch_bounds__(kThreads, 4) sps_onepass_kernel(const SpsArgs 
   __shared__ SpsSmem sm;
   const int b = blockIdx.y;
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the acceptance scan's results
+  // the retry pass may launch once every CTA has started; it waits for this
+  // grid to finish
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int jr = a.ws.sps_rej[b];
-  if (jr < 0) {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    return;
-  }
+  if (jr < 0) return;
   sps_stage_tables(sm);
   const RowResult *res = a.ws.results + static_cast<size_t>(b) * (2 * a.K + 1);
   const float4 rp = __ldcg(reinterpret_cast<const float4 *>(res + jr));
@@ -777,6 +775,10 @@ __global__ void __launch_bounds__(kThreads, 4) sps_onepass_kernel(const SpsArgs 
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kThreads) sps_retry_kernel(const SpsArgs a) {
   __shared__ SpsSmem sm;
+  // The next call's row pass may launch now and stream beside this pass: it
+  // writes only its own copy of the row partials and counters, and lets its
+  // own dependents launch only after this grid has ended.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the first pass's queue
   const unsigned n = __ldcg(a.ws.sps_retry_n);
   if (n > 0u) sps_stage_tables(sm);

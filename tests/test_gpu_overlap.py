@@ -59,3 +59,34 @@ def test_back_to_back_steps_match_serialised_steps(name, B, steps, top_p):
         states.append(_final_state(r))
     for got, want in zip(states[1], states[0]):
         assert np.array_equal(got, want)
+
+
+def test_back_to_back_verifies_match_serialised_verifies():
+    """sps_verify calls issued back to back, where each call's row pass streams
+    beside the previous call's residual passes, draw the same tokens as the
+    same calls with the host waiting for each to end."""
+    import smc_speculative_decoding_gb300 as smcsd
+    w = WORKLOADS["batched_serving_v128256"].with_(B=2)
+    nb, calls = w.B * w.N, 6
+    p = smcsd.make_params(nb, 1, w.K, w.V, w.dtype, 1.0, 0.5, 3, 0)
+    inputs = []
+    for s in range(calls):
+        inp = make_step_inputs(w, 31, device="cuda", step=s)
+        inputs.append((inp["target"].view(nb, w.K + 1, w.V), inp["draft"].view(nb, w.K, w.V),
+                       inp["draft_tokens"].view(nb, w.K)))
+    results = []
+    for serial in (True, False):
+        ws = smcsd.alloc_workspace(p)
+        outs = [(torch.empty(nb * (w.K + 1), dtype=torch.int32, device="cuda"),
+                 torch.empty(nb, dtype=torch.int32, device="cuda")) for _ in range(calls)]
+        torch.cuda.synchronize()
+        for s in range(calls):
+            ps = smcsd.make_params(nb, 1, w.K, w.V, w.dtype, 1.0, 0.5, 3, s)
+            smcsd.sps_verify(ps, *inputs[s], outs[s][0], outs[s][1], ws)
+            if serial:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        assert smcsd.smc_device_status(ws, clear=True) == 0
+        results.append([(t.cpu().numpy(), n.cpu().numpy()) for t, n in outs])
+    for (ta, na), (tb, nb_) in zip(results[1], results[0]):
+        assert np.array_equal(ta, tb) and np.array_equal(na, nb_)
