@@ -1166,7 +1166,6 @@ struct StreamArgs {
   int n_fast_items;   // all non-bonus items
   int n_bonus_items;  // bonus rows * snch (one chunk per item)
   int signal_rows;    // nonzero: each CTA adds 1 to ws.rows_done once its partials are out
-  int stream_early;   // nonzero: the consumers start before the previous grid ends
   int row_grid;       // CTAs of the streaming kernel
   unsigned long long *clk;  // step-clock hook (smc_set_step_clock), or null
   unsigned *clk_ctr;
@@ -1345,15 +1344,14 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
     const unsigned k = atomicAdd(sa.clk_ctr, 1u);
     if (k < static_cast<unsigned>(sa.clk_cap)) sa.clk[k] = global_timer_ns();
   }
-  // In an SMC step or a verify the consumers write only what the previous
-  // call's kernels have finished reading once that call let this grid launch
-  // (its prompt kernel once the weights are in, its tail once it has waited
-  // for the nucleus and the row combine, or its residual retry pass): the
-  // (item, warp) partials and this call's copy of the bonus partials and
-  // counters (consecutive calls alternate copies).  So they stream at once,
-  // and wait for the previous call only before they let the next kernels
-  // launch.  In the draft sampler they wait first.
-  if (!sa.stream_early) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The consumers write only what the previous call's kernels have finished
+  // reading once that call let this grid launch (an SMC step's prompt kernel
+  // once the weights are in, or its tail once it has waited for the nucleus
+  // and the row combine; a verify's residual retry pass; the draft sampler's
+  // row combine once it has waited for its row pass): the (item, warp)
+  // partials and this call's copy of the bonus partials and counters
+  // (consecutive calls alternate copies).  So they stream at once, and wait
+  // for the previous call only before they let the next kernels launch.
   const float l2s = a.tscale * kLog2e;  // log2(e) of the scaled logits
   float m_t = kNegInf, s_t = 0.f;  // this lane's running (max, sum exp) over the item
   for (int i = 0;; ++i) {
@@ -1511,9 +1509,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) row_stream_kernel(const Str
   // which the plain step's particle kernel waits on.
   if (lane == 0) {
     if (atom_add_acq_rel_cta(&s_exited, 1u) == kConsumerWarps - 1) {
-      if (sa.stream_early) {
-        asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous step has ended
-      }
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous call has ended
       if (sa.signal_rows) add_release_gpu(a.ws.rows_done, 1u);
       asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
       __threadfence();
@@ -2343,7 +2339,6 @@ static cudaError_t launch_stream(const StepArgs &a, long long rows, cudaStream_t
   const long long n_items = static_cast<long long>(sa.n_fast_items) + sa.n_bonus_items;
   const long long grid = grid_max < n_items ? grid_max : n_items;
   sa.signal_rows = fuse_tail ? 1 : 0;
-  sa.stream_early = a.mode == 0 || a.mode == 1 ? 1 : 0;
   sa.row_grid = static_cast<int>(grid);
   sa.clk = g_clk;
   sa.clk_ctr = g_clk_ctr;

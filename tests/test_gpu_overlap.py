@@ -90,3 +90,29 @@ def test_back_to_back_verifies_match_serialised_verifies():
         results.append([(t.cpu().numpy(), n.cpu().numpy()) for t, n in outs])
     for (ta, na), (tb, nb_) in zip(results[1], results[0]):
         assert np.array_equal(ta, tb) and np.array_equal(na, nb_)
+
+
+def test_back_to_back_draft_samples_match_serialised_ones():
+    """smc_draft_sample calls issued back to back, where each call's row pass
+    streams beside the previous call's row combine, draw the same tokens as
+    the same calls with the host waiting for each to end."""
+    import smc_speculative_decoding_gb300 as smcsd
+    w = WORKLOADS["batched_serving_v128256"].with_(B=4)
+    inp = make_step_inputs(w, 37, device="cuda")
+    sets = [inp["draft"][:, :, k].contiguous() for k in range(w.K)]
+    results = []
+    for serial in (True, False):
+        p0 = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, 1.0, w.ess_frac, 5, 0)
+        ws = smcsd.alloc_workspace(p0)
+        outs = [torch.empty(w.B * w.N, dtype=torch.int32, device="cuda") for _ in range(8)]
+        torch.cuda.synchronize()
+        for s in range(8):
+            p = smcsd.make_params(w.B, w.N, w.K, w.V, w.dtype, 1.0, w.ess_frac, 5, s)
+            smcsd.smc_draft_sample(p, sets[s % w.K], s % w.K, outs[s], ws)
+            if serial:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        assert smcsd.smc_device_status(ws, clear=True) == 0
+        results.append([o.cpu().numpy() for o in outs])
+    for a_, b_ in zip(results[1], results[0]):
+        assert np.array_equal(a_, b_)
