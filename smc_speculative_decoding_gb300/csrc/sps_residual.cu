@@ -531,6 +531,10 @@ template <typename T, bool VEC>
 __global__ void __launch_bounds__(kThreads) sps_stats_kernel(const SpsArgs a) {
   __shared__ SpsSmem sm;
   const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the acceptance scan's results
+  // the residual pass may launch once every CTA has started; it waits for
+  // this grid before it reads the statistics
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int jr = a.ws.sps_rej[b];
   if (jr < 0) return;
   sps_stage_tables(sm);
@@ -555,6 +559,10 @@ template <typename T, bool VEC>
 __global__ void __launch_bounds__(kThreads) sps_residual_kernel(const SpsArgs a) {
   __shared__ SpsSmem sm;
   const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
+  // the next call's row pass may launch once every CTA has started: it
+  // writes only its own copy of the row partials and counters
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the statistics
   const int jr = a.ws.sps_rej[b];
   if (jr < 0) return;
   sps_stage_tables(sm);
@@ -804,19 +812,21 @@ constexpr int kSpsRetryCtas = 8;  // queue entries the retry grid takes at once
 
 template <typename T, bool VEC>
 static void launch_sps_kernels(const SpsArgs &a, bool topp, dim3 g, cudaStream_t stream) {
+  // both kernels with programmatic dependent launch: each waits for the grid
+  // before it
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (topp) {
-    sps_stats_kernel<T, VEC><<<g, kThreads, 0, stream>>>(a);
-    sps_residual_kernel<T, VEC><<<g, kThreads, 0, stream>>>(a);
+    cfg.gridDim = g;
+    if (cudaLaunchKernelEx(&cfg, sps_stats_kernel<T, VEC>, a) != cudaSuccess) return;
+    (void)cudaLaunchKernelEx(&cfg, sps_residual_kernel<T, VEC>, a);
   } else {
-    // both with programmatic dependent launch: each waits for the grid before
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg{};
-    cfg.blockDim = dim3(kThreads);
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     cfg.gridDim = g;
     if (cudaLaunchKernelEx(&cfg, sps_onepass_kernel<T, VEC>, a) != cudaSuccess) return;
     cfg.gridDim = dim3(g.x, min(static_cast<int>(g.y), kSpsRetryCtas));

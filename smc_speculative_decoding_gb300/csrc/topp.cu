@@ -1017,6 +1017,11 @@ __global__ void __launch_bounds__(kToppThreads, 2)
 topp_kernel(const StepArgs a, unsigned long long p64, int qb) {
   extern __shared__ __align__(16) unsigned char topp_smem[];
   ToppShared &sh = *reinterpret_cast<ToppShared *>(topp_smem);
+  // programmatic dependent launch: the row combine's log-sum-exps first; the
+  // tail may launch once every CTA of this grid has started (it waits for
+  // this grid before it reads the nucleus results)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (qb > 0) {
     if (topp_mass_bins<T, VEC>(a, p64, qb, sh, topp_smem + kToppHighOff,
                                reinterpret_cast<uint4 *>(topp_smem + kToppQueueOff))) {
@@ -1045,8 +1050,17 @@ static cudaError_t launch_topp_t(const StepArgs &a, float top_p, long long rows,
   const size_t smem = kToppSmemBytes;
   cudaError_t e = allow_dyn_smem(topp_kernel<T, VEC>, smem);
   if (e != cudaSuccess) return e;
-  topp_kernel<T, VEC><<<static_cast<unsigned>(rows), kToppThreads, smem, stream>>>(a, p64, qb);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(rows));
+  cfg.blockDim = dim3(kToppThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, topp_kernel<T, VEC>, a, p64, qb);
 }
 
 cudaError_t launch_topp(const StepArgs &a, int dtype, float top_p, long long rows,
