@@ -45,6 +45,7 @@ size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws) 
   const size_t o_spq = take(sizeof(float4) * s.B * snch * 2);
   const size_t o_spr = take(sizeof(float2) * s.B * snch);
   const size_t o_srt = take(sizeof(int32_t) * s.B);
+  const size_t o_sff = take(sizeof(int32_t) * s.B);
   const size_t o_kt = take(sizeof(int32_t) * static_cast<size_t>(s.B) * s.N * (T > 0 ? T : 0));
   const size_t o_kl = take(sizeof(int32_t) * static_cast<size_t>(s.B) * s.N);
   if (ws && base) {
@@ -62,6 +63,7 @@ size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws) 
     ws->tail_ticket = ws->work_counter + 4;
     ws->sps_retry_n = ws->work_counter + 5;
     ws->sps_retry_done = ws->work_counter + 6;
+    ws->sps_ff_n = ws->work_counter + 7;
     ws->partials = reinterpret_cast<RowPartial *>(p + o_part);
     ws->item_part = reinterpret_cast<float2 *>(p + o_ip);
     ws->bonus_part = reinterpret_cast<int4 *>(p + o_bp);
@@ -71,6 +73,7 @@ size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws) 
     ws->sps_part_pq = reinterpret_cast<float4 *>(p + o_spq);
     ws->sps_part_r = reinterpret_cast<float2 *>(p + o_spr);
     ws->sps_retry = reinterpret_cast<int32_t *>(p + o_srt);
+    ws->sps_ff = reinterpret_cast<int32_t *>(p + o_sff);
     ws->kv_old_tables = reinterpret_cast<int32_t *>(p + o_kt);
     ws->kv_old_len = reinterpret_cast<int32_t *>(p + o_kl);
     ws->zero_bytes = zero_bytes;
@@ -87,6 +90,7 @@ void use_workspace_copy(Workspace *ws, unsigned which) {
   ws->tail_ticket += kCounterWords;
   ws->sps_retry_n += kCounterWords;
   ws->sps_retry_done += kCounterWords;
+  ws->sps_ff_n += kCounterWords;
   ws->bonus_part += ws->bonus_part_half;
 }
 

@@ -51,7 +51,9 @@ struct Workspace {
   unsigned *tail_ticket;     // [1]  prompt CTAs past their waits (plain step)
   unsigned *sps_retry_n;     // [1]  prompts queued for the SpS retry pass
   unsigned *sps_retry_done;  // [1]  retry-pass CTAs that finished
+  unsigned *sps_ff_n;        // [1]  prompts queued for the float-float pass
   int32_t *sps_retry;        // [B]  the queued prompts
+  int32_t *sps_ff;           // [B]  prompts the fp32 pass left to the float-float pass
   RowPartial *partials;      // [rows * nch]  (per-chunk kernel)
   float2 *item_part;         // [rows * nch * 8]  (m, s) per work item and warp (streaming kernel)
   int4 *bonus_part;          // [B * N * nch * 8] (ref bits, fixed-point sum lo, hi, -)
@@ -83,7 +85,7 @@ int chunks_per_row(int dtype, int V);
 int sps_chunks_per_row(int dtype, int V);  // chunks of the SpS residual kernels
 
 // Lays out `base` for the shape; returns the bytes needed (base may be null).
-// The counters (work_counter .. sps_retry_done) and bonus_part come twice; the
+// The counters (work_counter .. sps_ff_n) and bonus_part come twice; the
 // carve points at the first copy, use_workspace_copy(ws, 1) at the second.
 size_t carve_workspace(const Shape &s, int T, int P, void *base, Workspace *ws);
 void use_workspace_copy(Workspace *ws, unsigned which);

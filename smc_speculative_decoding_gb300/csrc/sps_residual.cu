@@ -5,16 +5,24 @@
 //
 // Runs after the row kernel in SpS mode, which wrote the first rejected
 // position of every prompt (or -1) and each row's log-sum-exp to about 1e-7.
-// Without top-p, sps_onepass_kernel, one CTA per (chunk, prompt): each CTA
-// sums p_v and q_v against the row kernel's log-sum-exps (provisional
-// shifts) and the residual at ratio 1, all in float-float; the last CTA of
-// the prompt turns those into the exact normalisers and chunk masses, picks
-// the chunk and the element.  Where the shifts' ratio or the close calls
-// (|p_v - q_v| <= tau q_v) could move the masses by more than 2e-10 of the
-// residual mass, the prompt is queued for sps_retry_kernel, the same pass
-// with the exact log-sum-exps as shifts; a prompt with no residual mass or a
-// non-finite row takes the two-pass route below in one CTA.  With top-p, two
-// launches:
+// Without top-p, three launches, each over what the one before it left:
+//   sps_fast_kernel:  one CTA per (8192-logit chunk, prompt), p_v and q_v in
+//                     fp32 with a proven bound E on the residual CDF's error;
+//                     the last CTA of the prompt draws when u R lies farther
+//                     than 2E from both edges of the chosen token, which makes
+//                     that token the exact one, and queues the prompt
+//                     otherwise;
+//   sps_ff_kernel:    the queued prompts in float-float: each CTA sums p_v and
+//                     q_v against the row kernel's log-sum-exps (provisional
+//                     shifts) and the residual at ratio 1; the last CTA of the
+//                     prompt turns those into the exact normalisers and chunk
+//                     masses, picks the chunk and the element.  Where the
+//                     shifts' ratio or the close calls (|p_v - q_v| <= tau
+//                     q_v) could move the masses by more than 2e-10 of the
+//                     residual mass, the prompt is queued again;
+//   sps_retry_kernel: the same pass with the exact log-sum-exps as shifts.
+// A prompt with no residual mass or a non-finite row takes the two-pass route
+// below in one CTA.  With top-p, two launches:
 //   sps_stats_kernel:    float-float log-sum-exp of rows p_j and q_j, so that
 //                        p_v and q_v are known to ~1e-10 relative;
 //   sps_residual_kernel: per-chunk residual mass; the last CTA of the prompt
@@ -48,9 +56,26 @@ int sps_chunks_per_row(int dtype, int V) {
   return (V + ch - 1) / ch;
 }
 
+// The fp32 pass's chunk: kNV 16-byte vectors per thread and row, all in
+// flight at once (twice the residual kernels' chunk).
+template <typename T> struct FastGeom {
+  static constexpr int kEPV = LogitTraits<T>::kPerVec;
+  static constexpr int kNV = 4;
+  static constexpr int kEPT = kNV * kEPV;
+  static constexpr int kCH = kThreads * kEPT;
+  static constexpr int kESZ = sizeof(T) == 4 ? 4 : 2;
+  static constexpr int kLaneTerms = kEPT / 2;  // terms in each fp32 lane sum
+};
+
+static int sps_fast_chunks_per_row(int dtype, int V) {
+  const int ch = dtype == SMC_BF16 ? FastGeom<bf16_tag>::kCH : FastGeom<float>::kCH;
+  return (V + ch - 1) / ch;
+}
+
 struct SpsArgs {
   const char *target, *draft;
   int B, K, V, nch;
+  int nchf;      // chunks of the fp32 pass (FastGeom)
   float tscale;  // s = 1/T
   int topp;      // nonzero: thresholds in ws.results[row].tok
   uint64_t seed;
@@ -129,6 +154,8 @@ struct SpsSmem {
   int ints[2 * kWarps];
   int last, sel, mode;
   float sel_m;
+  float fcp, fe2;       // the fp32 pass's normaliser and doubled error bound
+  int fsel;             // the fp32 pass's drawn token, or -1
   ff rem, lp, lq, total;
 };
 
@@ -583,6 +610,13 @@ __global__ void __launch_bounds__(kThreads) sps_residual_kernel(const SpsArgs a)
   residual_select<T, VEC>(a, b, jr, lp, lq, thr_p, thr_q, ff{-1.f, 0.f}, sm);
 }
 
+// Appends prompt b to a queue of capacity cap (one entry per prompt and call;
+// the bound only keeps a workspace left half-used by a failed call in range).
+__device__ __forceinline__ void queue_push(unsigned *n, int32_t *list, int cap, int b) {
+  const unsigned slot = atomicAdd(n, 1u);
+  if (slot < static_cast<unsigned>(cap)) list[slot] = b;
+}
+
 // The one-pass route's tolerances.  tau bounds the ratio error it accepts
 // (|rho - 1| <= tau / 2) and sets the close-call band |p_v - q_v| <= tau q_v;
 // the chunk masses may move by at most kSpsMassBound of the residual mass.
@@ -745,7 +779,7 @@ __device__ void onepass_chunk(const SpsArgs &a, int b, int jr, int c, ff lp0, ff
       ticket[b] = 0u;
       if (sm.mode == 1) {
         a.ws.sps_stats[b] = make_float4(lp.hi, lp.lo, lq.hi, lq.lo);
-        a.ws.sps_retry[atomicAdd(a.ws.sps_retry_n, 1u)] = b;
+        queue_push(a.ws.sps_retry_n, a.ws.sps_retry, a.B, b);
       }
     }
   }
@@ -756,25 +790,6 @@ __device__ void onepass_chunk(const SpsArgs &a, int b, int jr, int c, ff lp0, ff
   } else if (mode == 2) {
     sps_two_pass_one_cta<T, VEC>(a, b, jr, kNegInf, kNegInf, sm);
   }
-}
-
-// First pass, one CTA per (chunk, prompt), shifts from the row kernel.
-template <typename T, bool VEC>
-__global__ void __launch_bounds__(kThreads, 4) sps_onepass_kernel(const SpsArgs a) {
-  __shared__ SpsSmem sm;
-  const int b = blockIdx.y;
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // the acceptance scan's results
-  // the retry pass may launch once every CTA has started; it waits for this
-  // grid to finish
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int jr = a.ws.sps_rej[b];
-  if (jr < 0) return;
-  sps_stage_tables(sm);
-  const RowResult *res = a.ws.results + static_cast<size_t>(b) * (2 * a.K + 1);
-  const float4 rp = __ldcg(reinterpret_cast<const float4 *>(res + jr));
-  const float4 rq = __ldcg(reinterpret_cast<const float4 *>(res + a.K + 1 + jr));
-  onepass_chunk<T, VEC>(a, b, jr, blockIdx.x, ff{rp.x, rp.z}, ff{rq.x, rq.z}, false,
-                        a.ws.sps_ticket_a, sm);
 }
 
 // Retry pass over the queued prompts, shifts exact: CTA (c, k) takes chunk c
@@ -788,7 +803,9 @@ __global__ void __launch_bounds__(kThreads) sps_retry_kernel(const SpsArgs a) {
   // own dependents launch only after this grid has ended.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the first pass's queue
-  const unsigned n = __ldcg(a.ws.sps_retry_n);
+  // the float-float pass, and with it the fp32 pass, has finished
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.ws.sps_ff_n = 0u;
+  const unsigned n = min(__ldcg(a.ws.sps_retry_n), static_cast<unsigned>(a.B));
   if (n > 0u) sps_stage_tables(sm);
   for (unsigned k = blockIdx.y; k < n; k += gridDim.y) {
     const int b = __ldcg(a.ws.sps_retry + k);
@@ -806,13 +823,407 @@ __global__ void __launch_bounds__(kThreads) sps_retry_kernel(const SpsArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// The fp32 first pass (no top-p), ahead of sps_onepass_kernel.  Each
+// probability is taken in fp32 against the row kernel's log-sum-exp L:
+// P_v = 2^y_v, y_v = log2(e) (s x_v - L), with t = s x - L.hi by one FMA,
+// y = t log2(e) - L.lo log2(e) by another and 2^y by the hardware
+// approximation.  Per element
+//   |P^_v - P_v| <= P^_v (kArgErr |y_v| + kEx2Err):
+// the two roundings of y and the rounding of log2(e) move y by at most three
+// units in the last place of |y| (ln 2 of that through 2^y), and kEx2Err is
+// twice the 2-ulp accuracy CUDA documents for its exp2 approximation.  Below
+// 2^-126 the approximation flushes to 0, which no bound here can notice.
+// Lane sums are sequential fp32 sums of kLaneTerms non-negative terms (as many
+// units of their value); everything after them is float-float.
+//
+// With those, the prompt's last CTA bounds by E the distance between the
+// computed residual CDF and the exact one at every vocabulary prefix, and the
+// distance between its target u R and the exact one:
+//   E = 1.05 (2 kArgErr (B_p + B_q) / min(S_p, S_q) + 4 kEx2Err
+//             + kFastRoundUnits u + |cp - cq| S_q),
+// S the sums of P^ and Q^, B the sums of P^ |y| and Q^ |y|, cp = 1 / S_p,
+// cq = 1 / S_q.  The weights are cp max(P^ - Q^, 0).  Each row's element
+// errors count twice (once in the terms, once in the normaliser); the lane
+// sums, the normalisers' division and the roundings of the weights take at
+// most kFastRoundUnits units; and weighing Q^ by cp instead of cq moves each
+// weight by at most |cp - cq| Q^_v (max is 1-Lipschitz).  The CTA draws only
+// when u R lies farther than 2E from both edges of the chosen token's
+// interval: that token is then the exact one.  The prompts it leaves (the
+// draws that land among tokens narrower than about E, about one in five on
+// the serving rows) go to a queue for sps_ff_kernel.
+constexpr float kU32 = 0x1p-24f;
+constexpr float kArgErr = 2.09f * kU32;
+constexpr float kEx2Err = 0x1p-21f;
+constexpr float kFastRoundUnits = 64.f;  // >= 3 kLaneTerms + 12 for either dtype
+static_assert(3 * FastGeom<bf16_tag>::kLaneTerms + 12 <= 64, "rounding budget");
+
+// 2^(log2(e) (s x - L)) two logits at a time, in fp32, and |y| for the bound.
+struct FastShiftedExp {
+  unsigned long long s2, nlh, l2e, nll;
+  float lbx;
+  bool s1;
+
+  __device__ __forceinline__ void init(float s, ff big_l) {
+    s1 = s == 1.f;
+    s2 = f2dup(s);
+    nlh = f2dup(-big_l.hi);
+    l2e = f2dup(kLog2e);
+    nll = f2dup(-big_l.lo * kLog2e);
+    lbx = (big_l.hi - 140.f) / s;  // below it 2^y flushes to 0 (NaN logits too)
+  }
+
+  // lbx rounded down to a bfloat16, for clamping packed bf16 logits
+  __device__ __forceinline__ uint32_t lbx_bf16x2() const {
+    uint32_t bits = __float_as_uint(lbx) & 0xffff0000u;
+    if (__uint_as_float(bits) > lbx) bits += 0x10000u;  // negative: one step down
+    return bits | (bits >> 16);
+  }
+
+  // P = 2^y and y for logits x0, x1; kClamped: already at least lbx.
+  template <bool kClamped>
+  __device__ __forceinline__ void eval(float x0, float x1, float *p0, float *p1, float *y0,
+                                       float *y1) const {
+    const unsigned long long X =
+        kClamped ? f2pack(x0, x1) : f2pack(fmaxf(x0, lbx), fmaxf(x1, lbx));
+    const unsigned long long T = s1 ? add2(X, nlh) : fma2(s2, X, nlh);
+    f2unpack(fma2(T, l2e, nll), *y0, *y1);
+    *p0 = fast_exp2(*y0);
+    *p1 = fast_exp2(*y1);
+  }
+};
+
+// The fp32 pass's weights for elements [c0 + g, c0 + g + n) of rows p_j and
+// q_j, n = SpsGeom<T>::kEPT (elements at or past len weigh 0):
+// cp max(D_v, 0), D_v = P^_v - Q^_v, as the chunk sums took them.
+template <typename T, bool VEC>
+__device__ __forceinline__ void fast_group_weights(const char *prow, const char *qrow,
+                                                   int64_t c0, int len, int g,
+                                                   const FastShiftedExp &fp,
+                                                   const FastShiftedExp &fq, float cp,
+                                                   float (&v)[SpsGeom<T>::kEPT]) {
+  using G = SpsGeom<T>;
+  using Tr = LogitTraits<T>;
+  constexpr int E = G::kEPT;
+  float xp[E], xq[E];
+  if (VEC && g + E <= len) {
+    const uint4 *vp = reinterpret_cast<const uint4 *>(prow + (c0 + g) * G::kESZ);
+    const uint4 *vq = reinterpret_cast<const uint4 *>(qrow + (c0 + g) * G::kESZ);
+#pragma unroll
+    for (int i = 0; i < kSpsNV; ++i) {
+      const uint4 up = __ldcg(vp + i), uq = __ldcg(vq + i);
+#pragma unroll
+      for (int e = 0; e < G::kEPV; ++e) {
+        xp[i * G::kEPV + e] = Tr::at(up, e);
+        xq[i * G::kEPV + e] = Tr::at(uq, e);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const bool in = g + e < len;
+      xp[e] = in ? Tr::scalar(prow, c0 + g + e) : kNegInf;
+      xq[e] = in ? Tr::scalar(qrow, c0 + g + e) : kNegInf;
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; e += 2) {
+    float p0, p1, q0, q1, y0, y1, d0, d1;
+    fp.eval<false>(xp[e], xp[e + 1], &p0, &p1, &y0, &y1);
+    fq.eval<false>(xq[e], xq[e + 1], &q0, &q1, &y0, &y1);
+    f2unpack(sub2(f2pack(p0, p1), f2pack(q0, q1)), d0, d1);
+    v[e] = cp * fmaxf(d0, 0.f);
+    v[e + 1] = cp * fmaxf(d1, 0.f);
+  }
+}
+
+// The fp32 pass's draw inside chunk [c0, c0 + len) of rows p_j and q_j, by
+// the whole CTA: thread t takes the FastGeom<T>::kEPT consecutive elements
+// from t kEPT, sums their weights, and after a block scan walks them again.
+// Running sums are float-float.  Returns the first element whose running sum
+// passes `target` (chunk units) when its interval holds
+// [target - e2, target + e2], else -1.
+template <typename T, bool VEC>
+__device__ __noinline__ int fast_select_in_chunk(const char *prow, const char *qrow, int64_t c0,
+                                                 int len, ff target, float e2,
+                                                 const FastShiftedExp &fp,
+                                                 const FastShiftedExp &fq, float cp,
+                                                 SpsSmem &sm) {
+  constexpr int E = SpsGeom<T>::kEPT;
+  constexpr int kGroups = FastGeom<T>::kEPT / E;
+  const int tid = threadIdx.x;
+  const int beg = tid * FastGeom<T>::kEPT;
+  ff part{0.f, 0.f};
+#pragma unroll 1
+  for (int g = 0; g < kGroups; ++g) {
+    float v[E];
+    fast_group_weights<T, VEC>(prow, qrow, c0, len, beg + g * E, fp, fq, cp, v);
+#pragma unroll
+    for (int e = 0; e < E; ++e) part = ff_add(part, ff{v[e], 0.f});
+  }
+  ff total;
+  const ff incl = block_ff_scan(part, sm.ffs, &total);
+  ff run = ff_sub(incl, part), before{0.f, 0.f}, after{0.f, 0.f};
+  int cand = 0x7fffffff;
+#pragma unroll 1
+  for (int g = 0; g < kGroups && cand == 0x7fffffff; ++g) {
+    float v[E];
+    fast_group_weights<T, VEC>(prow, qrow, c0, len, beg + g * E, fp, fq, cp, v);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      if (v[e] != 0.f && cand == 0x7fffffff) {
+        const ff prev = run;
+        run = ff_add(run, ff{v[e], 0.f});
+        if (ff_gt(run, target)) {
+          cand = beg + g * E + e;
+          before = prev;
+          after = run;
+        }
+      }
+    }
+  }
+  if (tid == 0) sm.fsel = -1;
+  const int win = block_min_i(cand, sm.ints);  // its barriers order the store above
+  if (win != 0x7fffffff && cand == win) {
+    const bool ok = ff_sub(target, before).hi > e2 && ff_sub(after, target).hi > e2;
+    sm.fsel = ok ? static_cast<int>(c0 + cand) : -1;
+  }
+  __syncthreads();
+  return sm.fsel;
+}
+
+// One CTA per (fp32 chunk, prompt) without top-p: the chunk's sums of P^, Q^
+// and D+ = max(D, 0) and the bound sum P^ |y| + Q^ |y| to
+// sps_part_pq[(b nchf + c) 2 + {0, 1}]; the prompt's last CTA (ticket) draws
+// when E settles the token, else queues the prompt for the float-float pass.
+// Every vector of the chunk is requested before any arithmetic, bf16 logits
+// are clamped two at a time, and the four sums are added by four warps at
+// once.
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kThreads, 4) sps_fast_kernel(const SpsArgs a) {
+  __shared__ SpsSmem sm;
+  using G = FastGeom<T>;
+  using Tr = LogitTraits<T>;
+  constexpr float kInf = -kNegInf;
+  constexpr bool kPackedClamp = VEC && sizeof(T) == 2;
+  const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the acceptance scan's results
+  // the float-float pass may launch once every CTA has started; it waits for
+  // this grid to finish
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int jr = a.ws.sps_rej[b];
+  if (jr < 0) return;
+  const char *prow, *qrow;
+  sps_rows(a, b, jr, G::kESZ, &prow, &qrow);
+  const int64_t c0 = static_cast<int64_t>(c) * G::kCH;
+  const int n_valid = static_cast<int>(min(static_cast<int64_t>(G::kCH), a.V - c0));
+  uint4 rawp[G::kNV], rawq[G::kNV];
+  if (VEC) {
+    const uint4 *vp = reinterpret_cast<const uint4 *>(prow + c0 * G::kESZ);
+    const uint4 *vq = reinterpret_cast<const uint4 *>(qrow + c0 * G::kESZ);
+#pragma unroll
+    for (int i = 0; i < G::kNV; ++i) {
+      const int vi = i * kThreads + tid;
+      const bool in = vi * G::kEPV < n_valid;
+      rawp[i] = in ? ld_stream16(vp + vi) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+      rawq[i] = in ? ld_stream16(vq + vi) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+    }
+  }
+  const RowResult *res = a.ws.results + static_cast<size_t>(b) * (2 * a.K + 1);
+  const float4 rp = __ldcg(reinterpret_cast<const float4 *>(res + jr));
+  const float4 rq = __ldcg(reinterpret_cast<const float4 *>(res + a.K + 1 + jr));
+  const ff lp0{rp.x, rp.z}, lq0{rq.x, rq.z};
+  const bool live = fabsf(lp0.hi) < kInf && fabsf(lq0.hi) < kInf;
+  FastShiftedExp fp, fq;
+  fp.init(a.tscale, lp0);
+  fq.init(a.tscale, lq0);
+  float sp = 0.f, sq = 0.f, r1 = 0.f, bnd = 0.f;
+  if (live) {
+    const uint32_t lbp = fp.lbx_bf16x2(), lbq = fq.lbx_bf16x2();
+    unsigned long long SP = 0ull, SQ = 0ull, R1 = 0ull;
+#pragma unroll
+    for (int i = 0; i < G::kNV; ++i) {
+      const int vi = i * kThreads + tid;
+      float xp[G::kEPV], xq[G::kEPV];
+      if (kPackedClamp) {
+        // -inf past the row (the fill above) and NaN become the clamp too
+        uint4 wp = rawp[i], wq = rawq[i];
+        wp.x = bmax2(wp.x, lbp); wp.y = bmax2(wp.y, lbp);
+        wp.z = bmax2(wp.z, lbp); wp.w = bmax2(wp.w, lbp);
+        wq.x = bmax2(wq.x, lbq); wq.y = bmax2(wq.y, lbq);
+        wq.z = bmax2(wq.z, lbq); wq.w = bmax2(wq.w, lbq);
+#pragma unroll
+        for (int e = 0; e < G::kEPV; ++e) {
+          xp[e] = Tr::at(wp, e);
+          xq[e] = Tr::at(wq, e);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < G::kEPV; ++e) {
+          const int idx = vi * G::kEPV + e;
+          if (VEC) {
+            const bool in = vi * G::kEPV < n_valid;
+            xp[e] = in ? Tr::at(rawp[i], e) : kNegInf;
+            xq[e] = in ? Tr::at(rawq[i], e) : kNegInf;
+          } else {
+            xp[e] = idx < n_valid ? Tr::scalar(prow, c0 + idx) : kNegInf;
+            xq[e] = idx < n_valid ? Tr::scalar(qrow, c0 + idx) : kNegInf;
+          }
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < G::kEPV; e += 2) {
+        float p0, p1, q0, q1, yp0, yp1, yq0, yq1, d0, d1;
+        fp.eval<kPackedClamp>(xp[e], xp[e + 1], &p0, &p1, &yp0, &yp1);
+        fq.eval<kPackedClamp>(xq[e], xq[e + 1], &q0, &q1, &yq0, &yq1);
+        const unsigned long long P = f2pack(p0, p1), Q = f2pack(q0, q1);
+        SP = add2(SP, P);
+        SQ = add2(SQ, Q);
+        f2unpack(sub2(P, Q), d0, d1);
+        R1 = add2(R1, f2pack(fmaxf(d0, 0.f), fmaxf(d1, 0.f)));
+        bnd = fmaf(p0, fabsf(yp0), bnd);
+        bnd = fmaf(p1, fabsf(yp1), bnd);
+        bnd = fmaf(q0, fabsf(yq0), bnd);
+        bnd = fmaf(q1, fabsf(yq1), bnd);
+      }
+    }
+    float a0, a1;
+    f2unpack(SP, a0, a1);
+    sp = a0 + a1;
+    f2unpack(SQ, a0, a1);
+    sq = a0 + a1;
+    f2unpack(R1, a0, a1);
+    r1 = a0 + a1;
+  }
+  // the CTA's four sums, one per warp: warps 0-2 add S_p, S_q and D+ in
+  // float-float, warp 3 the bound sum
+  sm.tred[0][tid] = sp;
+  sm.tred[1][tid] = sq;
+  sm.tred[2][tid] = r1;
+  sm.tred[3][tid] = bnd;
+  __syncthreads();
+  if (warp < 3) {
+    ff t{0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) t = ff_add(t, ff{sm.tred[warp][lane + 32 * w], 0.f});
+    t = warp_ff_sum(t);
+    if (lane == 0) sm.ffs[warp] = make_float2(t.hi, t.lo);
+  } else if (warp == 3) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) t += sm.tred[3][lane + 32 * w];
+    t = warp_sum_f(t);
+    if (lane == 0) sm.red[0] = t;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float4 *rec = a.ws.sps_part_pq + (static_cast<size_t>(b) * a.nchf + c) * 2;
+    rec[0] = make_float4(sm.ffs[0].x, sm.ffs[0].y, sm.ffs[1].x, sm.ffs[1].y);
+    rec[1] = make_float4(sm.ffs[2].x, sm.ffs[2].y, 0.f, sm.red[0]);
+    __threadfence();
+    sm.last = atomicAdd(a.ws.sps_ticket_a + b, 1u) == static_cast<unsigned>(a.nchf - 1);
+  }
+  __syncthreads();
+  if (!sm.last) return;
+  __threadfence();
+  if (warp == 0) {
+    const float4 *rec = a.ws.sps_part_pq + static_cast<size_t>(b) * a.nchf * 2;
+    ff tp{0.f, 0.f}, tq{0.f, 0.f};
+    float tb = 0.f;
+    for (int cc = lane; cc < a.nchf; cc += 32) {
+      const float4 u0 = __ldcg(rec + 2 * cc), u1 = __ldcg(rec + 2 * cc + 1);
+      tp = ff_add(tp, ff{u0.x, u0.y});
+      tq = ff_add(tq, ff{u0.z, u0.w});
+      tb += u1.w;
+    }
+    tp = warp_ff_sum(tp);
+    tq = warp_ff_sum(tq);
+    tb = warp_sum_f(tb);
+    bool ok = live && tp.hi > 0.f && tp.hi < kInf && tq.hi > 0.f && tq.hi < kInf && tb < kInf;
+    int sel = -1;
+    ff rem{0.f, 0.f};
+    float cp = 0.f, e2 = 0.f;
+    if (ok) {
+      cp = 1.f / tp.hi;
+      // the weights are cp max(D, 0): against max(0, cp P^ - cq Q^) that
+      // moves each by at most |cp - cq| Q^ (max is 1-Lipschitz)
+      const float dc = cp - 1.f / tq.hi;
+      const float err = 1.05f * (2.f * kArgErr * tb / fminf(tp.hi, tq.hi) + 4.f * kEx2Err +
+                                 kFastRoundUnits * kU32 + 1.001f * fabsf(dc) * tq.hi);
+      e2 = 2.f * err;
+      auto chunk_mass = [&](int cc, ff *val, ff *f) {
+        const float4 u1 = __ldcg(rec + 2 * cc + 1);
+        const ff rc = ff_mul_f(ff{u1.x, u1.y}, cp);
+        *val = rc.hi > 0.f ? rc : ff{0.f, 0.f};
+      };
+      ff total{0.f, 0.f};
+      for (int c0w = 0; c0w < a.nchf; c0w += 32) {
+        const int cc = c0w + lane;
+        ff val{0.f, 0.f}, f{1.f, 0.f};
+        if (cc < a.nchf) chunk_mass(cc, &val, &f);
+        total = ff_add(total, warp_ff_sum(val));
+      }
+      ok = e2 < kInf && total.hi > 2.f * e2;
+      if (ok) {
+        const float u = philox_uniform(a.seed, a.step, b, jr, SMC_PURPOSE_RESIDUAL);
+        sel = warp_find_chunk(a.nchf, ff_mul_f(total, u), chunk_mass, &rem);
+        ok = sel >= 0;
+      }
+    }
+    if (lane == 0) {
+      sm.mode = ok ? 0 : 1;
+      sm.sel = sel;
+      sm.rem = rem;
+      sm.fcp = cp;
+      sm.fe2 = e2;
+      a.ws.sps_ticket_a[b] = 0u;
+    }
+  }
+  __syncthreads();
+  int tok = -1;
+  if (sm.mode == 0) {
+    const int64_t sc0 = static_cast<int64_t>(sm.sel) * G::kCH;
+    const int len = static_cast<int>(min(static_cast<int64_t>(G::kCH), a.V - sc0));
+    tok = fast_select_in_chunk<T, VEC>(prow, qrow, sc0, len, sm.rem, sm.fe2, fp, fq, sm.fcp, sm);
+  }
+  if (tid == 0) {
+    if (tok >= 0) a.tokens_out[static_cast<size_t>(b) * (a.K + 1) + jr] = tok;
+    else queue_push(a.ws.sps_ff_n, a.ws.sps_ff, a.B, b);
+  }
+}
+
+// The float-float pass over the prompts the fp32 pass left, shifts from the
+// row kernel: CTA (c, k) takes chunk c of queue entries k, k + gridDim.y, ...
+// Its own close calls go on to the retry pass, which clears this queue.
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kThreads, 4) sps_ff_kernel(const SpsArgs a) {
+  __shared__ SpsSmem sm;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the fp32 pass's queue
+  // the retry pass may launch once every CTA has started; it waits for this
+  // grid to finish
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const unsigned n = min(__ldcg(a.ws.sps_ff_n), static_cast<unsigned>(a.B));
+  if (n <= blockIdx.y) return;
+  sps_stage_tables(sm);
+  for (unsigned k = blockIdx.y; k < n; k += gridDim.y) {
+    const int b = __ldcg(a.ws.sps_ff + k);
+    const int jr = a.ws.sps_rej[b];
+    const RowResult *res = a.ws.results + static_cast<size_t>(b) * (2 * a.K + 1);
+    const float4 rp = __ldcg(reinterpret_cast<const float4 *>(res + jr));
+    const float4 rq = __ldcg(reinterpret_cast<const float4 *>(res + a.K + 1 + jr));
+    onepass_chunk<T, VEC>(a, b, jr, blockIdx.x, ff{rp.x, rp.z}, ff{rq.x, rq.z}, false,
+                          a.ws.sps_ticket_a, sm);
+  }
+}
+
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 constexpr int kSpsRetryCtas = 8;  // queue entries the retry grid takes at once
+constexpr int kSpsFfCtas = 64;    // queue entries the float-float grid takes at once
 
 template <typename T, bool VEC>
 static void launch_sps_kernels(const SpsArgs &a, bool topp, dim3 g, cudaStream_t stream) {
-  // both kernels with programmatic dependent launch: each waits for the grid
+  // every kernel with programmatic dependent launch: each waits for the grid
   // before it
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -827,8 +1238,10 @@ static void launch_sps_kernels(const SpsArgs &a, bool topp, dim3 g, cudaStream_t
     if (cudaLaunchKernelEx(&cfg, sps_stats_kernel<T, VEC>, a) != cudaSuccess) return;
     (void)cudaLaunchKernelEx(&cfg, sps_residual_kernel<T, VEC>, a);
   } else {
-    cfg.gridDim = g;
-    if (cudaLaunchKernelEx(&cfg, sps_onepass_kernel<T, VEC>, a) != cudaSuccess) return;
+    cfg.gridDim = dim3(a.nchf, g.y);
+    if (cudaLaunchKernelEx(&cfg, sps_fast_kernel<T, VEC>, a) != cudaSuccess) return;
+    cfg.gridDim = dim3(g.x, min(static_cast<int>(g.y), kSpsFfCtas));
+    if (cudaLaunchKernelEx(&cfg, sps_ff_kernel<T, VEC>, a) != cudaSuccess) return;
     cfg.gridDim = dim3(g.x, min(static_cast<int>(g.y), kSpsRetryCtas));
     (void)cudaLaunchKernelEx(&cfg, sps_retry_kernel<T, VEC>, a);
   }
@@ -841,6 +1254,7 @@ cudaError_t launch_sps_residual(const Shape &s, const void *target, const void *
   a.draft = static_cast<const char *>(draft);
   a.B = s.B; a.K = s.K; a.V = s.V;
   a.nch = sps_chunks_per_row(s.dtype, s.V);
+  a.nchf = sps_fast_chunks_per_row(s.dtype, s.V);
   a.tscale = s.tscale;
   a.topp = s.top_p < 1.f;
   a.seed = s.seed; a.step = s.step;
