@@ -55,6 +55,9 @@
  *     sampling sums (bonus and residual tokens), which are carried in
  *     float-float (about 48 significant bits) so that the drawn token agrees
  *     with an exact-arithmetic sampler except on genuine near ties.
+ *     sps_verify first tries each residual draw in fp32 with a proven bound
+ *     on its error, and keeps that draw only when the bound shows it is the
+ *     exact one; every other residual draw is made in float-float.
  *   - Randomness: Philox4x32-10, key (seed mod 2^32, seed >> 32), counter
  *     (step, stream, position, purpose); u = (word0 >> 8) * 2^-24.  Streams
  *     and purposes are listed with each entry point.
