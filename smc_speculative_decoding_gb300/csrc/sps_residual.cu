@@ -809,7 +809,10 @@ __global__ void __launch_bounds__(kThreads) sps_retry_kernel(const SpsArgs a) {
   if (n > 0u) sps_stage_tables(sm);
   for (unsigned k = blockIdx.y; k < n; k += gridDim.y) {
     const int b = __ldcg(a.ws.sps_retry + k);
+    // an entry left by a call that failed between its launches is skipped
+    if (b < 0 || b >= a.B) continue;
     const int jr = a.ws.sps_rej[b];
+    if (jr < 0 || jr >= a.K) continue;
     const float4 st = __ldcg(a.ws.sps_stats + b);
     onepass_chunk<T, VEC>(a, b, jr, blockIdx.x, ff{st.x, st.y}, ff{st.z, st.w}, true,
                           a.ws.sps_ticket_b, sm);
@@ -1207,7 +1210,10 @@ __global__ void __launch_bounds__(kThreads, 4) sps_ff_kernel(const SpsArgs a) {
   sps_stage_tables(sm);
   for (unsigned k = blockIdx.y; k < n; k += gridDim.y) {
     const int b = __ldcg(a.ws.sps_ff + k);
+    // an entry left by a call that failed between its launches is skipped
+    if (b < 0 || b >= a.B) continue;
     const int jr = a.ws.sps_rej[b];
+    if (jr < 0 || jr >= a.K) continue;
     const RowResult *res = a.ws.results + static_cast<size_t>(b) * (2 * a.K + 1);
     const float4 rp = __ldcg(reinterpret_cast<const float4 *>(res + jr));
     const float4 rq = __ldcg(reinterpret_cast<const float4 *>(res + a.K + 1 + jr));
